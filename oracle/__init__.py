@@ -1,0 +1,240 @@
+"""Python view of the fp64 CPU oracle (``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the package smoke check
+and by the benchmark's CPU-baseline leg, never by the product path.  It
+shares no code with the CUDA library.
+
+Functions mirror the C entry points and take/return numpy arrays.  bf16
+tensors are passed as their raw uint16 bit patterns; the C side widens them
+exactly to fp64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_SHARED_QUESTION, MASK_ZIGZAG_PAIR, MASK_SLICES = range(5)
+SLICE_FULL, SLICE_CAUSAL = 0, 1
+
+
+def compile_oracle(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (-O2, OpenMP) if missing or stale."""
+    stale = (not os.path.exists(_LIB)
+             or os.path.getmtime(_LIB) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Mask(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("num_prefix", ctypes.c_int32), ("cp", ctypes.c_int32),
+                ("q_rank", ctypes.c_int32), ("k_rank", ctypes.c_int32),
+                ("slices", ctypes.POINTER(ctypes.c_int32)), ("num_slices", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(compile_oracle())
+        P = ctypes.c_void_p
+        i32, i64 = ctypes.c_int32, ctypes.c_int64
+        _lib.or_num_threads.restype = i32
+        _lib.or_zigzag_map.restype = i32
+        _lib.or_zigzag_map.argtypes = [P, i32, i32, i32, P, P]
+        _lib.or_attention.restype = ctypes.c_int
+        _lib.or_attention.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, i32,
+                                      ctypes.POINTER(_Mask), ctypes.c_double, P, i64, i32, P, P]
+        _lib.or_pair_count.restype = i64
+        _lib.or_pair_count.argtypes = [i32, i32, P, i32, ctypes.POINTER(_Mask), i32]
+        _lib.or_allowed_matrix.restype = ctypes.c_int
+        _lib.or_allowed_matrix.argtypes = [i32, i32, P, i32, ctypes.POINTER(_Mask), P]
+        _lib.or_merge.restype = None
+        _lib.or_merge.argtypes = [P, P, P, P, P, P, i64, i32, i32]
+        _lib.or_lpt.restype = ctypes.c_int
+        _lib.or_lpt.argtypes = [P, i64, i32, P, P, P]
+        _lib.or_worklist.restype = ctypes.c_int
+        _lib.or_worklist.argtypes = [P, i32, ctypes.POINTER(_Mask), i32, i32, i32, i32, i32,
+                                     i64, P, P, P, P, P, P, P, P]
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Mask:
+    """Mask description understood by the oracle."""
+
+    def __init__(self, kind: int = MASK_CAUSAL, window: int = 0, num_prefix: int = 0,
+                 cp: int = 0, q_rank: int = 0, k_rank: int = 0,
+                 slices: Optional[np.ndarray] = None):
+        self.kind, self.window, self.num_prefix = kind, window, num_prefix
+        self.cp, self.q_rank, self.k_rank = cp, q_rank, k_rank
+        self.slices = None if slices is None else np.ascontiguousarray(slices, dtype=np.int32).reshape(-1, 8)
+
+    def c(self) -> _Mask:
+        m = _Mask(self.kind, self.window, self.num_prefix, self.cp, self.q_rank, self.k_rank,
+                  None, 0)
+        if self.slices is not None:
+            m.slices = self.slices.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+            m.num_slices = self.slices.shape[0]
+        return m
+
+
+def num_threads() -> int:
+    return int(lib().or_num_threads())
+
+
+def bf16_bits(t) -> np.ndarray:
+    """uint16 bit patterns of a bf16 torch tensor (any device)."""
+    import torch
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def zigzag_map(cu: np.ndarray, cp: int, rank: int):
+    """(gather map [T_r] int32, chunk table [ndocs, 2, 4]) for one rank."""
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    nd = cu.shape[0] - 1
+    n = lib().or_zigzag_map(_ptr(cu), nd, cp, rank, None, None)
+    if n < 0:
+        raise ValueError("bad zigzag arguments")
+    m = np.zeros(max(n, 1), dtype=np.int32)
+    table = np.zeros((max(nd, 1), 2, 4), dtype=np.int32)
+    lib().or_zigzag_map(_ptr(cu), nd, cp, rank, _ptr(m), _ptr(table))
+    return m[:n], table[:nd]
+
+
+def attention(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, cu: np.ndarray,
+              mask: Mask, scale: Optional[float] = None, jobs: Optional[np.ndarray] = None,
+              brute: bool = False):
+    """fp64 attention from bf16 bit patterns.
+
+    q_bits [Tq, Hq, d], k_bits/v_bits [Tk, Hkv, d] (uint16).  Returns
+    (out, lse): all rows -> out [Tq, Hq, d], lse [Hq, Tq]; with ``jobs``
+    ((row, head) int32 [n, 2]) -> out [n, d], lse [n].
+    """
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    Tq, Hq, d = q_bits.shape
+    Tk, Hkv, _ = k_bits.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    if jobs is None:
+        out = np.zeros((Tq, Hq, d), dtype=np.float64)
+        lse = np.zeros((Hq, Tq), dtype=np.float64)
+        nj = 0
+    else:
+        jobs = np.ascontiguousarray(jobs, dtype=np.int32).reshape(-1, 2)
+        nj = jobs.shape[0]
+        out = np.zeros((nj, d), dtype=np.float64)
+        lse = np.zeros((nj,), dtype=np.float64)
+    m = mask.c()
+    rc = lib().or_attention(_ptr(q_bits), _ptr(k_bits), _ptr(v_bits), Tq, Tk, Hq, Hkv, d,
+                            _ptr(cu), cu.shape[0] - 1, ctypes.byref(m), float(scale),
+                            _ptr(jobs), nj, 1 if brute else 0, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"or_attention failed ({rc})")
+    return out, lse
+
+
+def pair_count(cu: np.ndarray, mask: Mask, Tq: Optional[int] = None, Tk: Optional[int] = None,
+               brute: bool = False) -> int:
+    """Allowed (q, k) pairs per head."""
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    T = int(cu[-1])
+    Tq = T if Tq is None else Tq
+    Tk = T if Tk is None else Tk
+    m = mask.c()
+    r = lib().or_pair_count(Tq, Tk, _ptr(cu), cu.shape[0] - 1, ctypes.byref(m), 1 if brute else 0)
+    if r < 0:
+        raise ValueError("or_pair_count failed")
+    return int(r)
+
+
+def allowed_matrix(cu: np.ndarray, mask: Mask, Tq: Optional[int] = None,
+                   Tk: Optional[int] = None) -> np.ndarray:
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    T = int(cu[-1])
+    Tq = T if Tq is None else Tq
+    Tk = T if Tk is None else Tk
+    out = np.zeros((Tq, Tk), dtype=np.uint8)
+    m = mask.c()
+    if lib().or_allowed_matrix(Tq, Tk, _ptr(cu), cu.shape[0] - 1, ctypes.byref(m), _ptr(out)) != 0:
+        raise ValueError("or_allowed_matrix failed")
+    return out.astype(bool)
+
+
+def merge(oa, la, ob, lb):
+    """fp64 online-softmax merge; O [tokens, heads, d], lse [heads, tokens]."""
+    oa = np.ascontiguousarray(oa, dtype=np.float64)
+    ob = np.ascontiguousarray(ob, dtype=np.float64)
+    la = np.ascontiguousarray(la, dtype=np.float64)
+    lb = np.ascontiguousarray(lb, dtype=np.float64)
+    t, h, d = oa.shape
+    o = np.zeros_like(oa)
+    l = np.zeros_like(la)
+    lib().or_merge(_ptr(oa), _ptr(la), _ptr(ob), _ptr(lb), _ptr(o), _ptr(l), t, h, d)
+    return o, l
+
+
+def lpt(cost: Sequence[int], bins: int):
+    """LPT: (assign [n] bin per item, order [n] items in assignment order, loads [bins])."""
+    c = np.ascontiguousarray(np.asarray(cost, dtype=np.int64))
+    n = c.shape[0]
+    assign = np.zeros(max(n, 1), dtype=np.int32)
+    order = np.zeros(max(n, 1), dtype=np.int64)
+    loads = np.zeros(bins, dtype=np.int64)
+    if lib().or_lpt(_ptr(c), n, bins, _ptr(assign), _ptr(order), _ptr(loads)) != 0:
+        raise ValueError("or_lpt failed")
+    return assign[:n], order[:n], loads
+
+
+UNIT_FIELDS = ("uid", "seg", "t0", "t1", "h0", "h1", "kvh", "run_begin", "run_count", "cta")
+
+
+def worklist(cu: np.ndarray, mask: Mask, tile_m: int, tile_n: int, hq: int, hkv: int,
+             num_ctas: int, c_tile: int = 0) -> dict:
+    """Worklist of the method (segments, slices, units in CTA order, runs, CSR)."""
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    nd = cu.shape[0] - 1
+    counts = np.zeros(5, dtype=np.int64)
+    m = mask.c()
+    L = lib()
+    rc = L.or_worklist(_ptr(cu), nd, ctypes.byref(m), tile_m, tile_n, hq, hkv, num_ctas,
+                       int(c_tile), _ptr(counts), None, None, None, None, None, None, None)
+    if rc != 0:
+        raise ValueError(f"or_worklist failed ({rc})")
+    nseg, nsl, nu, nr = (int(x) for x in counts[:4])
+    slices = np.zeros((max(nsl, 1), 8), dtype=np.int32)
+    segs = np.zeros((max(nseg, 1), 5), dtype=np.int32)
+    units = np.zeros((max(nu, 1), 10), dtype=np.int32)
+    cost = np.zeros(max(nu, 1), dtype=np.int64)
+    pairs = np.zeros(max(nu, 1), dtype=np.int64)
+    runs = np.zeros((max(nr, 1), 3), dtype=np.int32)
+    off = np.zeros(num_ctas + 1, dtype=np.int32)
+    rc = L.or_worklist(_ptr(cu), nd, ctypes.byref(m), tile_m, tile_n, hq, hkv, num_ctas,
+                       int(c_tile), _ptr(counts), _ptr(slices), _ptr(segs), _ptr(units),
+                       _ptr(cost), _ptr(pairs), _ptr(runs), _ptr(off))
+    if rc != 0:
+        raise ValueError(f"or_worklist failed ({rc})")
+    return {"slices": slices[:nsl], "segs": segs[:nseg], "units": units[:nu],
+            "unit_cost": cost[:nu], "unit_pairs": pairs[:nu], "runs": runs[:nr],
+            "cta_off": off, "pairs_per_head": int(counts[4])}

@@ -1,0 +1,790 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for packed document-masked
+ * attention, its worklist, zigzag context-parallel maps and the
+ * online-softmax merge.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this code.  It shares no code, header
+ * or table with the CUDA library; the only thing both sides share is the
+ * seeded input generator (document lengths and bf16 tensors).
+ *
+ * Every function states the passage it follows.  Page titles:
+ *   [P1] "03 · 长文负载均衡" (llm-infra-atlas, long-context load balancing)
+ *   [P2] "数据并行负载均衡" (loongforge DP load balance)
+ *   [P4] "长序列训练与上下文并行" (long-sequence training and context parallelism)
+ *
+ * Parity status: every function below is pinned by the CPU tests
+ * (closed forms, brute force, library routines on tiny inputs, invariants).
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* bf16 -> double: the bf16 bit pattern is the top half of an fp32; the      */
+/* widening to double is exact.                                              */
+/* ------------------------------------------------------------------------ */
+static double bf16_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int32_t or_num_threads(void) {
+#ifdef _OPENMP
+    return (int32_t)omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Zigzag shard map.  [P1] §1.2 and §4.2: the sequence is cut into 2*cp      */
+/* chunks and rank i owns chunk i and chunk 2cp-1-i.  [P1] §4.3 (WLB-LLM     */
+/* per-document sharding): every document is cut on its own, so each rank   */
+/* gets a symmetric pair of chunks of every document.  Remainder rule (the   */
+/* page only says "round-robin"): chunk c of a document of length L gets     */
+/* floor(L/2cp) tokens plus one if c < L mod 2cp; chunks are contiguous in   */
+/* chunk order.  Rank r's local rows are, document by document, chunk r      */
+/* followed by chunk 2cp-1-r.                                                */
+/* ------------------------------------------------------------------------ */
+static void zz_chunk(int32_t len, int32_t cp, int32_t c, int32_t *off, int32_t *clen) {
+    int32_t n = 2 * cp;
+    int32_t base = len / n, rem = len % n;
+    *clen = base + (c < rem ? 1 : 0);
+    *off = c * base + (c < rem ? c : rem);
+}
+
+int32_t or_zigzag_map(const int32_t *cu, int32_t ndocs, int32_t cp, int32_t rank,
+                      int32_t *map, int32_t *chunk_table) {
+    if (cp <= 0 || rank < 0 || rank >= cp) return -1;
+    int32_t local = 0;
+    for (int32_t d = 0; d < ndocs; ++d) {
+        int32_t len = cu[d + 1] - cu[d];
+        int32_t chunks[2] = {rank, 2 * cp - 1 - rank};
+        for (int e = 0; e < 2; ++e) {
+            int32_t off, clen;
+            zz_chunk(len, cp, chunks[e], &off, &clen);
+            if (chunk_table) {
+                int32_t *row = chunk_table + ((int64_t)d * 2 + e) * 4;
+                row[0] = d;
+                row[1] = chunks[e];
+                row[2] = cu[d] + off;
+                row[3] = clen;
+            }
+            for (int32_t i = 0; i < clen; ++i) {
+                if (map) map[local] = cu[d] + off + i;
+                ++local;
+            }
+        }
+    }
+    return local;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Mask predicate: which (query row, key row) pairs are allowed.             */
+/*  - causal per document: [P1] §1.1 -- documents in a pack do not attend    */
+/*    to each other, so the work is sum_j l_j^2 (not (sum l_j)^2).           */
+/*  - sliding window and shared question: [P1] §1.2 (structured masks).      */
+/*    Reading: window w keeps keys with q_pos - k_pos < w (w keys including  */
+/*    the query itself).  Shared question: the first num_prefix documents   */
+/*    are questions that attend causally to themselves; every other          */
+/*    document (an answer) sees all question tokens and itself causally.    */
+/*  - zigzag pair (q rank r, kv rank s): rows are rank-local (map above);    */
+/*    allowed iff same document and k position <= q position ([P4] ring     */
+/*    attention, each rank's Q against one KV shard).                        */
+/*  - slices: [P1] §4.4 AttnSlice (QRange, KRange, FULL or CAUSAL), causal   */
+/*    compared on the slice's positions, with an optional window.            */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    const int32_t *cu;
+    int32_t ndocs;
+    or_mask_t m;
+    int32_t Tq, Tk;
+    int32_t *doc_q, *doc_k; /* document id of every q / k row */
+    int32_t *gq, *gk;       /* global token of every row (identity unless zigzag) */
+    int32_t *kdoc_lo, *kdoc_hi; /* per document: range of k rows holding it */
+} ctx_t;
+
+static int ctx_init(ctx_t *c, const int32_t *cu, int32_t ndocs, int32_t Tq, int32_t Tk,
+                    const or_mask_t *m) {
+    memset(c, 0, sizeof *c);
+    c->cu = cu;
+    c->ndocs = ndocs;
+    c->m = *m;
+    c->Tq = Tq;
+    c->Tk = Tk;
+    int32_t T = cu[ndocs];
+    int32_t *doc_of = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+    for (int32_t d = 0; d < ndocs; ++d)
+        for (int32_t t = cu[d]; t < cu[d + 1]; ++t) doc_of[t] = d;
+    c->gq = (int32_t *)malloc(sizeof(int32_t) * (size_t)(Tq > 0 ? Tq : 1));
+    c->gk = (int32_t *)malloc(sizeof(int32_t) * (size_t)(Tk > 0 ? Tk : 1));
+    if (m->kind == OR_MASK_ZIGZAG_PAIR) {
+        int32_t tq = or_zigzag_map(cu, ndocs, m->cp, m->q_rank, NULL, NULL);
+        int32_t tk = or_zigzag_map(cu, ndocs, m->cp, m->k_rank, NULL, NULL);
+        if (tq != Tq || tk != Tk) {
+            free(doc_of);
+            free(c->gq);
+            free(c->gk);
+            return -1;
+        }
+        or_zigzag_map(cu, ndocs, m->cp, m->q_rank, c->gq, NULL);
+        or_zigzag_map(cu, ndocs, m->cp, m->k_rank, c->gk, NULL);
+    } else {
+        if ((m->kind != OR_MASK_SLICES) && (Tq != T || Tk != T)) {
+            free(doc_of);
+            free(c->gq);
+            free(c->gk);
+            return -1;
+        }
+        for (int32_t i = 0; i < Tq; ++i) c->gq[i] = i;
+        for (int32_t j = 0; j < Tk; ++j) c->gk[j] = j;
+    }
+    c->doc_q = (int32_t *)malloc(sizeof(int32_t) * (size_t)(Tq > 0 ? Tq : 1));
+    c->doc_k = (int32_t *)malloc(sizeof(int32_t) * (size_t)(Tk > 0 ? Tk : 1));
+    for (int32_t i = 0; i < Tq; ++i) c->doc_q[i] = (c->gq[i] < T) ? doc_of[c->gq[i]] : -1;
+    for (int32_t j = 0; j < Tk; ++j) c->doc_k[j] = (c->gk[j] < T) ? doc_of[c->gk[j]] : -1;
+    c->kdoc_lo = (int32_t *)malloc(sizeof(int32_t) * (size_t)(ndocs > 0 ? ndocs : 1));
+    c->kdoc_hi = (int32_t *)malloc(sizeof(int32_t) * (size_t)(ndocs > 0 ? ndocs : 1));
+    for (int32_t d = 0; d < ndocs; ++d) {
+        c->kdoc_lo[d] = Tk;
+        c->kdoc_hi[d] = 0;
+    }
+    for (int32_t j = 0; j < Tk; ++j) {
+        int32_t d = c->doc_k[j];
+        if (d < 0) continue;
+        if (j < c->kdoc_lo[d]) c->kdoc_lo[d] = j;
+        if (j + 1 > c->kdoc_hi[d]) c->kdoc_hi[d] = j + 1;
+    }
+    free(doc_of);
+    return 0;
+}
+
+static void ctx_free(ctx_t *c) {
+    free(c->doc_q);
+    free(c->doc_k);
+    free(c->gq);
+    free(c->gk);
+    free(c->kdoc_lo);
+    free(c->kdoc_hi);
+}
+
+static int allowed(const ctx_t *c, int32_t i, int32_t j) {
+    const or_mask_t *m = &c->m;
+    switch (m->kind) {
+    case OR_MASK_CAUSAL:
+        return c->doc_q[i] == c->doc_k[j] && j <= i;
+    case OR_MASK_SLIDING_WINDOW:
+        return c->doc_q[i] == c->doc_k[j] && j <= i && (m->window <= 0 || i - j < m->window);
+    case OR_MASK_SHARED_QUESTION: {
+        int32_t dq = c->doc_q[i], dk = c->doc_k[j];
+        if (dq < m->num_prefix) return dk == dq && j <= i;
+        return dk < m->num_prefix || (dk == dq && j <= i);
+    }
+    case OR_MASK_ZIGZAG_PAIR:
+        return c->doc_q[i] == c->doc_k[j] && c->gk[j] <= c->gq[i];
+    case OR_MASK_SLICES:
+        for (int32_t s = 0; s < m->num_slices; ++s) {
+            const int32_t *sl = m->slices + 8 * s;
+            if (i < sl[0] || i >= sl[0] + sl[1] || j < sl[3] || j >= sl[3] + sl[4]) continue;
+            if (sl[6] == OR_SLICE_FULL) return 1;
+            int64_t qp = (int64_t)sl[2] + (i - sl[0]);
+            int64_t kp = (int64_t)sl[5] + (j - sl[3]);
+            if (kp <= qp && (sl[7] <= 0 || qp - kp < sl[7])) return 1;
+        }
+        return 0;
+    }
+    return 0;
+}
+
+/* Candidate key rows for query row i: a superset of the allowed set, so    */
+/* that large packs do not scan every key.  brute=1 scans all keys.          */
+static int candidates(const ctx_t *c, int32_t i, int brute, int32_t lo[2], int32_t hi[2]) {
+    if (brute || c->m.kind == OR_MASK_SLICES) {
+        lo[0] = 0;
+        hi[0] = c->Tk;
+        return 1;
+    }
+    int32_t d = c->doc_q[i];
+    if (d < 0) return 0;
+    switch (c->m.kind) {
+    case OR_MASK_CAUSAL:
+    case OR_MASK_SLIDING_WINDOW:
+        lo[0] = c->cu[d];
+        hi[0] = i + 1;
+        return 1;
+    case OR_MASK_SHARED_QUESTION:
+        if (d < c->m.num_prefix) {
+            lo[0] = c->cu[d];
+            hi[0] = i + 1;
+            return 1;
+        }
+        lo[0] = 0;
+        hi[0] = c->cu[c->m.num_prefix];
+        lo[1] = c->cu[d];
+        hi[1] = i + 1;
+        return 2;
+    case OR_MASK_ZIGZAG_PAIR:
+        lo[0] = c->kdoc_lo[d];
+        hi[0] = c->kdoc_hi[d];
+        return lo[0] < hi[0] ? 1 : 0;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Attention, by definition, in fp64 from the bf16 inputs.                   */
+/* For query row i and head h (kv head g = h / (Hq/Hkv), contiguous GQA      */
+/* groups), with A(i) the allowed keys:                                      */
+/*   s_j = scale * q_i . k_j,  LSE_i = ln sum_{j in A(i)} exp(s_j),          */
+/*   O_i = sum_{j in A(i)} exp(s_j - LSE_i) v_j.                             */
+/* The quadratic term of [P1] §1.1 (QK^T and PV), one row at a time.  Empty  */
+/* A(i): O = 0 and LSE = -inf.  The max is subtracted before exp only to     */
+/* keep fp64 in range; the value is the same.                                */
+/* ------------------------------------------------------------------------ */
+int or_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, int32_t Tq, int32_t Tk,
+                 int32_t Hq, int32_t Hkv, int32_t d, const int32_t *cu, int32_t ndocs,
+                 const or_mask_t *m, double scale, const int32_t *jobs, int64_t njobs,
+                 int32_t brute, double *out, double *lse) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    ctx_t c;
+    if (ctx_init(&c, cu, ndocs, Tq, Tk, m) != 0) return -2;
+    const int32_t G = Hq / Hkv;
+    const int64_t n = jobs ? njobs : (int64_t)Tq * Hq;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Tk > 0 ? Tk : 1));
+        int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)(Tk > 0 ? Tk : 1));
+        double *qi = (double *)malloc(sizeof(double) * (size_t)d);
+        double *acc = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t job = 0; job < n; ++job) {
+            int32_t i, h;
+            if (jobs) {
+                i = jobs[2 * job];
+                h = jobs[2 * job + 1];
+            } else {
+                i = (int32_t)(job / Hq);
+                h = (int32_t)(job % Hq);
+            }
+            if (i < 0 || i >= Tq || h < 0 || h >= Hq) {
+                err = 1;
+                continue;
+            }
+            const int32_t g = h / G;
+            for (int32_t e = 0; e < d; ++e) qi[e] = bf16_to_double(q[((int64_t)i * Hq + h) * d + e]);
+            int32_t lo[2], hi[2];
+            int nr = candidates(&c, i, brute, lo, hi);
+            int32_t cnt = 0;
+            double mx = -INFINITY;
+            for (int r = 0; r < nr; ++r) {
+                for (int32_t j = lo[r]; j < hi[r]; ++j) {
+                    if (!allowed(&c, i, j)) continue;
+                    const uint16_t *kj = k + ((int64_t)j * Hkv + g) * d;
+                    double dot = 0.0;
+                    for (int32_t e = 0; e < d; ++e) dot += qi[e] * bf16_to_double(kj[e]);
+                    s[cnt] = scale * dot;
+                    idx[cnt] = j;
+                    if (s[cnt] > mx) mx = s[cnt];
+                    ++cnt;
+                }
+            }
+            double *o = jobs ? out + job * d : out + ((int64_t)i * Hq + h) * d;
+            double *l = jobs ? lse + job : lse + (int64_t)h * Tq + i;
+            if (cnt == 0) {
+                for (int32_t e = 0; e < d; ++e) o[e] = 0.0;
+                *l = -INFINITY;
+                continue;
+            }
+            double sum = 0.0;
+            for (int32_t e = 0; e < d; ++e) acc[e] = 0.0;
+            for (int32_t t = 0; t < cnt; ++t) {
+                double p = exp(s[t] - mx);
+                sum += p;
+                const uint16_t *vj = v + ((int64_t)idx[t] * Hkv + g) * d;
+                for (int32_t e = 0; e < d; ++e) acc[e] += p * bf16_to_double(vj[e]);
+            }
+            for (int32_t e = 0; e < d; ++e) o[e] = acc[e] / sum;
+            *l = mx + log(sum);
+        }
+        free(s);
+        free(idx);
+        free(qi);
+        free(acc);
+    }
+    ctx_free(&c);
+    return err ? -3 : 0;
+}
+
+/* Number of allowed (q row, k row) pairs, per head.  [P1] §1.1: this is     */
+/* the work term W_attn ~ sum_j l_j^2 of a pack.                             */
+int64_t or_pair_count(int32_t Tq, int32_t Tk, const int32_t *cu, int32_t ndocs,
+                      const or_mask_t *m, int32_t brute) {
+    ctx_t c;
+    if (ctx_init(&c, cu, ndocs, Tq, Tk, m) != 0) return -1;
+    int64_t total = 0;
+#pragma omp parallel for schedule(dynamic, 64) reduction(+ : total)
+    for (int32_t i = 0; i < Tq; ++i) {
+        int32_t lo[2], hi[2];
+        int nr = candidates(&c, i, brute, lo, hi);
+        for (int r = 0; r < nr; ++r)
+            for (int32_t j = lo[r]; j < hi[r]; ++j) total += allowed(&c, i, j);
+    }
+    ctx_free(&c);
+    return total;
+}
+
+/* Pairwise predicate exposed for tests (brute-force tile checks). */
+int or_allowed_matrix(int32_t Tq, int32_t Tk, const int32_t *cu, int32_t ndocs,
+                      const or_mask_t *m, uint8_t *out) {
+    ctx_t c;
+    if (ctx_init(&c, cu, ndocs, Tq, Tk, m) != 0) return -1;
+    for (int32_t i = 0; i < Tq; ++i)
+        for (int32_t j = 0; j < Tk; ++j) out[(int64_t)i * Tk + j] = (uint8_t)allowed(&c, i, j);
+    ctx_free(&c);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Online-softmax merge of two partial results over disjoint key sets.       */
+/* [P1] §3.2 (DCP): partial outputs of several computation blocks of one O   */
+/* block are reduced by online-softmax rescale-and-sum; [P4] ring attention: */
+/* each step's local result is merged into the running state.                */
+/*   lse = ln(e^{lse_a} + e^{lse_b}),  O = e^{lse_a-lse} O_a + e^{lse_b-lse} O_b */
+/* Both -inf: O = 0, lse = -inf.  Layout O [tokens, heads, d], lse [heads,    */
+/* tokens].                                                                  */
+/* ------------------------------------------------------------------------ */
+void or_merge(const double *oa, const double *la, const double *ob, const double *lb, double *o,
+              double *l, int64_t tokens, int32_t heads, int32_t d) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < tokens; ++t) {
+        for (int32_t h = 0; h < heads; ++h) {
+            double a = la[(int64_t)h * tokens + t], b = lb[(int64_t)h * tokens + t];
+            const double *xa = oa + (t * heads + h) * d, *xb = ob + (t * heads + h) * d;
+            double *y = o + (t * heads + h) * d;
+            if (a == -INFINITY && b == -INFINITY) {
+                for (int32_t e = 0; e < d; ++e) y[e] = 0.0;
+                l[(int64_t)h * tokens + t] = -INFINITY;
+                continue;
+            }
+            double mx = a > b ? a : b;
+            double lse = mx + log(exp(a - mx) + exp(b - mx));
+            double wa = exp(a - lse), wb = exp(b - lse);
+            for (int32_t e = 0; e < d; ++e) y[e] = wa * xa[e] + wb * xb[e];
+            l[(int64_t)h * tokens + t] = lse;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Worklist.                                                                 */
+/* [P1] §3.2: attention is cut into tiles; Libra TAP charges each tile its   */
+/* exact causal query-key pair count, and DCP creates a computation block    */
+/* only for (Q block, KV block) pairs whose mask is not all zero.            */
+/* [P1] §2.1 (VRSP) and [P2] §4.4 phase 1: LPT -- sort by cost, descending,  */
+/* and put each item on the currently lightest bin.  Here the bins are the   */
+/* persistent CTAs of one GPU.                                               */
+/*                                                                           */
+/* Readings where the pages leave the step open:                             */
+/*  - segments: a maximal group of slices with the same query range; q tiles */
+/*    of tile_m rows are aligned at the segment start, kv tiles of tile_n    */
+/*    rows at each slice's key start (document-local tiles).                 */
+/*  - a slice's kv span for a q tile is [floor(min lo / tile_n),             */
+/*    ceil(max hi / tile_n)) over the rows' allowed key intervals.           */
+/*  - units: two query sub-tiles that share one kv head and the kv tiles.    */
+/*    With G = Hq/Hkv: heads (2p, 2p+1) of a group on the same q tile; if G  */
+/*    is odd the group's last head pairs consecutive q tiles (2u, 2u+1).     */
+/*    Enumeration order: segment, kv head, head pair, q tile; then the odd  */
+/*    head's tile pairs.                                                     */
+/*  - unit cost = exact allowed pairs of both sub-tiles + c_tile * (sub-tiles */
+/*    * kv tiles computed); c_tile = 0 is pure pair counting.                */
+/*  - LPT ties: sort is stable on the enumeration index; the lightest bin   */
+/*    with the lowest id wins a tie.  A bin's list is in assignment order.   */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int32_t q_row0, q_len, q_pos0, k_row0, k_len, k_pos0, type, window;
+} slice_t;
+
+typedef struct {
+    int32_t q_row0, q_len, q_pos0, slice_begin, slice_count;
+} seg_t;
+
+typedef struct {
+    slice_t *sl;
+    int64_t nsl, cap_sl;
+    seg_t *sg;
+    int64_t nsg, cap_sg;
+} plan_t;
+
+static void push_slice(plan_t *p, slice_t s) {
+    if (p->nsl == p->cap_sl) {
+        p->cap_sl = p->cap_sl ? 2 * p->cap_sl : 64;
+        p->sl = (slice_t *)realloc(p->sl, sizeof(slice_t) * (size_t)p->cap_sl);
+    }
+    p->sl[p->nsl++] = s;
+}
+
+static void push_seg(plan_t *p, int32_t q_row0, int32_t q_len, int32_t q_pos0, int64_t first) {
+    if (p->nsg == p->cap_sg) {
+        p->cap_sg = p->cap_sg ? 2 * p->cap_sg : 64;
+        p->sg = (seg_t *)realloc(p->sg, sizeof(seg_t) * (size_t)p->cap_sg);
+    }
+    seg_t g = {q_row0, q_len, q_pos0, (int32_t)first, (int32_t)(p->nsl - first)};
+    p->sg[p->nsg++] = g;
+}
+
+/* Slices of every mask kind, in the order the worklist enumerates them. */
+static int derive_plan(const int32_t *cu, int32_t ndocs, const or_mask_t *m, plan_t *p) {
+    memset(p, 0, sizeof *p);
+    switch (m->kind) {
+    case OR_MASK_CAUSAL:
+    case OR_MASK_SLIDING_WINDOW:
+        for (int32_t d = 0; d < ndocs; ++d) {
+            int32_t len = cu[d + 1] - cu[d];
+            if (len <= 0) continue;
+            int64_t first = p->nsl;
+            slice_t s = {cu[d], len, 0, cu[d], len, 0, OR_SLICE_CAUSAL,
+                         m->kind == OR_MASK_SLIDING_WINDOW ? m->window : 0};
+            push_slice(p, s);
+            push_seg(p, cu[d], len, 0, first);
+        }
+        return 0;
+    case OR_MASK_SHARED_QUESTION:
+        if (m->num_prefix < 0 || m->num_prefix > ndocs) return -1;
+        for (int32_t d = 0; d < ndocs; ++d) {
+            int32_t len = cu[d + 1] - cu[d];
+            if (len <= 0) continue;
+            int64_t first = p->nsl;
+            if (d >= m->num_prefix) {
+                for (int32_t q = 0; q < m->num_prefix; ++q) {
+                    int32_t ql = cu[q + 1] - cu[q];
+                    if (ql <= 0) continue;
+                    slice_t s = {cu[d], len, 0, cu[q], ql, 0, OR_SLICE_FULL, 0};
+                    push_slice(p, s);
+                }
+            }
+            slice_t s = {cu[d], len, 0, cu[d], len, 0, OR_SLICE_CAUSAL, 0};
+            push_slice(p, s);
+            push_seg(p, cu[d], len, 0, first);
+        }
+        return 0;
+    case OR_MASK_ZIGZAG_PAIR: {
+        int32_t cp = m->cp, r = m->q_rank, s = m->k_rank;
+        if (cp <= 0 || r < 0 || r >= cp || s < 0 || s >= cp) return -1;
+        int32_t qloc = 0, kloc = 0;
+        for (int32_t d = 0; d < ndocs; ++d) {
+            int32_t len = cu[d + 1] - cu[d];
+            int32_t qc[2] = {r, 2 * cp - 1 - r}, kc[2] = {s, 2 * cp - 1 - s};
+            int32_t qoff[2], qlen[2], koff[2], klen[2], kl0[2];
+            for (int e = 0; e < 2; ++e) {
+                zz_chunk(len, cp, qc[e], &qoff[e], &qlen[e]);
+                zz_chunk(len, cp, kc[e], &koff[e], &klen[e]);
+            }
+            kl0[0] = kloc;
+            kl0[1] = kloc + klen[0];
+            int32_t ql0 = qloc;
+            for (int e = 0; e < 2; ++e) {
+                if (qlen[e] > 0) {
+                    int64_t first = p->nsl;
+                    for (int f = 0; f < 2; ++f) {
+                        if (klen[f] <= 0) continue;
+                        if (koff[f] > qoff[e] + qlen[e] - 1) continue; /* no allowed pair */
+                        slice_t sl = {ql0, qlen[e], qoff[e], kl0[f], klen[f], koff[f],
+                                      OR_SLICE_CAUSAL, 0};
+                        push_slice(p, sl);
+                    }
+                    if (p->nsl > first) push_seg(p, ql0, qlen[e], qoff[e], first);
+                }
+                ql0 += qlen[e];
+            }
+            qloc += qlen[0] + qlen[1];
+            kloc += klen[0] + klen[1];
+        }
+        return 0;
+    }
+    case OR_MASK_SLICES: {
+        int64_t i = 0;
+        while (i < m->num_slices) {
+            const int32_t *a = m->slices + 8 * i;
+            int64_t first = p->nsl;
+            int64_t j = i;
+            while (j < m->num_slices) {
+                const int32_t *b = m->slices + 8 * j;
+                if (b[0] != a[0] || b[1] != a[1] || b[2] != a[2]) break;
+                slice_t s = {b[0], b[1], b[2], b[3], b[4], b[5], b[6], b[7]};
+                push_slice(p, s);
+                ++j;
+            }
+            push_seg(p, a[0], a[1], a[2], first);
+            i = j;
+        }
+        /* q ranges of different segments must not overlap */
+        for (int64_t x = 0; x < p->nsg; ++x)
+            for (int64_t y = x + 1; y < p->nsg; ++y) {
+                const seg_t *A = &p->sg[x], *B = &p->sg[y];
+                if (A->q_row0 < B->q_row0 + B->q_len && B->q_row0 < A->q_row0 + A->q_len)
+                    return -1;
+            }
+        return 0;
+    }
+    }
+    return -1;
+}
+
+/* Allowed key interval [lo, hi) (slice-local key index) of one query row.  */
+static void row_interval(const slice_t *s, int32_t r, int64_t *lo, int64_t *hi) {
+    if (s->type == OR_SLICE_FULL) {
+        *lo = 0;
+        *hi = s->k_len;
+        return;
+    }
+    int64_t qp = (int64_t)s->q_pos0 + r;
+    int64_t h = qp - s->k_pos0 + 1;
+    int64_t l = 0;
+    if (s->window > 0) l = qp - s->k_pos0 - s->window + 1;
+    if (l < 0) l = 0;
+    if (h > s->k_len) h = s->k_len;
+    *lo = l;
+    *hi = h;
+}
+
+/* kv tile span and pair count of q tile t of segment g against slice s.    */
+static void tile_span(const seg_t *g, const slice_t *s, int32_t t, int32_t tile_m, int32_t tile_n,
+                      int32_t *lo_t, int32_t *hi_t, int64_t *pairs) {
+    int64_t mn = INT64_MAX, mx = -1, cnt = 0;
+    int32_t r0 = t * tile_m, r1 = r0 + tile_m;
+    if (r1 > g->q_len) r1 = g->q_len;
+    for (int32_t r = r0; r < r1; ++r) {
+        int64_t lo, hi;
+        row_interval(s, r, &lo, &hi);
+        if (hi <= lo) continue;
+        cnt += hi - lo;
+        if (lo < mn) mn = lo;
+        if (hi > mx) mx = hi;
+    }
+    if (cnt == 0) {
+        *lo_t = *hi_t = 0;
+    } else {
+        *lo_t = (int32_t)(mn / tile_n);
+        *hi_t = (int32_t)((mx + tile_n - 1) / tile_n);
+    }
+    *pairs = cnt;
+}
+
+typedef struct {
+    int32_t seg, t0, t1, h0, h1, kvh;
+    int64_t run_begin;
+    int32_t run_count;
+    int64_t pairs, cost, tiles;
+} unit_t;
+
+typedef struct {
+    int64_t load;
+    int32_t id;
+} bin_t;
+
+static int bin_less(const bin_t *a, const bin_t *b) {
+    return a->load < b->load || (a->load == b->load && a->id < b->id);
+}
+
+static void heap_down(bin_t *h, int32_t n, int32_t i) {
+    for (;;) {
+        int32_t l = 2 * i + 1, r = l + 1, s = i;
+        if (l < n && bin_less(&h[l], &h[s])) s = l;
+        if (r < n && bin_less(&h[r], &h[s])) s = r;
+        if (s == i) return;
+        bin_t t = h[i];
+        h[i] = h[s];
+        h[s] = t;
+        i = s;
+    }
+}
+
+typedef struct {
+    int64_t cost;
+    int64_t idx;
+} key_t_;
+
+static int key_cmp(const void *a, const void *b) {
+    const key_t_ *x = (const key_t_ *)a, *y = (const key_t_ *)b;
+    if (x->cost != y->cost) return x->cost > y->cost ? -1 : 1; /* cost descending */
+    return x->idx < y->idx ? -1 : (x->idx > y->idx ? 1 : 0);  /* then index ascending */
+}
+
+/* LPT with a binary min-heap over (load, id). [P1] §2.1, [P2] §4.4.       */
+int or_lpt(const int64_t *cost, int64_t n, int32_t bins, int32_t *assign, int64_t *order,
+           int64_t *loads) {
+    if (bins <= 0) return -1;
+    key_t_ *keys = (key_t_ *)malloc(sizeof(key_t_) * (size_t)(n > 0 ? n : 1));
+    for (int64_t i = 0; i < n; ++i) {
+        keys[i].cost = cost[i];
+        keys[i].idx = i;
+    }
+    qsort(keys, (size_t)n, sizeof(key_t_), key_cmp);
+    bin_t *h = (bin_t *)malloc(sizeof(bin_t) * (size_t)bins);
+    for (int32_t b = 0; b < bins; ++b) {
+        h[b].load = 0;
+        h[b].id = b;
+    }
+    /* all loads zero: ids ascending already form a valid heap */
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t u = keys[i].idx;
+        assign[u] = h[0].id;
+        if (order) order[i] = u;
+        h[0].load += keys[i].cost;
+        heap_down(h, bins, 0);
+    }
+    if (loads) {
+        for (int32_t b = 0; b < bins; ++b) loads[h[b].id] = h[b].load;
+    }
+    free(h);
+    free(keys);
+    return 0;
+}
+
+/* Worklist: counts first (out arrays NULL), then fill. counts[0..4] =      */
+/* segments, slices, units, runs, total pairs per head.                      */
+int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t tile_m,
+                int32_t tile_n, int32_t Hq, int32_t Hkv, int32_t num_ctas, int64_t c_tile,
+                int64_t *counts, int32_t *slices_out, int32_t *segs_out, int32_t *units_out,
+                int64_t *unit_cost_out, int64_t *unit_pairs_out, int32_t *runs_out,
+                int32_t *cta_off_out) {
+    if (tile_m <= 0 || tile_n <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_ctas <= 0) return -1;
+    plan_t p;
+    if (derive_plan(cu, ndocs, m, &p) != 0) {
+        free(p.sl);
+        free(p.sg);
+        return -2;
+    }
+    const int32_t G = Hq / Hkv;
+    int64_t nunits = 0, nruns = 0, pairs_head = 0;
+    for (int64_t g = 0; g < p.nsg; ++g) {
+        int32_t nt = (p.sg[g].q_len + tile_m - 1) / tile_m;
+        int64_t u = (int64_t)Hkv * ((int64_t)(G / 2) * nt + (G % 2) * ((nt + 1) / 2));
+        nunits += u;
+        nruns += u * p.sg[g].slice_count;
+        for (int32_t sidx = 0; sidx < p.sg[g].slice_count; ++sidx)
+            for (int32_t t = 0; t < nt; ++t) {
+                int32_t a, b;
+                int64_t pr;
+                tile_span(&p.sg[g], &p.sl[p.sg[g].slice_begin + sidx], t, tile_m, tile_n, &a, &b,
+                          &pr);
+                pairs_head += pr;
+            }
+    }
+    counts[0] = p.nsg;
+    counts[1] = p.nsl;
+    counts[2] = nunits;
+    counts[3] = nruns;
+    counts[4] = pairs_head;
+    if (!units_out) {
+        free(p.sl);
+        free(p.sg);
+        return 0;
+    }
+    for (int64_t i = 0; i < p.nsl; ++i) {
+        const slice_t *s = &p.sl[i];
+        int32_t *o = slices_out + 8 * i;
+        o[0] = s->q_row0; o[1] = s->q_len; o[2] = s->q_pos0; o[3] = s->k_row0;
+        o[4] = s->k_len; o[5] = s->k_pos0; o[6] = s->type; o[7] = s->window;
+    }
+    for (int64_t g = 0; g < p.nsg; ++g) {
+        int32_t *o = segs_out + 5 * g;
+        o[0] = p.sg[g].q_row0; o[1] = p.sg[g].q_len; o[2] = p.sg[g].q_pos0;
+        o[3] = p.sg[g].slice_begin; o[4] = p.sg[g].slice_count;
+    }
+    unit_t *U = (unit_t *)malloc(sizeof(unit_t) * (size_t)(nunits > 0 ? nunits : 1));
+    int64_t ui = 0, ri = 0;
+    for (int64_t g = 0; g < p.nsg; ++g) {
+        const seg_t *sg = &p.sg[g];
+        int32_t nt = (sg->q_len + tile_m - 1) / tile_m;
+        for (int32_t kvh = 0; kvh < Hkv; ++kvh) {
+            /* head pairs on the same q tile, then the odd head's tile pairs */
+            int32_t npair = G / 2;
+            int64_t total_here = (int64_t)npair * nt + (G % 2) * ((nt + 1) / 2);
+            for (int64_t e = 0; e < total_here; ++e) {
+                unit_t u;
+                u.seg = (int32_t)g;
+                u.kvh = kvh;
+                if (e < (int64_t)npair * nt) {
+                    int32_t pp = (int32_t)(e / nt), t = (int32_t)(e % nt);
+                    u.t0 = u.t1 = t;
+                    u.h0 = kvh * G + 2 * pp;
+                    u.h1 = u.h0 + 1;
+                } else {
+                    int32_t uu = (int32_t)(e - (int64_t)npair * nt);
+                    u.t0 = 2 * uu;
+                    u.t1 = (2 * uu + 1 < nt) ? 2 * uu + 1 : -1;
+                    u.h0 = kvh * G + G - 1;
+                    u.h1 = (u.t1 >= 0) ? u.h0 : -1;
+                }
+                int nsub = (u.h1 >= 0) ? 2 : 1;
+                u.run_begin = ri;
+                u.run_count = sg->slice_count;
+                u.pairs = 0;
+                u.tiles = 0;
+                for (int32_t sidx = 0; sidx < sg->slice_count; ++sidx) {
+                    const slice_t *s = &p.sl[sg->slice_begin + sidx];
+                    int32_t lo = 0, hi = 0, have = 0;
+                    int32_t ts[2] = {u.t0, u.t1};
+                    for (int k2 = 0; k2 < nsub; ++k2) {
+                        int32_t a, b;
+                        int64_t pr;
+                        tile_span(sg, s, ts[k2], tile_m, tile_n, &a, &b, &pr);
+                        u.pairs += pr;
+                        if (b > a) {
+                            if (!have || a < lo) lo = a;
+                            if (!have || b > hi) hi = b;
+                            have = 1;
+                        }
+                    }
+                    int32_t *ro = runs_out + 3 * ri;
+                    ro[0] = sg->slice_begin + sidx;
+                    ro[1] = lo;
+                    ro[2] = hi;
+                    u.tiles += (int64_t)(hi - lo) * nsub;
+                    ++ri;
+                }
+                u.cost = u.pairs + c_tile * u.tiles;
+                U[ui++] = u;
+            }
+        }
+    }
+    int64_t *cost = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nunits > 0 ? nunits : 1));
+    int32_t *assign = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nunits > 0 ? nunits : 1));
+    int64_t *order = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nunits > 0 ? nunits : 1));
+    for (int64_t i = 0; i < nunits; ++i) cost[i] = U[i].cost;
+    or_lpt(cost, nunits, num_ctas, assign, order, NULL);
+    /* CSR: per bin, units in assignment order */
+    int32_t *fill = (int32_t *)calloc((size_t)num_ctas + 1, sizeof(int32_t));
+    for (int64_t i = 0; i < nunits; ++i) fill[assign[i] + 1]++;
+    for (int32_t b = 0; b < num_ctas; ++b) fill[b + 1] += fill[b];
+    for (int32_t b = 0; b <= num_ctas; ++b) cta_off_out[b] = fill[b];
+    for (int64_t i = 0; i < nunits; ++i) {
+        int64_t u = order[i];
+        int32_t pos = fill[assign[u]]++;
+        int32_t *o = units_out + 10 * (int64_t)pos;
+        o[0] = (int32_t)u; o[1] = U[u].seg; o[2] = U[u].t0; o[3] = U[u].t1; o[4] = U[u].h0;
+        o[5] = U[u].h1; o[6] = U[u].kvh; o[7] = (int32_t)U[u].run_begin; o[8] = U[u].run_count;
+        o[9] = assign[u];
+        unit_cost_out[pos] = U[u].cost;
+        unit_pairs_out[pos] = U[u].pairs;
+    }
+    free(fill);
+    free(order);
+    free(assign);
+    free(cost);
+    free(U);
+    free(p.sl);
+    free(p.sg);
+    return 0;
+}

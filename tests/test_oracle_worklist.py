@@ -1,0 +1,146 @@
+"""Pins of the oracle's worklist by brute force on tiny packs.
+
+"03 · 长文负载均衡" §3.2: a computation block exists only for a (Q block,
+KV block) pair whose mask is not all zero, and a tile is charged its exact
+query-key pair count.  These tests rebuild, element by element, the pairs
+each worklist unit would compute (slice semantics: FULL, or CAUSAL on
+positions with an optional window) and check them against the mask predicate
+written from the definitions: every allowed pair is computed exactly once per
+head and no tile in a run is empty.
+"""
+import numpy as np
+import pytest
+
+from packed_varlen_attention_cu_gb300 import workloads as W
+
+
+def slice_accepts(sl, i, j):
+    q_row0, q_len, q_pos0, k_row0, k_len, k_pos0, typ, win = (int(x) for x in sl)
+    if not (q_row0 <= i < q_row0 + q_len and k_row0 <= j < k_row0 + k_len):
+        return False
+    if typ == 0:
+        return True
+    qp, kp = q_pos0 + i - q_row0, k_pos0 + j - k_row0
+    return kp <= qp and (win <= 0 or qp - kp < win)
+
+
+def coverage(wl, tq, tk, hq, tile_m, tile_n):
+    cov = np.zeros((hq, tq, tk), dtype=np.int32)
+    per_unit = []
+    empty_tiles = 0
+    for u in wl["units"]:
+        uid, seg, t0, t1, h0, h1, kvh, rb, rc, cta = (int(x) for x in u)
+        sg = wl["segs"][seg]
+        subs = [(t0, h0)] + ([(t1, h1)] if h1 >= 0 else [])
+        cnt = 0
+        for r in range(rb, rb + rc):
+            sidx, lo, hi = (int(x) for x in wl["runs"][r])
+            sl = wl["slices"][sidx]
+            assert sl[0] == sg[0] and sl[1] == sg[1]
+            for kt in range(lo, hi):
+                k0 = sl[3] + kt * tile_n
+                k1 = min(k0 + tile_n, sl[3] + sl[4])
+                hit = 0
+                for (t, h) in subs:
+                    r0 = sg[0] + t * tile_m
+                    r1 = min(r0 + tile_m, sg[0] + sg[1])
+                    for i in range(r0, r1):
+                        for j in range(k0, k1):
+                            if slice_accepts(sl, i, j):
+                                cov[h, i, j] += 1
+                                cnt += 1
+                                hit += 1
+                empty_tiles += hit == 0
+        per_unit.append(cnt)
+    return cov, np.array(per_unit), empty_tiles
+
+
+CASES = [
+    ([5, 17, 1, 9, 0, 12], W.MASK_CAUSAL, {}),
+    ([23, 3, 16], W.MASK_SLIDING_WINDOW, {"window": 5}),
+    ([16, 7, 9, 13], W.MASK_SHARED_QUESTION, {"num_prefix": 1}),
+    ([6, 5, 11, 4], W.MASK_SHARED_QUESTION, {"num_prefix": 2}),
+]
+
+
+@pytest.mark.parametrize("lengths,kind,kw", CASES)
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2), (3, 1), (2, 1)])
+@pytest.mark.parametrize("tile_m,tile_n", [(4, 4), (8, 4), (4, 8)])
+def test_worklist_covers_allowed_pairs_once(oracle_mod, lengths, kind, kw, hq, hkv, tile_m, tile_n):
+    cu = W.cu_seqlens_of(lengths)
+    T = int(cu[-1])
+    m = oracle_mod.Mask(kind, **kw)
+    wl = oracle_mod.worklist(cu, m, tile_m, tile_n, hq, hkv, num_ctas=5, c_tile=3)
+    A = oracle_mod.allowed_matrix(cu, m)
+    cov, per_unit, empty = coverage(wl, T, T, hq, tile_m, tile_n)
+    for h in range(hq):
+        np.testing.assert_array_equal(cov[h], A.astype(np.int32))
+    assert empty == 0
+    np.testing.assert_array_equal(per_unit, wl["unit_pairs"])
+    assert wl["pairs_per_head"] == int(A.sum())
+    # cost = pairs + c_tile * (sub-tiles x kv tiles computed)
+    for u, c, p in zip(wl["units"], wl["unit_cost"], wl["unit_pairs"]):
+        nsub = 2 if u[5] >= 0 else 1
+        tiles = sum(int(wl["runs"][r][2] - wl["runs"][r][1]) for r in range(u[7], u[7] + u[8]))
+        assert c == p + 3 * nsub * tiles
+
+
+@pytest.mark.parametrize("cp", [2, 3])
+def test_worklist_zigzag_pairs_cover_once(oracle_mod, cp):
+    lengths = [19, 7, 2, 30, 0, 12]
+    cu = W.cu_seqlens_of(lengths)
+    for r in range(cp):
+        tq = oracle_mod.zigzag_map(cu, cp, r)[0].shape[0]
+        for s in range(cp):
+            tk = oracle_mod.zigzag_map(cu, cp, s)[0].shape[0]
+            m = oracle_mod.Mask(W.MASK_ZIGZAG_PAIR, cp=cp, q_rank=r, k_rank=s)
+            wl = oracle_mod.worklist(cu, m, 4, 4, 2, 1, num_ctas=3)
+            A = oracle_mod.allowed_matrix(cu, m, Tq=tq, Tk=tk)
+            cov, per_unit, empty = coverage(wl, tq, tk, 2, 4, 4)
+            for h in range(2):
+                np.testing.assert_array_equal(cov[h], A.astype(np.int32))
+            assert empty == 0
+            np.testing.assert_array_equal(per_unit, wl["unit_pairs"])
+
+
+def test_worklist_explicit_slices(oracle_mod):
+    # two q segments; the second sees a FULL block and a shifted causal block
+    sl = np.array([[0, 10, 0, 0, 10, 0, 1, 0],
+                   [10, 9, 30, 0, 6, 0, 0, 0],
+                   [10, 9, 30, 10, 12, 25, 1, 4]], dtype=np.int32)
+    m = oracle_mod.Mask(W.MASK_SLICES, slices=sl)
+    cu = W.cu_seqlens_of([22])
+    wl = oracle_mod.worklist(cu, m, 4, 4, 2, 2, num_ctas=2)
+    A = oracle_mod.allowed_matrix(cu, m, Tq=22, Tk=22)
+    cov, per_unit, empty = coverage(wl, 22, 22, 2, 4, 4)
+    np.testing.assert_array_equal(cov[0], A.astype(np.int32))
+    assert empty == 0
+    assert len(wl["segs"]) == 2
+
+
+def test_square_tiles_causal_doc_closed_form(oracle_mod):
+    b, n = 8, 9
+    cu = W.cu_seqlens_of([b * n])
+    wl = oracle_mod.worklist(cu, oracle_mod.Mask(), b, b, 2, 1, num_ctas=4)
+    tiles = sum(int(r[2] - r[1]) for r in wl["runs"])
+    assert tiles == n * (n + 1) // 2
+
+
+def test_worklist_csr_is_lpt(oracle_mod):
+    w = W.tiny_pack()
+    wl = oracle_mod.worklist(w.cu_seqlens, oracle_mod.Mask(), 128, 128, 4, 4, num_ctas=7, c_tile=100)
+    off = wl["cta_off"]
+    units = wl["units"]
+    assert off[0] == 0 and off[-1] == len(units) and np.all(np.diff(off) >= 0)
+    assert sorted(units[:, 0].tolist()) == list(range(len(units)))
+    # LPT over the enumeration-order costs gives the same bins
+    cost_by_uid = np.zeros(len(units), dtype=np.int64)
+    cost_by_uid[units[:, 0]] = wl["unit_cost"]
+    assign, _, loads = oracle_mod.lpt(cost_by_uid, 7)
+    for b in range(7):
+        seg = units[off[b]:off[b + 1]]
+        assert np.all(seg[:, 9] == b)
+        assert np.all(assign[seg[:, 0]] == b)
+        c = wl["unit_cost"][off[b]:off[b + 1]]
+        assert np.all(np.diff(c) <= 0)
+        assert c.sum() == loads[b]
