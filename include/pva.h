@@ -1,0 +1,194 @@
+/*
+ * pva.h -- packed varlen (document-masked) attention on one GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer is either a HOST pointer or a DEVICE pointer, as
+ * stated per argument.  The caller allocates and owns every buffer (the
+ * library allocates no memory); device work is enqueued on the caller's
+ * CUDA stream (`stream` is a cudaStream_t, NULL = legacy default stream) and
+ * is asynchronous.  Argument errors are detected on the host and returned
+ * before anything is enqueued.  A launch failure returns PVA_ERR_CUDA.
+ * Device-side failures (a bounded wait that timed out, a worklist that does
+ * not match the call) are recorded in the worklist's error word and read
+ * with pva_worklist_error().
+ *
+ * The method is the hot path of the long-context load-balancing pages:
+ *  - "03 · 长文负载均衡" §1.1: documents packed into one sequence attend only
+ *    to themselves, so a pack's attention work is sum_j l_j^2, not
+ *    (sum_j l_j)^2; THD packing with cu_seqlens (§2.4).
+ *  - §1.2: structured masks (sliding window, shared question).
+ *  - §3.2: tiles charged by their exact causal query-key pair count (Libra
+ *    TAP); a computation block exists only where the mask is non-zero (DCP).
+ *  - §2.1 and "数据并行负载均衡" §4.4: LPT (longest processing time first)
+ *    placement, here over the persistent CTAs of one GPU.
+ *  - §4.2-4.3: zigzag context parallelism, per document.
+ *  - §3.2 and the ring-attention notes of "长序列训练与上下文并行": partial
+ *    (O, LSE) results merged by online softmax.
+ *
+ * Layouts (all row-major, contiguous, 16-byte aligned):
+ *   Q     [q_tokens, num_q_heads,  head_dim]  bf16
+ *   K, V  [k_tokens, num_kv_heads, head_dim]  bf16
+ *   O     [q_tokens, num_q_heads,  head_dim]  bf16, or fp32 for partials
+ *   LSE   [num_q_heads, q_tokens]             fp32, natural log
+ *   cu_seqlens int32 [num_docs + 1], 0 = cu[0] <= cu[1] <= ... (empty docs allowed)
+ * GQA: q head h reads kv head h / (num_q_heads / num_kv_heads).
+ * Rows with no allowed key produce O = 0 and LSE = -inf.
+ */
+#ifndef PVA_H
+#define PVA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PVA_OK = 0,
+    PVA_ERR_INVALID_ARG = 1,      /* bad size, pointer, alignment or mask field */
+    PVA_ERR_BUFFER_TOO_SMALL = 2, /* worklist buffer smaller than pva_worklist_bytes() */
+    PVA_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed */
+    PVA_ERR_UNSUPPORTED = 4,      /* valid but not implemented (head_dim, tiles) */
+    PVA_ERR_TIMEOUT = 5,          /* a device-side bounded wait expired */
+    PVA_ERR_DEVICE = 6            /* device-side consistency check failed */
+} pva_status;
+
+/* Mask kinds ("03 · 长文负载均衡" §1.1, §1.2, §4.2-4.4). */
+typedef enum {
+    PVA_MASK_CAUSAL = 0,          /* per document: k <= q */
+    PVA_MASK_SLIDING_WINDOW = 1,  /* per document: k <= q and q - k < window */
+    PVA_MASK_SHARED_QUESTION = 2, /* docs [0, num_prefix_docs) are questions (causal on
+                                     themselves); every later doc sees all question
+                                     tokens and itself causally */
+    PVA_MASK_ZIGZAG_PAIR = 3,     /* Q = zigzag shard of q_rank, K/V = shard of k_rank
+                                     (rows in pva_zigzag_shard order); same document and
+                                     k position <= q position */
+    PVA_MASK_SLICES = 4           /* explicit slice list (AttnSlice, §4.4) */
+} pva_mask_kind;
+
+typedef enum { PVA_SLICE_FULL = 0, PVA_SLICE_CAUSAL = 1 } pva_slice_type;
+
+/* One AttnSlice ("03 · 长文负载均衡" §4.4: (QRange, KRange, MaskType)).
+ * Rows are indices into the Q / K buffers; positions are the rows' token
+ * positions used by the causal test k_pos <= q_pos (and q_pos - k_pos < window
+ * when window > 0).  Consecutive slices with the same (q_row0, q_len, q_pos0)
+ * form one query segment; the query ranges of different segments must not
+ * overlap.  Query rows outside every slice are not written. */
+typedef struct {
+    int32_t q_row0, q_len, q_pos0;
+    int32_t k_row0, k_len, k_pos0;
+    int32_t type;   /* pva_slice_type */
+    int32_t window; /* <= 0: no window */
+} pva_slice;
+
+typedef struct {
+    int32_t kind;            /* pva_mask_kind */
+    int32_t window;          /* SLIDING_WINDOW: window >= 1 */
+    int32_t num_prefix_docs; /* SHARED_QUESTION */
+    int32_t cp, q_rank, k_rank; /* ZIGZAG_PAIR: 0 <= ranks < cp */
+    const pva_slice* slices;    /* SLICES: HOST array of num_slices entries */
+    int32_t num_slices;
+    int32_t q_tokens;        /* rows of Q / O (for ZIGZAG_PAIR: pva_zigzag_shard_len(q_rank)) */
+    int32_t k_tokens;        /* rows of K / V */
+} pva_mask_desc;
+
+/* Worklist parameters.  The attention kernel supports tile_m = tile_n = 128,
+ * head_dim 64 or 128.  Work units pair two 128-row query sub-tiles that share
+ * one kv head: two q heads of a GQA group on the same q tile, or (for a
+ * group's odd last head, or MHA) two consecutive q tiles of one head. */
+typedef struct {
+    int32_t tile_m, tile_n;
+    int32_t num_q_heads, num_kv_heads;
+    int32_t num_ctas;   /* persistent CTAs (bins of the LPT); <= 0: number of SMs */
+    int32_t reserved;
+    int64_t c_tile;     /* cost of one computed (sub-tile, kv tile) in pair units, >= 0;
+                           unit cost = exact allowed pairs + c_tile * tiles computed */
+} pva_worklist_params;
+
+/* Upper bound, in bytes, of the device worklist for this problem.  HOST
+ * computation only.  num_docs is the length of cu_seqlens minus one.
+ * Returns 0 on invalid arguments. */
+size_t pva_worklist_bytes(int32_t num_docs, const pva_mask_desc* mask,
+                          const pva_worklist_params* params);
+
+/* Build the worklist on the device ("03 · 长文负载均衡" §3.2, §2.1):
+ * derive the slices of the mask, enumerate every (query sub-tile, kv tile)
+ * work item with at least one allowed pair, cost each work unit by its exact
+ * pair count (+ c_tile per tile), sort by cost descending (stable) and assign
+ * LPT-style to params->num_ctas bins (lightest bin, lowest id on ties).
+ *   cu_seqlens_dev  DEVICE int32 [num_docs + 1]
+ *   worklist_dev    DEVICE buffer of worklist_bytes >= pva_worklist_bytes(), 256-B aligned
+ * The result is deterministic and identical for identical inputs. */
+pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t num_docs,
+                              const pva_mask_desc* mask, const pva_worklist_params* params,
+                              void* worklist_dev, size_t worklist_bytes, void* stream);
+
+/* Attention forward over the worklist: one persistent launch of
+ * params->num_ctas CTAs (TMA-staged K/V tiles, tcgen05 MMAs into TMEM,
+ * online softmax in fp32, masked tiles never visited).
+ *   q, k, v         DEVICE bf16, layouts above; head_dim 64 or 128
+ *   worklist_dev    DEVICE, built by pva_build_worklist with the same mask/params
+ *   out             DEVICE, bf16 (out_is_fp32 = 0) or fp32 (out_is_fp32 = 1)
+ *   lse             DEVICE fp32 [num_q_heads, q_tokens]
+ *   softmax_scale   <= 0 selects 1/sqrt(head_dim)
+ *   cta_busy_ns     DEVICE uint64 [num_ctas, 2] (start, end) globaltimer stamps, or NULL
+ * cu_seqlens_dev and mask describe the same problem as the worklist and are
+ * used only for argument checks. */
+pva_status pva_attn_fwd(const void* q, const void* k, const void* v,
+                        const int32_t* cu_seqlens_dev, const pva_mask_desc* mask,
+                        const pva_worklist_params* params, int32_t head_dim,
+                        const void* worklist_dev, void* out, int32_t out_is_fp32, float* lse,
+                        float softmax_scale, uint64_t* cta_busy_ns, void* stream);
+
+/* Rows of zigzag shard `rank` ("03 · 长文负载均衡" §4.2-4.3): every document
+ * is cut into 2*cp contiguous chunks, chunk c holding floor(l/2cp) tokens
+ * plus one if c < l mod 2cp; rank r owns chunks r and 2cp-1-r of every
+ * document.  HOST computation on a HOST cu_seqlens.  Returns -1 on bad input. */
+int32_t pva_zigzag_shard_len(const int32_t* cu_seqlens_host, int32_t num_docs, int32_t cp,
+                             int32_t rank);
+
+/* Zigzag index maps on the device.
+ *   cu_seqlens_dev   DEVICE int32 [num_docs + 1]
+ *   gather_map_dev   DEVICE int32 [pva_zigzag_shard_len(...)]: local row -> global token;
+ *                    per document, chunk r then chunk 2cp-1-r
+ *   chunk_table_dev  DEVICE int32 [num_docs][2][4] (doc, chunk, global start, length), or NULL */
+pva_status pva_zigzag_shard(const int32_t* cu_seqlens_dev, int32_t num_docs, int32_t cp,
+                            int32_t rank, int32_t* gather_map_dev, int32_t* chunk_table_dev,
+                            void* stream);
+
+/* Row gather for shard emulation: dst[i] = src[map[i]] for i < rows, rows of
+ * row_bytes bytes (a multiple of 16); scatter = 1 writes dst[map[i]] = src[i].
+ *   src, dst  DEVICE, 16-byte aligned;  map_dev DEVICE int32 [rows]
+ *   indexed_rows  rows of the tensor that map[] indexes (src, or dst when
+ *                 scattering); entries outside [0, indexed_rows) are skipped. */
+pva_status pva_gather_rows(const void* src, const int32_t* map_dev, void* dst, int64_t rows,
+                           int64_t row_bytes, int64_t indexed_rows, int32_t scatter,
+                           void* stream);
+
+/* Online-softmax merge of two partials over disjoint key sets
+ * ("03 · 长文负载均衡" §3.2 DCP reduction; ring attention merge):
+ *   lse = ln(e^{lse_a} + e^{lse_b}),  O = e^{lse_a - lse} O_a + e^{lse_b - lse} O_b
+ * Both -inf gives O = 0, lse = -inf.  O_a, O_b, out: DEVICE [tokens, heads, head_dim]
+ * fp32 (o_is_fp32 = 1) or bf16; lse_*: DEVICE fp32 [heads, tokens].  In place
+ * (out == o_a, lse_out == lse_a) is allowed. */
+pva_status pva_merge_partials(const void* o_a, const float* lse_a, const void* o_b,
+                              const float* lse_b, void* out, float* lse_out, int64_t tokens,
+                              int32_t heads, int32_t head_dim, int32_t o_is_fp32, void* stream);
+
+/* Device error word of a worklist (0 = none; otherwise the failing wait site,
+ * see PVA_ERR_TIMEOUT / PVA_ERR_DEVICE).  Synchronizes `stream`.
+ *   worklist_dev DEVICE;  code_out HOST */
+pva_status pva_worklist_error(const void* worklist_dev, int32_t* code_out, void* stream);
+
+/* Summary counts of a built worklist (HOST out, synchronizes `stream`):
+ * out[0] segments, [1] slices, [2] units, [3] runs, [4] allowed pairs per head,
+ * [5] kv tiles computed per sub-tile summed over units. */
+pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out6, void* stream);
+
+const char* pva_status_string(pva_status status);
+int32_t pva_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PVA_H */

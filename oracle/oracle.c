@@ -502,7 +502,8 @@ static int derive_plan(const int32_t *cu, int32_t ndocs, const or_mask_t *m, pla
                                       OR_SLICE_CAUSAL, 0};
                         push_slice(p, sl);
                     }
-                    if (p->nsl > first) push_seg(p, ql0, qlen[e], qoff[e], first);
+                    /* kept even with no slice: its rows then read O = 0, LSE = -inf */
+                    push_seg(p, ql0, qlen[e], qoff[e], first);
                 }
                 ql0 += qlen[e];
             }

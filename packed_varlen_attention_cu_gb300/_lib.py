@@ -1,0 +1,93 @@
+"""ctypes view of ``libpva.so`` (declarations mirror include/pva.h).
+
+Loading fails loudly when the library has not been built: there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpva.so")
+
+PVA_OK = 0
+STATUS_NAMES = {0: "PVA_OK", 1: "PVA_ERR_INVALID_ARG", 2: "PVA_ERR_BUFFER_TOO_SMALL",
+                3: "PVA_ERR_CUDA", 4: "PVA_ERR_UNSUPPORTED", 5: "PVA_ERR_TIMEOUT",
+                6: "PVA_ERR_DEVICE"}
+
+# Every symbol declared by include/pva.h.
+EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_zigzag_shard_len",
+           "pva_zigzag_shard", "pva_gather_rows", "pva_merge_partials", "pva_worklist_error",
+           "pva_worklist_counts", "pva_status_string", "pva_version")
+
+
+class Slice(ctypes.Structure):
+    _fields_ = [("q_row0", ctypes.c_int32), ("q_len", ctypes.c_int32), ("q_pos0", ctypes.c_int32),
+                ("k_row0", ctypes.c_int32), ("k_len", ctypes.c_int32), ("k_pos0", ctypes.c_int32),
+                ("type", ctypes.c_int32), ("window", ctypes.c_int32)]
+
+
+class MaskDesc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("num_prefix_docs", ctypes.c_int32), ("cp", ctypes.c_int32),
+                ("q_rank", ctypes.c_int32), ("k_rank", ctypes.c_int32),
+                ("slices", ctypes.POINTER(Slice)), ("num_slices", ctypes.c_int32),
+                ("q_tokens", ctypes.c_int32), ("k_tokens", ctypes.c_int32)]
+
+
+class WorklistParams(ctypes.Structure):
+    _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("num_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("c_tile", ctypes.c_int64)]
+
+
+class PvaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                "g.build()\"` (needs nvcc); there is no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        MP, WP = ctypes.POINTER(MaskDesc), ctypes.POINTER(WorklistParams)
+        L.pva_worklist_bytes.restype = sz
+        L.pva_worklist_bytes.argtypes = [i32, MP, WP]
+        L.pva_build_worklist.restype = ctypes.c_int
+        L.pva_build_worklist.argtypes = [P, i32, MP, WP, P, sz, P]
+        L.pva_attn_fwd.restype = ctypes.c_int
+        L.pva_attn_fwd.argtypes = [P, P, P, P, MP, WP, i32, P, P, i32, P, ctypes.c_float, P, P]
+        L.pva_zigzag_shard_len.restype = i32
+        L.pva_zigzag_shard_len.argtypes = [P, i32, i32, i32]
+        L.pva_zigzag_shard.restype = ctypes.c_int
+        L.pva_zigzag_shard.argtypes = [P, i32, i32, i32, P, P, P]
+        L.pva_gather_rows.restype = ctypes.c_int
+        L.pva_gather_rows.argtypes = [P, P, P, i64, i64, i64, i32, P]
+        L.pva_merge_partials.restype = ctypes.c_int
+        L.pva_merge_partials.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, P]
+        L.pva_worklist_error.restype = ctypes.c_int
+        L.pva_worklist_error.argtypes = [P, ctypes.POINTER(i32), P]
+        L.pva_worklist_counts.restype = ctypes.c_int
+        L.pva_worklist_counts.argtypes = [P, ctypes.POINTER(i64), P]
+        L.pva_status_string.restype = ctypes.c_char_p
+        L.pva_status_string.argtypes = [ctypes.c_int]
+        L.pva_version.restype = i32
+        L.pva_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def check(fn: str, status: int) -> None:
+    if status != PVA_OK:
+        raise PvaError(fn, status)

@@ -1,0 +1,220 @@
+"""Thin Python binding of the C ABI (include/pva.h).
+
+Argument marshalling only: tensors are passed by ``data_ptr()`` and the
+current CUDA stream; every step of the computation runs in the library's
+kernels.  PyTorch supplies device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import MaskDesc, Slice, WorklistParams, check, lib
+from .workloads import (MASK_CAUSAL, MASK_SHARED_QUESTION, MASK_SLICES, MASK_SLIDING_WINDOW,
+                        MASK_ZIGZAG_PAIR)
+
+SLICE_FULL, SLICE_CAUSAL = 0, 1
+TILE = 128
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def make_mask(kind: int = MASK_CAUSAL, q_tokens: int = 0, k_tokens: int = 0, window: int = 0,
+              num_prefix_docs: int = 0, cp: int = 0, q_rank: int = 0, k_rank: int = 0,
+              slices: Optional[np.ndarray] = None) -> MaskDesc:
+    """pva_mask_desc.  ``slices``: int32 [n, 8] rows (q_row0, q_len, q_pos0, k_row0, k_len,
+    k_pos0, type, window); the array is kept alive on the returned object."""
+    m = MaskDesc()
+    m.kind, m.window, m.num_prefix_docs = kind, window, num_prefix_docs
+    m.cp, m.q_rank, m.k_rank = cp, q_rank, k_rank
+    m.q_tokens, m.k_tokens = q_tokens, k_tokens
+    if slices is not None:
+        arr = np.ascontiguousarray(slices, dtype=np.int32).reshape(-1, 8)
+        m._slices_keep = arr
+        m.slices = arr.ctypes.data_as(ctypes.POINTER(Slice))
+        m.num_slices = arr.shape[0]
+    return m
+
+
+def make_params(num_q_heads: int, num_kv_heads: int, num_ctas: int = 0, c_tile: int = 0,
+                tile_m: int = TILE, tile_n: int = TILE) -> WorklistParams:
+    p = WorklistParams()
+    p.tile_m, p.tile_n = tile_m, tile_n
+    p.num_q_heads, p.num_kv_heads = num_q_heads, num_kv_heads
+    p.num_ctas, p.c_tile = num_ctas, c_tile
+    return p
+
+
+def worklist_bytes(num_docs: int, mask: MaskDesc, params: WorklistParams) -> int:
+    n = lib().pva_worklist_bytes(num_docs, ctypes.byref(mask), ctypes.byref(params))
+    if n == 0:
+        raise _lib.PvaError("pva_worklist_bytes", 1)
+    return int(n)
+
+
+def alloc_worklist(num_docs: int, mask: MaskDesc, params: WorklistParams,
+                   device="cuda") -> torch.Tensor:
+    """Caller-owned device buffer for the worklist (256-byte aligned by the allocator)."""
+    return torch.empty(worklist_bytes(num_docs, mask, params), dtype=torch.uint8, device=device)
+
+
+def build_worklist(cu_seqlens: Optional[torch.Tensor], mask: MaskDesc, params: WorklistParams,
+                   worklist: torch.Tensor, stream=None) -> None:
+    nd = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None:
+        assert cu_seqlens.dtype == torch.int32 and cu_seqlens.is_cuda
+    check("pva_build_worklist", lib().pva_build_worklist(
+        _ptr(cu_seqlens), nd, ctypes.byref(mask), ctypes.byref(params), _ptr(worklist),
+        worklist.numel(), _stream(stream)))
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+             cu_seqlens: Optional[torch.Tensor], mask: MaskDesc, params: WorklistParams,
+             worklist: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+             softmax_scale: float = 0.0, cta_busy: Optional[torch.Tensor] = None,
+             stream=None) -> None:
+    """out [Tq, Hq, d] bf16 or fp32, lse [Hq, Tq] fp32 (written by the kernel)."""
+    for t in (q, k, v, out, lse):
+        assert t.is_cuda and t.is_contiguous()
+    assert q.dtype == k.dtype == v.dtype == torch.bfloat16
+    assert lse.dtype == torch.float32 and out.dtype in (torch.bfloat16, torch.float32)
+    check("pva_attn_fwd", lib().pva_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), ctypes.byref(mask), ctypes.byref(params),
+        q.shape[-1], _ptr(worklist), _ptr(out), 1 if out.dtype == torch.float32 else 0,
+        _ptr(lse), float(softmax_scale), _ptr(cta_busy), _stream(stream)))
+
+
+def zigzag_shard_len(cu_seqlens_host: np.ndarray, cp: int, rank: int) -> int:
+    cu = np.ascontiguousarray(cu_seqlens_host, dtype=np.int32)
+    n = lib().pva_zigzag_shard_len(cu.ctypes.data_as(ctypes.c_void_p), cu.shape[0] - 1, cp, rank)
+    if n < 0:
+        raise _lib.PvaError("pva_zigzag_shard_len", 1)
+    return int(n)
+
+
+def zigzag_shard(cu_seqlens: torch.Tensor, cp: int, rank: int, gather_map: torch.Tensor,
+                 chunk_table: Optional[torch.Tensor] = None, stream=None) -> None:
+    check("pva_zigzag_shard", lib().pva_zigzag_shard(
+        _ptr(cu_seqlens), cu_seqlens.numel() - 1, cp, rank, _ptr(gather_map), _ptr(chunk_table),
+        _stream(stream)))
+
+
+def gather_rows(src: torch.Tensor, index_map: torch.Tensor, dst: torch.Tensor,
+                scatter: bool = False, stream=None) -> None:
+    """dst[i] = src[map[i]] (or dst[map[i]] = src[i]) over the first dimension."""
+    rows = index_map.numel()
+    row_bytes = src[0].numel() * src.element_size()
+    indexed = dst.shape[0] if scatter else src.shape[0]
+    check("pva_gather_rows", lib().pva_gather_rows(
+        _ptr(src), _ptr(index_map), _ptr(dst), rows, row_bytes, indexed, 1 if scatter else 0,
+        _stream(stream)))
+
+
+def merge_partials(o_a: torch.Tensor, lse_a: torch.Tensor, o_b: torch.Tensor,
+                   lse_b: torch.Tensor, out: torch.Tensor, lse_out: torch.Tensor,
+                   stream=None) -> None:
+    tokens, heads, d = o_a.shape
+    check("pva_merge_partials", lib().pva_merge_partials(
+        _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(out), _ptr(lse_out), tokens, heads,
+        d, 1 if o_a.dtype == torch.float32 else 0, _stream(stream)))
+
+
+def worklist_error(worklist: torch.Tensor, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    check("pva_worklist_error", lib().pva_worklist_error(_ptr(worklist), ctypes.byref(code),
+                                                         _stream(stream)))
+    return int(code.value)
+
+
+def worklist_counts(worklist: torch.Tensor, stream=None) -> dict:
+    out = (ctypes.c_int64 * 6)()
+    st = lib().pva_worklist_counts(_ptr(worklist), out, _stream(stream))
+    names = ("segs", "slices", "units", "runs", "pairs_per_head", "tiles_per_head")
+    res = dict(zip(names, (int(x) for x in out)))
+    res["status"] = int(st)
+    return res
+
+
+# ----------------------------------------------------------------- decoding
+_HDR = np.dtype([("i32", "<i4", 20), ("c_tile", "<i8"), ("pair_sum", "<u8"), ("tile_sum", "<u8"),
+                 ("off", "<i8", 12)])
+_OFF = ("slices", "segs", "units_enum", "keys", "order", "assign", "local", "units", "runs",
+        "cta_off", "doc_scan", "total")
+
+
+def decode_worklist(worklist: torch.Tensor) -> dict:
+    """Copy a built worklist to the host and split it into numpy arrays
+    (segments, slices, units in CTA order, runs, CSR offsets)."""
+    raw = worklist.detach().cpu().numpy()
+    h = np.frombuffer(raw[:_HDR.itemsize].tobytes(), dtype=_HDR)[0]
+    i32 = h["i32"]
+    names = ("magic", "version", "error", "num_ctas", "tile_m", "tile_n", "hq", "hkv", "kind",
+             "q_tokens", "k_tokens", "num_docs", "cap_slices", "cap_segs", "cap_units",
+             "cap_runs", "nslices", "nsegs", "nunits", "nruns")
+    hd = {n: int(x) for n, x in zip(names, i32)}
+    off = {n: int(x) for n, x in zip(_OFF, h["off"])}
+
+    def arr(name, dtype, n, width):
+        b = raw[off[name]: off[name] + n * width * np.dtype(dtype).itemsize]
+        return np.frombuffer(b.tobytes(), dtype=dtype).reshape(n, width) if width > 1 else \
+            np.frombuffer(b.tobytes(), dtype=dtype)
+
+    units = arr("units", "<i4", hd["nunits"], 16)
+    costs = units[:, 12:14].copy().view("<i8").reshape(-1)
+    pairs = units[:, 14:16].copy().view("<i8").reshape(-1)
+    return {"header": hd, "pair_sum": int(h["pair_sum"]), "tile_sum": int(h["tile_sum"]),
+            "slices": arr("slices", "<i4", hd["nslices"], 8),
+            "segs": arr("segs", "<i4", hd["nsegs"], 8),
+            "units": units[:, :10].copy(), "unit_ntiles": units[:, 10].copy(),
+            "unit_cost": costs, "unit_pairs": pairs,
+            "runs": arr("runs", "<i4", hd["nruns"], 4)[:, :3].copy(),
+            "cta_off": arr("cta_off", "<i4", hd["num_ctas"] + 1, 1).copy()}
+
+
+class PackedAttention:
+    """Convenience holder: builds the worklist once for a pack/mask and runs
+    the forward on it.  Buffers come from PyTorch; all work is in libpva."""
+
+    def __init__(self, cu_seqlens: Optional[torch.Tensor], mask: MaskDesc,
+                 num_q_heads: int, num_kv_heads: int, num_ctas: int = 0, c_tile: int = 0):
+        self.cu = cu_seqlens
+        self.mask = mask
+        self.params = make_params(num_q_heads, num_kv_heads, num_ctas, c_tile)
+        nd = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+        dev = cu_seqlens.device if cu_seqlens is not None else torch.device("cuda")
+        self.worklist = alloc_worklist(nd, mask, self.params, dev)
+
+    def plan(self, stream=None) -> None:
+        build_worklist(self.cu, self.mask, self.params, self.worklist, stream)
+
+    def forward(self, q, k, v, out=None, lse=None, out_fp32: bool = False, softmax_scale=0.0,
+                cta_busy=None, stream=None):
+        tq, hq, d = q.shape
+        if out is None:
+            out = torch.empty((tq, hq, d), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                              device=q.device)
+        if lse is None:
+            lse = torch.empty((hq, tq), dtype=torch.float32, device=q.device)
+        attn_fwd(q, k, v, self.cu, self.mask, self.params, self.worklist, out, lse,
+                 softmax_scale, cta_busy, stream)
+        return out, lse
+
+
+def mask_for_workload(w, q_tokens: Optional[int] = None, k_tokens: Optional[int] = None,
+                      **kw) -> MaskDesc:
+    t = w.total_tokens
+    return make_mask(w.mask_kind, q_tokens if q_tokens is not None else t,
+                     k_tokens if k_tokens is not None else t, window=w.window,
+                     num_prefix_docs=w.num_prefix_docs, **kw)

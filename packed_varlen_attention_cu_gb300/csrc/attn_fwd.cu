@@ -1,0 +1,614 @@
+// attn_fwd.cu -- persistent packed document-masked attention forward on
+// sm_103a (tcgen05 MMAs into tensor memory, TMA-staged tiles).
+//
+// The method: "03 · 长文负载均衡" §1.1 (each document attends only to itself;
+// the quadratic work is QK^T and PV), §3.2 (only (Q block, KV block) pairs
+// with a non-zero mask are computed; partial results over key blocks are
+// combined by online-softmax rescale-and-sum), §1.2 (structured masks).
+//
+// One CTA per SM walks its list of work units (built by pva_build_worklist,
+// LPT-balanced).  A unit holds up to two 128-row query sub-tiles that share
+// one kv head and the same kv tiles.  Warp roles (384 threads, 3 warpgroups):
+//   warp 0      TMA producer: Q sub-tiles, then K_j / V_j tiles into a ring
+//   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T (SS), O_i += P_i V_j
+//               (TS: P read from tensor memory), completion via tcgen05.commit
+//   warps 4-7   softmax + epilogue of sub-tile 0 (one query row per thread)
+//   warps 8-11  softmax + epilogue of sub-tile 1
+// A warp reaches tensor-memory lanes 32*(warp % 4).
+// Tensor memory (512 columns): S0/P0 [0,128), S1/P1 [128,256), O0 [256,..),
+// O1 [384,..).  P (bf16) overwrites the first half of S in place.  With the
+// 32x32b tensor-memory layout a thread owns a whole row, so the row max and
+// row sum of the online softmax are thread-local (no shuffles needed).
+// The running max is only moved (and O rescaled in tensor memory) when it
+// grows by more than 2^8 in the base-2 exponent domain; until then P stays
+// below 2^8, which fp32 and bf16 hold exactly enough.
+//
+// Every wait is bounded; on timeout the CTA raises an abort flag, records
+// the wait site in the worklist error word, drains its own copies and MMAs,
+// frees tensor memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pva.h"
+#include "common.h"
+#include "ptx.cuh"
+#include "wl_layout.cuh"
+
+namespace pva {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
+constexpr float kRescaleThreshold = 8.0f;     // log2 domain
+
+template <int D>
+struct Cfg {
+    static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
+    static constexpr int kStages = D == 128 ? 4 : 8;
+    static constexpr int kSmem = 2 * kTileBytes + kStages * kTileBytes + 1024;
+    static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
+};
+
+struct AttnParams {
+    const uint8_t* wl;
+    void* out;
+    float* lse;
+    uint64_t* busy;
+    int32_t q_tokens, k_tokens, hq, hkv, out_fp32, num_ctas;
+    float scale_log2;
+};
+
+struct SubTile {
+    int32_t q_row, nrows, q_pos, head;
+};
+
+struct Unit {
+    int32_t nsub, kvh, run_begin, run_count, ntiles;
+    SubTile st[2];
+};
+
+__device__ __forceinline__ Unit decode_unit(const WlUnit& u, const WlSeg* segs) {
+    const WlSeg g = segs[u.seg];
+    Unit r;
+    r.nsub = u.h1 >= 0 ? 2 : 1;
+    r.kvh = u.kvh;
+    r.run_begin = u.run_begin;
+    r.run_count = u.run_count;
+    r.ntiles = u.ntiles;
+    const int32_t ts[2] = {u.t0, u.t1};
+    const int32_t hs[2] = {u.h0, u.h1};
+    for (int i = 0; i < 2; ++i) {
+        const int32_t t = ts[i] >= 0 ? ts[i] : 0;
+        r.st[i].q_row = g.q_row0 + t * 128;
+        r.st[i].nrows = min(128, g.q_len - t * 128);
+        r.st[i].q_pos = g.q_pos0 + t * 128;
+        r.st[i].head = hs[i];
+    }
+    return r;
+}
+
+struct Shared {
+    uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_empty[2], done;
+    uint64_t kv_full[8], kv_empty[8];
+    uint32_t tmem_base;
+    int32_t abort_flag;
+};
+
+__device__ __forceinline__ void write_empty_rows(const AttnParams& p, const SubTile& st, int r,
+                                                 int D) {
+    if (r >= st.nrows) return;
+    const int64_t row = (int64_t)(st.q_row + r) * p.hq + st.head;
+    if (p.out_fp32) {
+        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * D);
+        for (int c = 0; c < D / 4; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + row * D);
+        for (int c = 0; c < D / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+    }
+    p.lse[(int64_t)st.head * p.q_tokens + st.q_row + r] = -INFINITY;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sQ[2] = {smem, smem + C::kTileBytes};
+    uint8_t* sKV = smem + 2 * C::kTileBytes;
+    __shared__ Shared sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const WlHeader* h = reinterpret_cast<const WlHeader*>(p.wl);
+    int32_t* err_word = const_cast<int32_t*>(&h->error);
+    // the worklist must describe this call
+    const bool ok = h->magic == kWlMagic && h->tile_m == 128 && h->tile_n == 128 &&
+                    h->hq == p.hq && h->hkv == p.hkv && h->num_ctas == p.num_ctas &&
+                    (int)gridDim.x == p.num_ctas && h->q_tokens == p.q_tokens &&
+                    h->k_tokens == p.k_tokens;
+    if (!ok) {
+        if (tid == 0 && blockIdx.x == 0) atomicCAS(err_word, 0, kErrBadWorklist);
+        return;
+    }
+    if (h->error != 0) return;  // the build failed: nothing is written
+    const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
+    const WlUnit* units = reinterpret_cast<const WlUnit*>(p.wl + h->off.units);
+    const WlRun* runs = reinterpret_cast<const WlRun*>(p.wl + h->off.runs);
+    const WlSlice* slices = reinterpret_cast<const WlSlice*>(p.wl + h->off.slices);
+    const WlSeg* segs = reinterpret_cast<const WlSeg*>(p.wl + h->off.segs);
+    const int32_t ub = cta_off[blockIdx.x], ue = cta_off[blockIdx.x + 1];
+    const uint64_t t_start = globaltimer_ns();
+    if (ub >= ue) {
+        if (p.busy && tid == 0) {
+            p.busy[2 * blockIdx.x] = t_start;
+            p.busy[2 * blockIdx.x + 1] = t_start;
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh.q_full[i], 1);
+            mbar_init(&sh.q_empty[i], 1);
+            mbar_init(&sh.s_full[i], 1);
+            mbar_init(&sh.p_full[i], 128);
+            mbar_init(&sh.o_full[i], 1);
+            mbar_init(&sh.o_empty[i], 128);
+        }
+        mbar_init(&sh.done, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&sh.kv_full[s], 1);
+            mbar_init(&sh.kv_empty[s], 1);
+        }
+        sh.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    volatile int32_t* abort_flag = &sh.abort_flag;
+
+    if (warp < 4) {
+      if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t kv_it = 0, q_it[2] = {0, 0};
+            bool live = true;
+            for (int32_t ui = ub; ui < ue && live; ++ui) {
+                const WlUnit wu = units[ui];
+                const Unit u = decode_unit(wu, segs);
+                if (u.ntiles == 0) continue;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    if (i >= u.nsub || !live) break;
+                    live = mbar_wait(&sh.q_empty[i], (q_it[i] & 1) ^ 1, abort_flag, err_word,
+                                     kErrTimeoutBase + 1, kWaitNs);
+                    if (!live) break;
+                    mbar_arrive_expect_tx(&sh.q_full[i], C::kTileBytes);
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(sQ[i] + b * 16384, &tmq, &sh.q_full[i], b * 64, u.st[i].head,
+                                    u.st[i].q_row);
+                    ++q_it[i];
+                }
+                for (int32_t r = 0; r < u.run_count && live; ++r) {
+                    const WlRun run = runs[u.run_begin + r];
+                    const WlSlice s = slices[run.slice];
+                    for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
+                        const int32_t krow = s.k_row0 + jt * 128;
+                        for (int kv = 0; kv < 2 && live; ++kv) {
+                            const uint32_t st = kv_it % C::kStages;
+                            live = mbar_wait(&sh.kv_empty[st], ((kv_it / C::kStages) & 1) ^ 1,
+                                             abort_flag, err_word, kErrTimeoutBase + 2, kWaitNs);
+                            if (!live) break;
+                            mbar_arrive_expect_tx(&sh.kv_full[st], C::kTileBytes);
+                            uint8_t* dst = sKV + st * C::kTileBytes;
+                            for (int b = 0; b < D / 64; ++b)
+                                tma_load_3d(dst + b * 16384, kv == 0 ? &tmk : &tmv,
+                                            &sh.kv_full[st], b * 64, u.kvh, krow);
+                            ++kv_it;
+                        }
+                    }
+                }
+            }
+            if (!live) {
+                // drain: wait for the copies this thread issued last
+                const uint32_t n = kv_it < (uint32_t)C::kStages ? kv_it : (uint32_t)C::kStages;
+                for (uint32_t k = 0; k < n; ++k) {
+                    const uint32_t it = kv_it - 1 - k;
+                    mbar_wait_drain(&sh.kv_full[it % C::kStages], (it / C::kStages) & 1, kDrainNs);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (q_it[i] > 0) mbar_wait_drain(&sh.q_full[i], (q_it[i] - 1) & 1, kDrainNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t kv_it = 0, q_it[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+            bool live = true;
+            const uint32_t sQa[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
+            const uint32_t sKVa = smem_u32(sKV);
+            for (int32_t ui = ub; ui < ue && live; ++ui) {
+                const WlUnit wu = units[ui];
+                const Unit u = decode_unit(wu, segs);
+                const int32_t n = u.ntiles;
+                if (n == 0) continue;
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (i < u.nsub && live)
+                        live = mbar_wait(&sh.q_full[i], q_it[i] & 1, abort_flag, err_word,
+                                         kErrTimeoutBase + 3, kWaitNs);
+                if (!live) break;
+                // prologue: S_i = Q_i K_0^T
+                {
+                    const uint32_t st = kv_it % C::kStages;
+                    live = mbar_wait(&sh.kv_full[st], (kv_it / C::kStages) & 1, abort_flag,
+                                     err_word, kErrTimeoutBase + 4, kWaitNs);
+                    if (!live) break;
+                    tc_fence_after();
+                    const uint32_t kb = sKVa + st * C::kTileBytes;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        if (i >= u.nsub) break;
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                            mma_ss(tmem + i * 128, sdesc_sw128(sQa[i] + off, 16, 1024),
+                                   sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, k > 0);
+                        }
+                        mma_commit(&sh.s_full[i]);
+                        if (n == 1) mma_commit(&sh.q_empty[i]);
+                    }
+                    mma_commit(&sh.kv_empty[st]);
+                    ++kv_it;
+                }
+                for (int32_t j = 0; j < n && live; ++j) {
+                    const bool has_next = j + 1 < n;
+                    const uint32_t stv = kv_it % C::kStages;
+                    const uint32_t stk = (kv_it + 1) % C::kStages;
+                    live = mbar_wait(&sh.kv_full[stv], (kv_it / C::kStages) & 1, abort_flag,
+                                     err_word, kErrTimeoutBase + 5, kWaitNs);
+                    if (!live) break;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        if (i >= u.nsub || !live) break;
+                        live = mbar_wait(&sh.p_full[i], p_cnt[i] & 1, abort_flag, err_word,
+                                         kErrTimeoutBase + 6, kWaitNs);
+                        if (!live) break;
+                        ++p_cnt[i];
+                        if (j == 0) {
+                            live = mbar_wait(&sh.o_empty[i], (o_cnt[i] & 1) ^ 1, abort_flag,
+                                             err_word, kErrTimeoutBase + 7, kWaitNs);
+                            if (!live) break;
+                        }
+                        tc_fence_after();
+                        const uint32_t vb = sKVa + stv * C::kTileBytes;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            mma_ts(tmem + 256 + i * 128, tmem + i * 128 + k * 8,
+                                   sdesc_sw128(vb + k * 2048, 16384, 1024), C::kIdescPV,
+                                   (j > 0 || k > 0) ? 1u : 0u);
+                        if (has_next) {
+                            if (i == 0) {
+                                live = mbar_wait(&sh.kv_full[stk], ((kv_it + 1) / C::kStages) & 1,
+                                                 abort_flag, err_word, kErrTimeoutBase + 8, kWaitNs);
+                                if (!live) break;
+                                tc_fence_after();
+                            }
+                            const uint32_t kb = sKVa + stk * C::kTileBytes;
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k) {
+                                const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                                mma_ss(tmem + i * 128, sdesc_sw128(sQa[i] + off, 16, 1024),
+                                       sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, k > 0);
+                            }
+                            mma_commit(&sh.s_full[i]);
+                            if (j + 2 == n) mma_commit(&sh.q_empty[i]);
+                        }
+                    }
+                    if (!live) break;
+                    mma_commit(&sh.kv_empty[stv]);
+                    if (has_next) mma_commit(&sh.kv_empty[stk]);
+                    kv_it += has_next ? 2 : 1;
+                }
+                if (!live) break;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    if (i >= u.nsub) break;
+                    mma_commit(&sh.o_full[i]);
+                    ++o_cnt[i];
+                    ++q_it[i];
+                }
+            }
+            // drain every MMA this thread issued before tensor memory is freed
+            mma_commit(&sh.done);
+            mbar_wait_drain(&sh.done, 0, kDrainNs);
+        }
+        __syncwarp();
+      }
+    } else {
+        // ------------------------------------------------------- softmax / epilogue
+        const int i = (warp - 4) >> 2;           // sub-tile of this warpgroup
+        const int r = (warp & 3) * 32 + lane;    // query row = tensor-memory lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + i * 128;
+        const uint32_t tO = tmem + lane_base + 256 + i * 128;
+        uint32_t s_cnt = 0, o_cnt = 0;
+        bool live = true;
+        for (int32_t ui = ub; ui < ue && live; ++ui) {
+            const WlUnit wu = units[ui];
+            const Unit u = decode_unit(wu, segs);
+            if (i >= u.nsub) continue;
+            const SubTile st = i == 0 ? u.st[0] : u.st[1];
+            if (u.ntiles == 0) {
+                write_empty_rows(p, st, r, D);
+                continue;
+            }
+            const bool valid = r < st.nrows;
+            const int32_t q_pos = st.q_pos + r;
+            float m_used = -INFINITY, l_sum = 0.f;
+            for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
+                const WlRun run = runs[u.run_begin + rr];
+                const WlSlice s = slices[run.slice];
+                for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
+                    live = mbar_wait(&sh.s_full[i], s_cnt & 1, abort_flag, err_word,
+                                     kErrTimeoutBase + 9, kWaitNs);
+                    if (!live) break;
+                    ++s_cnt;
+                    tc_fence_after();
+                    uint32_t sr[4][32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+                    // allowed columns [c_lo, c_hi) of this row in this kv tile
+                    const int32_t kt0 = jt * 128;
+                    int32_t c_hi = min(128, s.k_len - kt0), c_lo = 0;
+                    if (s.type == PVA_SLICE_CAUSAL) {
+                        const int32_t d0 = q_pos - s.k_pos0 - kt0;
+                        c_hi = min(c_hi, d0 + 1);
+                        if (s.window > 0) c_lo = max(0, d0 - s.window + 1);
+                    }
+                    if (!valid) c_hi = 0;
+                    const bool need = c_lo > 0 || c_hi < 128;
+                    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int col = c * 32 + e;
+                                if (col < c_lo || col >= c_hi) sr[c][e] = __float_as_uint(-INFINITY);
+                            }
+                    }
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+                    const float m_tile = mx * p.scale_log2;  // -inf stays -inf
+                    float alpha = 1.f;
+                    bool rescale = false;
+                    if (m_tile > m_used) {
+                        if (m_used == -INFINITY) {
+                            m_used = m_tile;  // O and l are still zero
+                        } else if (m_tile > m_used + kRescaleThreshold) {
+                            alpha = ex2_approx(m_used - m_tile);
+                            m_used = m_tile;
+                            rescale = true;
+                        }
+                    }
+                    l_sum *= alpha;
+                    // P = 2^(s*scale*log2e - m), packed to bf16 pairs in place
+                    // (pair e/2 lands in a register already consumed)
+                    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+                    float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), p.scale_log2, neg_m));
+                            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), p.scale_log2, neg_m));
+                            part[c] += p0 + p1;
+                            sr[c][e >> 1] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(tS + c * 16, sr[c]);
+                    }
+                    l_sum += (part[0] + part[1]) + (part[2] + part[3]);
+                    // rare: the running max moved, rescale this row of O
+                    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c * 32, o);
+                            tmem_ld_wait(o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tO + c * 32, o);
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&sh.p_full[i]);
+                }
+            }
+            if (!live) break;
+            // epilogue: O / l -> global, LSE
+            live = mbar_wait(&sh.o_full[i], o_cnt & 1, abort_flag, err_word, kErrTimeoutBase + 10,
+                             kWaitNs);
+            if (!live) break;
+            ++o_cnt;
+            tc_fence_after();
+            const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            const int64_t row = (int64_t)(st.q_row + r) * p.hq + st.head;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                tmem_ld_wait(o);
+                if (valid) {
+                    if (p.out_fp32) {
+                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) +
+                                                                row * D + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv,
+                                                 __uint_as_float(o[4 * e + 1]) * inv,
+                                                 __uint_as_float(o[4 * e + 2]) * inv,
+                                                 __uint_as_float(o[4 * e + 3]) * inv);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_uint4(
+                                pack_bf16x2(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sh.o_empty[i]);
+            if (valid)
+                p.lse[(int64_t)st.head * p.q_tokens + st.q_row + r] =
+                    l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (p.busy && tid == 0) {
+        p.busy[2 * blockIdx.x] = t_start;
+        p.busy[2 * blockIdx.x + 1] = globaltimer_ns();
+    }
+}
+
+}  // namespace
+}  // namespace pva
+
+// ------------------------------------------------------------------ host side
+namespace pva {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// [rows, heads, d] bf16 viewed as a 3-D tensor (d, heads, rows); 128-row x
+// 64-element boxes with 128-byte swizzle; rows past the end read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, int32_t rows, int32_t heads, int32_t d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+pva_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                  const AttnParams& ap, cudaStream_t st) {
+    auto kern = attn_fwd_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem) !=
+        cudaSuccess)
+        return PVA_ERR_CUDA;
+    kern<<<ap.num_ctas, kThreads, Cfg<D>::kSmem, st>>>(mq, mk, mv, ap);
+    return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace pva
+
+using namespace pva;
+
+extern "C" pva_status pva_attn_fwd(const void* q, const void* k, const void* v,
+                                   const int32_t* cu_seqlens_dev, const pva_mask_desc* mask,
+                                   const pva_worklist_params* params, int32_t head_dim,
+                                   const void* worklist_dev, void* out, int32_t out_is_fp32,
+                                   float* lse, float softmax_scale, uint64_t* cta_busy_ns,
+                                   void* stream) {
+    if (!mask || !params || !worklist_dev || !out || !lse || !q) return PVA_ERR_INVALID_ARG;
+    if (mask->kind != PVA_MASK_SLICES && !cu_seqlens_dev) return PVA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PVA_ERR_UNSUPPORTED;
+    if (params->tile_m != 128 || params->tile_n != 128) return PVA_ERR_UNSUPPORTED;
+    if (params->num_q_heads <= 0 || params->num_kv_heads <= 0 ||
+        params->num_q_heads % params->num_kv_heads != 0)
+        return PVA_ERR_INVALID_ARG;
+    if (out_is_fp32 != 0 && out_is_fp32 != 1) return PVA_ERR_INVALID_ARG;
+    if (mask->q_tokens < 0 || mask->k_tokens < 0) return PVA_ERR_INVALID_ARG;
+    if (mask->k_tokens > 0 && (!k || !v)) return PVA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(lse) ||
+        (mask->k_tokens > 0 && (!aligned16(k) || !aligned16(v))) ||
+        (reinterpret_cast<uintptr_t>(worklist_dev) & 255u))
+        return PVA_ERR_INVALID_ARG;
+    const int32_t nc = resolve_num_ctas(params->num_ctas);
+    if (nc <= 0) return PVA_ERR_CUDA;
+    if (nc > kMaxBins) return PVA_ERR_INVALID_ARG;
+    if (mask->q_tokens == 0) return PVA_OK;
+    CUtensorMap mq, mk, mv;
+    const void* kp = mask->k_tokens > 0 ? k : q;  // no key rows: maps are never read
+    const void* vp = mask->k_tokens > 0 ? v : q;
+    const int32_t kh = mask->k_tokens > 0 ? params->num_kv_heads : params->num_q_heads;
+    if (!make_map(&mq, q, mask->q_tokens, params->num_q_heads, head_dim) ||
+        !make_map(&mk, kp, mask->k_tokens, kh, head_dim) ||
+        !make_map(&mv, vp, mask->k_tokens, kh, head_dim))
+        return PVA_ERR_CUDA;
+    AttnParams ap;
+    ap.wl = reinterpret_cast<const uint8_t*>(worklist_dev);
+    ap.out = out;
+    ap.lse = lse;
+    ap.busy = cta_busy_ns;
+    ap.q_tokens = mask->q_tokens;
+    ap.k_tokens = mask->k_tokens;
+    ap.hq = params->num_q_heads;
+    ap.hkv = params->num_kv_heads;
+    ap.out_fp32 = out_is_fp32;
+    ap.num_ctas = nc;
+    const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
+    ap.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return head_dim == 128 ? launch<128>(mq, mk, mv, ap, st) : launch<64>(mq, mk, mv, ap, st);
+}

@@ -1,0 +1,78 @@
+// wl_layout.cuh -- byte layout of the device worklist buffer.
+//
+// The buffer is owned by the caller; the host computes capacities and
+// section offsets from bounds (pva_worklist_bytes), the device kernels fill
+// it.  Sections (each 256-byte aligned):
+//   header     WlHeader
+//   slices     WlSlice[cap_slices]        slices of the mask, enumeration order
+//   segs       WlSeg[cap_segs]            query segments (slices sharing a q range)
+//   units_enum WlUnit[cap_units]          work units in enumeration order
+//   keys       uint64[cap_units]          sort keys: (~cost << 24) | uid
+//   order      int32[cap_units]           uid of the r-th unit in LPT order
+//   assign     int32[cap_units]           bin (CTA) of each uid
+//   local      int32[cap_units]           position of each uid inside its bin
+//   units      WlUnit[cap_units]          units grouped by CTA, in assignment order
+//   runs       WlRun[cap_runs]            per unit and slice: kv tile span [lo, hi)
+//   cta_off    int32[num_ctas + 1]        CSR offsets of the CTAs into `units`
+//   doc_scan   int32[4 * (num_docs + 1)]  per-document scan scratch
+#pragma once
+
+#include <stdint.h>
+
+namespace pva {
+
+constexpr int32_t kWlMagic = 0x57415650;  // "PVAW"
+constexpr int32_t kWlVersion = 1;
+constexpr int kMaxBins = 1024;
+constexpr int kUidBits = 24;   // units per worklist < 2^24
+constexpr int kCostBits = 40;  // unit cost < 2^40
+
+struct WlSlice {
+    int32_t q_row0, q_len, q_pos0, k_row0, k_len, k_pos0, type, window;
+};
+
+struct WlSeg {
+    int32_t q_row0, q_len, q_pos0, slice_begin, slice_count, unit_base, run_base, ntiles;
+};
+
+struct WlUnit {
+    int32_t uid, seg, t0, t1, h0, h1, kvh, run_begin, run_count, cta, ntiles, pad;
+    int64_t cost, pairs;
+};
+static_assert(sizeof(WlUnit) == 64, "WlUnit is 64 bytes");
+
+struct WlRun {
+    int32_t slice, lo, hi, pad;
+};
+
+struct WlOffsets {
+    int64_t slices, segs, units_enum, keys, order, assign, local, units, runs, cta_off, doc_scan,
+        total;
+};
+
+struct WlHeader {
+    int32_t magic, version;
+    int32_t error;     // device error word (0 = none)
+    int32_t num_ctas;
+    int32_t tile_m, tile_n, hq, hkv;
+    int32_t kind, q_tokens, k_tokens, num_docs;
+    int32_t cap_slices, cap_segs, cap_units, cap_runs;
+    int32_t nslices, nsegs, nunits, nruns;  // written by the device
+    int64_t c_tile;
+    unsigned long long pair_sum;   // sum over units of allowed pairs (all sub-tiles)
+    unsigned long long tile_sum;   // sum over units of sub-tiles x kv tiles
+    WlOffsets off;
+    int32_t pad_[8];
+};
+static_assert(sizeof(WlHeader) <= 256, "header fits in 256 bytes");
+
+// Device error codes (stored in WlHeader::error).
+enum : int32_t {
+    kErrNone = 0,
+    kErrCapacity = 100,       // a count exceeded its capacity
+    kErrCostRange = 101,      // a unit cost does not fit the sort key
+    kErrBadWorklist = 102,    // attention called with a worklist that does not match
+    kErrTimeoutBase = 200     // + wait site id: a bounded wait expired
+};
+
+}  // namespace pva

@@ -1,0 +1,783 @@
+// worklist.cu -- device construction of the attention worklist.
+//
+// "03 · 长文负载均衡" §3.2: attention is cut into tiles; Libra TAP charges
+// every tile its exact causal query-key pair count and DCP only creates a
+// computation block where the mask is not all zero.  §2.1 (VRSP) and
+// "数据并行负载均衡" §4.4 (phase 1): LPT -- sort by cost descending and put
+// each item on the currently lightest bin.  Here the bins are the persistent
+// CTAs of one GPU.
+//
+// Kernels (all on the caller's stream, no host round trip):
+//   wl_plan   1 CTA  : validate cu_seqlens, derive slices and query segments
+//                      of the mask, per-segment unit/run bases (block scans)
+//   wl_units  grid   : one thread per work unit: kv-tile span of every slice
+//                      for its two sub-tiles, exact pair count, cost, sort key
+//   wl_rank   grid   : stable sort by (cost desc, uid asc) as a rank count
+//   wl_lpt    1 CTA  : exact LPT in batches (see below), CSR by CTA
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "../../include/pva.h"
+#include "common.h"
+#include "wl_layout.cuh"
+
+namespace pva {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ void zz_chunk_dev(int32_t len, int32_t cp, int32_t c, int32_t& off,
+                                             int32_t& clen) {
+    const int32_t n = 2 * cp, base = len / n, rem = len % n;
+    clen = base + (c < rem ? 1 : 0);
+    off = c * base + (c < rem ? c : rem);
+}
+
+// Block-wide exclusive scan of N int32 lanes per thread (blockDim = 1024).
+template <int N>
+__device__ void block_scan_excl(int32_t (&v)[N], int32_t (&tot)[N], int32_t (*sm)[N]) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int32_t inc[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) inc[k] = v[k];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            int32_t t = __shfl_up_sync(0xffffffffu, inc[k], o);
+            if (lane >= o) inc[k] += t;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) sm[w][k] = inc[k];
+    }
+    __syncthreads();
+    if (w == 0) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            int32_t x = sm[lane][k];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int32_t t = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += t;
+            }
+            sm[lane][k] = x;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        int32_t base = w > 0 ? sm[w - 1][k] : 0;
+        tot[k] = sm[31][k];
+        v[k] = base + inc[k] - v[k];
+    }
+    __syncthreads();
+}
+
+struct PlanArgs {
+    WlHeader hinit;  // capacities and offsets computed on the host
+    uint8_t* base;
+    const int32_t* cu;
+    int32_t num_docs, kind, window, num_prefix, cp, q_rank, k_rank, num_slices;
+    int32_t tile_m, hq, hkv, q_tokens, k_tokens;
+};
+
+__device__ __forceinline__ void set_error(WlHeader* h, int32_t code) { atomicCAS(&h->error, 0, code); }
+
+// Slices per document and query segments of the mask (the same rules as the
+// header documents for pva_mask_kind).
+__global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
+    WlHeader* h = reinterpret_cast<WlHeader*>(a.base);
+    WlSlice* slices = reinterpret_cast<WlSlice*>(a.base + a.hinit.off.slices);
+    WlSeg* segs = reinterpret_cast<WlSeg*>(a.base + a.hinit.off.segs);
+    int32_t* scan = reinterpret_cast<int32_t*>(a.base + a.hinit.off.doc_scan);
+    const int tid = threadIdx.x;
+    const int nd = a.num_docs;
+    __shared__ int32_t sm4[32][4];
+    __shared__ int32_t carry[4];
+    __shared__ int32_t s_bad, s_npref, s_nseg, s_nsl;
+
+    if (tid == 0) {
+        s_bad = 0;
+        s_npref = 0;
+        *h = a.hinit;  // error word, counts and sums start at zero
+        for (int k = 0; k < 4; ++k) carry[k] = 0;
+    }
+    __syncthreads();
+
+    if (a.kind != PVA_MASK_SLICES) {
+        if (tid == 0 && a.cu[0] != 0) s_bad = 1;
+        for (int d = tid; d < nd; d += kPlanThreads) {
+            const int32_t len = a.cu[d + 1] - a.cu[d];
+            if (len < 0) s_bad = 1;
+            if (a.kind == PVA_MASK_SHARED_QUESTION && d < a.num_prefix && len > 0)
+                atomicAdd(&s_npref, 1);
+        }
+        __syncthreads();
+        const int32_t total = a.cu[nd];
+        if (a.kind != PVA_MASK_ZIGZAG_PAIR && (total != a.q_tokens || total != a.k_tokens))
+            s_bad = 1;
+        __syncthreads();
+        if (s_bad) {
+            if (tid == 0) set_error(h, kErrBadWorklist);
+            return;
+        }
+        // pass 1: per-document segment / slice counts and zigzag local offsets
+        for (int d0 = 0; d0 < nd; d0 += kPlanThreads) {
+            const int d = d0 + tid;
+            int32_t v[4] = {0, 0, 0, 0};
+            if (d < nd) {
+                const int32_t len = a.cu[d + 1] - a.cu[d];
+                if (a.kind == PVA_MASK_CAUSAL || a.kind == PVA_MASK_SLIDING_WINDOW) {
+                    v[0] = v[1] = len > 0;
+                } else if (a.kind == PVA_MASK_SHARED_QUESTION) {
+                    v[0] = len > 0;
+                    v[1] = len > 0 ? (d >= a.num_prefix ? s_npref + 1 : 1) : 0;
+                } else {
+                    const int32_t qc[2] = {a.q_rank, 2 * a.cp - 1 - a.q_rank};
+                    const int32_t kc[2] = {a.k_rank, 2 * a.cp - 1 - a.k_rank};
+                    int32_t qo[2], ql[2], ko[2], kl[2];
+                    for (int e = 0; e < 2; ++e) {
+                        zz_chunk_dev(len, a.cp, qc[e], qo[e], ql[e]);
+                        zz_chunk_dev(len, a.cp, kc[e], ko[e], kl[e]);
+                    }
+                    for (int e = 0; e < 2; ++e) {
+                        if (ql[e] <= 0) continue;
+                        v[0] += 1;
+                        for (int f = 0; f < 2; ++f)
+                            if (kl[f] > 0 && ko[f] <= qo[e] + ql[e] - 1) v[1] += 1;
+                    }
+                    v[2] = ql[0] + ql[1];
+                    v[3] = kl[0] + kl[1];
+                }
+            }
+            int32_t tot[4];
+            block_scan_excl<4>(v, tot, sm4);
+            if (d < nd) {
+                for (int k = 0; k < 4; ++k) scan[k * (nd + 1) + d] = carry[k] + v[k];
+            }
+            __syncthreads();
+            if (tid == 0)
+                for (int k = 0; k < 4; ++k) carry[k] += tot[k];
+            __syncthreads();
+        }
+        if (tid == 0) {
+            for (int k = 0; k < 4; ++k) scan[k * (nd + 1) + nd] = carry[k];
+            s_nseg = carry[0];
+            s_nsl = carry[1];
+            if (a.kind == PVA_MASK_ZIGZAG_PAIR && (carry[2] != a.q_tokens || carry[3] != a.k_tokens))
+                s_bad = 1;
+            if (carry[0] > h->cap_segs || carry[1] > h->cap_slices) s_bad = 2;
+        }
+        __syncthreads();
+        if (s_bad) {
+            if (tid == 0) set_error(h, s_bad == 2 ? kErrCapacity : kErrBadWorklist);
+            return;
+        }
+        // pass 2: write the slices and segments of every document
+        for (int d = tid; d < nd; d += kPlanThreads) {
+            const int32_t len = a.cu[d + 1] - a.cu[d];
+            int32_t sg = scan[d], sl = scan[(nd + 1) + d];
+            if (a.kind == PVA_MASK_CAUSAL || a.kind == PVA_MASK_SLIDING_WINDOW) {
+                if (len <= 0) continue;
+                const int32_t w = a.kind == PVA_MASK_SLIDING_WINDOW ? a.window : 0;
+                slices[sl] = WlSlice{a.cu[d], len, 0, a.cu[d], len, 0, PVA_SLICE_CAUSAL, w};
+                segs[sg] = WlSeg{a.cu[d], len, 0, sl, 1, 0, 0, 0};
+            } else if (a.kind == PVA_MASK_SHARED_QUESTION) {
+                if (len <= 0) continue;
+                const int32_t first = sl;
+                if (d >= a.num_prefix) {
+                    for (int q = 0; q < a.num_prefix; ++q) {
+                        const int32_t ql = a.cu[q + 1] - a.cu[q];
+                        if (ql <= 0) continue;
+                        slices[sl++] = WlSlice{a.cu[d], len, 0, a.cu[q], ql, 0, PVA_SLICE_FULL, 0};
+                    }
+                }
+                slices[sl++] = WlSlice{a.cu[d], len, 0, a.cu[d], len, 0, PVA_SLICE_CAUSAL, 0};
+                segs[sg] = WlSeg{a.cu[d], len, 0, first, sl - first, 0, 0, 0};
+            } else {
+                const int32_t qc[2] = {a.q_rank, 2 * a.cp - 1 - a.q_rank};
+                const int32_t kc[2] = {a.k_rank, 2 * a.cp - 1 - a.k_rank};
+                int32_t qo[2], ql[2], ko[2], kl[2];
+                for (int e = 0; e < 2; ++e) {
+                    zz_chunk_dev(len, a.cp, qc[e], qo[e], ql[e]);
+                    zz_chunk_dev(len, a.cp, kc[e], ko[e], kl[e]);
+                }
+                const int32_t qloc = scan[2 * (nd + 1) + d], kloc = scan[3 * (nd + 1) + d];
+                const int32_t krow[2] = {kloc, kloc + kl[0]};
+                int32_t qrow = qloc;
+                for (int e = 0; e < 2; ++e) {
+                    if (ql[e] > 0) {
+                        const int32_t first = sl;
+                        for (int f = 0; f < 2; ++f) {
+                            if (kl[f] <= 0 || ko[f] > qo[e] + ql[e] - 1) continue;
+                            slices[sl++] =
+                                WlSlice{qrow, ql[e], qo[e], krow[f], kl[f], ko[f], PVA_SLICE_CAUSAL, 0};
+                        }
+                        segs[sg++] = WlSeg{qrow, ql[e], qo[e], first, sl - first, 0, 0, 0};
+                    }
+                    qrow += ql[e];
+                }
+            }
+        }
+    } else {
+        // explicit slices (copied by the host): group consecutive equal q ranges
+        const int32_t ns = a.num_slices;
+        for (int i0 = 0; i0 < ns; i0 += kPlanThreads) {
+            const int i = i0 + tid;
+            int32_t v[1] = {0};
+            if (i < ns) {
+                const WlSlice s = slices[i];
+                if (i == 0) {
+                    v[0] = 1;
+                } else {
+                    const WlSlice p = slices[i - 1];
+                    v[0] = (p.q_row0 != s.q_row0 || p.q_len != s.q_len || p.q_pos0 != s.q_pos0);
+                }
+            }
+            const int32_t flag = v[0];
+            int32_t tot[1];
+            int32_t(*sm1)[1] = reinterpret_cast<int32_t(*)[1]>(&sm4[0][0]);
+            block_scan_excl<1>(v, tot, sm1);
+            if (i < ns && flag) {
+                const WlSlice s = slices[i];
+                const int32_t g = carry[0] + v[0];
+                if (g < h->cap_segs) segs[g] = WlSeg{s.q_row0, s.q_len, s.q_pos0, i, 0, 0, 0, 0};
+            }
+            __syncthreads();
+            if (tid == 0) carry[0] += tot[0];
+            __syncthreads();
+        }
+        if (tid == 0) {
+            s_nseg = carry[0];
+            s_nsl = ns;
+            if (carry[0] > h->cap_segs || ns > h->cap_slices) s_bad = 2;
+        }
+        __syncthreads();
+        if (s_bad) {
+            if (tid == 0) set_error(h, kErrCapacity);
+            return;
+        }
+        for (int g = tid; g < s_nseg; g += kPlanThreads) {
+            const int32_t next = (g + 1 < s_nseg) ? segs[g + 1].slice_begin : ns;
+            segs[g].slice_count = next - segs[g].slice_begin;
+        }
+    }
+    __syncthreads();
+
+    // per segment: q tiles, units and runs, then their exclusive scans
+    const int32_t nseg = s_nseg;
+    const int32_t G = a.hq / a.hkv;
+    if (tid == 0)
+        for (int k = 0; k < 4; ++k) carry[k] = 0;
+    __syncthreads();
+    for (int g0 = 0; g0 < nseg; g0 += kPlanThreads) {
+        const int g = g0 + tid;
+        int32_t v[2] = {0, 0};
+        int32_t nt = 0;
+        if (g < nseg) {
+            const WlSeg s = segs[g];
+            nt = (s.q_len + a.tile_m - 1) / a.tile_m;
+            const int32_t u = a.hkv * ((G / 2) * nt + (G % 2) * ((nt + 1) / 2));
+            v[0] = u;
+            v[1] = u * s.slice_count;
+        }
+        int32_t tot[2];
+        int32_t(*sm2)[2] = reinterpret_cast<int32_t(*)[2]>(&sm4[0][0]);
+        block_scan_excl<2>(v, tot, sm2);
+        if (g < nseg) {
+            segs[g].unit_base = carry[0] + v[0];
+            segs[g].run_base = carry[1] + v[1];
+            segs[g].ntiles = nt;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            carry[0] += tot[0];
+            carry[1] += tot[1];
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        h->nsegs = nseg;
+        h->nslices = s_nsl;
+        if (carry[0] > h->cap_units || carry[1] > h->cap_runs) {
+            set_error(h, kErrCapacity);
+        } else {
+            h->nunits = carry[0];
+            h->nruns = carry[1];
+        }
+    }
+}
+
+// kv-tile span [lo_t, hi_t) and allowed-pair count of q tile t against slice s.
+__device__ void tile_span(const WlSeg& g, const WlSlice& s, int32_t t, int32_t tile_m,
+                          int32_t tile_n, int32_t& lo_t, int32_t& hi_t, long long& pairs) {
+    long long mn = 0x7fffffffffffffffLL, mx = -1, cnt = 0;
+    const int32_t r0 = t * tile_m;
+    const int32_t r1 = min(r0 + tile_m, g.q_len);
+    for (int32_t r = r0; r < r1; ++r) {
+        long long lo, hi;
+        if (s.type == PVA_SLICE_FULL) {
+            lo = 0;
+            hi = s.k_len;
+        } else {
+            const long long qp = (long long)s.q_pos0 + r;
+            hi = qp - s.k_pos0 + 1;
+            lo = s.window > 0 ? qp - s.k_pos0 - s.window + 1 : 0;
+            if (lo < 0) lo = 0;
+            if (hi > s.k_len) hi = s.k_len;
+        }
+        if (hi <= lo) continue;
+        cnt += hi - lo;
+        mn = lo < mn ? lo : mn;
+        mx = hi > mx ? hi : mx;
+    }
+    if (cnt == 0) {
+        lo_t = hi_t = 0;
+    } else {
+        lo_t = (int32_t)(mn / tile_n);
+        hi_t = (int32_t)((mx + tile_n - 1) / tile_n);
+    }
+    pairs = cnt;
+}
+
+struct UnitArgs {
+    uint8_t* base;
+    int32_t tile_m, tile_n, hq, hkv;
+    long long c_tile;
+};
+
+// One thread per unit.  Enumeration inside a segment: kv head, then head
+// pairs (2p, 2p+1) x q tiles, then the odd last head's q-tile pairs.
+__global__ void __launch_bounds__(128) wl_units_kernel(UnitArgs a) {
+    WlHeader* h = reinterpret_cast<WlHeader*>(a.base);
+    if (h->error) return;
+    const int32_t n = h->nunits;
+    const int32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= n) return;
+    const WlSlice* slices = reinterpret_cast<const WlSlice*>(a.base + h->off.slices);
+    const WlSeg* segs = reinterpret_cast<const WlSeg*>(a.base + h->off.segs);
+    WlUnit* units = reinterpret_cast<WlUnit*>(a.base + h->off.units_enum);
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(a.base + h->off.keys);
+    WlRun* runs = reinterpret_cast<WlRun*>(a.base + h->off.runs);
+    // segment: last g with unit_base <= u (segments with zero units share a base)
+    int32_t lo = 0, hi = h->nsegs - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (segs[mid].unit_base <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    const int32_t gi = lo;
+    const WlSeg g = segs[gi];
+    const int32_t G = a.hq / a.hkv, nt = g.ntiles;
+    const int32_t per_kvh = (G / 2) * nt + (G % 2) * ((nt + 1) / 2);
+    const int32_t e = u - g.unit_base;
+    WlUnit w;
+    w.uid = u;
+    w.seg = gi;
+    w.kvh = e / per_kvh;
+    const int32_t e2 = e % per_kvh;
+    if (e2 < (G / 2) * nt) {
+        const int32_t p = e2 / nt, t = e2 % nt;
+        w.t0 = w.t1 = t;
+        w.h0 = w.kvh * G + 2 * p;
+        w.h1 = w.h0 + 1;
+    } else {
+        const int32_t uu = e2 - (G / 2) * nt;
+        w.t0 = 2 * uu;
+        w.t1 = (2 * uu + 1 < nt) ? 2 * uu + 1 : -1;
+        w.h0 = w.kvh * G + G - 1;
+        w.h1 = w.t1 >= 0 ? w.h0 : -1;
+    }
+    const int nsub = w.h1 >= 0 ? 2 : 1;
+    w.run_begin = g.run_base + e * g.slice_count;
+    w.run_count = g.slice_count;
+    w.cta = -1;
+    w.pad = 0;
+    long long pairs = 0, tiles = 0;
+    int32_t ntiles = 0;
+    for (int32_t si = 0; si < g.slice_count; ++si) {
+        const WlSlice s = slices[g.slice_begin + si];
+        int32_t rlo = 0, rhi = 0;
+        bool have = false;
+        const int32_t ts[2] = {w.t0, w.t1};
+        for (int k = 0; k < nsub; ++k) {
+            int32_t a0, b0;
+            long long pr;
+            tile_span(g, s, ts[k], a.tile_m, a.tile_n, a0, b0, pr);
+            pairs += pr;
+            if (b0 > a0) {
+                if (!have || a0 < rlo) rlo = a0;
+                if (!have || b0 > rhi) rhi = b0;
+                have = true;
+            }
+        }
+        runs[w.run_begin + si] = WlRun{g.slice_begin + si, rlo, rhi, 0};
+        tiles += (long long)(rhi - rlo) * nsub;
+        ntiles += rhi - rlo;
+    }
+    w.ntiles = ntiles;
+    w.pairs = pairs;
+    w.cost = pairs + a.c_tile * tiles;
+    units[u] = w;
+    if (w.cost < 0 || w.cost >= (1LL << kCostBits)) set_error(h, kErrCostRange);
+    const unsigned long long inv = ((1ULL << kCostBits) - 1) - (unsigned long long)w.cost;
+    keys[u] = (inv << kUidBits) | (unsigned long long)u;
+    atomicAdd(&h->pair_sum, (unsigned long long)pairs);
+    atomicAdd(&h->tile_sum, (unsigned long long)tiles);
+}
+
+// Stable sort by (cost desc, uid asc): every key is unique, so the rank of a
+// unit is the number of smaller keys.  order[rank] = uid.
+constexpr int kRankThreads = 256;
+constexpr int kRankTile = 2048;
+
+__global__ void __launch_bounds__(kRankThreads) wl_rank_kernel(uint8_t* base) {
+    WlHeader* h = reinterpret_cast<WlHeader*>(base);
+    if (h->error) return;
+    const int32_t n = h->nunits;
+    if ((int64_t)blockIdx.x * kRankThreads >= n) return;
+    const unsigned long long* keys = reinterpret_cast<const unsigned long long*>(base + h->off.keys);
+    int32_t* order = reinterpret_cast<int32_t*>(base + h->off.order);
+    __shared__ unsigned long long sk[kRankTile];
+    const int32_t i = blockIdx.x * kRankThreads + threadIdx.x;
+    const unsigned long long mine = i < n ? keys[i] : ~0ULL;
+    int32_t rank = 0;
+    for (int32_t j0 = 0; j0 < n; j0 += kRankTile) {
+        const int32_t m = min(kRankTile, n - j0);
+        for (int32_t j = threadIdx.x; j < m; j += kRankThreads) sk[j] = keys[j0 + j];
+        __syncthreads();
+        int32_t c = 0;
+        for (int32_t j = 0; j < m; ++j) c += sk[j] < mine;
+        rank += c;
+        __syncthreads();
+    }
+    if (i < n) order[rank] = i;
+}
+
+// LPT over num_ctas bins, exact and in parallel batches.
+// Bins are kept sorted by (load, id) as composite keys (load << 10 | id).
+// With tasks t, t+1, ... in LPT order, sequential LPT sends task t+j to the
+// j-th lightest bin S_j as long as S_j is lighter than every bin that
+// received a task earlier in the batch, i.e. S_j < min_{i<j} (S_i + c_{t+i});
+// the first j where this fails ends the batch.  Each batch is applied at once
+// and the bins are re-sorted by rank counting.
+constexpr int kLptThreads = 1024;
+
+__global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
+    WlHeader* h = reinterpret_cast<WlHeader*>(base);
+    if (h->error) return;
+    const int32_t n = h->nunits;
+    const int32_t B = h->num_ctas;
+    const WlUnit* units_enum = reinterpret_cast<const WlUnit*>(base + h->off.units_enum);
+    const int32_t* order = reinterpret_cast<const int32_t*>(base + h->off.order);
+    int32_t* assign = reinterpret_cast<int32_t*>(base + h->off.assign);
+    int32_t* local = reinterpret_cast<int32_t*>(base + h->off.local);
+    WlUnit* units = reinterpret_cast<WlUnit*>(base + h->off.units);
+    int32_t* cta_off = reinterpret_cast<int32_t*>(base + h->off.cta_off);
+    __shared__ unsigned long long S[kMaxBins], Snew[kMaxBins];
+    __shared__ unsigned long long wmin[32];
+    __shared__ int32_t cnt[kMaxBins];
+    __shared__ int32_t s_k;
+    __shared__ int32_t sm1[32][1];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    // bin keys hold load << 10: the total cost must stay below 2^53
+    const unsigned long long total_cost =
+        h->pair_sum + (unsigned long long)h->c_tile * h->tile_sum;
+    if (total_cost >= (1ULL << 53)) {
+        if (tid == 0) set_error(h, kErrCostRange);
+        return;
+    }
+    if (tid < B) {
+        S[tid] = (unsigned long long)tid;
+        cnt[tid] = 0;
+    }
+    __syncthreads();
+    for (int32_t t = 0; t < n;) {
+        // candidate value of bin j after receiving task t+j
+        unsigned long long val = ~0ULL;
+        long long c = 0;
+        if (tid < B && t + tid < n) {
+            c = units_enum[order[t + tid]].cost;
+            val = S[tid] + ((unsigned long long)c << 10);
+        }
+        // exclusive prefix-min of val over j
+        unsigned long long inc = val;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            unsigned long long x = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o && x < inc) inc = x;
+        }
+        if (lane == 31) wmin[w] = inc;
+        if (tid == 0) s_k = 0x7fffffff;
+        __syncthreads();
+        if (w == 0) {
+            unsigned long long x = wmin[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o && y < x) x = y;
+            }
+            wmin[lane] = x;
+        }
+        __syncthreads();
+        unsigned long long ex = __shfl_up_sync(0xffffffffu, inc, 1);
+        if (lane == 0) ex = ~0ULL;
+        if (w > 0 && wmin[w - 1] < ex) ex = wmin[w - 1];
+        // task t+j goes to S_j iff it exists and S_j < prefix-min (always for j = 0)
+        const bool ok = tid < B && t + tid < n && (tid == 0 || S[tid] < ex);
+        if (!ok) atomicMin(&s_k, tid);
+        __syncthreads();
+        const int32_t k = min(s_k, B);
+        if (tid < k) {
+            const int32_t uid = order[t + tid];
+            const int32_t bin = (int32_t)(S[tid] & 1023ULL);
+            assign[uid] = bin;
+            local[uid] = cnt[bin]++;
+            Snew[tid] = val;
+        } else if (tid < B) {
+            Snew[tid] = S[tid];
+        }
+        __syncthreads();
+        if (tid < B) {
+            const unsigned long long me = Snew[tid];
+            int32_t r = 0;
+            for (int32_t i = 0; i < B; ++i) r += Snew[i] < me;
+            S[r] = me;
+        }
+        t += k;
+        __syncthreads();
+    }
+    // CSR offsets (exclusive scan of the bin counts; B <= 1024)
+    int32_t v[1] = {tid < B ? cnt[tid] : 0};
+    int32_t tot[1];
+    block_scan_excl<1>(v, tot, sm1);
+    if (tid < B) cta_off[tid] = v[0];
+    if (tid == 0) cta_off[B] = tot[0];
+    if (tid < B) cnt[tid] = v[0];
+    __syncthreads();
+    for (int32_t u = tid; u < n; u += kLptThreads) {
+        WlUnit x = units_enum[u];
+        x.cta = assign[u];
+        units[cnt[x.cta] + local[u]] = x;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+// Capacities and offsets from bounds; false on invalid arguments.
+bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_params* p,
+                 int32_t num_ctas, WlHeader* h) {
+    if (!m || !p || num_docs < 0) return false;
+    if (p->tile_m <= 0 || p->tile_n <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
+        p->num_q_heads % p->num_kv_heads != 0 || p->c_tile < 0)
+        return false;
+    if (num_ctas <= 0 || num_ctas > kMaxBins) return false;
+    if (m->q_tokens < 0 || m->k_tokens < 0) return false;
+    int64_t cap_segs = 0, cap_slices = 0, max_group = 1;
+    switch (m->kind) {
+    case PVA_MASK_CAUSAL:
+        cap_segs = cap_slices = num_docs;
+        break;
+    case PVA_MASK_SLIDING_WINDOW:
+        if (m->window < 1) return false;
+        cap_segs = cap_slices = num_docs;
+        break;
+    case PVA_MASK_SHARED_QUESTION:
+        if (m->num_prefix_docs < 0 || m->num_prefix_docs > num_docs) return false;
+        cap_segs = num_docs;
+        cap_slices = (int64_t)num_docs * (m->num_prefix_docs + 1);
+        max_group = m->num_prefix_docs + 1;
+        break;
+    case PVA_MASK_ZIGZAG_PAIR:
+        if (m->cp < 1 || m->q_rank < 0 || m->q_rank >= m->cp || m->k_rank < 0 ||
+            m->k_rank >= m->cp)
+            return false;
+        cap_segs = 2 * (int64_t)num_docs;
+        cap_slices = 4 * (int64_t)num_docs;
+        max_group = 2;
+        break;
+    case PVA_MASK_SLICES: {
+        if (m->num_slices < 0 || (m->num_slices > 0 && !m->slices)) return false;
+        cap_segs = cap_slices = m->num_slices;
+        std::vector<std::pair<int32_t, int32_t>> ranges;
+        int64_t i = 0;
+        max_group = 1;
+        while (i < m->num_slices) {
+            const pva_slice& a = m->slices[i];
+            int64_t j = i;
+            while (j < m->num_slices) {
+                const pva_slice& b = m->slices[j];
+                if (b.q_row0 != a.q_row0 || b.q_len != a.q_len || b.q_pos0 != a.q_pos0) break;
+                if (b.q_len < 0 || b.k_len < 0 || b.q_row0 < 0 || b.k_row0 < 0 ||
+                    (int64_t)b.q_row0 + b.q_len > m->q_tokens ||
+                    (int64_t)b.k_row0 + b.k_len > m->k_tokens ||
+                    (b.type != PVA_SLICE_FULL && b.type != PVA_SLICE_CAUSAL))
+                    return false;
+                ++j;
+            }
+            max_group = std::max<int64_t>(max_group, j - i);
+            ranges.push_back({a.q_row0, a.q_len});
+            i = j;
+        }
+        std::sort(ranges.begin(), ranges.end());
+        for (size_t r = 1; r < ranges.size(); ++r)
+            if ((int64_t)ranges[r - 1].first + ranges[r - 1].second > ranges[r].first)
+                return false;  // overlapping query segments
+        break;
+    }
+    default:
+        return false;
+    }
+    const int64_t G = p->num_q_heads / p->num_kv_heads;
+    const int64_t qt = m->q_tokens / p->tile_m + cap_segs;  // bound on q tiles
+    int64_t cap_units = (int64_t)p->num_kv_heads * ((G / 2) * qt + (G % 2) * ((qt + cap_segs + 1) / 2)) + 1;
+    int64_t cap_runs = cap_units * max_group;
+    if (cap_units >= (1LL << kUidBits) || cap_runs > INT32_MAX || cap_slices > INT32_MAX ||
+        cap_segs > INT32_MAX)
+        return false;
+    memset(h, 0, sizeof *h);
+    h->magic = kWlMagic;
+    h->version = kWlVersion;
+    h->num_ctas = num_ctas;
+    h->tile_m = p->tile_m;
+    h->tile_n = p->tile_n;
+    h->hq = p->num_q_heads;
+    h->hkv = p->num_kv_heads;
+    h->kind = m->kind;
+    h->q_tokens = m->q_tokens;
+    h->k_tokens = m->k_tokens;
+    h->num_docs = num_docs;
+    h->cap_slices = (int32_t)std::max<int64_t>(cap_slices, 1);
+    h->cap_segs = (int32_t)std::max<int64_t>(cap_segs, 1);
+    h->cap_units = (int32_t)cap_units;
+    h->cap_runs = (int32_t)std::max<int64_t>(cap_runs, 1);
+    h->c_tile = p->c_tile;
+    int64_t o = 256;
+    WlOffsets& f = h->off;
+    f.slices = o; o = align256(o + (int64_t)h->cap_slices * sizeof(WlSlice));
+    f.segs = o; o = align256(o + (int64_t)h->cap_segs * sizeof(WlSeg));
+    f.units_enum = o; o = align256(o + cap_units * (int64_t)sizeof(WlUnit));
+    f.keys = o; o = align256(o + cap_units * 8);
+    f.order = o; o = align256(o + cap_units * 4);
+    f.assign = o; o = align256(o + cap_units * 4);
+    f.local = o; o = align256(o + cap_units * 4);
+    f.units = o; o = align256(o + cap_units * (int64_t)sizeof(WlUnit));
+    f.runs = o; o = align256(o + (int64_t)h->cap_runs * sizeof(WlRun));
+    f.cta_off = o; o = align256(o + ((int64_t)num_ctas + 1) * 4);
+    f.doc_scan = o; o = align256(o + 4 * ((int64_t)num_docs + 1) * 4);
+    f.total = o;
+    return true;
+}
+
+}  // namespace
+
+int32_t resolve_num_ctas(int32_t requested) {
+    if (requested > 0) return requested;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return sms;
+}
+
+}  // namespace pva
+
+using namespace pva;
+
+extern "C" size_t pva_worklist_bytes(int32_t num_docs, const pva_mask_desc* mask,
+                                     const pva_worklist_params* params) {
+    if (!params) return 0;
+    const int32_t nc = resolve_num_ctas(params->num_ctas);
+    WlHeader h;
+    if (!plan_layout(num_docs, mask, params, nc, &h)) return 0;
+    return (size_t)h.off.total;
+}
+
+extern "C" pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t num_docs,
+                                         const pva_mask_desc* mask,
+                                         const pva_worklist_params* params, void* worklist_dev,
+                                         size_t worklist_bytes, void* stream) {
+    if (!mask || !params || !worklist_dev) return PVA_ERR_INVALID_ARG;
+    if (mask->kind != PVA_MASK_SLICES && !cu_seqlens_dev) return PVA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(worklist_dev) % 256 != 0) return PVA_ERR_INVALID_ARG;
+    const int32_t nc = resolve_num_ctas(params->num_ctas);
+    if (nc <= 0) return PVA_ERR_CUDA;
+    WlHeader h;
+    if (!plan_layout(num_docs, mask, params, nc, &h)) return PVA_ERR_INVALID_ARG;
+    if ((int64_t)worklist_bytes < h.off.total) return PVA_ERR_BUFFER_TOO_SMALL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* base = reinterpret_cast<uint8_t*>(worklist_dev);
+    if (mask->kind == PVA_MASK_SLICES && mask->num_slices > 0) {
+        // the explicit slice list lives in host memory: copy it, and wait for
+        // the copy so that the caller may free its array on return
+        static_assert(sizeof(pva_slice) == sizeof(WlSlice), "slice layouts agree");
+        if (cudaMemcpyAsync(base + h.off.slices, mask->slices,
+                            (size_t)mask->num_slices * sizeof(pva_slice), cudaMemcpyHostToDevice,
+                            st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return PVA_ERR_CUDA;
+    }
+    PlanArgs pa;
+    pa.hinit = h;
+    pa.base = base;
+    pa.cu = cu_seqlens_dev;
+    pa.num_docs = num_docs;
+    pa.kind = mask->kind;
+    pa.window = mask->window;
+    pa.num_prefix = mask->num_prefix_docs;
+    pa.cp = mask->cp;
+    pa.q_rank = mask->q_rank;
+    pa.k_rank = mask->k_rank;
+    pa.num_slices = mask->num_slices;
+    pa.tile_m = params->tile_m;
+    pa.hq = params->num_q_heads;
+    pa.hkv = params->num_kv_heads;
+    pa.q_tokens = mask->q_tokens;
+    pa.k_tokens = mask->k_tokens;
+    wl_plan_kernel<<<1, kPlanThreads, 0, st>>>(pa);
+    UnitArgs ua{base, params->tile_m, params->tile_n, params->num_q_heads, params->num_kv_heads,
+                (long long)params->c_tile};
+    const int ub = (h.cap_units + 127) / 128;
+    wl_units_kernel<<<ub, 128, 0, st>>>(ua);
+    const int rb = (h.cap_units + kRankThreads - 1) / kRankThreads;
+    wl_rank_kernel<<<rb, kRankThreads, 0, st>>>(base);
+    wl_lpt_kernel<<<1, kLptThreads, 0, st>>>(base);
+    return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
+}
+
+extern "C" pva_status pva_worklist_error(const void* worklist_dev, int32_t* code_out,
+                                         void* stream) {
+    if (!worklist_dev || !code_out) return PVA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int32_t code = 0;
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(worklist_dev);
+    if (cudaMemcpyAsync(&code, base + offsetof(WlHeader, error), 4, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return PVA_ERR_CUDA;
+    *code_out = code;
+    return PVA_OK;
+}
+
+extern "C" pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out6, void* stream) {
+    if (!worklist_dev || !out6) return PVA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    WlHeader h;
+    if (cudaMemcpyAsync(&h, worklist_dev, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return PVA_ERR_CUDA;
+    if (h.magic != kWlMagic) return PVA_ERR_INVALID_ARG;
+    out6[0] = h.nsegs;
+    out6[1] = h.nslices;
+    out6[2] = h.nunits;
+    out6[3] = h.nruns;
+    out6[4] = h.hq > 0 ? (int64_t)(h.pair_sum / (unsigned long long)h.hq) : 0;
+    out6[5] = h.hq > 0 ? (int64_t)(h.tile_sum / (unsigned long long)h.hq) : 0;
+    return h.error ? (h.error >= kErrTimeoutBase ? PVA_ERR_TIMEOUT : PVA_ERR_DEVICE) : PVA_OK;
+}

@@ -1,0 +1,133 @@
+"""Device worklist vs the oracle's sequential worklist: bit-exact.
+
+"03 · 长文负载均衡" §3.2 (pair-exact tile costs; only non-empty blocks) and
+§2.1 / "数据并行负载均衡" §4.4 (LPT).  Every field is compared: slices,
+segments, units in CTA order (with costs and pair counts), kv-tile runs and
+the per-CTA CSR offsets.
+"""
+import numpy as np
+import pytest
+import torch
+
+from packed_varlen_attention_cu_gb300 import api
+from packed_varlen_attention_cu_gb300 import workloads as W
+
+from gpu_util import oracle_mask
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_worklist(cu_np, mask, hq, hkv, num_ctas, c_tile):
+    dev = torch.device("cuda")
+    cu = torch.from_numpy(np.ascontiguousarray(cu_np, dtype=np.int32)).to(dev)
+    params = api.make_params(hq, hkv, num_ctas=num_ctas, c_tile=c_tile)
+    wl = api.alloc_worklist(cu.numel() - 1, mask, params, dev)
+    api.build_worklist(cu, mask, params, wl)
+    torch.cuda.synchronize()
+    assert api.worklist_error(wl) == 0
+    return api.decode_worklist(wl), api.worklist_counts(wl)
+
+
+def _assert_same(g, o):
+    np.testing.assert_array_equal(g["slices"], o["slices"].reshape(-1, 8))
+    np.testing.assert_array_equal(g["segs"][:, :5], o["segs"].reshape(-1, 5))
+    np.testing.assert_array_equal(g["units"], o["units"].reshape(-1, 10))
+    np.testing.assert_array_equal(g["unit_cost"], o["unit_cost"])
+    np.testing.assert_array_equal(g["unit_pairs"], o["unit_pairs"])
+    np.testing.assert_array_equal(g["runs"], o["runs"].reshape(-1, 3))
+    np.testing.assert_array_equal(g["cta_off"], o["cta_off"])
+
+
+CASES = [
+    ("tiny", lambda: W.tiny_pack(), {}),
+    ("long-tail 2 packs GQA 7:1", lambda: W.long_tail_gqa(2), {}),
+    ("libra pair", lambda: W.libra_pair(), {}),
+    ("shared question", lambda: W.shared_question(), {}),
+    ("sliding window", lambda: W.sliding_window(), {}),
+    ("128K pack", lambda: W.zigzag_pack(), {}),
+]
+
+
+@pytest.mark.parametrize("name,mk,kw", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("num_ctas,c_tile", [(152, 0), (148, 4096), (7, 1)])
+def test_worklist_bit_exact(oracle_mod, name, mk, kw, num_ctas, c_tile):
+    w = mk()
+    cu = w.cu_seqlens
+    mask = api.mask_for_workload(w)
+    g, counts = _gpu_worklist(cu, mask, w.num_q_heads, w.num_kv_heads, num_ctas, c_tile)
+    o = oracle_mod.worklist(cu, oracle_mask(w.mask_kind, w.window, w.num_prefix_docs), 128, 128,
+                            w.num_q_heads, w.num_kv_heads, num_ctas, c_tile)
+    _assert_same(g, o)
+    assert counts["pairs_per_head"] == o["pairs_per_head"]
+
+
+def test_worklist_pair_count_matches_closed_form():
+    w = W.zigzag_pack()
+    mask = api.mask_for_workload(w)
+    _, counts = _gpu_worklist(w.cu_seqlens, mask, 32, 8, 152, 0)
+    assert counts["pairs_per_head"] == sum(l * (l + 1) // 2 for l in w.lengths) == 488185982
+
+
+@pytest.mark.parametrize("cp", [2, 8])
+def test_worklist_zigzag_pairs_bit_exact(oracle_mod, cp):
+    w = W.tiny_pack(seed=3)
+    cu = w.cu_seqlens
+    for r in range(cp):
+        tq = api.zigzag_shard_len(cu, cp, r)
+        for s in range(cp):
+            tk = api.zigzag_shard_len(cu, cp, s)
+            mask = api.make_mask(W.MASK_ZIGZAG_PAIR, tq, tk, cp=cp, q_rank=r, k_rank=s)
+            g, _ = _gpu_worklist(cu, mask, 4, 2, 13, 7)
+            o = oracle_mod.worklist(cu, oracle_mask(W.MASK_ZIGZAG_PAIR, cp=cp, q_rank=r, k_rank=s),
+                                    128, 128, 4, 2, 13, 7)
+            _assert_same(g, o)
+
+
+def test_worklist_explicit_slices_bit_exact(oracle_mod):
+    sl = np.array([[0, 300, 0, 0, 300, 0, 1, 0],
+                   [300, 200, 1000, 0, 150, 0, 0, 0],
+                   [300, 200, 1000, 300, 400, 900, 1, 64],
+                   [700, 5, 0, 700, 5, 0, 1, 0]], dtype=np.int32)
+    mask = api.make_mask(W.MASK_SLICES, 705, 705, slices=sl)
+    g, _ = _gpu_worklist(np.array([0, 705], dtype=np.int32), mask, 2, 1, 5, 0)
+    o = oracle_mod.worklist(np.array([0, 705], dtype=np.int32), oracle_mask(W.MASK_SLICES, slices=sl),
+                            128, 128, 2, 1, 5, 0)
+    _assert_same(g, o)
+
+
+def test_worklist_edge_lengths_bit_exact(oracle_mod):
+    lengths = [0, 1, 127, 128, 129, 0, 255, 256, 257, 1, 1, 383, 0]
+    cu = W.cu_seqlens_of(lengths)
+    for hq, hkv in ((1, 1), (3, 1), (6, 2), (8, 8)):
+        mask = api.make_mask(W.MASK_CAUSAL, int(cu[-1]), int(cu[-1]))
+        for nc in (1, 3, 1024):
+            g, _ = _gpu_worklist(cu, mask, hq, hkv, nc, 11)
+            o = oracle_mod.worklist(cu, oracle_mask(W.MASK_CAUSAL), 128, 128, hq, hkv, nc, 11)
+            _assert_same(g, o)
+
+
+def test_worklist_is_deterministic():
+    w = W.long_tail_gqa(1)
+    mask = api.mask_for_workload(w)
+    a, _ = _gpu_worklist(w.cu_seqlens, mask, 14, 2, 152, 0)
+    b, _ = _gpu_worklist(w.cu_seqlens, mask, 14, 2, 152, 0)
+    for key in ("units", "unit_cost", "runs", "cta_off"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_bad_cu_seqlens_sets_error_not_fault():
+    dev = torch.device("cuda")
+    cu = torch.tensor([0, 10, 5, 20], dtype=torch.int32, device=dev)  # decreasing
+    mask = api.make_mask(W.MASK_CAUSAL, 20, 20)
+    params = api.make_params(2, 2, num_ctas=4)
+    wl = api.alloc_worklist(3, mask, params, dev)
+    api.build_worklist(cu, mask, params, wl)
+    torch.cuda.synchronize()
+    assert api.worklist_error(wl) != 0
+    # attention on a failed worklist writes nothing and leaves the error in place
+    q = torch.zeros((20, 2, 64), dtype=torch.bfloat16, device=dev)
+    out = torch.full((20, 2, 64), 7.0, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((2, 20), 7.0, dtype=torch.float32, device=dev)
+    api.attn_fwd(q, q, q, cu, mask, params, wl, out, lse)
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0) and torch.all(lse == 7.0)

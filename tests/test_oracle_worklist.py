@@ -144,3 +144,15 @@ def test_worklist_csr_is_lpt(oracle_mod):
         c = wl["unit_cost"][off[b]:off[b + 1]]
         assert np.all(np.diff(c) <= 0)
         assert c.sum() == loads[b]
+
+
+def test_zigzag_chunk_without_keys_keeps_empty_segment(oracle_mod):
+    # rank 0's first chunk (positions [0, m)) sees nothing of rank 1's chunks
+    cp = 2
+    cu = W.cu_seqlens_of([16])
+    m = oracle_mod.Mask(W.MASK_ZIGZAG_PAIR, cp=cp, q_rank=0, k_rank=1)
+    wl = oracle_mod.worklist(cu, m, 4, 4, 2, 2, num_ctas=2)
+    segs = wl["segs"]
+    assert len(segs) == 2 and segs[0][4] == 0 and segs[1][4] == 2
+    empty_units = [u for u in wl["units"] if u[1] == 0]
+    assert all(u[8] == 0 for u in empty_units)
