@@ -1,0 +1,533 @@
+"""Benchmark: packed document-masked attention TFLOP/s on one GB300 (or N
+independent replicas under torchrun).
+
+A step is one pass of the hot path over one synthetic pack: the device
+worklist build (slices, exact pair costs, LPT over persistent CTAs) and the
+tcgen05 attention forward.  FLOPs count only allowed (unmasked) query-key
+pairs: 4 * head_dim per pair and q head (QK^T and PV).  The zigzag context-
+parallel path (shard maps, row gathers, per-pair partial attention, merges)
+is timed beside it on the same pack.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 128k]
+    python bench.py --impl reference     # the fp64 CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from packed_varlen_attention_cu_gb300 import workloads as W  # noqa: E402
+
+METRIC = "packed doc-masked attn TFLOP/s (unmasked pairs) and % of GB300 BF16 peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+WORKLOADS = {
+    "128k": (W.zigzag_pack, "128K causal pack: lognormal lengths (median 2048, sigma 1.5, "
+                            "clip [1, 65536], seed 0), 32 q / 8 kv heads, d=128, bf16 N(0,1)"),
+    "libra": (W.libra_pair, "Libra pair: 1x40960 + 10x4096 tokens, 16/16 heads, d=128"),
+    "longtail": (W.long_tail_gqa, "long-tail GQA: 8 packs x 32768 (median 644, sigma 1.6), "
+                                  "14 q / 2 kv heads, d=64"),
+    "sq": (W.shared_question, "shared question: 4096 + 8x2048, 16/4 heads, d=128"),
+    "window": (W.sliding_window, "sliding window 4096: docs 131072/65536/49152/16384, "
+                                 "16/4 heads, d=128"),
+    "tiny": (W.tiny_pack, "tiny pack: 2048 tokens, lognormal(5,1) clip [16,1024], 4/4 heads, d=64"),
+}
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profile_traffic(kernel_file: str, profile_name: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel
+    source is unchanged since it was taken (sha256 recorded in the summary)."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    src = os.path.join(ROOT, "packed_varlen_attention_cu_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples under load: drop the idle ramp at both ends
+        load = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    """(rank, world, local_rank) from the torchrun environment, NCCL group for N > 1."""
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def aggregate(seconds: float, flops: float, world: int):
+    """Whole-job numbers: max time over ranks, sum of FLOPs (weak scaling, no
+    data-path collective; the reduction only collects the timing)."""
+    if world <= 1:
+        return seconds, flops
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    f = torch.tensor([flops], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(f.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- device arm
+def run_pva(args, rank, world, local):
+    import torch
+
+    from packed_varlen_attention_cu_gb300 import api
+    from packed_varlen_attention_cu_gb300 import build as pva_build
+
+    pva_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mk, desc = WORKLOADS[args.workload]
+    w = mk()
+    T, hq, hkv, d = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
+    stream = torch.cuda.current_stream()
+    cu_np = w.cu_seqlens
+    cu = torch.from_numpy(cu_np).to(dev)
+    q, k, v = W.workload_qkv(w, device=str(dev))
+    mask = api.mask_for_workload(w)
+    params = api.make_params(hq, hkv, num_ctas=0, c_tile=args.c_tile)
+    wl = api.alloc_worklist(w.num_docs, mask, params, dev)
+    out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
+    num_ctas = torch.cuda.get_device_properties(dev).multi_processor_count
+    busy = torch.zeros((num_ctas, 2), dtype=torch.int64, device=dev)
+
+    api.build_worklist(cu, mask, params, wl)
+    counts = api.worklist_counts(wl)
+    assert counts["status"] == 0, counts
+    pairs = counts["pairs_per_head"]
+    flops = 4.0 * d * hq * pairs
+    n_wl_kernels = 4
+    io_bytes = (q.numel() + k.numel() + v.numel() + out.numel()) * 2 + lse.numel() * 4
+
+    def step(ev_a=None, ev_b=None):
+        api.build_worklist(cu, mask, params, wl, stream)
+        if ev_a is not None:
+            ev_a.record(stream)
+        api.attn_fwd(q, k, v, cu, mask, params, wl, out, lse, 0.0, None, stream)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert api.worklist_error(wl) == 0
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(K):
+            step(*evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    total_s = start.elapsed_time(end) / 1e3
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    wall_s, job_flops = aggregate(total_s, flops * K, world)
+    value = job_flops / wall_s / 1e12
+    attn_avg_s = sum(attn_ms) / len(attn_ms) / 1e3
+    achieved = flops / attn_avg_s / 1e12
+
+    # per-CTA busy time of one more launch (same configuration)
+    api.attn_fwd(q, k, v, cu, mask, params, wl, out, lse, 0.0, busy, stream)
+    torch.cuda.synchronize()
+    b = busy.cpu().numpy().astype(np.float64)
+    dur = b[:, 1] - b[:, 0]
+    worked = dur[dur > 0]
+    imbalance = float(worked.max() / worked.min() - 1.0) if worked.size else None
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    traffic = profile_traffic("attn_fwd.cu", f"attn_fwd_{args.workload}.txt")
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(wall_s / K * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator; lengths and values described in config)",
+        "config": {"workload": desc, "tokens": T, "docs": w.num_docs, "q_heads": hq,
+                   "kv_heads": hkv, "head_dim": d, "mask": w.mask_kind,
+                   "pairs_per_head": pairs, "flops_per_step": flops,
+                   "step": "device worklist build (4 kernels) + attention forward (1 kernel)",
+                   "l2": f"inputs larger than L2: Q+K+V+O+LSE = {io_bytes / 1e9:.2f} GB "
+                         f"> {L2_BYTES / 1e6:.0f} MB, no flush",
+                   "num_ctas": num_ctas, "c_tile": args.c_tile,
+                   "parallelism": f"{world} independent replica(s), one per GPU"},
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops (burst); frac vs sustained "
+                                    f"{peak_sus}: {achieved / peak_sus:.4f}",
+                     "kernel": "attn_fwd_kernel<128>" if d == 128 else "attn_fwd_kernel<64>",
+                     "algorithmic_flops_per_launch": flops,
+                     "avg_launch_ms": round(attn_avg_s * 1e3, 4)},
+        "imbalance": None if imbalance is None else round(imbalance, 4),
+        "gpu_launches": K * (n_wl_kernels + 1),
+        "clocks": clocks.summary(),
+        "worklist_ms": round((wall_s - attn_avg_s * K) / K * 1e3, 4),
+    }
+    return result, (w, q, k, v, cu_np, flops, mask, params, hbm)
+
+
+def run_e2e(args, ctx, world):
+    """Same metric through the public API with host buffers: per step, H2D of
+    Q/K/V/cu_seqlens from pinned memory, worklist + attention, D2H of O/LSE."""
+    import torch
+
+    from packed_varlen_attention_cu_gb300 import api
+    w, q, k, v, cu_np, flops, mask, params, _ = ctx
+    dev = q.device
+    stream = torch.cuda.current_stream()
+    hq_, hk_, hv_ = (t.cpu().pin_memory() for t in (q, k, v))
+    hcu = torch.from_numpy(cu_np).pin_memory()
+    T, hq, d = q.shape
+    o_h = torch.empty((T, hq, d), dtype=torch.bfloat16).pin_memory()
+    l_h = torch.empty((hq, T), dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dcu = torch.empty((cu_np.shape[0],), dtype=torch.int32, device=dev)
+    dout = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+    dlse = torch.empty((hq, T), dtype=torch.float32, device=dev)
+    wl = api.alloc_worklist(w.num_docs, mask, params, dev)
+
+    def step():
+        dq.copy_(hq_, non_blocking=True)
+        dk.copy_(hk_, non_blocking=True)
+        dv.copy_(hv_, non_blocking=True)
+        dcu.copy_(hcu, non_blocking=True)
+        api.build_worklist(dcu, mask, params, wl, stream)
+        api.attn_fwd(dq, dk, dv, dcu, mask, params, wl, dout, dlse, 0.0, None, stream)
+        o_h.copy_(dout, non_blocking=True)
+        l_h.copy_(dlse, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    K = max(3, args.steps // 5)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(K):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t, f = aggregate(s.elapsed_time(e) / 1e3, flops * K, world)
+    h2d = (q.numel() + k.numel() + v.numel()) * 2 + cu_np.nbytes
+    d2h = dout.numel() * 2 + dlse.numel() * 4
+    return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": round(t / K * 1e3, 4)}
+
+
+def run_zigzag(args, ctx, world):
+    """Zigzag CP emulation on one GPU: cp virtual ranks; rank r runs its Q
+    shard against the KV shard of rank (r - t) mod cp at ring step t (fp32
+    partials), merging into the running (O, LSE); results scattered back."""
+    import torch
+
+    from packed_varlen_attention_cu_gb300 import api
+    w, q, k, v, cu_np, flops, _, base_params, hbm = ctx
+    cp = w.cp or 8
+    dev = q.device
+    stream = torch.cuda.current_stream()
+    T, hq, d = q.shape
+    hkv = k.shape[1]
+    cu = torch.from_numpy(cu_np).to(dev)
+    lens = [api.zigzag_shard_len(cu_np, cp, r) for r in range(cp)]
+    maps = [torch.empty((n,), dtype=torch.int32, device=dev) for n in lens]
+    qs = [torch.empty((n, hq, d), dtype=torch.bfloat16, device=dev) for n in lens]
+    ks = [torch.empty((n, hkv, d), dtype=torch.bfloat16, device=dev) for n in lens]
+    vs = [torch.empty((n, hkv, d), dtype=torch.bfloat16, device=dev) for n in lens]
+    # per-rank outputs (fp32 partial layout, rank-local rows) and one scratch partial
+    acc_o = [torch.empty((n, hq, d), dtype=torch.float32, device=dev) for n in lens]
+    acc_l = [torch.empty((hq, n), dtype=torch.float32, device=dev) for n in lens]
+    nmax = max(lens)
+    part_o = torch.empty((nmax, hq, d), dtype=torch.float32, device=dev)
+    part_l = torch.empty((hq * nmax,), dtype=torch.float32, device=dev)
+    params = api.make_params(hq, hkv, num_ctas=0, c_tile=base_params.c_tile)
+    masks = {(r, s): api.make_mask(W.MASK_ZIGZAG_PAIR, lens[r], lens[s], cp=cp, q_rank=r, k_rank=s)
+             for r in range(cp) for s in range(cp)}
+    wls = {key: api.alloc_worklist(w.num_docs, m, params, dev) for key, m in masks.items()}
+    merge_ev = []
+
+    def step(record=False):
+        for r in range(cp):
+            api.zigzag_shard(cu, cp, r, maps[r], None, stream)
+            api.gather_rows(q, maps[r], qs[r], stream=stream)
+            api.gather_rows(k, maps[r], ks[r], stream=stream)
+            api.gather_rows(v, maps[r], vs[r], stream=stream)
+        for r in range(cp):
+            n = lens[r]
+            po, pl = part_o[:n], part_l[: hq * n].view(hq, n)
+            for t in range(cp):
+                s = (r - t) % cp
+                m = masks[(r, s)]
+                api.build_worklist(cu, m, params, wls[(r, s)], stream)
+                dst_o, dst_l = (acc_o[r], acc_l[r]) if t == 0 else (po, pl)
+                api.attn_fwd(qs[r], ks[s], vs[s], cu, m, params, wls[(r, s)], dst_o, dst_l, 0.0,
+                             None, stream)
+                if t > 0:
+                    if record:
+                        ea = torch.cuda.Event(enable_timing=True)
+                        eb = torch.cuda.Event(enable_timing=True)
+                        ea.record(stream)
+                    api.merge_partials(acc_o[r], acc_l[r], po, pl, acc_o[r], acc_l[r], stream)
+                    if record:
+                        eb.record(stream)
+                        merge_ev.append((ea, eb, n))
+
+    step()
+    torch.cuda.synchronize()
+    K = max(2, args.steps // 20)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for i in range(K):
+        step(record=(i == K - 1))
+    e.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t, f = aggregate(s.elapsed_time(e) / 1e3, flops * K, world)
+    mtimes = [a.elapsed_time(b) / 1e3 for a, b, _ in merge_ev]
+    mbytes = [n * hq * (3 * 4 * d + 3 * 4) for _, _, n in merge_ev]
+    merge_gbs = sum(mbytes) / sum(mtimes) / 1e9 if mtimes else None
+    launches = cp * 4 + cp * cp * 5 + cp * (cp - 1)
+    return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "cp": cp, "steps": K,
+            "ms_per_step": round(t / K * 1e3, 3),
+            "merge": {"bound": "hbm", "achieved": round(merge_gbs, 1) if merge_gbs else None,
+                      "peak": hbm, "unit": "GB/s",
+                      "frac": round(merge_gbs / hbm, 4) if merge_gbs else None,
+                      "bytes_per_row": 3 * 4 * d + 3 * 4, "launches_per_step": cp * (cp - 1)},
+            "gpu_launches_per_step": launches,
+            "note": "cp virtual ranks on one GPU: shard maps, row gathers, per-pair worklist + "
+                    "fp32 partial attention, in-place merges; outputs stay rank-local"}
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample(w, q_bits, k_bits, v_bits, seconds: float, seed: int = 7):
+    """Time the fp64 oracle on a bounded random sample of (row, head) jobs
+    of the workload; returns (TFLOP/s, cores, description, elapsed)."""
+    import oracle
+    oracle.compile_oracle()
+    T, hq, d = w.total_tokens, w.num_q_heads, w.head_dim
+    cu = w.cu_seqlens
+    docs = np.searchsorted(cu, np.arange(T), side="right") - 1
+    keys_per_row = (np.arange(T) - cu[docs] + 1).astype(np.int64)  # causal per document
+    if w.mask_kind == W.MASK_SLIDING_WINDOW:
+        keys_per_row = np.minimum(keys_per_row, w.window)
+    elif w.mask_kind == W.MASK_SHARED_QUESTION:
+        keys_per_row = keys_per_row + np.where(docs >= w.num_prefix_docs,
+                                               int(cu[w.num_prefix_docs]), 0)
+    m = oracle.Mask(w.mask_kind, window=w.window, num_prefix=w.num_prefix_docs)
+
+    def run(n, s):
+        jobs = W.random_rows(T, hq, n, seed=s)
+        t0 = time.perf_counter()
+        oracle.attention(q_bits, k_bits, v_bits, cu, m, jobs=jobs)
+        dt = time.perf_counter() - t0
+        return dt, float(keys_per_row[jobs[:, 0]].sum()), n
+
+    dt, _, n = run(256, seed)
+    n_target = int(max(256, min(2_000_000, 256 * seconds / max(dt, 1e-3))))
+    dt, pairs, n = run(n_target, seed + 1)
+    flops = 4.0 * d * pairs
+    cores = oracle.num_threads()
+    desc = (f"{n} random (row, head) jobs of the workload, fp64, OpenMP over {cores} threads, "
+            f"{pairs:.3e} allowed pairs, {dt:.1f} s")
+    return flops / dt / 1e12, cores, desc, dt
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: each step a bounded sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import torch
+    mk, desc = WORKLOADS[args.workload]
+    w = mk()
+    import oracle
+    q, k, v = W.workload_qkv(w, device="cpu")
+    qb, kb, vb = oracle.bf16_bits(q), oracle.bf16_bits(k), oracle.bf16_bits(v)
+    per_step = max(1.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    vals, times, cores, sample = [], [], 1, ""
+    for i in range(args.warmup + args.steps):
+        tf, cores, sample, dt = oracle_sample(w, qb, kb, vb, per_step, seed=100 + i)
+        if i >= args.warmup:
+            vals.append(tf)
+            times.append(dt)
+    value = float(np.mean(vals))
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(times)), 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": desc, "tokens": w.total_tokens,
+                                            "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                                            "head_dim": w.head_dim},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("pva", "reference"), default="pva")
+    ap.add_argument("--workload", choices=tuple(WORKLOADS), default="128k")
+    ap.add_argument("--c-tile", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-zigzag", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        res = run_reference(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+
+    rank, world, local = dist_setup(args.gpus)
+    res, ctx = run_pva(args, rank, world, local)
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, ctx, world)
+    if not args.no_zigzag and ctx[0].cp:
+        res["zigzag_cp"] = run_zigzag(args, ctx, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle  # noqa: F401  (CPU baseline leg only)
+        from oracle import bf16_bits
+        w, q, k, v = ctx[:4]
+        tf, cores, sample, _ = oracle_sample(w, bf16_bits(q), bf16_bits(k), bf16_bits(v),
+                                             args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": cores,
+                               "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
