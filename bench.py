@@ -49,6 +49,18 @@ WORKLOADS = {
 
 
 # ----------------------------------------------------------------- helpers
+def make_workload(args):
+    """The named workload; --pack-tokens shrinks the 128K pack to a smaller
+    pack drawn with the same length recipe (used for profiling captures)."""
+    mk, desc = WORKLOADS[args.workload]
+    if args.pack_tokens and args.workload == "128k":
+        w = W.Workload(f"{args.pack_tokens}-token causal pack H=32/8 d=128",
+                       W.lognormal_doc_lengths(args.pack_tokens, math.log(2048.0), 1.5, 1,
+                                               65536, 0), 32, 8, 128, cp=8)
+        return w, desc.replace("128K", f"{args.pack_tokens}-token")
+    return mk(), desc
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -184,8 +196,7 @@ def run_pva(args, rank, world, local):
     pva_build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    mk, desc = WORKLOADS[args.workload]
-    w = mk()
+    w, desc = make_workload(args)
     T, hq, hkv, d = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
     stream = torch.cuda.current_stream()
     cu_np = w.cu_seqlens
@@ -459,8 +470,7 @@ def run_reference(args):
     if rank != 0:
         return None
     import torch
-    mk, desc = WORKLOADS[args.workload]
-    w = mk()
+    w, desc = make_workload(args)
     import oracle
     q, k, v = W.workload_qkv(w, device="cpu")
     qb, kb, vb = oracle.bf16_bits(q), oracle.bf16_bits(k), oracle.bf16_bits(v)
@@ -492,7 +502,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("pva", "reference"), default="pva")
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="128k")
-    ap.add_argument("--c-tile", type=int, default=0)
+    ap.add_argument("--c-tile", type=int, default=8192)
+    ap.add_argument("--pack-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-zigzag", action="store_true")

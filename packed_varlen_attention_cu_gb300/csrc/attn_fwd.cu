@@ -397,11 +397,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (col < c_lo || col >= c_hi) sr[c][e] = __float_as_uint(-INFINITY);
                             }
                     }
-                    float mx = -INFINITY;
+                    // row max: 4 independent partial maxima, then a tree
+                    float pm[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < 4; ++c) {
+                        pm[c] = __uint_as_float(sr[c][0]);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+                        for (int e = 1; e < 32; ++e) pm[c] = fmaxf(pm[c], __uint_as_float(sr[c][e]));
+                    }
+                    const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
                     const float m_tile = mx * p.scale_log2;  // -inf stays -inf
                     float alpha = 1.f;
                     bool rescale = false;
@@ -458,36 +462,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
             const int64_t row = (int64_t)(st.q_row + r) * p.hq + st.head;
+            // read the whole row of O, hand the tensor memory back to the MMA
+            // warp, then normalise and store
+            uint32_t o[D / 32][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + c * 32, o);
-                tmem_ld_wait(o);
-                if (valid) {
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, o[c]);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
+            tc_fence_before();
+            mbar_arrive(&sh.o_empty[i]);
+            if (valid) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
                     if (p.out_fp32) {
                         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) +
                                                                 row * D + c * 32);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv,
-                                                 __uint_as_float(o[4 * e + 1]) * inv,
-                                                 __uint_as_float(o[4 * e + 2]) * inv,
-                                                 __uint_as_float(o[4 * e + 3]) * inv);
+                            dst[e] = make_float4(__uint_as_float(o[c][4 * e]) * inv,
+                                                 __uint_as_float(o[c][4 * e + 1]) * inv,
+                                                 __uint_as_float(o[c][4 * e + 2]) * inv,
+                                                 __uint_as_float(o[c][4 * e + 3]) * inv);
                     } else {
                         uint4* dst = reinterpret_cast<uint4*>(
                             reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + c * 32);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             dst[e] = make_uint4(
-                                pack_bf16x2(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
+                                pack_bf16x2(__uint_as_float(o[c][8 * e]) * inv, __uint_as_float(o[c][8 * e + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(o[c][8 * e + 2]) * inv, __uint_as_float(o[c][8 * e + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(o[c][8 * e + 4]) * inv, __uint_as_float(o[c][8 * e + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(o[c][8 * e + 6]) * inv, __uint_as_float(o[c][8 * e + 7]) * inv));
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&sh.o_empty[i]);
             if (valid)
                 p.lse[(int64_t)st.head * p.q_tokens + st.q_row + r] =
                     l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;

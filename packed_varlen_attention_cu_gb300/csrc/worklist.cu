@@ -12,7 +12,7 @@
 //                      of the mask, per-segment unit/run bases (block scans)
 //   wl_units  grid   : one thread per work unit: kv-tile span of every slice
 //                      for its two sub-tiles, exact pair count, cost, sort key
-//   wl_rank   grid   : stable sort by (cost desc, uid asc) as a rank count
+//   wl_sort_chunks / wl_merge_rank : stable sort by (cost desc, uid asc)
 //   wl_lpt    1 CTA  : exact LPT in batches (see below), CSR by CTA
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -352,6 +352,10 @@ struct UnitArgs {
     long long c_tile;
 };
 
+__device__ __forceinline__ void unit_body(const UnitArgs& a, WlHeader* h, int32_t u,
+                                          unsigned long long& pairs_out,
+                                          unsigned long long& tiles_out);
+
 // One thread per unit.  Enumeration inside a segment: kv head, then head
 // pairs (2p, 2p+1) x q tiles, then the odd last head's q-tile pairs.
 __global__ void __launch_bounds__(128) wl_units_kernel(UnitArgs a) {
@@ -359,7 +363,23 @@ __global__ void __launch_bounds__(128) wl_units_kernel(UnitArgs a) {
     if (h->error) return;
     const int32_t n = h->nunits;
     const int32_t u = blockIdx.x * blockDim.x + threadIdx.x;
-    if (u >= n) return;
+    if ((int64_t)blockIdx.x * blockDim.x >= n) return;  // whole warps stay for the reduction
+    unsigned long long pairs_out = 0, tiles_out = 0;
+    if (u < n) unit_body(a, h, u, pairs_out, tiles_out);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        pairs_out += __shfl_down_sync(0xffffffffu, pairs_out, o);
+        tiles_out += __shfl_down_sync(0xffffffffu, tiles_out, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&h->pair_sum, pairs_out);
+        atomicAdd(&h->tile_sum, tiles_out);
+    }
+}
+
+__device__ __forceinline__ void unit_body(const UnitArgs& a, WlHeader* h, int32_t u,
+                                          unsigned long long& pairs_out,
+                                          unsigned long long& tiles_out) {
     const WlSlice* slices = reinterpret_cast<const WlSlice*>(a.base + h->off.slices);
     const WlSeg* segs = reinterpret_cast<const WlSeg*>(a.base + h->off.segs);
     WlUnit* units = reinterpret_cast<WlUnit*>(a.base + h->off.units_enum);
@@ -428,36 +448,86 @@ __global__ void __launch_bounds__(128) wl_units_kernel(UnitArgs a) {
     if (w.cost < 0 || w.cost >= (1LL << kCostBits)) set_error(h, kErrCostRange);
     const unsigned long long inv = ((1ULL << kCostBits) - 1) - (unsigned long long)w.cost;
     keys[u] = (inv << kUidBits) | (unsigned long long)u;
-    atomicAdd(&h->pair_sum, (unsigned long long)pairs);
-    atomicAdd(&h->tile_sum, (unsigned long long)tiles);
+    pairs_out = (unsigned long long)pairs;
+    tiles_out = (unsigned long long)tiles;
 }
 
-// Stable sort by (cost desc, uid asc): every key is unique, so the rank of a
-// unit is the number of smaller keys.  order[rank] = uid.
-constexpr int kRankThreads = 256;
-constexpr int kRankTile = 2048;
+// Stable sort by (cost desc, uid asc).  Every key is unique, so a unit's
+// rank is the number of smaller keys.  Two kernels: each 2048-key chunk is
+// sorted in shared memory (bitonic network), then every key's rank is its
+// position in its own chunk plus its lower bound in each other chunk.
+constexpr int kSortChunk = 2048;
+constexpr int kSortThreads = 1024;
 
-__global__ void __launch_bounds__(kRankThreads) wl_rank_kernel(uint8_t* base) {
+__global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(uint8_t* base) {
     WlHeader* h = reinterpret_cast<WlHeader*>(base);
     if (h->error) return;
     const int32_t n = h->nunits;
-    if ((int64_t)blockIdx.x * kRankThreads >= n) return;
-    const unsigned long long* keys = reinterpret_cast<const unsigned long long*>(base + h->off.keys);
-    int32_t* order = reinterpret_cast<int32_t*>(base + h->off.order);
-    __shared__ unsigned long long sk[kRankTile];
-    const int32_t i = blockIdx.x * kRankThreads + threadIdx.x;
-    const unsigned long long mine = i < n ? keys[i] : ~0ULL;
-    int32_t rank = 0;
-    for (int32_t j0 = 0; j0 < n; j0 += kRankTile) {
-        const int32_t m = min(kRankTile, n - j0);
-        for (int32_t j = threadIdx.x; j < m; j += kRankThreads) sk[j] = keys[j0 + j];
-        __syncthreads();
-        int32_t c = 0;
-        for (int32_t j = 0; j < m; ++j) c += sk[j] < mine;
-        rank += c;
-        __syncthreads();
+    const int32_t c0 = blockIdx.x * kSortChunk;
+    if (c0 >= n) return;
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(base + h->off.keys);
+    __shared__ unsigned long long sk[kSortChunk];
+    const int32_t m = min(kSortChunk, n - c0);
+    for (int32_t i = threadIdx.x; i < kSortChunk; i += kSortThreads)
+        sk[i] = i < m ? keys[c0 + i] : ~0ULL;
+    __syncthreads();
+    for (int32_t size = 2; size <= kSortChunk; size <<= 1) {
+        for (int32_t stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int32_t t = threadIdx.x; t < kSortChunk / 2; t += kSortThreads) {
+                const int32_t lo = 2 * t - (t & (stride - 1));
+                const int32_t hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const unsigned long long x = sk[lo], y = sk[hi];
+                if ((x > y) == up) {
+                    sk[lo] = y;
+                    sk[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
     }
-    if (i < n) order[rank] = i;
+    for (int32_t i = threadIdx.x; i < m; i += kSortThreads) keys[c0 + i] = sk[i];
+}
+
+__global__ void __launch_bounds__(kSortThreads) wl_merge_rank_kernel(uint8_t* base) {
+    WlHeader* h = reinterpret_cast<WlHeader*>(base);
+    if (h->error) return;
+    const int32_t n = h->nunits;
+    const int32_t c0 = blockIdx.x * kSortChunk;
+    if (c0 >= n) return;
+    const unsigned long long* keys =
+        reinterpret_cast<const unsigned long long*>(base + h->off.keys);
+    int32_t* order = reinterpret_cast<int32_t*>(base + h->off.order);
+    __shared__ unsigned long long other[kSortChunk];
+    const int32_t m = min(kSortChunk, n - c0);
+    const int32_t nchunks = (n + kSortChunk - 1) / kSortChunk;
+    unsigned long long mine[2];
+    int32_t rank[2];
+    for (int e = 0; e < 2; ++e) {
+        const int32_t i = threadIdx.x + e * kSortThreads;
+        mine[e] = i < m ? keys[c0 + i] : ~0ULL;
+        rank[e] = i;
+    }
+    for (int32_t c = 0; c < nchunks; ++c) {
+        if (c == (int32_t)blockIdx.x) continue;
+        const int32_t oc = c * kSortChunk, om = min(kSortChunk, n - oc);
+        __syncthreads();
+        for (int32_t i = threadIdx.x; i < om; i += kSortThreads) other[i] = keys[oc + i];
+        __syncthreads();
+        for (int e = 0; e < 2; ++e) {
+            int32_t lo = 0, hi = om;  // number of keys < mine[e]
+            while (lo < hi) {
+                const int32_t mid = (lo + hi) >> 1;
+                if (other[mid] < mine[e]) lo = mid + 1;
+                else hi = mid;
+            }
+            rank[e] += lo;
+        }
+    }
+    for (int e = 0; e < 2; ++e) {
+        const int32_t i = threadIdx.x + e * kSortThreads;
+        if (i < m) order[rank[e]] = (int32_t)(mine[e] & ((1ULL << kUidBits) - 1));
+    }
 }
 
 // LPT over num_ctas bins, exact and in parallel batches.
@@ -468,6 +538,7 @@ __global__ void __launch_bounds__(kRankThreads) wl_rank_kernel(uint8_t* base) {
 // the first j where this fails ends the batch.  Each batch is applied at once
 // and the bins are re-sorted by rank counting.
 constexpr int kLptThreads = 1024;
+constexpr int kLptStage = 2048;
 
 __global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
     WlHeader* h = reinterpret_cast<WlHeader*>(base);
@@ -483,6 +554,9 @@ __global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
     __shared__ unsigned long long S[kMaxBins], Snew[kMaxBins];
     __shared__ unsigned long long wmin[32];
     __shared__ int32_t cnt[kMaxBins];
+    // the next kLptStage units in LPT order (cost, uid), refilled as t advances
+    __shared__ long long scost[kLptStage];
+    __shared__ int32_t suid[kLptStage];
     __shared__ int32_t s_k;
     __shared__ int32_t sm1[32][1];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -498,12 +572,22 @@ __global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
         cnt[tid] = 0;
     }
     __syncthreads();
+    int32_t stage0 = -kLptStage;
     for (int32_t t = 0; t < n;) {
+        if (t + B > stage0 + kLptStage) {  // a batch may run past the staged window
+            stage0 = t;
+            for (int32_t i = tid; i < kLptStage && t + i < n; i += kLptThreads) {
+                const int32_t uid = order[t + i];
+                suid[i] = uid;
+                scost[i] = units_enum[uid].cost;
+            }
+            __syncthreads();
+        }
         // candidate value of bin j after receiving task t+j
         unsigned long long val = ~0ULL;
         long long c = 0;
         if (tid < B && t + tid < n) {
-            c = units_enum[order[t + tid]].cost;
+            c = scost[t + tid - stage0];
             val = S[tid] + ((unsigned long long)c << 10);
         }
         // exclusive prefix-min of val over j
@@ -535,7 +619,7 @@ __global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
         __syncthreads();
         const int32_t k = min(s_k, B);
         if (tid < k) {
-            const int32_t uid = order[t + tid];
+            const int32_t uid = suid[t + tid - stage0];
             const int32_t bin = (int32_t)(S[tid] & 1023ULL);
             assign[uid] = bin;
             local[uid] = cnt[bin]++;
@@ -547,6 +631,7 @@ __global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
         if (tid < B) {
             const unsigned long long me = Snew[tid];
             int32_t r = 0;
+#pragma unroll 8
             for (int32_t i = 0; i < B; ++i) r += Snew[i] < me;
             S[r] = me;
         }
@@ -745,8 +830,9 @@ extern "C" pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t 
                 (long long)params->c_tile};
     const int ub = (h.cap_units + 127) / 128;
     wl_units_kernel<<<ub, 128, 0, st>>>(ua);
-    const int rb = (h.cap_units + kRankThreads - 1) / kRankThreads;
-    wl_rank_kernel<<<rb, kRankThreads, 0, st>>>(base);
+    const int sb = (h.cap_units + kSortChunk - 1) / kSortChunk;
+    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(base);
+    wl_merge_rank_kernel<<<sb, kSortThreads, 0, st>>>(base);
     wl_lpt_kernel<<<1, kLptThreads, 0, st>>>(base);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
