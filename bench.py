@@ -291,6 +291,8 @@ def run_pva(args, rank, world, local):
         "gpu_launches": K * (n_wl_kernels + 1),
         "clocks": clocks.summary(),
         "worklist_ms": round((wall_s - attn_avg_s * K) / K * 1e3, 4),
+        "worklist": {"units": counts["units"], "lpt_steps": counts["lpt_steps"],
+                     "tiles_per_head": counts["tiles_per_head"]},
     }
     return result, (w, q, k, v, cu_np, flops, mask, params, hbm)
 

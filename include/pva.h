@@ -101,8 +101,10 @@ typedef struct {
     int32_t num_q_heads, num_kv_heads;
     int32_t num_ctas;   /* persistent CTAs (bins of the LPT); <= 0: number of SMs */
     int32_t reserved;
-    int64_t c_tile;     /* cost of one computed (sub-tile, kv tile) in pair units, >= 0;
-                           unit cost = exact allowed pairs + c_tile * tiles computed */
+    int64_t c_tile;     /* fixed cost, in pair units (>= 0), of one computed (sub-tile, kv
+                           tile) and of one query sub-tile (Q load, output rows):
+                           unit cost = exact allowed pairs
+                                       + c_tile * (sub-tiles * kv tiles + sub-tiles) */
 } pva_worklist_params;
 
 /* Upper bound, in bytes, of the device worklist for this problem.  HOST
@@ -114,7 +116,7 @@ size_t pva_worklist_bytes(int32_t num_docs, const pva_mask_desc* mask,
 /* Build the worklist on the device ("03 · 长文负载均衡" §3.2, §2.1):
  * derive the slices of the mask, enumerate every (query sub-tile, kv tile)
  * work item with at least one allowed pair, cost each work unit by its exact
- * pair count (+ c_tile per tile), sort by cost descending (stable) and assign
+ * pair count (+ c_tile per tile and per sub-tile), sort by cost descending (stable) and assign
  * LPT-style to params->num_ctas bins (lightest bin, lowest id on ties).
  *   cu_seqlens_dev  DEVICE int32 [num_docs + 1]
  *   worklist_dev    DEVICE buffer of worklist_bytes >= pva_worklist_bytes(), 256-B aligned
@@ -182,8 +184,8 @@ pva_status pva_worklist_error(const void* worklist_dev, int32_t* code_out, void*
 
 /* Summary counts of a built worklist (HOST out, synchronizes `stream`):
  * out[0] segments, [1] slices, [2] units, [3] runs, [4] allowed pairs per head,
- * [5] kv tiles computed per sub-tile summed over units. */
-pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out6, void* stream);
+ * [5] kv tiles computed per head, [6] parallel steps the LPT took. */
+pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out7, void* stream);
 
 const char* pva_status_string(pva_status status);
 int32_t pva_version(void);

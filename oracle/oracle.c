@@ -406,7 +406,10 @@ void or_merge(const double *oa, const double *la, const double *ob, const double
 /*    Enumeration order: segment, kv head, head pair, q tile; then the odd  */
 /*    head's tile pairs.                                                     */
 /*  - unit cost = exact allowed pairs of both sub-tiles + c_tile * (sub-tiles */
-/*    * kv tiles computed); c_tile = 0 is pure pair counting.                */
+/*    * kv tiles computed + sub-tiles); c_tile = 0 is pure pair counting.    */
+/*    The last term is a fixed cost per query sub-tile (its Q load and its   */
+/*    output rows), the analogue of the per-sample constant c*n of the      */
+/*    fitted DP load model ([P2] §4.2).                                      */
 /*  - LPT ties: sort is stable on the enumeration index; the lightest bin   */
 /*    with the lowest id wins a tie.  A bin's list is in assignment order.   */
 /* ------------------------------------------------------------------------ */
@@ -755,7 +758,7 @@ int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t ti
                     u.tiles += (int64_t)(hi - lo) * nsub;
                     ++ri;
                 }
-                u.cost = u.pairs + c_tile * u.tiles;
+                u.cost = u.pairs + c_tile * (u.tiles + nsub);
                 U[ui++] = u;
             }
         }

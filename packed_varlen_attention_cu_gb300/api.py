@@ -139,9 +139,9 @@ def worklist_error(worklist: torch.Tensor, stream=None) -> int:
 
 
 def worklist_counts(worklist: torch.Tensor, stream=None) -> dict:
-    out = (ctypes.c_int64 * 6)()
+    out = (ctypes.c_int64 * 7)()
     st = lib().pva_worklist_counts(_ptr(worklist), out, _stream(stream))
-    names = ("segs", "slices", "units", "runs", "pairs_per_head", "tiles_per_head")
+    names = ("segs", "slices", "units", "runs", "pairs_per_head", "tiles_per_head", "lpt_steps")
     res = dict(zip(names, (int(x) for x in out)))
     res["status"] = int(st)
     return res

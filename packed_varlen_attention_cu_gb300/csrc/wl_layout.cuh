@@ -62,7 +62,8 @@ struct WlHeader {
     unsigned long long pair_sum;   // sum over units of allowed pairs (all sub-tiles)
     unsigned long long tile_sum;   // sum over units of sub-tiles x kv tiles
     WlOffsets off;
-    int32_t pad_[8];
+    int32_t lpt_steps;  // batches + runs taken by the LPT (diagnostic)
+    int32_t pad_[7];
 };
 static_assert(sizeof(WlHeader) <= 256, "header fits in 256 bytes");
 

@@ -314,13 +314,14 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
     }
 }
 
-// kv-tile span [lo_t, hi_t) and allowed-pair count of q tile t against slice s.
-__device__ void tile_span(const WlSeg& g, const WlSlice& s, int32_t t, int32_t tile_m,
-                          int32_t tile_n, int32_t& lo_t, int32_t& hi_t, long long& pairs) {
+// kv-tile span [lo_t, hi_t) and allowed-pair count of q tile t against slice
+// s, by the whole warp: lane l takes rows r0 + l, r0 + l + 32, ...
+__device__ void tile_span_warp(const WlSeg& g, const WlSlice& s, int32_t t, int32_t tile_m,
+                               int32_t tile_n, int32_t& lo_t, int32_t& hi_t, long long& pairs) {
     long long mn = 0x7fffffffffffffffLL, mx = -1, cnt = 0;
     const int32_t r0 = t * tile_m;
     const int32_t r1 = min(r0 + tile_m, g.q_len);
-    for (int32_t r = r0; r < r1; ++r) {
+    for (int32_t r = r0 + (int32_t)(threadIdx.x & 31); r < r1; r += 32) {
         long long lo, hi;
         if (s.type == PVA_SLICE_FULL) {
             lo = 0;
@@ -337,6 +338,14 @@ __device__ void tile_span(const WlSeg& g, const WlSlice& s, int32_t t, int32_t t
         mn = lo < mn ? lo : mn;
         mx = hi > mx ? hi : mx;
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        const long long a = __shfl_xor_sync(0xffffffffu, mn, o);
+        const long long b = __shfl_xor_sync(0xffffffffu, mx, o);
+        mn = a < mn ? a : mn;
+        mx = b > mx ? b : mx;
+    }
     if (cnt == 0) {
         lo_t = hi_t = 0;
     } else {
@@ -352,104 +361,108 @@ struct UnitArgs {
     long long c_tile;
 };
 
-__device__ __forceinline__ void unit_body(const UnitArgs& a, WlHeader* h, int32_t u,
-                                          unsigned long long& pairs_out,
-                                          unsigned long long& tiles_out);
+constexpr int kUnitWarps = 8;  // units per block of the units kernel
 
-// One thread per unit.  Enumeration inside a segment: kv head, then head
+// One warp per unit (every lane computes the same unit; the row loops are
+// split across lanes).  Enumeration inside a segment: kv head, then head
 // pairs (2p, 2p+1) x q tiles, then the odd last head's q-tile pairs.
-__global__ void __launch_bounds__(128) wl_units_kernel(UnitArgs a) {
+__global__ void __launch_bounds__(kUnitWarps * 32) wl_units_kernel(UnitArgs a) {
     WlHeader* h = reinterpret_cast<WlHeader*>(a.base);
     if (h->error) return;
     const int32_t n = h->nunits;
-    const int32_t u = blockIdx.x * blockDim.x + threadIdx.x;
-    if ((int64_t)blockIdx.x * blockDim.x >= n) return;  // whole warps stay for the reduction
+    if ((int64_t)blockIdx.x * kUnitWarps >= n) return;
+    __shared__ unsigned long long bsum[kUnitWarps][2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t u = blockIdx.x * kUnitWarps + warp;
     unsigned long long pairs_out = 0, tiles_out = 0;
-    if (u < n) unit_body(a, h, u, pairs_out, tiles_out);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        pairs_out += __shfl_down_sync(0xffffffffu, pairs_out, o);
-        tiles_out += __shfl_down_sync(0xffffffffu, tiles_out, o);
-    }
-    if ((threadIdx.x & 31) == 0) {
-        atomicAdd(&h->pair_sum, pairs_out);
-        atomicAdd(&h->tile_sum, tiles_out);
-    }
-}
-
-__device__ __forceinline__ void unit_body(const UnitArgs& a, WlHeader* h, int32_t u,
-                                          unsigned long long& pairs_out,
-                                          unsigned long long& tiles_out) {
-    const WlSlice* slices = reinterpret_cast<const WlSlice*>(a.base + h->off.slices);
-    const WlSeg* segs = reinterpret_cast<const WlSeg*>(a.base + h->off.segs);
-    WlUnit* units = reinterpret_cast<WlUnit*>(a.base + h->off.units_enum);
-    unsigned long long* keys = reinterpret_cast<unsigned long long*>(a.base + h->off.keys);
-    WlRun* runs = reinterpret_cast<WlRun*>(a.base + h->off.runs);
-    // segment: last g with unit_base <= u (segments with zero units share a base)
-    int32_t lo = 0, hi = h->nsegs - 1;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (segs[mid].unit_base <= u) lo = mid;
-        else hi = mid - 1;
-    }
-    const int32_t gi = lo;
-    const WlSeg g = segs[gi];
-    const int32_t G = a.hq / a.hkv, nt = g.ntiles;
-    const int32_t per_kvh = (G / 2) * nt + (G % 2) * ((nt + 1) / 2);
-    const int32_t e = u - g.unit_base;
-    WlUnit w;
-    w.uid = u;
-    w.seg = gi;
-    w.kvh = e / per_kvh;
-    const int32_t e2 = e % per_kvh;
-    if (e2 < (G / 2) * nt) {
-        const int32_t p = e2 / nt, t = e2 % nt;
-        w.t0 = w.t1 = t;
-        w.h0 = w.kvh * G + 2 * p;
-        w.h1 = w.h0 + 1;
-    } else {
-        const int32_t uu = e2 - (G / 2) * nt;
-        w.t0 = 2 * uu;
-        w.t1 = (2 * uu + 1 < nt) ? 2 * uu + 1 : -1;
-        w.h0 = w.kvh * G + G - 1;
-        w.h1 = w.t1 >= 0 ? w.h0 : -1;
-    }
-    const int nsub = w.h1 >= 0 ? 2 : 1;
-    w.run_begin = g.run_base + e * g.slice_count;
-    w.run_count = g.slice_count;
-    w.cta = -1;
-    w.pad = 0;
-    long long pairs = 0, tiles = 0;
-    int32_t ntiles = 0;
-    for (int32_t si = 0; si < g.slice_count; ++si) {
-        const WlSlice s = slices[g.slice_begin + si];
-        int32_t rlo = 0, rhi = 0;
-        bool have = false;
-        const int32_t ts[2] = {w.t0, w.t1};
-        for (int k = 0; k < nsub; ++k) {
-            int32_t a0, b0;
-            long long pr;
-            tile_span(g, s, ts[k], a.tile_m, a.tile_n, a0, b0, pr);
-            pairs += pr;
-            if (b0 > a0) {
-                if (!have || a0 < rlo) rlo = a0;
-                if (!have || b0 > rhi) rhi = b0;
-                have = true;
-            }
+    if (u < n) {
+        const WlSlice* slices = reinterpret_cast<const WlSlice*>(a.base + h->off.slices);
+        const WlSeg* segs = reinterpret_cast<const WlSeg*>(a.base + h->off.segs);
+        WlUnit* units = reinterpret_cast<WlUnit*>(a.base + h->off.units_enum);
+        unsigned long long* keys = reinterpret_cast<unsigned long long*>(a.base + h->off.keys);
+        WlRun* runs = reinterpret_cast<WlRun*>(a.base + h->off.runs);
+        // segment: last g with unit_base <= u
+        int32_t lo = 0, hi = h->nsegs - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (segs[mid].unit_base <= u) lo = mid;
+            else hi = mid - 1;
         }
-        runs[w.run_begin + si] = WlRun{g.slice_begin + si, rlo, rhi, 0};
-        tiles += (long long)(rhi - rlo) * nsub;
-        ntiles += rhi - rlo;
+        const int32_t gi = lo;
+        const WlSeg g = segs[gi];
+        const int32_t G = a.hq / a.hkv, nt = g.ntiles;
+        const int32_t per_kvh = (G / 2) * nt + (G % 2) * ((nt + 1) / 2);
+        const int32_t e = u - g.unit_base;
+        WlUnit w;
+        w.uid = u;
+        w.seg = gi;
+        w.kvh = e / per_kvh;
+        const int32_t e2 = e % per_kvh;
+        if (e2 < (G / 2) * nt) {
+            const int32_t p = e2 / nt, t = e2 % nt;
+            w.t0 = w.t1 = t;
+            w.h0 = w.kvh * G + 2 * p;
+            w.h1 = w.h0 + 1;
+        } else {
+            const int32_t uu = e2 - (G / 2) * nt;
+            w.t0 = 2 * uu;
+            w.t1 = (2 * uu + 1 < nt) ? 2 * uu + 1 : -1;
+            w.h0 = w.kvh * G + G - 1;
+            w.h1 = w.t1 >= 0 ? w.h0 : -1;
+        }
+        const int nsub = w.h1 >= 0 ? 2 : 1;
+        w.run_begin = g.run_base + e * g.slice_count;
+        w.run_count = g.slice_count;
+        w.cta = -1;
+        w.pad = 0;
+        long long pairs = 0, tiles = 0;
+        int32_t ntiles = 0;
+        for (int32_t si = 0; si < g.slice_count; ++si) {
+            const WlSlice sl = slices[g.slice_begin + si];
+            int32_t rlo = 0, rhi = 0;
+            bool have = false;
+            const int32_t ts[2] = {w.t0, w.t1};
+            for (int k = 0; k < nsub; ++k) {
+                int32_t a0, b0;
+                long long pr;
+                tile_span_warp(g, sl, ts[k], a.tile_m, a.tile_n, a0, b0, pr);
+                pairs += pr;
+                if (b0 > a0) {
+                    if (!have || a0 < rlo) rlo = a0;
+                    if (!have || b0 > rhi) rhi = b0;
+                    have = true;
+                }
+            }
+            if (lane == 0) runs[w.run_begin + si] = WlRun{g.slice_begin + si, rlo, rhi, 0};
+            tiles += (long long)(rhi - rlo) * nsub;
+            ntiles += rhi - rlo;
+        }
+        w.ntiles = ntiles;
+        w.pairs = pairs;
+        w.cost = pairs + a.c_tile * (tiles + nsub);
+        if (lane == 0) {
+            units[u] = w;
+            if (w.cost < 0 || w.cost >= (1LL << kCostBits)) set_error(h, kErrCostRange);
+            const unsigned long long inv = ((1ULL << kCostBits) - 1) - (unsigned long long)w.cost;
+            keys[u] = (inv << kUidBits) | (unsigned long long)u;
+        }
+        pairs_out = (unsigned long long)pairs;
+        tiles_out = (unsigned long long)tiles;
     }
-    w.ntiles = ntiles;
-    w.pairs = pairs;
-    w.cost = pairs + a.c_tile * tiles;
-    units[u] = w;
-    if (w.cost < 0 || w.cost >= (1LL << kCostBits)) set_error(h, kErrCostRange);
-    const unsigned long long inv = ((1ULL << kCostBits) - 1) - (unsigned long long)w.cost;
-    keys[u] = (inv << kUidBits) | (unsigned long long)u;
-    pairs_out = (unsigned long long)pairs;
-    tiles_out = (unsigned long long)tiles;
+    if (lane == 0) {
+        bsum[warp][0] = pairs_out;
+        bsum[warp][1] = tiles_out;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long p = 0, q = 0;
+        for (int i = 0; i < kUnitWarps; ++i) {
+            p += bsum[i][0];
+            q += bsum[i][1];
+        }
+        atomicAdd(&h->pair_sum, p);
+        atomicAdd(&h->tile_sum, q);
+    }
 }
 
 // Stable sort by (cost desc, uid asc).  Every key is unique, so a unit's
@@ -535,16 +548,40 @@ __global__ void __launch_bounds__(kSortThreads) wl_merge_rank_kernel(uint8_t* ba
 // With tasks t, t+1, ... in LPT order, sequential LPT sends task t+j to the
 // j-th lightest bin S_j as long as S_j is lighter than every bin that
 // received a task earlier in the batch, i.e. S_j < min_{i<j} (S_i + c_{t+i});
-// the first j where this fails ends the batch.  Each batch is applied at once
-// and the bins are re-sorted by rank counting.
-constexpr int kLptThreads = 1024;
-constexpr int kLptStage = 2048;
+// the first j where this fails ends the batch.  If it fails at j = 1, task
+// t+1 goes to S_0 again: a run of consecutive tasks then goes to S_0 while
+// S_0 plus their cost prefix stays below S_1.  After each step the bins are
+// re-sorted by rank counting, split F ways across the block.
+constexpr int kLptStage = 1024;
 
-__global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
+__device__ __forceinline__ void lpt_resort(unsigned long long* S, const unsigned long long* Snew,
+                                           int32_t* rc, int32_t B, int32_t Bp, int32_t F) {
+    const int tid = threadIdx.x;
+    const int32_t j = tid % Bp, q = tid / Bp;
+    const int32_t chunk = (B + F - 1) / F;
+    if (j < B && q < F) {
+        const unsigned long long me = Snew[j];
+        const int32_t i1 = min(B, (q + 1) * chunk);
+        int32_t r = 0;
+#pragma unroll 4
+        for (int32_t i = q * chunk; i < i1; ++i) r += Snew[i] < me;
+        rc[q * Bp + j] = r;
+    }
+    __syncthreads();
+    if (tid < B) {
+        int32_t r = 0;
+        for (int32_t qq = 0; qq < F; ++qq) r += rc[qq * Bp + tid];
+        S[r] = Snew[tid];
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t F) {
     WlHeader* h = reinterpret_cast<WlHeader*>(base);
     if (h->error) return;
     const int32_t n = h->nunits;
     const int32_t B = h->num_ctas;
+    const int32_t Bp = (B + 31) & ~31;  // bins rounded up to whole warps
     const WlUnit* units_enum = reinterpret_cast<const WlUnit*>(base + h->off.units_enum);
     const int32_t* order = reinterpret_cast<const int32_t*>(base + h->off.order);
     int32_t* assign = reinterpret_cast<int32_t*>(base + h->off.assign);
@@ -552,17 +589,20 @@ __global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
     WlUnit* units = reinterpret_cast<WlUnit*>(base + h->off.units);
     int32_t* cta_off = reinterpret_cast<int32_t*>(base + h->off.cta_off);
     __shared__ unsigned long long S[kMaxBins], Snew[kMaxBins];
-    __shared__ unsigned long long wmin[32];
     __shared__ int32_t cnt[kMaxBins];
+    __shared__ int32_t rc[kMaxBins];
     // the next kLptStage units in LPT order (cost, uid), refilled as t advances
     __shared__ long long scost[kLptStage];
     __shared__ int32_t suid[kLptStage];
-    __shared__ int32_t s_k;
-    __shared__ int32_t sm1[32][1];
+    __shared__ unsigned long long wmin[32];
+    __shared__ long long wsum[32];
+    __shared__ int32_t wint[32];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int nw = Bp >> 5;           // warps that hold bins
+    const bool main = tid < Bp;
     // bin keys hold load << 10: the total cost must stay below 2^53
     const unsigned long long total_cost =
-        h->pair_sum + (unsigned long long)h->c_tile * h->tile_sum;
+        h->pair_sum + (unsigned long long)h->c_tile * (h->tile_sum + 2ULL * (unsigned)n);
     if (total_cost >= (1ULL << 53)) {
         if (tid == 0) set_error(h, kErrCostRange);
         return;
@@ -572,52 +612,85 @@ __global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
         cnt[tid] = 0;
     }
     __syncthreads();
-    int32_t stage0 = -kLptStage;
-    for (int32_t t = 0; t < n;) {
-        if (t + B > stage0 + kLptStage) {  // a batch may run past the staged window
+    int32_t stage0 = -kLptStage, steps = 0;
+    for (int32_t t = 0; t < n; ++steps) {
+        if (t + Bp > stage0 + kLptStage) {  // a step may read past the staged window
             stage0 = t;
-            for (int32_t i = tid; i < kLptStage && t + i < n; i += kLptThreads) {
+            for (int32_t i = tid; i < kLptStage && t + i < n; i += blockDim.x) {
                 const int32_t uid = order[t + i];
                 suid[i] = uid;
                 scost[i] = units_enum[uid].cost;
             }
             __syncthreads();
         }
-        // candidate value of bin j after receiving task t+j
-        unsigned long long val = ~0ULL;
-        long long c = 0;
-        if (tid < B && t + tid < n) {
-            c = scost[t + tid - stage0];
-            val = S[tid] + ((unsigned long long)c << 10);
-        }
-        // exclusive prefix-min of val over j
+        const bool have = tid < B && t + tid < n;
+        const long long c = have ? scost[t + tid - stage0] : 0;
+        // candidate value of bin j after receiving task t+j; exclusive prefix-min
+        const unsigned long long val = have ? S[tid] + ((unsigned long long)c << 10) : ~0ULL;
         unsigned long long inc = val;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            unsigned long long x = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o && x < inc) inc = x;
-        }
-        if (lane == 31) wmin[w] = inc;
-        if (tid == 0) s_k = 0x7fffffff;
-        __syncthreads();
-        if (w == 0) {
-            unsigned long long x = wmin[lane];
+        if (main) {
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o && y < x) x = y;
+                const unsigned long long x = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o && x < inc) inc = x;
             }
-            wmin[lane] = x;
+            if (lane == 31) wmin[w] = inc;
         }
         __syncthreads();
-        unsigned long long ex = __shfl_up_sync(0xffffffffu, inc, 1);
-        if (lane == 0) ex = ~0ULL;
-        if (w > 0 && wmin[w - 1] < ex) ex = wmin[w - 1];
-        // task t+j goes to S_j iff it exists and S_j < prefix-min (always for j = 0)
-        const bool ok = tid < B && t + tid < n && (tid == 0 || S[tid] < ex);
-        if (!ok) atomicMin(&s_k, tid);
+        unsigned long long ex = ~0ULL;
+        if (main) {
+            ex = __shfl_up_sync(0xffffffffu, inc, 1);
+            if (lane == 0) ex = ~0ULL;
+            for (int i = 0; i < w; ++i) ex = wmin[i] < ex ? wmin[i] : ex;
+            // task t+j goes to S_j iff it exists and S_j < prefix-min (always for j = 0)
+            const bool ok = have && (tid == 0 || S[tid] < ex);
+            const unsigned fail = __ballot_sync(0xffffffffu, !ok);
+            if (lane == 0) wint[w] = fail ? w * 32 + __ffs(fail) - 1 : 0x7fffffff;
+        }
         __syncthreads();
-        const int32_t k = min(s_k, B);
+        int32_t k = B;
+        for (int i = 0; i < nw; ++i) k = min(k, wint[i]);
+        __syncthreads();  // wint is reused below
+        if (k == 1 && t + 1 < n) {
+            // run of consecutive tasks into S_0 (see above)
+            const int32_t j = tid;
+            const bool in = main && t + j < n && t + j - stage0 < kLptStage;
+            const long long cj = in ? scost[t + j - stage0] : 0;
+            long long incl = cj;
+            if (main) {
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long x = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += x;
+                }
+                if (lane == 31) wsum[w] = incl;
+            }
+            __syncthreads();
+            const unsigned long long s0 = S[0], s1 = B > 1 ? S[1] : ~0ULL;
+            long long excl = incl - cj;
+            if (main) {
+                for (int i = 0; i < w; ++i) excl += wsum[i];
+                const bool go = j >= 1 && in && s0 + ((unsigned long long)excl << 10) < s1;
+                const unsigned bal = __ballot_sync(0xffffffffu, go);
+                if (lane == 0) wint[w] = __popc(bal);
+            }
+            __syncthreads();
+            int32_t m = 1;
+            for (int i = 0; i < nw; ++i) m += wint[i];
+            const int32_t bin = (int32_t)(s0 & 1023ULL);
+            if (main && j < m) {
+                const int32_t uid = suid[t + j - stage0];
+                assign[uid] = bin;
+                local[uid] = cnt[bin] + j;
+            }
+            if (main && j == m - 1) Snew[0] = s0 + ((unsigned long long)(excl + cj) << 10);
+            if (tid > 0 && tid < B) Snew[tid] = S[tid];
+            __syncthreads();
+            if (tid == 0) cnt[bin] += m;
+            lpt_resort(S, Snew, rc, B, Bp, F);
+            t += m;
+            continue;
+        }
         if (tid < k) {
             const int32_t uid = suid[t + tid - stage0];
             const int32_t bin = (int32_t)(S[tid] & 1023ULL);
@@ -628,28 +701,35 @@ __global__ void __launch_bounds__(kLptThreads) wl_lpt_kernel(uint8_t* base) {
             Snew[tid] = S[tid];
         }
         __syncthreads();
-        if (tid < B) {
-            const unsigned long long me = Snew[tid];
-            int32_t r = 0;
-#pragma unroll 8
-            for (int32_t i = 0; i < B; ++i) r += Snew[i] < me;
-            S[r] = me;
-        }
+        lpt_resort(S, Snew, rc, B, Bp, F);
         t += k;
-        __syncthreads();
     }
-    // CSR offsets (exclusive scan of the bin counts; B <= 1024)
-    int32_t v[1] = {tid < B ? cnt[tid] : 0};
-    int32_t tot[1];
-    block_scan_excl<1>(v, tot, sm1);
-    if (tid < B) cta_off[tid] = v[0];
-    if (tid == 0) cta_off[B] = tot[0];
-    if (tid < B) cnt[tid] = v[0];
+    if (tid == 0) h->lpt_steps = steps;
+    // CSR offsets: exclusive scan of the bin counts (warp scans + warp totals)
+    int32_t inc = tid < B ? cnt[tid] : 0;
+    const int32_t mine = inc;
+    if (main) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t x = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += x;
+        }
+        if (lane == 31) wint[w] = inc;
+    }
     __syncthreads();
-    for (int32_t u = tid; u < n; u += kLptThreads) {
+    if (main) {
+        int32_t base_w = 0;
+        for (int i = 0; i < w; ++i) base_w += wint[i];
+        const int32_t excl = base_w + inc - mine;
+        if (tid < B) cta_off[tid] = excl;
+        if (tid == B - 1) cta_off[B] = excl + mine;
+        if (tid < B) rc[tid] = excl;
+    }
+    __syncthreads();
+    for (int32_t u = tid; u < n; u += blockDim.x) {
         WlUnit x = units_enum[u];
         x.cta = assign[u];
-        units[cnt[x.cta] + local[u]] = x;
+        units[rc[x.cta] + local[u]] = x;
     }
 }
 
@@ -828,12 +908,14 @@ extern "C" pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t 
     wl_plan_kernel<<<1, kPlanThreads, 0, st>>>(pa);
     UnitArgs ua{base, params->tile_m, params->tile_n, params->num_q_heads, params->num_kv_heads,
                 (long long)params->c_tile};
-    const int ub = (h.cap_units + 127) / 128;
-    wl_units_kernel<<<ub, 128, 0, st>>>(ua);
+    const int ub = (h.cap_units + kUnitWarps - 1) / kUnitWarps;
+    wl_units_kernel<<<ub, kUnitWarps * 32, 0, st>>>(ua);
     const int sb = (h.cap_units + kSortChunk - 1) / kSortChunk;
     wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(base);
     wl_merge_rank_kernel<<<sb, kSortThreads, 0, st>>>(base);
-    wl_lpt_kernel<<<1, kLptThreads, 0, st>>>(base);
+    const int bp = ((nc + 31) / 32) * 32;
+    const int lpt_f = bp >= 1024 ? 1 : (1024 / bp < 4 ? 1024 / bp : 4);
+    wl_lpt_kernel<<<1, bp * lpt_f, 0, st>>>(base, lpt_f);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
 
@@ -851,8 +933,9 @@ extern "C" pva_status pva_worklist_error(const void* worklist_dev, int32_t* code
     return PVA_OK;
 }
 
-extern "C" pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out6, void* stream) {
-    if (!worklist_dev || !out6) return PVA_ERR_INVALID_ARG;
+extern "C" pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out7, void* stream) {
+    if (!worklist_dev || !out7) return PVA_ERR_INVALID_ARG;
+    int64_t* out6 = out7;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     WlHeader h;
     if (cudaMemcpyAsync(&h, worklist_dev, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -865,5 +948,6 @@ extern "C" pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out
     out6[3] = h.nruns;
     out6[4] = h.hq > 0 ? (int64_t)(h.pair_sum / (unsigned long long)h.hq) : 0;
     out6[5] = h.hq > 0 ? (int64_t)(h.tile_sum / (unsigned long long)h.hq) : 0;
+    out6[6] = h.lpt_steps;
     return h.error ? (h.error >= kErrTimeoutBase ? PVA_ERR_TIMEOUT : PVA_ERR_DEVICE) : PVA_OK;
 }

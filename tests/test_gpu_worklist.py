@@ -68,8 +68,8 @@ def test_worklist_pair_count_matches_closed_form():
     assert counts["pairs_per_head"] == sum(l * (l + 1) // 2 for l in w.lengths) == 488185982
 
 
-@pytest.mark.parametrize("cp", [2, 8])
-def test_worklist_zigzag_pairs_bit_exact(oracle_mod, cp):
+@pytest.mark.parametrize("cp,c_tile", [(2, 7), (8, 7), (8, 0)])
+def test_worklist_zigzag_pairs_bit_exact(oracle_mod, cp, c_tile):
     w = W.tiny_pack(seed=3)
     cu = w.cu_seqlens
     for r in range(cp):
@@ -77,9 +77,9 @@ def test_worklist_zigzag_pairs_bit_exact(oracle_mod, cp):
         for s in range(cp):
             tk = api.zigzag_shard_len(cu, cp, s)
             mask = api.make_mask(W.MASK_ZIGZAG_PAIR, tq, tk, cp=cp, q_rank=r, k_rank=s)
-            g, _ = _gpu_worklist(cu, mask, 4, 2, 13, 7)
+            g, _ = _gpu_worklist(cu, mask, 4, 2, 13, c_tile)
             o = oracle_mod.worklist(cu, oracle_mask(W.MASK_ZIGZAG_PAIR, cp=cp, q_rank=r, k_rank=s),
-                                    128, 128, 4, 2, 13, 7)
+                                    128, 128, 4, 2, 13, c_tile)
             _assert_same(g, o)
 
 
@@ -131,3 +131,18 @@ def test_bad_cu_seqlens_sets_error_not_fault():
     api.attn_fwd(q, q, q, cu, mask, params, wl, out, lse)
     torch.cuda.synchronize()
     assert torch.all(out == 7.0) and torch.all(lse == 7.0)
+
+
+def test_worklist_single_cta_and_zero_costs(oracle_mod):
+    # one bin: every unit lands on CTA 0 in cost order; zero-cost units (c_tile = 0,
+    # query chunks with no key in the shard) exercise the run step of the LPT
+    w = W.zigzag_pack()
+    cu = w.cu_seqlens
+    tq = api.zigzag_shard_len(cu, 8, 0)
+    tk = api.zigzag_shard_len(cu, 8, 7)
+    mask = api.make_mask(W.MASK_ZIGZAG_PAIR, tq, tk, cp=8, q_rank=0, k_rank=7)
+    for nc in (1, 152):
+        g, _ = _gpu_worklist(cu, mask, 32, 8, nc, 0)
+        o = oracle_mod.worklist(cu, oracle_mask(W.MASK_ZIGZAG_PAIR, cp=8, q_rank=0, k_rank=7),
+                                128, 128, 32, 8, nc, 0)
+        _assert_same(g, o)

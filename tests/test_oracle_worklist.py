@@ -78,11 +78,11 @@ def test_worklist_covers_allowed_pairs_once(oracle_mod, lengths, kind, kw, hq, h
     assert empty == 0
     np.testing.assert_array_equal(per_unit, wl["unit_pairs"])
     assert wl["pairs_per_head"] == int(A.sum())
-    # cost = pairs + c_tile * (sub-tiles x kv tiles computed)
+    # cost = pairs + c_tile * (sub-tiles x kv tiles computed + sub-tiles)
     for u, c, p in zip(wl["units"], wl["unit_cost"], wl["unit_pairs"]):
         nsub = 2 if u[5] >= 0 else 1
         tiles = sum(int(wl["runs"][r][2] - wl["runs"][r][1]) for r in range(u[7], u[7] + u[8]))
-        assert c == p + 3 * nsub * tiles
+        assert c == p + 3 * (nsub * tiles + nsub)
 
 
 @pytest.mark.parametrize("cp", [2, 3])
