@@ -187,6 +187,31 @@ pva_status pva_worklist_error(const void* worklist_dev, int32_t* code_out, void*
  * [5] kv tiles computed per head, [6] parallel steps the LPT took. */
 pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out7, void* stream);
 
+/* Worklist build + attention forward for callers that cannot allocate device
+ * memory (a plugin in a runtime that owns a fixed memory pool, a serving
+ * process with a memory budget fixed up front, a C host without a device
+ * allocator).  The pages have no counterpart: this is a packaging variant of
+ * pva_build_worklist + pva_attn_fwd.  The caller passes inputs and outputs
+ * only (same meaning as there; cta_busy_ns is not recorded); the worklist
+ * lives in a static device array of pva_noalloc_scratch_bytes() (16 MiB) that
+ * every GPU loading the library holds until the process exits.
+ *  - Problems whose worklist (pva_worklist_bytes) exceeds that size are
+ *    rejected with PVA_ERR_BUFFER_TOO_SMALL before any device work.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls on a device share the array, which keeps the last call's
+ *    contents (the build rewrites everything it reads); calls that overlap on
+ *    the GPU race on it.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+pva_status pva_attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                                const int32_t* cu_seqlens_dev, int32_t num_docs,
+                                const pva_mask_desc* mask, const pva_worklist_params* params,
+                                int32_t head_dim, void* out, int32_t out_is_fp32, float* lse,
+                                float softmax_scale, void* stream);
+
+/* Size in bytes of the static worklist array used by pva_attn_fwd_noalloc. */
+size_t pva_noalloc_scratch_bytes(void);
+
 const char* pva_status_string(pva_status status);
 int32_t pva_version(void);
 

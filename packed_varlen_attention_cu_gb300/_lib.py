@@ -19,7 +19,8 @@ STATUS_NAMES = {0: "PVA_OK", 1: "PVA_ERR_INVALID_ARG", 2: "PVA_ERR_BUFFER_TOO_SM
 # Every symbol declared by include/pva.h.
 EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_zigzag_shard_len",
            "pva_zigzag_shard", "pva_gather_rows", "pva_merge_partials", "pva_worklist_error",
-           "pva_worklist_counts", "pva_status_string", "pva_version")
+           "pva_worklist_counts", "pva_attn_fwd_noalloc", "pva_noalloc_scratch_bytes",
+           "pva_status_string", "pva_version")
 
 
 class Slice(ctypes.Structure):
@@ -80,6 +81,11 @@ def lib() -> ctypes.CDLL:
         L.pva_worklist_error.argtypes = [P, ctypes.POINTER(i32), P]
         L.pva_worklist_counts.restype = ctypes.c_int
         L.pva_worklist_counts.argtypes = [P, ctypes.POINTER(i64), P]
+        L.pva_attn_fwd_noalloc.restype = ctypes.c_int
+        L.pva_attn_fwd_noalloc.argtypes = [P, P, P, P, i32, MP, WP, i32, P, i32, P,
+                                           ctypes.c_float, P]
+        L.pva_noalloc_scratch_bytes.restype = sz
+        L.pva_noalloc_scratch_bytes.argtypes = []
         L.pva_status_string.restype = ctypes.c_char_p
         L.pva_status_string.argtypes = [ctypes.c_int]
         L.pva_version.restype = i32
