@@ -432,6 +432,50 @@ def run_zigzag(args, ctx, world):
                     "fp32 partial attention, in-place merges; outputs stay rank-local"}
 
 
+def run_libra_ratio(args, ctx):
+    """Libra's example ("03 · 长文负载均衡" §1.1): the same token count as one
+    40960-token document (pack A) or ten 4096-token documents (pack B); the
+    attention work ratio is 10 in sum l^2.  Each pack is timed on its own."""
+    import torch
+
+    from packed_varlen_attention_cu_gb300 import api
+    w, q, k, v = ctx[:4]
+    dev = q.device
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, lengths, rows in (("A", [40960], slice(0, 40960)),
+                                ("B", [4096] * 10, slice(40960, 81920))):
+        cu_np = W.cu_seqlens_of(lengths)
+        cu = torch.from_numpy(cu_np).to(dev)
+        qa, ka, va = q[rows].contiguous(), k[rows].contiguous(), v[rows].contiguous()
+        T = qa.shape[0]
+        mask = api.make_mask(W.MASK_CAUSAL, T, T)
+        params = api.make_params(w.num_q_heads, w.num_kv_heads, num_ctas=0, c_tile=args.c_tile)
+        wl = api.alloc_worklist(len(lengths), mask, params, dev)
+        out = torch.empty_like(qa)
+        lse = torch.empty((qa.shape[1], T), dtype=torch.float32, device=dev)
+        api.build_worklist(cu, mask, params, wl)
+        for _ in range(3):
+            api.attn_fwd(qa, ka, va, cu, mask, params, wl, out, lse)
+        reps = 10
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record(stream)
+        for _ in range(reps):
+            api.attn_fwd(qa, ka, va, cu, mask, params, wl, out, lse)
+        e.record(stream)
+        torch.cuda.synchronize()
+        pairs = api.worklist_counts(wl)["pairs_per_head"]
+        t = s.elapsed_time(e) / reps
+        res[name] = {"ms": round(t, 4), "pairs_per_head": pairs,
+                     "tflops": round(4.0 * w.head_dim * w.num_q_heads * pairs / t / 1e9, 2)}
+    res["time_ratio_A_over_B"] = round(res["A"]["ms"] / res["B"]["ms"], 4)
+    res["sum_sq_ratio"] = 10.0
+    res["pairs_ratio"] = round(40961 / 4097, 5)
+    res["tile_ratio_b128"] = round(51360 / 5280, 5)
+    return res
+
+
 # ----------------------------------------------------------------- CPU oracle
 def oracle_sample(w, q_bits, k_bits, v_bits, seconds: float, seed: int = 7):
     """Time the fp64 oracle on a bounded random sample of (row, head) jobs
@@ -526,6 +570,8 @@ def main(argv=None):
         res["e2e"] = run_e2e(args, ctx, world)
     if not args.no_zigzag and ctx[0].cp:
         res["zigzag_cp"] = run_zigzag(args, ctx, world)
+    if args.workload == "libra":
+        res["libra_ratio"] = run_libra_ratio(args, ctx)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle  # noqa: F401  (CPU baseline leg only)
         from oracle import bf16_bits
