@@ -39,6 +39,9 @@ namespace pva {
 namespace {
 
 constexpr int kThreads = 384;
+// register split: the producer/MMA warpgroup hands registers to the two
+// softmax warpgroups (128 * kRegsCtrl + 256 * kRegsSoftmax <= 384 * 168)
+constexpr uint32_t kRegsCtrl = 104, kRegsSoftmax = 200;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 constexpr float kRescaleThreshold = 8.0f;     // log2 domain
@@ -183,7 +186,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sh.tmem_base;
     volatile int32_t* abort_flag = &sh.abort_flag;
 
+    // every role ends here: all 384 threads meet, warp 1 frees tensor memory
+    auto finish = [&]() {
+        tc_fence_before();
+        named_barrier(1, kThreads);
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, 512);
+        }
+        if (p.busy && tid == 0) {
+            p.busy[2 * blockIdx.x] = t_start;
+            p.busy[2 * blockIdx.x + 1] = globaltimer_ns();
+        }
+    };
     if (warp < 4) {
+      regs_dealloc<kRegsCtrl>();
       if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
@@ -343,7 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
+      finish();
+      return;
     } else {
+        regs_alloc<kRegsSoftmax>();
         // ------------------------------------------------------- softmax / epilogue
         const int i = (warp - 4) >> 2;           // sub-tile of this warpgroup
         const int r = (warp & 3) * 32 + lane;    // query row = tensor-memory lane
@@ -397,15 +417,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (col < c_lo || col >= c_hi) sr[c][e] = __float_as_uint(-INFINITY);
                             }
                     }
-                    // row max: 4 independent partial maxima, then a tree
+                    // row max: 4 independent chains of 3-input max, then a tree
                     float pm[4];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        pm[c] = __uint_as_float(sr[c][0]);
+                        float m3 = fmax3(__uint_as_float(sr[c][0]), __uint_as_float(sr[c][1]),
+                                         __uint_as_float(sr[c][2]));
 #pragma unroll
-                        for (int e = 1; e < 32; ++e) pm[c] = fmaxf(pm[c], __uint_as_float(sr[c][e]));
+                        for (int e = 3; e < 31; e += 2)
+                            m3 = fmax3(m3, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                        pm[c] = fmaxf(m3, __uint_as_float(sr[c][31]));
                     }
-                    const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+                    const float mx = fmax3(pm[0], pm[1], fmaxf(pm[2], pm[3]));
                     const float m_tile = mx * p.scale_log2;  // -inf stays -inf
                     float alpha = 1.f;
                     bool rescale = false;
@@ -422,19 +445,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // P = 2^(s*scale*log2e - m), packed to bf16 pairs in place
                     // (pair e/2 lands in a register already consumed)
                     const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-                    float part[4] = {0.f, 0.f, 0.f, 0.f};
+                    // packed fp32x2 FMA / add: two elements per instruction
+                    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+                    const float2 nm2 = make_float2(neg_m, neg_m);
+                    float2 part[4];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
+                        part[c] = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), p.scale_log2, neg_m));
-                            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), p.scale_log2, neg_m));
-                            part[c] += p0 + p1;
+                            const float2 x = __ffma2_rn(
+                                make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
+                                sl2, nm2);
+                            const float p0 = ex2_approx(x.x);
+                            const float p1 = ex2_approx(x.y);
+                            part[c] = __fadd2_rn(part[c], make_float2(p0, p1));
                             sr[c][e >> 1] = pack_bf16x2(p0, p1);
                         }
                         tmem_st16(tS + c * 16, sr[c]);
                     }
-                    l_sum += (part[0] + part[1]) + (part[2] + part[3]);
+                    const float2 ps = __fadd2_rn(__fadd2_rn(part[0], part[1]), __fadd2_rn(part[2], part[3]));
+                    l_sum += ps.x + ps.y;
                     // rare: the running max moved, rescale this row of O
                     if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -500,18 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.lse[(int64_t)st.head * p.q_tokens + st.q_row + r] =
                     l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
         }
+        finish();
     }
 
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
-    }
-    if (p.busy && tid == 0) {
-        p.busy[2 * blockIdx.x] = t_start;
-        p.busy[2 * blockIdx.x + 1] = globaltimer_ns();
-    }
 }
 
 }  // namespace
@@ -558,6 +580,13 @@ template <int D>
 pva_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                   const AttnParams& ap, cudaStream_t st) {
     auto kern = attn_fwd_kernel<D>;
+    // setmaxnreg.inc draws from the registers the block was launched with: the
+    // split must fit in (threads x registers per thread) or the increase would
+    // never be granted.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return PVA_ERR_CUDA;
+    if ((int64_t)fa.numRegs * kThreads < 128 * (int64_t)kRegsCtrl + 256 * (int64_t)kRegsSoftmax)
+        return PVA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem) !=
         cudaSuccess)
         return PVA_ERR_CUDA;
