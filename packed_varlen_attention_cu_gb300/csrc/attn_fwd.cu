@@ -260,8 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t kv_it = 0, q_it[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
             bool live = true;
-            const uint32_t sQa[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
-            const uint32_t sKVa = smem_u32(sKV);
+            // Descriptors are built once; an MMA only adds a byte offset >> 4 to the
+            // 14-bit start-address field (shared addresses stay below 256 KB).
+            const uint64_t dQ[2] = {sdesc_sw128(smem_u32(sQ[0]), 16, 1024),
+                                    sdesc_sw128(smem_u32(sQ[1]), 16, 1024)};
+            const uint64_t dK0 = sdesc_sw128(smem_u32(sKV), 16, 1024);     // K-major
+            const uint64_t dV0 = sdesc_sw128(smem_u32(sKV), 16384, 1024);  // MN-major
             for (int32_t ui = ub; ui < ue && live; ++ui) {
                 const WlUnit wu = units[ui];
                 const Unit u = decode_unit(wu, segs);
@@ -280,15 +284,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      err_word, kErrTimeoutBase + 4, kWaitNs);
                     if (!live) break;
                     tc_fence_after();
-                    const uint32_t kb = sKVa + st * C::kTileBytes;
+                    const uint64_t dK = dK0 + ((st * C::kTileBytes) >> 4);
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         if (i >= u.nsub) break;
 #pragma unroll
                         for (int k = 0; k < D / 16; ++k) {
-                            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                            mma_ss(tmem + i * 128, sdesc_sw128(sQa[i] + off, 16, 1024),
-                                   sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, k > 0);
+                            const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;  // bytes >> 4
+                            mma_ss(tmem + i * 128, dQ[i] + off16, dK + off16, C::kIdescQK, k > 0);
                         }
                         mma_commit(&sh.s_full[i]);
                         if (n == 1) mma_commit(&sh.q_empty[i]);
@@ -316,12 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!live) break;
                         }
                         tc_fence_after();
-                        const uint32_t vb = sKVa + stv * C::kTileBytes;
+                        const uint64_t dV = dV0 + ((stv * C::kTileBytes) >> 4);
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            mma_ts(tmem + 256 + i * 128, tmem + i * 128 + k * 8,
-                                   sdesc_sw128(vb + k * 2048, 16384, 1024), C::kIdescPV,
-                                   (j > 0 || k > 0) ? 1u : 0u);
+                            mma_ts(tmem + 256 + i * 128, tmem + i * 128 + k * 8, dV + k * 128,
+                                   C::kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
                         if (has_next) {
                             if (i == 0) {
                                 live = mbar_wait(&sh.kv_full[stk], ((kv_it + 1) / C::kStages) & 1,
@@ -329,12 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (!live) break;
                                 tc_fence_after();
                             }
-                            const uint32_t kb = sKVa + stk * C::kTileBytes;
+                            const uint64_t dK = dK0 + ((stk * C::kTileBytes) >> 4);
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
-                                const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                                mma_ss(tmem + i * 128, sdesc_sw128(sQa[i] + off, 16, 1024),
-                                       sdesc_sw128(kb + off, 16, 1024), C::kIdescQK, k > 0);
+                                const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                                mma_ss(tmem + i * 128, dQ[i] + off16, dK + off16, C::kIdescQK,
+                                       k > 0);
                             }
                             mma_commit(&sh.s_full[i]);
                             if (j + 2 == n) mma_commit(&sh.q_empty[i]);
