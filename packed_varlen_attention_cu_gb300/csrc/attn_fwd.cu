@@ -94,7 +94,7 @@ __device__ __forceinline__ Unit decode_unit(const WlUnit& u, const WlSeg* segs) 
 }
 
 struct Shared {
-    uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_empty[2], done;
+    uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_empty[2], done[2], turn[2];
     uint64_t kv_full[8], kv_empty[8];
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -159,14 +159,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.q_full[i], 1);
             mbar_init(&sh.q_empty[i], 1);
             mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.p_full[i], 128);
+            mbar_init(&sh.p_full[i], 4);   // one arrival per softmax warp
             mbar_init(&sh.o_full[i], 1);
             mbar_init(&sh.o_empty[i], 128);
+            mbar_init(&sh.done[i], 1);
+            mbar_init(&sh.turn[i], 1);
         }
-        mbar_init(&sh.done, 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&sh.kv_full[s], 1);
-            mbar_init(&sh.kv_empty[s], 1);
+            mbar_init(&sh.kv_empty[s], 2);
         }
         sh.abort_flag = 0;
         fence_barrier_init();
@@ -255,110 +256,140 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            uint32_t kv_it = 0, q_it[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------- MMA issuers
+        // Warp 1 issues sub-tile 0's MMAs and warp 2 sub-tile 1's.  An MMA
+        // instruction waits for room in the tensor pipe's short queue, so a
+        // single issuing thread would reach the second sub-tile's waits only
+        // after the first sub-tile's group had nearly drained; with one
+        // issuer per sub-tile the next group is queued the moment it may go.
+        // In units with two sub-tiles the groups still alternate (QK_0, QK_1,
+        // then PV_0 + QK_0, PV_1 + QK_1 per K/V tile) through a turn token, so
+        // that the two softmax warpgroups stay half a step apart.
+        // Both issuers walk every K/V item in ring order; a stage is free once
+        // both have released it (kv_empty counts 2 arrivals).
+        const int i = warp - 1;
+        // the whole warp runs the loop; one elected lane issues each operation
+        {
+            uint32_t kv_it = 0, q_it = 0, p_cnt = 0, o_cnt = 0, g = 0;
             bool live = true;
+            // group g of this issuer goes after group g - 1 (i = 0) or g (i = 1)
+            // of the other one
+            auto take_turn = [&](bool pair) -> bool {
+                if (!pair) return true;
+                if (i == 0 && g == 0) return true;
+                return mbar_wait_warp(&sh.turn[i], (i == 0 ? g - 1 : g) & 1, abort_flag, err_word,
+                                 kErrTimeoutBase + 11, kWaitNs);
+            };
+            auto pass_turn = [&](bool pair) {
+                if (!pair) return;
+                mbar_arrive_elect(&sh.turn[i ^ 1]);
+                ++g;
+            };
             // Descriptors are built once; an MMA only adds a byte offset >> 4 to the
             // 14-bit start-address field (shared addresses stay below 256 KB).
-            const uint64_t dQ[2] = {sdesc_sw128(smem_u32(sQ[0]), 16, 1024),
-                                    sdesc_sw128(smem_u32(sQ[1]), 16, 1024)};
+            const uint64_t dQ = sdesc_sw128(smem_u32(sQ[i]), 16, 1024);
             const uint64_t dK0 = sdesc_sw128(smem_u32(sKV), 16, 1024);     // K-major
             const uint64_t dV0 = sdesc_sw128(smem_u32(sKV), 16384, 1024);  // MN-major
+            const uint32_t tS = tmem + i * 128, tO = tmem + 256 + i * 128;
+            // a sub-tile this unit lacks still frees each stage after its load landed
+            auto release = [&](bool mine, uint32_t st) {
+                if (mine) mma_commit_elect(&sh.kv_empty[st]);
+                else mbar_arrive_elect(&sh.kv_empty[st]);
+            };
             for (int32_t ui = ub; ui < ue && live; ++ui) {
                 const WlUnit wu = units[ui];
                 const Unit u = decode_unit(wu, segs);
                 const int32_t n = u.ntiles;
                 if (n == 0) continue;
-#pragma unroll
-                for (int i = 0; i < 2; ++i)
-                    if (i < u.nsub && live)
-                        live = mbar_wait(&sh.q_full[i], q_it[i] & 1, abort_flag, err_word,
-                                         kErrTimeoutBase + 3, kWaitNs);
-                if (!live) break;
+                const bool mine = i < u.nsub;
+                const bool pair = u.nsub == 2;
+                if (mine) {
+                    live = mbar_wait_warp(&sh.q_full[i], q_it & 1, abort_flag, err_word,
+                                     kErrTimeoutBase + 3, kWaitNs);
+                    if (!live) break;
+                }
                 // prologue: S_i = Q_i K_0^T
                 {
                     const uint32_t st = kv_it % C::kStages;
-                    live = mbar_wait(&sh.kv_full[st], (kv_it / C::kStages) & 1, abort_flag,
+                    live = mbar_wait_warp(&sh.kv_full[st], (kv_it / C::kStages) & 1, abort_flag,
                                      err_word, kErrTimeoutBase + 4, kWaitNs);
                     if (!live) break;
-                    tc_fence_after();
-                    const uint64_t dK = dK0 + ((st * C::kTileBytes) >> 4);
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        if (i >= u.nsub) break;
+                    live = take_turn(pair);
+                    if (!live) break;
+                    if (mine) {
+                        tc_fence_after();
+                        const uint64_t dK = dK0 + ((st * C::kTileBytes) >> 4);
 #pragma unroll
                         for (int k = 0; k < D / 16; ++k) {
                             const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;  // bytes >> 4
-                            mma_ss(tmem + i * 128, dQ[i] + off16, dK + off16, C::kIdescQK, k > 0);
+                            mma_ss_elect(tS, dQ + off16, dK + off16, C::kIdescQK, k > 0);
                         }
-                        mma_commit(&sh.s_full[i]);
-                        if (n == 1) mma_commit(&sh.q_empty[i]);
+                        mma_commit_elect(&sh.s_full[i]);
+                        if (n == 1) mma_commit_elect(&sh.q_empty[i]);
                     }
-                    mma_commit(&sh.kv_empty[st]);
+                    pass_turn(pair);
+                    release(mine, st);
                     ++kv_it;
                 }
                 for (int32_t j = 0; j < n && live; ++j) {
                     const bool has_next = j + 1 < n;
                     const uint32_t stv = kv_it % C::kStages;
                     const uint32_t stk = (kv_it + 1) % C::kStages;
-                    live = mbar_wait(&sh.kv_full[stv], (kv_it / C::kStages) & 1, abort_flag,
-                                     err_word, kErrTimeoutBase + 5, kWaitNs);
+                    // Everything that is normally ready early is waited for first,
+                    // so that once P_i lands only one wait stands before the MMAs.
+                    live = mbar_wait_warp(&sh.kv_full[stv], (kv_it / C::kStages) & 1, abort_flag,
+                                          err_word, kErrTimeoutBase + 5, kWaitNs);
                     if (!live) break;
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        if (i >= u.nsub || !live) break;
-                        live = mbar_wait(&sh.p_full[i], p_cnt[i] & 1, abort_flag, err_word,
-                                         kErrTimeoutBase + 6, kWaitNs);
+                    if (has_next) {
+                        live = mbar_wait_warp(&sh.kv_full[stk], ((kv_it + 1) / C::kStages) & 1,
+                                              abort_flag, err_word, kErrTimeoutBase + 8, kWaitNs);
                         if (!live) break;
-                        ++p_cnt[i];
-                        if (j == 0) {
-                            live = mbar_wait(&sh.o_empty[i], (o_cnt[i] & 1) ^ 1, abort_flag,
-                                             err_word, kErrTimeoutBase + 7, kWaitNs);
-                            if (!live) break;
-                        }
+                    }
+                    if (mine && j == 0) {
+                        live = mbar_wait_warp(&sh.o_empty[i], (o_cnt & 1) ^ 1, abort_flag,
+                                              err_word, kErrTimeoutBase + 7, kWaitNs);
+                        if (!live) break;
+                    }
+                    live = take_turn(pair);
+                    if (!live) break;
+                    if (mine) {
+                        live = mbar_wait_warp(&sh.p_full[i], p_cnt & 1, abort_flag, err_word,
+                                              kErrTimeoutBase + 6, kWaitNs);
+                        if (!live) break;
+                        ++p_cnt;
                         tc_fence_after();
                         const uint64_t dV = dV0 + ((stv * C::kTileBytes) >> 4);
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            mma_ts(tmem + 256 + i * 128, tmem + i * 128 + k * 8, dV + k * 128,
-                                   C::kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+                            mma_ts_elect(tO, tS + k * 8, dV + k * 128, C::kIdescPV,
+                                         (j > 0 || k > 0) ? 1u : 0u);
                         if (has_next) {
-                            if (i == 0) {
-                                live = mbar_wait(&sh.kv_full[stk], ((kv_it + 1) / C::kStages) & 1,
-                                                 abort_flag, err_word, kErrTimeoutBase + 8, kWaitNs);
-                                if (!live) break;
-                                tc_fence_after();
-                            }
                             const uint64_t dK = dK0 + ((stk * C::kTileBytes) >> 4);
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
                                 const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
-                                mma_ss(tmem + i * 128, dQ[i] + off16, dK + off16, C::kIdescQK,
-                                       k > 0);
+                                mma_ss_elect(tS, dQ + off16, dK + off16, C::kIdescQK, k > 0);
                             }
-                            mma_commit(&sh.s_full[i]);
-                            if (j + 2 == n) mma_commit(&sh.q_empty[i]);
+                            mma_commit_elect(&sh.s_full[i]);
+                            if (j + 2 == n) mma_commit_elect(&sh.q_empty[i]);
                         }
                     }
-                    if (!live) break;
-                    mma_commit(&sh.kv_empty[stv]);
-                    if (has_next) mma_commit(&sh.kv_empty[stk]);
+                    pass_turn(pair);
+                    release(mine, stv);
+                    if (has_next) release(mine, stk);
                     kv_it += has_next ? 2 : 1;
                 }
                 if (!live) break;
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    if (i >= u.nsub) break;
-                    mma_commit(&sh.o_full[i]);
-                    ++o_cnt[i];
-                    ++q_it[i];
+                if (mine) {
+                    mma_commit_elect(&sh.o_full[i]);
+                    ++o_cnt;
+                    ++q_it;
                 }
             }
             // drain every MMA this thread issued before tensor memory is freed
-            mma_commit(&sh.done);
-            mbar_wait_drain(&sh.done, 0, kDrainNs);
+            mma_commit_elect(&sh.done[i]);
+            mbar_wait_drain(&sh.done[i], 0, kDrainNs);
         }
         __syncwarp();
       }
@@ -483,7 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(&sh.p_full[i]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.p_full[i]);
                 }
             }
             if (!live) break;
