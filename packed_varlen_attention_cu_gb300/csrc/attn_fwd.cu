@@ -94,7 +94,8 @@ __device__ __forceinline__ Unit decode_unit(const WlUnit& u, const WlSeg* segs) 
 }
 
 struct Shared {
-    uint64_t q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], o_empty[2], done[2], turn[2];
+    uint64_t q_full[2], q_empty[2], s_full[2], p_half[2], p_full[2], o_full[2], o_empty[2], done[2],
+        turn[2];
     uint64_t kv_full[8], kv_empty[8];
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -159,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.q_full[i], 1);
             mbar_init(&sh.q_empty[i], 1);
             mbar_init(&sh.s_full[i], 1);
-            mbar_init(&sh.p_full[i], 4);   // one arrival per softmax warp
+            mbar_init(&sh.p_half[i], 4);   // one arrival per softmax warp
+            mbar_init(&sh.p_full[i], 4);
             mbar_init(&sh.o_full[i], 1);
             mbar_init(&sh.o_empty[i], 128);
             mbar_init(&sh.done[i], 1);
@@ -354,16 +356,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     live = take_turn(pair);
                     if (!live) break;
                     if (mine) {
-                        live = mbar_wait_warp(&sh.p_full[i], p_cnt & 1, abort_flag, err_word,
+                        // P_i lands in two halves (key columns [0, 64) and [64, 128));
+                        // the first half's MMAs run while the softmax finishes the second
+                        const uint64_t dV = dV0 + ((stv * C::kTileBytes) >> 4);
+                        live = mbar_wait_warp(&sh.p_half[i], p_cnt & 1, abort_flag, err_word,
                                               kErrTimeoutBase + 6, kWaitNs);
+                        if (!live) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_ts_elect(tO, tS + k * 8, dV + k * 128, C::kIdescPV,
+                                         (j > 0 || k > 0) ? 1u : 0u);
+                        live = mbar_wait_warp(&sh.p_full[i], p_cnt & 1, abort_flag, err_word,
+                                              kErrTimeoutBase + 12, kWaitNs);
                         if (!live) break;
                         ++p_cnt;
                         tc_fence_after();
-                        const uint64_t dV = dV0 + ((stv * C::kTileBytes) >> 4);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            mma_ts_elect(tO, tS + k * 8, dV + k * 128, C::kIdescPV,
-                                         (j > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 4; k < 8; ++k)
+                            mma_ts_elect(tO, tS + k * 8, dV + k * 128, C::kIdescPV, 1u);
                         if (has_next) {
                             const uint64_t dK = dK0 + ((stk * C::kTileBytes) >> 4);
 #pragma unroll
@@ -420,7 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
                 const WlRun run = runs[u.run_begin + rr];
                 const WlSlice s = slices[run.slice];
+                // allowed keys of this row, relative to the slice's first key:
+                // [lim_lo, lim_hi) (the diagonal for causal slices, a sliding window
+                // below it, nothing for padding rows)
+                const bool causal = s.type == PVA_SLICE_CAUSAL;
+                const int32_t d_base = q_pos - s.k_pos0;
+                const int32_t lim_hi = !valid ? 0 : causal ? min(s.k_len, d_base + 1) : s.k_len;
+                const int32_t lim_lo =
+                    causal && s.window > 0 ? d_base - s.window + 1 : -(1 << 30);
                 for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
+                    // allowed columns [c_lo, c_hi) in this kv tile, settled while S
+                    // is still being computed
+                    const int32_t kt0 = jt * 128;
+                    const int32_t c_hi = min(128, lim_hi - kt0), c_lo = max(0, lim_lo - kt0);
+                    const bool need_mask = __any_sync(0xffffffffu, c_lo > 0 || c_hi < 128);
                     live = mbar_wait(&sh.s_full[i], s_cnt & 1, abort_flag, err_word,
                                      kErrTimeoutBase + 9, kWaitNs);
                     if (!live) break;
@@ -431,17 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-                    // allowed columns [c_lo, c_hi) of this row in this kv tile
-                    const int32_t kt0 = jt * 128;
-                    int32_t c_hi = min(128, s.k_len - kt0), c_lo = 0;
-                    if (s.type == PVA_SLICE_CAUSAL) {
-                        const int32_t d0 = q_pos - s.k_pos0 - kt0;
-                        c_hi = min(c_hi, d0 + 1);
-                        if (s.window > 0) c_lo = max(0, d0 - s.window + 1);
-                    }
-                    if (!valid) c_hi = 0;
-                    const bool need = c_lo > 0 || c_hi < 128;
-                    if (__any_sync(0xffffffffu, need)) {
+                    if (need_mask) {
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -450,33 +464,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (col < c_lo || col >= c_hi) sr[c][e] = __float_as_uint(-INFINITY);
                             }
                     }
-                    // row max: 4 independent chains of 3-input max, then a tree
-                    float pm[4];
+                    // row max: 16 partial maxima over 8 columns each (3-input max), then
+                    // a 3-input tree; 7 dependent steps instead of one long chain
+                    float pm[16];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float m3 = fmax3(__uint_as_float(sr[c][0]), __uint_as_float(sr[c][1]),
-                                         __uint_as_float(sr[c][2]));
-#pragma unroll
-                        for (int e = 3; e < 31; e += 2)
-                            m3 = fmax3(m3, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-                        pm[c] = fmaxf(m3, __uint_as_float(sr[c][31]));
+                    for (int q = 0; q < 16; ++q) {
+                        const uint32_t* v = &sr[q >> 2][(q & 3) * 8];
+                        float m3 = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]),
+                                         __uint_as_float(v[2]));
+                        m3 = fmax3(m3, __uint_as_float(v[3]), __uint_as_float(v[4]));
+                        m3 = fmax3(m3, __uint_as_float(v[5]), __uint_as_float(v[6]));
+                        pm[q] = fmaxf(m3, __uint_as_float(v[7]));
                     }
-                    const float mx = fmax3(pm[0], pm[1], fmaxf(pm[2], pm[3]));
+                    const float t0 = fmax3(pm[0], pm[1], pm[2]), t1 = fmax3(pm[3], pm[4], pm[5]);
+                    const float t2 = fmax3(pm[6], pm[7], pm[8]), t3 = fmax3(pm[9], pm[10], pm[11]);
+                    const float t4 = fmax3(pm[12], pm[13], pm[14]);
+                    const float mx = fmaxf(fmax3(t0, t1, t2), fmax3(t3, t4, pm[15]));
                     const float m_tile = mx * p.scale_log2;  // -inf stays -inf
+                    // Lazy rescaling: the reference maximum moves only when this tile's
+                    // maximum exceeds it by more than the threshold (or it is still -inf,
+                    // when O and l are zero and need no rescale).
                     float alpha = 1.f;
                     bool rescale = false;
-                    if (m_tile > m_used) {
-                        if (m_used == -INFINITY) {
-                            m_used = m_tile;  // O and l are still zero
-                        } else if (m_tile > m_used + kRescaleThreshold) {
-                            alpha = ex2_approx(m_used - m_tile);
-                            m_used = m_tile;
-                            rescale = true;
-                        }
+                    if (m_tile > m_used + kRescaleThreshold) {
+                        rescale = m_used != -INFINITY;
+                        if (rescale) alpha = ex2_approx(m_used - m_tile);
+                        m_used = m_tile;
                     }
                     l_sum *= alpha;
+                    // rare: the running max moved, rescale this row of O first (PV of
+                    // the previous tile has completed: it ran before QK of this one)
+                    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c * 32, o);
+                            tmem_ld_wait(o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tO + c * 32, o);
+                        }
+                    }
                     // P = 2^(s*scale*log2e - m), packed to bf16 pairs in place
-                    // (pair e/2 lands in a register already consumed)
+                    // (pair e/2 lands in a register already consumed), handed to
+                    // the MMA warp in two halves of 64 key columns
                     const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
                     // packed fp32x2 FMA / add: two elements per instruction
                     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
@@ -496,26 +528,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             sr[c][e >> 1] = pack_bf16x2(p0, p1);
                         }
                         tmem_st16(tS + c * 16, sr[c]);
+                        if (c == 1 || c == 3) {
+                            tmem_st_wait();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(c == 1 ? &sh.p_half[i] : &sh.p_full[i]);
+                        }
                     }
                     const float2 ps = __fadd2_rn(__fadd2_rn(part[0], part[1]), __fadd2_rn(part[2], part[3]));
                     l_sum += ps.x + ps.y;
-                    // rare: the running max moved, rescale this row of O
-                    if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t o[32];
-                            tmem_ld32(tO + c * 32, o);
-                            tmem_ld_wait(o);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st32(tO + c * 32, o);
-                        }
-                    }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sh.p_full[i]);
                 }
             }
             if (!live) break;
