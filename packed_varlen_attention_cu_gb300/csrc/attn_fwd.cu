@@ -527,12 +527,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                             part[c] = __fadd2_rn(part[c], make_float2(p0, p1));
                             sr[c][e >> 1] = pack_bf16x2(p0, p1);
                         }
-                        tmem_st16(tS + c * 16, sr[c]);
-                        if (c == 1 || c == 3) {
+                        // the first half is announced after chunk 2's exponentials, so
+                        // that the wait for its stores overlaps them
+                        if (c == 2) {
                             tmem_st_wait();
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(c == 1 ? &sh.p_half[i] : &sh.p_full[i]);
+                            if (lane == 0) mbar_arrive(&sh.p_half[i]);
+                        }
+                        tmem_st16(tS + c * 16, sr[c]);
+                        if (c == 3) {
+                            tmem_st_wait();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&sh.p_full[i]);
                         }
                     }
                     const float2 ps = __fadd2_rn(__fadd2_rn(part[0], part[1]), __fadd2_rn(part[2], part[3]));
