@@ -57,8 +57,12 @@ def make_workload(args):
         w = W.Workload(f"{args.pack_tokens}-token causal pack H=32/8 d=128",
                        W.lognormal_doc_lengths(args.pack_tokens, math.log(2048.0), 1.5, 1,
                                                65536, 0), 32, 8, 128, cp=8)
-        return w, desc.replace("128K", f"{args.pack_tokens}-token")
-    return mk(), desc
+        desc = desc.replace("128K", f"{args.pack_tokens}-token")
+    else:
+        w = mk()
+    if args.c_tile is None:
+        args.c_tile = api.default_c_tile(w.head_dim)
+    return w, desc
 
 
 def load_peaks():
@@ -548,7 +552,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("pva", "reference"), default="pva")
     ap.add_argument("--workload", choices=tuple(WORKLOADS), default="128k")
-    ap.add_argument("--c-tile", type=int, default=8192)
+    ap.add_argument("--c-tile", type=int, default=None,
+                    help="per-tile fixed cost in pair units (default: api.default_c_tile(d))")
     ap.add_argument("--pack-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -48,6 +48,14 @@ def make_mask(kind: int = MASK_CAUSAL, q_tokens: int = 0, k_tokens: int = 0, win
     return m
 
 
+def default_c_tile(head_dim: int) -> int:
+    """Per-tile fixed cost (pair units) that balanced CTA busy time best on GB300:
+    a computed 128 x 128 tile costs about its 16384 pairs of MMA work plus a
+    softmax/hand-off term that does not shrink with the head dimension, so the
+    fixed term doubles when d halves (32768 at d = 128, 65536 at d = 64)."""
+    return 32768 * 128 // int(head_dim)
+
+
 def make_params(num_q_heads: int, num_kv_heads: int, num_ctas: int = 0, c_tile: int = 0,
                 tile_m: int = TILE, tile_n: int = TILE) -> WorklistParams:
     p = WorklistParams()
@@ -188,9 +196,12 @@ class PackedAttention:
     the forward on it.  Buffers come from PyTorch; all work is in libpva."""
 
     def __init__(self, cu_seqlens: Optional[torch.Tensor], mask: MaskDesc,
-                 num_q_heads: int, num_kv_heads: int, num_ctas: int = 0, c_tile: int = 0):
+                 num_q_heads: int, num_kv_heads: int, num_ctas: int = 0,
+                 c_tile: Optional[int] = None, head_dim: int = 128):
         self.cu = cu_seqlens
         self.mask = mask
+        if c_tile is None:
+            c_tile = default_c_tile(head_dim)
         self.params = make_params(num_q_heads, num_kv_heads, num_ctas, c_tile)
         nd = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
         dev = cu_seqlens.device if cu_seqlens is not None else torch.device("cuda")
