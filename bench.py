@@ -61,6 +61,7 @@ def make_workload(args):
     else:
         w = mk()
     if args.c_tile is None:
+        from packed_varlen_attention_cu_gb300 import api
         args.c_tile = api.default_c_tile(w.head_dim)
     return w, desc
 

@@ -63,3 +63,19 @@ def test_reference_arm_on_other_ranks_prints_nothing(monkeypatch, capsys):
     assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "1",
                        "--warmup", "3"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_make_workload_default_c_tile():
+    """Every bench workload resolves; the per-tile cost defaults from its head dim."""
+    sys.path.insert(0, ROOT)
+    import types
+    import bench
+    from packed_varlen_attention_cu_gb300 import api
+    for name in bench.WORKLOADS:
+        args = types.SimpleNamespace(workload=name, pack_tokens=0, c_tile=None)
+        w, desc = bench.make_workload(args)
+        assert args.c_tile == api.default_c_tile(w.head_dim) == 32768 * 128 // w.head_dim
+        assert desc
+    args = types.SimpleNamespace(workload="128k", pack_tokens=32768, c_tile=777)
+    w, _ = bench.make_workload(args)
+    assert w.total_tokens == 32768 and args.c_tile == 777
