@@ -411,7 +411,10 @@ void or_merge(const double *oa, const double *la, const double *ob, const double
 /*    output rows), the analogue of the per-sample constant c*n of the      */
 /*    fitted DP load model ([P2] §4.2).                                      */
 /*  - LPT ties: sort is stable on the enumeration index; the lightest bin   */
-/*    with the lowest id wins a tie.  A bin's list is in assignment order.   */
+/*    with the lowest id wins a tie.                                         */
+/*  - LPT fixes which bin runs a unit, not when; a bin's list is in          */
+/*    enumeration order (ascending unit id), so bins that run at the same   */
+/*    time work on the same segments and kv heads.                           */
 /* ------------------------------------------------------------------------ */
 typedef struct {
     int32_t q_row0, q_len, q_pos0, k_row0, k_len, k_pos0, type, window;
@@ -763,18 +766,16 @@ int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t ti
             }
         }
     }
-    int64_t *cost = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nunits > 0 ? nunits : 1));
+    int64_t *cost = (int64_t *)calloc((size_t)(nunits > 0 ? nunits : 1), sizeof(int64_t));
     int32_t *assign = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nunits > 0 ? nunits : 1));
-    int64_t *order = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nunits > 0 ? nunits : 1));
     for (int64_t i = 0; i < nunits; ++i) cost[i] = U[i].cost;
-    or_lpt(cost, nunits, num_ctas, assign, order, NULL);
-    /* CSR: per bin, units in assignment order */
+    or_lpt(cost, nunits, num_ctas, assign, NULL, NULL);
+    /* CSR: per bin, units in enumeration order */
     int32_t *fill = (int32_t *)calloc((size_t)num_ctas + 1, sizeof(int32_t));
     for (int64_t i = 0; i < nunits; ++i) fill[assign[i] + 1]++;
     for (int32_t b = 0; b < num_ctas; ++b) fill[b + 1] += fill[b];
     for (int32_t b = 0; b <= num_ctas; ++b) cta_off_out[b] = fill[b];
-    for (int64_t i = 0; i < nunits; ++i) {
-        int64_t u = order[i];
+    for (int64_t u = 0; u < nunits; ++u) {
         int32_t pos = fill[assign[u]]++;
         int32_t *o = units_out + 10 * (int64_t)pos;
         o[0] = (int32_t)u; o[1] = U[u].seg; o[2] = U[u].t0; o[3] = U[u].t1; o[4] = U[u].h0;
@@ -784,7 +785,6 @@ int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t ti
         unit_pairs_out[pos] = U[u].pairs;
     }
     free(fill);
-    free(order);
     free(assign);
     free(cost);
     free(U);

@@ -157,8 +157,8 @@ def worklist_counts(worklist: torch.Tensor, stream=None) -> dict:
 
 # ----------------------------------------------------------------- decoding
 _HDR = np.dtype([("i32", "<i4", 20), ("c_tile", "<i8"), ("pair_sum", "<u8"), ("tile_sum", "<u8"),
-                 ("off", "<i8", 12)])
-_OFF = ("slices", "segs", "units_enum", "keys", "order", "assign", "local", "units", "runs",
+                 ("off", "<i8", 11)])
+_OFF = ("slices", "segs", "units_enum", "keys", "order", "assign", "units", "runs",
         "cta_off", "doc_scan", "total")
 
 

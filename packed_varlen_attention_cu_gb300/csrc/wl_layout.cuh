@@ -7,11 +7,10 @@
 //   slices     WlSlice[cap_slices]        slices of the mask, enumeration order
 //   segs       WlSeg[cap_segs]            query segments (slices sharing a q range)
 //   units_enum WlUnit[cap_units]          work units in enumeration order
-//   keys       uint64[cap_units]          sort keys: (~cost << 24) | uid
+//   keys       uint64[cap_units]          sort keys: (~cost << 24) | uid, then (cta << 24) | uid
 //   order      int32[cap_units]           uid of the r-th unit in LPT order
 //   assign     int32[cap_units]           bin (CTA) of each uid
-//   local      int32[cap_units]           position of each uid inside its bin
-//   units      WlUnit[cap_units]          units grouped by CTA, in assignment order
+//   units      WlUnit[cap_units]          units grouped by CTA, in enumeration order inside a CTA
 //   runs       WlRun[cap_runs]            per unit and slice: kv tile span [lo, hi)
 //   cta_off    int32[num_ctas + 1]        CSR offsets of the CTAs into `units`
 //   doc_scan   int32[4 * (num_docs + 1)]  per-document scan scratch
@@ -22,7 +21,7 @@
 namespace pva {
 
 constexpr int32_t kWlMagic = 0x57415650;  // "PVAW"
-constexpr int32_t kWlVersion = 1;
+constexpr int32_t kWlVersion = 2;
 constexpr int kMaxBins = 1024;
 constexpr int kUidBits = 24;   // units per worklist < 2^24
 constexpr int kCostBits = 40;  // unit cost < 2^40
@@ -46,8 +45,7 @@ struct WlRun {
 };
 
 struct WlOffsets {
-    int64_t slices, segs, units_enum, keys, order, assign, local, units, runs, cta_off, doc_scan,
-        total;
+    int64_t slices, segs, units_enum, keys, order, assign, units, runs, cta_off, doc_scan, total;
 };
 
 struct WlHeader {

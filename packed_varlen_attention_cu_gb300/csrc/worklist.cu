@@ -13,7 +13,9 @@
 //   wl_units  grid   : one thread per work unit: kv-tile span of every slice
 //                      for its two sub-tiles, exact pair count, cost, sort key
 //   wl_sort_chunks / wl_merge_rank : stable sort by (cost desc, uid asc)
-//   wl_lpt    1 CTA  : exact LPT in batches (see below), CSR by CTA
+//   wl_lpt    1 CTA  : exact LPT in batches (see below), CTA offsets
+//   wl_sort_chunks / wl_merge_rank : sort by (cta, uid): each CTA's list in
+//                      enumeration order
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -502,6 +504,10 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(uint8_t* b
     for (int32_t i = threadIdx.x; i < m; i += kSortThreads) keys[c0 + i] = sk[i];
 }
 
+// kCtaOrder = false: keys are (~cost, uid) and order[rank] = uid (LPT order).
+// kCtaOrder = true: keys are (cta, uid) and units[rank] = the unit with its
+// CTA, i.e. the CSR list of every CTA in enumeration order.
+template <bool kCtaOrder>
 __global__ void __launch_bounds__(kSortThreads) wl_merge_rank_kernel(uint8_t* base) {
     WlHeader* h = reinterpret_cast<WlHeader*>(base);
     if (h->error) return;
@@ -539,7 +545,17 @@ __global__ void __launch_bounds__(kSortThreads) wl_merge_rank_kernel(uint8_t* ba
     }
     for (int e = 0; e < 2; ++e) {
         const int32_t i = threadIdx.x + e * kSortThreads;
-        if (i < m) order[rank[e]] = (int32_t)(mine[e] & ((1ULL << kUidBits) - 1));
+        if (i >= m) continue;
+        const int32_t uid = (int32_t)(mine[e] & ((1ULL << kUidBits) - 1));
+        if (kCtaOrder) {
+            const WlUnit* units_enum = reinterpret_cast<const WlUnit*>(base + h->off.units_enum);
+            WlUnit* units = reinterpret_cast<WlUnit*>(base + h->off.units);
+            WlUnit x = units_enum[uid];
+            x.cta = (int32_t)(mine[e] >> kUidBits);
+            units[rank[e]] = x;
+        } else {
+            order[rank[e]] = uid;
+        }
     }
 }
 
@@ -585,8 +601,6 @@ __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t
     const WlUnit* units_enum = reinterpret_cast<const WlUnit*>(base + h->off.units_enum);
     const int32_t* order = reinterpret_cast<const int32_t*>(base + h->off.order);
     int32_t* assign = reinterpret_cast<int32_t*>(base + h->off.assign);
-    int32_t* local = reinterpret_cast<int32_t*>(base + h->off.local);
-    WlUnit* units = reinterpret_cast<WlUnit*>(base + h->off.units);
     int32_t* cta_off = reinterpret_cast<int32_t*>(base + h->off.cta_off);
     __shared__ unsigned long long S[kMaxBins], Snew[kMaxBins];
     __shared__ int32_t cnt[kMaxBins];
@@ -681,7 +695,6 @@ __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t
             if (main && j < m) {
                 const int32_t uid = suid[t + j - stage0];
                 assign[uid] = bin;
-                local[uid] = cnt[bin] + j;
             }
             if (main && j == m - 1) Snew[0] = s0 + ((unsigned long long)(excl + cj) << 10);
             if (tid > 0 && tid < B) Snew[tid] = S[tid];
@@ -695,7 +708,7 @@ __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t
             const int32_t uid = suid[t + tid - stage0];
             const int32_t bin = (int32_t)(S[tid] & 1023ULL);
             assign[uid] = bin;
-            local[uid] = cnt[bin]++;
+            ++cnt[bin];
             Snew[tid] = val;
         } else if (tid < B) {
             Snew[tid] = S[tid];
@@ -726,11 +739,12 @@ __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t
         if (tid < B) rc[tid] = excl;
     }
     __syncthreads();
-    for (int32_t u = tid; u < n; u += blockDim.x) {
-        WlUnit x = units_enum[u];
-        x.cta = assign[u];
-        units[rc[x.cta] + local[u]] = x;
-    }
+    // Each CTA runs its units in enumeration order (segment, kv head, head pair,
+    // q tile): CTAs that run at the same time then walk the K/V of the same
+    // documents, which stay in L2.  Keys (cta, uid) are sorted next.
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(base + h->off.keys);
+    for (int32_t u = tid; u < n; u += blockDim.x)
+        keys[u] = ((unsigned long long)assign[u] << kUidBits) | (unsigned long long)u;
 }
 
 // ------------------------------------------------------------------ host side
@@ -832,7 +846,6 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     f.keys = o; o = align256(o + cap_units * 8);
     f.order = o; o = align256(o + cap_units * 4);
     f.assign = o; o = align256(o + cap_units * 4);
-    f.local = o; o = align256(o + cap_units * 4);
     f.units = o; o = align256(o + cap_units * (int64_t)sizeof(WlUnit));
     f.runs = o; o = align256(o + (int64_t)h->cap_runs * sizeof(WlRun));
     f.cta_off = o; o = align256(o + ((int64_t)num_ctas + 1) * 4);
@@ -912,10 +925,12 @@ extern "C" pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t 
     wl_units_kernel<<<ub, kUnitWarps * 32, 0, st>>>(ua);
     const int sb = (h.cap_units + kSortChunk - 1) / kSortChunk;
     wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(base);
-    wl_merge_rank_kernel<<<sb, kSortThreads, 0, st>>>(base);
+    wl_merge_rank_kernel<false><<<sb, kSortThreads, 0, st>>>(base);
     const int bp = ((nc + 31) / 32) * 32;
     const int lpt_f = bp >= 1024 ? 1 : (1024 / bp < 4 ? 1024 / bp : 4);
     wl_lpt_kernel<<<1, bp * lpt_f, 0, st>>>(base, lpt_f);
+    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(base);
+    wl_merge_rank_kernel<true><<<sb, kSortThreads, 0, st>>>(base);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
 
