@@ -212,6 +212,16 @@ pva_status pva_attn_fwd_noalloc(const void* q, const void* k, const void* v,
 /* Size in bytes of the static worklist array used by pva_attn_fwd_noalloc. */
 size_t pva_noalloc_scratch_bytes(void);
 
+/* Test hook for the failure path of the bounded waits (the pages have no
+ * counterpart).  While `enable` is non-zero, pva_attn_fwd launches made by
+ * this process tell CTA 0's TMA producer to skip its second K/V load.  The
+ * MMA warps of that CTA then wait for a copy that never comes; their bounded
+ * wait (2 s) expires, the CTA raises its abort flag, drains its own copies and
+ * MMAs, frees tensor memory and returns, and pva_worklist_error() reports
+ * 200 + the wait site.  Nothing faults and the CUDA context stays usable;
+ * every other CTA finishes its work.  For tests only. */
+void pva_debug_withhold_kv_load(int32_t enable);
+
 const char* pva_status_string(pva_status status);
 int32_t pva_version(void);
 

@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "PVA_OK", 1: "PVA_ERR_INVALID_ARG", 2: "PVA_ERR_BUFFER_TOO_SM
 EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_zigzag_shard_len",
            "pva_zigzag_shard", "pva_gather_rows", "pva_merge_partials", "pva_worklist_error",
            "pva_worklist_counts", "pva_attn_fwd_noalloc", "pva_noalloc_scratch_bytes",
-           "pva_status_string", "pva_version")
+           "pva_debug_withhold_kv_load", "pva_status_string", "pva_version")
 
 
 class Slice(ctypes.Structure):
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_float, P]
         L.pva_noalloc_scratch_bytes.restype = sz
         L.pva_noalloc_scratch_bytes.argtypes = []
+        L.pva_debug_withhold_kv_load.restype = None
+        L.pva_debug_withhold_kv_load.argtypes = [i32]
         L.pva_status_string.restype = ctypes.c_char_p
         L.pva_status_string.argtypes = [ctypes.c_int]
         L.pva_version.restype = i32

@@ -146,6 +146,13 @@ def worklist_error(worklist: torch.Tensor, stream=None) -> int:
     return int(code.value)
 
 
+def debug_withhold_kv_load(enable: bool) -> None:
+    """Test hook (see pva_debug_withhold_kv_load): while enabled, CTA 0 of each
+    attention launch waits for a K/V copy that is never issued, so its bounded
+    wait expires and worklist_error() reports the wait site."""
+    lib().pva_debug_withhold_kv_load(1 if enable else 0)
+
+
 def worklist_counts(worklist: torch.Tensor, stream=None) -> dict:
     out = (ctypes.c_int64 * 7)()
     st = lib().pva_worklist_counts(_ptr(worklist), out, _stream(stream))

@@ -30,6 +30,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/pva.h"
 #include "common.h"
 #include "ptx.cuh"
@@ -62,6 +64,7 @@ struct AttnParams {
     uint64_t* busy;
     int32_t q_tokens, k_tokens, hq, hkv, out_fp32, num_ctas;
     float scale_log2;
+    int32_t withhold_kv;  // test hook: CTA 0's producer skips K/V item 1
 };
 
 struct SubTile {
@@ -231,6 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
                         const int32_t krow = s.k_row0 + jt * 128;
                         for (int kv = 0; kv < 2 && live; ++kv) {
+                            if (p.withhold_kv && blockIdx.x == 0 && kv_it == 1) {
+                                ++kv_it;  // test hook: this copy never arrives
+                                continue;
+                            }
                             const uint32_t st = kv_it % C::kStages;
                             live = mbar_wait(&sh.kv_empty[st], ((kv_it / C::kStages) & 1) ^ 1,
                                              abort_flag, err_word, kErrTimeoutBase + 2, kWaitNs);
@@ -606,6 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace pva {
 namespace {
 
+std::atomic<int32_t> g_withhold_kv{0};  // pva_debug_withhold_kv_load
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -709,6 +718,11 @@ extern "C" pva_status pva_attn_fwd(const void* q, const void* k, const void* v,
     ap.num_ctas = nc;
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
     ap.scale_log2 = scale * 1.4426950408889634f;
+    ap.withhold_kv = g_withhold_kv.load(std::memory_order_relaxed);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return head_dim == 128 ? launch<128>(mq, mk, mv, ap, st) : launch<64>(mq, mk, mv, ap, st);
+}
+
+extern "C" void pva_debug_withhold_kv_load(int32_t enable) {
+    g_withhold_kv.store(enable != 0 ? 1 : 0, std::memory_order_relaxed);
 }
