@@ -220,7 +220,7 @@ def run_pva(args, rank, world, local):
     assert counts["status"] == 0, counts
     pairs = counts["pairs_per_head"]
     flops = 4.0 * d * hq * pairs
-    n_wl_kernels = 4
+    n_wl_kernels = api.WORKLIST_BUILD_KERNELS
     io_bytes = (q.numel() + k.numel() + v.numel() + out.numel()) * 2 + lse.numel() * 4
 
     def step(ev_a=None, ev_b=None):
@@ -278,7 +278,7 @@ def run_pva(args, rank, world, local):
         "config": {"workload": desc, "tokens": T, "docs": w.num_docs, "q_heads": hq,
                    "kv_heads": hkv, "head_dim": d, "mask": w.mask_kind,
                    "pairs_per_head": pairs, "flops_per_step": flops,
-                   "step": "device worklist build (4 kernels) + attention forward (1 kernel)",
+                   "step": f"device worklist build ({n_wl_kernels} kernels) + attention forward (1 kernel)",
                    "l2": f"inputs larger than L2: Q+K+V+O+LSE = {io_bytes / 1e9:.2f} GB "
                          f"> {L2_BYTES / 1e6:.0f} MB, no flush",
                    "num_ctas": num_ctas, "c_tile": args.c_tile,
@@ -352,10 +352,12 @@ def run_e2e(args, ctx, world):
             "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": round(t / K * 1e3, 4)}
 
 
-def run_zigzag(args, ctx, world):
+def run_zigzag(args, ctx, world, fused=False):
     """Zigzag CP emulation on one GPU: cp virtual ranks; rank r runs its Q
     shard against the KV shard of rank (r - t) mod cp at ring step t (fp32
-    partials), merging into the running (O, LSE); results scattered back."""
+    partials), merging into the running (O, LSE); results scattered back.
+    fused: steps t > 0 merge in the attention epilogue (pva_attn_fwd_accumulate)
+    instead of writing a partial and running pva_merge_partials."""
     import torch
 
     from packed_varlen_attention_cu_gb300 import api
@@ -396,6 +398,10 @@ def run_zigzag(args, ctx, world):
                 s = (r - t) % cp
                 m = masks[(r, s)]
                 api.build_worklist(cu, m, params, wls[(r, s)], stream)
+                if fused and t > 0:
+                    api.attn_fwd_accumulate(qs[r], ks[s], vs[s], cu, m, params, wls[(r, s)],
+                                            acc_o[r], acc_l[r], 0.0, None, stream)
+                    continue
                 dst_o, dst_l = (acc_o[r], acc_l[r]) if t == 0 else (po, pl)
                 api.attn_fwd(qs[r], ks[s], vs[s], cu, m, params, wls[(r, s)], dst_o, dst_l, 0.0,
                              None, stream)
@@ -422,10 +428,16 @@ def run_zigzag(args, ctx, world):
     torch.cuda.synchronize()
     barrier(world)
     t, f = aggregate(s.elapsed_time(e) / 1e3, flops * K, world)
+    if fused:
+        launches = cp * 4 + cp * cp * (api.WORKLIST_BUILD_KERNELS + 1)
+        return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "cp": cp, "steps": K,
+                "ms_per_step": round(t / K * 1e3, 3), "gpu_launches_per_step": launches,
+                "note": "as zigzag_cp, but ring steps t > 0 merge into the running (O, LSE) in "
+                        "the attention epilogue: no partial buffers, no merge launches"}
     mtimes = [a.elapsed_time(b) / 1e3 for a, b, _ in merge_ev]
     mbytes = [n * hq * (3 * 4 * d + 3 * 4) for _, _, n in merge_ev]
     merge_gbs = sum(mbytes) / sum(mtimes) / 1e9 if mtimes else None
-    launches = cp * 4 + cp * cp * 5 + cp * (cp - 1)
+    launches = cp * 4 + cp * cp * (api.WORKLIST_BUILD_KERNELS + 1) + cp * (cp - 1)
     return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "cp": cp, "steps": K,
             "ms_per_step": round(t / K * 1e3, 3),
             "merge": {"bound": "hbm", "achieved": round(merge_gbs, 1) if merge_gbs else None,
@@ -576,6 +588,7 @@ def main(argv=None):
         res["e2e"] = run_e2e(args, ctx, world)
     if not args.no_zigzag and ctx[0].cp:
         res["zigzag_cp"] = run_zigzag(args, ctx, world)
+        res["zigzag_cp_fused"] = run_zigzag(args, ctx, world, fused=True)
     if args.workload == "libra":
         res["libra_ratio"] = run_libra_ratio(args, ctx)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

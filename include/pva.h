@@ -142,6 +142,27 @@ pva_status pva_attn_fwd(const void* q, const void* k, const void* v,
                         const void* worklist_dev, void* out, int32_t out_is_fp32, float* lse,
                         float softmax_scale, uint64_t* cta_busy_ns, void* stream);
 
+/* Fused ring step ("03 · 长文负载均衡" §3.2: DCP reduces partial outputs;
+ * "长序列训练与上下文并行", ring attention: each step's local result is merged
+ * into the running state).  Same arguments as pva_attn_fwd, except that the
+ * output is a running pair that the call reads and updates in place:
+ *   o_run    DEVICE fp32 [q_tokens, num_q_heads, head_dim]
+ *   lse_run  DEVICE fp32 [num_q_heads, q_tokens]
+ * For every query row with at least one allowed key in this call:
+ *   lse' = ln(e^lse_run + e^lse_step),
+ *   o'   = e^(lse_run - lse') o_run + e^(lse_step - lse') o_step
+ * (o_run is not read where lse_run = -inf).  Rows with no allowed key in this
+ * call keep their running values.  Start a ring with o_run = 0 and
+ * lse_run = -inf (rows that never receive a key then end as O = 0,
+ * LSE = -inf, as with separate partials and merges).  The
+ * result equals pva_attn_fwd into fp32 partials followed by pva_merge_partials,
+ * without the partial buffers or the separate merge pass. */
+pva_status pva_attn_fwd_accumulate(const void* q, const void* k, const void* v,
+                                   const int32_t* cu_seqlens_dev, const pva_mask_desc* mask,
+                                   const pva_worklist_params* params, int32_t head_dim,
+                                   const void* worklist_dev, float* o_run, float* lse_run,
+                                   float softmax_scale, uint64_t* cta_busy_ns, void* stream);
+
 /* Rows of zigzag shard `rank` ("03 · 长文负载均衡" §4.2-4.3): every document
  * is cut into 2*cp contiguous chunks, chunk c holding floor(l/2cp) tokens
  * plus one if c < l mod 2cp; rank r owns chunks r and 2cp-1-r of every

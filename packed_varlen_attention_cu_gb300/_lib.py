@@ -17,7 +17,8 @@ STATUS_NAMES = {0: "PVA_OK", 1: "PVA_ERR_INVALID_ARG", 2: "PVA_ERR_BUFFER_TOO_SM
                 6: "PVA_ERR_DEVICE"}
 
 # Every symbol declared by include/pva.h.
-EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_zigzag_shard_len",
+EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_attn_fwd_accumulate",
+           "pva_zigzag_shard_len",
            "pva_zigzag_shard", "pva_gather_rows", "pva_merge_partials", "pva_worklist_error",
            "pva_worklist_counts", "pva_attn_fwd_noalloc", "pva_noalloc_scratch_bytes",
            "pva_debug_withhold_kv_load", "pva_status_string", "pva_version")
@@ -69,6 +70,9 @@ def lib() -> ctypes.CDLL:
         L.pva_build_worklist.argtypes = [P, i32, MP, WP, P, sz, P]
         L.pva_attn_fwd.restype = ctypes.c_int
         L.pva_attn_fwd.argtypes = [P, P, P, P, MP, WP, i32, P, P, i32, P, ctypes.c_float, P, P]
+        L.pva_attn_fwd_accumulate.restype = ctypes.c_int
+        L.pva_attn_fwd_accumulate.argtypes = [P, P, P, P, MP, WP, i32, P, P, P, ctypes.c_float, P,
+                                              P]
         L.pva_zigzag_shard_len.restype = i32
         L.pva_zigzag_shard_len.argtypes = [P, i32, i32, i32]
         L.pva_zigzag_shard.restype = ctypes.c_int

@@ -48,6 +48,11 @@ def make_mask(kind: int = MASK_CAUSAL, q_tokens: int = 0, k_tokens: int = 0, win
     return m
 
 
+# Kernels one pva_build_worklist launches: plan, units, chunk sort + merge
+# rank (LPT order), LPT, chunk sort + merge rank (per-CTA order).
+WORKLIST_BUILD_KERNELS = 7
+
+
 def default_c_tile(head_dim: int) -> int:
     """Per-tile fixed cost (pair units) that balanced CTA busy time best on GB300:
     a computed 128 x 128 tile costs about its 16384 pairs of MMA work plus a
@@ -102,6 +107,23 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), ctypes.byref(mask), ctypes.byref(params),
         q.shape[-1], _ptr(worklist), _ptr(out), 1 if out.dtype == torch.float32 else 0,
         _ptr(lse), float(softmax_scale), _ptr(cta_busy), _stream(stream)))
+
+
+def attn_fwd_accumulate(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        cu_seqlens: Optional[torch.Tensor], mask: MaskDesc,
+                        params: WorklistParams, worklist: torch.Tensor, o_run: torch.Tensor,
+                        lse_run: torch.Tensor, softmax_scale: float = 0.0,
+                        cta_busy: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Fused ring step: merge this call's attention into the running fp32
+    o_run [Tq, Hq, d] and lse_run [Hq, Tq] in place (start with lse_run = -inf)."""
+    for t in (q, k, v, o_run, lse_run):
+        assert t.is_cuda and t.is_contiguous()
+    assert q.dtype == k.dtype == v.dtype == torch.bfloat16
+    assert o_run.dtype == lse_run.dtype == torch.float32
+    check("pva_attn_fwd_accumulate", lib().pva_attn_fwd_accumulate(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), ctypes.byref(mask), ctypes.byref(params),
+        q.shape[-1], _ptr(worklist), _ptr(o_run), _ptr(lse_run), float(softmax_scale),
+        _ptr(cta_busy), _stream(stream)))
 
 
 def zigzag_shard_len(cu_seqlens_host: np.ndarray, cp: int, rank: int) -> int:

@@ -64,6 +64,7 @@ struct AttnParams {
     uint64_t* busy;
     int32_t q_tokens, k_tokens, hq, hkv, out_fp32, num_ctas;
     float scale_log2;
+    int32_t accumulate;   // merge into the running fp32 (out, lse) instead of writing
     int32_t withhold_kv;  // test hook: CTA 0's producer skips K/V item 1
 };
 
@@ -429,7 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i >= u.nsub) continue;
             const SubTile st = i == 0 ? u.st[0] : u.st[1];
             if (u.ntiles == 0) {
-                write_empty_rows(p, st, r, D);
+                // no key for these rows: O = 0, LSE = -inf, which a running
+                // (O, LSE) absorbs unchanged
+                if (!p.accumulate) write_empty_rows(p, st, r, D);
                 continue;
             }
             const bool valid = r < st.nrows;
@@ -572,7 +575,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
             tc_fence_before();
             mbar_arrive(&sh.o_empty[i]);
-            if (valid) {
+            const float lse_new =
+                l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+            float* lrow = p.lse + (int64_t)st.head * p.q_tokens + st.q_row + r;
+            if (valid && p.accumulate) {
+                // fused ring step: merge this partial into the running fp32 (O, LSE)
+                //   lse = ln(e^lse_run + e^lse_new),
+                //   O = e^(lse_run - lse) O_run + e^(lse_new - lse) O_new
+                // a row without keys here (lse_new = -inf) keeps its running values
+                if (lse_new != -INFINITY) {
+                    const float lse_old = *lrow;
+                    const float mx = fmaxf(lse_old, lse_new);
+                    const float ea = lse_old == -INFINITY ? 0.f : expf(lse_old - mx);
+                    const float eb = expf(lse_new - mx);
+                    const float wa = ea / (ea + eb), wb = eb / (ea + eb) * inv;
+                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * D);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            // a running value never merged before may be anything
+                            const float4 x = ea == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                       : dst[c * 8 + e];
+                            dst[c * 8 + e] =
+                                make_float4(wa * x.x + wb * __uint_as_float(o[c][4 * e]),
+                                            wa * x.y + wb * __uint_as_float(o[c][4 * e + 1]),
+                                            wa * x.z + wb * __uint_as_float(o[c][4 * e + 2]),
+                                            wa * x.w + wb * __uint_as_float(o[c][4 * e + 3]));
+                        }
+                    }
+                    *lrow = mx + logf(ea + eb);
+                }
+            } else if (valid) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     if (p.out_fp32) {
@@ -596,10 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pack_bf16x2(__uint_as_float(o[c][8 * e + 6]) * inv, __uint_as_float(o[c][8 * e + 7]) * inv));
                     }
                 }
+                *lrow = lse_new;
             }
-            if (valid)
-                p.lse[(int64_t)st.head * p.q_tokens + st.q_row + r] =
-                    l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
         }
         finish();
     }
@@ -673,12 +705,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 using namespace pva;
 
-extern "C" pva_status pva_attn_fwd(const void* q, const void* k, const void* v,
-                                   const int32_t* cu_seqlens_dev, const pva_mask_desc* mask,
-                                   const pva_worklist_params* params, int32_t head_dim,
-                                   const void* worklist_dev, void* out, int32_t out_is_fp32,
-                                   float* lse, float softmax_scale, uint64_t* cta_busy_ns,
-                                   void* stream) {
+namespace {
+
+pva_status attn_fwd_impl(const void* q, const void* k, const void* v,
+                         const int32_t* cu_seqlens_dev, const pva_mask_desc* mask,
+                         const pva_worklist_params* params, int32_t head_dim,
+                         const void* worklist_dev, void* out, int32_t out_is_fp32, float* lse,
+                         float softmax_scale, uint64_t* cta_busy_ns, int32_t accumulate,
+                         void* stream) {
     if (!mask || !params || !worklist_dev || !out || !lse || !q) return PVA_ERR_INVALID_ARG;
     if (mask->kind != PVA_MASK_SLICES && !cu_seqlens_dev) return PVA_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return PVA_ERR_UNSUPPORTED;
@@ -715,12 +749,36 @@ extern "C" pva_status pva_attn_fwd(const void* q, const void* k, const void* v,
     ap.hq = params->num_q_heads;
     ap.hkv = params->num_kv_heads;
     ap.out_fp32 = out_is_fp32;
+    ap.accumulate = accumulate;
     ap.num_ctas = nc;
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
     ap.scale_log2 = scale * 1.4426950408889634f;
     ap.withhold_kv = g_withhold_kv.load(std::memory_order_relaxed);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return head_dim == 128 ? launch<128>(mq, mk, mv, ap, st) : launch<64>(mq, mk, mv, ap, st);
+}
+
+}  // namespace
+
+extern "C" pva_status pva_attn_fwd(const void* q, const void* k, const void* v,
+                                   const int32_t* cu_seqlens_dev, const pva_mask_desc* mask,
+                                   const pva_worklist_params* params, int32_t head_dim,
+                                   const void* worklist_dev, void* out, int32_t out_is_fp32,
+                                   float* lse, float softmax_scale, uint64_t* cta_busy_ns,
+                                   void* stream) {
+    return attn_fwd_impl(q, k, v, cu_seqlens_dev, mask, params, head_dim, worklist_dev, out,
+                         out_is_fp32, lse, softmax_scale, cta_busy_ns, 0, stream);
+}
+
+extern "C" pva_status pva_attn_fwd_accumulate(const void* q, const void* k, const void* v,
+                                              const int32_t* cu_seqlens_dev,
+                                              const pva_mask_desc* mask,
+                                              const pva_worklist_params* params,
+                                              int32_t head_dim, const void* worklist_dev,
+                                              float* o_run, float* lse_run, float softmax_scale,
+                                              uint64_t* cta_busy_ns, void* stream) {
+    return attn_fwd_impl(q, k, v, cu_seqlens_dev, mask, params, head_dim, worklist_dev, o_run, 1,
+                         lse_run, softmax_scale, cta_busy_ns, 1, stream);
 }
 
 extern "C" void pva_debug_withhold_kv_load(int32_t enable) {

@@ -66,5 +66,21 @@ def run_gpu(q, k, v, cu_np, mask, hq, hkv, num_ctas=0, c_tile=0, out_fp32=False,
     return out, lse, wl
 
 
+def accumulate_gpu(q, k, v, cu_np, mask, hq, hkv, o_run, lse_run, num_ctas=0, c_tile=0,
+                   scale=0.0):
+    """Build the worklist and run one fused ring step into (o_run, lse_run)."""
+    dev = torch.device("cuda")
+    cu = torch.from_numpy(np.ascontiguousarray(cu_np, dtype=np.int32)).to(dev)
+    params = api.make_params(hq, hkv, num_ctas=num_ctas, c_tile=c_tile)
+    wl = api.alloc_worklist(cu.numel() - 1, mask, params, dev)
+    api.build_worklist(cu, mask, params, wl)
+    api.attn_fwd_accumulate(q.to(dev), k.to(dev), v.to(dev), cu, mask, params, wl, o_run, lse_run,
+                            scale)
+    torch.cuda.synchronize()
+    err = api.worklist_error(wl)
+    assert err == 0, f"device error word {err}"
+    return wl
+
+
 def to_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)

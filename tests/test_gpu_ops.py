@@ -11,7 +11,7 @@ import torch
 from packed_varlen_attention_cu_gb300 import api
 from packed_varlen_attention_cu_gb300 import workloads as W
 
-from gpu_util import compare, oracle_mask, run_gpu, to_np
+from gpu_util import accumulate_gpu, compare, oracle_mask, run_gpu, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -101,10 +101,12 @@ def test_gather_scatter_roundtrip():
     assert torch.all(dst2[:5] == 0) and torch.equal(dst2[5:], src[perm[5:].long()])
 
 
-def _ring(q, k, v, cu, cp, hq, hkv, d):
+def _ring(q, k, v, cu, cp, hq, hkv, d, fused=False):
     """Zigzag CP emulation: per rank, its Q shard against the KV shard of rank
     (r - t) mod cp at ring step t, partials merged left to right; the result
-    is scattered back to global row order."""
+    is scattered back to global row order.  fused: each step merges into the
+    running (O, LSE) in the attention epilogue (pva_attn_fwd_accumulate)
+    instead of writing partials for pva_merge_partials."""
     dev = torch.device("cuda")
     T = q.shape[0]
     cu_d = torch.from_numpy(cu).to(dev)
@@ -121,6 +123,10 @@ def _ring(q, k, v, cu, cp, hq, hkv, d):
         qr = torch.empty((n, hq, d), dtype=torch.bfloat16, device=dev)
         api.gather_rows(q, maps[r], qr)
         acc_o = acc_l = None
+        if fused:
+            # never-merged running rows may hold anything: the kernel must not read them
+            acc_o = torch.full((n, hq, d), float("nan"), dtype=torch.float32, device=dev)
+            acc_l = torch.full((hq, n), float("-inf"), dtype=torch.float32, device=dev)
         for t in range(cp):
             s = (r - t) % cp
             ns = maps[s].numel()
@@ -129,6 +135,9 @@ def _ring(q, k, v, cu, cp, hq, hkv, d):
             api.gather_rows(k, maps[s], ks)
             api.gather_rows(v, maps[s], vs)
             mask = api.make_mask(W.MASK_ZIGZAG_PAIR, n, ns, cp=cp, q_rank=r, k_rank=s)
+            if fused:
+                accumulate_gpu(qr, ks, vs, cu, mask, hq, hkv, acc_o, acc_l)
+                continue
             o, l, _ = run_gpu(qr, ks, vs, cu, mask, hq, hkv, out_fp32=True)
             if acc_o is None:
                 acc_o, acc_l = o, l
@@ -142,14 +151,57 @@ def _ring(q, k, v, cu, cp, hq, hkv, d):
     return o_full, l_full
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("cp", [2, 4])
-def test_zigzag_ring_equals_unsharded(oracle_mod, cp):
+def test_zigzag_ring_equals_unsharded(oracle_mod, cp, fused):
     lengths = [900, 5, 300, 1300, 64, 1]
     cu = W.cu_seqlens_of(lengths)
     T = int(cu[-1])
     hq, hkv, d = 4, 2, 128
     q, k, v = W.make_qkv(T, T, hq, hkv, d, 31)
-    o, l = _ring(q.cuda(), k.cuda(), v.cuda(), cu, cp, hq, hkv, d)
+    o, l = _ring(q.cuda(), k.cuda(), v.cuda(), cu, cp, hq, hkv, d, fused=fused)
     ref_o, ref_l = oracle_mod.attention(oracle_mod.bf16_bits(q), oracle_mod.bf16_bits(k),
                                         oracle_mod.bf16_bits(v), cu, oracle_mask(W.MASK_CAUSAL))
     compare(to_np(o), to_np(l), ref_o, ref_l, f"ring cp={cp}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fused_step_matches_oracle_merge(oracle_mod, d):
+    """One fused ring step = oracle merge(running, oracle attention of the step).
+    The q shard of rank 0 against rank 1's kv shard has rows with no key (they
+    keep the running values); running rows with LSE -inf hold NaN, which the
+    kernel must not read."""
+    cp, qr, kr = 2, 0, 1
+    lengths = [700, 130, 1, 260]
+    cu = W.cu_seqlens_of(lengths)
+    T = int(cu[-1])
+    hq, hkv = 4, 2
+    q, k, v = W.make_qkv(T, T, hq, hkv, d, 7 + d)
+    mq = oracle_mod.zigzag_map(cu, cp, qr)[0]
+    mk = oracle_mod.zigzag_map(cu, cp, kr)[0]
+    qs, ks, vs = q[mq], k[mk], v[mk]
+    n = qs.shape[0]
+    g = torch.Generator().manual_seed(d)
+    o_run = torch.randn((n, hq, d), generator=g)
+    l_run = torch.randn((hq, n), generator=g) * 3
+    l_run[:, ::3] = -float("inf")
+    o_run[::3, :, :] = float("nan")       # rows whose LSE is -inf in every head
+    o_run0, l_run0 = o_run.double().numpy(), l_run.double().numpy()
+    o_dev, l_dev = o_run.cuda(), l_run.cuda()
+    mask = api.make_mask(W.MASK_ZIGZAG_PAIR, n, ks.shape[0], cp=cp, q_rank=qr, k_rank=kr)
+    accumulate_gpu(qs, ks, vs, cu, mask, hq, hkv, o_dev, l_dev)
+    so, sl = oracle_mod.attention(oracle_mod.bf16_bits(qs), oracle_mod.bf16_bits(ks),
+                                  oracle_mod.bf16_bits(vs), cu,
+                                  oracle_mask(W.MASK_ZIGZAG_PAIR, cp=cp, q_rank=qr, k_rank=kr))
+    assert np.isneginf(sl).any() and np.isfinite(sl).any()   # both kinds of rows occur
+    o_run0 = np.where(np.isneginf(l_run0).T[:, :, None], 0.0, o_run0)  # merge identity
+    ro, rl = oracle_mod.merge(o_run0, l_run0, so, sl)
+    got_o, got_l = to_np(o_dev), l_dev.cpu().numpy()
+    # rows without keys in this step keep their running values bit for bit
+    keep = np.isneginf(sl)
+    np.testing.assert_array_equal(got_l[keep], l_run.numpy()[keep])
+    np.testing.assert_array_equal(got_o.transpose(1, 0, 2)[keep],
+                                  o_run.double().numpy().transpose(1, 0, 2)[keep])
+    # where nothing was ever merged (LSE still -inf) O is the untouched running value
+    empty = np.isneginf(rl).T[:, :, None]
+    compare(np.where(empty, 0.0, got_o), got_l, ro, rl, f"fused step d={d}")
