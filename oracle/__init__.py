@@ -68,6 +68,14 @@ def lib():
         _lib.or_merge.argtypes = [P, P, P, P, P, P, i64, i32, i32]
         _lib.or_lpt.restype = ctypes.c_int
         _lib.or_lpt.argtypes = [P, i64, i32, P, P, P]
+        _lib.or_chunk_areas.restype = ctypes.c_int
+        _lib.or_chunk_areas.argtypes = [i32, P, i32, ctypes.POINTER(_Mask), i32, P]
+        _lib.or_dispatch_minheap.restype = ctypes.c_int
+        _lib.or_dispatch_minheap.argtypes = [P, i32, i32, P, P]
+        _lib.or_striped_map.restype = i32
+        _lib.or_striped_map.argtypes = [i32, i32, i32, i32, P]
+        _lib.or_wlb_choose.restype = ctypes.c_int
+        _lib.or_wlb_choose.argtypes = [P, i32, i32, i32, i32, P]
         _lib.or_worklist.restype = ctypes.c_int
         _lib.or_worklist.argtypes = [P, i32, ctypes.POINTER(_Mask), i32, i32, i32, i32, i32,
                                      i64, P, P, P, P, P, P, P, P]
@@ -238,3 +246,49 @@ def worklist(cu: np.ndarray, mask: Mask, tile_m: int, tile_n: int, hq: int, hkv:
     return {"slices": slices[:nsl], "segs": segs[:nseg], "units": units[:nu],
             "unit_cost": cost[:nu], "unit_pairs": pairs[:nu], "runs": runs[:nr],
             "cta_off": off, "pairs_per_head": int(counts[4])}
+
+
+# ----------------------------------------------------------- dispatch / sharding
+def chunk_areas(cu: np.ndarray, mask: Mask, chunk_size: int) -> np.ndarray:
+    """Allowed pairs of every chunk of chunk_size query rows ("03" §4.4)."""
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    T = int(cu[-1])
+    n = (T + chunk_size - 1) // chunk_size
+    areas = np.zeros(max(n, 1), dtype=np.int64)
+    m = mask.c()
+    rc = lib().or_chunk_areas(T, _ptr(cu), cu.shape[0] - 1, ctypes.byref(m), chunk_size,
+                              _ptr(areas))
+    if rc < 0:
+        raise ValueError("or_chunk_areas failed")
+    return areas[:n]
+
+
+def dispatch_minheap(areas: Sequence[int], cp: int):
+    """Greedy min-heap dispatch ("03" §4.4): (bucket [n], loads [cp])."""
+    a = np.ascontiguousarray(np.asarray(areas, dtype=np.int64))
+    n = a.shape[0]
+    bucket = np.zeros(max(n, 1), dtype=np.int32)
+    loads = np.zeros(cp, dtype=np.int64)
+    if lib().or_dispatch_minheap(_ptr(a), n, cp, _ptr(bucket), _ptr(loads)) != 0:
+        raise ValueError("or_dispatch_minheap failed")
+    return bucket[:n], loads
+
+
+def striped_map(T: int, cp: int, rank: int, stripe: int) -> np.ndarray:
+    """Tokens of `rank` under striped sharding ("03" §4.2), in order."""
+    n = lib().or_striped_map(T, cp, rank, stripe, None)
+    if n < 0:
+        raise ValueError("bad striped arguments")
+    out = np.zeros(max(n, 1), dtype=np.int32)
+    lib().or_striped_map(T, cp, rank, stripe, _ptr(out))
+    return out[:n]
+
+
+def wlb_choose(cu: np.ndarray, cp: int, tile: int, d: int):
+    """WLB-LLM per-seq vs per-doc choice ("03" §4.3): (choice, costs [2, cp])."""
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    costs = np.zeros(2 * cp, dtype=np.int64)
+    rc = lib().or_wlb_choose(_ptr(cu), cu.shape[0] - 1, cp, tile, d, _ptr(costs))
+    if rc < 0:
+        raise ValueError("or_wlb_choose failed")
+    return int(rc), costs.reshape(2, cp)

@@ -792,3 +792,156 @@ int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t ti
     free(p.sg);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Dispatch and sharding solvers ("03 · 长文负载均衡" §4.2-§4.4).              */
+/* ------------------------------------------------------------------------ */
+
+/* Mask area of equal query chunks (§4.4, MagiAttention's dispatch: the      */
+/* global sequence is cut along the query dimension into chunks of           */
+/* chunk_size rows, the last one possibly shorter; a chunk's area is the     */
+/* number of allowed query-key pairs of its rows).  Masks over the whole     */
+/* pack only (causal, sliding window, shared question).                      */
+int or_chunk_areas(int32_t T, const int32_t *cu, int32_t ndocs, const or_mask_t *m,
+                   int32_t chunk_size, int64_t *areas) {
+    if (chunk_size <= 0 || T < 0) return -1;
+    if (m->kind == OR_MASK_ZIGZAG_PAIR || m->kind == OR_MASK_SLICES) return -1;
+    ctx_t c;
+    if (ctx_init(&c, cu, ndocs, T, T, m) != 0) return -2;
+    int32_t n = (T + chunk_size - 1) / chunk_size;
+    for (int32_t k = 0; k < n; ++k) areas[k] = 0;
+    for (int32_t i = 0; i < T; ++i) {
+        int32_t lo[2], hi[2];
+        int nr = candidates(&c, i, 0, lo, hi);
+        int64_t cnt = 0;
+        for (int r = 0; r < nr; ++r)
+            for (int32_t j = lo[r]; j < hi[r]; ++j) cnt += allowed(&c, i, j);
+        areas[i / chunk_size] += cnt;
+    }
+    ctx_free(&c);
+    return n;
+}
+
+/* Greedy dispatch of n chunks into cp buckets of exactly n/cp chunks each,  */
+/* minimising the largest bucket area (§4.4): chunks are taken by area,      */
+/* largest first (equal areas: lower chunk index first); each goes to the    */
+/* bucket with the smallest area that still has room (equal areas: lower     */
+/* bucket id), the buckets kept in a binary min-heap from which a full       */
+/* bucket is removed.  bucket[n] gets each chunk's bucket, loads[cp] the     */
+/* bucket areas.                                                             */
+typedef struct {
+    int64_t area;
+    int32_t idx;
+} chunk_key_t;
+
+static int chunk_key_cmp(const void *a, const void *b) {
+    const chunk_key_t *x = (const chunk_key_t *)a, *y = (const chunk_key_t *)b;
+    if (x->area != y->area) return x->area > y->area ? -1 : 1;
+    return x->idx < y->idx ? -1 : x->idx > y->idx;
+}
+
+int or_dispatch_minheap(const int64_t *areas, int32_t n, int32_t cp, int32_t *bucket,
+                        int64_t *loads) {
+    if (cp <= 0 || n < 0 || n % cp != 0) return -1;
+    chunk_key_t *key = (chunk_key_t *)malloc(sizeof(chunk_key_t) * (size_t)(n > 0 ? n : 1));
+    for (int32_t i = 0; i < n; ++i) {
+        key[i].area = areas[i];
+        key[i].idx = i;
+    }
+    qsort(key, (size_t)n, sizeof(chunk_key_t), chunk_key_cmp);
+    bin_t *heap = (bin_t *)malloc(sizeof(bin_t) * (size_t)cp);
+    int32_t *fill = (int32_t *)calloc((size_t)cp, sizeof(int32_t));
+    for (int32_t b = 0; b < cp; ++b) {
+        heap[b].load = 0;
+        heap[b].id = b;
+    }
+    for (int32_t b = 0; b < cp; ++b) loads[b] = 0;
+    int32_t hn = cp;  /* all loads 0 and ids ascending: already a heap */
+    const int32_t cap = n / cp;
+    for (int32_t t = 0; t < n; ++t) {
+        bin_t top = heap[0];
+        bucket[key[t].idx] = top.id;
+        top.load += key[t].area;
+        if (++fill[top.id] == cap) {
+            heap[0] = heap[--hn];  /* full: leaves the heap */
+        } else {
+            heap[0] = top;
+        }
+        if (hn > 0) heap_down(heap, hn, 0);
+        loads[top.id] = top.load;
+    }
+    free(fill);
+    free(heap);
+    free(key);
+    return 0;
+}
+
+/* Striped sharding (§4.2: Striped Attention interleaves stripes of the      */
+/* whole sequence across the ranks): token i belongs to rank                 */
+/* (i / stripe) mod cp.  Writes rank r's tokens in order (map may be NULL)   */
+/* and returns their count.                                                  */
+int32_t or_striped_map(int32_t T, int32_t cp, int32_t rank, int32_t stripe, int32_t *map) {
+    if (cp <= 0 || rank < 0 || rank >= cp || stripe <= 0 || T < 0) return -1;
+    int32_t n = 0;
+    for (int32_t i = 0; i < T; ++i)
+        if ((i / stripe) % cp == rank) {
+            if (map) map[n] = i;
+            ++n;
+        }
+    return n;
+}
+
+/* Tile-rounded causal attention FLOPs of query positions [p0, p1) of one    */
+/* document (§4.1 via §4.3: a block shorter than a tile is charged a whole   */
+/* tile): q tiles of `tile` rows aligned at p0; q tile rows with last        */
+/* position P see keys [0, P], i.e. ceil((P + 1) / tile) key tiles of        */
+/* tile x tile pairs, each pair 4 d FLOPs.                                   */
+static int64_t piece_flops(int32_t p0, int32_t p1, int32_t tile, int32_t d) {
+    int64_t tiles = 0;
+    for (int32_t r = p0; r < p1; r += tile) {
+        int32_t last = r + tile < p1 ? r + tile - 1 : p1 - 1;
+        tiles += (last + 1 + tile - 1) / tile;
+    }
+    return tiles * (int64_t)tile * tile * 4 * d;
+}
+
+/* WLB-LLM's per-micro-batch choice between per-sequence and per-document    */
+/* zigzag sharding (§4.3): for each scheme, every CP worker's attention work  */
+/* in tile-rounded FLOPs; the predicted latency of a scheme is its most      */
+/* loaded worker and the smaller one wins (equal: per-sequence).             */
+/*  - per-sequence: the whole pack is cut into 2 cp chunks by the zigzag     */
+/*    chunk rule and worker r takes chunks r and 2 cp - 1 - r; each chunk's  */
+/*    pieces inside documents are charged as above (positions are document  */
+/*    positions, the causal mask never crosses documents).                   */
+/*  - per-document: every document is cut into 2 cp chunks and worker r     */
+/*    takes its chunks r and 2 cp - 1 - r.                                    */
+/* costs[2 cp]: per worker, per-sequence then per-document.  Returns 0       */
+/* (per-sequence) or 1 (per-document), -1 on bad arguments.                 */
+int or_wlb_choose(const int32_t *cu, int32_t ndocs, int32_t cp, int32_t tile, int32_t d,
+                  int64_t *costs) {
+    if (cp <= 0 || tile <= 0 || d <= 0 || ndocs < 0) return -1;
+    int32_t T = cu[ndocs];
+    for (int32_t r = 0; r < 2 * cp; ++r) costs[r] = 0;
+    for (int32_t r = 0; r < cp; ++r) {
+        int32_t chunks[2] = {r, 2 * cp - 1 - r};
+        for (int e = 0; e < 2; ++e) {
+            int32_t off, len;
+            zz_chunk(T, cp, chunks[e], &off, &len);
+            for (int32_t dd = 0; dd < ndocs; ++dd) {
+                int32_t a = off > cu[dd] ? off : cu[dd];
+                int32_t b = off + len < cu[dd + 1] ? off + len : cu[dd + 1];
+                if (a < b) costs[r] += piece_flops(a - cu[dd], b - cu[dd], tile, d);
+            }
+            for (int32_t dd = 0; dd < ndocs; ++dd) {
+                zz_chunk(cu[dd + 1] - cu[dd], cp, chunks[e], &off, &len);
+                if (len > 0) costs[cp + r] += piece_flops(off, off + len, tile, d);
+            }
+        }
+    }
+    int64_t mseq = 0, mdoc = 0;
+    for (int32_t r = 0; r < cp; ++r) {
+        if (costs[r] > mseq) mseq = costs[r];
+        if (costs[cp + r] > mdoc) mdoc = costs[cp + r];
+    }
+    return mdoc < mseq ? 1 : 0;
+}

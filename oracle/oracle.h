@@ -51,6 +51,14 @@ int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t ti
                 int64_t *unit_cost_out, int64_t *unit_pairs_out, int32_t *runs_out,
                 int32_t *cta_off_out);
 
+int or_chunk_areas(int32_t T, const int32_t *cu, int32_t ndocs, const or_mask_t *m,
+                   int32_t chunk_size, int64_t *areas);
+int or_dispatch_minheap(const int64_t *areas, int32_t n, int32_t cp, int32_t *bucket,
+                        int64_t *loads);
+int32_t or_striped_map(int32_t T, int32_t cp, int32_t rank, int32_t stripe, int32_t *map);
+int or_wlb_choose(const int32_t *cu, int32_t ndocs, int32_t cp, int32_t tile, int32_t d,
+                  int64_t *costs);
+
 #ifdef __cplusplus
 }
 #endif
