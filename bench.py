@@ -449,6 +449,67 @@ def run_zigzag(args, ctx, world, fused=False):
                     "fp32 partial attention, in-place merges; outputs stay rank-local"}
 
 
+def run_dispatch(args, ctx):
+    """Sharding solvers ("03 · 长文负载均衡" §4.2-§4.4) on this pack: device chunk
+    areas + min-heap dispatch (timed), the balance they reach against contiguous,
+    zigzag and striped chunk placement, and WLB-LLM's per-seq / per-doc choice."""
+    import torch
+
+    from packed_varlen_attention_cu_gb300 import api
+    w, q, k, v, cu_np, flops, _, base_params, hbm = ctx
+    if w.mask_kind not in (W.MASK_CAUSAL, W.MASK_SLIDING_WINDOW, W.MASK_SHARED_QUESTION):
+        return None
+    cp = w.cp or 8
+    T = w.total_tokens
+    cs = 1024
+    while ((T + cs - 1) // cs) % cp and cs > 1:
+        cs //= 2
+    n = (T + cs - 1) // cs
+    if n % cp or n > 8192:
+        return None
+    dev = q.device
+    stream = torch.cuda.current_stream()
+    cu = torch.from_numpy(cu_np).to(dev)
+    mask = api.mask_for_workload(w)
+    areas = torch.empty((n,), dtype=torch.int64, device=dev)
+    bucket = torch.empty((n,), dtype=torch.int32, device=dev)
+    loads = torch.empty((cp,), dtype=torch.int64, device=dev)
+    reps = 20
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for i in range(reps + 3):
+        if i == 3:
+            ev[0].record(stream)
+        api.chunk_areas(cu, mask, cs, areas, stream)
+        if i == 3:
+            ev[1].record(stream)
+        api.dispatch_chunks(areas, cp, bucket, loads, stream)
+        if i == 3:
+            ev[2].record(stream)
+    torch.cuda.synchronize()
+    t_areas = ev[0].elapsed_time(ev[1]) * 1e3
+    t_disp = ev[1].elapsed_time(ev[2]) * 1e3
+    a = areas.cpu().numpy()
+    mean = a.sum() / cp
+
+    def ratio(assign):
+        return round(float(np.bincount(assign, weights=a, minlength=cp).max() / mean), 4)
+
+    idx = np.arange(n)
+    zz_rank = np.where((idx * 2 * cp // n) < cp, idx * 2 * cp // n, 2 * cp - 1 - idx * 2 * cp // n)
+    choice, costs = api.wlb_choose(cu_np, cp, 128, w.head_dim)
+    return {"chunk_size": cs, "chunks": n, "cp": cp,
+            "chunk_areas_us": round(t_areas, 1), "dispatch_us": round(t_disp, 1),
+            "max_bucket_over_mean": {"minheap": ratio(bucket.cpu().numpy()),
+                                     "contiguous": ratio(idx * cp // n),
+                                     "zigzag_chunks": ratio(zz_rank),
+                                     "striped_chunks": ratio(idx % cp)},
+            "wlb": {"choice": ("per-sequence", "per-document")[choice],
+                    "max_worker_tflop": {"per_sequence": round(costs[0].max() * w.num_q_heads / 1e12, 3),
+                                         "per_document": round(costs[1].max() * w.num_q_heads / 1e12, 3)}},
+            "note": "areas = allowed pairs per query chunk; buckets hold n/cp chunks each; "
+                    "WLB costs are tile-rounded (128) FLOPs of the most loaded worker"}
+
+
 def run_libra_ratio(args, ctx):
     """Libra's example ("03 · 长文负载均衡" §1.1): the same token count as one
     40960-token document (pack A) or ten 4096-token documents (pack B); the
@@ -589,6 +650,10 @@ def main(argv=None):
     if not args.no_zigzag and ctx[0].cp:
         res["zigzag_cp"] = run_zigzag(args, ctx, world)
         res["zigzag_cp_fused"] = run_zigzag(args, ctx, world, fused=True)
+    if not args.no_zigzag:
+        disp = run_dispatch(args, ctx)
+        if disp is not None:
+            res["dispatch"] = disp
     if args.workload == "libra":
         res["libra_ratio"] = run_libra_ratio(args, ctx)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -198,6 +198,58 @@ pva_status pva_merge_partials(const void* o_a, const float* lse_a, const void* o
                               const float* lse_b, void* out, float* lse_out, int64_t tokens,
                               int32_t heads, int32_t head_dim, int32_t o_is_fp32, void* stream);
 
+/* ---- Sharding solvers for context parallelism ("03 · 长文负载均衡" §4.2-§4.4) ----
+ * They plan how the query rows of a pack are split over cp ranks; the pieces
+ * then run through pva_build_worklist / pva_attn_fwd (e.g. as AttnSlices). */
+
+/* Mask area of equal query chunks (§4.4, MagiAttention's dispatch input): the
+ * pack's rows are cut into chunks of chunk_size rows (the last one possibly
+ * shorter) and areas_dev[c] = allowed (query, key) pairs of chunk c's rows.
+ * Mask kinds over the whole pack only: PVA_MASK_CAUSAL, _SLIDING_WINDOW,
+ * _SHARED_QUESTION (mask->q_tokens = mask->k_tokens = cu_seqlens[num_docs]);
+ * others return PVA_ERR_UNSUPPORTED.
+ *   cu_seqlens_dev DEVICE int32 [num_docs + 1]
+ *   areas_dev      DEVICE int64 [ceil(q_tokens / chunk_size)], written */
+pva_status pva_chunk_areas(const int32_t* cu_seqlens_dev, int32_t num_docs,
+                           const pva_mask_desc* mask, int32_t chunk_size, int64_t* areas_dev,
+                           void* stream);
+
+/* Greedy dispatch of num_chunks chunks into cp buckets of exactly
+ * num_chunks / cp chunks each, minimising the largest bucket area (§4.4:
+ * chunks by area descending, ties by lower chunk index; each to the bucket
+ * with the smallest area that still has room, ties by lower bucket id).
+ * num_chunks must be a multiple of cp; at most 8192 chunks and 1024 buckets
+ * (PVA_ERR_UNSUPPORTED beyond).  One CTA; deterministic.
+ *   areas_dev        DEVICE int64 [num_chunks] (>= 0)
+ *   bucket_dev       DEVICE int32 [num_chunks], written: bucket of each chunk
+ *   bucket_area_dev  DEVICE int64 [cp], written: area of each bucket */
+pva_status pva_dispatch_chunks(const int64_t* areas_dev, int32_t num_chunks, int32_t cp,
+                               int32_t* bucket_dev, int64_t* bucket_area_dev, void* stream);
+
+/* Striped sharding (§4.2, Striped Attention: stripes of the whole sequence
+ * interleaved across ranks): token i belongs to rank (i / stripe) mod cp.
+ * _len is HOST computation (-1 on bad arguments); pva_striped_shard writes
+ * rank's tokens in ascending order to map_dev (DEVICE int32 [len]). */
+int32_t pva_striped_shard_len(int32_t total_tokens, int32_t cp, int32_t rank, int32_t stripe);
+pva_status pva_striped_shard(int32_t total_tokens, int32_t cp, int32_t rank, int32_t stripe,
+                             int32_t* map_dev, void* stream);
+
+/* WLB-LLM's choice between per-sequence and per-document zigzag sharding of a
+ * causal pack (§4.3): for each scheme, each of the cp workers' attention work
+ * in tile-rounded FLOPs (a piece shorter than a tile is charged whole tiles:
+ * q tiles of `tile` rows aligned at each piece start, ceil((P + 1) / tile) key
+ * tiles for a q tile whose last document position is P, 4 * head_dim FLOPs
+ * per pair of a computed tile).  Per-sequence cuts the whole pack into 2 cp
+ * zigzag chunks (worker r: chunks r and 2cp - 1 - r), per-document cuts every
+ * document that way.  HOST computation.
+ *   cu_seqlens_host HOST int32 [num_docs + 1]
+ *   costs_host      HOST int64 [2 * cp], written: per worker, per-sequence then
+ *                   per-document
+ * Returns 0 (per-sequence) or 1 (per-document): the scheme whose most loaded
+ * worker is lighter (per-sequence on ties); -1 on bad arguments. */
+int32_t pva_wlb_choose(const int32_t* cu_seqlens_host, int32_t num_docs, int32_t cp,
+                       int32_t tile, int32_t head_dim, int64_t* costs_host);
+
 /* Device error word of a worklist (0 = none; otherwise the failing wait site,
  * see PVA_ERR_TIMEOUT / PVA_ERR_DEVICE).  Synchronizes `stream`.
  *   worklist_dev DEVICE;  code_out HOST */

@@ -21,7 +21,9 @@ EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_attn
            "pva_zigzag_shard_len",
            "pva_zigzag_shard", "pva_gather_rows", "pva_merge_partials", "pva_worklist_error",
            "pva_worklist_counts", "pva_attn_fwd_noalloc", "pva_noalloc_scratch_bytes",
-           "pva_debug_withhold_kv_load", "pva_status_string", "pva_version")
+           "pva_debug_withhold_kv_load", "pva_chunk_areas", "pva_dispatch_chunks",
+           "pva_striped_shard_len", "pva_striped_shard", "pva_wlb_choose",
+           "pva_status_string", "pva_version")
 
 
 class Slice(ctypes.Structure):
@@ -90,6 +92,16 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_float, P]
         L.pva_noalloc_scratch_bytes.restype = sz
         L.pva_noalloc_scratch_bytes.argtypes = []
+        L.pva_chunk_areas.restype = ctypes.c_int
+        L.pva_chunk_areas.argtypes = [P, i32, MP, i32, P, P]
+        L.pva_dispatch_chunks.restype = ctypes.c_int
+        L.pva_dispatch_chunks.argtypes = [P, i32, i32, P, P, P]
+        L.pva_striped_shard_len.restype = i32
+        L.pva_striped_shard_len.argtypes = [i32, i32, i32, i32]
+        L.pva_striped_shard.restype = ctypes.c_int
+        L.pva_striped_shard.argtypes = [i32, i32, i32, i32, P, P]
+        L.pva_wlb_choose.restype = i32
+        L.pva_wlb_choose.argtypes = [P, i32, i32, i32, i32, P]
         L.pva_debug_withhold_kv_load.restype = None
         L.pva_debug_withhold_kv_load.argtypes = [i32]
         L.pva_status_string.restype = ctypes.c_char_p

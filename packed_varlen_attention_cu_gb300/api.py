@@ -168,6 +168,56 @@ def worklist_error(worklist: torch.Tensor, stream=None) -> int:
     return int(code.value)
 
 
+# ------------------------------------------------------ sharding solvers
+def chunk_areas(cu_seqlens: torch.Tensor, mask: MaskDesc, chunk_size: int,
+                areas: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Allowed pairs of every chunk of chunk_size query rows (device int64)."""
+    n = (mask.q_tokens + chunk_size - 1) // chunk_size
+    if areas is None:
+        areas = torch.empty((n,), dtype=torch.int64, device=cu_seqlens.device)
+    check("pva_chunk_areas", lib().pva_chunk_areas(
+        _ptr(cu_seqlens), cu_seqlens.numel() - 1, ctypes.byref(mask), chunk_size, _ptr(areas),
+        _stream(stream)))
+    return areas
+
+
+def dispatch_chunks(areas: torch.Tensor, cp: int, bucket: Optional[torch.Tensor] = None,
+                    bucket_area: Optional[torch.Tensor] = None, stream=None):
+    """Greedy min-heap dispatch: (bucket [n] int32, bucket_area [cp] int64), device."""
+    n = areas.numel()
+    if bucket is None:
+        bucket = torch.empty((max(n, 1),), dtype=torch.int32, device=areas.device)
+    if bucket_area is None:
+        bucket_area = torch.empty((cp,), dtype=torch.int64, device=areas.device)
+    check("pva_dispatch_chunks", lib().pva_dispatch_chunks(
+        _ptr(areas), n, cp, _ptr(bucket), _ptr(bucket_area), _stream(stream)))
+    return bucket[:n], bucket_area
+
+
+def striped_shard_len(total_tokens: int, cp: int, rank: int, stripe: int) -> int:
+    n = lib().pva_striped_shard_len(total_tokens, cp, rank, stripe)
+    if n < 0:
+        raise _lib.PvaError("pva_striped_shard_len", 1)
+    return int(n)
+
+
+def striped_shard(total_tokens: int, cp: int, rank: int, stripe: int, map_out: torch.Tensor,
+                  stream=None) -> None:
+    check("pva_striped_shard", lib().pva_striped_shard(
+        total_tokens, cp, rank, stripe, _ptr(map_out), _stream(stream)))
+
+
+def wlb_choose(cu_seqlens_host: np.ndarray, cp: int, tile: int, head_dim: int):
+    """(choice 0 per-sequence / 1 per-document, costs [2, cp] int64)."""
+    cu = np.ascontiguousarray(cu_seqlens_host, dtype=np.int32)
+    costs = np.zeros(2 * cp, dtype=np.int64)
+    rc = lib().pva_wlb_choose(cu.ctypes.data_as(ctypes.c_void_p), cu.shape[0] - 1, cp, tile,
+                              head_dim, costs.ctypes.data_as(ctypes.c_void_p))
+    if rc < 0:
+        raise _lib.PvaError("pva_wlb_choose", 1)
+    return int(rc), costs.reshape(2, cp)
+
+
 def debug_withhold_kv_load(enable: bool) -> None:
     """Test hook (see pva_debug_withhold_kv_load): while enabled, CTA 0 of each
     attention launch waits for a K/V copy that is never issued, so its bounded

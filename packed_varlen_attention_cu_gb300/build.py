@@ -16,7 +16,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libpva.so")
-SOURCES = ["api.cu", "worklist.cu", "attn_fwd.cu", "ops.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "worklist.cu", "attn_fwd.cu", "ops.cu", "noalloc.cu", "dispatch.cu"]
 HEADERS = ["ptx.cuh", "wl_layout.cuh", "common.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]

@@ -105,6 +105,41 @@ def test_host_argument_checks_return_codes(L):
     assert L.pva_zigzag_shard(fake, 3, 2, 5, fake, None, None) == 1
 
 
+def test_sharding_solver_host_checks(L):
+    fake = ctypes.c_void_p(256)
+    m = api.make_mask(W.MASK_CAUSAL, 128, 128)
+    # chunk areas: bad chunk size; rank-local mask kinds are not whole-pack masks
+    assert L.pva_chunk_areas(fake, 1, ctypes.byref(m), 0, fake, None) == 1
+    mz = api.make_mask(W.MASK_ZIGZAG_PAIR, 64, 64, cp=2, q_rank=0, k_rank=1)
+    assert L.pva_chunk_areas(fake, 1, ctypes.byref(mz), 16, fake, None) == 4
+    # dispatch: buckets must take whole shares; size limits
+    assert L.pva_dispatch_chunks(fake, 10, 4, fake, fake, None) == 1
+    assert L.pva_dispatch_chunks(fake, 16384, 8, fake, fake, None) == 4
+    assert L.pva_dispatch_chunks(fake, 2048, 2048, fake, fake, None) == 4
+    # striped: bad stripe / rank
+    assert L.pva_striped_shard_len(100, 4, 4, 1) == -1 and L.pva_striped_shard_len(100, 4, 0, 0) == -1
+    assert L.pva_striped_shard(100, 4, 0, 0, fake, None) == 1
+
+
+@pytest.mark.parametrize("T,cp,stripe", [(131072, 8, 1), (131072, 8, 1024), (1000, 3, 7), (5, 8, 2)])
+def test_striped_shard_len_matches_oracle(oracle_mod, T, cp, stripe):
+    lens = [api.striped_shard_len(T, cp, r, stripe) for r in range(cp)]
+    assert lens == [oracle_mod.striped_map(T, cp, r, stripe).shape[0] for r in range(cp)]
+    assert sum(lens) == T
+
+
+def test_wlb_choose_matches_oracle(oracle_mod):
+    packs = [W.zigzag_pack().cu_seqlens, W.cu_seqlens_of([64] * 64),
+             W.cu_seqlens_of([256] * 16 + [16384]), W.cu_seqlens_of([8192]),
+             W.cu_seqlens_of([70, 5, 300, 129, 1, 200])]
+    packs += [W.long_tail_gqa().cu_seqlens[:9] - 0]  # first 8 documents
+    for cu in packs:
+        for cp, tile, d in ((2, 32, 64), (4, 128, 128), (8, 128, 128)):
+            got = api.wlb_choose(cu, cp, tile, d)
+            want = oracle_mod.wlb_choose(cu, cp, tile, d)
+            assert got[0] == want[0] and np.array_equal(got[1], want[1])
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "nope.so"))
     monkeypatch.setattr(_lib, "_lib", None)
