@@ -78,7 +78,11 @@ def lib():
         _lib.or_wlb_choose.argtypes = [P, i32, i32, i32, i32, P]
         _lib.or_worklist.restype = ctypes.c_int
         _lib.or_worklist.argtypes = [P, i32, ctypes.POINTER(_Mask), i32, i32, i32, i32, i32,
-                                     i64, P, P, P, P, P, P, P, P]
+                                     i64, i32, P, P, P, P, P, P, P, P]
+        _lib.or_refine_move_swap.restype = ctypes.c_int
+        _lib.or_refine_move_swap.argtypes = [P, i64, i32, P, P, i32]
+        _lib.or_fit_tile_cost.restype = i64
+        _lib.or_fit_tile_cost.argtypes = [P, P, P, i32, P]
     return _lib
 
 
@@ -219,7 +223,7 @@ UNIT_FIELDS = ("uid", "seg", "t0", "t1", "h0", "h1", "kvh", "run_begin", "run_co
 
 
 def worklist(cu: np.ndarray, mask: Mask, tile_m: int, tile_n: int, hq: int, hkv: int,
-             num_ctas: int, c_tile: int = 0) -> dict:
+             num_ctas: int, c_tile: int = 0, refine_iters: int = 0) -> dict:
     """Worklist of the method (segments, slices, units in CTA order, runs, CSR)."""
     cu = np.ascontiguousarray(cu, dtype=np.int32)
     nd = cu.shape[0] - 1
@@ -227,7 +231,8 @@ def worklist(cu: np.ndarray, mask: Mask, tile_m: int, tile_n: int, hq: int, hkv:
     m = mask.c()
     L = lib()
     rc = L.or_worklist(_ptr(cu), nd, ctypes.byref(m), tile_m, tile_n, hq, hkv, num_ctas,
-                       int(c_tile), _ptr(counts), None, None, None, None, None, None, None)
+                       int(c_tile), int(refine_iters), _ptr(counts), None, None, None, None,
+                       None, None, None)
     if rc != 0:
         raise ValueError(f"or_worklist failed ({rc})")
     nseg, nsl, nu, nr = (int(x) for x in counts[:4])
@@ -239,7 +244,8 @@ def worklist(cu: np.ndarray, mask: Mask, tile_m: int, tile_n: int, hq: int, hkv:
     runs = np.zeros((max(nr, 1), 3), dtype=np.int32)
     off = np.zeros(num_ctas + 1, dtype=np.int32)
     rc = L.or_worklist(_ptr(cu), nd, ctypes.byref(m), tile_m, tile_n, hq, hkv, num_ctas,
-                       int(c_tile), _ptr(counts), _ptr(slices), _ptr(segs), _ptr(units),
+                       int(c_tile), int(refine_iters), _ptr(counts), _ptr(slices), _ptr(segs),
+                       _ptr(units),
                        _ptr(cost), _ptr(pairs), _ptr(runs), _ptr(off))
     if rc != 0:
         raise ValueError(f"or_worklist failed ({rc})")
@@ -292,3 +298,25 @@ def wlb_choose(cu: np.ndarray, cp: int, tile: int, d: int):
     if rc < 0:
         raise ValueError("or_wlb_choose failed")
     return int(rc), costs.reshape(2, cp)
+
+
+def refine_move_swap(cost: Sequence[int], assign: Sequence[int], bins: int, max_iters: int):
+    """Move/swap refinement after LPT ("数据并行负载均衡" §4.4 phase 2):
+    (assign [n], loads [bins], rounds applied)."""
+    c = np.ascontiguousarray(np.asarray(cost, dtype=np.int64))
+    a = np.array(assign, dtype=np.int32)
+    loads = np.zeros(bins, dtype=np.int64)
+    np.add.at(loads, a, c)
+    k = lib().or_refine_move_swap(_ptr(c), c.shape[0], bins, _ptr(a), _ptr(loads), max_iters)
+    return a, loads, int(k)
+
+
+def fit_tile_cost(P: Sequence[int], U: Sequence[int], t: Sequence[float]):
+    """Per-tile cost from per-bin times ("数据并行负载均衡" §4.2):
+    (c_tile, (g, a, c)) with t ~ g + a P + c U; c_tile = -1 if degenerate."""
+    p = np.ascontiguousarray(np.asarray(P, dtype=np.int64))
+    u = np.ascontiguousarray(np.asarray(U, dtype=np.int64))
+    tt = np.ascontiguousarray(np.asarray(t, dtype=np.float64))
+    coef = np.zeros(3, dtype=np.float64)
+    ct = lib().or_fit_tile_cost(_ptr(p), _ptr(u), _ptr(tt), p.shape[0], _ptr(coef))
+    return int(ct), tuple(float(x) for x in coef)

@@ -660,8 +660,119 @@ int or_lpt(const int64_t *cost, int64_t n, int32_t bins, int32_t *assign, int64_
 
 /* Worklist: counts first (out arrays NULL), then fill. counts[0..4] =      */
 /* segments, slices, units, runs, total pairs per head.                      */
+/* Iterative move/swap refinement after LPT ("数据并行负载均衡" §4.4, phase 2), */
+/* at most max_iters rounds.  Each round takes the most loaded bin (ties:    */
+/* lower id) and the least loaded one (ties: lower id) and stops once their */
+/* gap is under 5% of the largest load.  Candidates: move the costliest item */
+/* of the heavy bin to the light one, or swap it with the cheapest item of  */
+/* the light bin (ties between items: lower index).  The candidate leaving  */
+/* the smaller gap between the two bins is applied (a move on a tie) if it  */
+/* is smaller than the current gap; otherwise the refinement stops.         */
+/* Returns the number of rounds applied; loads are updated with assign.     */
+int or_refine_move_swap(const int64_t *cost, int64_t n, int32_t bins, int32_t *assign,
+                        int64_t *loads, int32_t max_iters) {
+    int32_t done = 0;
+    for (int32_t it = 0; it < max_iters && bins > 1; ++it) {
+        int32_t bmax = 0, bmin = 0;
+        for (int32_t b = 1; b < bins; ++b) {
+            if (loads[b] > loads[bmax]) bmax = b;
+            if (loads[b] < loads[bmin]) bmin = b;
+        }
+        int64_t gap = loads[bmax] - loads[bmin];
+        if (gap * 20 < loads[bmax] || gap == 0) break;
+        int64_t x = -1, y = -1;
+        for (int64_t u = 0; u < n; ++u) {
+            if (assign[u] == bmax && (x < 0 || cost[u] > cost[x])) x = u;
+            if (assign[u] == bmin && (y < 0 || cost[u] < cost[y])) y = u;
+        }
+        if (x < 0) break;
+        int64_t g_move = gap - 2 * cost[x];
+        if (g_move < 0) g_move = -g_move;
+        int64_t g_swap = INT64_MAX;
+        if (y >= 0) {
+            g_swap = gap - 2 * (cost[x] - cost[y]);
+            if (g_swap < 0) g_swap = -g_swap;
+        }
+        if (g_move >= gap && g_swap >= gap) break;
+        if (g_move <= g_swap) {
+            assign[x] = bmin;
+            loads[bmax] -= cost[x];
+            loads[bmin] += cost[x];
+        } else {
+            assign[x] = bmin;
+            assign[y] = bmax;
+            loads[bmax] += cost[y] - cost[x];
+            loads[bmin] += cost[x] - cost[y];
+        }
+        ++done;
+    }
+    return done;
+}
+
+/* Least-squares fit of the per-tile cost to measured per-bin times         */
+/* ("数据并行负载均衡" §4.2: the load model's coefficients are fitted to       */
+/* measured iteration times during warm-up).  Per bin b with P_b allowed     */
+/* pairs and U_b = (sub-tile, kv tile) steps + query sub-tiles:              */
+/*   t_b ~ g + a P_b + c U_b,                                                */
+/* solved from the 3x3 normal equations; c < 0 is clamped to 0 (refit of g   */
+/* and a).  coef = {g, a, c}.  Returns round(c / a), the per-tile cost in    */
+/* pair units, or -1 if a <= 0 or the system is singular.                    */
+static int solve3(double A[3][3], double y[3], double x[3]) {
+    double M[3][4];
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 3; ++j) M[i][j] = A[i][j];
+        M[i][3] = y[i];
+    }
+    for (int c = 0; c < 3; ++c) {
+        int piv = c;
+        for (int r = c + 1; r < 3; ++r)
+            if (fabs(M[r][c]) > fabs(M[piv][c])) piv = r;
+        if (fabs(M[piv][c]) < 1e-300) return -1;
+        for (int j = 0; j < 4; ++j) {
+            double t = M[c][j];
+            M[c][j] = M[piv][j];
+            M[piv][j] = t;
+        }
+        for (int r = 0; r < 3; ++r) {
+            if (r == c) continue;
+            double f = M[r][c] / M[c][c];
+            for (int j = c; j < 4; ++j) M[r][j] -= f * M[c][j];
+        }
+    }
+    for (int i = 0; i < 3; ++i) x[i] = M[i][3] / M[i][i];
+    return 0;
+}
+
+int64_t or_fit_tile_cost(const int64_t *P, const int64_t *U, const double *t, int32_t nb,
+                         double *coef) {
+    double A[3][3] = {{0}}, y[3] = {0}, x[3];
+    for (int32_t b = 0; b < nb; ++b) {
+        double f[3] = {1.0, (double)P[b], (double)U[b]};
+        for (int i = 0; i < 3; ++i) {
+            for (int j = 0; j < 3; ++j) A[i][j] += f[i] * f[j];
+            y[i] += f[i] * t[b];
+        }
+    }
+    if (solve3(A, y, x) != 0) return -1;
+    if (x[2] < 0.0) {  /* clamp c = 0: refit g and a */
+        double det = A[0][0] * A[1][1] - A[0][1] * A[1][0];
+        if (fabs(det) < 1e-300) return -1;
+        x[0] = (y[0] * A[1][1] - A[0][1] * y[1]) / det;
+        x[1] = (A[0][0] * y[1] - A[1][0] * y[0]) / det;
+        x[2] = 0.0;
+    }
+    if (coef) {
+        coef[0] = x[0];
+        coef[1] = x[1];
+        coef[2] = x[2];
+    }
+    if (!(x[1] > 0.0)) return -1;
+    return (int64_t)llround(x[2] / x[1]);
+}
+
 int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t tile_m,
                 int32_t tile_n, int32_t Hq, int32_t Hkv, int32_t num_ctas, int64_t c_tile,
+                int32_t refine_iters,
                 int64_t *counts, int32_t *slices_out, int32_t *segs_out, int32_t *units_out,
                 int64_t *unit_cost_out, int64_t *unit_pairs_out, int32_t *runs_out,
                 int32_t *cta_off_out) {
@@ -769,7 +880,10 @@ int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t ti
     int64_t *cost = (int64_t *)calloc((size_t)(nunits > 0 ? nunits : 1), sizeof(int64_t));
     int32_t *assign = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nunits > 0 ? nunits : 1));
     for (int64_t i = 0; i < nunits; ++i) cost[i] = U[i].cost;
-    or_lpt(cost, nunits, num_ctas, assign, NULL, NULL);
+    int64_t *bload = (int64_t *)calloc((size_t)num_ctas, sizeof(int64_t));
+    or_lpt(cost, nunits, num_ctas, assign, NULL, bload);
+    if (refine_iters > 0) or_refine_move_swap(cost, nunits, num_ctas, assign, bload, refine_iters);
+    free(bload);
     /* CSR: per bin, units in enumeration order */
     int32_t *fill = (int32_t *)calloc((size_t)num_ctas + 1, sizeof(int32_t));
     for (int64_t i = 0; i < nunits; ++i) fill[assign[i] + 1]++;

@@ -45,8 +45,13 @@ void or_merge(const double *oa, const double *la, const double *ob, const double
               double *l, int64_t tokens, int32_t heads, int32_t d);
 int or_lpt(const int64_t *cost, int64_t n, int32_t bins, int32_t *assign, int64_t *order,
            int64_t *loads);
+int or_refine_move_swap(const int64_t *cost, int64_t n, int32_t bins, int32_t *assign,
+                        int64_t *loads, int32_t max_iters);
+int64_t or_fit_tile_cost(const int64_t *P, const int64_t *U, const double *t, int32_t nb,
+                         double *coef);
 int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t tile_m,
                 int32_t tile_n, int32_t Hq, int32_t Hkv, int32_t num_ctas, int64_t c_tile,
+                int32_t refine_iters,
                 int64_t *counts, int32_t *slices_out, int32_t *segs_out, int32_t *units_out,
                 int64_t *unit_cost_out, int64_t *unit_pairs_out, int32_t *runs_out,
                 int32_t *cta_off_out);
