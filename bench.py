@@ -208,12 +208,35 @@ def run_pva(args, rank, world, local):
     cu = torch.from_numpy(cu_np).to(dev)
     q, k, v = W.workload_qkv(w, device=str(dev))
     mask = api.mask_for_workload(w)
-    params = api.make_params(hq, hkv, num_ctas=0, c_tile=args.c_tile)
-    wl = api.alloc_worklist(w.num_docs, mask, params, dev)
     out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
     num_ctas = torch.cuda.get_device_properties(dev).multi_processor_count
     busy = torch.zeros((num_ctas, 2), dtype=torch.int64, device=dev)
+    fit = None
+    if args.fit_cost:
+        # warm-up calibration ("数据并行负载均衡" §4.2): two runs whose worklists are
+        # balanced with different per-tile costs, per-CTA times pooled into the fit
+        cal_wl, cal_busy = [], []
+        for ct in (0, 4 * args.c_tile):
+            cp_ = api.make_params(hq, hkv, num_ctas=0, c_tile=ct)
+            cw = api.alloc_worklist(w.num_docs, mask, cp_, dev)
+            cb = torch.zeros((num_ctas, 2), dtype=torch.int64, device=dev)
+            api.build_worklist(cu, mask, cp_, cw, stream)
+            for _ in range(2):
+                api.attn_fwd(q, k, v, cu, mask, cp_, cw, out, lse, 0.0, cb, stream)
+            cal_wl.append(cw)
+            cal_busy.append(cb)
+        torch.cuda.synchronize()
+        fitted, coef = api.fit_tile_cost(cal_wl, cal_busy)
+        fit = {"default_c_tile": args.c_tile, "fitted_c_tile": fitted,
+               "ns_per_pair": coef[0], "ns_per_tile": coef[1],
+               "calibration": "warm-up: 2 runs with c_tile 0 and 4x default, per-CTA times "
+                              "fitted t = a*pairs + c*(tiles + sub-tiles), a, c >= 0"}
+        args.c_tile = fitted
+        del cal_wl, cal_busy
+    params = api.make_params(hq, hkv, num_ctas=0, c_tile=args.c_tile,
+                             refine_iters=args.refine_iters)
+    wl = api.alloc_worklist(w.num_docs, mask, params, dev)
 
     api.build_worklist(cu, mask, params, wl)
     counts = api.worklist_counts(wl)
@@ -281,7 +304,8 @@ def run_pva(args, rank, world, local):
                    "step": f"device worklist build ({n_wl_kernels} kernels) + attention forward (1 kernel)",
                    "l2": f"inputs larger than L2: Q+K+V+O+LSE = {io_bytes / 1e9:.2f} GB "
                          f"> {L2_BYTES / 1e6:.0f} MB, no flush",
-                   "num_ctas": num_ctas, "c_tile": args.c_tile,
+                   "num_ctas": num_ctas, "c_tile": args.c_tile, "c_tile_fit": fit,
+                   "refine_iters": args.refine_iters,
                    "parallelism": f"{world} independent replica(s), one per GPU"},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
@@ -297,7 +321,8 @@ def run_pva(args, rank, world, local):
         "clocks": clocks.summary(),
         "worklist_ms": round((wall_s - attn_avg_s * K) / K * 1e3, 4),
         "worklist": {"units": counts["units"], "lpt_steps": counts["lpt_steps"],
-                     "tiles_per_head": counts["tiles_per_head"]},
+                     "tiles_per_head": counts["tiles_per_head"],
+                     "refine_rounds": api.worklist_refine_rounds(wl)},
     }
     return result, (w, q, k, v, cu_np, flops, mask, params, hbm)
 
@@ -632,6 +657,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-zigzag", action="store_true")
+    ap.add_argument("--fit-cost", action="store_true",
+                    help="fit the per-tile cost to per-CTA times of two warm-up runs")
+    ap.add_argument("--refine-iters", type=int, default=20,
+                    help="move/swap rounds after LPT (0: none)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

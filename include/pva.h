@@ -100,7 +100,11 @@ typedef struct {
     int32_t tile_m, tile_n;
     int32_t num_q_heads, num_kv_heads;
     int32_t num_ctas;   /* persistent CTAs (bins of the LPT); <= 0: number of SMs */
-    int32_t reserved;
+    int32_t refine_iters; /* move/swap rounds after LPT ("数据并行负载均衡" §4.4 phase 2):
+                             the most and least loaded CTAs, stop under a 5% gap; the
+                             better of moving the heavy CTA's costliest unit or swapping it
+                             with the light CTA's cheapest one, if it shrinks their gap.
+                             0: none.  At most 1000. */
     int64_t c_tile;     /* fixed cost, in pair units (>= 0), of one computed (sub-tile, kv
                            tile) and of one query sub-tile (Q load, output rows):
                            unit cost = exact allowed pairs
@@ -249,6 +253,27 @@ pva_status pva_striped_shard(int32_t total_tokens, int32_t cp, int32_t rank, int
  * worker is lighter (per-sequence on ties); -1 on bad arguments. */
 int32_t pva_wlb_choose(const int32_t* cu_seqlens_host, int32_t num_docs, int32_t cp,
                        int32_t tile, int32_t head_dim, int64_t* costs_host);
+
+/* Fitted per-tile cost ("数据并行负载均衡" §4.2: the load model's coefficients are
+ * fitted to measured times during warm-up iterations, non-negative, with no
+ * constant term).  From num_runs pva_attn_fwd runs, each over worklists_dev[r]
+ * with cta_busy_ns recorded in cta_busy_ns_dev[r], every CTA that had work
+ * gives one sample
+ *   t_b = a * pairs_b + c * (tiles_b + subtiles_b),   a, c >= 0
+ * (its summed allowed pairs, (sub-tile, kv tile) steps and query sub-tiles),
+ * fitted by non-negative least squares over all samples.
+ * A worklist balanced by LPT makes every CTA's cost about equal, so pool runs
+ * whose worklists were built with different c_tile (e.g. 0 and a large one).
+ *   worklists_dev    HOST array [num_runs] of DEVICE worklists
+ *   cta_busy_ns_dev  HOST array [num_runs] of DEVICE uint64 [num_ctas, 2]
+ *   c_tile_out       HOST: round(c / a) (at most 2^24; 2^24 when a = 0 < c: the
+ *                    time follows tiles alone), for pva_worklist_params.c_tile
+ *   coef_out         HOST double [2] {a ns per pair, c ns per tile}, or NULL
+ * Copies the worklists' units to the host and synchronizes `stream`.
+ * PVA_ERR_INVALID_ARG if both coefficients are zero (no usable sample). */
+pva_status pva_fit_tile_cost(const void* const* worklists_dev,
+                             const uint64_t* const* cta_busy_ns_dev, int32_t num_runs,
+                             int64_t* c_tile_out, double* coef_out, void* stream);
 
 /* Device error word of a worklist (0 = none; otherwise the failing wait site,
  * see PVA_ERR_TIMEOUT / PVA_ERR_DEVICE).  Synchronizes `stream`.

@@ -313,10 +313,10 @@ def refine_move_swap(cost: Sequence[int], assign: Sequence[int], bins: int, max_
 
 def fit_tile_cost(P: Sequence[int], U: Sequence[int], t: Sequence[float]):
     """Per-tile cost from per-bin times ("数据并行负载均衡" §4.2):
-    (c_tile, (g, a, c)) with t ~ g + a P + c U; c_tile = -1 if degenerate."""
+    (c_tile, (a, c)) with t ~ a P + c U, a, c >= 0; c_tile = -1 if degenerate."""
     p = np.ascontiguousarray(np.asarray(P, dtype=np.int64))
     u = np.ascontiguousarray(np.asarray(U, dtype=np.int64))
     tt = np.ascontiguousarray(np.asarray(t, dtype=np.float64))
-    coef = np.zeros(3, dtype=np.float64)
+    coef = np.zeros(2, dtype=np.float64)
     ct = lib().or_fit_tile_cost(_ptr(p), _ptr(u), _ptr(tt), p.shape[0], _ptr(coef))
     return int(ct), tuple(float(x) for x in coef)

@@ -709,65 +709,61 @@ int or_refine_move_swap(const int64_t *cost, int64_t n, int32_t bins, int32_t *a
     return done;
 }
 
-/* Least-squares fit of the per-tile cost to measured per-bin times         */
-/* ("数据并行负载均衡" §4.2: the load model's coefficients are fitted to       */
-/* measured iteration times during warm-up).  Per bin b with P_b allowed     */
-/* pairs and U_b = (sub-tile, kv tile) steps + query sub-tiles:              */
-/*   t_b ~ g + a P_b + c U_b,                                                */
-/* solved from the 3x3 normal equations; c < 0 is clamped to 0 (refit of g   */
-/* and a).  coef = {g, a, c}.  Returns round(c / a), the per-tile cost in    */
-/* pair units, or -1 if a <= 0 or the system is singular.                    */
-static int solve3(double A[3][3], double y[3], double x[3]) {
-    double M[3][4];
-    for (int i = 0; i < 3; ++i) {
-        for (int j = 0; j < 3; ++j) M[i][j] = A[i][j];
-        M[i][3] = y[i];
-    }
-    for (int c = 0; c < 3; ++c) {
-        int piv = c;
-        for (int r = c + 1; r < 3; ++r)
-            if (fabs(M[r][c]) > fabs(M[piv][c])) piv = r;
-        if (fabs(M[piv][c]) < 1e-300) return -1;
-        for (int j = 0; j < 4; ++j) {
-            double t = M[c][j];
-            M[c][j] = M[piv][j];
-            M[piv][j] = t;
-        }
-        for (int r = 0; r < 3; ++r) {
-            if (r == c) continue;
-            double f = M[r][c] / M[c][c];
-            for (int j = c; j < 4; ++j) M[r][j] -= f * M[c][j];
-        }
-    }
-    for (int i = 0; i < 3; ++i) x[i] = M[i][3] / M[i][i];
-    return 0;
-}
+/* Non-negative least-squares fit of the per-tile cost to measured per-bin  */
+/* times ("数据并行负载均衡" §4.2: the load model a·Σlen² + b·Σlen + c·n is     */
+/* fitted to measured times with non-negative coefficients, no constant).    */
+/* Per bin b with P_b allowed pairs and U_b = (sub-tile, kv tile) steps +    */
+/* query sub-tiles:  t_b ~ a P_b + c U_b,  a, c >= 0.  With two unknowns the */
+/* exact non-negative solution is the unconstrained one if it is feasible,   */
+/* else the better (smaller residual) of (a, 0) and (0, c) fitted alone.     */
+/* coef = {a, c}.  Returns round(c / a), the per-tile cost in pair units,   */
+/* at most 2^24;                                                             */
+/* a = 0 < c (time follows tiles alone) returns 2^24; -1 if both are zero    */
+/* or there is no sample.                                                    */
+#define OR_FIT_TILE_CAP (1LL << 24)
 
 int64_t or_fit_tile_cost(const int64_t *P, const int64_t *U, const double *t, int32_t nb,
                          double *coef) {
-    double A[3][3] = {{0}}, y[3] = {0}, x[3];
+    double pp = 0, uu = 0, pu = 0, pt = 0, ut = 0, tt = 0;
     for (int32_t b = 0; b < nb; ++b) {
-        double f[3] = {1.0, (double)P[b], (double)U[b]};
-        for (int i = 0; i < 3; ++i) {
-            for (int j = 0; j < 3; ++j) A[i][j] += f[i] * f[j];
-            y[i] += f[i] * t[b];
+        double p = (double)P[b], u = (double)U[b];
+        pp += p * p;
+        uu += u * u;
+        pu += p * u;
+        pt += p * t[b];
+        ut += u * t[b];
+        tt += t[b] * t[b];
+    }
+    double a = 0, c = 0;
+    double det = pp * uu - pu * pu;
+    int ok = 0;
+    if (det > 0) {
+        a = (pt * uu - pu * ut) / det;
+        c = (pp * ut - pu * pt) / det;
+        ok = a >= 0 && c >= 0;
+    }
+    if (!ok) {
+        /* residual of t ~ x f: tt - 2 x ft + x^2 ff */
+        double a1 = pp > 0 && pt > 0 ? pt / pp : 0, c1 = uu > 0 && ut > 0 ? ut / uu : 0;
+        double r_a = tt - 2 * a1 * pt + a1 * a1 * pp;
+        double r_c = tt - 2 * c1 * ut + c1 * c1 * uu;
+        if (r_a <= r_c) {
+            a = a1;
+            c = 0;
+        } else {
+            a = 0;
+            c = c1;
         }
     }
-    if (solve3(A, y, x) != 0) return -1;
-    if (x[2] < 0.0) {  /* clamp c = 0: refit g and a */
-        double det = A[0][0] * A[1][1] - A[0][1] * A[1][0];
-        if (fabs(det) < 1e-300) return -1;
-        x[0] = (y[0] * A[1][1] - A[0][1] * y[1]) / det;
-        x[1] = (A[0][0] * y[1] - A[1][0] * y[0]) / det;
-        x[2] = 0.0;
-    }
     if (coef) {
-        coef[0] = x[0];
-        coef[1] = x[1];
-        coef[2] = x[2];
+        coef[0] = a;
+        coef[1] = c;
     }
-    if (!(x[1] > 0.0)) return -1;
-    return (int64_t)llround(x[2] / x[1]);
+    if (a > 0) {
+        double r = c / a;
+        return r >= (double)OR_FIT_TILE_CAP ? OR_FIT_TILE_CAP : (int64_t)llround(r);
+    }
+    return c > 0 ? OR_FIT_TILE_CAP : -1;
 }
 
 int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t tile_m,

@@ -23,6 +23,7 @@ EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_attn
            "pva_worklist_counts", "pva_attn_fwd_noalloc", "pva_noalloc_scratch_bytes",
            "pva_debug_withhold_kv_load", "pva_chunk_areas", "pva_dispatch_chunks",
            "pva_striped_shard_len", "pva_striped_shard", "pva_wlb_choose",
+           "pva_fit_tile_cost",
            "pva_status_string", "pva_version")
 
 
@@ -43,7 +44,7 @@ class MaskDesc(ctypes.Structure):
 class WorklistParams(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
-                ("num_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("num_ctas", ctypes.c_int32), ("refine_iters", ctypes.c_int32),
                 ("c_tile", ctypes.c_int64)]
 
 
@@ -102,6 +103,8 @@ def lib() -> ctypes.CDLL:
         L.pva_striped_shard.argtypes = [i32, i32, i32, i32, P, P]
         L.pva_wlb_choose.restype = i32
         L.pva_wlb_choose.argtypes = [P, i32, i32, i32, i32, P]
+        L.pva_fit_tile_cost.restype = ctypes.c_int
+        L.pva_fit_tile_cost.argtypes = [P, P, i32, P, P, P]
         L.pva_debug_withhold_kv_load.restype = None
         L.pva_debug_withhold_kv_load.argtypes = [i32]
         L.pva_status_string.restype = ctypes.c_char_p

@@ -62,8 +62,9 @@ def default_c_tile(head_dim: int) -> int:
 
 
 def make_params(num_q_heads: int, num_kv_heads: int, num_ctas: int = 0, c_tile: int = 0,
-                tile_m: int = TILE, tile_n: int = TILE) -> WorklistParams:
+                tile_m: int = TILE, tile_n: int = TILE, refine_iters: int = 0) -> WorklistParams:
     p = WorklistParams()
+    p.refine_iters = refine_iters
     p.tile_m, p.tile_n = tile_m, tile_n
     p.num_q_heads, p.num_kv_heads = num_q_heads, num_kv_heads
     p.num_ctas, p.c_tile = num_ctas, c_tile
@@ -166,6 +167,27 @@ def worklist_error(worklist: torch.Tensor, stream=None) -> int:
     check("pva_worklist_error", lib().pva_worklist_error(_ptr(worklist), ctypes.byref(code),
                                                          _stream(stream)))
     return int(code.value)
+
+
+def fit_tile_cost(worklists: Sequence[torch.Tensor], cta_busy: Sequence[torch.Tensor],
+                  stream=None):
+    """Per-tile cost fitted to the per-CTA times of several runs (one worklist and
+    one busy-stamp tensor per run): (c_tile, (a ns per pair, c ns per tile))."""
+    n = len(worklists)
+    assert n == len(cta_busy) and n > 0
+    wl = (ctypes.c_void_p * n)(*[w.data_ptr() for w in worklists])
+    bz = (ctypes.c_void_p * n)(*[b.data_ptr() for b in cta_busy])
+    ct = ctypes.c_int64(0)
+    coef = (ctypes.c_double * 2)()
+    check("pva_fit_tile_cost", lib().pva_fit_tile_cost(wl, bz, n, ctypes.byref(ct), coef,
+                                                       _stream(stream)))
+    return int(ct.value), (coef[0], coef[1])
+
+
+def worklist_refine_rounds(worklist: torch.Tensor) -> int:
+    """Move/swap rounds the worklist build applied after LPT (header field)."""
+    off = _HDR.itemsize + 8  # after lpt_steps and refine_iters
+    return int(np.frombuffer(worklist[off:off + 4].cpu().numpy().tobytes(), dtype="<i4")[0])
 
 
 # ------------------------------------------------------ sharding solvers

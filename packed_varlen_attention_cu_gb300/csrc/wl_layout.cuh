@@ -61,7 +61,9 @@ struct WlHeader {
     unsigned long long tile_sum;   // sum over units of sub-tiles x kv tiles
     WlOffsets off;
     int32_t lpt_steps;  // batches + runs taken by the LPT (diagnostic)
-    int32_t pad_[7];
+    int32_t refine_iters;   // move/swap rounds allowed after LPT
+    int32_t refine_rounds;  // move/swap rounds applied (diagnostic)
+    int32_t pad_[5];
 };
 static_assert(sizeof(WlHeader) <= 256, "header fits in 256 bytes");
 

@@ -18,6 +18,9 @@
 //                      enumeration order
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <climits>
+#include <cmath>
 #include <string.h>
 
 #include <algorithm>
@@ -592,6 +595,124 @@ __device__ __forceinline__ void lpt_resort(unsigned long long* S, const unsigned
     __syncthreads();
 }
 
+// Move/swap refinement after LPT ("数据并行负载均衡" §4.4, phase 2), by the
+// whole block: each round takes the most and the least loaded bins (ties:
+// lower id) and stops once their gap is under 5% of the larger load.  The
+// heavy bin's costliest unit x and the light bin's cheapest unit y (ties:
+// lower uid) are found by block-wide scans; moving x or swapping x and y,
+// whichever leaves the smaller gap between the two bins (a move on a tie), is
+// applied if it shrinks the gap, else the refinement ends.
+__device__ void lpt_refine(WlHeader* h, const WlUnit* units_enum, int32_t* assign,
+                           const unsigned long long* S, int32_t* cnt, int32_t n, int32_t B) {
+    __shared__ long long load[kMaxBins];
+    __shared__ unsigned long long rx[32], ry[32];
+    __shared__ int32_t r_bmax, r_bmin, r_go;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = (blockDim.x + 31) >> 5;
+    for (int32_t i = tid; i < B; i += blockDim.x) load[S[i] & 1023ULL] = (long long)(S[i] >> 10);
+    __syncthreads();
+    int32_t rounds = 0;
+    for (int32_t it = 0; it < h->refine_iters; ++it) {
+        if (w == 0) {
+            long long mx = LLONG_MIN, mn = LLONG_MAX;
+            int32_t bx = INT32_MAX, bn = INT32_MAX;
+            for (int32_t b = lane; b < B; b += 32) {
+                if (load[b] > mx) { mx = load[b]; bx = b; }
+                if (load[b] < mn) { mn = load[b]; bn = b; }
+            }
+            for (int o = 16; o > 0; o >>= 1) {
+                const long long omx = __shfl_xor_sync(0xffffffffu, mx, o);
+                const int32_t obx = __shfl_xor_sync(0xffffffffu, bx, o);
+                const long long omn = __shfl_xor_sync(0xffffffffu, mn, o);
+                const int32_t obn = __shfl_xor_sync(0xffffffffu, bn, o);
+                if (omx > mx || (omx == mx && obx < bx)) { mx = omx; bx = obx; }
+                if (omn < mn || (omn == mn && obn < bn)) { mn = omn; bn = obn; }
+            }
+            if (lane == 0) {
+                r_bmax = bx;
+                r_bmin = bn;
+                const long long gap = mx - mn;
+                r_go = !(gap * 20 < mx || gap == 0);
+            }
+        }
+        __syncthreads();
+        if (!r_go) break;
+        const int32_t bmax = r_bmax, bmin = r_bmin;
+        // x: max of (cost, lowest uid); y: min of (cost, lowest uid)
+        unsigned long long kx = 0, ky = ~0ULL;
+        for (int32_t u = tid; u < n; u += blockDim.x) {
+            const int32_t a = assign[u];
+            if (a != bmax && a != bmin) continue;
+            const unsigned long long c = (unsigned long long)units_enum[u].cost;
+            if (a == bmax) {
+                const unsigned long long k = (c << kUidBits) | ((1ULL << kUidBits) - 1 - u);
+                if (k > kx) kx = k;  // 0 stays "none": a real key has uid bits < 2^24 - 1 - u
+            } else {
+                const unsigned long long k = (c << kUidBits) | (unsigned long long)u;
+                if (k < ky) ky = k;
+            }
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long a = __shfl_xor_sync(0xffffffffu, kx, o);
+            const unsigned long long b = __shfl_xor_sync(0xffffffffu, ky, o);
+            if (a > kx) kx = a;
+            if (b < ky) ky = b;
+        }
+        if (lane == 0) {
+            rx[w] = kx;
+            ry[w] = ky;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            bool have_x = false;
+            unsigned long long bx = 0, by = ~0ULL;
+            for (int i = 0; i < nw; ++i) {
+                if (rx[i] > bx) bx = rx[i];
+                if (ry[i] < by) by = ry[i];
+            }
+            // a heavy bin always holds a unit (its load is positive); a key of 0
+            // would be a unit of cost 0 and uid 2^24 - 1, which the uid bound excludes
+            have_x = bx != 0;
+            r_go = 0;
+            if (have_x) {
+                const int32_t x = (int32_t)((1ULL << kUidBits) - 1 - (bx & ((1ULL << kUidBits) - 1)));
+                const long long cx = (long long)(bx >> kUidBits);
+                const long long gap = load[bmax] - load[bmin];
+                long long gm = gap - 2 * cx;
+                if (gm < 0) gm = -gm;
+                long long gs = LLONG_MAX;
+                int32_t y = -1;
+                long long cy = 0;
+                if (by != ~0ULL) {
+                    y = (int32_t)(by & ((1ULL << kUidBits) - 1));
+                    cy = (long long)(by >> kUidBits);
+                    gs = gap - 2 * (cx - cy);
+                    if (gs < 0) gs = -gs;
+                }
+                if (gm < gap || gs < gap) {
+                    if (gm <= gs) {
+                        assign[x] = bmin;
+                        load[bmax] -= cx;
+                        load[bmin] += cx;
+                        --cnt[bmax];
+                        ++cnt[bmin];
+                    } else {
+                        assign[x] = bmin;
+                        assign[y] = bmax;
+                        load[bmax] += cy - cx;
+                        load[bmin] += cx - cy;
+                    }
+                    r_go = 1;
+                }
+            }
+        }
+        __syncthreads();
+        if (!r_go) break;
+        ++rounds;
+    }
+    if (tid == 0) h->refine_rounds = rounds;
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t F) {
     WlHeader* h = reinterpret_cast<WlHeader*>(base);
     if (h->error) return;
@@ -718,6 +839,7 @@ __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t
         t += k;
     }
     if (tid == 0) h->lpt_steps = steps;
+    if (h->refine_iters > 0 && B > 1) lpt_refine(h, units_enum, assign, S, cnt, n, B);
     // CSR offsets: exclusive scan of the bin counts (warp scans + warp totals)
     int32_t inc = tid < B ? cnt[tid] : 0;
     const int32_t mine = inc;
@@ -755,7 +877,8 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
                  int32_t num_ctas, WlHeader* h) {
     if (!m || !p || num_docs < 0) return false;
     if (p->tile_m <= 0 || p->tile_n <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
-        p->num_q_heads % p->num_kv_heads != 0 || p->c_tile < 0)
+        p->num_q_heads % p->num_kv_heads != 0 || p->c_tile < 0 || p->refine_iters < 0 ||
+        p->refine_iters > 1000)
         return false;
     if (num_ctas <= 0 || num_ctas > kMaxBins) return false;
     if (m->q_tokens < 0 || m->k_tokens < 0) return false;
@@ -838,6 +961,8 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     h->cap_units = (int32_t)cap_units;
     h->cap_runs = (int32_t)std::max<int64_t>(cap_runs, 1);
     h->c_tile = p->c_tile;
+    h->refine_iters = p->refine_iters;
+    h->refine_rounds = 0;
     int64_t o = 256;
     WlOffsets& f = h->off;
     f.slices = o; o = align256(o + (int64_t)h->cap_slices * sizeof(WlSlice));
@@ -965,4 +1090,105 @@ extern "C" pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out
     out6[5] = h.hq > 0 ? (int64_t)(h.tile_sum / (unsigned long long)h.hq) : 0;
     out6[6] = h.lpt_steps;
     return h.error ? (h.error >= kErrTimeoutBase ? PVA_ERR_TIMEOUT : PVA_ERR_DEVICE) : PVA_OK;
+}
+
+namespace {
+
+constexpr int64_t kFitTileCap = 1LL << 24;  // per-tile cost when pairs carry no time
+
+// Adds one run's per-CTA samples (CTAs that had work) to the sums of the
+// two-feature normal equations: pp, uu, pu, pt, ut, tt.
+pva_status add_fit_samples(const void* worklist_dev, const uint64_t* cta_busy_ns_dev,
+                           cudaStream_t st, double sums[6]) {
+    if (!worklist_dev || !cta_busy_ns_dev) return PVA_ERR_INVALID_ARG;
+    WlHeader h;
+    if (cudaMemcpyAsync(&h, worklist_dev, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return PVA_ERR_CUDA;
+    if (h.magic != kWlMagic || h.error != 0 || h.num_ctas <= 0 || h.nunits < 0)
+        return PVA_ERR_INVALID_ARG;
+    const int32_t B = h.num_ctas, n = h.nunits;
+    std::vector<WlUnit> units((size_t)(n > 0 ? n : 1));
+    std::vector<uint64_t> busy(2 * (size_t)B);
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(worklist_dev);
+    if ((n > 0 && cudaMemcpyAsync(units.data(), base + h.off.units, (size_t)n * sizeof(WlUnit),
+                                  cudaMemcpyDeviceToHost, st) != cudaSuccess) ||
+        cudaMemcpyAsync(busy.data(), cta_busy_ns_dev, busy.size() * sizeof(uint64_t),
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return PVA_ERR_CUDA;
+    // per CTA: allowed pairs, (sub-tile, kv tile) steps + sub-tiles, busy time
+    std::vector<int64_t> P(B, 0), U(B, 0), cntu(B, 0);
+    for (int32_t i = 0; i < n; ++i) {
+        const WlUnit& u = units[i];
+        if (u.cta < 0 || u.cta >= B) return PVA_ERR_INVALID_ARG;
+        const int64_t nsub = u.h1 >= 0 ? 2 : 1;
+        P[u.cta] += u.pairs;
+        U[u.cta] += nsub * ((int64_t)u.ntiles + 1);
+        ++cntu[u.cta];
+    }
+    for (int32_t b = 0; b < B; ++b) {
+        if (cntu[b] == 0) continue;  // CTAs without units return at once
+        const double t = (double)(busy[2 * b + 1] - busy[2 * b]);
+        const double p = (double)P[b], u = (double)U[b];
+        sums[0] += p * p;
+        sums[1] += u * u;
+        sums[2] += p * u;
+        sums[3] += p * t;
+        sums[4] += u * t;
+        sums[5] += t * t;
+    }
+    return PVA_OK;
+}
+
+}  // namespace
+
+extern "C" pva_status pva_fit_tile_cost(const void* const* worklists_dev,
+                                        const uint64_t* const* cta_busy_ns_dev, int32_t num_runs,
+                                        int64_t* c_tile_out, double* coef_out, void* stream) {
+    if (!worklists_dev || !cta_busy_ns_dev || !c_tile_out || num_runs <= 0)
+        return PVA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    double sm[6] = {0, 0, 0, 0, 0, 0};
+    for (int32_t r = 0; r < num_runs; ++r) {
+        const pva_status s = add_fit_samples(worklists_dev[r], cta_busy_ns_dev[r], st, sm);
+        if (s != PVA_OK) return s;
+    }
+    const double pp = sm[0], uu = sm[1], pu = sm[2], pt = sm[3], ut = sm[4], tt = sm[5];
+    // non-negative least squares in two unknowns: the unconstrained solution if
+    // feasible, else the better of the two one-feature fits
+    double a = 0, c = 0;
+    const double det = pp * uu - pu * pu;
+    bool ok = false;
+    if (det > 0) {
+        a = (pt * uu - pu * ut) / det;
+        c = (pp * ut - pu * pt) / det;
+        ok = a >= 0 && c >= 0;
+    }
+    if (!ok) {
+        const double a1 = pp > 0 && pt > 0 ? pt / pp : 0, c1 = uu > 0 && ut > 0 ? ut / uu : 0;
+        const double r_a = tt - 2 * a1 * pt + a1 * a1 * pp;
+        const double r_c = tt - 2 * c1 * ut + c1 * c1 * uu;
+        if (r_a <= r_c) {
+            a = a1;
+            c = 0;
+        } else {
+            a = 0;
+            c = c1;
+        }
+    }
+    if (coef_out) {
+        coef_out[0] = a;
+        coef_out[1] = c;
+    }
+    if (a > 0) {
+        const double r = c / a;
+        *c_tile_out = r >= (double)kFitTileCap ? kFitTileCap : (int64_t)std::llround(r);
+        return PVA_OK;
+    }
+    if (c > 0) {
+        *c_tile_out = kFitTileCap;
+        return PVA_OK;
+    }
+    return PVA_ERR_INVALID_ARG;
 }

@@ -146,3 +146,90 @@ def test_worklist_single_cta_and_zero_costs(oracle_mod):
         o = oracle_mod.worklist(cu, oracle_mask(W.MASK_ZIGZAG_PAIR, cp=8, q_rank=0, k_rank=7),
                                 128, 128, 32, 8, nc, 0)
         _assert_same(g, o)
+
+
+REFINE_CASES = [
+    ("tiny", lambda: W.tiny_pack()),
+    ("shared question", lambda: W.shared_question()),
+    ("libra pair", lambda: W.libra_pair()),
+    ("long-tail 2 packs GQA 7:1", lambda: W.long_tail_gqa(2)),
+]
+
+
+@pytest.mark.parametrize("name,mk", REFINE_CASES, ids=[c[0] for c in REFINE_CASES])
+@pytest.mark.parametrize("num_ctas,c_tile", [(16, 0), (40, 4096), (152, 32768), (3, 0)])
+def test_worklist_refinement_bit_exact(oracle_mod, name, mk, num_ctas, c_tile):
+    """Move/swap rounds after LPT ("数据并行负载均衡" §4.4 phase 2) on the device
+    give the oracle's worklist, and apply as many rounds as the oracle's own
+    LPT + refinement of the unit costs."""
+    w = mk()
+    cu = w.cu_seqlens
+    mask = api.mask_for_workload(w)
+    dev = torch.device("cuda")
+    cu_d = torch.from_numpy(np.ascontiguousarray(cu, dtype=np.int32)).to(dev)
+    params = api.make_params(w.num_q_heads, w.num_kv_heads, num_ctas=num_ctas, c_tile=c_tile,
+                             refine_iters=20)
+    wl = api.alloc_worklist(cu_d.numel() - 1, mask, params, dev)
+    api.build_worklist(cu_d, mask, params, wl)
+    torch.cuda.synchronize()
+    assert api.worklist_error(wl) == 0
+    g = api.decode_worklist(wl)
+    om = oracle_mask(w.mask_kind, w.window, w.num_prefix_docs)
+    o = oracle_mod.worklist(cu, om, 128, 128, w.num_q_heads, w.num_kv_heads, num_ctas, c_tile,
+                            refine_iters=20)
+    _assert_same(g, o)
+    # rounds: LPT of the enumeration-order costs, then the refinement
+    plain = oracle_mod.worklist(cu, om, 128, 128, w.num_q_heads, w.num_kv_heads, num_ctas, c_tile)
+    cost = np.zeros(len(plain["units"]), dtype=np.int64)
+    cost[plain["units"][:, 0]] = plain["unit_cost"]
+    assign, _, _ = oracle_mod.lpt(cost, num_ctas)
+    _, _, rounds = oracle_mod.refine_move_swap(cost, assign, num_ctas, 20)
+    assert api.worklist_refine_rounds(wl) == rounds
+
+
+def test_fit_tile_cost_matches_oracle(oracle_mod):
+    """The per-tile cost fitted to per-CTA times ("数据并行负载均衡" §4.2), pooled
+    over two runs whose worklists were balanced with different per-tile costs:
+    the device aggregates and fit equal the oracle's on the same stamps."""
+    w = W.long_tail_gqa(2)
+    cu = w.cu_seqlens
+    dev = torch.device("cuda")
+    cu_d = torch.from_numpy(cu).to(dev)
+    mask = api.mask_for_workload(w)
+    q, k, v = W.workload_qkv(w, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty((w.num_q_heads, w.total_tokens), dtype=torch.float32, device=dev)
+    nc = torch.cuda.get_device_properties(0).multi_processor_count
+    wls, busys, Ps, Us, ts = [], [], [], [], []
+    for c_tile in (0, 65536):
+        params = api.make_params(w.num_q_heads, w.num_kv_heads, num_ctas=0, c_tile=c_tile)
+        wl = api.alloc_worklist(w.num_docs, mask, params, dev)
+        api.build_worklist(cu_d, mask, params, wl)
+        busy = torch.zeros(2 * nc, dtype=torch.int64, device=dev)
+        for _ in range(2):
+            api.attn_fwd(q, k, v, cu_d, mask, params, wl, out, lse, 0.0, busy)
+        torch.cuda.synchronize()
+        wls.append(wl)
+        busys.append(busy)
+        # oracle side: the same worklist from the oracle, the same stamps
+        o = oracle_mod.worklist(cu, oracle_mask(w.mask_kind), 128, 128, w.num_q_heads,
+                                w.num_kv_heads, nc, c_tile)
+        units = o["units"]
+        ntiles = np.array([sum(int(r[2] - r[1]) for r in o["runs"][u[7]:u[7] + u[8]])
+                           for u in units], dtype=np.int64)
+        nsub = np.where(units[:, 5] >= 0, 2, 1)
+        P = np.zeros(nc, dtype=np.int64)
+        U = np.zeros(nc, dtype=np.int64)
+        np.add.at(P, units[:, 9], o["unit_pairs"])
+        np.add.at(U, units[:, 9], nsub * (ntiles + 1))
+        b = busy.cpu().numpy().reshape(-1, 2)
+        has = np.bincount(units[:, 9], minlength=nc) > 0
+        Ps.append(P[has])
+        Us.append(U[has])
+        ts.append((b[has, 1] - b[has, 0]).astype(np.float64))
+    ct, coef = api.fit_tile_cost(wls, busys)
+    oct_, ocoef = oracle_mod.fit_tile_cost(np.concatenate(Ps), np.concatenate(Us),
+                                           np.concatenate(ts))
+    assert ct == oct_
+    np.testing.assert_allclose(coef, ocoef, rtol=1e-9, atol=1e-12)
+    assert 0 <= ct <= 1 << 24 and max(coef) > 0 and min(coef) >= 0
