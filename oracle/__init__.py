@@ -60,6 +60,9 @@ def lib():
         _lib.or_attention.restype = ctypes.c_int
         _lib.or_attention.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, i32,
                                       ctypes.POINTER(_Mask), ctypes.c_double, P, i64, i32, P, P]
+        _lib.or_attention_bwd.restype = ctypes.c_int
+        _lib.or_attention_bwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, i32,
+                                          ctypes.POINTER(_Mask), ctypes.c_double, P, P, P]
         _lib.or_pair_count.restype = i64
         _lib.or_pair_count.argtypes = [i32, i32, P, i32, ctypes.POINTER(_Mask), i32]
         _lib.or_allowed_matrix.restype = ctypes.c_int
@@ -165,6 +168,31 @@ def attention(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, cu: np
     if rc != 0:
         raise ValueError(f"or_attention failed ({rc})")
     return out, lse
+
+
+def attention_bwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
+                  do_bits: np.ndarray, cu: np.ndarray, mask: Mask, scale: Optional[float] = None):
+    """fp64 gradients (dq [Tq, Hq, d], dk, dv [Tk, Hkv, d]) of attention with
+    output gradient dO, from bf16 bit patterns.  Brute force: O(Tq Tk Hq d)."""
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    do_bits = np.ascontiguousarray(do_bits, dtype=np.uint16)
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    Tq, Hq, d = q_bits.shape
+    Tk, Hkv, _ = k_bits.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.zeros((Tq, Hq, d), dtype=np.float64)
+    dk = np.zeros((Tk, Hkv, d), dtype=np.float64)
+    dv = np.zeros((Tk, Hkv, d), dtype=np.float64)
+    m = mask.c()
+    rc = lib().or_attention_bwd(_ptr(q_bits), _ptr(k_bits), _ptr(v_bits), _ptr(do_bits), Tq, Tk,
+                                Hq, Hkv, d, _ptr(cu), cu.shape[0] - 1, ctypes.byref(m),
+                                float(scale), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"or_attention_bwd failed ({rc})")
+    return dq, dk, dv
 
 
 def pair_count(cu: np.ndarray, mask: Mask, Tq: Optional[int] = None, Tk: Optional[int] = None,

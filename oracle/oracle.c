@@ -325,6 +325,129 @@ int or_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, int32_
     return err ? -3 : 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Attention backward, by definition, in fp64 from bf16 inputs and the bf16  */
+/* output gradient dO.  With A(i) the allowed keys of row i, s_ij =          */
+/* scale q_i.k_j, P_ij = exp(s_ij - LSE_i) (the forward's probabilities):    */
+/*   dP_ij = dO_i . v_j,   D_i = sum_{j in A(i)} P_ij dP_ij  (= dO_i . O_i), */
+/*   dS_ij = P_ij (dP_ij - D_i),                                             */
+/*   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,            */
+/*   dV_j = sum_i P_ij dO_i,                                                 */
+/* the gradients of the quadratic term of [P1] §1.1 (QK^T and PV); a kv head */
+/* sums over the q heads of its group.  Rows with no key get no gradient.    */
+/* dK and dV are gathered key by key over all query rows (brute force).      */
+/* ------------------------------------------------------------------------ */
+int or_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const uint16_t *dout, int32_t Tq, int32_t Tk, int32_t Hq, int32_t Hkv,
+                     int32_t d, const int32_t *cu, int32_t ndocs, const or_mask_t *m,
+                     double scale, double *dq, double *dk, double *dv) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    ctx_t c;
+    if (ctx_init(&c, cu, ndocs, Tq, Tk, m) != 0) return -2;
+    const int32_t G = Hq / Hkv;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)Tq * Hq + 1);
+    double *Dv = (double *)malloc(sizeof(double) * (size_t)Tq * Hq + 1);
+    /* pass 1, per (row, head): LSE, D and dQ */
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Tk > 0 ? Tk : 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(Tk > 0 ? Tk : 1));
+        int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (size_t)(Tk > 0 ? Tk : 1));
+        double *qi = (double *)malloc(sizeof(double) * (size_t)d);
+        double *gi = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t job = 0; job < (int64_t)Tq * Hq; ++job) {
+            const int32_t i = (int32_t)(job / Hq), h = (int32_t)(job % Hq), g = h / G;
+            for (int32_t e = 0; e < d; ++e) {
+                qi[e] = bf16_to_double(q[((int64_t)i * Hq + h) * d + e]);
+                gi[e] = bf16_to_double(dout[((int64_t)i * Hq + h) * d + e]);
+            }
+            double *dqi = dq + ((int64_t)i * Hq + h) * d;
+            for (int32_t e = 0; e < d; ++e) dqi[e] = 0.0;
+            int32_t cnt = 0;
+            double mx = -INFINITY;
+            for (int32_t j = 0; j < Tk; ++j) {
+                if (!allowed(&c, i, j)) continue;
+                const uint16_t *kj = k + ((int64_t)j * Hkv + g) * d;
+                const uint16_t *vj = v + ((int64_t)j * Hkv + g) * d;
+                double dot = 0.0, dd = 0.0;
+                for (int32_t e = 0; e < d; ++e) {
+                    dot += qi[e] * bf16_to_double(kj[e]);
+                    dd += gi[e] * bf16_to_double(vj[e]);
+                }
+                s[cnt] = scale * dot;
+                dp[cnt] = dd;
+                idx[cnt] = j;
+                if (s[cnt] > mx) mx = s[cnt];
+                ++cnt;
+            }
+            if (cnt == 0) {
+                lse[job] = -INFINITY;
+                Dv[job] = 0.0;
+                continue;
+            }
+            double sum = 0.0;
+            for (int32_t t = 0; t < cnt; ++t) sum += exp(s[t] - mx);
+            const double l = mx + log(sum);
+            double D = 0.0;
+            for (int32_t t = 0; t < cnt; ++t) D += exp(s[t] - l) * dp[t];
+            lse[job] = l;
+            Dv[job] = D;
+            for (int32_t t = 0; t < cnt; ++t) {
+                const double ds = exp(s[t] - l) * (dp[t] - D);
+                const uint16_t *kj = k + ((int64_t)idx[t] * Hkv + g) * d;
+                for (int32_t e = 0; e < d; ++e) dqi[e] += scale * ds * bf16_to_double(kj[e]);
+            }
+        }
+        free(s);
+        free(dp);
+        free(idx);
+        free(qi);
+        free(gi);
+    }
+    /* pass 2, per (key, kv head): dK and dV over every query row of the group */
+#pragma omp parallel
+    {
+        double *kj = (double *)malloc(sizeof(double) * (size_t)d);
+        double *vj = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t job = 0; job < (int64_t)Tk * Hkv; ++job) {
+            const int32_t j = (int32_t)(job / Hkv), g = (int32_t)(job % Hkv);
+            for (int32_t e = 0; e < d; ++e) {
+                kj[e] = bf16_to_double(k[((int64_t)j * Hkv + g) * d + e]);
+                vj[e] = bf16_to_double(v[((int64_t)j * Hkv + g) * d + e]);
+            }
+            double *dkj = dk + ((int64_t)j * Hkv + g) * d;
+            double *dvj = dv + ((int64_t)j * Hkv + g) * d;
+            for (int32_t e = 0; e < d; ++e) dkj[e] = dvj[e] = 0.0;
+            for (int32_t i = 0; i < Tq; ++i) {
+                if (!allowed(&c, i, j)) continue;
+                for (int32_t h = g * G; h < (g + 1) * G; ++h) {
+                    const int64_t r = (int64_t)i * Hq + h;
+                    const uint16_t *qi = q + r * d, *gi = dout + r * d;
+                    double dot = 0.0, dd = 0.0;
+                    for (int32_t e = 0; e < d; ++e) {
+                        dot += bf16_to_double(qi[e]) * kj[e];
+                        dd += bf16_to_double(gi[e]) * vj[e];
+                    }
+                    const double p = exp(scale * dot - lse[r]);
+                    const double ds = p * (dd - Dv[r]);
+                    for (int32_t e = 0; e < d; ++e) {
+                        dkj[e] += scale * ds * bf16_to_double(qi[e]);
+                        dvj[e] += p * bf16_to_double(gi[e]);
+                    }
+                }
+            }
+        }
+        free(kj);
+        free(vj);
+    }
+    free(lse);
+    free(Dv);
+    ctx_free(&c);
+    return 0;
+}
+
 /* Number of allowed (q row, k row) pairs, per head.  [P1] §1.1: this is     */
 /* the work term W_attn ~ sum_j l_j^2 of a pack.                             */
 int64_t or_pair_count(int32_t Tq, int32_t Tk, const int32_t *cu, int32_t ndocs,
