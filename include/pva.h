@@ -202,6 +202,50 @@ pva_status pva_merge_partials(const void* o_a, const float* lse_a, const void* o
                               const float* lse_b, void* out, float* lse_out, int64_t tokens,
                               int32_t heads, int32_t head_dim, int32_t o_is_fp32, void* stream);
 
+/* ---- Backward ("03 · 长文负载均衡" §1.1: gradients of the QK^T and PV terms) ----
+ * With P = exp(scale S - LSE) recomputed from the forward's LSE:
+ *   dP = dO V^T, D = rowsum(dO * O), dS = P (dP - D),
+ *   dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO (a kv head sums its group).
+ * dQ runs over the forward worklist (same units and CTA lists); dK and dV run
+ * over a backward plan of kv-major units: slices with the same key range form
+ * a key group, and a unit is one 128-key tile of a group for one kv head,
+ * covering every q tile of every slice of the group and every head of the kv
+ * head's group that may see the tile's keys, accumulated in tensor memory
+ * (each output row has one writer; results are deterministic).  Explicit
+ * slices whose key ranges overlap without being equal, or more than 8192
+ * slices, have no plan (0 bytes). */
+
+/* Size of the backward plan (HOST computation; 0 if unsupported or invalid).
+ * It also holds the D scratch, [num_q_heads, q_tokens] fp32. */
+size_t pva_bwd_plan_bytes(int32_t num_docs, const pva_mask_desc* mask,
+                          const pva_worklist_params* params);
+
+/* Build the backward plan on the device from a built forward worklist of the
+ * same problem: kv-major units, their cost (q-tile steps over the group's
+ * heads + 1), sorted by cost descending; CTAs take them in snake order.
+ *   worklist_dev DEVICE (pva_build_worklist output);  plan_dev DEVICE, 256-B
+ *   aligned, plan_bytes >= pva_bwd_plan_bytes() */
+pva_status pva_build_bwd_plan(const void* worklist_dev, int32_t num_docs,
+                              const pva_mask_desc* mask, const pva_worklist_params* params,
+                              void* plan_dev, size_t plan_bytes, void* stream);
+
+/* Attention backward over the forward worklist and the backward plan.
+ *   q, k, v        DEVICE bf16, as for pva_attn_fwd
+ *   out, lse       DEVICE: the forward's bf16 output and fp32 LSE [Hq, q_tokens]
+ *   dout           DEVICE bf16 [q_tokens, Hq, head_dim]
+ *   dq             DEVICE [q_tokens, Hq, head_dim], dk/dv DEVICE [k_tokens, Hkv,
+ *                  head_dim]; bf16 (grads_are_fp32 = 0) or fp32 (= 1); written
+ *                  (rows no slice reaches get 0)
+ *   softmax_scale  <= 0 selects 1/sqrt(head_dim)
+ * Four kernels on `stream` (D, dQ, dK/dV); device failures go to the forward
+ * worklist's error word. */
+pva_status pva_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, const int32_t* cu_seqlens_dev,
+                        int32_t num_docs, const pva_mask_desc* mask,
+                        const pva_worklist_params* params, int32_t head_dim,
+                        const void* worklist_dev, void* plan_dev, void* dq, void* dk, void* dv,
+                        int32_t grads_are_fp32, float softmax_scale, void* stream);
+
 /* ---- Sharding solvers for context parallelism ("03 · 长文负载均衡" §4.2-§4.4) ----
  * They plan how the query rows of a pack are split over cp ranks; the pieces
  * then run through pva_build_worklist / pva_attn_fwd (e.g. as AttnSlices). */

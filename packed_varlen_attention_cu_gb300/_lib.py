@@ -24,6 +24,7 @@ EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_attn
            "pva_debug_withhold_kv_load", "pva_chunk_areas", "pva_dispatch_chunks",
            "pva_striped_shard_len", "pva_striped_shard", "pva_wlb_choose",
            "pva_fit_tile_cost",
+           "pva_bwd_plan_bytes", "pva_build_bwd_plan", "pva_attn_bwd",
            "pva_status_string", "pva_version")
 
 
@@ -105,6 +106,13 @@ def lib() -> ctypes.CDLL:
         L.pva_wlb_choose.argtypes = [P, i32, i32, i32, i32, P]
         L.pva_fit_tile_cost.restype = ctypes.c_int
         L.pva_fit_tile_cost.argtypes = [P, P, i32, P, P, P]
+        L.pva_bwd_plan_bytes.restype = sz
+        L.pva_bwd_plan_bytes.argtypes = [i32, MP, WP]
+        L.pva_build_bwd_plan.restype = ctypes.c_int
+        L.pva_build_bwd_plan.argtypes = [P, i32, MP, WP, P, sz, P]
+        L.pva_attn_bwd.restype = ctypes.c_int
+        L.pva_attn_bwd.argtypes = [P, P, P, P, P, P, P, i32, MP, WP, i32, P, P, P, P, P, i32,
+                                   ctypes.c_float, P]
         L.pva_debug_withhold_kv_load.restype = None
         L.pva_debug_withhold_kv_load.argtypes = [i32]
         L.pva_status_string.restype = ctypes.c_char_p

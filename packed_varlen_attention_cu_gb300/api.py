@@ -190,6 +190,41 @@ def worklist_refine_rounds(worklist: torch.Tensor) -> int:
     return int(np.frombuffer(worklist[off:off + 4].cpu().numpy().tobytes(), dtype="<i4")[0])
 
 
+# ------------------------------------------------------ backward
+def bwd_plan_bytes(num_docs: int, mask: MaskDesc, params: WorklistParams) -> int:
+    n = lib().pva_bwd_plan_bytes(num_docs, ctypes.byref(mask), ctypes.byref(params))
+    if n == 0:
+        raise _lib.PvaError("pva_bwd_plan_bytes", 4)
+    return int(n)
+
+
+def alloc_bwd_plan(num_docs: int, mask: MaskDesc, params: WorklistParams,
+                   device="cuda") -> torch.Tensor:
+    return torch.empty(bwd_plan_bytes(num_docs, mask, params), dtype=torch.uint8, device=device)
+
+
+def build_bwd_plan(worklist: torch.Tensor, num_docs: int, mask: MaskDesc,
+                   params: WorklistParams, plan: torch.Tensor, stream=None) -> None:
+    check("pva_build_bwd_plan", lib().pva_build_bwd_plan(
+        _ptr(worklist), num_docs, ctypes.byref(mask), ctypes.byref(params), _ptr(plan),
+        plan.numel(), _stream(stream)))
+
+
+def attn_bwd(q, k, v, out, lse, dout, cu_seqlens: Optional[torch.Tensor], num_docs: int,
+             mask: MaskDesc, params: WorklistParams, worklist: torch.Tensor, plan: torch.Tensor,
+             dq: torch.Tensor, dk: torch.Tensor, dv: torch.Tensor, softmax_scale: float = 0.0,
+             stream=None) -> None:
+    """Gradients into dq [Tq, Hq, d], dk/dv [Tk, Hkv, d] (all bf16 or all fp32)."""
+    for t in (q, k, v, out, lse, dout, dq, dk, dv):
+        assert t.is_cuda and t.is_contiguous()
+    assert dq.dtype == dk.dtype == dv.dtype and dq.dtype in (torch.bfloat16, torch.float32)
+    check("pva_attn_bwd", lib().pva_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(cu_seqlens), num_docs,
+        ctypes.byref(mask), ctypes.byref(params), q.shape[-1], _ptr(worklist), _ptr(plan),
+        _ptr(dq), _ptr(dk), _ptr(dv), 1 if dq.dtype == torch.float32 else 0,
+        float(softmax_scale), _stream(stream)))
+
+
 # ------------------------------------------------------ sharding solvers
 def chunk_areas(cu_seqlens: torch.Tensor, mask: MaskDesc, chunk_size: int,
                 areas: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

@@ -1,0 +1,830 @@
+// attn_bwd.cu -- backward of the packed document-masked attention on sm_103a.
+//
+// The gradients of the quadratic term of "03 · 长文负载均衡" §1.1 (QK^T and
+// PV) over the same AttnSlices as the forward.  With P = exp(scale S - LSE)
+// recomputed from the forward's LSE:
+//   dP = dO V^T,  D = rowsum(dO * O),  dS = P (dP - D),
+//   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+// Three kernels, no atomics (each output row has one writer):
+//   bwd_pre   D per (row, head), HBM-bound;
+//   bwd_dq    q-major over the forward worklist (its LPT-balanced CTA lists):
+//             per query sub-tile, every kv tile of its runs: S and dP (two SS
+//             MMAs), then dS in the softmax warps, then dQ += dS K (TS MMA);
+//   bwd_dkdv  kv-major over the backward plan: per 128-key tile of one key
+//             group (the slices sharing a key range) and one kv head, every q
+//             tile of every slice of the group and every head: S^T = K Q^T and
+//             dP^T = V dO^T, then P^T and dS^T, then dV += P^T dO and
+//             dK += dS^T Q, accumulated in tensor memory over the group.
+// Tensor-memory columns: bwd_dq S [0,128) dP [128,256) dQ [256,256+d);
+// bwd_dkdv S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d,256+2d).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/pva.h"
+#include "common.h"
+#include "ptx.cuh"
+#include "tma_map.h"
+#include "wl_layout.cuh"
+
+namespace pva {
+namespace {
+
+constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 4-7 element-wise + epilogue
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 200000000ull;
+
+template <int D>
+struct BCfg {
+    static constexpr int kTileBytes = 128 * D * 2;
+    // bwd_dq: Q, dO, then a K/V ring; bwd_dkdv: K, V, then a (Q, dO) ring
+    static constexpr int kStages = D == 128 ? 4 : 8;
+    static constexpr int kSmem = 2 * kTileBytes + kStages * kTileBytes + 1024;
+    static constexpr uint32_t kIdescNT = idesc_bf16_f32(128, 128, false);  // A, B K-major
+    static constexpr uint32_t kIdescNN = idesc_bf16_f32(128, D, true);     // B MN-major
+};
+
+struct BwdParams {
+    const uint8_t* wl;
+    const uint8_t* plan;
+    const void* out;     // forward output O, bf16 [Tq, Hq, d]
+    const void* dout;    // dO, bf16 [Tq, Hq, d]
+    const float* lse;    // forward LSE (natural log) [Hq, Tq]
+    float* dvec;         // D [Hq, Tq]
+    void* dq;            // [Tq, Hq, d]
+    void* dk;            // [Tk, Hkv, d]
+    void* dv;            // [Tk, Hkv, d]
+    int32_t q_tokens, k_tokens, hq, hkv, grads_fp32, num_ctas, d;
+    float scale, scale_log2;
+};
+
+struct BShared {
+    uint64_t a_full, a_empty, s_full, p_full, o_full, o_empty, done;
+    uint64_t r_full[8], r_empty[8];
+    uint32_t tmem_base;
+    int32_t abort_flag;
+};
+
+// ------------------------------------------------------------ D = rowsum(dO O)
+// 8 threads per (row, head), 16 bytes each per step.
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
+    const int64_t rows = (int64_t)p.q_tokens * p.hq;
+    const int sub = threadIdx.x & 7;
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 3;
+         r - (threadIdx.x & 31) / 8 < rows; r += ((int64_t)gridDim.x * blockDim.x) >> 3) {
+        float acc = 0.f;
+        if (r < rows) {
+            const uint4* o = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const __nv_bfloat16*>(p.out) + r * p.d);
+            const uint4* g = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const __nv_bfloat16*>(p.dout) + r * p.d);
+            for (int c = sub; c < p.d / 8; c += 8) {
+                const uint4 a = o[c], b = g[c];
+                const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+                    const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[e]));
+                    acc += fa.x * fb.x + fa.y * fb.y;
+                }
+            }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        if (r < rows && sub == 0) {
+            const int64_t t = r / p.hq;
+            const int32_t h = (int32_t)(r - t * p.hq);
+            p.dvec[(int64_t)h * p.q_tokens + t] = acc;
+        }
+    }
+}
+
+// Writes 32 fp32 accumulator columns of one row, scaled, as fp32 or bf16.
+__device__ __forceinline__ void store_row32(void* base, int64_t row_elem, bool fp32,
+                                            const uint32_t (&v)[32], float scale) {
+    if (fp32) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + row_elem);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(v[4 * e]) * scale, __uint_as_float(v[4 * e + 1]) * scale,
+                                 __uint_as_float(v[4 * e + 2]) * scale,
+                                 __uint_as_float(v[4 * e + 3]) * scale);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + row_elem);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * e]) * scale, __uint_as_float(v[8 * e + 1]) * scale),
+                pack_bf16x2(__uint_as_float(v[8 * e + 2]) * scale, __uint_as_float(v[8 * e + 3]) * scale),
+                pack_bf16x2(__uint_as_float(v[8 * e + 4]) * scale, __uint_as_float(v[8 * e + 5]) * scale),
+                pack_bf16x2(__uint_as_float(v[8 * e + 6]) * scale, __uint_as_float(v[8 * e + 7]) * scale));
+    }
+}
+
+__device__ __forceinline__ void store_zero_row(void* base, int64_t row_elem, bool fp32, int D) {
+    if (fp32) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + row_elem);
+        for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + row_elem);
+        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+__device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_threads) {
+    mbar_init(&sh.a_full, 1);
+    mbar_init(&sh.a_empty, 1);
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.p_full, 4);  // one arrival per element-wise warp
+    mbar_init(&sh.o_full, 1);
+    mbar_init(&sh.o_empty, elem_threads / 32);
+    mbar_init(&sh.done, 1);
+    for (int s = 0; s < stages; ++s) {
+        mbar_init(&sh.r_full[s], 1);
+        mbar_init(&sh.r_empty[s], 1);
+    }
+    sh.abort_flag = 0;
+    fence_barrier_init();
+}
+
+// ==================================================================== dQ
+// Per query sub-tile (forward worklist units, sub-tiles one after the other):
+// a_full/a_empty guard the Q and dO tiles, r_full/r_empty the K/V ring (items
+// K_j, V_j in order), s_full: S and dP computed, p_full: dS stored over S,
+// o_full/o_empty: dQ accumulated / read out.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                  const BwdParams p) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sDO = smem + C::kTileBytes;
+    uint8_t* sKV = smem + 2 * C::kTileBytes;
+    __shared__ BShared sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const WlHeader* h = reinterpret_cast<const WlHeader*>(p.wl);
+    int32_t* err_word = const_cast<int32_t*>(&h->error);
+    if (h->error != 0) return;
+    const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
+    const WlUnit* units = reinterpret_cast<const WlUnit*>(p.wl + h->off.units);
+    const WlRun* runs = reinterpret_cast<const WlRun*>(p.wl + h->off.runs);
+    const WlSlice* slices = reinterpret_cast<const WlSlice*>(p.wl + h->off.slices);
+    const WlSeg* segs = reinterpret_cast<const WlSeg*>(p.wl + h->off.segs);
+    const int32_t ub = cta_off[blockIdx.x], ue = cta_off[blockIdx.x + 1];
+    if (ub >= ue) return;
+    if (tid == 0) init_barriers(sh, C::kStages, 128);
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&tmdo);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    volatile int32_t* abort_flag = &sh.abort_flag;
+
+    // the two query sub-tiles of a unit, one after the other
+    auto sub_of = [&](const WlUnit& u, int i, int32_t& q_row, int32_t& nrows, int32_t& q_pos,
+                      int32_t& head) {
+        const WlSeg g = segs[u.seg];
+        const int32_t t = i == 0 ? u.t0 : u.t1;
+        q_row = g.q_row0 + t * 128;
+        nrows = min(128, g.q_len - t * 128);
+        q_pos = g.q_pos0 + t * 128;
+        head = i == 0 ? u.h0 : u.h1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t it = 0, a_it = 0;
+            bool live = true;
+            for (int32_t ui = ub; ui < ue && live; ++ui) {
+                const WlUnit u = units[ui];
+                if (u.ntiles == 0) continue;
+                const int nsub = u.h1 >= 0 ? 2 : 1;
+                for (int i = 0; i < nsub && live; ++i) {
+                    int32_t q_row, nrows, q_pos, head;
+                    sub_of(u, i, q_row, nrows, q_pos, head);
+                    live = mbar_wait(&sh.a_empty, (a_it & 1) ^ 1, abort_flag, err_word,
+                                     kErrTimeoutBase + 21, kWaitNs);
+                    if (!live) break;
+                    mbar_arrive_expect_tx(&sh.a_full, 2 * C::kTileBytes);
+                    for (int b = 0; b < D / 64; ++b) {
+                        tma_load_3d(sQ + b * 16384, &tmq, &sh.a_full, b * 64, head, q_row);
+                        tma_load_3d(sDO + b * 16384, &tmdo, &sh.a_full, b * 64, head, q_row);
+                    }
+                    ++a_it;
+                    for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
+                        const WlRun run = runs[u.run_begin + rr];
+                        const WlSlice s = slices[run.slice];
+                        for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
+                            const int32_t krow = s.k_row0 + jt * 128;
+                            for (int kv = 0; kv < 2 && live; ++kv) {
+                                const uint32_t st = it % C::kStages;
+                                live = mbar_wait(&sh.r_empty[st], ((it / C::kStages) & 1) ^ 1,
+                                                 abort_flag, err_word, kErrTimeoutBase + 22,
+                                                 kWaitNs);
+                                if (!live) break;
+                                mbar_arrive_expect_tx(&sh.r_full[st], C::kTileBytes);
+                                for (int b = 0; b < D / 64; ++b)
+                                    tma_load_3d(sKV + st * C::kTileBytes + b * 16384,
+                                                kv == 0 ? &tmk : &tmv, &sh.r_full[st], b * 64,
+                                                u.kvh, krow);
+                                ++it;
+                            }
+                        }
+                    }
+                }
+            }
+            if (!live) {
+                const uint32_t n = it < (uint32_t)C::kStages ? it : (uint32_t)C::kStages;
+                for (uint32_t k = 0; k < n; ++k) {
+                    const uint32_t x = it - 1 - k;
+                    mbar_wait_drain(&sh.r_full[x % C::kStages], (x / C::kStages) & 1, kDrainNs);
+                }
+                if (a_it > 0) mbar_wait_drain(&sh.a_full, (a_it - 1) & 1, kDrainNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer (whole warp)
+        uint32_t it = 0, a_it = 0, p_cnt = 0, o_cnt = 0;
+        bool live = true;
+        const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
+        const uint64_t dKn = sdesc_sw128(smem_u32(sKV), 16, 1024);     // K-major (S, dP)
+        const uint64_t dKm = sdesc_sw128(smem_u32(sKV), 16384, 1024);  // MN-major (dQ)
+        const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;
+        for (int32_t ui = ub; ui < ue && live; ++ui) {
+            const WlUnit u = units[ui];
+            if (u.ntiles == 0) continue;
+            const int nsub = u.h1 >= 0 ? 2 : 1;
+            for (int i = 0; i < nsub && live; ++i) {
+                live = mbar_wait_warp(&sh.a_full, a_it & 1, abort_flag, err_word,
+                                      kErrTimeoutBase + 23, kWaitNs);
+                if (!live) break;
+                live = mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
+                                      kErrTimeoutBase + 24, kWaitNs);
+                if (!live) break;
+                int32_t j = 0;
+                for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
+                    const WlRun run = runs[u.run_begin + rr];
+                    for (int32_t jt = run.lo; jt < run.hi && live; ++jt, ++j) {
+                        const uint32_t stk = it % C::kStages, stv = (it + 1) % C::kStages;
+                        live = mbar_wait_warp(&sh.r_full[stk], (it / C::kStages) & 1, abort_flag,
+                                              err_word, kErrTimeoutBase + 25, kWaitNs);
+                        if (!live) break;
+                        live = mbar_wait_warp(&sh.r_full[stv], ((it + 1) / C::kStages) & 1,
+                                              abort_flag, err_word, kErrTimeoutBase + 25, kWaitNs);
+                        if (!live) break;
+                        tc_fence_after();
+                        const uint64_t oK = (stk * C::kTileBytes) >> 4, oV = (stv * C::kTileBytes) >> 4;
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                            mma_ss_elect(tS, dQd + off16, dKn + oK + off16, C::kIdescNT, k > 0);
+                        }
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                            mma_ss_elect(tP, dDO + off16, dKn + oV + off16, C::kIdescNT, k > 0);
+                        }
+                        mma_commit_elect(&sh.s_full);
+                        // V_j is read by dP only
+                        mma_commit_elect(&sh.r_empty[stv]);
+                        live = mbar_wait_warp(&sh.p_full, p_cnt & 1, abort_flag, err_word,
+                                              kErrTimeoutBase + 26, kWaitNs);
+                        if (!live) break;
+                        ++p_cnt;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            mma_ts_elect(tQ, tS + k * 8, dKm + oK + k * 128, C::kIdescNN,
+                                         (j > 0 || k > 0) ? 1u : 0u);
+                        mma_commit_elect(&sh.r_empty[stk]);
+                        it += 2;
+                    }
+                }
+                if (!live) break;
+                mma_commit_elect(&sh.a_empty);  // Q, dO read by the last MMAs
+                mma_commit_elect(&sh.o_full);
+                ++o_cnt;
+                ++a_it;
+            }
+        }
+        mma_commit_elect(&sh.done);
+        mbar_wait_drain(&sh.done, 0, kDrainNs);
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- dS and the dQ epilogue
+        const int r = (warp & 3) * 32 + lane;  // query row = tensor-memory lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base, tP = tmem + lane_base + 128,
+                       tQ = tmem + lane_base + 256;
+        uint32_t s_cnt = 0, o_cnt = 0;
+        bool live = true;
+        for (int32_t ui = ub; ui < ue && live; ++ui) {
+            const WlUnit u = units[ui];
+            const int nsub = u.h1 >= 0 ? 2 : 1;
+            for (int i = 0; i < nsub && live; ++i) {
+                int32_t q_row, nrows, q_pos0, head;
+                sub_of(u, i, q_row, nrows, q_pos0, head);
+                const bool valid = r < nrows;
+                const int64_t grow = ((int64_t)(q_row + r) * p.hq + head) * D;
+                if (u.ntiles == 0) {  // rows without keys: zero gradient
+                    if (valid) store_zero_row(p.dq, grow, p.grads_fp32, D);
+                    continue;
+                }
+                const int32_t q_pos = q_pos0 + r;
+                const int64_t li = (int64_t)head * p.q_tokens + q_row + r;
+                float lse2 = INFINITY, dd = 0.f;  // no key: every P is 0
+                if (valid) {
+                    const float l = p.lse[li];
+                    if (l != -INFINITY) lse2 = l * 1.4426950408889634f;
+                    dd = p.dvec[li];
+                }
+                for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
+                    const WlRun run = runs[u.run_begin + rr];
+                    const WlSlice s = slices[run.slice];
+                    const bool causal = s.type == PVA_SLICE_CAUSAL;
+                    const int32_t d_base = q_pos - s.k_pos0;
+                    const int32_t lim_hi = !valid ? 0 : causal ? min(s.k_len, d_base + 1) : s.k_len;
+                    const int32_t lim_lo = causal && s.window > 0 ? d_base - s.window + 1 : -(1 << 30);
+                    for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
+                        const int32_t kt0 = jt * 128;
+                        const int32_t c_hi = min(128, lim_hi - kt0), c_lo = max(0, lim_lo - kt0);
+                        live = mbar_wait(&sh.s_full, s_cnt & 1, abort_flag, err_word,
+                                         kErrTimeoutBase + 27, kWaitNs);
+                        if (!live) break;
+                        ++s_cnt;
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t sv[32], pv[32];
+                            tmem_ld32(tS + c * 32, sv);
+                            tmem_ld32(tP + c * 32, pv);
+                            tmem_ld_wait(sv);
+                            tmem_ld_wait(pv);
+                            uint32_t ds[16];
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2) {
+                                const int col = c * 32 + e;
+                                float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - lse2);
+                                float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lse2);
+                                if (col < c_lo || col >= c_hi) p0 = 0.f;
+                                if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                                const float g0 = p0 * (__uint_as_float(pv[e]) - dd);
+                                const float g1 = p1 * (__uint_as_float(pv[e + 1]) - dd);
+                                ds[e >> 1] = pack_bf16x2(g0, g1);
+                            }
+                            uint32_t dsw[32];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) dsw[e] = ds[e];
+                            tmem_st16(tS + c * 16, dsw);
+                        }
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sh.p_full);
+                    }
+                }
+                if (!live) break;
+                live = mbar_wait(&sh.o_full, o_cnt & 1, abort_flag, err_word,
+                                 kErrTimeoutBase + 28, kWaitNs);
+                if (!live) break;
+                ++o_cnt;
+                tc_fence_after();
+                uint32_t o[D / 32][32];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) tmem_ld32(tQ + c * 32, o[c]);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.o_empty);
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c)
+                        store_row32(p.dq, grow + c * 32, p.grads_fp32, o[c], p.scale);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ==================================================================== dK, dV
+// Per backward-plan unit (128 keys of one slice, one kv head): K and V stay in
+// shared memory (a_full/a_empty), the (Q, dO) tiles of every (head, q tile)
+// item stream through a ring of item pairs (r_full/r_empty per item).
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv,
+                    const __grid_constant__ CUtensorMap tmdo, const BwdParams p) {
+    using C = BCfg<D>;
+    constexpr int kItems = C::kStages / 2;  // (Q, dO) pairs in the ring
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sK = smem;
+    uint8_t* sV = smem + C::kTileBytes;
+    uint8_t* sR = smem + 2 * C::kTileBytes;  // item x: Q at 2x, dO at 2x + 1
+    __shared__ BShared sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const WlHeader* h = reinterpret_cast<const WlHeader*>(p.wl);
+    const BwdHeader* bh = reinterpret_cast<const BwdHeader*>(p.plan);
+    int32_t* err_word = const_cast<int32_t*>(&h->error);
+    if (h->error != 0) return;
+    if (bh->magic != kBwdMagic || bh->hq != p.hq || bh->hkv != p.hkv ||
+        bh->q_tokens != p.q_tokens || bh->k_tokens != p.k_tokens || bh->error != 0) {
+        if (tid == 0 && blockIdx.x == 0) atomicCAS(err_word, 0, kErrBadWorklist);
+        return;
+    }
+    const WlSlice* slices = reinterpret_cast<const WlSlice*>(p.wl + h->off.slices);
+    const BwdUnit* bunits = reinterpret_cast<const BwdUnit*>(p.plan + bh->off_units);
+    const int32_t* order = reinterpret_cast<const int32_t*>(p.plan + bh->off_order);
+    const int32_t* gsl = reinterpret_cast<const int32_t*>(p.plan + bh->off_gslices);
+    const int32_t n = bh->nunits, B = gridDim.x;
+    const int32_t G = p.hq / p.hkv;
+    if ((int32_t)blockIdx.x >= n) return;
+    if (tid == 0) init_barriers(sh, kItems, 128);
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&tmdo);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    volatile int32_t* abort_flag = &sh.abort_flag;
+    // units sorted by cost, dealt to the CTAs in snake order: b, 2B-1-b, 2B+b, ...
+    auto pos_of = [&](int32_t round) -> int32_t {
+        return round * B + ((round & 1) ? B - 1 - (int32_t)blockIdx.x : (int32_t)blockIdx.x);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t it = 0, a_it = 0;
+            bool live = true;
+            for (int32_t rd = 0; pos_of(rd) < n && live; ++rd) {
+                const BwdUnit u = bunits[order[pos_of(rd)]];
+                if (u.cost <= 1) continue;  // no query sees these keys
+                const WlSlice s = slices[gsl[u.gbegin]];
+                live = mbar_wait(&sh.a_empty, (a_it & 1) ^ 1, abort_flag, err_word,
+                                 kErrTimeoutBase + 31, kWaitNs);
+                if (!live) break;
+                mbar_arrive_expect_tx(&sh.a_full, 2 * C::kTileBytes);
+                for (int b = 0; b < D / 64; ++b) {
+                    tma_load_3d(sK + b * 16384, &tmk, &sh.a_full, b * 64, u.kvh, s.k_row0 + u.kt * 128);
+                    tma_load_3d(sV + b * 16384, &tmv, &sh.a_full, b * 64, u.kvh, s.k_row0 + u.kt * 128);
+                }
+                ++a_it;
+                for (int32_t hh = 0; hh < G && live; ++hh) {
+                    const int32_t head = u.kvh * G + hh;
+                    for (int32_t m = 0; m < u.gcount && live; ++m) {
+                        const WlSlice sm = slices[gsl[u.gbegin + m]];
+                        int32_t qlo, qhi;
+                        bwd_q_span(sm, u.kt, qlo, qhi);
+                        for (int32_t t = qlo; t < qhi && live; ++t) {
+                            const uint32_t st = it % kItems;
+                            live = mbar_wait(&sh.r_empty[st], ((it / kItems) & 1) ^ 1, abort_flag,
+                                             err_word, kErrTimeoutBase + 32, kWaitNs);
+                            if (!live) break;
+                            mbar_arrive_expect_tx(&sh.r_full[st], 2 * C::kTileBytes);
+                            uint8_t* dq_ = sR + (2 * st) * C::kTileBytes;
+                            uint8_t* ddo = sR + (2 * st + 1) * C::kTileBytes;
+                            for (int b = 0; b < D / 64; ++b) {
+                                tma_load_3d(dq_ + b * 16384, &tmq, &sh.r_full[st], b * 64, head,
+                                            sm.q_row0 + t * 128);
+                                tma_load_3d(ddo + b * 16384, &tmdo, &sh.r_full[st], b * 64, head,
+                                            sm.q_row0 + t * 128);
+                            }
+                            ++it;
+                        }
+                    }
+                }
+            }
+            if (!live) {
+                const uint32_t nn = it < (uint32_t)kItems ? it : (uint32_t)kItems;
+                for (uint32_t k = 0; k < nn; ++k) {
+                    const uint32_t x = it - 1 - k;
+                    mbar_wait_drain(&sh.r_full[x % kItems], (x / kItems) & 1, kDrainNs);
+                }
+                if (a_it > 0) mbar_wait_drain(&sh.a_full, (a_it - 1) & 1, kDrainNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer (whole warp)
+        uint32_t it = 0, a_it = 0, p_cnt = 0, o_cnt = 0;
+        bool live = true;
+        const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t dV = sdesc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t dRn = sdesc_sw128(smem_u32(sR), 16, 1024);     // K-major
+        const uint64_t dRm = sdesc_sw128(smem_u32(sR), 16384, 1024);  // MN-major
+        const uint32_t tS = tmem, tP = tmem + 128, tV = tmem + 256, tK = tmem + 256 + D;
+        for (int32_t rd = 0; pos_of(rd) < n && live; ++rd) {
+            const BwdUnit u = bunits[order[pos_of(rd)]];
+            if (u.cost <= 1) continue;
+            live = mbar_wait_warp(&sh.a_full, a_it & 1, abort_flag, err_word,
+                                  kErrTimeoutBase + 33, kWaitNs);
+            if (!live) break;
+            live = mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
+                                  kErrTimeoutBase + 34, kWaitNs);
+            if (!live) break;
+            const int32_t nitems = (int32_t)(u.cost - 1);
+            for (int32_t j = 0; j < nitems && live; ++j) {
+                {
+                    const uint32_t st = it % kItems;
+                    live = mbar_wait_warp(&sh.r_full[st], (it / kItems) & 1, abort_flag, err_word,
+                                          kErrTimeoutBase + 35, kWaitNs);
+                    if (!live) break;
+                    tc_fence_after();
+                    const uint64_t oQ = ((2 * st) * C::kTileBytes) >> 4;
+                    const uint64_t oO = ((2 * st + 1) * C::kTileBytes) >> 4;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                        mma_ss_elect(tS, dK + off16, dRn + oQ + off16, C::kIdescNT, k > 0);
+                    }
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                        mma_ss_elect(tP, dV + off16, dRn + oO + off16, C::kIdescNT, k > 0);
+                    }
+                    mma_commit_elect(&sh.s_full);
+                    live = mbar_wait_warp(&sh.p_full, p_cnt & 1, abort_flag, err_word,
+                                          kErrTimeoutBase + 36, kWaitNs);
+                    if (!live) break;
+                    ++p_cnt;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_ts_elect(tV, tS + k * 8, dRm + oO + k * 128, C::kIdescNN,
+                                     (j > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_ts_elect(tK, tP + k * 8, dRm + oQ + k * 128, C::kIdescNN,
+                                     (j > 0 || k > 0) ? 1u : 0u);
+                    mma_commit_elect(&sh.r_empty[st]);
+                    ++it;
+                }
+            }
+            if (!live) break;
+            mma_commit_elect(&sh.a_empty);
+            mma_commit_elect(&sh.o_full);
+            ++o_cnt;
+            ++a_it;
+        }
+        mma_commit_elect(&sh.done);
+        mbar_wait_drain(&sh.done, 0, kDrainNs);
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- P^T, dS^T and the dK/dV epilogue
+        const int kr = (warp & 3) * 32 + lane;  // key row = tensor-memory lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base, tP = tmem + lane_base + 128,
+                       tV = tmem + lane_base + 256, tK = tmem + lane_base + 256 + D;
+        uint32_t s_cnt = 0, o_cnt = 0;
+        bool live = true;
+        for (int32_t rd = 0; pos_of(rd) < n && live; ++rd) {
+            const BwdUnit u = bunits[order[pos_of(rd)]];
+            const WlSlice s0 = slices[gsl[u.gbegin]];  // the group's key range
+            const int32_t krows = min(128, s0.k_len - u.kt * 128);
+            const bool kvalid = kr < krows;
+            const int64_t grow = ((int64_t)(s0.k_row0 + u.kt * 128 + kr) * p.hkv + u.kvh) * D;
+            if (u.cost <= 1) {  // keys no query sees: zero gradient
+                if (kvalid) {
+                    store_zero_row(p.dk, grow, p.grads_fp32, D);
+                    store_zero_row(p.dv, grow, p.grads_fp32, D);
+                }
+                continue;
+            }
+            for (int32_t hh = 0; hh < G && live; ++hh) {
+                const int32_t head = u.kvh * G + hh;
+                for (int32_t m = 0; m < u.gcount && live; ++m) {
+                const WlSlice s = slices[gsl[u.gbegin + m]];
+                const bool causal = s.type == PVA_SLICE_CAUSAL;
+                const int32_t k_pos = s.k_pos0 + u.kt * 128 + kr;
+                int32_t qlo, qhi;
+                bwd_q_span(s, u.kt, qlo, qhi);
+                for (int32_t t = qlo; t < qhi && live; ++t) {
+                    // this q tile's rows: query c has position q_pos0 + t*128 + c
+                    const int32_t qrow0 = s.q_row0 + t * 128;
+                    const int32_t nq = min(128, s.q_len - t * 128);
+                    const int32_t cpos0 = s.q_pos0 + t * 128;
+                    int32_t c_lo = 0, c_hi = kvalid ? nq : 0;
+                    if (causal) {
+                        c_lo = max(c_lo, k_pos - cpos0);
+                        if (s.window > 0) c_hi = min(c_hi, k_pos + s.window - cpos0);
+                    }
+                    live = mbar_wait(&sh.s_full, s_cnt & 1, abort_flag, err_word,
+                                     kErrTimeoutBase + 37, kWaitNs);
+                    if (!live) break;
+                    ++s_cnt;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        // LSE (log2) and D of query column c*32 + lane, shared by shuffles
+                        const int qc = c * 32 + lane;
+                        float my_l2 = INFINITY, my_d = 0.f;  // no query: every P is 0
+                        if (qc < nq) {
+                            const int64_t li = (int64_t)head * p.q_tokens + qrow0 + qc;
+                            const float l = p.lse[li];
+                            if (l != -INFINITY) my_l2 = l * 1.4426950408889634f;
+                            my_d = p.dvec[li];
+                        }
+                        uint32_t sv[32], pv[32];
+                        tmem_ld32(tS + c * 32, sv);
+                        tmem_ld32(tP + c * 32, pv);
+                        tmem_ld_wait(sv);
+                        tmem_ld_wait(pv);
+                        uint32_t pw[32], dw[32];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int col = c * 32 + e;
+                            const float l0 = __shfl_sync(0xffffffffu, my_l2, e);
+                            const float l1 = __shfl_sync(0xffffffffu, my_l2, e + 1);
+                            const float d0 = __shfl_sync(0xffffffffu, my_d, e);
+                            const float d1 = __shfl_sync(0xffffffffu, my_d, e + 1);
+                            float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - l0);
+                            float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - l1);
+                            if (col < c_lo || col >= c_hi) p0 = 0.f;
+                            if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                            const float g0 = p0 * (__uint_as_float(pv[e]) - d0);
+                            const float g1 = p1 * (__uint_as_float(pv[e + 1]) - d1);
+                            pw[e >> 1] = pack_bf16x2(p0, p1);
+                            dw[e >> 1] = pack_bf16x2(g0, g1);
+                        }
+                        tmem_st16(tS + c * 16, pw);
+                        tmem_st16(tP + c * 16, dw);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.p_full);
+                }
+                }
+            }
+            if (!live) break;
+            live = mbar_wait(&sh.o_full, o_cnt & 1, abort_flag, err_word, kErrTimeoutBase + 38,
+                             kWaitNs);
+            if (!live) break;
+            ++o_cnt;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32], b[32];
+                tmem_ld32(tV + c * 32, a);
+                tmem_ld32(tK + c * 32, b);
+                tmem_ld_wait(a);
+                tmem_ld_wait(b);
+                if (kvalid) {
+                    store_row32(p.dv, grow + c * 32, p.grads_fp32, a, 1.f);
+                    store_row32(p.dk, grow + c * 32, p.grads_fp32, b, p.scale);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.o_empty);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+pva_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                      const CUtensorMap& mdo, const BwdParams& bp, int32_t dkdv_ctas,
+                      cudaStream_t st) {
+    const int grid_pre = 4 * bp.num_ctas;
+    bwd_pre_kernel<<<grid_pre, 256, 0, st>>>(bp);
+    auto kq = bwd_dq_kernel<D>;
+    auto kk = bwd_dkdv_kernel<D>;
+    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem) !=
+            cudaSuccess)
+        return PVA_ERR_CUDA;
+    kq<<<bp.num_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq, mk, mv, mdo, bp);
+    kk<<<dkdv_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq, mk, mv, mdo, bp);
+    return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace pva
+
+using namespace pva;
+
+extern "C" pva_status pva_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                                   const float* lse, const void* dout,
+                                   const int32_t* cu_seqlens_dev, int32_t num_docs,
+                                   const pva_mask_desc* mask,
+                                   const pva_worklist_params* params, int32_t head_dim,
+                                   const void* worklist_dev, void* plan_dev, void* dq, void* dk,
+                                   void* dv, int32_t grads_are_fp32, float softmax_scale,
+                                   void* stream) {
+    if (!mask || !params || !worklist_dev || !plan_dev || !q || !out || !lse || !dout || !dq ||
+        !dk || !dv)
+        return PVA_ERR_INVALID_ARG;
+    if (mask->kind != PVA_MASK_SLICES && !cu_seqlens_dev) return PVA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PVA_ERR_UNSUPPORTED;
+    if (params->tile_m != 128 || params->tile_n != 128) return PVA_ERR_UNSUPPORTED;
+    if (params->num_q_heads <= 0 || params->num_kv_heads <= 0 ||
+        params->num_q_heads % params->num_kv_heads != 0)
+        return PVA_ERR_INVALID_ARG;
+    if (grads_are_fp32 != 0 && grads_are_fp32 != 1) return PVA_ERR_INVALID_ARG;
+    if (mask->q_tokens < 0 || mask->k_tokens < 0) return PVA_ERR_INVALID_ARG;
+    if (mask->k_tokens > 0 && (!k || !v)) return PVA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(dout) || !aligned16(lse) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv) ||
+        (mask->k_tokens > 0 && (!aligned16(k) || !aligned16(v))) ||
+        (reinterpret_cast<uintptr_t>(worklist_dev) & 255u) ||
+        (reinterpret_cast<uintptr_t>(plan_dev) & 255u))
+        return PVA_ERR_INVALID_ARG;
+    const int32_t nc = resolve_num_ctas(params->num_ctas);
+    if (nc <= 0) return PVA_ERR_CUDA;
+    if (nc > kMaxBins) return PVA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t es = grads_are_fp32 ? 4 : 2;
+    // Keys that no slice covers get no gradient: explicit slices, and a zigzag
+    // pair's key chunks that lie after every query chunk of their document.
+    // Queries outside every segment: explicit slices only.
+    if (mask->kind == PVA_MASK_SLICES &&
+        cudaMemsetAsync(dq, 0, (size_t)mask->q_tokens * params->num_q_heads * head_dim * es, st) !=
+            cudaSuccess)
+        return PVA_ERR_CUDA;
+    if ((mask->kind == PVA_MASK_SLICES || mask->kind == PVA_MASK_ZIGZAG_PAIR) &&
+        (cudaMemsetAsync(dk, 0, (size_t)mask->k_tokens * params->num_kv_heads * head_dim * es,
+                         st) != cudaSuccess ||
+         cudaMemsetAsync(dv, 0, (size_t)mask->k_tokens * params->num_kv_heads * head_dim * es,
+                         st) != cudaSuccess))
+        return PVA_ERR_CUDA;
+    if (mask->q_tokens == 0) return PVA_OK;
+    // the plan's D scratch (its header is checked on the device)
+    const int64_t off_dvec = bwd_plan_dvec_offset(num_docs, mask, params);
+    if (off_dvec < 0) return PVA_ERR_INVALID_ARG;
+    CUtensorMap mq, mk, mv, mdo;
+    const void* kp = mask->k_tokens > 0 ? k : q;
+    const void* vp = mask->k_tokens > 0 ? v : q;
+    const int32_t kh = mask->k_tokens > 0 ? params->num_kv_heads : params->num_q_heads;
+    if (!make_map(&mq, q, mask->q_tokens, params->num_q_heads, head_dim) ||
+        !make_map(&mk, kp, mask->k_tokens, kh, head_dim) ||
+        !make_map(&mv, vp, mask->k_tokens, kh, head_dim) ||
+        !make_map(&mdo, dout, mask->q_tokens, params->num_q_heads, head_dim))
+        return PVA_ERR_CUDA;
+    BwdParams bp;
+    bp.wl = reinterpret_cast<const uint8_t*>(worklist_dev);
+    bp.plan = reinterpret_cast<const uint8_t*>(plan_dev);
+    bp.out = out;
+    bp.dout = dout;
+    bp.lse = lse;
+    bp.dvec = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(plan_dev) + off_dvec);
+    bp.dq = dq;
+    bp.dk = dk;
+    bp.dv = dv;
+    bp.q_tokens = mask->q_tokens;
+    bp.k_tokens = mask->k_tokens;
+    bp.hq = params->num_q_heads;
+    bp.hkv = params->num_kv_heads;
+    bp.grads_fp32 = grads_are_fp32;
+    bp.num_ctas = nc;
+    bp.d = head_dim;
+    bp.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
+    bp.scale_log2 = bp.scale * 1.4426950408889634f;
+    return head_dim == 128 ? launch_bwd<128>(mq, mk, mv, mdo, bp, nc, st)
+                           : launch_bwd<64>(mq, mk, mv, mdo, bp, nc, st);
+}

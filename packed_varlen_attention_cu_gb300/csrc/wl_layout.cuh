@@ -67,6 +67,51 @@ struct WlHeader {
 };
 static_assert(sizeof(WlHeader) <= 256, "header fits in 256 bytes");
 
+// Backward plan: kv-major units.  Slices with the same key range form a key
+// group (a document's keys under a causal mask; a question's keys shared by
+// its own slice and every answer's; a zigzag key chunk seen by two query
+// chunks); different groups' key ranges are disjoint.  A unit is one 128-key
+// tile of a group for one kv head; it covers every slice of the group and
+// every head of the kv head's group, so each key row has one writer.
+// Buffer sections (256-byte aligned): header, units, sort keys, order (rank ->
+// unit), gslices (slice indices sorted by key range), D scratch [hq, q_tokens].
+constexpr int32_t kBwdMagic = 0x42415650;  // "PVAB"
+constexpr int32_t kBwdMaxSlices = 8192;    // slices the plan kernel groups in shared memory
+
+struct BwdUnit {
+    int32_t gbegin, gcount;  // the group's slices: gslices[gbegin, gbegin + gcount)
+    int32_t kt, kvh;
+    int64_t cost;  // q-tile steps over the group's slices and heads + 1
+};
+static_assert(sizeof(BwdUnit) == 24, "BwdUnit is 24 bytes");
+
+struct BwdHeader {
+    int32_t magic, error, nunits, cap_units;
+    int32_t hq, hkv, q_tokens, k_tokens;
+    int64_t off_units, off_keys, off_order, off_gslices, off_dvec, total;
+};
+static_assert(sizeof(BwdHeader) <= 256, "backward header fits in 256 bytes");
+
+// q tiles [qlo, qhi) of slice `sl` (aligned at its query start, like the
+// forward) holding a row that may see a key of key tile kt of the slice.
+__host__ __device__ inline void bwd_q_span(const WlSlice& sl, int32_t kt, int32_t& qlo,
+                                           int32_t& qhi) {
+    const int32_t ka = kt * 128, kb = (sl.k_len < ka + 128) ? sl.k_len : ka + 128;
+    int64_t r_lo = 0, r_hi = sl.q_len;
+    if (sl.type == 1) {  // causal by position, optional window
+        r_lo = (int64_t)sl.k_pos0 + ka - sl.q_pos0;
+        if (sl.window > 0) r_hi = (int64_t)sl.k_pos0 + kb - 1 + sl.window - sl.q_pos0;
+    }
+    if (r_lo < 0) r_lo = 0;
+    if (r_hi > sl.q_len) r_hi = sl.q_len;
+    if (kb <= ka || r_hi <= r_lo) {
+        qlo = qhi = 0;
+        return;
+    }
+    qlo = (int32_t)(r_lo / 128);
+    qhi = (int32_t)((r_hi + 127) / 128);
+}
+
 // Device error codes (stored in WlHeader::error).
 enum : int32_t {
     kErrNone = 0,

@@ -477,13 +477,23 @@ __global__ void __launch_bounds__(kUnitWarps * 32) wl_units_kernel(UnitArgs a) {
 constexpr int kSortChunk = 2048;
 constexpr int kSortThreads = 1024;
 
-__global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(uint8_t* base) {
-    WlHeader* h = reinterpret_cast<WlHeader*>(base);
-    if (h->error) return;
-    const int32_t n = h->nunits;
+// What the sort kernels work on: n keys (a device count, read when the kernel
+// runs), and where a failed earlier stage left its error word.
+struct SortArgs {
+    const int32_t* err;
+    const int32_t* n;
+    unsigned long long* keys;
+    int32_t* order;             // rank -> uid (LPT order)
+    const WlUnit* units_enum;   // CTA order: units by uid ...
+    WlUnit* units;              // ... written at their rank
+};
+
+__global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a) {
+    if (*a.err) return;
+    const int32_t n = *a.n;
     const int32_t c0 = blockIdx.x * kSortChunk;
     if (c0 >= n) return;
-    unsigned long long* keys = reinterpret_cast<unsigned long long*>(base + h->off.keys);
+    unsigned long long* keys = a.keys;
     __shared__ unsigned long long sk[kSortChunk];
     const int32_t m = min(kSortChunk, n - c0);
     for (int32_t i = threadIdx.x; i < kSortChunk; i += kSortThreads)
@@ -511,15 +521,12 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(uint8_t* b
 // kCtaOrder = true: keys are (cta, uid) and units[rank] = the unit with its
 // CTA, i.e. the CSR list of every CTA in enumeration order.
 template <bool kCtaOrder>
-__global__ void __launch_bounds__(kSortThreads) wl_merge_rank_kernel(uint8_t* base) {
-    WlHeader* h = reinterpret_cast<WlHeader*>(base);
-    if (h->error) return;
-    const int32_t n = h->nunits;
+__global__ void __launch_bounds__(kSortThreads) wl_merge_rank_kernel(SortArgs a) {
+    if (*a.err) return;
+    const int32_t n = *a.n;
     const int32_t c0 = blockIdx.x * kSortChunk;
     if (c0 >= n) return;
-    const unsigned long long* keys =
-        reinterpret_cast<const unsigned long long*>(base + h->off.keys);
-    int32_t* order = reinterpret_cast<int32_t*>(base + h->off.order);
+    const unsigned long long* keys = a.keys;
     __shared__ unsigned long long other[kSortChunk];
     const int32_t m = min(kSortChunk, n - c0);
     const int32_t nchunks = (n + kSortChunk - 1) / kSortChunk;
@@ -551,13 +558,11 @@ __global__ void __launch_bounds__(kSortThreads) wl_merge_rank_kernel(uint8_t* ba
         if (i >= m) continue;
         const int32_t uid = (int32_t)(mine[e] & ((1ULL << kUidBits) - 1));
         if (kCtaOrder) {
-            const WlUnit* units_enum = reinterpret_cast<const WlUnit*>(base + h->off.units_enum);
-            WlUnit* units = reinterpret_cast<WlUnit*>(base + h->off.units);
-            WlUnit x = units_enum[uid];
+            WlUnit x = a.units_enum[uid];
             x.cta = (int32_t)(mine[e] >> kUidBits);
-            units[rank[e]] = x;
+            a.units[rank[e]] = x;
         } else {
-            order[rank[e]] = uid;
+            a.order[rank[e]] = uid;
         }
     }
 }
@@ -869,6 +874,130 @@ __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t
         keys[u] = ((unsigned long long)assign[u] << kUidBits) | (unsigned long long)u;
 }
 
+// Backward plan (kv-major units) from the forward worklist's slices, one CTA.
+// 1. Sort the slice indices by (k_row0, k_len, index) in shared memory
+//    (bitonic); equal key ranges become runs: the key groups.
+// 2. A block scan over the groups of their key-tile counts.
+// 3. One unit per (group, key tile, kv head) with its cost (q-tile steps over
+//    the group's slices and the heads of the kv head's group, + 1) and a sort
+//    key (cost desc, uid asc).
+constexpr int kBwdPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kBwdPlanThreads)
+    bwd_plan_kernel(const uint8_t* wl, uint8_t* plan) {
+    extern __shared__ unsigned long long bsm[];
+    const WlHeader* h = reinterpret_cast<const WlHeader*>(wl);
+    BwdHeader* bh = reinterpret_cast<BwdHeader*>(plan);
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    if (h->error != 0) {
+        if (threadIdx.x == 0) bh->error = h->error;
+        return;
+    }
+    const int32_t ns = h->nslices;
+    if (ns > kBwdMaxSlices) {
+        if (threadIdx.x == 0) bh->error = kErrCapacity;
+        return;
+    }
+    const WlSlice* slices = reinterpret_cast<const WlSlice*>(wl + h->off.slices);
+    BwdUnit* units = reinterpret_cast<BwdUnit*>(plan + bh->off_units);
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(plan + bh->off_keys);
+    int32_t* gsl = reinterpret_cast<int32_t*>(plan + bh->off_gslices);
+    const int32_t hkv = bh->hkv, G = bh->hq / bh->hkv;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    int32_t np2 = 1;
+    while (np2 < ns) np2 <<= 1;
+    // (k_row0, k_len) packed, k_len < 2^31; the slice index rides in sidx
+    unsigned long long* skey = bsm;                               // [np2]
+    int32_t* sidx = reinterpret_cast<int32_t*>(bsm + np2);        // [np2]
+    int32_t* lead = sidx + np2;                                   // [np2] 1 at a group's first
+    for (int32_t i = tid; i < np2; i += kBwdPlanThreads) {
+        if (i < ns) {
+            const WlSlice sl = slices[i];
+            skey[i] = ((unsigned long long)(uint32_t)sl.k_row0 << 32) | (uint32_t)sl.k_len;
+        } else {
+            skey[i] = ~0ULL;
+        }
+        sidx[i] = i;
+    }
+    __syncthreads();
+    for (int32_t size = 2; size <= np2; size <<= 1) {
+        for (int32_t stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int32_t t = tid; t < np2 / 2; t += kBwdPlanThreads) {
+                const int32_t lo = 2 * t - (t & (stride - 1));
+                const int32_t hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const unsigned long long xk = skey[lo], yk = skey[hi];
+                const int32_t xi = sidx[lo], yi = sidx[hi];
+                const bool x_first = xk < yk || (xk == yk && xi < yi);
+                if (x_first != up) {
+                    skey[lo] = yk;
+                    skey[hi] = xk;
+                    sidx[lo] = yi;
+                    sidx[hi] = xi;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int32_t i = tid; i < ns; i += kBwdPlanThreads) {
+        gsl[i] = sidx[i];
+        lead[i] = (i == 0 || skey[i] != skey[i - 1]) ? 1 : 0;
+    }
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    // groups: a leader at position i runs to the next leader
+    for (int32_t c0 = 0; c0 < ns; c0 += kBwdPlanThreads) {
+        const int32_t i = c0 + tid;
+        int32_t nk = 0, gcount = 0;
+        WlSlice sl{0, 0, 0, 0, 0, 0, 0, 0};
+        if (i < ns && lead[i]) {
+            sl = slices[sidx[i]];
+            nk = sl.k_len > 0 ? (sl.k_len + 127) / 128 : 0;
+            gcount = 1;
+            while (i + gcount < ns && !lead[i + gcount]) ++gcount;
+        }
+        int32_t inc = nk;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t x = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += x;
+        }
+        if (lane == 31) warp_tot[w] = inc;
+        __syncthreads();
+        int32_t base = carry;
+        for (int j = 0; j < w; ++j) base += warp_tot[j];
+        const int32_t first = base + inc - nk;  // this group's first key tile
+        for (int32_t kt = 0; kt < nk; ++kt) {
+            int64_t steps = 0;
+            for (int32_t m = 0; m < gcount; ++m) {
+                int32_t qlo, qhi;
+                bwd_q_span(slices[sidx[i + m]], kt, qlo, qhi);
+                steps += qhi - qlo;
+            }
+            for (int32_t g = 0; g < hkv; ++g) {
+                const int32_t uid = (first + kt) * hkv + g;
+                if (uid >= bh->cap_units) {
+                    atomicCAS(&bh->error, 0, kErrCapacity);
+                    continue;
+                }
+                BwdUnit u;
+                u.gbegin = i;
+                u.gcount = gcount;
+                u.kt = kt;
+                u.kvh = g;
+                u.cost = (int64_t)G * steps + 1;
+                units[uid] = u;
+                const unsigned long long inv = ((1ULL << kCostBits) - 1) - (unsigned long long)u.cost;
+                keys[uid] = (inv << kUidBits) | (unsigned long long)uid;
+            }
+        }
+        __syncthreads();
+        if (tid == kBwdPlanThreads - 1) carry = base + inc;
+        __syncthreads();
+    }
+    if (tid == 0) bh->nunits = carry * hkv;
+}
+
 // ------------------------------------------------------------------ host side
 int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
@@ -1049,13 +1178,20 @@ extern "C" pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t 
     const int ub = (h.cap_units + kUnitWarps - 1) / kUnitWarps;
     wl_units_kernel<<<ub, kUnitWarps * 32, 0, st>>>(ua);
     const int sb = (h.cap_units + kSortChunk - 1) / kSortChunk;
-    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(base);
-    wl_merge_rank_kernel<false><<<sb, kSortThreads, 0, st>>>(base);
+    SortArgs sa;
+    sa.err = reinterpret_cast<const int32_t*>(base + offsetof(WlHeader, error));
+    sa.n = reinterpret_cast<const int32_t*>(base + offsetof(WlHeader, nunits));
+    sa.keys = reinterpret_cast<unsigned long long*>(base + h.off.keys);
+    sa.order = reinterpret_cast<int32_t*>(base + h.off.order);
+    sa.units_enum = reinterpret_cast<const WlUnit*>(base + h.off.units_enum);
+    sa.units = reinterpret_cast<WlUnit*>(base + h.off.units);
+    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(sa);
+    wl_merge_rank_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
     const int bp = ((nc + 31) / 32) * 32;
     const int lpt_f = bp >= 1024 ? 1 : (1024 / bp < 4 ? 1024 / bp : 4);
     wl_lpt_kernel<<<1, bp * lpt_f, 0, st>>>(base, lpt_f);
-    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(base);
-    wl_merge_rank_kernel<true><<<sb, kSortThreads, 0, st>>>(base);
+    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(sa);
+    wl_merge_rank_kernel<true><<<sb, kSortThreads, 0, st>>>(sa);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
 
@@ -1191,4 +1327,97 @@ extern "C" pva_status pva_fit_tile_cost(const void* const* worklists_dev,
         return PVA_OK;
     }
     return PVA_ERR_INVALID_ARG;
+}
+
+namespace {
+
+bool bwd_layout(int32_t num_docs, const pva_mask_desc* mask, const pva_worklist_params* params,
+                BwdHeader* bh) {
+    if (!mask || !params) return false;
+    // slices' key ranges must be identical or disjoint: a key group then owns
+    // its key rows (the built-in mask kinds satisfy this by construction)
+    if (mask->kind == PVA_MASK_SLICES) {
+        if (!mask->slices || mask->num_slices < 0) return false;
+        std::vector<std::pair<int32_t, int32_t>> kr;
+        for (int32_t i = 0; i < mask->num_slices; ++i)
+            if (mask->slices[i].k_len > 0)
+                kr.push_back({mask->slices[i].k_row0, mask->slices[i].k_row0 + mask->slices[i].k_len});
+        std::sort(kr.begin(), kr.end());
+        kr.erase(std::unique(kr.begin(), kr.end()), kr.end());
+        for (size_t i = 1; i < kr.size(); ++i)
+            if (kr[i].first < kr[i - 1].second) return false;
+    }
+    WlHeader h;
+    const int32_t nc = resolve_num_ctas(params->num_ctas);
+    if (nc <= 0 || !plan_layout(num_docs, mask, params, nc, &h)) return false;
+    if (h.cap_slices > kBwdMaxSlices) return false;
+    const int64_t hkv = params->num_kv_heads;
+    const int64_t cap = ((int64_t)(mask->k_tokens + 127) / 128 + h.cap_slices) * hkv + 1;
+    if (cap >= (1LL << kUidBits)) return false;
+    memset(bh, 0, sizeof *bh);
+    bh->magic = kBwdMagic;
+    bh->cap_units = (int32_t)cap;
+    bh->hq = params->num_q_heads;
+    bh->hkv = params->num_kv_heads;
+    bh->q_tokens = mask->q_tokens;
+    bh->k_tokens = mask->k_tokens;
+    int64_t o = 256;
+    bh->off_units = o; o = align256(o + cap * (int64_t)sizeof(BwdUnit));
+    bh->off_keys = o; o = align256(o + cap * 8);
+    bh->off_order = o; o = align256(o + cap * 4);
+    bh->off_gslices = o; o = align256(o + (int64_t)h.cap_slices * 4 + 4);
+    bh->off_dvec = o; o = align256(o + (int64_t)params->num_q_heads * mask->q_tokens * 4);
+    bh->total = o;
+    return true;
+}
+
+}  // namespace
+
+namespace pva {
+int64_t bwd_plan_dvec_offset(int32_t num_docs, const pva_mask_desc* mask,
+                             const pva_worklist_params* params) {
+    BwdHeader bh;
+    if (!bwd_layout(num_docs, mask, params, &bh)) return -1;
+    return bh.off_dvec;
+}
+}  // namespace pva
+
+extern "C" size_t pva_bwd_plan_bytes(int32_t num_docs, const pva_mask_desc* mask,
+                                     const pva_worklist_params* params) {
+    BwdHeader bh;
+    if (!bwd_layout(num_docs, mask, params, &bh)) return 0;
+    return (size_t)bh.total;
+}
+
+extern "C" pva_status pva_build_bwd_plan(const void* worklist_dev, int32_t num_docs,
+                                         const pva_mask_desc* mask,
+                                         const pva_worklist_params* params, void* plan_dev,
+                                         size_t plan_bytes, void* stream) {
+    if (!worklist_dev || !plan_dev || (reinterpret_cast<uintptr_t>(plan_dev) & 255u))
+        return PVA_ERR_INVALID_ARG;
+    BwdHeader bh;
+    if (!bwd_layout(num_docs, mask, params, &bh)) return PVA_ERR_INVALID_ARG;
+    if (plan_bytes < (size_t)bh.total) return PVA_ERR_BUFFER_TOO_SMALL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* base = reinterpret_cast<uint8_t*>(plan_dev);
+    if (cudaMemcpyAsync(base, &bh, sizeof bh, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return PVA_ERR_CUDA;
+    // shared memory: sort keys, slice indices and group flags for every slice
+    const size_t smem = (size_t)kBwdMaxSlices * 16;
+    if (cudaFuncSetAttribute(bwd_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return PVA_ERR_CUDA;
+    bwd_plan_kernel<<<1, kBwdPlanThreads, smem, st>>>(
+        reinterpret_cast<const uint8_t*>(worklist_dev), base);
+    SortArgs sa;
+    sa.err = reinterpret_cast<const int32_t*>(base + offsetof(BwdHeader, error));
+    sa.n = reinterpret_cast<const int32_t*>(base + offsetof(BwdHeader, nunits));
+    sa.keys = reinterpret_cast<unsigned long long*>(base + bh.off_keys);
+    sa.order = reinterpret_cast<int32_t*>(base + bh.off_order);
+    sa.units_enum = nullptr;
+    sa.units = nullptr;
+    const int sb = (bh.cap_units + kSortChunk - 1) / kSortChunk;
+    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(sa);
+    wl_merge_rank_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
+    return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }

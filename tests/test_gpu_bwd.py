@@ -1,0 +1,130 @@
+"""Backward on the GPU against the fp64 oracle: dq, dk, dv element by element
+(relative L2 and max-abs against the gradient's scale), for document-causal,
+sliding-window, zigzag-pair and explicit-slice masks, GQA, d = 64 and 128,
+bf16 and fp32 gradients, ragged documents."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from packed_varlen_attention_cu_gb300 import api
+from packed_varlen_attention_cu_gb300 import workloads as W
+
+from gpu_util import oracle_mask, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+# bf16 P and dS (2^-9 relative rounding per term) feed the gradient MMAs; measured
+# 1.5-2.6e-3 relative L2 and at most 3.8e-3 of the largest magnitude
+REL_L2 = 6e-3
+MAX_ABS_REL = 1.5e-2   # of the largest reference magnitude
+
+
+def _bwd(q, k, v, cu, mask, hq, hkv, dout, fp32):
+    dev = torch.device("cuda")
+    out, lse, wl = run_gpu(q, k, v, cu, mask, hq, hkv)
+    nd = len(cu) - 1
+    params = api.make_params(hq, hkv)
+    plan = api.alloc_bwd_plan(nd, mask, params, dev)
+    api.build_bwd_plan(wl, nd, mask, params, plan)
+    dt = torch.float32 if fp32 else torch.bfloat16
+    dq = torch.full(q.shape, float("nan"), dtype=dt, device=dev)
+    dk = torch.full(k.shape, float("nan"), dtype=dt, device=dev)
+    dv = torch.full(v.shape, float("nan"), dtype=dt, device=dev)
+    cu_d = torch.from_numpy(np.ascontiguousarray(cu, dtype=np.int32)).to(dev)
+    api.attn_bwd(q.to(dev), k.to(dev), v.to(dev), out, lse, dout.to(dev), cu_d, nd, mask, params,
+                 wl, plan, dq, dk, dv)
+    torch.cuda.synchronize()
+    assert api.worklist_error(wl) == 0
+    return [t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv)]
+
+
+def _check(got, ref, label):
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.isfinite(g).all(), f"{label} {name}: non-finite"
+        scale = max(float(np.abs(r).max()), 1e-6)
+        err = np.abs(g - r)
+        rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-12))
+        msg = f"{label} {name}: rel_l2={rel:.3e} max_abs/scale={err.max() / scale:.3e}"
+        print(msg)
+        assert rel <= REL_L2, msg
+        assert err.max() <= MAX_ABS_REL * scale, msg
+
+
+def _case(oracle_mod, lengths, hq, hkv, d, kind, fp32, seed, **mkw):
+    cu = W.cu_seqlens_of(lengths)
+    T = int(cu[-1])
+    q, k, v = W.make_qkv(T, T, hq, hkv, d, seed)
+    dout = W.make_qkv(T, T, hq, hkv, d, seed + 100)[0]
+    mask = api.make_mask(kind, T, T, **mkw)
+    okw = {"window": mkw.get("window", 0), "num_prefix": mkw.get("num_prefix_docs", 0)}
+    got = _bwd(q, k, v, cu, mask, hq, hkv, dout, fp32)
+    ref = oracle_mod.attention_bwd(oracle_mod.bf16_bits(q), oracle_mod.bf16_bits(k),
+                                   oracle_mod.bf16_bits(v), oracle_mod.bf16_bits(dout), cu,
+                                   oracle_mask(kind, **okw))
+    _check(got, ref, f"{kind} d={d} hq={hq}/{hkv} fp32={fp32}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("fp32", [True, False])
+def test_bwd_causal_gqa(oracle_mod, d, fp32):
+    _case(oracle_mod, [300, 5, 130, 700, 1, 129], 4, 2, d, W.MASK_CAUSAL, fp32, 21)
+
+
+def test_bwd_causal_mha_long_doc(oracle_mod):
+    _case(oracle_mod, [1500, 37], 2, 2, 128, W.MASK_CAUSAL, True, 22)
+
+
+def test_bwd_sliding_window(oracle_mod):
+    _case(oracle_mod, [900, 250, 64], 4, 1, 128, W.MASK_SLIDING_WINDOW, True, 23, window=200)
+
+
+def test_bwd_zigzag_pair(oracle_mod):
+    cp, qr, kr = 2, 1, 0
+    lengths = [700, 130, 1, 260]
+    cu = W.cu_seqlens_of(lengths)
+    T = int(cu[-1])
+    hq, hkv, d = 4, 2, 128
+    q, k, v = W.make_qkv(T, T, hq, hkv, d, 24)
+    dout = W.make_qkv(T, T, hq, hkv, d, 124)[0]
+    mq = oracle_mod.zigzag_map(cu, cp, qr)[0]
+    mk = oracle_mod.zigzag_map(cu, cp, kr)[0]
+    qs, ks, vs, ds = q[mq], k[mk], v[mk], dout[mq]
+    mask = api.make_mask(W.MASK_ZIGZAG_PAIR, qs.shape[0], ks.shape[0], cp=cp, q_rank=qr, k_rank=kr)
+    got = _bwd(qs, ks, vs, cu, mask, hq, hkv, ds, True)
+    ref = oracle_mod.attention_bwd(oracle_mod.bf16_bits(qs), oracle_mod.bf16_bits(ks),
+                                   oracle_mod.bf16_bits(vs), oracle_mod.bf16_bits(ds), cu,
+                                   oracle_mask(W.MASK_ZIGZAG_PAIR, cp=cp, q_rank=qr, k_rank=kr))
+    _check(got, ref, "zigzag pair")
+
+
+def test_bwd_explicit_slices_with_unseen_keys(oracle_mod):
+    # queries [0, 300) see keys [0, 200) causally and queries [300, 420) see keys
+    # [250, 400) fully; keys [200, 250) and [400, 450) are never seen (zero gradient)
+    sl = np.array([[0, 300, 0, 0, 200, 0, 1, 0], [300, 120, 0, 250, 150, 0, 0, 0]], dtype=np.int32)
+    Tq, Tk, hq, hkv, d = 420, 450, 2, 1, 64
+    q, _, _ = W.make_qkv(Tq, Tq, hq, hkv, d, 25)
+    _, k, v = W.make_qkv(Tk, Tk, hq, hkv, d, 26)
+    dout = W.make_qkv(Tq, Tq, hq, hkv, d, 27)[0]
+    mask = api.make_mask(W.MASK_SLICES, Tq, Tk, slices=sl)
+    cu = W.cu_seqlens_of([Tq])
+    got = _bwd(q, k, v, cu, mask, hq, hkv, dout, True)
+    ref = oracle_mod.attention_bwd(oracle_mod.bf16_bits(q), oracle_mod.bf16_bits(k),
+                                   oracle_mod.bf16_bits(v), oracle_mod.bf16_bits(dout), cu,
+                                   oracle_mask(W.MASK_SLICES, slices=sl))
+    _check(got, ref, "slices")
+    assert np.all(got[1][200:250] == 0) and np.all(got[2][400:] == 0)
+
+
+def test_bwd_shared_question(oracle_mod):
+    # the question's keys form one key group: its own causal slice and every answer
+    _case(oracle_mod, [400, 300, 200, 129], 4, 2, 128, W.MASK_SHARED_QUESTION, True, 28,
+          num_prefix_docs=1)
+
+
+def test_bwd_plan_rejects_partly_overlapping_key_ranges():
+    sl = np.array([[0, 10, 0, 0, 10, 0, 1, 0], [10, 10, 0, 5, 10, 0, 0, 0]], dtype=np.int32)
+    m = api.make_mask(W.MASK_SLICES, 20, 20, slices=sl)
+    p = api.make_params(2, 2)
+    assert api.lib().pva_bwd_plan_bytes(1, ctypes.byref(m), ctypes.byref(p)) == 0
