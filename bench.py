@@ -535,6 +535,59 @@ def run_dispatch(args, ctx):
                     "WLB costs are tile-rounded (128) FLOPs of the most loaded worker"}
 
 
+def run_backward(args, ctx, world):
+    """Attention backward on this pack (pva_attn_bwd): per step the backward
+    plan build (2 kernels + sort) and the backward (D, dQ, dK/dV kernels), with
+    a seeded dO.  FLOPs = 10 d per allowed pair per q head (S, dP, dV, dK, dQ;
+    the dQ and dK/dV passes each recompute S and dP, not counted)."""
+    import torch
+
+    from packed_varlen_attention_cu_gb300 import api
+    w, q, k, v, cu_np, flops_fwd, mask, params, hbm = ctx
+    dev = q.device
+    stream = torch.cuda.current_stream()
+    T, hq, d = q.shape
+    cu = torch.from_numpy(cu_np).to(dev)
+    wl = api.alloc_worklist(w.num_docs, mask, params, dev)
+    api.build_worklist(cu, mask, params, wl, stream)
+    out = torch.empty_like(q)
+    lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
+    api.attn_fwd(q, k, v, cu, mask, params, wl, out, lse, 0.0, None, stream)
+    dout = W.make_qkv(T, T, hq, k.shape[1], d, w.seed + 1000, device=str(dev))[0]
+    plan = api.alloc_bwd_plan(w.num_docs, mask, params, dev)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+
+    def step():
+        api.build_bwd_plan(wl, w.num_docs, mask, params, plan, stream)
+        api.attn_bwd(q, k, v, out, lse, dout, cu, w.num_docs, mask, params, wl, plan, dq, dk,
+                     dv, 0.0, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert api.worklist_error(wl) == 0
+    K = max(3, args.steps // 2)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(K):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    flops = flops_fwd * 2.5
+    t, f = aggregate(s.elapsed_time(e) / 1e3, flops * K, world)
+    return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "steps": K,
+            "ms_per_step": round(t / K * 1e3, 4),
+            "frac_of_peak": None,
+            "flops_per_step": flops, "gpu_launches_per_step": 3 + 4,
+            "note": "backward plan (plan kernel, chunk sort, merge rank) + D, dQ and dK/dV "
+                    "kernels, bf16 gradients; 10 d FLOPs per allowed pair per q head"}
+
+
 def run_libra_ratio(args, ctx):
     """Libra's example ("03 · 长文负载均衡" §1.1): the same token count as one
     40960-token document (pack A) or ten 4096-token documents (pack B); the
@@ -657,6 +710,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-zigzag", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--fit-cost", action="store_true",
                     help="fit the per-tile cost to per-CTA times of two warm-up runs")
     ap.add_argument("--refine-iters", type=int, default=20,
@@ -679,6 +733,11 @@ def main(argv=None):
     if not args.no_zigzag and ctx[0].cp:
         res["zigzag_cp"] = run_zigzag(args, ctx, world)
         res["zigzag_cp_fused"] = run_zigzag(args, ctx, world, fused=True)
+    if not args.no_backward:
+        bwd = run_backward(args, ctx, world)
+        if bwd is not None:
+            bwd["frac_of_peak"] = round(bwd["value"] / res["roofline"]["peak"], 4)
+            res["backward"] = bwd
     if not args.no_zigzag:
         disp = run_dispatch(args, ctx)
         if disp is not None:

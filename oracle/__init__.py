@@ -63,6 +63,10 @@ def lib():
         _lib.or_attention_bwd.restype = ctypes.c_int
         _lib.or_attention_bwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, i32,
                                           ctypes.POINTER(_Mask), ctypes.c_double, P, P, P]
+        _lib.or_attention_bwd_jobs.restype = ctypes.c_int
+        _lib.or_attention_bwd_jobs.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, i32,
+                                               ctypes.POINTER(_Mask), ctypes.c_double, P, i64,
+                                               P, i64, P, P, P]
         _lib.or_pair_count.restype = i64
         _lib.or_pair_count.argtypes = [i32, i32, P, i32, ctypes.POINTER(_Mask), i32]
         _lib.or_allowed_matrix.restype = ctypes.c_int
@@ -193,6 +197,34 @@ def attention_bwd(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray,
     if rc != 0:
         raise ValueError(f"or_attention_bwd failed ({rc})")
     return dq, dk, dv
+
+
+def attention_bwd_jobs(q_bits, k_bits, v_bits, do_bits, cu, mask: Mask, qjobs, kjobs,
+                       scale: Optional[float] = None):
+    """Sampled gradients: dq [nq, d] of (row, head) jobs, dk and dv [nk, d] of
+    (key, kv head) jobs, each by definition (bf16 bit patterns in)."""
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v_bits = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    do_bits = np.ascontiguousarray(do_bits, dtype=np.uint16)
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    qj = np.ascontiguousarray(qjobs, dtype=np.int32).reshape(-1, 2)
+    kj = np.ascontiguousarray(kjobs, dtype=np.int32).reshape(-1, 2)
+    Tq, Hq, d = q_bits.shape
+    Tk, Hkv, _ = k_bits.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.zeros((max(len(qj), 1), d))
+    dk = np.zeros((max(len(kj), 1), d))
+    dv = np.zeros((max(len(kj), 1), d))
+    m = mask.c()
+    rc = lib().or_attention_bwd_jobs(_ptr(q_bits), _ptr(k_bits), _ptr(v_bits), _ptr(do_bits), Tq,
+                                     Tk, Hq, Hkv, d, _ptr(cu), cu.shape[0] - 1, ctypes.byref(m),
+                                     float(scale), _ptr(qj), len(qj), _ptr(kj), len(kj), _ptr(dq),
+                                     _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError(f"or_attention_bwd_jobs failed ({rc})")
+    return dq[:len(qj)], dk[:len(kj)], dv[:len(kj)]
 
 
 def pair_count(cu: np.ndarray, mask: Mask, Tq: Optional[int] = None, Tk: Optional[int] = None,

@@ -448,6 +448,136 @@ int or_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     return 0;
 }
 
+/* The same gradients on sampled outputs: dQ of (row, head) jobs and dK, dV  */
+/* of (key, kv head) jobs, each from its definition (a key job visits every  */
+/* query row that may see the key and recomputes that row's LSE and D).      */
+/* Rows' statistics are computed by row_stats below.                         */
+static void row_stats(const ctx_t *c, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const uint16_t *dout, int32_t Hq, int32_t Hkv, int32_t d, double scale,
+                      int32_t i, int32_t h, double *lse, double *D) {
+    const int32_t G = Hq / Hkv, g = h / G;
+    const uint16_t *qi = q + ((int64_t)i * Hq + h) * d, *gi = dout + ((int64_t)i * Hq + h) * d;
+    int32_t lo[2], hi[2];
+    int nr = candidates(c, i, 0, lo, hi);
+    double mx = -INFINITY;
+    for (int r = 0; r < nr; ++r)
+        for (int32_t j = lo[r]; j < hi[r]; ++j) {
+            if (!allowed(c, i, j)) continue;
+            const uint16_t *kj = k + ((int64_t)j * Hkv + g) * d;
+            double dot = 0.0;
+            for (int32_t e = 0; e < d; ++e) dot += bf16_to_double(qi[e]) * bf16_to_double(kj[e]);
+            if (scale * dot > mx) mx = scale * dot;
+        }
+    if (mx == -INFINITY) {
+        *lse = -INFINITY;
+        *D = 0.0;
+        return;
+    }
+    double sum = 0.0, acc = 0.0;
+    for (int r = 0; r < nr; ++r)
+        for (int32_t j = lo[r]; j < hi[r]; ++j) {
+            if (!allowed(c, i, j)) continue;
+            const uint16_t *kj = k + ((int64_t)j * Hkv + g) * d;
+            const uint16_t *vj = v + ((int64_t)j * Hkv + g) * d;
+            double dot = 0.0, dd = 0.0;
+            for (int32_t e = 0; e < d; ++e) {
+                dot += bf16_to_double(qi[e]) * bf16_to_double(kj[e]);
+                dd += bf16_to_double(gi[e]) * bf16_to_double(vj[e]);
+            }
+            const double pexp = exp(scale * dot - mx);
+            sum += pexp;
+            acc += pexp * dd;
+        }
+    *lse = mx + log(sum);
+    *D = acc / sum;
+}
+
+int or_attention_bwd_jobs(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const uint16_t *dout, int32_t Tq, int32_t Tk, int32_t Hq, int32_t Hkv,
+                          int32_t d, const int32_t *cu, int32_t ndocs, const or_mask_t *m,
+                          double scale, const int32_t *qjobs, int64_t nq, const int32_t *kjobs,
+                          int64_t nk, double *dq, double *dk, double *dv) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    ctx_t c;
+    if (ctx_init(&c, cu, ndocs, Tq, Tk, m) != 0) return -2;
+    const int32_t G = Hq / Hkv;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t job = 0; job < nq; ++job) {
+        const int32_t i = qjobs[2 * job], h = qjobs[2 * job + 1], g = h / G;
+        double *o = dq + job * d;
+        for (int32_t e = 0; e < d; ++e) o[e] = 0.0;
+        if (i < 0 || i >= Tq || h < 0 || h >= Hq) {
+            err = 1;
+            continue;
+        }
+        double lse, D;
+        row_stats(&c, q, k, v, dout, Hq, Hkv, d, scale, i, h, &lse, &D);
+        if (lse == -INFINITY) continue;
+        const uint16_t *qi = q + ((int64_t)i * Hq + h) * d, *gi = dout + ((int64_t)i * Hq + h) * d;
+        int32_t lo[2], hi[2];
+        int nr = candidates(&c, i, 0, lo, hi);
+        for (int r = 0; r < nr; ++r)
+            for (int32_t j = lo[r]; j < hi[r]; ++j) {
+                if (!allowed(&c, i, j)) continue;
+                const uint16_t *kj = k + ((int64_t)j * Hkv + g) * d;
+                const uint16_t *vj = v + ((int64_t)j * Hkv + g) * d;
+                double dot = 0.0, dd = 0.0;
+                for (int32_t e = 0; e < d; ++e) {
+                    dot += bf16_to_double(qi[e]) * bf16_to_double(kj[e]);
+                    dd += bf16_to_double(gi[e]) * bf16_to_double(vj[e]);
+                }
+                const double ds = exp(scale * dot - lse) * (dd - D);
+                for (int32_t e = 0; e < d; ++e) o[e] += scale * ds * bf16_to_double(kj[e]);
+            }
+    }
+    for (int64_t job = 0; job < nk; ++job) {
+        const int32_t j = kjobs[2 * job], g = kjobs[2 * job + 1];
+        double *ok = dk + job * d, *ov = dv + job * d;
+        for (int32_t e = 0; e < d; ++e) ok[e] = ov[e] = 0.0;
+        if (j < 0 || j >= Tk || g < 0 || g >= Hkv) {
+            err = 1;
+            continue;
+        }
+        const uint16_t *kj = k + ((int64_t)j * Hkv + g) * d, *vj = v + ((int64_t)j * Hkv + g) * d;
+#pragma omp parallel
+        {
+            double *pk = (double *)calloc((size_t)d, sizeof(double));
+            double *pv = (double *)calloc((size_t)d, sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+            for (int32_t i = 0; i < Tq; ++i) {
+                if (!allowed(&c, i, j)) continue;
+                for (int32_t h = g * G; h < (g + 1) * G; ++h) {
+                    double lse, D;
+                    row_stats(&c, q, k, v, dout, Hq, Hkv, d, scale, i, h, &lse, &D);
+                    const uint16_t *qi = q + ((int64_t)i * Hq + h) * d;
+                    const uint16_t *gi = dout + ((int64_t)i * Hq + h) * d;
+                    double dot = 0.0, dd = 0.0;
+                    for (int32_t e = 0; e < d; ++e) {
+                        dot += bf16_to_double(qi[e]) * bf16_to_double(kj[e]);
+                        dd += bf16_to_double(gi[e]) * bf16_to_double(vj[e]);
+                    }
+                    const double p = exp(scale * dot - lse);
+                    const double ds = p * (dd - D);
+                    for (int32_t e = 0; e < d; ++e) {
+                        pk[e] += scale * ds * bf16_to_double(qi[e]);
+                        pv[e] += p * bf16_to_double(gi[e]);
+                    }
+                }
+            }
+#pragma omp critical
+            for (int32_t e = 0; e < d; ++e) {
+                ok[e] += pk[e];
+                ov[e] += pv[e];
+            }
+            free(pk);
+            free(pv);
+        }
+    }
+    ctx_free(&c);
+    return err ? -3 : 0;
+}
+
 /* Number of allowed (q row, k row) pairs, per head.  [P1] §1.1: this is     */
 /* the work term W_attn ~ sum_j l_j^2 of a pack.                             */
 int64_t or_pair_count(int32_t Tq, int32_t Tk, const int32_t *cu, int32_t ndocs,

@@ -41,6 +41,11 @@ int or_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      const uint16_t *dout, int32_t Tq, int32_t Tk, int32_t Hq, int32_t Hkv,
                      int32_t d, const int32_t *cu, int32_t ndocs, const or_mask_t *m,
                      double scale, double *dq, double *dk, double *dv);
+int or_attention_bwd_jobs(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const uint16_t *dout, int32_t Tq, int32_t Tk, int32_t Hq, int32_t Hkv,
+                          int32_t d, const int32_t *cu, int32_t ndocs, const or_mask_t *m,
+                          double scale, const int32_t *qjobs, int64_t nq, const int32_t *kjobs,
+                          int64_t nk, double *dq, double *dk, double *dv);
 int64_t or_pair_count(int32_t Tq, int32_t Tk, const int32_t *cu, int32_t ndocs,
                       const or_mask_t *m, int32_t brute);
 int or_allowed_matrix(int32_t Tq, int32_t Tk, const int32_t *cu, int32_t ndocs,

@@ -128,3 +128,28 @@ def test_bwd_plan_rejects_partly_overlapping_key_ranges():
     m = api.make_mask(W.MASK_SLICES, 20, 20, slices=sl)
     p = api.make_params(2, 2)
     assert api.lib().pva_bwd_plan_bytes(1, ctypes.byref(m), ctypes.byref(p)) == 0
+
+
+def test_bwd_128k_pack_sampled(oracle_mod):
+    """The bench's configuration (128K causal pack, 32 q / 8 kv heads, d = 128, bf16
+    gradients): sampled dq rows and dk/dv keys against the oracle, each by definition."""
+    w = W.zigzag_pack()
+    cu = w.cu_seqlens
+    T, hq, hkv, d = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
+    q, k, v = W.workload_qkv(w, device="cpu")
+    dout = W.make_qkv(T, T, hq, hkv, d, w.seed + 1000)[0]
+    mask = api.mask_for_workload(w)
+    got = _bwd(q, k, v, cu, mask, hq, hkv, dout, False)
+    rng = np.random.default_rng(7)
+    lens = np.diff(cu)
+    qj = np.stack([rng.integers(0, T, 48), rng.integers(0, hq, 48)], axis=1)
+    # keys: random ones, plus the first and last key of the longest document
+    big = int(np.argmax(lens))
+    kj = np.stack([rng.integers(0, T, 14), rng.integers(0, hkv, 14)], axis=1)
+    kj = np.concatenate([kj, [[cu[big], 0], [cu[big + 1] - 1, hkv - 1]]])
+    bits = [oracle_mod.bf16_bits(x) for x in (q, k, v, dout)]
+    rq, rk, rv = oracle_mod.attention_bwd_jobs(*bits, cu, oracle_mask(W.MASK_CAUSAL), qj, kj)
+    gq = got[0][qj[:, 0], qj[:, 1]]
+    gk = got[1][kj[:, 0], kj[:, 1]]
+    gv = got[2][kj[:, 0], kj[:, 1]]
+    _check((gq, gk, gv), (rq, rk, rv), "128K pack sampled")

@@ -112,3 +112,16 @@ def test_unseen_keys_get_no_gradient():
                                       oracle.bf16_bits(do), cu, m)
     assert np.all(dk[10:] == 0) and np.all(dv[10:] == 0)
     assert np.abs(dk[:10]).max() > 0 and np.abs(dq).max() > 0
+
+
+def test_sampled_jobs_equal_full_backward(case):
+    # every sampled output equals the full backward's entry (both by definition)
+    cu, q, k, v, do = case
+    bits = [oracle.bf16_bits(x) for x in (q, k, v, do)]
+    dq, dk, dv = oracle.attention_bwd(*bits, cu, oracle.Mask())
+    qj = np.array([[0, 0], [7, 3], [19, 1], [20, 2], [39, 3], [27, 0]])
+    kj = np.array([[0, 0], [5, 1], [19, 0], [26, 1], [39, 1]])
+    sq, sk, sv = oracle.attention_bwd_jobs(*bits, cu, oracle.Mask(), qj, kj)
+    np.testing.assert_allclose(sq, dq[qj[:, 0], qj[:, 1]], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(sk, dk[kj[:, 0], kj[:, 1]], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(sv, dv[kj[:, 0], kj[:, 1]], rtol=1e-12, atol=1e-13)
