@@ -62,6 +62,7 @@ struct BwdParams {
 
 struct BShared {
     uint64_t a_full, a_empty, s_full, p_full, o_full, o_empty, done;
+    uint64_t s2_full[2], p2_full[2];  // bwd_dkdv: per half-item tensor-memory buffer
     uint64_t r_full[8], r_empty[8];
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -142,6 +143,10 @@ __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_
     mbar_init(&sh.o_full, 1);
     mbar_init(&sh.o_empty, elem_threads / 32);
     mbar_init(&sh.done, 1);
+    for (int b = 0; b < 2; ++b) {
+        mbar_init(&sh.s2_full[b], 1);
+        mbar_init(&sh.p2_full[b], 4);
+    }
     for (int s = 0; s < stages; ++s) {
         mbar_init(&sh.r_full[s], 1);
         mbar_init(&sh.r_empty[s], 1);
@@ -441,14 +446,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv,
                     const __grid_constant__ CUtensorMap tmdo, const BwdParams p) {
+    // tmq and tmdo have 64-row boxes here: the ring holds half-items, the 64
+    // queries [64 hf, 64 hf + 64) of a q tile as (Q, dO) halves of 8 KB per
+    // 64-column atom (a stage: Q half at +0, dO half at +D/64 * 8 KB)
     using C = BCfg<D>;
-    constexpr int kItems = C::kStages / 2;  // (Q, dO) pairs in the ring
+    constexpr int kItems = C::kStages;          // half-items in the ring
+    constexpr int kHalfBytes = 64 * D * 2;      // one 64-row bf16 half tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* sK = smem;
     uint8_t* sV = smem + C::kTileBytes;
-    uint8_t* sR = smem + 2 * C::kTileBytes;  // item x: Q at 2x, dO at 2x + 1
+    uint8_t* sR = smem + 2 * C::kTileBytes;  // half-item stage x at x * 2 * kHalfBytes
     __shared__ BShared sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const WlHeader* h = reinterpret_cast<const WlHeader*>(p.wl);
@@ -513,20 +522,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         int32_t qlo, qhi;
                         bwd_q_span(sm, u.kt, qlo, qhi);
                         for (int32_t t = qlo; t < qhi && live; ++t) {
-                            const uint32_t st = it % kItems;
-                            live = mbar_wait(&sh.r_empty[st], ((it / kItems) & 1) ^ 1, abort_flag,
-                                             err_word, kErrTimeoutBase + 32, kWaitNs);
-                            if (!live) break;
-                            mbar_arrive_expect_tx(&sh.r_full[st], 2 * C::kTileBytes);
-                            uint8_t* dq_ = sR + (2 * st) * C::kTileBytes;
-                            uint8_t* ddo = sR + (2 * st + 1) * C::kTileBytes;
-                            for (int b = 0; b < D / 64; ++b) {
-                                tma_load_3d(dq_ + b * 16384, &tmq, &sh.r_full[st], b * 64, head,
-                                            sm.q_row0 + t * 128);
-                                tma_load_3d(ddo + b * 16384, &tmdo, &sh.r_full[st], b * 64, head,
-                                            sm.q_row0 + t * 128);
+                            const int32_t nq = min(128, sm.q_len - t * 128);
+                            const int32_t halves = nq > 64 ? 2 : 1;
+                            for (int32_t hf = 0; hf < halves && live; ++hf) {
+                                const uint32_t st = it % kItems;
+                                live = mbar_wait(&sh.r_empty[st], ((it / kItems) & 1) ^ 1,
+                                                 abort_flag, err_word, kErrTimeoutBase + 32,
+                                                 kWaitNs);
+                                if (!live) break;
+                                mbar_arrive_expect_tx(&sh.r_full[st], 2 * kHalfBytes);
+                                uint8_t* dq_ = sR + st * 2 * kHalfBytes;
+                                uint8_t* ddo = dq_ + kHalfBytes;
+                                for (int b = 0; b < D / 64; ++b) {
+                                    tma_load_3d(dq_ + b * 8192, &tmq, &sh.r_full[st], b * 64, head,
+                                                sm.q_row0 + t * 128 + hf * 64);
+                                    tma_load_3d(ddo + b * 8192, &tmdo, &sh.r_full[st], b * 64,
+                                                head, sm.q_row0 + t * 128 + hf * 64);
+                                }
+                                ++it;
                             }
-                            ++it;
                         }
                     }
                 }
@@ -543,13 +557,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer (whole warp)
-        uint32_t it = 0, a_it = 0, p_cnt = 0, o_cnt = 0;
+        // Half-items: the 64 queries [64 hf, 64 hf + 64) of one (head, slice, q tile)
+        // item.  S^T and dP^T of half-item u go to buffer u % 2 (64 columns each);
+        // they are issued before dV/dK of half-item u - 1, so the element-wise
+        // warps work on u - 1 while the tensor pipe computes u.
+        uint32_t it = 0, a_it = 0, gu = 0, o_cnt = 0;
         bool live = true;
         const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
         const uint64_t dV = sdesc_sw128(smem_u32(sV), 16, 1024);
-        const uint64_t dRn = sdesc_sw128(smem_u32(sR), 16, 1024);     // K-major
-        const uint64_t dRm = sdesc_sw128(smem_u32(sR), 16384, 1024);  // MN-major
-        const uint32_t tS = tmem, tP = tmem + 128, tV = tmem + 256, tK = tmem + 256 + D;
+        const uint64_t dRn = sdesc_sw128(smem_u32(sR), 16, 1024);    // K-major
+        const uint64_t dRm = sdesc_sw128(smem_u32(sR), 8192, 1024);  // MN-major, 64-row atoms
+        constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, false);
+        const uint32_t tVa = tmem + 256, tKa = tmem + 256 + D;
+        // the half-item whose dV/dK MMAs are still to be issued
+        bool pend = false, first = true;
+        uint32_t pend_u = 0, pend_st = 0;
+        auto finish_pending = [&]() -> bool {
+            const uint32_t b = pend_u & 1;
+            if (!mbar_wait_warp(&sh.p2_full[b], (pend_u >> 1) & 1, abort_flag, err_word,
+                                kErrTimeoutBase + 36, kWaitNs))
+                return false;
+            tc_fence_after();
+            const uint64_t oQ = (pend_st * 2 * kHalfBytes) >> 4;
+            const uint64_t oO = (pend_st * 2 * kHalfBytes + kHalfBytes) >> 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_ts_elect(tVa, tmem + 64 * b + k * 8, dRm + oO + k * 128, C::kIdescNN,
+                             (!first || k > 0) ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_ts_elect(tKa, tmem + 128 + 64 * b + k * 8, dRm + oQ + k * 128, C::kIdescNN,
+                             (!first || k > 0) ? 1u : 0u);
+            first = false;
+            mma_commit_elect(&sh.r_empty[pend_st]);
+            pend = false;
+            return true;
+        };
         for (int32_t rd = 0; pos_of(rd) < n && live; ++rd) {
             const BwdUnit u = bunits[order[pos_of(rd)]];
             if (u.cost <= 1) continue;
@@ -559,45 +602,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             live = mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
                                   kErrTimeoutBase + 34, kWaitNs);
             if (!live) break;
-            const int32_t nitems = (int32_t)(u.cost - 1);
-            for (int32_t j = 0; j < nitems && live; ++j) {
-                {
-                    const uint32_t st = it % kItems;
-                    live = mbar_wait_warp(&sh.r_full[st], (it / kItems) & 1, abort_flag, err_word,
-                                          kErrTimeoutBase + 35, kWaitNs);
-                    if (!live) break;
-                    tc_fence_after();
-                    const uint64_t oQ = ((2 * st) * C::kTileBytes) >> 4;
-                    const uint64_t oO = ((2 * st + 1) * C::kTileBytes) >> 4;
+            first = true;
+            for (int32_t hh = 0; hh < G && live; ++hh) {
+                for (int32_t m = 0; m < u.gcount && live; ++m) {
+                    const WlSlice sm = slices[gsl[u.gbegin + m]];
+                    int32_t qlo, qhi;
+                    bwd_q_span(sm, u.kt, qlo, qhi);
+                    for (int32_t t = qlo; t < qhi && live; ++t) {
+                        const int32_t nq = min(128, sm.q_len - t * 128);
+                        const uint32_t halves = nq > 64 ? 2 : 1;
+                        for (uint32_t hf = 0; hf < halves && live; ++hf) {
+                            const uint32_t st = it % kItems;
+                            live = mbar_wait_warp(&sh.r_full[st], (it / kItems) & 1, abort_flag,
+                                                  err_word, kErrTimeoutBase + 35, kWaitNs);
+                            if (!live) break;
+                            tc_fence_after();
+                            const uint32_t b = gu & 1;
+                            const uint64_t oQ = (st * 2 * kHalfBytes) >> 4;
+                            const uint64_t oO = (st * 2 * kHalfBytes + kHalfBytes) >> 4;
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
-                        mma_ss_elect(tS, dK + off16, dRn + oQ + off16, C::kIdescNT, k > 0);
+                            for (int k = 0; k < D / 16; ++k) {
+                                // K (resident, 128-row atoms) and the Q half (64-row atoms)
+                                const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
+                                const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                                mma_ss_elect(tmem + 64 * b, dK + off16, dRn + oQ + kq, kIdescHalf,
+                                             k > 0);
+                            }
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k) {
+                                const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
+                                const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                                mma_ss_elect(tmem + 128 + 64 * b, dV + off16, dRn + oO + kq,
+                                             kIdescHalf, k > 0);
+                            }
+                            mma_commit_elect(&sh.s2_full[b]);
+                            if (pend && !finish_pending()) {
+                                live = false;
+                                break;
+                            }
+                            pend = true;
+                            pend_u = gu;
+                            pend_st = st;
+                            ++gu;
+                            ++it;
+                        }
                     }
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
-                        mma_ss_elect(tP, dV + off16, dRn + oO + off16, C::kIdescNT, k > 0);
-                    }
-                    mma_commit_elect(&sh.s_full);
-                    live = mbar_wait_warp(&sh.p_full, p_cnt & 1, abort_flag, err_word,
-                                          kErrTimeoutBase + 36, kWaitNs);
-                    if (!live) break;
-                    ++p_cnt;
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        mma_ts_elect(tV, tS + k * 8, dRm + oO + k * 128, C::kIdescNN,
-                                     (j > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        mma_ts_elect(tK, tP + k * 8, dRm + oQ + k * 128, C::kIdescNN,
-                                     (j > 0 || k > 0) ? 1u : 0u);
-                    mma_commit_elect(&sh.r_empty[st]);
-                    ++it;
                 }
             }
             if (!live) break;
+            if (pend && !finish_pending()) break;
             mma_commit_elect(&sh.a_empty);
             mma_commit_elect(&sh.o_full);
             ++o_cnt;
@@ -610,9 +663,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- P^T, dS^T and the dK/dV epilogue
         const int kr = (warp & 3) * 32 + lane;  // key row = tensor-memory lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_base, tP = tmem + lane_base + 128,
-                       tV = tmem + lane_base + 256, tK = tmem + lane_base + 256 + D;
-        uint32_t s_cnt = 0, o_cnt = 0;
+        const uint32_t tS = tmem + lane_base, tV = tmem + lane_base + 256,
+                       tK = tmem + lane_base + 256 + D;
+        uint32_t gu = 0, o_cnt = 0;
         bool live = true;
         for (int32_t rd = 0; pos_of(rd) < n && live; ++rd) {
             const BwdUnit u = bunits[order[pos_of(rd)]];
@@ -645,51 +698,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                         c_lo = max(c_lo, k_pos - cpos0);
                         if (s.window > 0) c_hi = min(c_hi, k_pos + s.window - cpos0);
                     }
-                    live = mbar_wait(&sh.s_full, s_cnt & 1, abort_flag, err_word,
-                                     kErrTimeoutBase + 37, kWaitNs);
-                    if (!live) break;
-                    ++s_cnt;
-                    tc_fence_after();
+                    const uint32_t halves = nq > 64 ? 2 : 1;
+                    for (uint32_t hf = 0; hf < halves && live; ++hf, ++gu) {
+                        const uint32_t b = gu & 1;
+                        live = mbar_wait(&sh.s2_full[b], (gu >> 1) & 1, abort_flag, err_word,
+                                         kErrTimeoutBase + 37, kWaitNs);
+                        if (!live) break;
+                        tc_fence_after();
+                        const uint32_t tSb = tS + 64 * b, tPb = tS + 128 + 64 * b;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        // LSE (log2) and D of query column c*32 + lane, shared by shuffles
-                        const int qc = c * 32 + lane;
-                        float my_l2 = INFINITY, my_d = 0.f;  // no query: every P is 0
-                        if (qc < nq) {
-                            const int64_t li = (int64_t)head * p.q_tokens + qrow0 + qc;
-                            const float l = p.lse[li];
-                            if (l != -INFINITY) my_l2 = l * 1.4426950408889634f;
-                            my_d = p.dvec[li];
-                        }
-                        uint32_t sv[32], pv[32];
-                        tmem_ld32(tS + c * 32, sv);
-                        tmem_ld32(tP + c * 32, pv);
-                        tmem_ld_wait(sv);
-                        tmem_ld_wait(pv);
-                        uint32_t pw[32], dw[32];
+                        for (int c = 0; c < 2; ++c) {
+                            // LSE (log2) and D of query column 64 hf + 32 c + lane, by shuffles
+                            const int qc = (int)hf * 64 + c * 32 + lane;
+                            float my_l2 = INFINITY, my_d = 0.f;  // no query: every P is 0
+                            if (qc < nq) {
+                                const int64_t li = (int64_t)head * p.q_tokens + qrow0 + qc;
+                                const float l = p.lse[li];
+                                if (l != -INFINITY) my_l2 = l * 1.4426950408889634f;
+                                my_d = p.dvec[li];
+                            }
+                            uint32_t sv[32], pv[32];
+                            tmem_ld32(tSb + c * 32, sv);
+                            tmem_ld32(tPb + c * 32, pv);
+                            tmem_ld_wait(sv);
+                            tmem_ld_wait(pv);
+                            uint32_t pw[32], dw[32];
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const int col = c * 32 + e;
-                            const float l0 = __shfl_sync(0xffffffffu, my_l2, e);
-                            const float l1 = __shfl_sync(0xffffffffu, my_l2, e + 1);
-                            const float d0 = __shfl_sync(0xffffffffu, my_d, e);
-                            const float d1 = __shfl_sync(0xffffffffu, my_d, e + 1);
-                            float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - l0);
-                            float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - l1);
-                            if (col < c_lo || col >= c_hi) p0 = 0.f;
-                            if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
-                            const float g0 = p0 * (__uint_as_float(pv[e]) - d0);
-                            const float g1 = p1 * (__uint_as_float(pv[e + 1]) - d1);
-                            pw[e >> 1] = pack_bf16x2(p0, p1);
-                            dw[e >> 1] = pack_bf16x2(g0, g1);
+                            for (int e = 0; e < 32; e += 2) {
+                                const int col = (int)hf * 64 + c * 32 + e;
+                                const float l0 = __shfl_sync(0xffffffffu, my_l2, e);
+                                const float l1 = __shfl_sync(0xffffffffu, my_l2, e + 1);
+                                const float d0 = __shfl_sync(0xffffffffu, my_d, e);
+                                const float d1 = __shfl_sync(0xffffffffu, my_d, e + 1);
+                                float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - l0);
+                                float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - l1);
+                                if (col < c_lo || col >= c_hi) p0 = 0.f;
+                                if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                                const float g0 = p0 * (__uint_as_float(pv[e]) - d0);
+                                const float g1 = p1 * (__uint_as_float(pv[e + 1]) - d1);
+                                pw[e >> 1] = pack_bf16x2(p0, p1);
+                                dw[e >> 1] = pack_bf16x2(g0, g1);
+                            }
+                            tmem_st16(tSb + c * 16, pw);
+                            tmem_st16(tPb + c * 16, dw);
                         }
-                        tmem_st16(tS + c * 16, pw);
-                        tmem_st16(tP + c * 16, dw);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sh.p2_full[b]);
                     }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sh.p_full);
                 }
                 }
             }
@@ -726,8 +783,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 pva_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                      const CUtensorMap& mdo, const BwdParams& bp, int32_t dkdv_ctas,
-                      cudaStream_t st) {
+                      const CUtensorMap& mdo, const CUtensorMap& mq64, const CUtensorMap& mdo64,
+                      const BwdParams& bp, int32_t dkdv_ctas, cudaStream_t st) {
     const int grid_pre = 4 * bp.num_ctas;
     bwd_pre_kernel<<<grid_pre, 256, 0, st>>>(bp);
     auto kq = bwd_dq_kernel<D>;
@@ -738,7 +795,7 @@ pva_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
             cudaSuccess)
         return PVA_ERR_CUDA;
     kq<<<bp.num_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq, mk, mv, mdo, bp);
-    kk<<<dkdv_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq, mk, mv, mdo, bp);
+    kk<<<dkdv_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq64, mk, mv, mdo64, bp);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
 
@@ -797,14 +854,16 @@ extern "C" pva_status pva_attn_bwd(const void* q, const void* k, const void* v, 
     // the plan's D scratch (its header is checked on the device)
     const int64_t off_dvec = bwd_plan_dvec_offset(num_docs, mask, params);
     if (off_dvec < 0) return PVA_ERR_INVALID_ARG;
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mq64, mdo64;
     const void* kp = mask->k_tokens > 0 ? k : q;
     const void* vp = mask->k_tokens > 0 ? v : q;
     const int32_t kh = mask->k_tokens > 0 ? params->num_kv_heads : params->num_q_heads;
     if (!make_map(&mq, q, mask->q_tokens, params->num_q_heads, head_dim) ||
         !make_map(&mk, kp, mask->k_tokens, kh, head_dim) ||
         !make_map(&mv, vp, mask->k_tokens, kh, head_dim) ||
-        !make_map(&mdo, dout, mask->q_tokens, params->num_q_heads, head_dim))
+        !make_map(&mdo, dout, mask->q_tokens, params->num_q_heads, head_dim) ||
+        !make_map(&mq64, q, mask->q_tokens, params->num_q_heads, head_dim, 64) ||
+        !make_map(&mdo64, dout, mask->q_tokens, params->num_q_heads, head_dim, 64))
         return PVA_ERR_CUDA;
     BwdParams bp;
     bp.wl = reinterpret_cast<const uint8_t*>(worklist_dev);
@@ -825,6 +884,6 @@ extern "C" pva_status pva_attn_bwd(const void* q, const void* k, const void* v, 
     bp.d = head_dim;
     bp.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
     bp.scale_log2 = bp.scale * 1.4426950408889634f;
-    return head_dim == 128 ? launch_bwd<128>(mq, mk, mv, mdo, bp, nc, st)
-                           : launch_bwd<64>(mq, mk, mv, mdo, bp, nc, st);
+    return head_dim == 128 ? launch_bwd<128>(mq, mk, mv, mdo, mq64, mdo64, bp, nc, st)
+                           : launch_bwd<64>(mq, mk, mv, mdo, mq64, mdo64, bp, nc, st);
 }

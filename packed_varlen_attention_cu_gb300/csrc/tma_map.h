@@ -26,14 +26,15 @@ inline EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [rows, heads, d] bf16 viewed as a 3-D tensor (d, heads, rows); 128-row x
-// 64-element boxes with 128-byte swizzle; rows past the end read as zero.
-inline bool make_map(CUtensorMap* m, const void* ptr, int32_t rows, int32_t heads, int32_t d) {
+// [rows, heads, d] bf16 viewed as a 3-D tensor (d, heads, rows); box_rows-row
+// x 64-element boxes with 128-byte swizzle; rows past the end read as zero.
+inline bool make_map(CUtensorMap* m, const void* ptr, int32_t rows, int32_t heads, int32_t d,
+                     uint32_t box_rows = 128) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
-    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t box[3] = {64, 1, box_rows};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
