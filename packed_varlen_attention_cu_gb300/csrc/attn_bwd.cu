@@ -42,7 +42,6 @@ struct BCfg {
     // bwd_dq: Q, dO, then a K/V ring; bwd_dkdv: K, V, then a (Q, dO) ring
     static constexpr int kStages = D == 128 ? 4 : 8;
     static constexpr int kSmem = 2 * kTileBytes + kStages * kTileBytes + 1024;
-    static constexpr uint32_t kIdescNT = idesc_bf16_f32(128, 128, false);  // A, B K-major
     static constexpr uint32_t kIdescNN = idesc_bf16_f32(128, D, true);     // B MN-major
 };
 
@@ -61,8 +60,8 @@ struct BwdParams {
 };
 
 struct BShared {
-    uint64_t a_full, a_empty, s_full, p_full, o_full, o_empty, done;
-    uint64_t s2_full[2], p2_full[2];  // bwd_dkdv: per half-item tensor-memory buffer
+    uint64_t a_full, a_empty, o_full, o_empty, done;
+    uint64_t s2_full[2], p2_full[2];  // per half-item tensor-memory buffer
     uint64_t r_full[8], r_empty[8];
     uint32_t tmem_base;
     int32_t abort_flag;
@@ -138,14 +137,12 @@ __device__ __forceinline__ void store_zero_row(void* base, int64_t row_elem, boo
 __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_threads) {
     mbar_init(&sh.a_full, 1);
     mbar_init(&sh.a_empty, 1);
-    mbar_init(&sh.s_full, 1);
-    mbar_init(&sh.p_full, 4);  // one arrival per element-wise warp
     mbar_init(&sh.o_full, 1);
     mbar_init(&sh.o_empty, elem_threads / 32);
     mbar_init(&sh.done, 1);
     for (int b = 0; b < 2; ++b) {
         mbar_init(&sh.s2_full[b], 1);
-        mbar_init(&sh.p2_full[b], 4);
+        mbar_init(&sh.p2_full[b], 4);  // one arrival per element-wise warp
     }
     for (int s = 0; s < stages; ++s) {
         mbar_init(&sh.r_full[s], 1);
@@ -157,15 +154,20 @@ __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_
 
 // ==================================================================== dQ
 // Per query sub-tile (forward worklist units, sub-tiles one after the other):
-// a_full/a_empty guard the Q and dO tiles, r_full/r_empty the K/V ring (items
-// K_j, V_j in order), s_full: S and dP computed, p_full: dS stored over S,
+// a_full/a_empty guard the Q and dO tiles; the keys stream as half-items (64
+// keys [64 hf, 64 hf + 64) of a kv tile: K and V halves, 64-row TMA boxes)
+// through a ring (r_full/r_empty).  S and dP of half-item u (N = 64) go to one
+// of two 64-column buffers (s2_full/p2_full) and are issued before dQ += dS K
+// of half-item u - 1, so dS of u - 1 is computed while the pipe works on u.
 // o_full/o_empty: dQ accumulated / read out.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                   const BwdParams p) {
+    // tmk and tmv have 64-row boxes here (key half-items)
     using C = BCfg<D>;
+    constexpr int kHalfBytes = 64 * D * 2;  // one 64-row bf16 half tile; a stage holds K and V halves
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -237,18 +239,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const WlRun run = runs[u.run_begin + rr];
                         const WlSlice s = slices[run.slice];
                         for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
-                            const int32_t krow = s.k_row0 + jt * 128;
-                            for (int kv = 0; kv < 2 && live; ++kv) {
+                            const int32_t halves = min(128, s.k_len - jt * 128) > 64 ? 2 : 1;
+                            for (int32_t hf = 0; hf < halves && live; ++hf) {
+                                const int32_t krow = s.k_row0 + jt * 128 + hf * 64;
                                 const uint32_t st = it % C::kStages;
                                 live = mbar_wait(&sh.r_empty[st], ((it / C::kStages) & 1) ^ 1,
                                                  abort_flag, err_word, kErrTimeoutBase + 22,
                                                  kWaitNs);
                                 if (!live) break;
-                                mbar_arrive_expect_tx(&sh.r_full[st], C::kTileBytes);
-                                for (int b = 0; b < D / 64; ++b)
-                                    tma_load_3d(sKV + st * C::kTileBytes + b * 16384,
-                                                kv == 0 ? &tmk : &tmv, &sh.r_full[st], b * 64,
+                                mbar_arrive_expect_tx(&sh.r_full[st], 2 * kHalfBytes);
+                                uint8_t* dk_ = sKV + st * 2 * kHalfBytes;
+                                for (int b = 0; b < D / 64; ++b) {
+                                    tma_load_3d(dk_ + b * 8192, &tmk, &sh.r_full[st], b * 64,
                                                 u.kvh, krow);
+                                    tma_load_3d(dk_ + kHalfBytes + b * 8192, &tmv, &sh.r_full[st],
+                                                b * 64, u.kvh, krow);
+                                }
                                 ++it;
                             }
                         }
@@ -267,13 +273,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer (whole warp)
-        uint32_t it = 0, a_it = 0, p_cnt = 0, o_cnt = 0;
+        uint32_t it = 0, a_it = 0, gu = 0, o_cnt = 0;
         bool live = true;
         const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t dDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
-        const uint64_t dKn = sdesc_sw128(smem_u32(sKV), 16, 1024);     // K-major (S, dP)
-        const uint64_t dKm = sdesc_sw128(smem_u32(sKV), 16384, 1024);  // MN-major (dQ)
-        const uint32_t tS = tmem, tP = tmem + 128, tQ = tmem + 256;
+        const uint64_t dKn = sdesc_sw128(smem_u32(sKV), 16, 1024);    // K-major, 64-row atoms
+        const uint64_t dKm = sdesc_sw128(smem_u32(sKV), 8192, 1024);  // MN-major, 64-row atoms
+        constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, false);
+        const uint32_t tQa = tmem + 256;
+        bool pend = false, first = true;
+        uint32_t pend_u = 0, pend_st = 0;
+        auto finish_pending = [&]() -> bool {
+            const uint32_t b = pend_u & 1;
+            if (!mbar_wait_warp(&sh.p2_full[b], (pend_u >> 1) & 1, abort_flag, err_word,
+                                kErrTimeoutBase + 26, kWaitNs))
+                return false;
+            tc_fence_after();
+            const uint64_t oK = (pend_st * 2 * kHalfBytes) >> 4;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_ts_elect(tQa, tmem + 64 * b + k * 8, dKm + oK + k * 128, C::kIdescNN,
+                             (!first || k > 0) ? 1u : 0u);
+            first = false;
+            mma_commit_elect(&sh.r_empty[pend_st]);
+            pend = false;
+            return true;
+        };
         for (int32_t ui = ub; ui < ue && live; ++ui) {
             const WlUnit u = units[ui];
             if (u.ntiles == 0) continue;
@@ -285,46 +310,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 live = mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
                                       kErrTimeoutBase + 24, kWaitNs);
                 if (!live) break;
-                int32_t j = 0;
+                first = true;
                 for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
                     const WlRun run = runs[u.run_begin + rr];
-                    for (int32_t jt = run.lo; jt < run.hi && live; ++jt, ++j) {
-                        const uint32_t stk = it % C::kStages, stv = (it + 1) % C::kStages;
-                        live = mbar_wait_warp(&sh.r_full[stk], (it / C::kStages) & 1, abort_flag,
-                                              err_word, kErrTimeoutBase + 25, kWaitNs);
-                        if (!live) break;
-                        live = mbar_wait_warp(&sh.r_full[stv], ((it + 1) / C::kStages) & 1,
-                                              abort_flag, err_word, kErrTimeoutBase + 25, kWaitNs);
-                        if (!live) break;
-                        tc_fence_after();
-                        const uint64_t oK = (stk * C::kTileBytes) >> 4, oV = (stv * C::kTileBytes) >> 4;
+                    const WlSlice s = slices[run.slice];
+                    for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
+                        const int32_t halves = min(128, s.k_len - jt * 128) > 64 ? 2 : 1;
+                        for (int32_t hf = 0; hf < halves && live; ++hf) {
+                            const uint32_t st = it % C::kStages;
+                            live = mbar_wait_warp(&sh.r_full[st], (it / C::kStages) & 1,
+                                                  abort_flag, err_word, kErrTimeoutBase + 25,
+                                                  kWaitNs);
+                            if (!live) break;
+                            tc_fence_after();
+                            const uint32_t b = gu & 1;
+                            const uint64_t oK = (st * 2 * kHalfBytes) >> 4;
+                            const uint64_t oV = (st * 2 * kHalfBytes + kHalfBytes) >> 4;
 #pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
-                            mma_ss_elect(tS, dQd + off16, dKn + oK + off16, C::kIdescNT, k > 0);
+                            for (int k = 0; k < D / 16; ++k) {
+                                // Q, dO (128-row atoms) against the K, V halves (64-row atoms)
+                                const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                                const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
+                                mma_ss_elect(tmem + 64 * b, dQd + off16, dKn + oK + kq, kIdescHalf,
+                                             k > 0);
+                            }
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k) {
+                                const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                                const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
+                                mma_ss_elect(tmem + 128 + 64 * b, dDO + off16, dKn + oV + kq,
+                                             kIdescHalf, k > 0);
+                            }
+                            mma_commit_elect(&sh.s2_full[b]);
+                            if (pend && !finish_pending()) {
+                                live = false;
+                                break;
+                            }
+                            pend = true;
+                            pend_u = gu;
+                            pend_st = st;
+                            ++gu;
+                            ++it;
                         }
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
-                            mma_ss_elect(tP, dDO + off16, dKn + oV + off16, C::kIdescNT, k > 0);
-                        }
-                        mma_commit_elect(&sh.s_full);
-                        // V_j is read by dP only
-                        mma_commit_elect(&sh.r_empty[stv]);
-                        live = mbar_wait_warp(&sh.p_full, p_cnt & 1, abort_flag, err_word,
-                                              kErrTimeoutBase + 26, kWaitNs);
-                        if (!live) break;
-                        ++p_cnt;
-                        tc_fence_after();
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            mma_ts_elect(tQ, tS + k * 8, dKm + oK + k * 128, C::kIdescNN,
-                                         (j > 0 || k > 0) ? 1u : 0u);
-                        mma_commit_elect(&sh.r_empty[stk]);
-                        it += 2;
                     }
                 }
                 if (!live) break;
+                if (pend && !finish_pending()) break;
                 mma_commit_elect(&sh.a_empty);  // Q, dO read by the last MMAs
                 mma_commit_elect(&sh.o_full);
                 ++o_cnt;
@@ -338,9 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- dS and the dQ epilogue
         const int r = (warp & 3) * 32 + lane;  // query row = tensor-memory lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_base, tP = tmem + lane_base + 128,
-                       tQ = tmem + lane_base + 256;
-        uint32_t s_cnt = 0, o_cnt = 0;
+        const uint32_t tS = tmem + lane_base, tQ = tmem + lane_base + 256;
+        uint32_t gu = 0, o_cnt = 0;
         bool live = true;
         for (int32_t ui = ub; ui < ue && live; ++ui) {
             const WlUnit u = units[ui];
@@ -372,39 +402,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
                         const int32_t kt0 = jt * 128;
                         const int32_t c_hi = min(128, lim_hi - kt0), c_lo = max(0, lim_lo - kt0);
-                        live = mbar_wait(&sh.s_full, s_cnt & 1, abort_flag, err_word,
-                                         kErrTimeoutBase + 27, kWaitNs);
-                        if (!live) break;
-                        ++s_cnt;
-                        tc_fence_after();
+                        const int32_t halves = min(128, s.k_len - kt0) > 64 ? 2 : 1;
+                        for (int32_t hf = 0; hf < halves && live; ++hf, ++gu) {
+                            const uint32_t b = gu & 1;
+                            live = mbar_wait(&sh.s2_full[b], (gu >> 1) & 1, abort_flag, err_word,
+                                             kErrTimeoutBase + 27, kWaitNs);
+                            if (!live) break;
+                            tc_fence_after();
+                            const uint32_t tSb = tS + 64 * b, tPb = tS + 128 + 64 * b;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t sv[32], pv[32];
-                            tmem_ld32(tS + c * 32, sv);
-                            tmem_ld32(tP + c * 32, pv);
-                            tmem_ld_wait(sv);
-                            tmem_ld_wait(pv);
-                            uint32_t ds[16];
+                            for (int c = 0; c < 2; ++c) {
+                                uint32_t sv[32], pv[32];
+                                tmem_ld32(tSb + c * 32, sv);
+                                tmem_ld32(tPb + c * 32, pv);
+                                tmem_ld_wait(sv);
+                                tmem_ld_wait(pv);
+                                uint32_t dsw[32];
 #pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const int col = c * 32 + e;
-                                float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - lse2);
-                                float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lse2);
-                                if (col < c_lo || col >= c_hi) p0 = 0.f;
-                                if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
-                                const float g0 = p0 * (__uint_as_float(pv[e]) - dd);
-                                const float g1 = p1 * (__uint_as_float(pv[e + 1]) - dd);
-                                ds[e >> 1] = pack_bf16x2(g0, g1);
+                                for (int e = 0; e < 32; e += 2) {
+                                    const int col = hf * 64 + c * 32 + e;
+                                    float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - lse2);
+                                    float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lse2);
+                                    if (col < c_lo || col >= c_hi) p0 = 0.f;
+                                    if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                                    const float g0 = p0 * (__uint_as_float(pv[e]) - dd);
+                                    const float g1 = p1 * (__uint_as_float(pv[e + 1]) - dd);
+                                    dsw[e >> 1] = pack_bf16x2(g0, g1);
+                                }
+                                tmem_st16(tSb + c * 16, dsw);
                             }
-                            uint32_t dsw[32];
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) dsw[e] = ds[e];
-                            tmem_st16(tS + c * 16, dsw);
+                            tmem_st_wait();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&sh.p2_full[b]);
                         }
-                        tmem_st_wait();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&sh.p_full);
                     }
                 }
                 if (!live) break;
@@ -784,7 +815,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 pva_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                       const CUtensorMap& mdo, const CUtensorMap& mq64, const CUtensorMap& mdo64,
-                      const BwdParams& bp, int32_t dkdv_ctas, cudaStream_t st) {
+                      const CUtensorMap& mk64, const CUtensorMap& mv64, const BwdParams& bp,
+                      int32_t dkdv_ctas, cudaStream_t st) {
     const int grid_pre = 4 * bp.num_ctas;
     bwd_pre_kernel<<<grid_pre, 256, 0, st>>>(bp);
     auto kq = bwd_dq_kernel<D>;
@@ -794,7 +826,7 @@ pva_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
         cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem) !=
             cudaSuccess)
         return PVA_ERR_CUDA;
-    kq<<<bp.num_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq, mk, mv, mdo, bp);
+    kq<<<bp.num_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq, mk64, mv64, mdo, bp);
     kk<<<dkdv_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq64, mk, mv, mdo64, bp);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
@@ -854,7 +886,7 @@ extern "C" pva_status pva_attn_bwd(const void* q, const void* k, const void* v, 
     // the plan's D scratch (its header is checked on the device)
     const int64_t off_dvec = bwd_plan_dvec_offset(num_docs, mask, params);
     if (off_dvec < 0) return PVA_ERR_INVALID_ARG;
-    CUtensorMap mq, mk, mv, mdo, mq64, mdo64;
+    CUtensorMap mq, mk, mv, mdo, mq64, mdo64, mk64, mv64;
     const void* kp = mask->k_tokens > 0 ? k : q;
     const void* vp = mask->k_tokens > 0 ? v : q;
     const int32_t kh = mask->k_tokens > 0 ? params->num_kv_heads : params->num_q_heads;
@@ -863,7 +895,9 @@ extern "C" pva_status pva_attn_bwd(const void* q, const void* k, const void* v, 
         !make_map(&mv, vp, mask->k_tokens, kh, head_dim) ||
         !make_map(&mdo, dout, mask->q_tokens, params->num_q_heads, head_dim) ||
         !make_map(&mq64, q, mask->q_tokens, params->num_q_heads, head_dim, 64) ||
-        !make_map(&mdo64, dout, mask->q_tokens, params->num_q_heads, head_dim, 64))
+        !make_map(&mdo64, dout, mask->q_tokens, params->num_q_heads, head_dim, 64) ||
+        !make_map(&mk64, kp, mask->k_tokens, kh, head_dim, 64) ||
+        !make_map(&mv64, vp, mask->k_tokens, kh, head_dim, 64))
         return PVA_ERR_CUDA;
     BwdParams bp;
     bp.wl = reinterpret_cast<const uint8_t*>(worklist_dev);
@@ -884,6 +918,6 @@ extern "C" pva_status pva_attn_bwd(const void* q, const void* k, const void* v, 
     bp.d = head_dim;
     bp.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
     bp.scale_log2 = bp.scale * 1.4426950408889634f;
-    return head_dim == 128 ? launch_bwd<128>(mq, mk, mv, mdo, mq64, mdo64, bp, nc, st)
-                           : launch_bwd<64>(mq, mk, mv, mdo, mq64, mdo64, bp, nc, st);
+    return head_dim == 128 ? launch_bwd<128>(mq, mk, mv, mdo, mq64, mdo64, mk64, mv64, bp, nc, st)
+                           : launch_bwd<64>(mq, mk, mv, mdo, mq64, mdo64, mk64, mv64, bp, nc, st);
 }
