@@ -75,14 +75,30 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# device headers every kernel source includes: a change to them changes the kernel too
+KERNEL_HEADERS = ("common.h", "ptx.cuh", "tma_map.h", "wl_layout.cuh")
+
+
+def kernel_source_sha(kernel_file: str):
+    """sha256 over a kernel source and the device headers it includes (None if missing)."""
+    csrc = os.path.join(ROOT, "packed_varlen_attention_cu_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (kernel_file,) + KERNEL_HEADERS:
+        path = os.path.join(csrc, name)
+        if not os.path.exists(path):
+            return None
+        h.update(open(path, "rb").read())
+    return h.hexdigest()
+
+
 def profile_traffic(kernel_file: str, profile_name: str):
     """Per-launch DRAM bytes from a committed ncu summary, if the kernel
-    source is unchanged since it was taken (sha256 recorded in the summary)."""
+    source and its headers are unchanged since it was taken (sha256 recorded
+    in the summary, from kernel_source_sha)."""
     path = os.path.join(ROOT, "profiles", profile_name)
-    src = os.path.join(ROOT, "packed_varlen_attention_cu_gb300", "csrc", kernel_file)
-    if not (os.path.exists(path) and os.path.exists(src)):
+    sha = kernel_source_sha(kernel_file)
+    if not os.path.exists(path) or sha is None:
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     vals = {}
     for line in open(path):
         if ":" in line:
