@@ -307,7 +307,9 @@ def run_pva(args, rank, world, local):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    traffic = profile_traffic("attn_fwd.cu", f"attn_fwd_{args.workload}.txt")
+    # a summary covers one workload at its full size; a shrunk pack has none
+    traffic = None if args.pack_tokens else profile_traffic("attn_fwd.cu",
+                                                            f"attn_fwd_{args.workload}.txt")
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
