@@ -66,14 +66,29 @@ typedef enum {
     PVA_MASK_SLICES = 4           /* explicit slice list (AttnSlice, §4.4) */
 } pva_mask_kind;
 
-typedef enum { PVA_SLICE_FULL = 0, PVA_SLICE_CAUSAL = 1 } pva_slice_type;
+/* The four MaskTypes of "03 · 长文负载均衡" §4.4 (the pages name them without
+ * geometry; the tests below use token positions, like the per-document masks):
+ *   FULL         every (query, key) pair of the rectangle
+ *   CAUSAL       k_pos <= q_pos           (window w > 0: and q_pos - k_pos < w)
+ *   INV_CAUSAL   k_pos >= q_pos           (window w > 0: and k_pos - q_pos < w)
+ *   BI_CAUSAL    k_pos >= q_pos and k_end - k_pos >= q_end - q_pos, with
+ *                q_end = q_pos0 + q_len, k_end = k_pos0 + k_len: inverse-causal
+ *                from the slice's start and causal from its end (for q_pos0 =
+ *                k_pos0 the band q_pos <= k_pos <= q_pos + k_len - q_len);
+ *                window must be 0. */
+typedef enum {
+    PVA_SLICE_FULL = 0,
+    PVA_SLICE_CAUSAL = 1,
+    PVA_SLICE_INV_CAUSAL = 2,
+    PVA_SLICE_BI_CAUSAL = 3
+} pva_slice_type;
 
 /* One AttnSlice ("03 · 长文负载均衡" §4.4: (QRange, KRange, MaskType)).
  * Rows are indices into the Q / K buffers; positions are the rows' token
- * positions used by the causal test k_pos <= q_pos (and q_pos - k_pos < window
- * when window > 0).  Consecutive slices with the same (q_row0, q_len, q_pos0)
- * form one query segment; the query ranges of different segments must not
- * overlap.  Query rows outside every slice are not written. */
+ * positions used by the mask tests above.  Consecutive slices with the same
+ * (q_row0, q_len, q_pos0) form one query segment; the query ranges of
+ * different segments must not overlap.  Query rows outside every slice are
+ * not written. */
 typedef struct {
     int32_t q_row0, q_len, q_pos0;
     int32_t k_row0, k_len, k_pos0;

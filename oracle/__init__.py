@@ -23,7 +23,7 @@ _HDR = os.path.join(_HERE, "oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_SHARED_QUESTION, MASK_ZIGZAG_PAIR, MASK_SLICES = range(5)
-SLICE_FULL, SLICE_CAUSAL = 0, 1
+SLICE_FULL, SLICE_CAUSAL, SLICE_INV_CAUSAL, SLICE_BI_CAUSAL = 0, 1, 2, 3
 
 
 def compile_oracle(force: bool = False) -> str:

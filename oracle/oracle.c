@@ -100,8 +100,12 @@ int32_t or_zigzag_map(const int32_t *cu, int32_t ndocs, int32_t cp, int32_t rank
 /*  - zigzag pair (q rank r, kv rank s): rows are rank-local (map above);    */
 /*    allowed iff same document and k position <= q position ([P4] ring     */
 /*    attention, each rank's Q against one KV shard).                        */
-/*  - slices: [P1] §4.4 AttnSlice (QRange, KRange, FULL or CAUSAL), causal   */
-/*    compared on the slice's positions, with an optional window.            */
+/*  - slices: [P1] §4.4 AttnSlice (QRange, KRange, MaskType).  The pages     */
+/*    name FULL / CAUSAL / INV-CAUSAL / BI-CAUSAL without geometry; reading: */
+/*    tests on the slice's token positions, CAUSAL k <= q and INV-CAUSAL     */
+/*    k >= q (each with an optional window w: |q - k| < w), BI-CAUSAL        */
+/*    k >= q and k_end - k >= q_end - q (inverse-causal from the start,      */
+/*    causal from the end of the slice).                                     */
 /* ------------------------------------------------------------------------ */
 typedef struct {
     const int32_t *cu;
@@ -192,13 +196,31 @@ static int allowed(const ctx_t *c, int32_t i, int32_t j) {
     case OR_MASK_ZIGZAG_PAIR:
         return c->doc_q[i] == c->doc_k[j] && c->gk[j] <= c->gq[i];
     case OR_MASK_SLICES:
+        /* AttnSlice MaskTypes ("03 · 长文负载均衡" §4.4), tested on token positions:
+         * CAUSAL k <= q, INV_CAUSAL k >= q (each with an optional window), and
+         * BI_CAUSAL k >= q with k_end - k >= q_end - q (inverse-causal from the
+         * slice start, causal from its end). */
         for (int32_t s = 0; s < m->num_slices; ++s) {
             const int32_t *sl = m->slices + 8 * s;
             if (i < sl[0] || i >= sl[0] + sl[1] || j < sl[3] || j >= sl[3] + sl[4]) continue;
-            if (sl[6] == OR_SLICE_FULL) return 1;
             int64_t qp = (int64_t)sl[2] + (i - sl[0]);
             int64_t kp = (int64_t)sl[5] + (j - sl[3]);
-            if (kp <= qp && (sl[7] <= 0 || qp - kp < sl[7])) return 1;
+            int64_t w = sl[7];
+            switch (sl[6]) {
+            case OR_SLICE_FULL:
+                return 1;
+            case OR_SLICE_CAUSAL:
+                if (kp <= qp && (w <= 0 || qp - kp < w)) return 1;
+                break;
+            case OR_SLICE_INV_CAUSAL:
+                if (kp >= qp && (w <= 0 || kp - qp < w)) return 1;
+                break;
+            case OR_SLICE_BI_CAUSAL: {
+                int64_t q_end = (int64_t)sl[2] + sl[1], k_end = (int64_t)sl[5] + sl[4];
+                if (kp >= qp && k_end - kp >= q_end - qp) return 1;
+                break;
+            }
+            }
         }
         return 0;
     }
@@ -800,17 +822,27 @@ static int derive_plan(const int32_t *cu, int32_t ndocs, const or_mask_t *m, pla
     return -1;
 }
 
-/* Allowed key interval [lo, hi) (slice-local key index) of one query row.  */
+/* Allowed key interval [lo, hi) (slice-local key index) of one query row    */
+/* r (slice-local): d is the index of the key at the query's position.       */
 static void row_interval(const slice_t *s, int32_t r, int64_t *lo, int64_t *hi) {
-    if (s->type == OR_SLICE_FULL) {
-        *lo = 0;
-        *hi = s->k_len;
-        return;
+    int64_t d = (int64_t)s->q_pos0 + r - s->k_pos0;
+    int64_t l = 0, h = s->k_len;
+    switch (s->type) {
+    case OR_SLICE_CAUSAL:
+        h = d + 1;
+        if (s->window > 0) l = d - s->window + 1;
+        break;
+    case OR_SLICE_INV_CAUSAL:
+        l = d;
+        if (s->window > 0) h = d + s->window;
+        break;
+    case OR_SLICE_BI_CAUSAL:
+        l = d;
+        h = (int64_t)s->k_len - s->q_len + r + 1;
+        break;
+    default: /* FULL */
+        break;
     }
-    int64_t qp = (int64_t)s->q_pos0 + r;
-    int64_t h = qp - s->k_pos0 + 1;
-    int64_t l = 0;
-    if (s->window > 0) l = qp - s->k_pos0 - s->window + 1;
     if (l < 0) l = 0;
     if (h > s->k_len) h = s->k_len;
     *lo = l;

@@ -19,7 +19,7 @@ enum {
     OR_MASK_ZIGZAG_PAIR = 3,
     OR_MASK_SLICES = 4
 };
-enum { OR_SLICE_FULL = 0, OR_SLICE_CAUSAL = 1 };
+enum { OR_SLICE_FULL = 0, OR_SLICE_CAUSAL = 1, OR_SLICE_INV_CAUSAL = 2, OR_SLICE_BI_CAUSAL = 3 };
 
 typedef struct {
     int32_t kind;

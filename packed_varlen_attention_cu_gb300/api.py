@@ -17,7 +17,7 @@ from ._lib import MaskDesc, Slice, WorklistParams, check, lib
 from .workloads import (MASK_CAUSAL, MASK_SHARED_QUESTION, MASK_SLICES, MASK_SLIDING_WINDOW,
                         MASK_ZIGZAG_PAIR)
 
-SLICE_FULL, SLICE_CAUSAL = 0, 1
+SLICE_FULL, SLICE_CAUSAL, SLICE_INV_CAUSAL, SLICE_BI_CAUSAL = 0, 1, 2, 3
 TILE = 128
 
 

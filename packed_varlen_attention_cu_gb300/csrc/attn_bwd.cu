@@ -395,10 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
                     const WlRun run = runs[u.run_begin + rr];
                     const WlSlice s = slices[run.slice];
-                    const bool causal = s.type == PVA_SLICE_CAUSAL;
-                    const int32_t d_base = q_pos - s.k_pos0;
-                    const int32_t lim_hi = !valid ? 0 : causal ? min(s.k_len, d_base + 1) : s.k_len;
-                    const int32_t lim_lo = causal && s.window > 0 ? d_base - s.window + 1 : -(1 << 30);
+                    int64_t klo, khi;  // allowed keys of this row (slice-local)
+                    slice_keys_of_query(s, q_pos, klo, khi);
+                    const int32_t lim_hi = valid ? (int32_t)khi : 0;
+                    const int32_t lim_lo = (int32_t)klo;
                     for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
                         const int32_t kt0 = jt * 128;
                         const int32_t c_hi = min(128, lim_hi - kt0), c_lo = max(0, lim_lo - kt0);
@@ -715,8 +715,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t head = u.kvh * G + hh;
                 for (int32_t m = 0; m < u.gcount && live; ++m) {
                 const WlSlice s = slices[gsl[u.gbegin + m]];
-                const bool causal = s.type == PVA_SLICE_CAUSAL;
                 const int32_t k_pos = s.k_pos0 + u.kt * 128 + kr;
+                int64_t qa, qb;  // query positions that may see this key
+                slice_queries_of_key(s, k_pos, qa, qb);
                 int32_t qlo, qhi;
                 bwd_q_span(s, u.kt, qlo, qhi);
                 for (int32_t t = qlo; t < qhi && live; ++t) {
@@ -724,11 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t qrow0 = s.q_row0 + t * 128;
                     const int32_t nq = min(128, s.q_len - t * 128);
                     const int32_t cpos0 = s.q_pos0 + t * 128;
-                    int32_t c_lo = 0, c_hi = kvalid ? nq : 0;
-                    if (causal) {
-                        c_lo = max(c_lo, k_pos - cpos0);
-                        if (s.window > 0) c_hi = min(c_hi, k_pos + s.window - cpos0);
-                    }
+                    const int32_t c_lo = (int32_t)max((int64_t)0, qa - cpos0);
+                    const int32_t c_hi = kvalid ? (int32_t)min((int64_t)nq, qb - cpos0) : 0;
                     const uint32_t halves = nq > 64 ? 2 : 1;
                     for (uint32_t hf = 0; hf < halves && live; ++hf, ++gu) {
                         const uint32_t b = gu & 1;

@@ -443,13 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const WlRun run = runs[u.run_begin + rr];
                 const WlSlice s = slices[run.slice];
                 // allowed keys of this row, relative to the slice's first key:
-                // [lim_lo, lim_hi) (the diagonal for causal slices, a sliding window
-                // below it, nothing for padding rows)
-                const bool causal = s.type == PVA_SLICE_CAUSAL;
-                const int32_t d_base = q_pos - s.k_pos0;
-                const int32_t lim_hi = !valid ? 0 : causal ? min(s.k_len, d_base + 1) : s.k_len;
-                const int32_t lim_lo =
-                    causal && s.window > 0 ? d_base - s.window + 1 : -(1 << 30);
+                // [lim_lo, lim_hi) (by the slice's MaskType; nothing for padding rows)
+                int64_t klo, khi;
+                slice_keys_of_query(s, q_pos, klo, khi);
+                const int32_t lim_hi = valid ? (int32_t)khi : 0;
+                const int32_t lim_lo = (int32_t)klo;
                 for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
                     // allowed columns [c_lo, c_hi) in this kv tile, settled while S
                     // is still being computed

@@ -92,22 +92,63 @@ struct BwdHeader {
 };
 static_assert(sizeof(BwdHeader) <= 256, "backward header fits in 256 bytes");
 
+// The slice MaskTypes (pva_slice_type), on token positions: CAUSAL k <= q,
+// INV_CAUSAL k >= q (each with an optional window |q - k| < w), BI_CAUSAL
+// k >= q and k_end - k >= q_end - q.
+// Keys of slice s a query at position qp may see, as slice-local key indices
+// [lo, hi) (empty when hi <= lo).
+__host__ __device__ inline void slice_keys_of_query(const WlSlice& s, int64_t qp, int64_t& lo,
+                                                    int64_t& hi) {
+    const int64_t d = qp - s.k_pos0;  // local index of the key at the query's position
+    lo = 0;
+    hi = s.k_len;
+    if (s.type == 1) {  // CAUSAL
+        hi = d + 1;
+        if (s.window > 0) lo = d - s.window + 1;
+    } else if (s.type == 2) {  // INV_CAUSAL
+        lo = d;
+        if (s.window > 0) hi = d + s.window;
+    } else if (s.type == 3) {  // BI_CAUSAL: local key j <= k_len - q_len + local row
+        lo = d;
+        hi = (int64_t)s.k_len - s.q_len + (qp - s.q_pos0) + 1;
+    }
+    if (lo < 0) lo = 0;
+    if (hi > s.k_len) hi = s.k_len;
+}
+
+// Query positions [lo, hi) of slice s that may see a key at position kp (both
+// ends are non-decreasing in kp for every type).
+__host__ __device__ inline void slice_queries_of_key(const WlSlice& s, int64_t kp, int64_t& lo,
+                                                     int64_t& hi) {
+    lo = s.q_pos0;
+    hi = (int64_t)s.q_pos0 + s.q_len;
+    int64_t a = lo, b = hi;
+    if (s.type == 1) {  // CAUSAL
+        a = kp;
+        if (s.window > 0) b = kp + s.window;
+    } else if (s.type == 2) {  // INV_CAUSAL
+        b = kp + 1;
+        if (s.window > 0) a = kp - s.window + 1;
+    } else if (s.type == 3) {  // BI_CAUSAL: q >= q_end - k_end + k
+        b = kp + 1;
+        a = ((int64_t)s.q_pos0 + s.q_len) - ((int64_t)s.k_pos0 + s.k_len) + kp;
+    }
+    if (a > lo) lo = a;
+    if (b < hi) hi = b;
+}
+
 // q tiles [qlo, qhi) of slice `sl` (aligned at its query start, like the
 // forward) holding a row that may see a key of key tile kt of the slice.
 __host__ __device__ inline void bwd_q_span(const WlSlice& sl, int32_t kt, int32_t& qlo,
                                            int32_t& qhi) {
     const int32_t ka = kt * 128, kb = (sl.k_len < ka + 128) ? sl.k_len : ka + 128;
-    int64_t r_lo = 0, r_hi = sl.q_len;
-    if (sl.type == 1) {  // causal by position, optional window
-        r_lo = (int64_t)sl.k_pos0 + ka - sl.q_pos0;
-        if (sl.window > 0) r_hi = (int64_t)sl.k_pos0 + kb - 1 + sl.window - sl.q_pos0;
-    }
-    if (r_lo < 0) r_lo = 0;
-    if (r_hi > sl.q_len) r_hi = sl.q_len;
-    if (kb <= ka || r_hi <= r_lo) {
-        qlo = qhi = 0;
-        return;
-    }
+    qlo = qhi = 0;
+    if (kb <= ka) return;
+    int64_t a0, a1, b0, b1;
+    slice_queries_of_key(sl, (int64_t)sl.k_pos0 + ka, a0, a1);
+    slice_queries_of_key(sl, (int64_t)sl.k_pos0 + kb - 1, b0, b1);
+    const int64_t r_lo = a0 - sl.q_pos0, r_hi = b1 - sl.q_pos0;
+    if (r_hi <= r_lo) return;
     qlo = (int32_t)(r_lo / 128);
     qhi = (int32_t)((r_hi + 127) / 128);
 }

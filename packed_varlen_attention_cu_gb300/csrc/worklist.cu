@@ -327,17 +327,8 @@ __device__ void tile_span_warp(const WlSeg& g, const WlSlice& s, int32_t t, int3
     const int32_t r0 = t * tile_m;
     const int32_t r1 = min(r0 + tile_m, g.q_len);
     for (int32_t r = r0 + (int32_t)(threadIdx.x & 31); r < r1; r += 32) {
-        long long lo, hi;
-        if (s.type == PVA_SLICE_FULL) {
-            lo = 0;
-            hi = s.k_len;
-        } else {
-            const long long qp = (long long)s.q_pos0 + r;
-            hi = qp - s.k_pos0 + 1;
-            lo = s.window > 0 ? qp - s.k_pos0 - s.window + 1 : 0;
-            if (lo < 0) lo = 0;
-            if (hi > s.k_len) hi = s.k_len;
-        }
+        int64_t lo, hi;
+        slice_keys_of_query(s, (int64_t)s.q_pos0 + r, lo, hi);
         if (hi <= lo) continue;
         cnt += hi - lo;
         mn = lo < mn ? lo : mn;
@@ -1049,7 +1040,8 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
                 if (b.q_len < 0 || b.k_len < 0 || b.q_row0 < 0 || b.k_row0 < 0 ||
                     (int64_t)b.q_row0 + b.q_len > m->q_tokens ||
                     (int64_t)b.k_row0 + b.k_len > m->k_tokens ||
-                    (b.type != PVA_SLICE_FULL && b.type != PVA_SLICE_CAUSAL))
+                    b.type < PVA_SLICE_FULL || b.type > PVA_SLICE_BI_CAUSAL ||
+                    (b.type == PVA_SLICE_BI_CAUSAL && b.window != 0))
                     return false;
                 ++j;
             }

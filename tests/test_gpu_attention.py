@@ -105,6 +105,25 @@ def test_explicit_slices_and_unwritten_rows(oracle_mod):
     assert torch.isnan(out[500:700]).all() and torch.isnan(lse[:, 500:700]).all()
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_inv_and_bi_causal_slices(oracle_mod, d):
+    # INV-CAUSAL (with and without a window), BI-CAUSAL on a 200 x 300 rectangle,
+    # CAUSAL with a window and FULL, over three query segments; ragged tiles
+    sl = np.array([[0, 300, 0, 0, 300, 0, 2, 0],
+                   [300, 200, 1000, 300, 300, 1000, 3, 0],
+                   [300, 200, 1000, 0, 300, 900, 1, 64],
+                   [500, 400, 0, 600, 300, 50, 2, 200],
+                   [500, 400, 0, 300, 300, 0, 0, 0]], dtype=np.int32)
+    T = 900
+    q, k, v = W.make_qkv(T, T, 4, 2, d, 40 + d)
+    mask = api.make_mask(W.MASK_SLICES, T, T, slices=sl)
+    out, lse, _ = run_gpu(q, k, v, np.array([0, T], dtype=np.int32), mask, 4, 2)
+    ref_o, ref_l = oracle_mod.attention(oracle_mod.bf16_bits(q), oracle_mod.bf16_bits(k),
+                                        oracle_mod.bf16_bits(v), np.array([0, T], dtype=np.int32),
+                                        oracle_mask(W.MASK_SLICES, slices=sl))
+    compare(to_np(out), to_np(lse), ref_o, ref_l, f"inv/bi slices d{d}")
+
+
 @pytest.mark.parametrize("cp", [2, 4])
 def test_zigzag_pairs_each_partial(oracle_mod, cp):
     lengths = [700, 3, 260, 1100, 40]

@@ -117,6 +117,27 @@ def test_bwd_explicit_slices_with_unseen_keys(oracle_mod):
     assert np.all(got[1][200:250] == 0) and np.all(got[2][400:] == 0)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_inv_and_bi_causal_slices(oracle_mod, d):
+    # INV-CAUSAL, BI-CAUSAL, windowed CAUSAL and FULL slices over three key ranges
+    # (identical or disjoint, as the backward plan requires)
+    sl = np.array([[0, 300, 0, 0, 300, 0, 2, 0],
+                   [300, 200, 1000, 300, 300, 1000, 3, 0],
+                   [300, 200, 1000, 0, 300, 900, 1, 64],
+                   [500, 400, 0, 600, 300, 50, 2, 200],
+                   [500, 400, 0, 300, 300, 0, 0, 0]], dtype=np.int32)
+    T, hq, hkv = 900, 4, 2
+    q, k, v = W.make_qkv(T, T, hq, hkv, d, 50 + d)
+    dout = W.make_qkv(T, T, hq, hkv, d, 150 + d)[0]
+    mask = api.make_mask(W.MASK_SLICES, T, T, slices=sl)
+    cu = W.cu_seqlens_of([T])
+    got = _bwd(q, k, v, cu, mask, hq, hkv, dout, True)
+    ref = oracle_mod.attention_bwd(oracle_mod.bf16_bits(q), oracle_mod.bf16_bits(k),
+                                   oracle_mod.bf16_bits(v), oracle_mod.bf16_bits(dout), cu,
+                                   oracle_mask(W.MASK_SLICES, slices=sl))
+    _check(got, ref, f"inv/bi slices d={d}")
+
+
 def test_bwd_shared_question(oracle_mod):
     # the question's keys form one key group: its own causal slice and every answer
     _case(oracle_mod, [400, 300, 200, 129], 4, 2, 128, W.MASK_SHARED_QUESTION, True, 28,

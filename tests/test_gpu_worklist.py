@@ -95,6 +95,24 @@ def test_worklist_explicit_slices_bit_exact(oracle_mod):
     _assert_same(g, o)
 
 
+# INV-CAUSAL and BI-CAUSAL slices ("03 · 长文负载均衡" §4.4), mixed with CAUSAL and
+# FULL, over three query segments and three key ranges
+SLICE_TYPES_CASE = np.array([[0, 300, 0, 0, 300, 0, 2, 0],
+                             [300, 200, 1000, 300, 300, 1000, 3, 0],
+                             [300, 200, 1000, 0, 300, 900, 1, 64],
+                             [500, 400, 0, 600, 300, 50, 2, 200],
+                             [500, 400, 0, 300, 300, 0, 0, 0]], dtype=np.int32)
+
+
+def test_worklist_inv_bi_causal_slices_bit_exact(oracle_mod):
+    sl = SLICE_TYPES_CASE
+    mask = api.make_mask(W.MASK_SLICES, 900, 900, slices=sl)
+    g, _ = _gpu_worklist(np.array([0, 900], dtype=np.int32), mask, 4, 2, 7, 0)
+    o = oracle_mod.worklist(np.array([0, 900], dtype=np.int32), oracle_mask(W.MASK_SLICES, slices=sl),
+                            128, 128, 4, 2, 7, 0)
+    _assert_same(g, o)
+
+
 def test_worklist_edge_lengths_bit_exact(oracle_mod):
     lengths = [0, 1, 127, 128, 129, 0, 255, 256, 257, 1, 1, 383, 0]
     cu = W.cu_seqlens_of(lengths)
