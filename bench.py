@@ -34,6 +34,7 @@ from packed_varlen_attention_cu_gb300 import workloads as W  # noqa: E402
 METRIC = "packed doc-masked attn TFLOP/s (unmasked pairs) and % of GB300 BF16 peak"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+DISPATCH = {"dynamic": 0, "static": 1}  # pva_dispatch
 
 WORKLOADS = {
     "128k": (W.zigzag_pack, "128K causal pack: lognormal lengths (median 2048, sigma 1.5, "
@@ -234,7 +235,7 @@ def run_pva(args, rank, world, local):
         # balanced with different per-tile costs, per-CTA times pooled into the fit
         cal_wl, cal_busy = [], []
         for ct in (0, 4 * args.c_tile):
-            cp_ = api.make_params(hq, hkv, num_ctas=0, c_tile=ct)
+            cp_ = api.make_params(hq, hkv, num_ctas=0, c_tile=ct, dispatch=api.DISPATCH_STATIC)
             cw = api.alloc_worklist(w.num_docs, mask, cp_, dev)
             cb = torch.zeros((num_ctas, 2), dtype=torch.int64, device=dev)
             api.build_worklist(cu, mask, cp_, cw, stream)
@@ -251,7 +252,7 @@ def run_pva(args, rank, world, local):
         args.c_tile = fitted
         del cal_wl, cal_busy
     params = api.make_params(hq, hkv, num_ctas=0, c_tile=args.c_tile,
-                             refine_iters=args.refine_iters)
+                             refine_iters=args.refine_iters, dispatch=DISPATCH[args.dispatch])
     wl = api.alloc_worklist(w.num_docs, mask, params, dev)
 
     api.build_worklist(cu, mask, params, wl)
@@ -259,7 +260,7 @@ def run_pva(args, rank, world, local):
     assert counts["status"] == 0, counts
     pairs = counts["pairs_per_head"]
     flops = 4.0 * d * hq * pairs
-    n_wl_kernels = api.WORKLIST_BUILD_KERNELS
+    n_wl_kernels = api.worklist_build_kernels(params)
     io_bytes = (q.numel() + k.numel() + v.numel() + out.numel()) * 2 + lse.numel() * 4
 
     def step(ev_a=None, ev_b=None):
@@ -323,6 +324,7 @@ def run_pva(args, rank, world, local):
                    "l2": f"inputs larger than L2: Q+K+V+O+LSE = {io_bytes / 1e9:.2f} GB "
                          f"> {L2_BYTES / 1e6:.0f} MB, no flush",
                    "num_ctas": num_ctas, "c_tile": args.c_tile, "c_tile_fit": fit,
+                   "dispatch": args.dispatch,
                    "refine_iters": args.refine_iters,
                    "parallelism": f"{world} independent replica(s), one per GPU"},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
@@ -422,7 +424,8 @@ def run_zigzag(args, ctx, world, fused=False):
     nmax = max(lens)
     part_o = torch.empty((nmax, hq, d), dtype=torch.float32, device=dev)
     part_l = torch.empty((hq * nmax,), dtype=torch.float32, device=dev)
-    params = api.make_params(hq, hkv, num_ctas=0, c_tile=base_params.c_tile)
+    params = api.make_params(hq, hkv, num_ctas=0, c_tile=base_params.c_tile,
+                             dispatch=base_params.dispatch)
     masks = {(r, s): api.make_mask(W.MASK_ZIGZAG_PAIR, lens[r], lens[s], cp=cp, q_rank=r, k_rank=s)
              for r in range(cp) for s in range(cp)}
     wls = {key: api.alloc_worklist(w.num_docs, m, params, dev) for key, m in masks.items()}
@@ -472,7 +475,7 @@ def run_zigzag(args, ctx, world, fused=False):
     barrier(world)
     t, f = aggregate(s.elapsed_time(e) / 1e3, flops * K, world)
     if fused:
-        launches = cp * 4 + cp * cp * (api.WORKLIST_BUILD_KERNELS + 1)
+        launches = cp * 4 + cp * cp * (api.worklist_build_kernels(params) + 1)
         return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "cp": cp, "steps": K,
                 "ms_per_step": round(t / K * 1e3, 3), "gpu_launches_per_step": launches,
                 "note": "as zigzag_cp, but ring steps t > 0 merge into the running (O, LSE) in "
@@ -480,7 +483,7 @@ def run_zigzag(args, ctx, world, fused=False):
     mtimes = [a.elapsed_time(b) / 1e3 for a, b, _ in merge_ev]
     mbytes = [n * hq * (3 * 4 * d + 3 * 4) for _, _, n in merge_ev]
     merge_gbs = sum(mbytes) / sum(mtimes) / 1e9 if mtimes else None
-    launches = cp * 4 + cp * cp * (api.WORKLIST_BUILD_KERNELS + 1) + cp * (cp - 1)
+    launches = cp * 4 + cp * cp * (api.worklist_build_kernels(params) + 1) + cp * (cp - 1)
     return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "cp": cp, "steps": K,
             "ms_per_step": round(t / K * 1e3, 3),
             "merge": {"bound": "hbm", "achieved": round(merge_gbs, 1) if merge_gbs else None,
@@ -624,7 +627,8 @@ def run_libra_ratio(args, ctx):
         qa, ka, va = q[rows].contiguous(), k[rows].contiguous(), v[rows].contiguous()
         T = qa.shape[0]
         mask = api.make_mask(W.MASK_CAUSAL, T, T)
-        params = api.make_params(w.num_q_heads, w.num_kv_heads, num_ctas=0, c_tile=args.c_tile)
+        params = api.make_params(w.num_q_heads, w.num_kv_heads, num_ctas=0, c_tile=args.c_tile,
+                                 dispatch=DISPATCH[args.dispatch])
         wl = api.alloc_worklist(len(lengths), mask, params, dev)
         out = torch.empty_like(qa)
         lse = torch.empty((qa.shape[1], T), dtype=torch.float32, device=dev)
@@ -725,6 +729,9 @@ def main(argv=None):
     ap.add_argument("--c-tile", type=int, default=None,
                     help="per-tile fixed cost in pair units (default: api.default_c_tile(d))")
     ap.add_argument("--pack-tokens", type=int, default=0)
+    ap.add_argument("--dispatch", choices=tuple(DISPATCH), default="dynamic",
+                    help="forward units: claimed in LPT order at run time, or the builder's "
+                         "static per-CTA LPT lists")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-zigzag", action="store_true")

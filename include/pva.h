@@ -124,7 +124,29 @@ typedef struct {
                            tile) and of one query sub-tile (Q load, output rows):
                            unit cost = exact allowed pairs
                                        + c_tile * (sub-tiles * kv tiles + sub-tiles) */
+    int32_t dispatch;   /* pva_dispatch: how the forward kernel's CTAs take their units */
+    int32_t reserved_;  /* 0 */
 } pva_worklist_params;
+
+/* How the forward kernel hands units to its persistent CTAs.  Both follow the
+ * LPT rule of "数据并行负载均衡" §4.4 (units in decreasing cost, each to the
+ * least loaded CTA).  The worklist is built for one of them and the forward
+ * launch must name the same one (else the kernel reports a bad worklist).
+ *   DYNAMIC (default): the builder also writes a dispatch order (power-of-two
+ *     cost classes floor(log2(max(cost, 1))) in decreasing order, enumeration
+ *     order inside a class, so that concurrent CTAs share the same documents'
+ *     K/V in L2); a CTA that runs out of work claims the next unit of that
+ *     order from a counter kept in the worklist, so "least loaded" is decided
+ *     by measured time (list scheduling).  One worklist then serves one
+ *     forward launch at a time (stream-ordered launches are fine); the last
+ *     CTA to finish resets the counter.
+ *   STATIC: each CTA runs the list the builder assigned it by cost (the exact
+ *     LPT bins + refinement, the per-CTA CSR lists, enumeration order).
+ * The per-CTA lists are built in both modes (the backward's dQ pass uses them). */
+typedef enum {
+    PVA_DISPATCH_DYNAMIC = 0,
+    PVA_DISPATCH_STATIC = 1,
+} pva_dispatch;
 
 /* Upper bound, in bytes, of the device worklist for this problem.  HOST
  * computation only.  num_docs is the length of cu_seqlens minus one.
@@ -371,7 +393,9 @@ size_t pva_noalloc_scratch_bytes(void);
 
 /* Test hook for the failure path of the bounded waits (the pages have no
  * counterpart).  While `enable` is non-zero, pva_attn_fwd launches made by
- * this process tell CTA 0's TMA producer to skip its second K/V load.  The
+ * this process tell one CTA's TMA producer (CTA 0's under STATIC dispatch,
+ * that of the CTA which claimed the first unit under DYNAMIC) to skip its
+ * second K/V load.  The
  * MMA warps of that CTA then wait for a copy that never comes; their bounded
  * wait (2 s) expires, the CTA raises its abort flag, drains its own copies and
  * MMAs, frees tensor memory and returns, and pva_worklist_error() reports

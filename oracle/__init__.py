@@ -279,6 +279,35 @@ def lpt(cost: Sequence[int], bins: int):
     return assign[:n], order[:n], loads
 
 
+def dispatch_order(cost_by_uid: Sequence[int], num_ctas: int) -> np.ndarray:
+    """Run-time dispatch order of a worklist's units (uids), for CTAs that claim
+    their next unit when they run out of work.  It follows the LPT rule
+    ("数据并行负载均衡" §4.4: largest cost first, each to whichever worker is
+    least loaded) over power-of-two cost classes k = floor(log2(max(cost, 1))):
+    classes above a split class go first, in decreasing class, enumeration
+    order (uid) inside a class; the split class and all below it follow in
+    exact LPT order (cost desc, uid asc).  The split is the highest non-empty
+    class k whose units the work below it could not absorb, i.e. the work of
+    the classes under k is below num_ctas * 2^(k+1) (capped at 38).  Plain
+    Python: bit lengths, sums and sorts."""
+    cost = [int(c) for c in cost_by_uid]
+    classes = [max(c, 1).bit_length() - 1 for c in cost]
+    work = {}
+    for c, k in zip(cost, classes):
+        work[k] = work.get(k, 0) + c
+    split = 0
+    for k in sorted(work, reverse=True):
+        below = sum(wk for kk, wk in work.items() if kk < k)
+        if below < num_ctas * 2 ** (k + 1):
+            split = min(k, 38)
+            break
+    upper = sorted((u for u in range(len(cost)) if classes[u] > split),
+                   key=lambda u: (-classes[u], u))
+    lower = sorted((u for u in range(len(cost)) if classes[u] <= split),
+                   key=lambda u: (-cost[u], u))
+    return np.asarray(upper + lower, dtype=np.int32)
+
+
 UNIT_FIELDS = ("uid", "seg", "t0", "t1", "h0", "h1", "kvh", "run_begin", "run_count", "cta")
 
 

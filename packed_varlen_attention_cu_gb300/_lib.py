@@ -46,7 +46,8 @@ class WorklistParams(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("num_ctas", ctypes.c_int32), ("refine_iters", ctypes.c_int32),
-                ("c_tile", ctypes.c_int64)]
+                ("c_tile", ctypes.c_int64), ("dispatch", ctypes.c_int32),
+                ("reserved_", ctypes.c_int32)]
 
 
 class PvaError(RuntimeError):

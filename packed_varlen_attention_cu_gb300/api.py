@@ -48,9 +48,16 @@ def make_mask(kind: int = MASK_CAUSAL, q_tokens: int = 0, k_tokens: int = 0, win
     return m
 
 
+DISPATCH_DYNAMIC, DISPATCH_STATIC = 0, 1  # pva_dispatch
+
 # Kernels one pva_build_worklist launches: plan, units, chunk sort + merge
-# rank (LPT order), LPT, chunk sort + merge rank (per-CTA order).
+# rank (LPT order), LPT, chunk sort + merge rank (per-CTA order), and for
+# dynamic dispatch chunk sort + merge rank (dispatch order).
 WORKLIST_BUILD_KERNELS = 7
+
+
+def worklist_build_kernels(params) -> int:
+    return WORKLIST_BUILD_KERNELS + (2 if params.dispatch == DISPATCH_DYNAMIC else 0)
 
 
 def default_c_tile(head_dim: int) -> int:
@@ -62,9 +69,11 @@ def default_c_tile(head_dim: int) -> int:
 
 
 def make_params(num_q_heads: int, num_kv_heads: int, num_ctas: int = 0, c_tile: int = 0,
-                tile_m: int = TILE, tile_n: int = TILE, refine_iters: int = 0) -> WorklistParams:
+                tile_m: int = TILE, tile_n: int = TILE, refine_iters: int = 0,
+                dispatch: int = DISPATCH_DYNAMIC) -> WorklistParams:
     p = WorklistParams()
     p.refine_iters = refine_iters
+    p.dispatch = dispatch
     p.tile_m, p.tile_n = tile_m, tile_n
     p.num_q_heads, p.num_kv_heads = num_q_heads, num_kv_heads
     p.num_ctas, p.c_tile = num_ctas, c_tile
@@ -276,9 +285,10 @@ def wlb_choose(cu_seqlens_host: np.ndarray, cp: int, tile: int, head_dim: int):
 
 
 def debug_withhold_kv_load(enable: bool) -> None:
-    """Test hook (see pva_debug_withhold_kv_load): while enabled, CTA 0 of each
-    attention launch waits for a K/V copy that is never issued, so its bounded
-    wait expires and worklist_error() reports the wait site."""
+    """Test hook (see pva_debug_withhold_kv_load): while enabled, one CTA of each
+    attention launch (CTA 0 under static dispatch, the one that claimed the
+    first unit under dynamic dispatch) waits for a K/V copy that is never
+    issued, so its bounded wait expires and worklist_error() reports the site."""
     lib().pva_debug_withhold_kv_load(1 if enable else 0)
 
 
@@ -293,14 +303,15 @@ def worklist_counts(worklist: torch.Tensor, stream=None) -> dict:
 
 # ----------------------------------------------------------------- decoding
 _HDR = np.dtype([("i32", "<i4", 20), ("c_tile", "<i8"), ("pair_sum", "<u8"), ("tile_sum", "<u8"),
-                 ("off", "<i8", 11)])
+                 ("off", "<i8", 12)])
 _OFF = ("slices", "segs", "units_enum", "keys", "order", "assign", "units", "runs",
-        "cta_off", "doc_scan", "total")
+        "cta_off", "doc_scan", "dorder", "total")
 
 
 def decode_worklist(worklist: torch.Tensor) -> dict:
     """Copy a built worklist to the host and split it into numpy arrays
-    (segments, slices, units in CTA order, runs, CSR offsets)."""
+    (segments, slices, units in CTA order, runs, CSR offsets, and for a
+    worklist built for dynamic dispatch the dispatch order of the uids)."""
     raw = worklist.detach().cpu().numpy()
     h = np.frombuffer(raw[:_HDR.itemsize].tobytes(), dtype=_HDR)[0]
     i32 = h["i32"]
@@ -309,6 +320,10 @@ def decode_worklist(worklist: torch.Tensor) -> dict:
              "cap_runs", "nslices", "nsegs", "nunits", "nruns")
     hd = {n: int(x) for n, x in zip(names, i32)}
     off = {n: int(x) for n, x in zip(_OFF, h["off"])}
+    # after the offsets: lpt_steps, refine_iters, refine_rounds, dispatch_next,
+    # dispatch_done, dispatch
+    tail = np.frombuffer(raw[_HDR.itemsize:_HDR.itemsize + 24].tobytes(), dtype="<i4")
+    dispatch = tail[5]
 
     def arr(name, dtype, n, width):
         b = raw[off[name]: off[name] + n * width * np.dtype(dtype).itemsize]
@@ -324,7 +339,10 @@ def decode_worklist(worklist: torch.Tensor) -> dict:
             "units": units[:, :10].copy(), "unit_ntiles": units[:, 10].copy(),
             "unit_cost": costs, "unit_pairs": pairs,
             "runs": arr("runs", "<i4", hd["nruns"], 4)[:, :3].copy(),
-            "cta_off": arr("cta_off", "<i4", hd["num_ctas"] + 1, 1).copy()}
+            "cta_off": arr("cta_off", "<i4", hd["num_ctas"] + 1, 1).copy(),
+            "dispatch": int(dispatch),
+            "dispatch_order": (arr("dorder", "<i4", hd["nunits"], 1).copy()
+                               if dispatch == DISPATCH_DYNAMIC else None)}
 
 
 class PackedAttention:

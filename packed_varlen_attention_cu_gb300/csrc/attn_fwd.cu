@@ -48,6 +48,10 @@ constexpr uint32_t kRegsCtrl = 104, kRegsSoftmax = 200;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 constexpr float kRescaleThreshold = 8.0f;     // log2 domain
+constexpr int kURing = 8;                     // units the producer may run ahead
+// readers of a unit slot: the two MMA warps (one arrival each) and every
+// softmax thread
+constexpr uint32_t kUReaders = 2 + 256;
 
 template <int D>
 struct Cfg {
@@ -66,7 +70,9 @@ struct AttnParams {
     int32_t q_tokens, k_tokens, hq, hkv, out_fp32, num_ctas;
     float scale_log2;
     int32_t accumulate;   // merge into the running fp32 (out, lse) instead of writing
-    int32_t withhold_kv;  // test hook: CTA 0's producer skips K/V item 1
+    int32_t withhold_kv;  // test hook: the producer of CTA 0 (static dispatch) or of the CTA
+                          // that claimed LPT rank 0 (dynamic) skips its K/V item 1
+    int32_t dynamic;      // 1: claim units in LPT order from the worklist's counter
 };
 
 struct SubTile {
@@ -102,6 +108,9 @@ struct Shared {
     uint64_t q_full[2], q_empty[2], s_full[2], p_half[2], p_full[2], o_full[2], o_empty[2], done[2],
         turn[2];
     uint64_t kv_full[8], kv_empty[8];
+    // the producer hands each unit (its index, or -1 at the end) to the other roles
+    uint64_t u_full[kURing], u_empty[kURing];
+    int32_t u_slot[kURing];
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -139,7 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ok = h->magic == kWlMagic && h->tile_m == 128 && h->tile_n == 128 &&
                     h->hq == p.hq && h->hkv == p.hkv && h->num_ctas == p.num_ctas &&
                     (int)gridDim.x == p.num_ctas && h->q_tokens == p.q_tokens &&
-                    h->k_tokens == p.k_tokens;
+                    h->k_tokens == p.k_tokens &&
+                    (h->dispatch == PVA_DISPATCH_DYNAMIC) == (p.dynamic != 0);
     if (!ok) {
         if (tid == 0 && blockIdx.x == 0) atomicCAS(err_word, 0, kErrBadWorklist);
         return;
@@ -150,9 +160,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WlRun* runs = reinterpret_cast<const WlRun*>(p.wl + h->off.runs);
     const WlSlice* slices = reinterpret_cast<const WlSlice*>(p.wl + h->off.slices);
     const WlSeg* segs = reinterpret_cast<const WlSeg*>(p.wl + h->off.segs);
+    // Static dispatch: this CTA's CSR list of `units`.  Dynamic dispatch: the
+    // CTA claims ranks one by one from the worklist's counter and runs
+    // units_enum[dorder[rank]], so a unit goes to whichever CTA frees up first
+    // (list scheduling over power-of-two cost classes in decreasing order;
+    // inside a class, enumeration order keeps concurrent units on the same
+    // documents' K/V in L2).
+    const int32_t* order = reinterpret_cast<const int32_t*>(p.wl + h->off.dorder);
+    const WlUnit* ubase =
+        p.dynamic ? reinterpret_cast<const WlUnit*>(p.wl + h->off.units_enum) : units;
+    WlHeader* hw = const_cast<WlHeader*>(h);
+    const int32_t nunits = h->nunits;
     const int32_t ub = cta_off[blockIdx.x], ue = cta_off[blockIdx.x + 1];
     const uint64_t t_start = globaltimer_ns();
-    if (ub >= ue) {
+    if (!p.dynamic && ub >= ue) {
         if (p.busy && tid == 0) {
             p.busy[2 * blockIdx.x] = t_start;
             p.busy[2 * blockIdx.x + 1] = t_start;
@@ -175,6 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&sh.kv_full[s], 1);
             mbar_init(&sh.kv_empty[s], 2);
+        }
+        for (int s = 0; s < kURing; ++s) {
+            mbar_init(&sh.u_full[s], 1);
+            mbar_init(&sh.u_empty[s], kUReaders);
         }
         sh.abort_flag = 0;
         fence_barrier_init();
@@ -206,6 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.busy[2 * blockIdx.x] = t_start;
             p.busy[2 * blockIdx.x + 1] = globaltimer_ns();
         }
+        // every claim of this CTA came before its finish; the last CTA to
+        // finish leaves the counter at 0 for the next launch on this worklist
+        if (p.dynamic && tid == 0) {
+            __threadfence();
+            if (atomicAdd(&hw->dispatch_done, 1) == (int)gridDim.x - 1) {
+                atomicExch(&hw->dispatch_next, 0);
+                atomicExch(&hw->dispatch_done, 0);
+            }
+        }
     };
     if (warp < 4) {
       regs_dealloc<kRegsCtrl>();
@@ -214,8 +248,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t kv_it = 0, q_it[2] = {0, 0};
             bool live = true;
-            for (int32_t ui = ub; ui < ue && live; ++ui) {
-                const WlUnit wu = units[ui];
+            bool hook = p.withhold_kv && !p.dynamic && blockIdx.x == 0;
+            for (uint32_t nu = 0; live; ++nu) {
+                const uint32_t us = nu % kURing;
+                live = mbar_wait(&sh.u_empty[us], ((nu / kURing) & 1) ^ 1, abort_flag, err_word,
+                                 kErrTimeoutBase + 13, kWaitNs);
+                if (!live) break;
+                int32_t idx;
+                if (p.dynamic) {
+                    // claimed once this CTA's producer has issued every load of
+                    // its previous unit, a few K/V steps before the CTA needs it
+                    const int32_t rank = atomicAdd(&hw->dispatch_next, 1);
+                    idx = rank < nunits ? order[rank] : -1;
+                    if (rank == 0 && p.withhold_kv) hook = true;
+                } else {
+                    idx = ub + (int32_t)nu < ue ? ub + (int32_t)nu : -1;
+                }
+                sh.u_slot[us] = idx;
+                mbar_arrive(&sh.u_full[us]);
+                if (idx < 0) break;
+                const WlUnit wu = ubase[idx];
                 const Unit u = decode_unit(wu, segs);
                 if (u.ntiles == 0) continue;
 #pragma unroll
@@ -236,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
                         const int32_t krow = s.k_row0 + jt * 128;
                         for (int kv = 0; kv < 2 && live; ++kv) {
-                            if (p.withhold_kv && blockIdx.x == 0 && kv_it == 1) {
+                            if (hook && kv_it == 1) {
                                 ++kv_it;  // test hook: this copy never arrives
                                 continue;
                             }
@@ -308,8 +360,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (mine) mma_commit_elect(&sh.kv_empty[st]);
                 else mbar_arrive_elect(&sh.kv_empty[st]);
             };
-            for (int32_t ui = ub; ui < ue && live; ++ui) {
-                const WlUnit wu = units[ui];
+            for (uint32_t nu = 0; live; ++nu) {
+                const uint32_t us = nu % kURing;
+                live = mbar_wait_warp(&sh.u_full[us], (nu / kURing) & 1, abort_flag, err_word,
+                                      kErrTimeoutBase + 14, kWaitNs);
+                if (!live) break;
+                const int32_t idx = sh.u_slot[us];
+                __syncwarp();
+                mbar_arrive_elect(&sh.u_empty[us]);
+                if (idx < 0) break;
+                const WlUnit wu = ubase[idx];
                 const Unit u = decode_unit(wu, segs);
                 const int32_t n = u.ntiles;
                 if (n == 0) continue;
@@ -425,8 +485,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_base + 256 + i * 128;
         uint32_t s_cnt = 0, o_cnt = 0;
         bool live = true;
-        for (int32_t ui = ub; ui < ue && live; ++ui) {
-            const WlUnit wu = units[ui];
+        for (uint32_t nu = 0; live; ++nu) {
+            const uint32_t us = nu % kURing;
+            live = mbar_wait(&sh.u_full[us], (nu / kURing) & 1, abort_flag, err_word,
+                             kErrTimeoutBase + 14, kWaitNs);
+            if (!live) break;
+            const int32_t idx = sh.u_slot[us];
+            mbar_arrive(&sh.u_empty[us]);
+            if (idx < 0) break;
+            const WlUnit wu = ubase[idx];
             const Unit u = decode_unit(wu, segs);
             if (i >= u.nsub) continue;
             const SubTile st = i == 0 ? u.st[0] : u.st[1];
@@ -720,6 +787,7 @@ pva_status attn_fwd_impl(const void* q, const void* k, const void* v,
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
     ap.scale_log2 = scale * 1.4426950408889634f;
     ap.withhold_kv = g_withhold_kv.load(std::memory_order_relaxed);
+    ap.dynamic = params->dispatch == PVA_DISPATCH_STATIC ? 0 : 1;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return head_dim == 128 ? launch<128>(mq, mk, mv, ap, st) : launch<64>(mq, mk, mv, ap, st);
 }

@@ -14,6 +14,7 @@
 //   runs       WlRun[cap_runs]            per unit and slice: kv tile span [lo, hi)
 //   cta_off    int32[num_ctas + 1]        CSR offsets of the CTAs into `units`
 //   doc_scan   int32[4 * (num_docs + 1)]  per-document scan scratch
+//   dorder     int32[cap_units]           uid of the r-th unit in dispatch order
 #pragma once
 
 #include <stdint.h>
@@ -21,7 +22,7 @@
 namespace pva {
 
 constexpr int32_t kWlMagic = 0x57415650;  // "PVAW"
-constexpr int32_t kWlVersion = 2;
+constexpr int32_t kWlVersion = 3;
 constexpr int kMaxBins = 1024;
 constexpr int kUidBits = 24;   // units per worklist < 2^24
 constexpr int kCostBits = 40;  // unit cost < 2^40
@@ -40,12 +41,28 @@ struct WlUnit {
 };
 static_assert(sizeof(WlUnit) == 64, "WlUnit is 64 bytes");
 
+// Dispatch class of a unit: floor(log2(max(cost, 1))).  The dynamic dispatch
+// order: classes above a split class in decreasing order, units of one class
+// in enumeration order (segment, kv head, head pair, q tile), so that CTAs
+// running at the same time share the same documents' K/V in L2; then every
+// unit of the split class and below in exact LPT order (cost desc, uid asc).
+// The split is the highest class c whose units could not be absorbed by the
+// work below it: W(classes < c) < num_ctas * 2^(c + 1) (capped at 38, so that
+// the LPT part's costs fit the sort key).
+__host__ __device__ inline int32_t dispatch_class(int64_t cost) {
+    uint64_t c = cost > 1 ? (uint64_t)cost : 1u;
+    int32_t e = 0;
+    while (c >>= 1) ++e;
+    return e;
+}
+
 struct WlRun {
     int32_t slice, lo, hi, pad;
 };
 
 struct WlOffsets {
-    int64_t slices, segs, units_enum, keys, order, assign, units, runs, cta_off, doc_scan, total;
+    int64_t slices, segs, units_enum, keys, order, assign, units, runs, cta_off, doc_scan, dorder,
+        total;
 };
 
 struct WlHeader {
@@ -63,7 +80,13 @@ struct WlHeader {
     int32_t lpt_steps;  // batches + runs taken by the LPT (diagnostic)
     int32_t refine_iters;   // move/swap rounds allowed after LPT
     int32_t refine_rounds;  // move/swap rounds applied (diagnostic)
-    int32_t pad_[5];
+    // Dynamic dispatch of the forward kernel: the next rank of `dorder` to hand
+    // out and the CTAs that have finished; the last CTA to finish puts both
+    // back to 0.
+    int32_t dispatch_next, dispatch_done;
+    int32_t dispatch;  // pva_dispatch the worklist was built for (dorder exists if DYNAMIC)
+    int32_t dispatch_split;  // classes <= this one are dispatched in exact LPT order
+    int32_t pad_[1];
 };
 static_assert(sizeof(WlHeader) <= 256, "header fits in 256 bytes");
 

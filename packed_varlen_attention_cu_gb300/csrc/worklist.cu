@@ -473,12 +473,17 @@ constexpr int kSortThreads = 1024;
 struct SortArgs {
     const int32_t* err;
     const int32_t* n;
+    const int32_t* split;       // dispatch split class (dispatch keys only)
     unsigned long long* keys;
     int32_t* order;             // rank -> uid (LPT order)
+    int32_t* dorder;            // rank -> uid (dispatch order)
     const WlUnit* units_enum;   // CTA order: units by uid ...
     WlUnit* units;              // ... written at their rank
 };
 
+// kDispatchKeys: the chunk's keys are made here from the units (class desc,
+// uid asc) instead of read from `keys`.
+template <bool kDispatchKeys>
 __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a) {
     if (*a.err) return;
     const int32_t n = *a.n;
@@ -487,8 +492,23 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
     unsigned long long* keys = a.keys;
     __shared__ unsigned long long sk[kSortChunk];
     const int32_t m = min(kSortChunk, n - c0);
-    for (int32_t i = threadIdx.x; i < kSortChunk; i += kSortThreads)
-        sk[i] = i < m ? keys[c0 + i] : ~0ULL;
+    for (int32_t i = threadIdx.x; i < kSortChunk; i += kSortThreads) {
+        unsigned long long key = ~0ULL;
+        if (i < m) {
+            if (kDispatchKeys) {
+                // above the split: (0, 63 - class, uid); else (1, 2^39 - 1 - cost, uid)
+                const long long c = a.units_enum[c0 + i].cost;
+                const int32_t cls = dispatch_class(c);
+                key = cls > *a.split
+                          ? ((unsigned long long)(63 - cls) << 57)
+                          : (1ULL << 63) | ((((1ULL << 39) - 1) - (unsigned long long)c) << kUidBits);
+                key |= (unsigned long long)(c0 + i);
+            } else {
+                key = keys[c0 + i];
+            }
+        }
+        sk[i] = key;
+    }
     __syncthreads();
     for (int32_t size = 2; size <= kSortChunk; size <<= 1) {
         for (int32_t stride = size >> 1; stride > 0; stride >>= 1) {
@@ -508,10 +528,12 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
     for (int32_t i = threadIdx.x; i < m; i += kSortThreads) keys[c0 + i] = sk[i];
 }
 
-// kCtaOrder = false: keys are (~cost, uid) and order[rank] = uid (LPT order).
-// kCtaOrder = true: keys are (cta, uid) and units[rank] = the unit with its
-// CTA, i.e. the CSR list of every CTA in enumeration order.
-template <bool kCtaOrder>
+// kMode kRankLpt: keys are (~cost, uid) and order[rank] = uid (LPT order).
+// kRankCta: keys are (cta, uid) and units[rank] = the unit with its CTA, i.e.
+// the CSR list of every CTA in enumeration order.
+// kRankDispatch: keys are (63 - class, uid) and dorder[rank] = uid.
+enum RankMode { kRankLpt = 0, kRankCta = 1, kRankDispatch = 2 };
+template <int kMode>
 __global__ void __launch_bounds__(kSortThreads) wl_merge_rank_kernel(SortArgs a) {
     if (*a.err) return;
     const int32_t n = *a.n;
@@ -548,10 +570,12 @@ __global__ void __launch_bounds__(kSortThreads) wl_merge_rank_kernel(SortArgs a)
         const int32_t i = threadIdx.x + e * kSortThreads;
         if (i >= m) continue;
         const int32_t uid = (int32_t)(mine[e] & ((1ULL << kUidBits) - 1));
-        if (kCtaOrder) {
+        if (kMode == kRankCta) {
             WlUnit x = a.units_enum[uid];
             x.cta = (int32_t)(mine[e] >> kUidBits);
             a.units[rank[e]] = x;
+        } else if (kMode == kRankDispatch) {
+            a.dorder[rank[e]] = uid;
         } else {
             a.order[rank[e]] = uid;
         }
@@ -836,6 +860,45 @@ __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t
     }
     if (tid == 0) h->lpt_steps = steps;
     if (h->refine_iters > 0 && B > 1) lpt_refine(h, units_enum, assign, S, cnt, n, B);
+    if (h->dispatch == PVA_DISPATCH_DYNAMIC) {
+        // work per cost class, then the split class of the dispatch order
+        __shared__ unsigned long long cls_work[64];
+        if (tid < 64) cls_work[tid] = 0;
+        __syncthreads();
+        // one shared atomic per class present in a warp (warp sums by class)
+        const int32_t nr = (n + 31) & ~31;
+        for (int32_t u = tid; u < nr; u += blockDim.x) {
+            const unsigned long long c = u < n ? (unsigned long long)units_enum[u].cost : 0ULL;
+            const int32_t cls = u < n ? dispatch_class((long long)c) : 0;
+            unsigned todo = 0xffffffffu;
+            while (todo) {
+                const int leader = __ffs(todo) - 1;
+                const int32_t lc = __shfl_sync(0xffffffffu, cls, leader);
+                const bool mine = cls == lc;
+                unsigned long long v = mine ? c : 0ULL;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == leader) atomicAdd(&cls_work[lc], v);
+                todo &= ~__ballot_sync(0xffffffffu, mine);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long below = 0;
+            for (int c = 0; c < 64; ++c) below += cls_work[c];
+            int32_t split = 0;
+            for (int c = 63; c >= 0; --c) {
+                if (cls_work[c] == 0) continue;
+                below -= cls_work[c];  // work of the classes under c
+                if (below < ((unsigned long long)B << (c + 1))) {
+                    split = c < 38 ? c : 38;
+                    break;
+                }
+            }
+            h->dispatch_split = split;
+        }
+        __syncthreads();
+    }
     // CSR offsets: exclusive scan of the bin counts (warp scans + warp totals)
     int32_t inc = tid < B ? cnt[tid] : 0;
     const int32_t mine = inc;
@@ -998,7 +1061,8 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     if (!m || !p || num_docs < 0) return false;
     if (p->tile_m <= 0 || p->tile_n <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
         p->num_q_heads % p->num_kv_heads != 0 || p->c_tile < 0 || p->refine_iters < 0 ||
-        p->refine_iters > 1000)
+        p->refine_iters > 1000 || (p->dispatch != PVA_DISPATCH_DYNAMIC &&
+                                   p->dispatch != PVA_DISPATCH_STATIC))
         return false;
     if (num_ctas <= 0 || num_ctas > kMaxBins) return false;
     if (m->q_tokens < 0 || m->k_tokens < 0) return false;
@@ -1084,6 +1148,7 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     h->c_tile = p->c_tile;
     h->refine_iters = p->refine_iters;
     h->refine_rounds = 0;
+    h->dispatch = p->dispatch;
     int64_t o = 256;
     WlOffsets& f = h->off;
     f.slices = o; o = align256(o + (int64_t)h->cap_slices * sizeof(WlSlice));
@@ -1096,6 +1161,7 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     f.runs = o; o = align256(o + (int64_t)h->cap_runs * sizeof(WlRun));
     f.cta_off = o; o = align256(o + ((int64_t)num_ctas + 1) * 4);
     f.doc_scan = o; o = align256(o + 4 * ((int64_t)num_docs + 1) * 4);
+    f.dorder = o; o = align256(o + cap_units * 4);
     f.total = o;
     return true;
 }
@@ -1175,15 +1241,21 @@ extern "C" pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t 
     sa.n = reinterpret_cast<const int32_t*>(base + offsetof(WlHeader, nunits));
     sa.keys = reinterpret_cast<unsigned long long*>(base + h.off.keys);
     sa.order = reinterpret_cast<int32_t*>(base + h.off.order);
+    sa.dorder = reinterpret_cast<int32_t*>(base + h.off.dorder);
+    sa.split = reinterpret_cast<const int32_t*>(base + offsetof(WlHeader, dispatch_split));
     sa.units_enum = reinterpret_cast<const WlUnit*>(base + h.off.units_enum);
     sa.units = reinterpret_cast<WlUnit*>(base + h.off.units);
-    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(sa);
-    wl_merge_rank_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
+    wl_sort_chunks_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
+    wl_merge_rank_kernel<kRankLpt><<<sb, kSortThreads, 0, st>>>(sa);
     const int bp = ((nc + 31) / 32) * 32;
     const int lpt_f = bp >= 1024 ? 1 : (1024 / bp < 4 ? 1024 / bp : 4);
     wl_lpt_kernel<<<1, bp * lpt_f, 0, st>>>(base, lpt_f);
-    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(sa);
-    wl_merge_rank_kernel<true><<<sb, kSortThreads, 0, st>>>(sa);
+    wl_sort_chunks_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
+    wl_merge_rank_kernel<kRankCta><<<sb, kSortThreads, 0, st>>>(sa);
+    if (params->dispatch == PVA_DISPATCH_DYNAMIC) {
+        wl_sort_chunks_kernel<true><<<sb, kSortThreads, 0, st>>>(sa);
+        wl_merge_rank_kernel<kRankDispatch><<<sb, kSortThreads, 0, st>>>(sa);
+    }
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
 
@@ -1406,10 +1478,12 @@ extern "C" pva_status pva_build_bwd_plan(const void* worklist_dev, int32_t num_d
     sa.n = reinterpret_cast<const int32_t*>(base + offsetof(BwdHeader, nunits));
     sa.keys = reinterpret_cast<unsigned long long*>(base + bh.off_keys);
     sa.order = reinterpret_cast<int32_t*>(base + bh.off_order);
+    sa.dorder = nullptr;
+    sa.split = nullptr;
     sa.units_enum = nullptr;
     sa.units = nullptr;
     const int sb = (bh.cap_units + kSortChunk - 1) / kSortChunk;
-    wl_sort_chunks_kernel<<<sb, kSortThreads, 0, st>>>(sa);
-    wl_merge_rank_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
+    wl_sort_chunks_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
+    wl_merge_rank_kernel<kRankLpt><<<sb, kSortThreads, 0, st>>>(sa);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }

@@ -19,13 +19,14 @@ pytestmark = pytest.mark.gpu
 
 
 def _full_check(oracle_mod, lengths, hq, hkv, d, kind=W.MASK_CAUSAL, window=0, num_prefix=0,
-                seed=0, out_fp32=False, num_ctas=0, c_tile=0, scale_v=1.0):
+                seed=0, out_fp32=False, num_ctas=0, c_tile=0, scale_v=1.0,
+                dispatch=api.DISPATCH_DYNAMIC):
     cu = W.cu_seqlens_of(lengths)
     T = int(cu[-1])
     q, k, v = W.make_qkv(T, T, hq, hkv, d, seed, scale_v)
     mask = api.make_mask(kind, T, T, window=window, num_prefix_docs=num_prefix)
     out, lse, _ = run_gpu(q, k, v, cu, mask, hq, hkv, num_ctas=num_ctas, c_tile=c_tile,
-                          out_fp32=out_fp32)
+                          out_fp32=out_fp32, dispatch=dispatch)
     ref_o, ref_l = oracle_mod.attention(oracle_mod.bf16_bits(q), oracle_mod.bf16_bits(k),
                                         oracle_mod.bf16_bits(v), cu,
                                         oracle_mask(kind, window, num_prefix))
@@ -66,9 +67,43 @@ def test_single_long_document_many_tiles(oracle_mod):
     _full_check(oracle_mod, [3000], 2, 1, 128, seed=9, scale_v=0.5)
 
 
+@pytest.mark.parametrize("dispatch", [api.DISPATCH_DYNAMIC, api.DISPATCH_STATIC])
 @pytest.mark.parametrize("num_ctas,c_tile", [(1, 0), (3, 100), (1024, 0)])
-def test_cta_counts(oracle_mod, num_ctas, c_tile):
-    _full_check(oracle_mod, [520, 130, 900], 4, 2, 64, num_ctas=num_ctas, c_tile=c_tile, seed=4)
+def test_cta_counts(oracle_mod, num_ctas, c_tile, dispatch):
+    _full_check(oracle_mod, [520, 130, 900], 4, 2, 64, num_ctas=num_ctas, c_tile=c_tile, seed=4,
+                dispatch=dispatch)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_dynamic_and_static_dispatch_agree_bitwise(d):
+    """A unit computes the same bits whichever CTA runs it: dynamic dispatch
+    (units claimed in LPT order at run time) and the static per-CTA lists give
+    identical outputs, and repeated launches on one worklist (whose claim
+    counter the last CTA resets) repeat them."""
+    lengths = [int(x) for x in W.lognormal_doc_lengths(12000, np.log(900.0), 1.2, 1, 6000, 3)]
+    cu_np = W.cu_seqlens_of(lengths)
+    T = int(cu_np[-1])
+    q, k, v = (x.cuda() for x in W.make_qkv(T, T, 4, 2, d, 11, 1.0))
+    mask = api.make_mask(W.MASK_CAUSAL, T, T)
+    cu = torch.from_numpy(cu_np).cuda()
+    res = {}
+    for disp in (api.DISPATCH_STATIC, api.DISPATCH_DYNAMIC):
+        params = api.make_params(4, 2, c_tile=api.default_c_tile(d), dispatch=disp)
+        wl = api.alloc_worklist(len(lengths), mask, params)
+        api.build_worklist(cu, mask, params, wl)
+        runs = []
+        for _ in range(3):
+            out = torch.empty_like(q)
+            lse = torch.empty((4, T), dtype=torch.float32, device="cuda")
+            api.attn_fwd(q, k, v, cu, mask, params, wl, out, lse, 0.0)
+            runs.append((out, lse))
+        torch.cuda.synchronize()
+        assert api.worklist_error(wl) == 0
+        for o, l in runs[1:]:
+            assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1])
+        res[disp] = runs[0]
+    assert torch.equal(res[api.DISPATCH_STATIC][0], res[api.DISPATCH_DYNAMIC][0])
+    assert torch.equal(res[api.DISPATCH_STATIC][1], res[api.DISPATCH_DYNAMIC][1])
 
 
 def test_large_logits_rescale_path(oracle_mod):

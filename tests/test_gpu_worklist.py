@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from packed_varlen_attention_cu_gb300 import api
 from packed_varlen_attention_cu_gb300 import workloads as W
 
@@ -29,6 +30,12 @@ def _gpu_worklist(cu_np, mask, hq, hkv, num_ctas, c_tile):
 
 
 def _assert_same(g, o):
+    if g["dispatch_order"] is not None:
+        # run-time dispatch order: oracle.dispatch_order of the costs by uid
+        cost = np.zeros(len(o["unit_cost"]), dtype=np.int64)
+        cost[o["units"].reshape(-1, 10)[:, 0]] = o["unit_cost"]
+        np.testing.assert_array_equal(g["dispatch_order"],
+                                      oracle.dispatch_order(cost, g["header"]["num_ctas"]))
     np.testing.assert_array_equal(g["slices"], o["slices"].reshape(-1, 8))
     np.testing.assert_array_equal(g["segs"][:, :5], o["segs"].reshape(-1, 5))
     np.testing.assert_array_equal(g["units"], o["units"].reshape(-1, 10))

@@ -157,3 +157,51 @@ def test_zigzag_chunk_without_keys_keeps_empty_segment(oracle_mod):
     assert len(segs) == 2 and segs[0][4] == 0 and segs[1][4] == 2
     empty_units = [u for u in wl["units"] if u[1] == 0]
     assert all(u[8] == 0 for u in empty_units)
+
+
+# ------------------------------------------------------ run-time dispatch order
+def test_dispatch_order_worked_examples(oracle_mod):
+    # classes floor(log2(max(c, 1))): 100, 70, 120 -> 6; 40 -> 5; 20, 30 -> 4; 10 -> 3; 5 -> 2
+    costs = [100, 70, 120, 40, 20, 40, 30, 10, 5]
+    # one CTA: class 6 has 145 below it (>= 2^7), class 5 has 65 (>= 2^6), class 4
+    # only 15 (< 2^5): classes 6 and 5 in uid order, then 30, 20, 10, 5 by cost
+    assert oracle_mod.dispatch_order(costs, 1).tolist() == [0, 1, 2, 3, 5, 6, 4, 7, 8]
+    # two CTAs: 145 < 2 * 2^7 already at class 6, so the whole order is LPT
+    assert oracle_mod.dispatch_order(costs, 2).tolist() == [2, 0, 1, 3, 5, 6, 4, 7, 8]
+    # the lowest class always takes the LPT order (nothing below it)
+    assert oracle_mod.dispatch_order([1, 3, 2, 0], 1).tolist() == [1, 2, 0, 3]
+
+
+def test_dispatch_order_is_lpt_over_power_of_two_classes(oracle_mod):
+    """On a real worklist the order is a permutation of the uids: a prefix whose
+    cost classes never increase, uids ascending inside a class, then a suffix
+    of the lowest classes sorted by (cost desc, uid asc); the class of each cost
+    is checked by integer shifts (2^k <= c < 2^(k+1)), and the suffix starts
+    where the work left below a class drops under 152 * 2^(k+1)."""
+    w = W.long_tail_gqa(1)
+    wl = oracle_mod.worklist(w.cu_seqlens, oracle_mod.Mask(), 128, 128, w.num_q_heads,
+                             w.num_kv_heads, 152, 65536)
+    uid = wl["units"][:, 0]
+    cost = np.zeros(uid.shape[0], dtype=np.int64)
+    cost[uid] = wl["unit_cost"]
+    order = oracle_mod.dispatch_order(cost, 152)
+    assert sorted(order.tolist()) == list(range(uid.shape[0]))
+    c = np.maximum(cost[order], 1)
+    k = np.zeros_like(c)
+    for e in range(63):
+        k[(c >> e) >= 1] = e
+    assert np.all((np.left_shift(1, k) <= c) & (c < np.left_shift(1, k + 1)))
+    assert np.all(np.diff(k) <= 0)
+    # the LPT suffix: from the first unit after which the order is cost-sorted
+    # and whose class fails the absorption test
+    cls_work = {int(x): int(cost[order][k == x].sum()) for x in np.unique(k)}
+    fails = [x for x in sorted(cls_work, reverse=True)
+             if sum(v for y, v in cls_work.items() if y < x) < 152 * 2 ** (x + 1)]
+    split = fails[0]
+    head = k > split
+    assert 0 < head.sum() < len(order)
+    assert np.all(head[:head.sum()]) and not np.any(head[head.sum():])
+    kh, oh = k[head], order[head]
+    assert np.all(np.diff(oh)[np.diff(kh) == 0] > 0)
+    ct, ot = cost[order][~head], order[~head]
+    assert np.all((np.diff(ct) < 0) | ((np.diff(ct) == 0) & (np.diff(ot) > 0)))
