@@ -77,7 +77,7 @@ def load_peaks():
 
 
 # device headers every kernel source includes: a change to them changes the kernel too
-KERNEL_HEADERS = ("common.h", "ptx.cuh", "tma_map.h", "wl_layout.cuh")
+KERNEL_HEADERS = ("common.h", "ptx.cuh", "tma_map.h", "unit_feed.cuh", "wl_layout.cuh")
 
 
 def kernel_source_sha(kernel_file: str):

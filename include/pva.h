@@ -351,7 +351,9 @@ int32_t pva_wlb_choose(const int32_t* cu_seqlens_host, int32_t num_docs, int32_t
  *                    time follows tiles alone), for pva_worklist_params.c_tile
  *   coef_out         HOST double [2] {a ns per pair, c ns per tile}, or NULL
  * Copies the worklists' units to the host and synchronizes `stream`.
- * PVA_ERR_INVALID_ARG if both coefficients are zero (no usable sample). */
+ * The worklists must be built for PVA_DISPATCH_STATIC (per-CTA samples need
+ * the static assignment); PVA_ERR_INVALID_ARG otherwise, and if both
+ * coefficients are zero (no usable sample). */
 pva_status pva_fit_tile_cost(const void* const* worklists_dev,
                              const uint64_t* const* cta_busy_ns_dev, int32_t num_runs,
                              int64_t* c_tile_out, double* coef_out, void* stream);

@@ -50,14 +50,11 @@ def make_mask(kind: int = MASK_CAUSAL, q_tokens: int = 0, k_tokens: int = 0, win
 
 DISPATCH_DYNAMIC, DISPATCH_STATIC = 0, 1  # pva_dispatch
 
-# Kernels one pva_build_worklist launches: plan, units, chunk sort + merge
-# rank (LPT order), LPT, chunk sort + merge rank (per-CTA order), and for
-# dynamic dispatch chunk sort + merge rank (dispatch order).
-WORKLIST_BUILD_KERNELS = 7
-
-
+# Kernels one pva_build_worklist launches: plan, units, then for static
+# dispatch chunk sort + merge rank (LPT order), LPT, chunk sort + merge rank
+# (per-CTA order); for dynamic dispatch chunk sort + merge rank (dispatch order).
 def worklist_build_kernels(params) -> int:
-    return WORKLIST_BUILD_KERNELS + (2 if params.dispatch == DISPATCH_DYNAMIC else 0)
+    return 4 if params.dispatch == DISPATCH_DYNAMIC else 7
 
 
 def default_c_tile(head_dim: int) -> int:
@@ -303,15 +300,17 @@ def worklist_counts(worklist: torch.Tensor, stream=None) -> dict:
 
 # ----------------------------------------------------------------- decoding
 _HDR = np.dtype([("i32", "<i4", 20), ("c_tile", "<i8"), ("pair_sum", "<u8"), ("tile_sum", "<u8"),
-                 ("off", "<i8", 12)])
+                 ("off", "<i8", 13)])
 _OFF = ("slices", "segs", "units_enum", "keys", "order", "assign", "units", "runs",
-        "cta_off", "doc_scan", "dorder", "total")
+        "cta_off", "doc_scan", "dorder", "cls_work", "total")
 
 
 def decode_worklist(worklist: torch.Tensor) -> dict:
-    """Copy a built worklist to the host and split it into numpy arrays
-    (segments, slices, units in CTA order, runs, CSR offsets, and for a
-    worklist built for dynamic dispatch the dispatch order of the uids)."""
+    """Copy a built worklist to the host and split it into numpy arrays:
+    segments, slices, runs and the units.  A static-dispatch worklist gives
+    its units in CTA order with the CSR offsets of the CTAs; a dynamic one
+    gives them in enumeration (uid) order (cta -1, no offsets) with the
+    dispatch order of the uids."""
     raw = worklist.detach().cpu().numpy()
     h = np.frombuffer(raw[:_HDR.itemsize].tobytes(), dtype=_HDR)[0]
     i32 = h["i32"]
@@ -321,8 +320,8 @@ def decode_worklist(worklist: torch.Tensor) -> dict:
     hd = {n: int(x) for n, x in zip(names, i32)}
     off = {n: int(x) for n, x in zip(_OFF, h["off"])}
     # after the offsets: lpt_steps, refine_iters, refine_rounds, dispatch_next,
-    # dispatch_done, dispatch
-    tail = np.frombuffer(raw[_HDR.itemsize:_HDR.itemsize + 24].tobytes(), dtype="<i4")
+    # dispatch_done, dispatch, dispatch_split
+    tail = np.frombuffer(raw[_HDR.itemsize:_HDR.itemsize + 28].tobytes(), dtype="<i4")
     dispatch = tail[5]
 
     def arr(name, dtype, n, width):
@@ -330,7 +329,9 @@ def decode_worklist(worklist: torch.Tensor) -> dict:
         return np.frombuffer(b.tobytes(), dtype=dtype).reshape(n, width) if width > 1 else \
             np.frombuffer(b.tobytes(), dtype=dtype)
 
-    units = arr("units", "<i4", hd["nunits"], 16)
+    dynamic = dispatch == DISPATCH_DYNAMIC
+    # dynamic dispatch: no per-CTA lists; the units in enumeration (uid) order
+    units = arr("units_enum" if dynamic else "units", "<i4", hd["nunits"], 16)
     costs = units[:, 12:14].copy().view("<i8").reshape(-1)
     pairs = units[:, 14:16].copy().view("<i8").reshape(-1)
     return {"header": hd, "pair_sum": int(h["pair_sum"]), "tile_sum": int(h["tile_sum"]),
@@ -339,10 +340,9 @@ def decode_worklist(worklist: torch.Tensor) -> dict:
             "units": units[:, :10].copy(), "unit_ntiles": units[:, 10].copy(),
             "unit_cost": costs, "unit_pairs": pairs,
             "runs": arr("runs", "<i4", hd["nruns"], 4)[:, :3].copy(),
-            "cta_off": arr("cta_off", "<i4", hd["num_ctas"] + 1, 1).copy(),
-            "dispatch": int(dispatch),
-            "dispatch_order": (arr("dorder", "<i4", hd["nunits"], 1).copy()
-                               if dispatch == DISPATCH_DYNAMIC else None)}
+            "cta_off": None if dynamic else arr("cta_off", "<i4", hd["num_ctas"] + 1, 1).copy(),
+            "dispatch": int(dispatch), "dispatch_split": int(tail[6]),
+            "dispatch_order": arr("dorder", "<i4", hd["nunits"], 1).copy() if dynamic else None}
 
 
 class PackedAttention:

@@ -7,7 +7,8 @@
 //   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
 // Three kernels, no atomics (each output row has one writer):
 //   bwd_pre   D per (row, head), HBM-bound;
-//   bwd_dq    q-major over the forward worklist (its LPT-balanced CTA lists):
+//   bwd_dq    q-major over the forward worklist's units, dispatched as the
+//             worklist says (static per-CTA LPT lists, or claimed at run time):
 //             per query sub-tile, every kv tile of its runs: S and dP (two SS
 //             MMAs), then dS in the softmax warps, then dQ += dS K (TS MMA);
 //   bwd_dkdv  kv-major over the backward plan: per 128-key tile of one key
@@ -27,6 +28,7 @@
 #include "common.h"
 #include "ptx.cuh"
 #include "tma_map.h"
+#include "unit_feed.cuh"
 #include "wl_layout.cuh"
 
 namespace pva {
@@ -63,6 +65,7 @@ struct BShared {
     uint64_t a_full, a_empty, o_full, o_empty, done;
     uint64_t s2_full[2], p2_full[2];  // per half-item tensor-memory buffer
     uint64_t r_full[8], r_empty[8];
+    UnitRing<8> ur;  // the producer hands each unit's index to the other roles
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -148,6 +151,8 @@ __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_
         mbar_init(&sh.r_full[s], 1);
         mbar_init(&sh.r_empty[s], 1);
     }
+    // unit readers: the MMA warp (one arrival) and every element-wise thread
+    uring_init(sh.ur, 1 + elem_threads);
     sh.abort_flag = 0;
     fence_barrier_init();
 }
@@ -179,13 +184,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WlHeader* h = reinterpret_cast<const WlHeader*>(p.wl);
     int32_t* err_word = const_cast<int32_t*>(&h->error);
     if (h->error != 0) return;
-    const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
-    const WlUnit* units = reinterpret_cast<const WlUnit*>(p.wl + h->off.units);
+    // the worklist's dispatch: static per-CTA lists of `units`, or (dynamic)
+    // ranks of `dorder` claimed at run time from the worklist's counter
+    const bool dyn = h->dispatch == PVA_DISPATCH_DYNAMIC;
+    WlHeader* hw = const_cast<WlHeader*>(h);
+    const int32_t nunits = h->nunits;
+    const int32_t* dorder = reinterpret_cast<const int32_t*>(p.wl + h->off.dorder);
+    const WlUnit* ubase = reinterpret_cast<const WlUnit*>(p.wl + (dyn ? h->off.units_enum
+                                                                       : h->off.units));
     const WlRun* runs = reinterpret_cast<const WlRun*>(p.wl + h->off.runs);
     const WlSlice* slices = reinterpret_cast<const WlSlice*>(p.wl + h->off.slices);
     const WlSeg* segs = reinterpret_cast<const WlSeg*>(p.wl + h->off.segs);
-    const int32_t ub = cta_off[blockIdx.x], ue = cta_off[blockIdx.x + 1];
-    if (ub >= ue) return;
+    const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
+    const int32_t ub = dyn ? 0 : cta_off[blockIdx.x], ue = dyn ? 0 : cta_off[blockIdx.x + 1];
+    if (!dyn && ub >= ue) return;
     if (tid == 0) init_barriers(sh, C::kStages, 128);
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
@@ -219,8 +231,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0, a_it = 0;
             bool live = true;
-            for (int32_t ui = ub; ui < ue && live; ++ui) {
-                const WlUnit u = units[ui];
+            for (uint32_t nu = 0; live; ++nu) {
+                live = uring_wait_free(sh.ur, nu, abort_flag, err_word, kErrTimeoutBase + 29,
+                                       kWaitNs);
+                if (!live) break;
+                int32_t idx;
+                if (dyn) {
+                    const int32_t rank = dispatch_claim(&hw->dispatch_next);
+                    idx = rank < nunits ? dorder[rank] : -1;
+                } else {
+                    idx = ub + (int32_t)nu < ue ? ub + (int32_t)nu : -1;
+                }
+                uring_put(sh.ur, nu, idx);
+                if (idx < 0) break;
+                const WlUnit u = ubase[idx];
                 if (u.ntiles == 0) continue;
                 const int nsub = u.h1 >= 0 ? 2 : 1;
                 for (int i = 0; i < nsub && live; ++i) {
@@ -299,8 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             pend = false;
             return true;
         };
-        for (int32_t ui = ub; ui < ue && live; ++ui) {
-            const WlUnit u = units[ui];
+        for (uint32_t nu = 0; live; ++nu) {
+            int32_t idx;
+            live = uring_get_warp(sh.ur, nu, idx, abort_flag, err_word, kErrTimeoutBase + 30,
+                                  kWaitNs);
+            if (!live || idx < 0) break;
+            const WlUnit u = ubase[idx];
             if (u.ntiles == 0) continue;
             const int nsub = u.h1 >= 0 ? 2 : 1;
             for (int i = 0; i < nsub && live; ++i) {
@@ -372,8 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_base, tQ = tmem + lane_base + 256;
         uint32_t gu = 0, o_cnt = 0;
         bool live = true;
-        for (int32_t ui = ub; ui < ue && live; ++ui) {
-            const WlUnit u = units[ui];
+        for (uint32_t nu = 0; live; ++nu) {
+            int32_t idx;
+            live = uring_get(sh.ur, nu, idx, abort_flag, err_word, kErrTimeoutBase + 30, kWaitNs);
+            if (!live || idx < 0) break;
+            const WlUnit u = ubase[idx];
             const int nsub = u.h1 >= 0 ? 2 : 1;
             for (int i = 0; i < nsub && live; ++i) {
                 int32_t q_row, nrows, q_pos0, head;
@@ -466,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    if (dyn && tid == 0) dispatch_exit(&hw->dispatch_next, &hw->dispatch_done);
 }
 
 // ==================================================================== dK, dV
@@ -506,7 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* gsl = reinterpret_cast<const int32_t*>(p.plan + bh->off_gslices);
     const int32_t n = bh->nunits, B = gridDim.x;
     const int32_t G = p.hq / p.hkv;
-    if ((int32_t)blockIdx.x >= n) return;
+    // dispatch as the forward worklist says: units claimed at run time in the
+    // plan's LPT order (dynamic), or dealt to the CTAs in snake order (static)
+    const bool dyn = h->dispatch == PVA_DISPATCH_DYNAMIC;
+    BwdHeader* bhw = const_cast<BwdHeader*>(bh);
+    if (!dyn && (int32_t)blockIdx.x >= n) return;
     if (tid == 0) init_barriers(sh, kItems, 128);
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
@@ -523,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     volatile int32_t* abort_flag = &sh.abort_flag;
-    // units sorted by cost, dealt to the CTAs in snake order: b, 2B-1-b, 2B+b, ...
+    // static: units sorted by cost, dealt to the CTAs in snake order: b, 2B-1-b, 2B+b, ...
     auto pos_of = [&](int32_t round) -> int32_t {
         return round * B + ((round & 1) ? B - 1 - (int32_t)blockIdx.x : (int32_t)blockIdx.x);
     };
@@ -533,8 +569,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0, a_it = 0;
             bool live = true;
-            for (int32_t rd = 0; pos_of(rd) < n && live; ++rd) {
-                const BwdUnit u = bunits[order[pos_of(rd)]];
+            for (uint32_t rd = 0; live; ++rd) {
+                live = uring_wait_free(sh.ur, rd, abort_flag, err_word, kErrTimeoutBase + 39,
+                                       kWaitNs);
+                if (!live) break;
+                int32_t pos = dyn ? dispatch_claim(&bhw->dispatch_next) : pos_of((int32_t)rd);
+                const int32_t idx = pos < n ? order[pos] : -1;
+                uring_put(sh.ur, rd, idx);
+                if (idx < 0) break;
+                const BwdUnit u = bunits[idx];
                 if (u.cost <= 1) continue;  // no query sees these keys
                 const WlSlice s = slices[gsl[u.gbegin]];
                 live = mbar_wait(&sh.a_empty, (a_it & 1) ^ 1, abort_flag, err_word,
@@ -624,8 +667,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             pend = false;
             return true;
         };
-        for (int32_t rd = 0; pos_of(rd) < n && live; ++rd) {
-            const BwdUnit u = bunits[order[pos_of(rd)]];
+        for (uint32_t rd = 0; live; ++rd) {
+            int32_t idx;
+            live = uring_get_warp(sh.ur, rd, idx, abort_flag, err_word, kErrTimeoutBase + 40,
+                                  kWaitNs);
+            if (!live || idx < 0) break;
+            const BwdUnit u = bunits[idx];
             if (u.cost <= 1) continue;
             live = mbar_wait_warp(&sh.a_full, a_it & 1, abort_flag, err_word,
                                   kErrTimeoutBase + 33, kWaitNs);
@@ -698,8 +745,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                        tK = tmem + lane_base + 256 + D;
         uint32_t gu = 0, o_cnt = 0;
         bool live = true;
-        for (int32_t rd = 0; pos_of(rd) < n && live; ++rd) {
-            const BwdUnit u = bunits[order[pos_of(rd)]];
+        for (uint32_t rd = 0; live; ++rd) {
+            int32_t idx;
+            live = uring_get(sh.ur, rd, idx, abort_flag, err_word, kErrTimeoutBase + 40, kWaitNs);
+            if (!live || idx < 0) break;
+            const BwdUnit u = bunits[idx];
             const WlSlice s0 = slices[gsl[u.gbegin]];  // the group's key range
             const int32_t krows = min(128, s0.k_len - u.kt * 128);
             const bool kvalid = kr < krows;
@@ -808,6 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    if (dyn && tid == 0) dispatch_exit(&bhw->dispatch_next, &bhw->dispatch_done);
 }
 
 template <int D>

@@ -36,6 +36,7 @@
 #include "common.h"
 #include "ptx.cuh"
 #include "tma_map.h"
+#include "unit_feed.cuh"
 #include "wl_layout.cuh"
 
 namespace pva {
@@ -108,9 +109,7 @@ struct Shared {
     uint64_t q_full[2], q_empty[2], s_full[2], p_half[2], p_full[2], o_full[2], o_empty[2], done[2],
         turn[2];
     uint64_t kv_full[8], kv_empty[8];
-    // the producer hands each unit (its index, or -1 at the end) to the other roles
-    uint64_t u_full[kURing], u_empty[kURing];
-    int32_t u_slot[kURing];
+    UnitRing<kURing> ur;  // the producer hands each unit's index to the other roles
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -171,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.dynamic ? reinterpret_cast<const WlUnit*>(p.wl + h->off.units_enum) : units;
     WlHeader* hw = const_cast<WlHeader*>(h);
     const int32_t nunits = h->nunits;
-    const int32_t ub = cta_off[blockIdx.x], ue = cta_off[blockIdx.x + 1];
+    // (a dynamic-dispatch worklist has no per-CTA lists)
+    const int32_t ub = p.dynamic ? 0 : cta_off[blockIdx.x];
+    const int32_t ue = p.dynamic ? 0 : cta_off[blockIdx.x + 1];
     const uint64_t t_start = globaltimer_ns();
     if (!p.dynamic && ub >= ue) {
         if (p.busy && tid == 0) {
@@ -197,10 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.kv_full[s], 1);
             mbar_init(&sh.kv_empty[s], 2);
         }
-        for (int s = 0; s < kURing; ++s) {
-            mbar_init(&sh.u_full[s], 1);
-            mbar_init(&sh.u_empty[s], kUReaders);
-        }
+        uring_init(sh.ur, kUReaders);
         sh.abort_flag = 0;
         fence_barrier_init();
     }
@@ -233,13 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // every claim of this CTA came before its finish; the last CTA to
         // finish leaves the counter at 0 for the next launch on this worklist
-        if (p.dynamic && tid == 0) {
-            __threadfence();
-            if (atomicAdd(&hw->dispatch_done, 1) == (int)gridDim.x - 1) {
-                atomicExch(&hw->dispatch_next, 0);
-                atomicExch(&hw->dispatch_done, 0);
-            }
-        }
+        if (p.dynamic && tid == 0) dispatch_exit(&hw->dispatch_next, &hw->dispatch_done);
     };
     if (warp < 4) {
       regs_dealloc<kRegsCtrl>();
@@ -250,22 +242,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool live = true;
             bool hook = p.withhold_kv && !p.dynamic && blockIdx.x == 0;
             for (uint32_t nu = 0; live; ++nu) {
-                const uint32_t us = nu % kURing;
-                live = mbar_wait(&sh.u_empty[us], ((nu / kURing) & 1) ^ 1, abort_flag, err_word,
-                                 kErrTimeoutBase + 13, kWaitNs);
+                live = uring_wait_free(sh.ur, nu, abort_flag, err_word, kErrTimeoutBase + 13,
+                                       kWaitNs);
                 if (!live) break;
                 int32_t idx;
                 if (p.dynamic) {
                     // claimed once this CTA's producer has issued every load of
                     // its previous unit, a few K/V steps before the CTA needs it
-                    const int32_t rank = atomicAdd(&hw->dispatch_next, 1);
+                    const int32_t rank = dispatch_claim(&hw->dispatch_next);
                     idx = rank < nunits ? order[rank] : -1;
                     if (rank == 0 && p.withhold_kv) hook = true;
                 } else {
                     idx = ub + (int32_t)nu < ue ? ub + (int32_t)nu : -1;
                 }
-                sh.u_slot[us] = idx;
-                mbar_arrive(&sh.u_full[us]);
+                uring_put(sh.ur, nu, idx);
                 if (idx < 0) break;
                 const WlUnit wu = ubase[idx];
                 const Unit u = decode_unit(wu, segs);
@@ -361,14 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else mbar_arrive_elect(&sh.kv_empty[st]);
             };
             for (uint32_t nu = 0; live; ++nu) {
-                const uint32_t us = nu % kURing;
-                live = mbar_wait_warp(&sh.u_full[us], (nu / kURing) & 1, abort_flag, err_word,
-                                      kErrTimeoutBase + 14, kWaitNs);
-                if (!live) break;
-                const int32_t idx = sh.u_slot[us];
-                __syncwarp();
-                mbar_arrive_elect(&sh.u_empty[us]);
-                if (idx < 0) break;
+                int32_t idx;
+                live = uring_get_warp(sh.ur, nu, idx, abort_flag, err_word, kErrTimeoutBase + 14,
+                                      kWaitNs);
+                if (!live || idx < 0) break;
                 const WlUnit wu = ubase[idx];
                 const Unit u = decode_unit(wu, segs);
                 const int32_t n = u.ntiles;
@@ -486,13 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t s_cnt = 0, o_cnt = 0;
         bool live = true;
         for (uint32_t nu = 0; live; ++nu) {
-            const uint32_t us = nu % kURing;
-            live = mbar_wait(&sh.u_full[us], (nu / kURing) & 1, abort_flag, err_word,
-                             kErrTimeoutBase + 14, kWaitNs);
-            if (!live) break;
-            const int32_t idx = sh.u_slot[us];
-            mbar_arrive(&sh.u_empty[us]);
-            if (idx < 0) break;
+            int32_t idx;
+            live = uring_get(sh.ur, nu, idx, abort_flag, err_word, kErrTimeoutBase + 14, kWaitNs);
+            if (!live || idx < 0) break;
             const WlUnit wu = ubase[idx];
             const Unit u = decode_unit(wu, segs);
             if (i >= u.nsub) continue;

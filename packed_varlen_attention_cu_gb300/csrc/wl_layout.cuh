@@ -15,6 +15,9 @@
 //   cta_off    int32[num_ctas + 1]        CSR offsets of the CTAs into `units`
 //   doc_scan   int32[4 * (num_docs + 1)]  per-document scan scratch
 //   dorder     int32[cap_units]           uid of the r-th unit in dispatch order
+//   cls_work   uint64[64]                 summed cost per dispatch class
+// A worklist built for dynamic dispatch has no LPT bins: order, assign,
+// units and cta_off are left unwritten (units_enum and dorder describe it).
 #pragma once
 
 #include <stdint.h>
@@ -62,7 +65,7 @@ struct WlRun {
 
 struct WlOffsets {
     int64_t slices, segs, units_enum, keys, order, assign, units, runs, cta_off, doc_scan, dorder,
-        total;
+        cls_work, total;
 };
 
 struct WlHeader {
@@ -111,6 +114,7 @@ static_assert(sizeof(BwdUnit) == 24, "BwdUnit is 24 bytes");
 struct BwdHeader {
     int32_t magic, error, nunits, cap_units;
     int32_t hq, hkv, q_tokens, k_tokens;
+    int32_t dispatch_next, dispatch_done;  // dynamic dispatch counter of the dK/dV pass
     int64_t off_units, off_keys, off_order, off_gslices, off_dvec, total;
 };
 static_assert(sizeof(BwdHeader) <= 256, "backward header fits in 256 bytes");

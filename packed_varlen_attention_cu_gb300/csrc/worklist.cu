@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
         *h = a.hinit;  // error word, counts and sums start at zero
         for (int k = 0; k < 4; ++k) carry[k] = 0;
     }
+    if (tid < 64)
+        reinterpret_cast<unsigned long long*>(a.base + a.hinit.off.cls_work)[tid] = 0ULL;
     __syncthreads();
 
     if (a.kind != PVA_MASK_SLICES) {
@@ -368,9 +370,11 @@ __global__ void __launch_bounds__(kUnitWarps * 32) wl_units_kernel(UnitArgs a) {
     const int32_t n = h->nunits;
     if ((int64_t)blockIdx.x * kUnitWarps >= n) return;
     __shared__ unsigned long long bsum[kUnitWarps][2];
+    __shared__ long long bcost[kUnitWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t u = blockIdx.x * kUnitWarps + warp;
     unsigned long long pairs_out = 0, tiles_out = 0;
+    long long cost_out = -1;  // -1: no unit
     if (u < n) {
         const WlSlice* slices = reinterpret_cast<const WlSlice*>(a.base + h->off.slices);
         const WlSeg* segs = reinterpret_cast<const WlSeg*>(a.base + h->off.segs);
@@ -444,10 +448,12 @@ __global__ void __launch_bounds__(kUnitWarps * 32) wl_units_kernel(UnitArgs a) {
         }
         pairs_out = (unsigned long long)pairs;
         tiles_out = (unsigned long long)tiles;
+        cost_out = w.cost;
     }
     if (lane == 0) {
         bsum[warp][0] = pairs_out;
         bsum[warp][1] = tiles_out;
+        bcost[warp] = cost_out;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -458,6 +464,22 @@ __global__ void __launch_bounds__(kUnitWarps * 32) wl_units_kernel(UnitArgs a) {
         }
         atomicAdd(&h->pair_sum, p);
         atomicAdd(&h->tile_sum, q);
+        if (h->dispatch == PVA_DISPATCH_DYNAMIC) {
+            // summed cost per dispatch class: one atomic per class in the block
+            unsigned long long* cw =
+                reinterpret_cast<unsigned long long*>(a.base + h->off.cls_work);
+            for (int i = 0; i < kUnitWarps; ++i) {
+                if (bcost[i] < 0) continue;
+                const int32_t ci = dispatch_class(bcost[i]);
+                bool seen = false;
+                for (int j = 0; j < i; ++j) seen |= bcost[j] >= 0 && dispatch_class(bcost[j]) == ci;
+                if (seen) continue;
+                unsigned long long sum = 0;
+                for (int j = i; j < kUnitWarps; ++j)
+                    if (bcost[j] >= 0 && dispatch_class(bcost[j]) == ci) sum += bcost[j];
+                atomicAdd(&cw[ci], sum);
+            }
+        }
     }
 }
 
@@ -473,7 +495,9 @@ constexpr int kSortThreads = 1024;
 struct SortArgs {
     const int32_t* err;
     const int32_t* n;
-    const int32_t* split;       // dispatch split class (dispatch keys only)
+    const unsigned long long* cls_work;  // summed cost per class (dispatch keys only)
+    int32_t* split;                      // where block 0 records the split class
+    int32_t num_ctas;                    // CTAs of the forward launch
     unsigned long long* keys;
     int32_t* order;             // rank -> uid (LPT order)
     int32_t* dorder;            // rank -> uid (dispatch order)
@@ -491,7 +515,29 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
     if (c0 >= n) return;
     unsigned long long* keys = a.keys;
     __shared__ unsigned long long sk[kSortChunk];
+    __shared__ int32_t s_split;
     const int32_t m = min(kSortChunk, n - c0);
+    if (kDispatchKeys) {
+        // the split: the highest non-empty class c with less work below it than
+        // num_ctas * 2^(c+1) (capped at 38)
+        if (threadIdx.x == 0) {
+            const int64_t B = a.num_ctas;
+            unsigned long long below = 0;
+            for (int c = 0; c < 64; ++c) below += a.cls_work[c];
+            int32_t split = 0;
+            for (int c = 63; c >= 0; --c) {
+                if (a.cls_work[c] == 0) continue;
+                below -= a.cls_work[c];  // work of the classes under c
+                if (below < ((unsigned long long)B << (c + 1))) {
+                    split = c < 38 ? c : 38;
+                    break;
+                }
+            }
+            s_split = split;
+            if (blockIdx.x == 0) *a.split = split;
+        }
+        __syncthreads();
+    }
     for (int32_t i = threadIdx.x; i < kSortChunk; i += kSortThreads) {
         unsigned long long key = ~0ULL;
         if (i < m) {
@@ -499,7 +545,7 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
                 // above the split: (0, 63 - class, uid); else (1, 2^39 - 1 - cost, uid)
                 const long long c = a.units_enum[c0 + i].cost;
                 const int32_t cls = dispatch_class(c);
-                key = cls > *a.split
+                key = cls > s_split
                           ? ((unsigned long long)(63 - cls) << 57)
                           : (1ULL << 63) | ((((1ULL << 39) - 1) - (unsigned long long)c) << kUidBits);
                 key |= (unsigned long long)(c0 + i);
@@ -860,45 +906,6 @@ __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t
     }
     if (tid == 0) h->lpt_steps = steps;
     if (h->refine_iters > 0 && B > 1) lpt_refine(h, units_enum, assign, S, cnt, n, B);
-    if (h->dispatch == PVA_DISPATCH_DYNAMIC) {
-        // work per cost class, then the split class of the dispatch order
-        __shared__ unsigned long long cls_work[64];
-        if (tid < 64) cls_work[tid] = 0;
-        __syncthreads();
-        // one shared atomic per class present in a warp (warp sums by class)
-        const int32_t nr = (n + 31) & ~31;
-        for (int32_t u = tid; u < nr; u += blockDim.x) {
-            const unsigned long long c = u < n ? (unsigned long long)units_enum[u].cost : 0ULL;
-            const int32_t cls = u < n ? dispatch_class((long long)c) : 0;
-            unsigned todo = 0xffffffffu;
-            while (todo) {
-                const int leader = __ffs(todo) - 1;
-                const int32_t lc = __shfl_sync(0xffffffffu, cls, leader);
-                const bool mine = cls == lc;
-                unsigned long long v = mine ? c : 0ULL;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == leader) atomicAdd(&cls_work[lc], v);
-                todo &= ~__ballot_sync(0xffffffffu, mine);
-            }
-        }
-        __syncthreads();
-        if (tid == 0) {
-            unsigned long long below = 0;
-            for (int c = 0; c < 64; ++c) below += cls_work[c];
-            int32_t split = 0;
-            for (int c = 63; c >= 0; --c) {
-                if (cls_work[c] == 0) continue;
-                below -= cls_work[c];  // work of the classes under c
-                if (below < ((unsigned long long)B << (c + 1))) {
-                    split = c < 38 ? c : 38;
-                    break;
-                }
-            }
-            h->dispatch_split = split;
-        }
-        __syncthreads();
-    }
     // CSR offsets: exclusive scan of the bin counts (warp scans + warp totals)
     int32_t inc = tid < B ? cnt[tid] : 0;
     const int32_t mine = inc;
@@ -1162,6 +1169,7 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     f.cta_off = o; o = align256(o + ((int64_t)num_ctas + 1) * 4);
     f.doc_scan = o; o = align256(o + 4 * ((int64_t)num_docs + 1) * 4);
     f.dorder = o; o = align256(o + cap_units * 4);
+    f.cls_work = o; o = align256(o + 64 * 8);
     f.total = o;
     return true;
 }
@@ -1242,19 +1250,23 @@ extern "C" pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t 
     sa.keys = reinterpret_cast<unsigned long long*>(base + h.off.keys);
     sa.order = reinterpret_cast<int32_t*>(base + h.off.order);
     sa.dorder = reinterpret_cast<int32_t*>(base + h.off.dorder);
-    sa.split = reinterpret_cast<const int32_t*>(base + offsetof(WlHeader, dispatch_split));
+    sa.cls_work = reinterpret_cast<const unsigned long long*>(base + h.off.cls_work);
+    sa.split = reinterpret_cast<int32_t*>(base + offsetof(WlHeader, dispatch_split));
+    sa.num_ctas = nc;
     sa.units_enum = reinterpret_cast<const WlUnit*>(base + h.off.units_enum);
     sa.units = reinterpret_cast<WlUnit*>(base + h.off.units);
-    wl_sort_chunks_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
-    wl_merge_rank_kernel<kRankLpt><<<sb, kSortThreads, 0, st>>>(sa);
-    const int bp = ((nc + 31) / 32) * 32;
-    const int lpt_f = bp >= 1024 ? 1 : (1024 / bp < 4 ? 1024 / bp : 4);
-    wl_lpt_kernel<<<1, bp * lpt_f, 0, st>>>(base, lpt_f);
-    wl_sort_chunks_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
-    wl_merge_rank_kernel<kRankCta><<<sb, kSortThreads, 0, st>>>(sa);
     if (params->dispatch == PVA_DISPATCH_DYNAMIC) {
+        // the CTAs take units at run time in dispatch order: no LPT bins
         wl_sort_chunks_kernel<true><<<sb, kSortThreads, 0, st>>>(sa);
         wl_merge_rank_kernel<kRankDispatch><<<sb, kSortThreads, 0, st>>>(sa);
+    } else {
+        wl_sort_chunks_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
+        wl_merge_rank_kernel<kRankLpt><<<sb, kSortThreads, 0, st>>>(sa);
+        const int bp = ((nc + 31) / 32) * 32;
+        const int lpt_f = bp >= 1024 ? 1 : (1024 / bp < 4 ? 1024 / bp : 4);
+        wl_lpt_kernel<<<1, bp * lpt_f, 0, st>>>(base, lpt_f);
+        wl_sort_chunks_kernel<false><<<sb, kSortThreads, 0, st>>>(sa);
+        wl_merge_rank_kernel<kRankCta><<<sb, kSortThreads, 0, st>>>(sa);
     }
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
@@ -1305,7 +1317,9 @@ pva_status add_fit_samples(const void* worklist_dev, const uint64_t* cta_busy_ns
     if (cudaMemcpyAsync(&h, worklist_dev, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return PVA_ERR_CUDA;
-    if (h.magic != kWlMagic || h.error != 0 || h.num_ctas <= 0 || h.nunits < 0)
+    // per-CTA samples need the static assignment
+    if (h.magic != kWlMagic || h.error != 0 || h.num_ctas <= 0 || h.nunits < 0 ||
+        h.dispatch != PVA_DISPATCH_STATIC)
         return PVA_ERR_INVALID_ARG;
     const int32_t B = h.num_ctas, n = h.nunits;
     std::vector<WlUnit> units((size_t)(n > 0 ? n : 1));
@@ -1479,7 +1493,9 @@ extern "C" pva_status pva_build_bwd_plan(const void* worklist_dev, int32_t num_d
     sa.keys = reinterpret_cast<unsigned long long*>(base + bh.off_keys);
     sa.order = reinterpret_cast<int32_t*>(base + bh.off_order);
     sa.dorder = nullptr;
+    sa.cls_work = nullptr;
     sa.split = nullptr;
+    sa.num_ctas = 0;
     sa.units_enum = nullptr;
     sa.units = nullptr;
     const int sb = (bh.cap_units + kSortChunk - 1) / kSortChunk;

@@ -18,10 +18,10 @@ from gpu_util import oracle_mask
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_worklist(cu_np, mask, hq, hkv, num_ctas, c_tile):
+def _gpu_worklist(cu_np, mask, hq, hkv, num_ctas, c_tile, dispatch=api.DISPATCH_STATIC):
     dev = torch.device("cuda")
     cu = torch.from_numpy(np.ascontiguousarray(cu_np, dtype=np.int32)).to(dev)
-    params = api.make_params(hq, hkv, num_ctas=num_ctas, c_tile=c_tile)
+    params = api.make_params(hq, hkv, num_ctas=num_ctas, c_tile=c_tile, dispatch=dispatch)
     wl = api.alloc_worklist(cu.numel() - 1, mask, params, dev)
     api.build_worklist(cu, mask, params, wl)
     torch.cuda.synchronize()
@@ -30,19 +30,26 @@ def _gpu_worklist(cu_np, mask, hq, hkv, num_ctas, c_tile):
 
 
 def _assert_same(g, o):
+    """A static worklist equals the oracle's (units in CTA order, CSR offsets);
+    a dynamic one has the same units in uid order without CTAs, and its
+    dispatch order is oracle.dispatch_order of the costs by uid."""
+    ou = o["units"].reshape(-1, 10)
+    oc, op = o["unit_cost"], o["unit_pairs"]
     if g["dispatch_order"] is not None:
-        # run-time dispatch order: oracle.dispatch_order of the costs by uid
-        cost = np.zeros(len(o["unit_cost"]), dtype=np.int64)
-        cost[o["units"].reshape(-1, 10)[:, 0]] = o["unit_cost"]
+        by_uid = np.argsort(ou[:, 0], kind="stable")
+        ou, oc, op = ou[by_uid].copy(), oc[by_uid], op[by_uid]
+        ou[:, 9] = -1
         np.testing.assert_array_equal(g["dispatch_order"],
-                                      oracle.dispatch_order(cost, g["header"]["num_ctas"]))
+                                      oracle.dispatch_order(oc, g["header"]["num_ctas"]))
+        assert g["cta_off"] is None
+    else:
+        np.testing.assert_array_equal(g["cta_off"], o["cta_off"])
     np.testing.assert_array_equal(g["slices"], o["slices"].reshape(-1, 8))
     np.testing.assert_array_equal(g["segs"][:, :5], o["segs"].reshape(-1, 5))
-    np.testing.assert_array_equal(g["units"], o["units"].reshape(-1, 10))
-    np.testing.assert_array_equal(g["unit_cost"], o["unit_cost"])
-    np.testing.assert_array_equal(g["unit_pairs"], o["unit_pairs"])
+    np.testing.assert_array_equal(g["units"], ou)
+    np.testing.assert_array_equal(g["unit_cost"], oc)
+    np.testing.assert_array_equal(g["unit_pairs"], op)
     np.testing.assert_array_equal(g["runs"], o["runs"].reshape(-1, 3))
-    np.testing.assert_array_equal(g["cta_off"], o["cta_off"])
 
 
 CASES = [
@@ -57,11 +64,13 @@ CASES = [
 
 @pytest.mark.parametrize("name,mk,kw", CASES, ids=[c[0] for c in CASES])
 @pytest.mark.parametrize("num_ctas,c_tile", [(152, 0), (148, 4096), (7, 1)])
-def test_worklist_bit_exact(oracle_mod, name, mk, kw, num_ctas, c_tile):
+@pytest.mark.parametrize("dispatch", [api.DISPATCH_STATIC, api.DISPATCH_DYNAMIC])
+def test_worklist_bit_exact(oracle_mod, name, mk, kw, num_ctas, c_tile, dispatch):
     w = mk()
     cu = w.cu_seqlens
     mask = api.mask_for_workload(w)
-    g, counts = _gpu_worklist(cu, mask, w.num_q_heads, w.num_kv_heads, num_ctas, c_tile)
+    g, counts = _gpu_worklist(cu, mask, w.num_q_heads, w.num_kv_heads, num_ctas, c_tile,
+                              dispatch)
     o = oracle_mod.worklist(cu, oracle_mask(w.mask_kind, w.window, w.num_prefix_docs), 128, 128,
                             w.num_q_heads, w.num_kv_heads, num_ctas, c_tile)
     _assert_same(g, o)
@@ -193,7 +202,7 @@ def test_worklist_refinement_bit_exact(oracle_mod, name, mk, num_ctas, c_tile):
     dev = torch.device("cuda")
     cu_d = torch.from_numpy(np.ascontiguousarray(cu, dtype=np.int32)).to(dev)
     params = api.make_params(w.num_q_heads, w.num_kv_heads, num_ctas=num_ctas, c_tile=c_tile,
-                             refine_iters=20)
+                             refine_iters=20, dispatch=api.DISPATCH_STATIC)
     wl = api.alloc_worklist(cu_d.numel() - 1, mask, params, dev)
     api.build_worklist(cu_d, mask, params, wl)
     torch.cuda.synchronize()
@@ -227,7 +236,8 @@ def test_fit_tile_cost_matches_oracle(oracle_mod):
     nc = torch.cuda.get_device_properties(0).multi_processor_count
     wls, busys, Ps, Us, ts = [], [], [], [], []
     for c_tile in (0, 65536):
-        params = api.make_params(w.num_q_heads, w.num_kv_heads, num_ctas=0, c_tile=c_tile)
+        params = api.make_params(w.num_q_heads, w.num_kv_heads, num_ctas=0, c_tile=c_tile,
+                                 dispatch=api.DISPATCH_STATIC)
         wl = api.alloc_worklist(w.num_docs, mask, params, dev)
         api.build_worklist(cu_d, mask, params, wl)
         busy = torch.zeros(2 * nc, dtype=torch.int64, device=dev)
