@@ -157,8 +157,10 @@ size_t pva_worklist_bytes(int32_t num_docs, const pva_mask_desc* mask,
 /* Build the worklist on the device ("03 · 长文负载均衡" §3.2, §2.1):
  * derive the slices of the mask, enumerate every (query sub-tile, kv tile)
  * work item with at least one allowed pair, cost each work unit by its exact
- * pair count (+ c_tile per tile and per sub-tile), sort by cost descending (stable) and assign
- * LPT-style to params->num_ctas bins (lightest bin, lowest id on ties).
+ * pair count (+ c_tile per tile and per sub-tile), then as params->dispatch
+ * says: STATIC sorts by cost descending (stable) and assigns LPT-style to
+ * params->num_ctas bins (lightest bin, lowest id on ties); DYNAMIC writes the
+ * dispatch order the CTAs claim from at run time (pva_dispatch).
  *   cu_seqlens_dev  DEVICE int32 [num_docs + 1]
  *   worklist_dev    DEVICE buffer of worklist_bytes >= pva_worklist_bytes(), 256-B aligned
  * The result is deterministic and identical for identical inputs. */
@@ -389,6 +391,31 @@ pva_status pva_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                                 const pva_mask_desc* mask, const pva_worklist_params* params,
                                 int32_t head_dim, void* out, int32_t out_is_fp32, float* lse,
                                 float softmax_scale, void* stream);
+
+/* One forward pass for a caller whose inputs and results are in HOST memory
+ * ("03 · 长文负载均衡" §1.1: the packed pack's attention).  Enqueued on
+ * `stream`, in order: the copies of Q, K, V and cu_seqlens to the caller's
+ * device buffers (one cudaMemcpyAsync each), pva_build_worklist,
+ * pva_attn_fwd (bf16 output), and the copies of O and LSE back to the host.
+ *   q_host, k_host, v_host   HOST bf16, the pva_attn_fwd layouts
+ *   cu_seqlens_host          HOST int32 [num_docs + 1] (unused for PVA_MASK_SLICES)
+ *   out_host                 HOST bf16 [q_tokens, num_q_heads, head_dim]
+ *   lse_host                 HOST fp32 [num_q_heads, q_tokens]
+ *   q_dev .. lse_dev         DEVICE buffers of the same sizes (caller-owned),
+ *                            worklist_dev of worklist_bytes (as for pva_build_worklist)
+ * The host buffers should be page-locked: with pageable memory the copies
+ * still happen, but the call then waits for them.  The call returns once
+ * everything is enqueued; the results are in out_host / lse_host when the
+ * stream reaches this point.  Device-side failures go to the worklist's error
+ * word.  Callers streaming packs alternate two streams and two sets of device
+ * buffers, so that one pack's copies overlap the previous pack's attention. */
+pva_status pva_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host,
+                             const int32_t* cu_seqlens_host, int32_t num_docs,
+                             const pva_mask_desc* mask, const pva_worklist_params* params,
+                             int32_t head_dim, void* out_host, float* lse_host,
+                             float softmax_scale, void* q_dev, void* k_dev, void* v_dev,
+                             int32_t* cu_seqlens_dev, void* worklist_dev, size_t worklist_bytes,
+                             void* out_dev, float* lse_dev, void* stream);
 
 /* Size in bytes of the static worklist array used by pva_attn_fwd_noalloc. */
 size_t pva_noalloc_scratch_bytes(void);

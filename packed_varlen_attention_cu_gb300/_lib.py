@@ -21,6 +21,7 @@ EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_attn
            "pva_zigzag_shard_len",
            "pva_zigzag_shard", "pva_gather_rows", "pva_merge_partials", "pva_worklist_error",
            "pva_worklist_counts", "pva_attn_fwd_noalloc", "pva_noalloc_scratch_bytes",
+           "pva_attn_fwd_host",
            "pva_debug_withhold_kv_load", "pva_chunk_areas", "pva_dispatch_chunks",
            "pva_striped_shard_len", "pva_striped_shard", "pva_wlb_choose",
            "pva_fit_tile_cost",
@@ -95,6 +96,9 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_float, P]
         L.pva_noalloc_scratch_bytes.restype = sz
         L.pva_noalloc_scratch_bytes.argtypes = []
+        L.pva_attn_fwd_host.restype = ctypes.c_int
+        L.pva_attn_fwd_host.argtypes = [P, P, P, P, i32, MP, WP, i32, P, P, ctypes.c_float,
+                                        P, P, P, P, P, sz, P, P, P]
         L.pva_chunk_areas.restype = ctypes.c_int
         L.pva_chunk_areas.argtypes = [P, i32, MP, i32, P, P]
         L.pva_dispatch_chunks.restype = ctypes.c_int

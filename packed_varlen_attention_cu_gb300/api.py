@@ -116,6 +116,39 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         _ptr(lse), float(softmax_scale), _ptr(cta_busy), _stream(stream)))
 
 
+def attn_fwd_host(q_host: torch.Tensor, k_host: torch.Tensor, v_host: torch.Tensor,
+                  cu_host: Optional[torch.Tensor], num_docs: int, mask: MaskDesc,
+                  params: WorklistParams, out_host: torch.Tensor, lse_host: torch.Tensor,
+                  dev_bufs: dict, softmax_scale: float = 0.0, stream=None) -> None:
+    """pva_attn_fwd_host: copies in, worklist, attention and copies out on one
+    stream.  Host tensors (pinned for asynchronous copies) hold the inputs and
+    receive O and LSE; dev_bufs holds the device buffers "q", "k", "v", "cu",
+    "worklist", "out", "lse" (see alloc_host_path_buffers)."""
+    for t in (q_host, k_host, v_host, out_host, lse_host):
+        assert not t.is_cuda and t.is_contiguous()
+    wl = dev_bufs["worklist"]
+    check("pva_attn_fwd_host", lib().pva_attn_fwd_host(
+        _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(cu_host), num_docs, ctypes.byref(mask),
+        ctypes.byref(params), q_host.shape[-1], _ptr(out_host), _ptr(lse_host),
+        float(softmax_scale), _ptr(dev_bufs["q"]), _ptr(dev_bufs["k"]), _ptr(dev_bufs["v"]),
+        _ptr(dev_bufs["cu"]), _ptr(wl), wl.numel(), _ptr(dev_bufs["out"]), _ptr(dev_bufs["lse"]),
+        _stream(stream)))
+
+
+def alloc_host_path_buffers(q_host: torch.Tensor, k_host: torch.Tensor, num_docs: int,
+                            mask: MaskDesc, params: WorklistParams, device=None) -> dict:
+    """Device buffers for attn_fwd_host with the shapes of q_host / k_host."""
+    dev = device or torch.device("cuda")
+    tq, hq, d = q_host.shape
+    return {"q": torch.empty(q_host.shape, dtype=torch.bfloat16, device=dev),
+            "k": torch.empty(k_host.shape, dtype=torch.bfloat16, device=dev),
+            "v": torch.empty(k_host.shape, dtype=torch.bfloat16, device=dev),
+            "cu": torch.empty((num_docs + 1,), dtype=torch.int32, device=dev),
+            "worklist": alloc_worklist(num_docs, mask, params, dev),
+            "out": torch.empty((tq, hq, d), dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty((hq, tq), dtype=torch.float32, device=dev)}
+
+
 def attn_fwd_accumulate(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                         cu_seqlens: Optional[torch.Tensor], mask: MaskDesc,
                         params: WorklistParams, worklist: torch.Tensor, o_run: torch.Tensor,

@@ -16,7 +16,8 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libpva.so")
-SOURCES = ["api.cu", "worklist.cu", "attn_fwd.cu", "ops.cu", "noalloc.cu", "dispatch.cu", "attn_bwd.cu"]
+SOURCES = ["api.cu", "worklist.cu", "attn_fwd.cu", "ops.cu", "noalloc.cu", "dispatch.cu", "attn_bwd.cu",
+           "host_io.cu"]
 HEADERS = ["ptx.cuh", "wl_layout.cuh", "common.h", "tma_map.h", "unit_feed.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
