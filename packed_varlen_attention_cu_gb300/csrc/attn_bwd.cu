@@ -34,7 +34,13 @@
 namespace pva {
 namespace {
 
-constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 4-7 element-wise + epilogue
+// warp 0 TMA, warp 1 MMA, warps 4-11 element-wise + epilogue (two warpgroups
+// taking alternate half-items)
+constexpr int kThreads = 384;
+// bwd_dkdv's register split (kSplitRegs): the TMA/MMA warpgroup gives registers
+// to the two element-wise warpgroups
+constexpr bool kSplitRegs = false;
+constexpr uint32_t kRegsCtrl = 152, kRegsElem = 176;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
@@ -198,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
     const int32_t ub = dyn ? 0 : cta_off[blockIdx.x], ue = dyn ? 0 : cta_off[blockIdx.x + 1];
     if (!dyn && ub >= ue) return;
-    if (tid == 0) init_barriers(sh, C::kStages, 128);
+    if (tid == 0) init_barriers(sh, C::kStages, 256);
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -395,6 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- dS and the dQ epilogue
+        // Two warpgroups: wg takes the half-items u with u % 2 == wg (tensor-memory
+        // buffer wg); each stores half of the dQ columns.
+        const int wg = (warp - 4) >> 2;
         const int r = (warp & 3) * 32 + lane;  // query row = tensor-memory lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base, tQ = tmem + lane_base + 256;
@@ -412,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = r < nrows;
                 const int64_t grow = ((int64_t)(q_row + r) * p.hq + head) * D;
                 if (u.ntiles == 0) {  // rows without keys: zero gradient
-                    if (valid) store_zero_row(p.dq, grow, p.grads_fp32, D);
+                    if (valid) store_zero_row(p.dq, grow + wg * (D / 2), p.grads_fp32, D / 2);
                     continue;
                 }
                 const int32_t q_pos = q_pos0 + r;
@@ -435,7 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t c_hi = min(128, lim_hi - kt0), c_lo = max(0, lim_lo - kt0);
                         const int32_t halves = min(128, s.k_len - kt0) > 64 ? 2 : 1;
                         for (int32_t hf = 0; hf < halves && live; ++hf, ++gu) {
+                            if ((int)(gu & 1) != wg) continue;
                             const uint32_t b = gu & 1;
+                            // the warp masks only when some row has a limit inside the half
+                            const int h0 = hf * 64;
+                            const bool need_mask =
+                                __any_sync(0xffffffffu, c_lo > h0 || c_hi < h0 + 64);
                             live = mbar_wait(&sh.s2_full[b], (gu >> 1) & 1, abort_flag, err_word,
                                              kErrTimeoutBase + 27, kWaitNs);
                             if (!live) break;
@@ -454,8 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     const int col = hf * 64 + c * 32 + e;
                                     float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - lse2);
                                     float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lse2);
-                                    if (col < c_lo || col >= c_hi) p0 = 0.f;
-                                    if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                                    if (need_mask) {
+                                        if (col < c_lo || col >= c_hi) p0 = 0.f;
+                                        if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                                    }
                                     const float g0 = p0 * (__uint_as_float(pv[e]) - dd);
                                     const float g1 = p1 * (__uint_as_float(pv[e + 1]) - dd);
                                     dsw[e >> 1] = pack_bf16x2(g0, g1);
@@ -475,18 +491,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!live) break;
                 ++o_cnt;
                 tc_fence_after();
-                uint32_t o[D / 32][32];
+                // this warpgroup's half of the dQ columns
+                constexpr int kHalfChunks = D / 64;
+                uint32_t o[kHalfChunks][32];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) tmem_ld32(tQ + c * 32, o[c]);
+                for (int c = 0; c < kHalfChunks; ++c)
+                    tmem_ld32(tQ + (wg * kHalfChunks + c) * 32, o[c]);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
+                for (int c = 0; c < kHalfChunks; ++c) tmem_ld_wait(o[c]);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.o_empty);
                 if (valid) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c)
-                        store_row32(p.dq, grow + c * 32, p.grads_fp32, o[c], p.scale);
+                    for (int c = 0; c < kHalfChunks; ++c)
+                        store_row32(p.dq, grow + (wg * kHalfChunks + c) * 32, p.grads_fp32, o[c],
+                                    p.scale);
                 }
             }
         }
@@ -543,7 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool dyn = h->dispatch == PVA_DISPATCH_DYNAMIC;
     BwdHeader* bhw = const_cast<BwdHeader*>(bh);
     if (!dyn && (int32_t)blockIdx.x >= n) return;
-    if (tid == 0) init_barriers(sh, kItems, 128);
+    if (tid == 0) init_barriers(sh, kItems, 256);
+    // per element-wise warp: (LSE log2, D) of the 64 queries of its half-item
+    __shared__ __align__(16) float2 s_ld[8][64];
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -564,6 +586,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return round * B + ((round & 1) ? B - 1 - (int32_t)blockIdx.x : (int32_t)blockIdx.x);
     };
 
+    // register split (128 * kRegsCtrl + 256 * kRegsElem <= 384 * 168)
+    if (kSplitRegs) {
+        if (warp < 4) regs_dealloc<kRegsCtrl>();
+        else regs_alloc<kRegsElem>();
+    }
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
@@ -739,10 +766,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- P^T, dS^T and the dK/dV epilogue
+        // Two warpgroups: wg takes the half-items u with u % 2 == wg (tensor-memory
+        // buffer wg); at the end of a unit wg 0 stores dV and wg 1 dK.
+        const int wg = (warp - 4) >> 2;
         const int kr = (warp & 3) * 32 + lane;  // key row = tensor-memory lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base, tV = tmem + lane_base + 256,
                        tK = tmem + lane_base + 256 + D;
+        float2* my_ld = s_ld[warp - 4];
         uint32_t gu = 0, o_cnt = 0;
         bool live = true;
         for (uint32_t rd = 0; live; ++rd) {
@@ -756,8 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t grow = ((int64_t)(s0.k_row0 + u.kt * 128 + kr) * p.hkv + u.kvh) * D;
             if (u.cost <= 1) {  // keys no query sees: zero gradient
                 if (kvalid) {
-                    store_zero_row(p.dk, grow, p.grads_fp32, D);
-                    store_zero_row(p.dv, grow, p.grads_fp32, D);
+                    store_zero_row(wg == 0 ? p.dv : p.dk, grow, p.grads_fp32, D);
                 }
                 continue;
             }
@@ -779,7 +809,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t c_hi = kvalid ? (int32_t)min((int64_t)nq, qb - cpos0) : 0;
                     const uint32_t halves = nq > 64 ? 2 : 1;
                     for (uint32_t hf = 0; hf < halves && live; ++hf, ++gu) {
+                        if ((int)(gu & 1) != wg) continue;
                         const uint32_t b = gu & 1;
+                        // (LSE log2, D) of this half's 64 queries into the warp's slots,
+                        // loaded before the wait for S^T; a query past the tile has
+                        // LSE = +inf, so every P of it is 0
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const int qc = (int)hf * 64 + c * 32 + lane;
+                            float l2 = INFINITY, dd = 0.f;
+                            if (qc < nq) {
+                                const int64_t li = (int64_t)head * p.q_tokens + qrow0 + qc;
+                                const float l = p.lse[li];
+                                if (l != -INFINITY) l2 = l * 1.4426950408889634f;
+                                dd = p.dvec[li];
+                            }
+                            my_ld[c * 32 + lane] = make_float2(l2, dd);
+                        }
+                        __syncwarp();
+                        // columns [c_lo, c_hi) of this key row are allowed; the warp
+                        // masks only when some row of it has a limit inside the half
+                        const int h0 = (int)hf * 64;
+                        const bool need_mask =
+                            __any_sync(0xffffffffu, c_lo > h0 || c_hi < min(h0 + 64, nq));
                         live = mbar_wait(&sh.s2_full[b], (gu >> 1) & 1, abort_flag, err_word,
                                          kErrTimeoutBase + 37, kWaitNs);
                         if (!live) break;
@@ -787,15 +839,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t tSb = tS + 64 * b, tPb = tS + 128 + 64 * b;
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
-                            // LSE (log2) and D of query column 64 hf + 32 c + lane, by shuffles
-                            const int qc = (int)hf * 64 + c * 32 + lane;
-                            float my_l2 = INFINITY, my_d = 0.f;  // no query: every P is 0
-                            if (qc < nq) {
-                                const int64_t li = (int64_t)head * p.q_tokens + qrow0 + qc;
-                                const float l = p.lse[li];
-                                if (l != -INFINITY) my_l2 = l * 1.4426950408889634f;
-                                my_d = p.dvec[li];
-                            }
                             uint32_t sv[32], pv[32];
                             tmem_ld32(tSb + c * 32, sv);
                             tmem_ld32(tPb + c * 32, pv);
@@ -804,17 +847,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint32_t pw[32], dw[32];
 #pragma unroll
                             for (int e = 0; e < 32; e += 2) {
-                                const int col = (int)hf * 64 + c * 32 + e;
-                                const float l0 = __shfl_sync(0xffffffffu, my_l2, e);
-                                const float l1 = __shfl_sync(0xffffffffu, my_l2, e + 1);
-                                const float d0 = __shfl_sync(0xffffffffu, my_d, e);
-                                const float d1 = __shfl_sync(0xffffffffu, my_d, e + 1);
-                                float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - l0);
-                                float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - l1);
-                                if (col < c_lo || col >= c_hi) p0 = 0.f;
-                                if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
-                                const float g0 = p0 * (__uint_as_float(pv[e]) - d0);
-                                const float g1 = p1 * (__uint_as_float(pv[e + 1]) - d1);
+                                const float4 ld = *reinterpret_cast<const float4*>(&my_ld[c * 32 + e]);
+                                float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - ld.x);
+                                float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - ld.z);
+                                if (need_mask) {
+                                    const int col = h0 + c * 32 + e;
+                                    if (col < c_lo || col >= c_hi) p0 = 0.f;
+                                    if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                                }
+                                const float g0 = p0 * (__uint_as_float(pv[e]) - ld.y);
+                                const float g1 = p1 * (__uint_as_float(pv[e + 1]) - ld.w);
                                 pw[e >> 1] = pack_bf16x2(p0, p1);
                                 dw[e >> 1] = pack_bf16x2(g0, g1);
                             }
@@ -823,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tmem_st_wait();
                         tc_fence_before();
-                        __syncwarp();
+                        __syncwarp();  // also: every lane has read my_ld before its next write
                         if (lane == 0) mbar_arrive(&sh.p2_full[b]);
                     }
                 }
@@ -835,17 +877,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!live) break;
             ++o_cnt;
             tc_fence_after();
+            // wg 0: dV = P^T dO; wg 1: dK = scale dS^T Q
+            const uint32_t tOut = wg == 0 ? tV : tK;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[32], b[32];
-                tmem_ld32(tV + c * 32, a);
-                tmem_ld32(tK + c * 32, b);
+                uint32_t a[32];
+                tmem_ld32(tOut + c * 32, a);
                 tmem_ld_wait(a);
-                tmem_ld_wait(b);
-                if (kvalid) {
-                    store_row32(p.dv, grow + c * 32, p.grads_fp32, a, 1.f);
-                    store_row32(p.dk, grow + c * 32, p.grads_fp32, b, p.scale);
-                }
+                if (kvalid)
+                    store_row32(wg == 0 ? p.dv : p.dk, grow + c * 32, p.grads_fp32, a,
+                                wg == 0 ? 1.f : p.scale);
             }
             tc_fence_before();
             __syncwarp();
@@ -870,6 +911,13 @@ pva_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
     bwd_pre_kernel<<<grid_pre, 256, 0, st>>>(bp);
     auto kq = bwd_dq_kernel<D>;
     auto kk = bwd_dkdv_kernel<D>;
+    // setmaxnreg.inc draws from the registers the block was launched with: the
+    // dK/dV split must fit in (threads x registers per thread)
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kk) != cudaSuccess) return PVA_ERR_CUDA;
+    if (kSplitRegs &&
+        (int64_t)fa.numRegs * kThreads < 128 * (int64_t)kRegsCtrl + 256 * (int64_t)kRegsElem)
+        return PVA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem) !=
