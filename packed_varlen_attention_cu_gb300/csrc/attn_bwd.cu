@@ -16,7 +16,8 @@
 //             tile of every slice of the group and every head: S^T = K Q^T and
 //             dP^T = V dO^T, then P^T and dS^T, then dV += P^T dO and
 //             dK += dS^T Q, accumulated in tensor memory over the group.
-// Tensor-memory columns: bwd_dq S [0,128) dP [128,256) dQ [256,256+d);
+// Tensor-memory columns: bwd_dq S [0,128) dP [128,256) dQ [256,256+d), then Q and
+// dO as bf16 MMA A operands (d/2 columns each);
 // bwd_dkdv S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d,256+2d).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -311,6 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dKm = sdesc_sw128(smem_u32(sKV), 8192, 1024);  // MN-major, 64-row atoms
         constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, false);
         const uint32_t tQa = tmem + 256;
+        // Q and dO of the sub-tile, copied into tensor memory as the A operands of
+        // S = Q K^T and dP = dO V^T (TS MMAs read only the K / V halves from shared
+        // memory, so N = 64 runs at the full rate)
+        const uint32_t tQA = tmem + 256 + D, tDOA = tmem + 256 + D + D / 2;
         bool pend = false, first = true;
         uint32_t pend_u = 0, pend_st = 0;
         auto finish_pending = [&]() -> bool {
@@ -344,6 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 live = mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
                                       kErrTimeoutBase + 24, kWaitNs);
                 if (!live) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                    tmem_cp_elect(tQA + k * 8, dQd + off16);
+                    tmem_cp_elect(tDOA + k * 8, dDO + off16);
+                }
+                mma_commit_elect(&sh.a_empty);  // Q, dO copied: the producer may refill them
                 first = true;
                 for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
                     const WlRun run = runs[u.run_begin + rr];
@@ -362,17 +375,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint64_t oV = (st * 2 * kHalfBytes + kHalfBytes) >> 4;
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
-                                // Q, dO (128-row atoms) against the K, V halves (64-row atoms)
-                                const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                                // Q, dO (tensor memory) against the K, V halves (64-row atoms)
                                 const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
-                                mma_ss_elect(tmem + 64 * b, dQd + off16, dKn + oK + kq, kIdescHalf,
+                                mma_ts_elect(tmem + 64 * b, tQA + k * 8, dKn + oK + kq, kIdescHalf,
                                              k > 0);
                             }
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
-                                const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
                                 const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
-                                mma_ss_elect(tmem + 128 + 64 * b, dDO + off16, dKn + oV + kq,
+                                mma_ts_elect(tmem + 128 + 64 * b, tDOA + k * 8, dKn + oV + kq,
                                              kIdescHalf, k > 0);
                             }
                             mma_commit_elect(&sh.s2_full[b]);
@@ -390,7 +401,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!live) break;
                 if (pend && !finish_pending()) break;
-                mma_commit_elect(&sh.a_empty);  // Q, dO read by the last MMAs
                 mma_commit_elect(&sh.o_full);
                 ++o_cnt;
                 ++a_it;

@@ -248,6 +248,19 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
         : "memory");
 }
 
+// One elected lane copies 128 rows x 256 bits (one K = 16 slice of a 128-row
+// bf16 operand, 128-byte swizzled K-major, described like an MMA operand) from
+// shared memory into 8 tensor-memory columns, in the layout an MMA reads its A
+// operand from tensor memory; ordered with the MMAs issued after it.
+__device__ __forceinline__ void tmem_cp_elect(uint32_t taddr, uint64_t sdesc) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(sdesc)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_elect(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t.reg .b64 st;\n\t"
