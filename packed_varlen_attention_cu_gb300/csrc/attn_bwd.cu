@@ -134,6 +134,12 @@ __device__ __forceinline__ void store_row32(void* base, int64_t row_elem, bool f
     }
 }
 
+// The element-wise warpgroup c (0, 1) turns the 32 fp32 columns [32c, 32c + 32)
+// of a 64-column S / dP buffer into 32 bf16 values packed in its first 16
+// columns, so the warpgroups never overwrite columns the other still reads.
+// The 16-wide K slice k of that bf16 operand therefore starts at column:
+__device__ __forceinline__ uint32_t kslice_col(int k) { return (k >> 1) * 32 + (k & 1) * 8; }
+
 __device__ __forceinline__ void store_zero_row(void* base, int64_t row_elem, bool fp32, int D) {
     if (fp32) {
         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + row_elem);
@@ -152,7 +158,7 @@ __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_
     mbar_init(&sh.done, 1);
     for (int b = 0; b < 2; ++b) {
         mbar_init(&sh.s2_full[b], 1);
-        mbar_init(&sh.p2_full[b], 4);  // one arrival per element-wise warp
+        mbar_init(&sh.p2_full[b], elem_threads / 32);  // one arrival per element-wise warp
     }
     for (int s = 0; s < stages; ++s) {
         mbar_init(&sh.r_full[s], 1);
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t oK = (pend_st * 2 * kHalfBytes) >> 4;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_ts_elect(tQa, tmem + 64 * b + k * 8, dKm + oK + k * 128, C::kIdescNN,
+                mma_ts_elect(tQa, tmem + 64 * b + kslice_col(k), dKm + oK + k * 128, C::kIdescNN,
                              (!first || k > 0) ? 1u : 0u);
             first = false;
             mma_commit_elect(&sh.r_empty[pend_st]);
@@ -411,8 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- dS and the dQ epilogue
-        // Two warpgroups: wg takes the half-items u with u % 2 == wg (tensor-memory
-        // buffer wg); each stores half of the dQ columns.
+        // Two warpgroups share every half-item: wg takes its 32 key columns
+        // [32 wg, 32 wg + 32), so a half-item's dS is ready in half the time;
+        // each stores half of the dQ columns.
         const int wg = (warp - 4) >> 2;
         const int r = (warp & 3) * 32 + lane;  // query row = tensor-memory lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -454,19 +461,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t c_hi = min(128, lim_hi - kt0), c_lo = max(0, lim_lo - kt0);
                         const int32_t halves = min(128, s.k_len - kt0) > 64 ? 2 : 1;
                         for (int32_t hf = 0; hf < halves && live; ++hf, ++gu) {
-                            if ((int)(gu & 1) != wg) continue;
                             const uint32_t b = gu & 1;
-                            // the warp masks only when some row has a limit inside the half
-                            const int h0 = hf * 64;
+                            // this warpgroup's 32 key columns [h0, h0 + 32) of the half; the
+                            // warp masks only when some row has a limit inside them
+                            const int h0 = hf * 64 + wg * 32;
                             const bool need_mask =
-                                __any_sync(0xffffffffu, c_lo > h0 || c_hi < h0 + 64);
+                                __any_sync(0xffffffffu, c_lo > h0 || c_hi < h0 + 32);
                             live = mbar_wait(&sh.s2_full[b], (gu >> 1) & 1, abort_flag, err_word,
                                              kErrTimeoutBase + 27, kWaitNs);
                             if (!live) break;
                             tc_fence_after();
                             const uint32_t tSb = tS + 64 * b, tPb = tS + 128 + 64 * b;
-#pragma unroll
-                            for (int c = 0; c < 2; ++c) {
+                            {
+                                const int c = wg;
                                 uint32_t sv[32], pv[32];
                                 tmem_ld32(tSb + c * 32, sv);
                                 tmem_ld32(tPb + c * 32, pv);
@@ -486,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     const float g1 = p1 * (__uint_as_float(pv[e + 1]) - dd);
                                     dsw[e >> 1] = pack_bf16x2(g0, g1);
                                 }
-                                tmem_st16(tSb + c * 16, dsw);
+                                tmem_st16(tSb + c * 32, dsw);
                             }
                             tmem_st_wait();
                             tc_fence_before();
@@ -574,8 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     BwdHeader* bhw = const_cast<BwdHeader*>(bh);
     if (!dyn && (int32_t)blockIdx.x >= n) return;
     if (tid == 0) init_barriers(sh, kItems, 256);
-    // per element-wise warp: (LSE log2, D) of the 64 queries of its half-item
-    __shared__ __align__(16) float2 s_ld[8][64];
+    // per element-wise warp: (LSE log2, D) of its 32 queries of the half-item
+    __shared__ __align__(16) float2 s_ld[8][32];
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -693,11 +700,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t oO = (pend_st * 2 * kHalfBytes + kHalfBytes) >> 4;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_ts_elect(tVa, tmem + 64 * b + k * 8, dRm + oO + k * 128, C::kIdescNN,
+                mma_ts_elect(tVa, tmem + 64 * b + kslice_col(k), dRm + oO + k * 128, C::kIdescNN,
                              (!first || k > 0) ? 1u : 0u);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_ts_elect(tKa, tmem + 128 + 64 * b + k * 8, dRm + oQ + k * 128, C::kIdescNN,
+                mma_ts_elect(tKa, tmem + 128 + 64 * b + kslice_col(k), dRm + oQ + k * 128,
+                             C::kIdescNN,
                              (!first || k > 0) ? 1u : 0u);
             first = false;
             mma_commit_elect(&sh.r_empty[pend_st]);
@@ -776,8 +784,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- P^T, dS^T and the dK/dV epilogue
-        // Two warpgroups: wg takes the half-items u with u % 2 == wg (tensor-memory
-        // buffer wg); at the end of a unit wg 0 stores dV and wg 1 dK.
+        // Two warpgroups share every half-item: wg takes its 32 query columns
+        // [32 wg, 32 wg + 32), so a half-item's P^T and dS^T are ready in half
+        // the time; at the end of a unit wg 0 stores dV and wg 1 dK.
         const int wg = (warp - 4) >> 2;
         const int kr = (warp & 3) * 32 + lane;  // key row = tensor-memory lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -819,14 +828,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t c_hi = kvalid ? (int32_t)min((int64_t)nq, qb - cpos0) : 0;
                     const uint32_t halves = nq > 64 ? 2 : 1;
                     for (uint32_t hf = 0; hf < halves && live; ++hf, ++gu) {
-                        if ((int)(gu & 1) != wg) continue;
                         const uint32_t b = gu & 1;
-                        // (LSE log2, D) of this half's 64 queries into the warp's slots,
-                        // loaded before the wait for S^T; a query past the tile has
-                        // LSE = +inf, so every P of it is 0
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const int qc = (int)hf * 64 + c * 32 + lane;
+                        // this warpgroup's 32 query columns [h0, h0 + 32) of the half:
+                        // their (LSE log2, D) into the warp's slots, loaded before the
+                        // wait for S^T; a query past the tile has LSE = +inf, so every
+                        // P of it is 0
+                        const int h0 = (int)hf * 64 + wg * 32;
+                        {
+                            const int qc = h0 + lane;
                             float l2 = INFINITY, dd = 0.f;
                             if (qc < nq) {
                                 const int64_t li = (int64_t)head * p.q_tokens + qrow0 + qc;
@@ -834,21 +843,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (l != -INFINITY) l2 = l * 1.4426950408889634f;
                                 dd = p.dvec[li];
                             }
-                            my_ld[c * 32 + lane] = make_float2(l2, dd);
+                            my_ld[lane] = make_float2(l2, dd);
                         }
                         __syncwarp();
                         // columns [c_lo, c_hi) of this key row are allowed; the warp
-                        // masks only when some row of it has a limit inside the half
-                        const int h0 = (int)hf * 64;
+                        // masks only when some row of it has a limit inside its columns
                         const bool need_mask =
-                            __any_sync(0xffffffffu, c_lo > h0 || c_hi < min(h0 + 64, nq));
+                            __any_sync(0xffffffffu, c_lo > h0 || c_hi < min(h0 + 32, nq));
                         live = mbar_wait(&sh.s2_full[b], (gu >> 1) & 1, abort_flag, err_word,
                                          kErrTimeoutBase + 37, kWaitNs);
                         if (!live) break;
                         tc_fence_after();
                         const uint32_t tSb = tS + 64 * b, tPb = tS + 128 + 64 * b;
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
+                        {
+                            const int c = wg;
                             uint32_t sv[32], pv[32];
                             tmem_ld32(tSb + c * 32, sv);
                             tmem_ld32(tPb + c * 32, pv);
@@ -857,11 +865,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint32_t pw[32], dw[32];
 #pragma unroll
                             for (int e = 0; e < 32; e += 2) {
-                                const float4 ld = *reinterpret_cast<const float4*>(&my_ld[c * 32 + e]);
+                                const float4 ld = *reinterpret_cast<const float4*>(&my_ld[e]);
                                 float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - ld.x);
                                 float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - ld.z);
                                 if (need_mask) {
-                                    const int col = h0 + c * 32 + e;
+                                    const int col = h0 + e;
                                     if (col < c_lo || col >= c_hi) p0 = 0.f;
                                     if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
                                 }
@@ -870,8 +878,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pw[e >> 1] = pack_bf16x2(p0, p1);
                                 dw[e >> 1] = pack_bf16x2(g0, g1);
                             }
-                            tmem_st16(tSb + c * 16, pw);
-                            tmem_st16(tPb + c * 16, dw);
+                            tmem_st16(tSb + c * 32, pw);
+                            tmem_st16(tPb + c * 32, dw);
                         }
                         tmem_st_wait();
                         tc_fence_before();
