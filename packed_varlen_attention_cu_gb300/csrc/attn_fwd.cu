@@ -45,7 +45,7 @@ namespace {
 constexpr int kThreads = 384;
 // register split: the producer/MMA warpgroup hands registers to the two
 // softmax warpgroups (128 * kRegsCtrl + 256 * kRegsSoftmax <= 384 * 168)
-constexpr uint32_t kRegsCtrl = 104, kRegsSoftmax = 200;
+constexpr uint32_t kRegsCtrl = 72, kRegsSoftmax = 216;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 constexpr float kRescaleThreshold = 8.0f;     // log2 domain
