@@ -68,11 +68,16 @@ struct BwdParams {
     float scale, scale_log2;
 };
 
+constexpr int kLdSlots = 8;
+
 struct BShared {
     uint64_t a_full, a_empty, o_full, o_empty, done;
     uint64_t s2_full[2], p2_full[2];  // per half-item tensor-memory buffer
     uint64_t r_full[8], r_empty[8];
     UnitRing<8> ur;  // the producer hands each unit's index to the other roles
+    // bwd_dkdv: (LSE log2, D) of each half-item's 64 queries, staged ahead by a
+    // loader warp (ld_full: 32 lane arrivals; ld_empty: one per element-wise warp)
+    uint64_t ld_full[kLdSlots], ld_empty[kLdSlots];
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -150,7 +155,8 @@ __device__ __forceinline__ void store_zero_row(void* base, int64_t row_elem, boo
     }
 }
 
-__device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_threads) {
+__device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_threads,
+                                              int extra_readers) {
     mbar_init(&sh.a_full, 1);
     mbar_init(&sh.a_empty, 1);
     mbar_init(&sh.o_full, 1);
@@ -165,7 +171,11 @@ __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_
         mbar_init(&sh.r_empty[s], 1);
     }
     // unit readers: the MMA warp (one arrival) and every element-wise thread
-    uring_init(sh.ur, 1 + elem_threads);
+    uring_init(sh.ur, 1 + elem_threads + extra_readers);
+    for (int s = 0; s < kLdSlots; ++s) {
+        mbar_init(&sh.ld_full[s], 32);
+        mbar_init(&sh.ld_empty[s], elem_threads / 32);
+    }
     sh.abort_flag = 0;
     fence_barrier_init();
 }
@@ -211,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
     const int32_t ub = dyn ? 0 : cta_off[blockIdx.x], ue = dyn ? 0 : cta_off[blockIdx.x + 1];
     if (!dyn && ub >= ue) return;
-    if (tid == 0) init_barriers(sh, C::kStages, 256);
+    if (tid == 0) init_barriers(sh, C::kStages, 256, 0);
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -580,9 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool dyn = h->dispatch == PVA_DISPATCH_DYNAMIC;
     BwdHeader* bhw = const_cast<BwdHeader*>(bh);
     if (!dyn && (int32_t)blockIdx.x >= n) return;
-    if (tid == 0) init_barriers(sh, kItems, 256);
-    // per element-wise warp: (LSE log2, D) of its 32 queries of the half-item
-    __shared__ __align__(16) float2 s_ld[8][32];
+    // unit readers beyond the MMA and element-wise warps: the loader warp
+    if (tid == 0) init_barriers(sh, kItems, 256, 1);
+    // (LSE log2, D) of the 64 queries of each staged half-item
+    __shared__ __align__(16) float2 s_ld[kLdSlots][64];
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -782,6 +793,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_elect(&sh.done);
         mbar_wait_drain(&sh.done, 0, kDrainNs);
         __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------- (LSE, D) loader
+        // Walks the half-items in the element-wise warps' order and stages the
+        // (LSE log2, D) of their 64 queries up to kLdSlots half-items ahead, so
+        // the global-load latency stays off the element-wise warps' path.  A
+        // query past the tile gets LSE = +inf: every P of it is 0.
+        uint32_t li = 0;
+        bool live = true;
+        for (uint32_t rd = 0; live; ++rd) {
+            int32_t idx;
+            live = uring_get_warp(sh.ur, rd, idx, abort_flag, err_word, kErrTimeoutBase + 41,
+                                  kWaitNs);
+            if (!live || idx < 0) break;
+            const BwdUnit u = bunits[idx];
+            if (u.cost <= 1) continue;
+            for (int32_t hh = 0; hh < G && live; ++hh) {
+                const int32_t head = u.kvh * G + hh;
+                for (int32_t m = 0; m < u.gcount && live; ++m) {
+                    const WlSlice s = slices[gsl[u.gbegin + m]];
+                    int32_t qlo, qhi;
+                    bwd_q_span(s, u.kt, qlo, qhi);
+                    for (int32_t t = qlo; t < qhi && live; ++t) {
+                        const int32_t qrow0 = s.q_row0 + t * 128;
+                        const int32_t nq = min(128, s.q_len - t * 128);
+                        const uint32_t halves = nq > 64 ? 2 : 1;
+                        for (uint32_t hf = 0; hf < halves && live; ++hf, ++li) {
+                            const uint32_t slot = li % kLdSlots;
+                            live = mbar_wait_warp(&sh.ld_empty[slot], ((li / kLdSlots) & 1) ^ 1,
+                                                  abort_flag, err_word, kErrTimeoutBase + 42,
+                                                  kWaitNs);
+                            if (!live) break;
+#pragma unroll
+                            for (int c = 0; c < 2; ++c) {
+                                const int qc = (int)hf * 64 + c * 32 + lane;
+                                float l2 = INFINITY, dd = 0.f;
+                                if (qc < nq) {
+                                    const int64_t li_ = (int64_t)head * p.q_tokens + qrow0 + qc;
+                                    const float l = p.lse[li_];
+                                    if (l != -INFINITY) l2 = l * 1.4426950408889634f;
+                                    dd = p.dvec[li_];
+                                }
+                                s_ld[slot][c * 32 + lane] = make_float2(l2, dd);
+                            }
+                            mbar_arrive(&sh.ld_full[slot]);  // every lane, after its writes
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- P^T, dS^T and the dK/dV epilogue
         // Two warpgroups share every half-item: wg takes its 32 query columns
@@ -792,8 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base, tV = tmem + lane_base + 256,
                        tK = tmem + lane_base + 256 + D;
-        float2* my_ld = s_ld[warp - 4];
-        uint32_t gu = 0, o_cnt = 0;
+        uint32_t gu = 0, o_cnt = 0, li = 0;
         bool live = true;
         for (uint32_t rd = 0; live; ++rd) {
             int32_t idx;
@@ -811,7 +871,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             for (int32_t hh = 0; hh < G && live; ++hh) {
-                const int32_t head = u.kvh * G + hh;
                 for (int32_t m = 0; m < u.gcount && live; ++m) {
                 const WlSlice s = slices[gsl[u.gbegin + m]];
                 const int32_t k_pos = s.k_pos0 + u.kt * 128 + kr;
@@ -821,7 +880,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bwd_q_span(s, u.kt, qlo, qhi);
                 for (int32_t t = qlo; t < qhi && live; ++t) {
                     // this q tile's rows: query c has position q_pos0 + t*128 + c
-                    const int32_t qrow0 = s.q_row0 + t * 128;
                     const int32_t nq = min(128, s.q_len - t * 128);
                     const int32_t cpos0 = s.q_pos0 + t * 128;
                     const int32_t c_lo = (int32_t)max((int64_t)0, qa - cpos0);
@@ -834,18 +892,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // wait for S^T; a query past the tile has LSE = +inf, so every
                         // P of it is 0
                         const int h0 = (int)hf * 64 + wg * 32;
-                        {
-                            const int qc = h0 + lane;
-                            float l2 = INFINITY, dd = 0.f;
-                            if (qc < nq) {
-                                const int64_t li = (int64_t)head * p.q_tokens + qrow0 + qc;
-                                const float l = p.lse[li];
-                                if (l != -INFINITY) l2 = l * 1.4426950408889634f;
-                                dd = p.dvec[li];
-                            }
-                            my_ld[lane] = make_float2(l2, dd);
-                        }
-                        __syncwarp();
+                        const uint32_t slot = li % kLdSlots;
+                        live = mbar_wait(&sh.ld_full[slot], (li / kLdSlots) & 1, abort_flag,
+                                         err_word, kErrTimeoutBase + 43, kWaitNs);
+                        if (!live) break;
+                        const float2* my_ld = s_ld[slot] + wg * 32;
                         // columns [c_lo, c_hi) of this key row are allowed; the warp
                         // masks only when some row of it has a limit inside its columns
                         const bool need_mask =
@@ -883,8 +934,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tmem_st_wait();
                         tc_fence_before();
-                        __syncwarp();  // also: every lane has read my_ld before its next write
-                        if (lane == 0) mbar_arrive(&sh.p2_full[b]);
+                        __syncwarp();  // also: every lane has read its staged (LSE, D)
+                        if (lane == 0) {
+                            mbar_arrive(&sh.p2_full[b]);
+                            mbar_arrive(&sh.ld_empty[slot]);
+                        }
+                        ++li;
                     }
                 }
                 }
