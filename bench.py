@@ -375,7 +375,7 @@ def run_e2e(args, ctx, world):
         api.attn_fwd_host(hq_, hk_, hv_, hcu, w.num_docs, mask, params, o_h, l_h, bufs[i],
                           0.0, streams[i])
 
-    for _ in range(2):
+    for _ in range(4):
         step()
     torch.cuda.synchronize()
     K = max(4, (args.steps // 5) // 2 * 2)
