@@ -53,10 +53,14 @@ static_assert(sizeof(WlUnit) == 64, "WlUnit is 64 bytes");
 // work below it: W(classes < c) < num_ctas * 2^(c + 1) (capped at 38, so that
 // the LPT part's costs fit the sort key).
 __host__ __device__ inline int32_t dispatch_class(int64_t cost) {
-    uint64_t c = cost > 1 ? (uint64_t)cost : 1u;
+    const uint64_t c = cost > 1 ? (uint64_t)cost : 1u;
+#ifdef __CUDA_ARCH__
+    return 63 - __clzll((long long)c);
+#else
     int32_t e = 0;
-    while (c >>= 1) ++e;
+    for (uint64_t x = c; x >>= 1;) ++e;
     return e;
+#endif
 }
 
 struct WlRun {

@@ -347,8 +347,9 @@ __device__ void tile_span_warp(const WlSeg& g, const WlSlice& s, int32_t t, int3
     if (cnt == 0) {
         lo_t = hi_t = 0;
     } else {
-        lo_t = (int32_t)(mn / tile_n);
-        hi_t = (int32_t)((mx + tile_n - 1) / tile_n);
+        // slice-local key indices: 0 <= mn < mx <= k_len < 2^31
+        lo_t = (int32_t)mn / tile_n;
+        hi_t = (int32_t)(((uint32_t)mx + (uint32_t)tile_n - 1u) / (uint32_t)tile_n);
     }
     pairs = cnt;
 }
