@@ -58,6 +58,9 @@ template <int D>
 struct Cfg {
     static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
     static constexpr int kStages = D == 128 ? 4 : 8;
+    // d = 64 leaves 64 free tensor-memory columns per sub-tile: P goes there
+    // instead of over S, so QK of the next kv tile need not wait for PV
+    static constexpr bool kSplitP = D == 64;
     static constexpr int kSmem = 2 * kTileBytes + kStages * kTileBytes + 1024;
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
@@ -108,6 +111,8 @@ __device__ __forceinline__ Unit decode_unit(const WlUnit& u, const WlSeg* segs) 
 struct Shared {
     uint64_t q_full[2], q_empty[2], s_full[2], p_half[2], p_full[2], o_full[2], o_empty[2], done[2],
         turn[2];
+    // C::kSplitP only: S read by the softmax (4 warp arrivals), PV complete (commit)
+    uint64_t s_free[2], pv_done[2];
     uint64_t kv_full[8], kv_empty[8];
     UnitRing<kURing> ur;  // the producer hands each unit's index to the other roles
     uint32_t tmem_base;
@@ -193,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.o_empty[i], 128);
             mbar_init(&sh.done[i], 1);
             mbar_init(&sh.turn[i], 1);
+            mbar_init(&sh.s_free[i], 4);
+            mbar_init(&sh.pv_done[i], 1);
         }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&sh.kv_full[s], 1);
@@ -272,29 +279,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     u.st[i].q_row);
                     ++q_it[i];
                 }
+                // one K or V tile into the next ring stage
+                auto load_item = [&](int kv, int32_t krow) {
+                    if (hook && kv_it == 1) {
+                        ++kv_it;  // test hook: this copy never arrives
+                        return;
+                    }
+                    const uint32_t st = kv_it % C::kStages;
+                    live = mbar_wait(&sh.kv_empty[st], ((kv_it / C::kStages) & 1) ^ 1,
+                                     abort_flag, err_word, kErrTimeoutBase + 2, kWaitNs);
+                    if (!live) return;
+                    mbar_arrive_expect_tx(&sh.kv_full[st], C::kTileBytes);
+                    uint8_t* dst = sKV + st * C::kTileBytes;
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(dst + b * 16384, kv == 0 ? &tmk : &tmv, &sh.kv_full[st],
+                                    b * 64, u.kvh, krow);
+                    ++kv_it;
+                };
+                // the MMA warps' order: K_j, V_j per tile; with P apart from S
+                // (C::kSplitP), K_0, then K_{j+1} before V_j
+                int32_t pend_v = -1;
                 for (int32_t r = 0; r < u.run_count && live; ++r) {
                     const WlRun run = runs[u.run_begin + r];
                     const WlSlice s = slices[run.slice];
                     for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
                         const int32_t krow = s.k_row0 + jt * 128;
-                        for (int kv = 0; kv < 2 && live; ++kv) {
-                            if (hook && kv_it == 1) {
-                                ++kv_it;  // test hook: this copy never arrives
-                                continue;
-                            }
-                            const uint32_t st = kv_it % C::kStages;
-                            live = mbar_wait(&sh.kv_empty[st], ((kv_it / C::kStages) & 1) ^ 1,
-                                             abort_flag, err_word, kErrTimeoutBase + 2, kWaitNs);
-                            if (!live) break;
-                            mbar_arrive_expect_tx(&sh.kv_full[st], C::kTileBytes);
-                            uint8_t* dst = sKV + st * C::kTileBytes;
-                            for (int b = 0; b < D / 64; ++b)
-                                tma_load_3d(dst + b * 16384, kv == 0 ? &tmk : &tmv,
-                                            &sh.kv_full[st], b * 64, u.kvh, krow);
-                            ++kv_it;
+                        load_item(0, krow);
+                        if (!live) break;
+                        if (C::kSplitP) {
+                            if (pend_v >= 0) load_item(1, pend_v);
+                            pend_v = krow;
+                        } else {
+                            load_item(1, krow);
                         }
                     }
                 }
+                if (C::kSplitP && live && pend_v >= 0) load_item(1, pend_v);
             }
             if (!live) {
                 // drain: wait for the copies this thread issued last
@@ -350,6 +370,111 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (mine) mma_commit_elect(&sh.kv_empty[st]);
                 else mbar_arrive_elect(&sh.kv_empty[st]);
             };
+            if constexpr (C::kSplitP) {
+            // P in its own columns (tP): QK of kv tile j+1 is issued as soon as the
+            // softmax has read S_j (s_free), before PV of tile j; the two issuers
+            // run independently.  Items arrive as K_0, then K_{j+1}, V_j per tile.
+            const uint32_t tP = tO + 64;
+            uint32_t s_used = 0;  // QKs issued into S_i
+            auto issue_qk = [&](uint32_t st) {
+                // S_i is free once the softmax has read the previous S
+                if (s_used > 0)
+                    live = mbar_wait_warp(&sh.s_free[i], (s_used - 1) & 1, abort_flag, err_word,
+                                          kErrTimeoutBase + 15, kWaitNs);
+                if (!live) return;
+                tc_fence_after();
+                const uint64_t dK = dK0 + ((st * C::kTileBytes) >> 4);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
+                    mma_ss_elect(tS, dQ + off16, dK + off16, C::kIdescQK, k > 0);
+                }
+                mma_commit_elect(&sh.s_full[i]);
+                ++s_used;
+            };
+            for (uint32_t nu = 0; live; ++nu) {
+                int32_t idx;
+                live = uring_get_warp(sh.ur, nu, idx, abort_flag, err_word, kErrTimeoutBase + 14,
+                                      kWaitNs);
+                if (!live || idx < 0) break;
+                const WlUnit wu = ubase[idx];
+                const Unit u = decode_unit(wu, segs);
+                const int32_t n = u.ntiles;
+                if (n == 0) continue;
+                const bool mine = i < u.nsub;
+                if (mine) {
+                    live = mbar_wait_warp(&sh.q_full[i], q_it & 1, abort_flag, err_word,
+                                          kErrTimeoutBase + 3, kWaitNs);
+                    if (!live) break;
+                }
+                {  // K_0
+                    const uint32_t st = kv_it % C::kStages;
+                    live = mbar_wait_warp(&sh.kv_full[st], (kv_it / C::kStages) & 1, abort_flag,
+                                          err_word, kErrTimeoutBase + 4, kWaitNs);
+                    if (!live) break;
+                    if (mine) {
+                        issue_qk(st);
+                        if (!live) break;
+                        if (n == 1) mma_commit_elect(&sh.q_empty[i]);
+                    }
+                    release(mine, st);
+                    ++kv_it;
+                }
+                for (int32_t j = 0; j < n && live; ++j) {
+                    if (j + 1 < n) {  // K_{j+1}
+                        const uint32_t st = kv_it % C::kStages;
+                        live = mbar_wait_warp(&sh.kv_full[st], (kv_it / C::kStages) & 1,
+                                              abort_flag, err_word, kErrTimeoutBase + 8, kWaitNs);
+                        if (!live) break;
+                        if (mine) {
+                            issue_qk(st);
+                            if (!live) break;
+                            if (j + 2 == n) mma_commit_elect(&sh.q_empty[i]);
+                        }
+                        release(mine, st);
+                        ++kv_it;
+                    }
+                    // V_j: O_i += P_j V_j, P in two halves of 64 key columns
+                    const uint32_t stv = kv_it % C::kStages;
+                    live = mbar_wait_warp(&sh.kv_full[stv], (kv_it / C::kStages) & 1, abort_flag,
+                                          err_word, kErrTimeoutBase + 5, kWaitNs);
+                    if (!live) break;
+                    if (mine) {
+                        if (j == 0) {
+                            live = mbar_wait_warp(&sh.o_empty[i], (o_cnt & 1) ^ 1, abort_flag,
+                                                  err_word, kErrTimeoutBase + 7, kWaitNs);
+                            if (!live) break;
+                        }
+                        const uint64_t dV = dV0 + ((stv * C::kTileBytes) >> 4);
+                        live = mbar_wait_warp(&sh.p_half[i], p_cnt & 1, abort_flag, err_word,
+                                              kErrTimeoutBase + 6, kWaitNs);
+                        if (!live) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_ts_elect(tO, tP + k * 8, dV + k * 128, C::kIdescPV,
+                                         (j > 0 || k > 0) ? 1u : 0u);
+                        live = mbar_wait_warp(&sh.p_full[i], p_cnt & 1, abort_flag, err_word,
+                                              kErrTimeoutBase + 12, kWaitNs);
+                        if (!live) break;
+                        ++p_cnt;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 4; k < 8; ++k)
+                            mma_ts_elect(tO, tP + k * 8, dV + k * 128, C::kIdescPV, 1u);
+                        mma_commit_elect(&sh.pv_done[i]);
+                    }
+                    release(mine, stv);
+                    ++kv_it;
+                }
+                if (!live) break;
+                if (mine) {
+                    mma_commit_elect(&sh.o_full[i]);
+                    ++o_cnt;
+                    ++q_it;
+                }
+            }
+            } else {
             for (uint32_t nu = 0; live; ++nu) {
                 int32_t idx;
                 live = uring_get_warp(sh.ur, nu, idx, abort_flag, err_word, kErrTimeoutBase + 14,
@@ -453,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++q_it;
                 }
             }
+            }
             // drain every MMA this thread issued before tensor memory is freed
             mma_commit_elect(&sh.done[i]);
             mbar_wait_drain(&sh.done[i], 0, kDrainNs);
@@ -513,6 +639,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+                    if (C::kSplitP) {
+                        // S_i has been read: QK of the next kv tile may overwrite it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sh.s_free[i]);
+                    }
                     if (need_mask) {
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
@@ -542,6 +674,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Lazy rescaling: the reference maximum moves only when this tile's
                     // maximum exceeds it by more than the threshold (or it is still -inf,
                     // when O and l are zero and need no rescale).
+                    if (C::kSplitP && s_cnt >= 2) {
+                        // O and the P columns: PV of the previous tile must be complete
+                        live = mbar_wait(&sh.pv_done[i], (s_cnt - 2) & 1, abort_flag, err_word,
+                                         kErrTimeoutBase + 16, kWaitNs);
+                        if (!live) break;
+                        tc_fence_after();
+                    }
                     float alpha = 1.f;
                     bool rescale = false;
                     if (m_tile > m_used + kRescaleThreshold) {
@@ -551,7 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     l_sum *= alpha;
                     // rare: the running max moved, rescale this row of O first (PV of
-                    // the previous tile has completed: it ran before QK of this one)
+                    // the previous tile has completed: it ran before QK of this one, or
+                    // with P apart from S, pv_done said so)
                     if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
                         for (int c = 0; c < D / 32; ++c) {
@@ -593,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&sh.p_half[i]);
                         }
-                        tmem_st16(tS + c * 16, sr[c]);
+                        tmem_st16((C::kSplitP ? tO + 64 : tS) + c * 16, sr[c]);
                         if (c == 3) {
                             tmem_st_wait();
                             tc_fence_before();

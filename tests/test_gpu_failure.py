@@ -13,10 +13,12 @@ from packed_varlen_attention_cu_gb300 import api, workloads as W
 pytestmark = pytest.mark.gpu
 
 TIMEOUT_BASE = 200      # device error code = 200 + wait site
-# The MMA warps wait for V_0 (site 5) from the start; the softmax warps' next
-# wait (site 9 or 10) starts microseconds later.  With up to 200 us between
-# polls either may be the first to record its expiry.
-SITES = {5, 9, 10}
+# The MMA warps wait for the withheld item from the start: V_0 (site 5) at
+# d = 128; at d = 64, where K_1 is loaded before V_0, K_1 (site 8) or, for a
+# single-tile unit, V_0.  The softmax warps' next wait (site 9 or 10) starts
+# microseconds later; with up to 200 us between polls either may be the first
+# to record its expiry.
+SITES = {5, 8, 9, 10}
 
 
 def _run(w, q, k, v, cu, dispatch):
