@@ -63,8 +63,16 @@ def test_shared_question(oracle_mod, num_prefix):
                 num_prefix=num_prefix, seed=num_prefix)
 
 
-def test_single_long_document_many_tiles(oracle_mod):
-    _full_check(oracle_mod, [3000], 2, 1, 128, seed=9, scale_v=0.5)
+@pytest.mark.parametrize("d", [64, 128])
+def test_single_long_document_many_tiles(oracle_mod, d):
+    _full_check(oracle_mod, [3000], 2, 1, d, seed=9, scale_v=0.5)
+
+
+def test_d64_odd_group_and_single_tile_units(oracle_mod):
+    """d = 64 with an odd GQA group (its last head pairs consecutive q tiles, so
+    some units have one sub-tile) and documents of one tile or less: the split-P
+    pipeline's K_{j+1}-before-V_j order with one-tile units and idle issuers."""
+    _full_check(oracle_mod, [100, 128, 129, 40, 700, 1, 255, 900], 7, 1, 64, seed=13)
 
 
 @pytest.mark.parametrize("dispatch", [api.DISPATCH_DYNAMIC, api.DISPATCH_STATIC])
@@ -106,12 +114,14 @@ def test_dynamic_and_static_dispatch_agree_bitwise(d):
     assert torch.equal(res[api.DISPATCH_STATIC][1], res[api.DISPATCH_DYNAMIC][1])
 
 
-def test_large_logits_rescale_path(oracle_mod):
-    # scaled inputs push the running max up across kv tiles (exercises O rescaling)
+@pytest.mark.parametrize("d", [64, 128])
+def test_large_logits_rescale_path(oracle_mod, d):
+    # scaled inputs push the running max up across kv tiles (exercises O rescaling;
+    # at d = 64 after the wait for the previous tile's PV, P being apart from S)
     lengths = [1500, 700]
     cu = W.cu_seqlens_of(lengths)
     T = int(cu[-1])
-    q, k, v = W.make_qkv(T, T, 2, 2, 128, 21)
+    q, k, v = W.make_qkv(T, T, 2, 2, d, 21)
     ramp = torch.linspace(0.2, 3.0, T).to(torch.bfloat16)[:, None, None]
     k = (k.float() * ramp.float()).to(torch.bfloat16)
     q = (q.float() * 2.0).to(torch.bfloat16)
