@@ -49,8 +49,12 @@ template <int D>
 struct BCfg {
     static constexpr int kTileBytes = 128 * D * 2;
     // bwd_dq: Q, dO, then a K/V ring; bwd_dkdv: K, V, then a (Q, dO) ring
-    static constexpr int kStages = D == 128 ? 4 : 8;
-    static constexpr int kSmem = 2 * kTileBytes + kStages * kTileBytes + 1024;
+    // ring stages: as many as fit beside the two resident tiles within 227 KB of
+    // shared memory per block (bwd_dkdv also holds 2.3 KB of static staging)
+    static constexpr int kStagesDq = D == 128 ? 5 : 12;
+    static constexpr int kStagesKv = D == 128 ? 4 : 11;
+    static constexpr int kSmemDq = 2 * kTileBytes + kStagesDq * kTileBytes + 1024;
+    static constexpr int kSmemKv = 2 * kTileBytes + kStagesKv * kTileBytes + 1024;
     static constexpr uint32_t kIdescNN = idesc_bf16_f32(128, D, true);     // B MN-major
 };
 
@@ -69,11 +73,12 @@ struct BwdParams {
 };
 
 constexpr int kLdSlots = 8;
+constexpr int kMaxStages = 12;
 
 struct BShared {
     uint64_t a_full, a_empty, o_full, o_empty, done;
     uint64_t s2_full[2], p2_full[2];  // per half-item tensor-memory buffer
-    uint64_t r_full[8], r_empty[8];
+    uint64_t r_full[kMaxStages], r_empty[kMaxStages];
     UnitRing<8> ur;  // the producer hands each unit's index to the other roles
     // bwd_dkdv: (LSE log2, D) of each half-item's 64 queries, staged ahead by a
     // loader warp (ld_full: 32 lane arrivals; ld_empty: one per element-wise warp)
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
     const int32_t ub = dyn ? 0 : cta_off[blockIdx.x], ue = dyn ? 0 : cta_off[blockIdx.x + 1];
     if (!dyn && ub >= ue) return;
-    if (tid == 0) init_barriers(sh, C::kStages, 256, 0);
+    if (tid == 0) init_barriers(sh, C::kStagesDq, 256, 0);
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -289,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int32_t halves = min(128, s.k_len - jt * 128) > 64 ? 2 : 1;
                             for (int32_t hf = 0; hf < halves && live; ++hf) {
                                 const int32_t krow = s.k_row0 + jt * 128 + hf * 64;
-                                const uint32_t st = it % C::kStages;
-                                live = mbar_wait(&sh.r_empty[st], ((it / C::kStages) & 1) ^ 1,
+                                const uint32_t st = it % C::kStagesDq;
+                                live = mbar_wait(&sh.r_empty[st], ((it / C::kStagesDq) & 1) ^ 1,
                                                  abort_flag, err_word, kErrTimeoutBase + 22,
                                                  kWaitNs);
                                 if (!live) break;
@@ -309,10 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!live) {
-                const uint32_t n = it < (uint32_t)C::kStages ? it : (uint32_t)C::kStages;
+                const uint32_t n = it < (uint32_t)C::kStagesDq ? it : (uint32_t)C::kStagesDq;
                 for (uint32_t k = 0; k < n; ++k) {
                     const uint32_t x = it - 1 - k;
-                    mbar_wait_drain(&sh.r_full[x % C::kStages], (x / C::kStages) & 1, kDrainNs);
+                    mbar_wait_drain(&sh.r_full[x % C::kStagesDq], (x / C::kStagesDq) & 1, kDrainNs);
                 }
                 if (a_it > 0) mbar_wait_drain(&sh.a_full, (a_it - 1) & 1, kDrainNs);
             }
@@ -380,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
                         const int32_t halves = min(128, s.k_len - jt * 128) > 64 ? 2 : 1;
                         for (int32_t hf = 0; hf < halves && live; ++hf) {
-                            const uint32_t st = it % C::kStages;
-                            live = mbar_wait_warp(&sh.r_full[st], (it / C::kStages) & 1,
+                            const uint32_t st = it % C::kStagesDq;
+                            live = mbar_wait_warp(&sh.r_full[st], (it / C::kStagesDq) & 1,
                                                   abort_flag, err_word, kErrTimeoutBase + 25,
                                                   kWaitNs);
                             if (!live) break;
@@ -560,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // queries [64 hf, 64 hf + 64) of a q tile as (Q, dO) halves of 8 KB per
     // 64-column atom (a stage: Q half at +0, dO half at +D/64 * 8 KB)
     using C = BCfg<D>;
-    constexpr int kItems = C::kStages;          // half-items in the ring
+    constexpr int kItems = C::kStagesKv;        // half-items in the ring
     constexpr int kHalfBytes = 64 * D * 2;      // one 64-row bf16 half tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -991,13 +996,13 @@ pva_status launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
     if (kSplitRegs &&
         (int64_t)fa.numRegs * kThreads < 128 * (int64_t)kRegsCtrl + 256 * (int64_t)kRegsElem)
         return PVA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem) !=
+    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmemDq) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmem) !=
+        cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, BCfg<D>::kSmemKv) !=
             cudaSuccess)
         return PVA_ERR_CUDA;
-    kq<<<bp.num_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq, mk64, mv64, mdo, bp);
-    kk<<<dkdv_ctas, kThreads, BCfg<D>::kSmem, st>>>(mq64, mk, mv, mdo64, bp);
+    kq<<<bp.num_ctas, kThreads, BCfg<D>::kSmemDq, st>>>(mq, mk64, mv64, mdo, bp);
+    kk<<<dkdv_ctas, kThreads, BCfg<D>::kSmemKv, st>>>(mq64, mk, mv, mdo64, bp);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
 
