@@ -9,13 +9,17 @@
 //   bwd_pre   D per (row, head), HBM-bound;
 //   bwd_dq    q-major over the forward worklist's units, dispatched as the
 //             worklist says (static per-CTA LPT lists, or claimed at run time):
-//             per query sub-tile, every kv tile of its runs: S and dP (two SS
-//             MMAs), then dS in the softmax warps, then dQ += dS K (TS MMA);
+//             per query sub-tile (Q and dO copied into tensor memory), every
+//             kv tile of its runs as two 64-key halves: S and dP (TS MMAs),
+//             then dS in the element-wise warps, then dQ += dS K (TS MMA);
 //   bwd_dkdv  kv-major over the backward plan: per 128-key tile of one key
 //             group (the slices sharing a key range) and one kv head, every q
 //             tile of every slice of the group and every head: S^T = K Q^T and
 //             dP^T = V dO^T, then P^T and dS^T, then dV += P^T dO and
-//             dK += dS^T Q, accumulated in tensor memory over the group.
+//             dK += dS^T Q, accumulated in tensor memory over the group; a
+//             loader warp stages each 64-query half's LSE and D ahead.
+// In both passes two element-wise warpgroups share every half-item (32
+// columns each) so that its P / dS are ready as early as possible.
 // Tensor-memory columns: bwd_dq S [0,128) dP [128,256) dQ [256,256+d), then Q and
 // dO as bf16 MMA A operands (d/2 columns each);
 // bwd_dkdv S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d,256+2d).

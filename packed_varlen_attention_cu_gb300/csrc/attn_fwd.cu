@@ -6,19 +6,26 @@
 // with a non-zero mask are computed; partial results over key blocks are
 // combined by online-softmax rescale-and-sum), §1.2 (structured masks).
 //
-// One CTA per SM walks its list of work units (built by pva_build_worklist,
-// LPT-balanced).  A unit holds up to two 128-row query sub-tiles that share
-// one kv head and the same kv tiles.  Warp roles (384 threads, 3 warpgroups):
-//   warp 0      TMA producer: Q sub-tiles, then K_j / V_j tiles into a ring
-//   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T (SS), O_i += P_i V_j
-//               (TS: P read from tensor memory), completion via tcgen05.commit
+// One CTA per SM runs work units until none is left: under dynamic dispatch
+// it claims the next unit of the worklist's dispatch order from a counter
+// (LPT rule, "数据并行负载均衡" §4.4, decided by measured time), under static
+// dispatch it walks its LPT-assigned list.  A unit holds up to two 128-row
+// query sub-tiles that share one kv head and the same kv tiles.  Warp roles
+// (384 threads, 3 warpgroups):
+//   warp 0      TMA producer: picks the units (unit_feed.cuh ring), loads the
+//               Q sub-tiles, then the K / V tiles into a ring
+//   warps 1, 2  MMA issuers, one per sub-tile (one elected lane issues):
+//               S_i = Q_i K_j^T (SS), O_i += P_i V_j (TS: P read from tensor
+//               memory), completion via tcgen05.commit
 //   warps 4-7   softmax + epilogue of sub-tile 0 (one query row per thread)
 //   warps 8-11  softmax + epilogue of sub-tile 1
 // A warp reaches tensor-memory lanes 32*(warp % 4).
-// Tensor memory (512 columns): S0/P0 [0,128), S1/P1 [128,256), O0 [256,..),
-// O1 [384,..).  P (bf16) overwrites the first half of S in place.  With the
-// 32x32b tensor-memory layout a thread owns a whole row, so the row max and
-// row sum of the online softmax are thread-local (no shuffles needed).
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,..),
+// O1 [384,..).  At d = 128 P (bf16) overwrites the first half of S in place,
+// so QK of tile j+1 follows PV of tile j; at d = 64 P has its own 64 columns
+// after O (Cfg::kSplitP) and QK of tile j+1 runs as soon as the softmax has
+// read S_j.  With the 32x32b tensor-memory layout a thread owns a whole row,
+// so the row max and row sum of the online softmax are thread-local.
 // The running max is only moved (and O rescaled in tensor memory) when it
 // grows by more than 2^8 in the base-2 exponent domain; until then P stays
 // below 2^8, which fp32 and bf16 hold exactly enough.
