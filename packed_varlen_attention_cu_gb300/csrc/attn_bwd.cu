@@ -271,6 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (dyn) {
                     const int32_t rank = dispatch_claim(&hw->dispatch_next);
                     idx = rank < nunits ? dorder[rank] : -1;
+                    if (idx >= nunits || idx < -1) {  // a damaged order: stop, report
+                        atomicCAS(err_word, 0, kErrBadWorklist);
+                        idx = -1;
+                    }
                 } else {
                     idx = ub + (int32_t)nu < ue ? ub + (int32_t)nu : -1;
                 }
@@ -638,7 +642,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        kWaitNs);
                 if (!live) break;
                 int32_t pos = dyn ? dispatch_claim(&bhw->dispatch_next) : pos_of((int32_t)rd);
-                const int32_t idx = pos < n ? order[pos] : -1;
+                int32_t idx = pos < n ? order[pos] : -1;
+                if (idx >= n || idx < -1) {  // a damaged order: stop, report
+                    atomicCAS(err_word, 0, kErrBadWorklist);
+                    idx = -1;
+                }
                 uring_put(sh.ur, rd, idx);
                 if (idx < 0) break;
                 const BwdUnit u = bunits[idx];

@@ -265,6 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // its previous unit, a few K/V steps before the CTA needs it
                     const int32_t rank = dispatch_claim(&hw->dispatch_next);
                     idx = rank < nunits ? order[rank] : -1;
+                    if (idx >= nunits || idx < -1) {  // a damaged order: stop, report
+                        atomicCAS(err_word, 0, kErrBadWorklist);
+                        idx = -1;
+                    }
                     if (rank == 0 && p.withhold_kv) hook = true;
                 } else {
                     idx = ub + (int32_t)nu < ue ? ub + (int32_t)nu : -1;

@@ -569,7 +569,15 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
                     sk[hi] = x;
                 }
             }
-            __syncthreads();
+            // a stage of stride <= 32 only touches its warp's own 64 keys (thread t
+            // pairs keys in [64 (t / 32), 64 (t / 32) + 64)): between two such
+            // stages a warp barrier suffices; a block barrier is needed when this
+            // stage or the next one reaches across warps, and after the last
+            const int32_t next = stride > 1 ? stride >> 1 : size;
+            static_assert(kSortChunk / 2 == kSortThreads, "one pair per thread and stage");
+            const bool last = stride == 1 && size == kSortChunk;
+            if (stride > 32 || next > 32 || last) __syncthreads();
+            else __syncwarp();
         }
     }
     for (int32_t i = threadIdx.x; i < m; i += kSortThreads) keys[c0 + i] = sk[i];
