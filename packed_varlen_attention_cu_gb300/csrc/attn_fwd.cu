@@ -68,6 +68,10 @@ struct Cfg {
     // d = 64 leaves 64 free tensor-memory columns per sub-tile: P goes there
     // instead of over S, so QK of the next kv tile need not wait for PV
     static constexpr bool kSplitP = D == 64;
+    // K/V ring: one tile per stage; with kSplitP a stage holds K_{j+1} (at +0) and
+    // V_j (at +kTileBytes), waited for and released once per kv tile
+    static constexpr int kRingStages = kSplitP ? kStages / 2 : kStages;
+    static constexpr int kStageBytes = kSplitP ? 2 * kTileBytes : kTileBytes;
     static constexpr int kSmem = 2 * kTileBytes + kStages * kTileBytes + 1024;
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
@@ -290,49 +294,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     u.st[i].q_row);
                     ++q_it[i];
                 }
-                // one K or V tile into the next ring stage
-                auto load_item = [&](int kv, int32_t krow) {
+                // the next ring stage: the K tile of key row krow_k and/or the V tile of
+                // krow_v (-1: none)
+                auto load_stage = [&](int32_t krow_k, int32_t krow_v) {
                     if (hook && kv_it == 1) {
                         ++kv_it;  // test hook: this copy never arrives
                         return;
                     }
-                    const uint32_t st = kv_it % C::kStages;
-                    live = mbar_wait(&sh.kv_empty[st], ((kv_it / C::kStages) & 1) ^ 1,
+                    const uint32_t st = kv_it % C::kRingStages;
+                    live = mbar_wait(&sh.kv_empty[st], ((kv_it / C::kRingStages) & 1) ^ 1,
                                      abort_flag, err_word, kErrTimeoutBase + 2, kWaitNs);
                     if (!live) return;
-                    mbar_arrive_expect_tx(&sh.kv_full[st], C::kTileBytes);
-                    uint8_t* dst = sKV + st * C::kTileBytes;
-                    for (int b = 0; b < D / 64; ++b)
-                        tma_load_3d(dst + b * 16384, kv == 0 ? &tmk : &tmv, &sh.kv_full[st],
-                                    b * 64, u.kvh, krow);
+                    const uint32_t bytes =
+                        (uint32_t)((krow_k >= 0 ? 1 : 0) + (krow_v >= 0 ? 1 : 0)) * C::kTileBytes;
+                    mbar_arrive_expect_tx(&sh.kv_full[st], bytes);
+                    uint8_t* dst = sKV + st * C::kStageBytes;
+                    if (krow_k >= 0)
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_load_3d(dst + b * 16384, &tmk, &sh.kv_full[st], b * 64, u.kvh,
+                                        krow_k);
+                    if (krow_v >= 0)
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_load_3d(dst + (C::kSplitP ? C::kTileBytes : 0) + b * 16384, &tmv,
+                                        &sh.kv_full[st], b * 64, u.kvh, krow_v);
                     ++kv_it;
                 };
-                // the MMA warps' order: K_j, V_j per tile; with P apart from S
-                // (C::kSplitP), K_0, then K_{j+1} before V_j
+                // the MMA warps' order: K_j, V_j per tile; with kSplitP the stages
+                // (K_0), (K_1, V_0), (K_2, V_1), ..., (V_{n-1})
                 int32_t pend_v = -1;
                 for (int32_t r = 0; r < u.run_count && live; ++r) {
                     const WlRun run = runs[u.run_begin + r];
                     const WlSlice s = slices[run.slice];
                     for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
                         const int32_t krow = s.k_row0 + jt * 128;
-                        load_item(0, krow);
-                        if (!live) break;
                         if (C::kSplitP) {
-                            if (pend_v >= 0) load_item(1, pend_v);
+                            load_stage(krow, pend_v);
                             pend_v = krow;
                         } else {
-                            load_item(1, krow);
+                            load_stage(krow, -1);
+                            if (!live) break;
+                            load_stage(-1, krow);
                         }
                     }
                 }
-                if (C::kSplitP && live && pend_v >= 0) load_item(1, pend_v);
+                if (C::kSplitP && live && pend_v >= 0) load_stage(-1, pend_v);
             }
             if (!live) {
                 // drain: wait for the copies this thread issued last
-                const uint32_t n = kv_it < (uint32_t)C::kStages ? kv_it : (uint32_t)C::kStages;
+                const uint32_t n =
+                    kv_it < (uint32_t)C::kRingStages ? kv_it : (uint32_t)C::kRingStages;
                 for (uint32_t k = 0; k < n; ++k) {
                     const uint32_t it = kv_it - 1 - k;
-                    mbar_wait_drain(&sh.kv_full[it % C::kStages], (it / C::kStages) & 1, kDrainNs);
+                    mbar_wait_drain(&sh.kv_full[it % C::kRingStages], (it / C::kRingStages) & 1,
+                                    kDrainNs);
                 }
 #pragma unroll
                 for (int i = 0; i < 2; ++i)
@@ -384,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (C::kSplitP) {
             // P in its own columns (tP): QK of kv tile j+1 is issued as soon as the
             // softmax has read S_j (s_free), before PV of tile j; the two issuers
-            // run independently.  Items arrive as K_0, then K_{j+1}, V_j per tile.
+            // run independently.  Ring stages: (K_0), then (K_{j+1}, V_j) per tile.
             const uint32_t tP = tO + 64;
             uint32_t s_used = 0;  // QKs issued into S_i
             auto issue_qk = [&](uint32_t st) {
@@ -394,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           kErrTimeoutBase + 15, kWaitNs);
                 if (!live) return;
                 tc_fence_after();
-                const uint64_t dK = dK0 + ((st * C::kTileBytes) >> 4);
+                const uint64_t dK = dK0 + ((st * C::kStageBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
@@ -418,10 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           kErrTimeoutBase + 3, kWaitNs);
                     if (!live) break;
                 }
-                {  // K_0
-                    const uint32_t st = kv_it % C::kStages;
-                    live = mbar_wait_warp(&sh.kv_full[st], (kv_it / C::kStages) & 1, abort_flag,
-                                          err_word, kErrTimeoutBase + 4, kWaitNs);
+                {  // stage (K_0)
+                    const uint32_t st = kv_it % C::kRingStages;
+                    live = mbar_wait_warp(&sh.kv_full[st], (kv_it / C::kRingStages) & 1,
+                                          abort_flag, err_word, kErrTimeoutBase + 4, kWaitNs);
                     if (!live) break;
                     if (mine) {
                         issue_qk(st);
@@ -432,31 +446,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++kv_it;
                 }
                 for (int32_t j = 0; j < n && live; ++j) {
-                    if (j + 1 < n) {  // K_{j+1}
-                        const uint32_t st = kv_it % C::kStages;
-                        live = mbar_wait_warp(&sh.kv_full[st], (kv_it / C::kStages) & 1,
-                                              abort_flag, err_word, kErrTimeoutBase + 8, kWaitNs);
-                        if (!live) break;
-                        if (mine) {
+                    // stage (K_{j+1}, V_j): S_i of tile j+1, then O_i += P_j V_j with P
+                    // in two halves of 64 key columns; the stage is released once
+                    const uint32_t st = kv_it % C::kRingStages;
+                    live = mbar_wait_warp(&sh.kv_full[st], (kv_it / C::kRingStages) & 1,
+                                          abort_flag, err_word, kErrTimeoutBase + 5, kWaitNs);
+                    if (!live) break;
+                    if (mine) {
+                        if (j + 1 < n) {
                             issue_qk(st);
                             if (!live) break;
                             if (j + 2 == n) mma_commit_elect(&sh.q_empty[i]);
                         }
-                        release(mine, st);
-                        ++kv_it;
-                    }
-                    // V_j: O_i += P_j V_j, P in two halves of 64 key columns
-                    const uint32_t stv = kv_it % C::kStages;
-                    live = mbar_wait_warp(&sh.kv_full[stv], (kv_it / C::kStages) & 1, abort_flag,
-                                          err_word, kErrTimeoutBase + 5, kWaitNs);
-                    if (!live) break;
-                    if (mine) {
                         if (j == 0) {
                             live = mbar_wait_warp(&sh.o_empty[i], (o_cnt & 1) ^ 1, abort_flag,
                                                   err_word, kErrTimeoutBase + 7, kWaitNs);
                             if (!live) break;
                         }
-                        const uint64_t dV = dV0 + ((stv * C::kTileBytes) >> 4);
+                        const uint64_t dV = dV0 + ((st * C::kStageBytes + C::kTileBytes) >> 4);
                         live = mbar_wait_warp(&sh.p_half[i], p_cnt & 1, abort_flag, err_word,
                                               kErrTimeoutBase + 6, kWaitNs);
                         if (!live) break;
@@ -475,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_ts_elect(tO, tP + k * 8, dV + k * 128, C::kIdescPV, 1u);
                         mma_commit_elect(&sh.pv_done[i]);
                     }
-                    release(mine, stv);
+                    release(mine, st);
                     ++kv_it;
                 }
                 if (!live) break;
