@@ -68,6 +68,15 @@ def test_single_long_document_many_tiles(oracle_mod, d):
     _full_check(oracle_mod, [3000], 2, 1, d, seed=9, scale_v=0.5)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dispatch", [api.DISPATCH_DYNAMIC, api.DISPATCH_STATIC])
+def test_zero_length_and_single_token_documents(oracle_mod, d, dispatch):
+    """Degenerate packs: empty documents between others, one-token documents,
+    and far fewer units than CTAs (most CTAs claim nothing but the end)."""
+    _full_check(oracle_mod, [0, 1, 0, 5, 0, 0, 130, 1, 0], 4, 2, d, seed=17, dispatch=dispatch)
+    _full_check(oracle_mod, [1] * 37, 2, 1, d, seed=18, dispatch=dispatch)
+
+
 def test_d64_odd_group_and_single_tile_units(oracle_mod):
     """d = 64 with an odd GQA group (its last head pairs consecutive q tiles, so
     some units have one sub-tile) and documents of one tile or less: the split-P
