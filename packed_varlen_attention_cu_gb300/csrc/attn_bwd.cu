@@ -349,6 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pend_u = 0, pend_st = 0;
         auto finish_pending = [&]() -> bool {
             const uint32_t b = pend_u & 1;
+            // the sub-tile's first dQ MMA overwrites the accumulator: the previous
+            // sub-tile's epilogue must have read it (waited only here, so that S and
+            // dP of the first half-items overlap that epilogue)
+            if (first && !mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
+                                         kErrTimeoutBase + 24, kWaitNs))
+                return false;
             if (!mbar_wait_warp(&sh.p2_full[b], (pend_u >> 1) & 1, abort_flag, err_word,
                                 kErrTimeoutBase + 26, kWaitNs))
                 return false;
@@ -374,9 +380,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < nsub && live; ++i) {
                 live = mbar_wait_warp(&sh.a_full, a_it & 1, abort_flag, err_word,
                                       kErrTimeoutBase + 23, kWaitNs);
-                if (!live) break;
-                live = mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
-                                      kErrTimeoutBase + 24, kWaitNs);
                 if (!live) break;
                 tc_fence_after();
 #pragma unroll
@@ -720,6 +723,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pend_u = 0, pend_st = 0;
         auto finish_pending = [&]() -> bool {
             const uint32_t b = pend_u & 1;
+            // the unit's first dV/dK MMAs overwrite the accumulators: the previous
+            // unit's epilogue must have read them (waited only here, so that S^T and
+            // dP^T of the first half-items overlap that epilogue)
+            if (first && !mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
+                                         kErrTimeoutBase + 34, kWaitNs))
+                return false;
             if (!mbar_wait_warp(&sh.p2_full[b], (pend_u >> 1) & 1, abort_flag, err_word,
                                 kErrTimeoutBase + 36, kWaitNs))
                 return false;
@@ -749,9 +758,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (u.cost <= 1) continue;
             live = mbar_wait_warp(&sh.a_full, a_it & 1, abort_flag, err_word,
                                   kErrTimeoutBase + 33, kWaitNs);
-            if (!live) break;
-            live = mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
-                                  kErrTimeoutBase + 34, kWaitNs);
             if (!live) break;
             first = true;
             for (int32_t hh = 0; hh < G && live; ++hh) {
