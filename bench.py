@@ -21,7 +21,9 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
+from typing import Optional
 
 import numpy as np
 
@@ -59,6 +61,9 @@ def make_workload(args):
                        W.lognormal_doc_lengths(args.pack_tokens, math.log(2048.0), 1.5, 1,
                                                65536, 0), 32, 8, 128, cp=8)
         desc = desc.replace("128K", f"{args.pack_tokens}-token")
+    elif args.workload == "longtail" and args.longtail_packs != 8:
+        w = W.long_tail_gqa(args.longtail_packs)
+        desc = desc.replace("8 packs", f"{args.longtail_packs} pack(s)")
     else:
         w = mk()
     if args.c_tile is None:
@@ -120,10 +125,11 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, out_dir: Optional[str] = None):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        out_dir = out_dir or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"pva_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -280,7 +286,7 @@ def run_pva(args, rank, world, local):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
+    with ClockSampler(local, args.clocks_dir) as clocks:
         barrier(world)
         torch.cuda.synchronize()
         start.record(stream)
@@ -309,7 +315,7 @@ def run_pva(args, rank, world, local):
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     # a summary covers one workload at its full size; a shrunk pack has none
-    traffic = None if args.pack_tokens else profile_traffic("attn_fwd.cu",
+    traffic = None if (args.pack_tokens or args.longtail_packs != 8) else profile_traffic("attn_fwd.cu",
                                                             f"attn_fwd_{args.workload}.txt")
 
     result = {
@@ -403,71 +409,26 @@ def run_e2e(args, ctx, world):
             "path": "pva_attn_fwd_host (pinned host buffers), two streams alternating"}
 
 
-def run_zigzag(args, ctx, world, fused=False):
-    """Zigzag CP emulation on one GPU: cp virtual ranks; rank r runs its Q
-    shard against the KV shard of rank (r - t) mod cp at ring step t (fp32
-    partials), merging into the running (O, LSE); results scattered back.
+def run_zigzag(args, ctx, world, per_step=False, fused=False):
+    """Zigzag CP emulation on one GPU (packed_varlen_attention_cu_gb300.ring):
+    cp virtual ranks; rank r runs its Q shard against the KV shard of rank
+    (r - t) mod cp at ring step t, merging into the running (O, LSE); outputs
+    stay rank-local.  per_step: one worklist + attention launch per ring step
+    over every rank (Q/K/V in ring order) instead of one per (rank, step) pair.
     fused: steps t > 0 merge in the attention epilogue (pva_attn_fwd_accumulate)
     instead of writing a partial and running pva_merge_partials."""
     import torch
 
-    from packed_varlen_attention_cu_gb300 import api
+    from packed_varlen_attention_cu_gb300.ring import ZigzagRing
     w, q, k, v, cu_np, flops, _, base_params, hbm = ctx
     cp = w.cp or 8
     dev = q.device
     stream = torch.cuda.current_stream()
     T, hq, d = q.shape
-    hkv = k.shape[1]
-    cu = torch.from_numpy(cu_np).to(dev)
-    lens = [api.zigzag_shard_len(cu_np, cp, r) for r in range(cp)]
-    maps = [torch.empty((n,), dtype=torch.int32, device=dev) for n in lens]
-    qs = [torch.empty((n, hq, d), dtype=torch.bfloat16, device=dev) for n in lens]
-    ks = [torch.empty((n, hkv, d), dtype=torch.bfloat16, device=dev) for n in lens]
-    vs = [torch.empty((n, hkv, d), dtype=torch.bfloat16, device=dev) for n in lens]
-    # per-rank outputs (fp32 partial layout, rank-local rows) and one scratch partial
-    acc_o = [torch.empty((n, hq, d), dtype=torch.float32, device=dev) for n in lens]
-    acc_l = [torch.empty((hq, n), dtype=torch.float32, device=dev) for n in lens]
-    nmax = max(lens)
-    part_o = torch.empty((nmax, hq, d), dtype=torch.float32, device=dev)
-    part_l = torch.empty((hq * nmax,), dtype=torch.float32, device=dev)
-    params = api.make_params(hq, hkv, num_ctas=0, c_tile=base_params.c_tile,
-                             dispatch=base_params.dispatch)
-    masks = {(r, s): api.make_mask(W.MASK_ZIGZAG_PAIR, lens[r], lens[s], cp=cp, q_rank=r, k_rank=s)
-             for r in range(cp) for s in range(cp)}
-    wls = {key: api.alloc_worklist(w.num_docs, m, params, dev) for key, m in masks.items()}
+    ring = ZigzagRing(cu_np, cp, hq, k.shape[1], d, c_tile=base_params.c_tile,
+                      dispatch=base_params.dispatch, per_step=per_step, fused=fused, device=dev)
     merge_ev = []
-
-    def step(record=False):
-        for r in range(cp):
-            api.zigzag_shard(cu, cp, r, maps[r], None, stream)
-            api.gather_rows(q, maps[r], qs[r], stream=stream)
-            api.gather_rows(k, maps[r], ks[r], stream=stream)
-            api.gather_rows(v, maps[r], vs[r], stream=stream)
-        for r in range(cp):
-            n = lens[r]
-            po, pl = part_o[:n], part_l[: hq * n].view(hq, n)
-            for t in range(cp):
-                s = (r - t) % cp
-                m = masks[(r, s)]
-                api.build_worklist(cu, m, params, wls[(r, s)], stream)
-                if fused and t > 0:
-                    api.attn_fwd_accumulate(qs[r], ks[s], vs[s], cu, m, params, wls[(r, s)],
-                                            acc_o[r], acc_l[r], 0.0, None, stream)
-                    continue
-                dst_o, dst_l = (acc_o[r], acc_l[r]) if t == 0 else (po, pl)
-                api.attn_fwd(qs[r], ks[s], vs[s], cu, m, params, wls[(r, s)], dst_o, dst_l, 0.0,
-                             None, stream)
-                if t > 0:
-                    if record:
-                        ea = torch.cuda.Event(enable_timing=True)
-                        eb = torch.cuda.Event(enable_timing=True)
-                        ea.record(stream)
-                    api.merge_partials(acc_o[r], acc_l[r], po, pl, acc_o[r], acc_l[r], stream)
-                    if record:
-                        eb.record(stream)
-                        merge_ev.append((ea, eb, n))
-
-    step()
+    ring.step(q, k, v, stream)
     torch.cuda.synchronize()
     K = max(2, args.steps // 20)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -475,30 +436,32 @@ def run_zigzag(args, ctx, world, fused=False):
     torch.cuda.synchronize()
     s.record(stream)
     for i in range(K):
-        step(record=(i == K - 1))
+        ring.step(q, k, v, stream, merge_ev if i == K - 1 else None)
     e.record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    import packed_varlen_attention_cu_gb300.api as api
+    for wl in ring.worklists():
+        assert api.worklist_error(wl) == 0
     t, f = aggregate(s.elapsed_time(e) / 1e3, flops * K, world)
-    if fused:
-        launches = cp * 4 + cp * cp * (api.worklist_build_kernels(params) + 1)
-        return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "cp": cp, "steps": K,
-                "ms_per_step": round(t / K * 1e3, 3), "gpu_launches_per_step": launches,
-                "note": "as zigzag_cp, but ring steps t > 0 merge into the running (O, LSE) in "
-                        "the attention epilogue: no partial buffers, no merge launches"}
-    mtimes = [a.elapsed_time(b) / 1e3 for a, b, _ in merge_ev]
-    mbytes = [n * hq * (3 * 4 * d + 3 * 4) for _, _, n in merge_ev]
-    merge_gbs = sum(mbytes) / sum(mtimes) / 1e9 if mtimes else None
-    launches = cp * 4 + cp * cp * (api.worklist_build_kernels(params) + 1) + cp * (cp - 1)
-    return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "cp": cp, "steps": K,
-            "ms_per_step": round(t / K * 1e3, 3),
-            "merge": {"bound": "hbm", "achieved": round(merge_gbs, 1) if merge_gbs else None,
-                      "peak": hbm, "unit": "GB/s",
-                      "frac": round(merge_gbs / hbm, 4) if merge_gbs else None,
-                      "bytes_per_row": 3 * 4 * d + 3 * 4, "launches_per_step": cp * (cp - 1)},
-            "gpu_launches_per_step": launches,
-            "note": "cp virtual ranks on one GPU: shard maps, row gathers, per-pair worklist + "
-                    "fp32 partial attention, in-place merges; outputs stay rank-local"}
+    scheme = ("one worklist + attention launch per ring step over all ranks (Q/K/V in ring "
+              "order)" if per_step else "one worklist + attention launch per (rank, step) pair")
+    res = {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "cp": cp, "steps": K,
+           "ms_per_step": round(t / K * 1e3, 3),
+           "gpu_launches_per_step": ring.launches_per_step(),
+           "note": f"cp virtual ranks on one GPU: {scheme}; "
+                   + ("ring steps t > 0 merge into the running (O, LSE) in the attention "
+                      "epilogue (no partials, no merge launches)" if fused else
+                      "fp32 partials merged in place by pva_merge_partials")}
+    if merge_ev:
+        mtimes = [a.elapsed_time(b) / 1e3 for a, b, _ in merge_ev]
+        mbytes = [n * hq * (3 * 4 * d + 3 * 4) for _, _, n in merge_ev]
+        gbs = sum(mbytes) / sum(mtimes) / 1e9
+        res["merge"] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                        "frac": round(gbs / hbm, 4), "bytes_per_row": 3 * 4 * d + 3 * 4,
+                        "launches_per_step": len(merge_ev),
+                        "avg_launch_ms": round(1e3 * sum(mtimes) / len(mtimes), 4)}
+    return res
 
 
 def run_dispatch(args, ctx):
@@ -735,6 +698,8 @@ def main(argv=None):
     ap.add_argument("--c-tile", type=int, default=None,
                     help="per-tile fixed cost in pair units (default: api.default_c_tile(d))")
     ap.add_argument("--pack-tokens", type=int, default=0)
+    ap.add_argument("--longtail-packs", type=int, default=8,
+                    help="packs of the long-tail workload (seeds 0..n-1)")
     ap.add_argument("--dispatch", choices=tuple(DISPATCH), default="dynamic",
                     help="forward units: claimed in LPT order at run time, or the builder's "
                          "static per-CTA LPT lists")
@@ -747,6 +712,9 @@ def main(argv=None):
     ap.add_argument("--refine-iters", type=int, default=20,
                     help="move/swap rounds after LPT (0: none)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--clocks-dir", default=None,
+                    help="folder for the nvidia-smi clock samples of the timed region "
+                         "(default: the system temp folder)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -764,6 +732,8 @@ def main(argv=None):
     if not args.no_zigzag and ctx[0].cp:
         res["zigzag_cp"] = run_zigzag(args, ctx, world)
         res["zigzag_cp_fused"] = run_zigzag(args, ctx, world, fused=True)
+        res["zigzag_cp_step"] = run_zigzag(args, ctx, world, per_step=True)
+        res["zigzag_cp_step_fused"] = run_zigzag(args, ctx, world, per_step=True, fused=True)
     if not args.no_backward:
         bwd = run_backward(args, ctx, world)
         if bwd is not None:

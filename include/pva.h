@@ -63,7 +63,12 @@ typedef enum {
     PVA_MASK_ZIGZAG_PAIR = 3,     /* Q = zigzag shard of q_rank, K/V = shard of k_rank
                                      (rows in pva_zigzag_shard order); same document and
                                      k position <= q position */
-    PVA_MASK_SLICES = 4           /* explicit slice list (AttnSlice, §4.4) */
+    PVA_MASK_SLICES = 4,          /* explicit slice list (AttnSlice, §4.4) */
+    PVA_MASK_ZIGZAG_STEP = 5      /* one ring step of all cp zigzag ranks at once: Q, K and V
+                                     in ring order (rank 0's shard rows, then rank 1's, ...;
+                                     pva_zigzag_ring_map), the query rows of rank r see the
+                                     key rows of rank (r - ring_step) mod cp under the
+                                     ZIGZAG_PAIR rule; q_tokens = k_tokens = cu[num_docs] */
 } pva_mask_kind;
 
 /* The four MaskTypes of "03 · 长文负载均衡" §4.4 (the pages name them without
@@ -105,6 +110,7 @@ typedef struct {
     int32_t num_slices;
     int32_t q_tokens;        /* rows of Q / O (for ZIGZAG_PAIR: pva_zigzag_shard_len(q_rank)) */
     int32_t k_tokens;        /* rows of K / V */
+    int32_t ring_step;       /* ZIGZAG_STEP (with cp): 0 <= ring_step < cp */
 } pva_mask_desc;
 
 /* Worklist parameters.  The attention kernel supports tile_m = tile_n = 128,
@@ -221,6 +227,15 @@ int32_t pva_zigzag_shard_len(const int32_t* cu_seqlens_host, int32_t num_docs, i
 pva_status pva_zigzag_shard(const int32_t* cu_seqlens_dev, int32_t num_docs, int32_t cp,
                             int32_t rank, int32_t* gather_map_dev, int32_t* chunk_table_dev,
                             void* stream);
+
+/* Ring order of all zigzag shards on the device ("长序列训练与上下文并行", ring
+ * attention over cp ranks, each holding its zigzag shard): ring_map_dev[i] =
+ * global token of row i of the concatenation of the shards of ranks 0, 1, ...,
+ * cp-1, each in pva_zigzag_shard order (cu_seqlens[num_docs] entries).  Q, K
+ * and V gathered through this map are the inputs of PVA_MASK_ZIGZAG_STEP.
+ *   cu_seqlens_dev DEVICE int32 [num_docs + 1];  ring_map_dev DEVICE int32 */
+pva_status pva_zigzag_ring_map(const int32_t* cu_seqlens_dev, int32_t num_docs, int32_t cp,
+                               int32_t* ring_map_dev, void* stream);
 
 /* Row gather for shard emulation: dst[i] = src[map[i]] for i < rows, rows of
  * row_bytes bytes (a multiple of 16); scatter = 1 writes dst[map[i]] = src[i].
@@ -382,9 +397,18 @@ pva_status pva_worklist_counts(const void* worklist_dev, int64_t* out7, void* st
  *    rejected with PVA_ERR_BUFFER_TOO_SMALL before any device work.
  *  - The first call on each device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
+ *    Under CUDA's lazy module loading (the default) that first lookup is also
+ *    when the driver loads the module and commits the 16 MiB on the device, so
+ *    a caller with a fixed memory budget makes one warm-up call at start-up,
+ *    before it fixes the budget.  The address is cached per device and per
+ *    CUDA context (a new context, e.g. after cudaDeviceReset, is looked up
+ *    again).
  *  - All calls on a device share the array, which keeps the last call's
  *    contents (the build rewrites everything it reads); calls that overlap on
  *    the GPU race on it.
+ *  - Device-side failures (cu_seqlens that do not match the mask, a capacity
+ *    overflow, a bounded wait that expired) leave out / lse unwritten and are
+ *    recorded in the array's error word: read it with pva_noalloc_error().
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
 pva_status pva_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                                 const int32_t* cu_seqlens_dev, int32_t num_docs,
@@ -419,6 +443,13 @@ pva_status pva_attn_fwd_host(const void* q_host, const void* k_host, const void*
 
 /* Size in bytes of the static worklist array used by pva_attn_fwd_noalloc. */
 size_t pva_noalloc_scratch_bytes(void);
+
+/* Device error word of the last pva_attn_fwd_noalloc call on the current
+ * device (0 = none; otherwise as pva_worklist_error: 100 capacity, 102 a
+ * worklist that does not match, 200 + a wait site).  Synchronizes `stream`
+ * (the stream of that call) and copies 4 bytes to code_out (HOST).  The pages
+ * have no counterpart.  Allocates nothing. */
+pva_status pva_noalloc_error(int32_t* code_out, void* stream);
 
 /* Test hook for the failure path of the bounded waits (the pages have no
  * counterpart).  While `enable` is non-zero, pva_attn_fwd launches made by

@@ -22,7 +22,8 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _HDR = os.path.join(_HERE, "oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_SHARED_QUESTION, MASK_ZIGZAG_PAIR, MASK_SLICES = range(5)
+(MASK_CAUSAL, MASK_SLIDING_WINDOW, MASK_SHARED_QUESTION, MASK_ZIGZAG_PAIR, MASK_SLICES,
+ MASK_ZIGZAG_STEP) = range(6)
 SLICE_FULL, SLICE_CAUSAL, SLICE_INV_CAUSAL, SLICE_BI_CAUSAL = 0, 1, 2, 3
 
 
@@ -42,7 +43,8 @@ class _Mask(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("num_prefix", ctypes.c_int32), ("cp", ctypes.c_int32),
                 ("q_rank", ctypes.c_int32), ("k_rank", ctypes.c_int32),
-                ("slices", ctypes.POINTER(ctypes.c_int32)), ("num_slices", ctypes.c_int32)]
+                ("slices", ctypes.POINTER(ctypes.c_int32)), ("num_slices", ctypes.c_int32),
+                ("ring_step", ctypes.c_int32)]
 
 
 _lib = None
@@ -102,14 +104,15 @@ class Mask:
 
     def __init__(self, kind: int = MASK_CAUSAL, window: int = 0, num_prefix: int = 0,
                  cp: int = 0, q_rank: int = 0, k_rank: int = 0,
-                 slices: Optional[np.ndarray] = None):
+                 slices: Optional[np.ndarray] = None, ring_step: int = 0):
         self.kind, self.window, self.num_prefix = kind, window, num_prefix
         self.cp, self.q_rank, self.k_rank = cp, q_rank, k_rank
+        self.ring_step = ring_step
         self.slices = None if slices is None else np.ascontiguousarray(slices, dtype=np.int32).reshape(-1, 8)
 
     def c(self) -> _Mask:
         m = _Mask(self.kind, self.window, self.num_prefix, self.cp, self.q_rank, self.k_rank,
-                  None, 0)
+                  None, 0, self.ring_step)
         if self.slices is not None:
             m.slices = self.slices.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
             m.num_slices = self.slices.shape[0]
@@ -124,6 +127,11 @@ def bf16_bits(t) -> np.ndarray:
     """uint16 bit patterns of a bf16 torch tensor (any device)."""
     import torch
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def ring_map(cu: np.ndarray, cp: int) -> np.ndarray:
+    """Ring order of all zigzag shards: the maps of ranks 0..cp-1 concatenated."""
+    return np.concatenate([zigzag_map(cu, cp, r)[0] for r in range(cp)]).astype(np.int32)
 
 
 def zigzag_map(cu: np.ndarray, cp: int, rank: int):

@@ -100,6 +100,11 @@ int32_t or_zigzag_map(const int32_t *cu, int32_t ndocs, int32_t cp, int32_t rank
 /*  - zigzag pair (q rank r, kv rank s): rows are rank-local (map above);    */
 /*    allowed iff same document and k position <= q position ([P4] ring     */
 /*    attention, each rank's Q against one KV shard).                        */
+/*  - zigzag ring step t: every rank's shard at once, rows in ring order     */
+/*    (rank 0's shard, then rank 1's, ...); a query row of rank r sees the   */
+/*    key rows of rank (r - t) mod cp that hold the same document at a       */
+/*    position <= its own ([P4] ring loop: at step t rank r works on the KV  */
+/*    that started on rank r - t).                                           */
 /*  - slices: [P1] §4.4 AttnSlice (QRange, KRange, MaskType).  The pages     */
 /*    name FULL / CAUSAL / INV-CAUSAL / BI-CAUSAL without geometry; reading: */
 /*    tests on the slice's token positions, CAUSAL k <= q and INV-CAUSAL     */
@@ -115,7 +120,23 @@ typedef struct {
     int32_t *doc_q, *doc_k; /* document id of every q / k row */
     int32_t *gq, *gk;       /* global token of every row (identity unless zigzag) */
     int32_t *kdoc_lo, *kdoc_hi; /* per document: range of k rows holding it */
+    int32_t *rank_q, *rank_k;   /* ring step: rank of every q / k row */
+    int32_t *krd_lo, *krd_hi;   /* ring step: per (rank, document), its k rows */
 } ctx_t;
+
+/* Ring order of all zigzag shards: map[i] = global token of row i, rank[i] =
+ * the rank whose shard holds it (ranks 0..cp-1 in turn).  Returns the rows. */
+static int32_t ring_order(const int32_t *cu, int32_t ndocs, int32_t cp, int32_t *map,
+                          int32_t *rank) {
+    int32_t n = 0;
+    for (int32_t r = 0; r < cp; ++r) {
+        int32_t nr = or_zigzag_map(cu, ndocs, cp, r, map ? map + n : NULL, NULL);
+        if (rank)
+            for (int32_t i = 0; i < nr; ++i) rank[n + i] = r;
+        n += nr;
+    }
+    return n;
+}
 
 static int ctx_init(ctx_t *c, const int32_t *cu, int32_t ndocs, int32_t Tq, int32_t Tk,
                     const or_mask_t *m) {
@@ -142,6 +163,17 @@ static int ctx_init(ctx_t *c, const int32_t *cu, int32_t ndocs, int32_t Tq, int3
         }
         or_zigzag_map(cu, ndocs, m->cp, m->q_rank, c->gq, NULL);
         or_zigzag_map(cu, ndocs, m->cp, m->k_rank, c->gk, NULL);
+    } else if (m->kind == OR_MASK_ZIGZAG_STEP) {
+        if (m->cp <= 0 || m->ring_step < 0 || m->ring_step >= m->cp || Tq != T || Tk != T) {
+            free(doc_of);
+            free(c->gq);
+            free(c->gk);
+            return -1;
+        }
+        c->rank_q = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+        c->rank_k = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+        ring_order(cu, ndocs, m->cp, c->gq, c->rank_q);
+        ring_order(cu, ndocs, m->cp, c->gk, c->rank_k);
     } else {
         if ((m->kind != OR_MASK_SLICES) && (Tq != T || Tk != T)) {
             free(doc_of);
@@ -168,6 +200,20 @@ static int ctx_init(ctx_t *c, const int32_t *cu, int32_t ndocs, int32_t Tq, int3
         if (j < c->kdoc_lo[d]) c->kdoc_lo[d] = j;
         if (j + 1 > c->kdoc_hi[d]) c->kdoc_hi[d] = j + 1;
     }
+    if (m->kind == OR_MASK_ZIGZAG_STEP) {
+        int64_t nrd = (int64_t)m->cp * ndocs;
+        c->krd_lo = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nrd > 0 ? nrd : 1));
+        c->krd_hi = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nrd > 0 ? nrd : 1));
+        for (int64_t x = 0; x < nrd; ++x) {
+            c->krd_lo[x] = Tk;
+            c->krd_hi[x] = 0;
+        }
+        for (int32_t j = 0; j < Tk; ++j) {
+            int64_t x = (int64_t)c->rank_k[j] * ndocs + c->doc_k[j];
+            if (j < c->krd_lo[x]) c->krd_lo[x] = j;
+            if (j + 1 > c->krd_hi[x]) c->krd_hi[x] = j + 1;
+        }
+    }
     free(doc_of);
     return 0;
 }
@@ -179,6 +225,10 @@ static void ctx_free(ctx_t *c) {
     free(c->gk);
     free(c->kdoc_lo);
     free(c->kdoc_hi);
+    free(c->rank_q);
+    free(c->rank_k);
+    free(c->krd_lo);
+    free(c->krd_hi);
 }
 
 static int allowed(const ctx_t *c, int32_t i, int32_t j) {
@@ -195,6 +245,10 @@ static int allowed(const ctx_t *c, int32_t i, int32_t j) {
     }
     case OR_MASK_ZIGZAG_PAIR:
         return c->doc_q[i] == c->doc_k[j] && c->gk[j] <= c->gq[i];
+    case OR_MASK_ZIGZAG_STEP:
+        return c->doc_q[i] == c->doc_k[j] &&
+               c->rank_k[j] == (c->rank_q[i] - m->ring_step + m->cp) % m->cp &&
+               c->gk[j] <= c->gq[i];
     case OR_MASK_SLICES:
         /* AttnSlice MaskTypes ("03 · 长文负载均衡" §4.4), tested on token positions:
          * CAUSAL k <= q, INV_CAUSAL k >= q (each with an optional window), and
@@ -258,6 +312,12 @@ static int candidates(const ctx_t *c, int32_t i, int brute, int32_t lo[2], int32
         lo[0] = c->kdoc_lo[d];
         hi[0] = c->kdoc_hi[d];
         return lo[0] < hi[0] ? 1 : 0;
+    case OR_MASK_ZIGZAG_STEP: {
+        int64_t x = (int64_t)((c->rank_q[i] - c->m.ring_step + c->m.cp) % c->m.cp) * c->ndocs + d;
+        lo[0] = c->krd_lo[x];
+        hi[0] = c->krd_hi[x];
+        return lo[0] < hi[0] ? 1 : 0;
+    }
     }
     return 0;
 }
@@ -723,6 +783,44 @@ static void push_seg(plan_t *p, int32_t q_row0, int32_t q_len, int32_t q_pos0, i
     p->sg[p->nsg++] = g;
 }
 
+/* Slices of one zigzag pair (q rank r against the KV shard of rank s):     */
+/* per document, each of r's two chunks is a segment, with a CAUSAL slice   */
+/* (on positions) against each of s's chunks that has an allowed pair.     */
+/* qbase / kbase: first row of r's / s's shard in the Q / K buffers.        */
+static void derive_zigzag_pair(const int32_t *cu, int32_t ndocs, int32_t cp, int32_t r,
+                               int32_t s, int32_t qbase, int32_t kbase, plan_t *p) {
+    int32_t qloc = qbase, kloc = kbase;
+    for (int32_t d = 0; d < ndocs; ++d) {
+        int32_t len = cu[d + 1] - cu[d];
+        int32_t qc[2] = {r, 2 * cp - 1 - r}, kc[2] = {s, 2 * cp - 1 - s};
+        int32_t qoff[2], qlen[2], koff[2], klen[2], kl0[2];
+        for (int e = 0; e < 2; ++e) {
+            zz_chunk(len, cp, qc[e], &qoff[e], &qlen[e]);
+            zz_chunk(len, cp, kc[e], &koff[e], &klen[e]);
+        }
+        kl0[0] = kloc;
+        kl0[1] = kloc + klen[0];
+        int32_t ql0 = qloc;
+        for (int e = 0; e < 2; ++e) {
+            if (qlen[e] > 0) {
+                int64_t first = p->nsl;
+                for (int f = 0; f < 2; ++f) {
+                    if (klen[f] <= 0) continue;
+                    if (koff[f] > qoff[e] + qlen[e] - 1) continue; /* no allowed pair */
+                    slice_t sl = {ql0, qlen[e], qoff[e], kl0[f], klen[f], koff[f],
+                                  OR_SLICE_CAUSAL, 0};
+                    push_slice(p, sl);
+                }
+                /* kept even with no slice: its rows then read O = 0, LSE = -inf */
+                push_seg(p, ql0, qlen[e], qoff[e], first);
+            }
+            ql0 += qlen[e];
+        }
+        qloc += qlen[0] + qlen[1];
+        kloc += klen[0] + klen[1];
+    }
+}
+
 /* Slices of every mask kind, in the order the worklist enumerates them. */
 static int derive_plan(const int32_t *cu, int32_t ndocs, const or_mask_t *m, plan_t *p) {
     memset(p, 0, sizeof *p);
@@ -761,36 +859,22 @@ static int derive_plan(const int32_t *cu, int32_t ndocs, const or_mask_t *m, pla
     case OR_MASK_ZIGZAG_PAIR: {
         int32_t cp = m->cp, r = m->q_rank, s = m->k_rank;
         if (cp <= 0 || r < 0 || r >= cp || s < 0 || s >= cp) return -1;
-        int32_t qloc = 0, kloc = 0;
-        for (int32_t d = 0; d < ndocs; ++d) {
-            int32_t len = cu[d + 1] - cu[d];
-            int32_t qc[2] = {r, 2 * cp - 1 - r}, kc[2] = {s, 2 * cp - 1 - s};
-            int32_t qoff[2], qlen[2], koff[2], klen[2], kl0[2];
-            for (int e = 0; e < 2; ++e) {
-                zz_chunk(len, cp, qc[e], &qoff[e], &qlen[e]);
-                zz_chunk(len, cp, kc[e], &koff[e], &klen[e]);
-            }
-            kl0[0] = kloc;
-            kl0[1] = kloc + klen[0];
-            int32_t ql0 = qloc;
-            for (int e = 0; e < 2; ++e) {
-                if (qlen[e] > 0) {
-                    int64_t first = p->nsl;
-                    for (int f = 0; f < 2; ++f) {
-                        if (klen[f] <= 0) continue;
-                        if (koff[f] > qoff[e] + qlen[e] - 1) continue; /* no allowed pair */
-                        slice_t sl = {ql0, qlen[e], qoff[e], kl0[f], klen[f], koff[f],
-                                      OR_SLICE_CAUSAL, 0};
-                        push_slice(p, sl);
-                    }
-                    /* kept even with no slice: its rows then read O = 0, LSE = -inf */
-                    push_seg(p, ql0, qlen[e], qoff[e], first);
-                }
-                ql0 += qlen[e];
-            }
-            qloc += qlen[0] + qlen[1];
-            kloc += klen[0] + klen[1];
+        derive_zigzag_pair(cu, ndocs, cp, r, s, 0, 0, p);
+        return 0;
+    }
+    case OR_MASK_ZIGZAG_STEP: {
+        /* rank r's Q rows start after the shards of ranks < r (ring order);   */
+        /* at step t they meet the K rows of rank (r - t) mod cp, likewise     */
+        int32_t cp = m->cp, t = m->ring_step;
+        if (cp <= 0 || t < 0 || t >= cp) return -1;
+        int32_t *base = (int32_t *)calloc((size_t)cp + 1, sizeof(int32_t));
+        for (int32_t r = 0; r < cp; ++r)
+            base[r + 1] = base[r] + or_zigzag_map(cu, ndocs, cp, r, NULL, NULL);
+        for (int32_t r = 0; r < cp; ++r) {
+            int32_t s = (r - t + cp) % cp;
+            derive_zigzag_pair(cu, ndocs, cp, r, s, base[r], base[s], p);
         }
+        free(base);
         return 0;
     }
     case OR_MASK_SLICES: {
@@ -1200,7 +1284,9 @@ int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t ti
 int or_chunk_areas(int32_t T, const int32_t *cu, int32_t ndocs, const or_mask_t *m,
                    int32_t chunk_size, int64_t *areas) {
     if (chunk_size <= 0 || T < 0) return -1;
-    if (m->kind == OR_MASK_ZIGZAG_PAIR || m->kind == OR_MASK_SLICES) return -1;
+    if (m->kind == OR_MASK_ZIGZAG_PAIR || m->kind == OR_MASK_ZIGZAG_STEP ||
+        m->kind == OR_MASK_SLICES)
+        return -1;
     ctx_t c;
     if (ctx_init(&c, cu, ndocs, T, T, m) != 0) return -2;
     int32_t n = (T + chunk_size - 1) / chunk_size;

@@ -17,7 +17,8 @@ enum {
     OR_MASK_SLIDING_WINDOW = 1,
     OR_MASK_SHARED_QUESTION = 2,
     OR_MASK_ZIGZAG_PAIR = 3,
-    OR_MASK_SLICES = 4
+    OR_MASK_SLICES = 4,
+    OR_MASK_ZIGZAG_STEP = 5
 };
 enum { OR_SLICE_FULL = 0, OR_SLICE_CAUSAL = 1, OR_SLICE_INV_CAUSAL = 2, OR_SLICE_BI_CAUSAL = 3 };
 
@@ -28,6 +29,7 @@ typedef struct {
     int32_t cp, q_rank, k_rank; /* zigzag pair */
     const int32_t *slices;      /* [num_slices][8]: q_row0 q_len q_pos0 k_row0 k_len k_pos0 type window */
     int32_t num_slices;
+    int32_t ring_step;          /* zigzag ring step (with cp): every rank at step ring_step */
 } or_mask_t;
 
 int32_t or_num_threads(void);

@@ -19,8 +19,9 @@ STATUS_NAMES = {0: "PVA_OK", 1: "PVA_ERR_INVALID_ARG", 2: "PVA_ERR_BUFFER_TOO_SM
 # Every symbol declared by include/pva.h.
 EXPORTS = ("pva_worklist_bytes", "pva_build_worklist", "pva_attn_fwd", "pva_attn_fwd_accumulate",
            "pva_zigzag_shard_len",
-           "pva_zigzag_shard", "pva_gather_rows", "pva_merge_partials", "pva_worklist_error",
+           "pva_zigzag_shard", "pva_zigzag_ring_map", "pva_gather_rows", "pva_merge_partials", "pva_worklist_error",
            "pva_worklist_counts", "pva_attn_fwd_noalloc", "pva_noalloc_scratch_bytes",
+           "pva_noalloc_error",
            "pva_attn_fwd_host",
            "pva_debug_withhold_kv_load", "pva_chunk_areas", "pva_dispatch_chunks",
            "pva_striped_shard_len", "pva_striped_shard", "pva_wlb_choose",
@@ -40,7 +41,8 @@ class MaskDesc(ctypes.Structure):
                 ("num_prefix_docs", ctypes.c_int32), ("cp", ctypes.c_int32),
                 ("q_rank", ctypes.c_int32), ("k_rank", ctypes.c_int32),
                 ("slices", ctypes.POINTER(Slice)), ("num_slices", ctypes.c_int32),
-                ("q_tokens", ctypes.c_int32), ("k_tokens", ctypes.c_int32)]
+                ("q_tokens", ctypes.c_int32), ("k_tokens", ctypes.c_int32),
+                ("ring_step", ctypes.c_int32)]
 
 
 class WorklistParams(ctypes.Structure):
@@ -83,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.pva_zigzag_shard_len.argtypes = [P, i32, i32, i32]
         L.pva_zigzag_shard.restype = ctypes.c_int
         L.pva_zigzag_shard.argtypes = [P, i32, i32, i32, P, P, P]
+        L.pva_zigzag_ring_map.restype = ctypes.c_int
+        L.pva_zigzag_ring_map.argtypes = [P, i32, i32, P, P]
         L.pva_gather_rows.restype = ctypes.c_int
         L.pva_gather_rows.argtypes = [P, P, P, i64, i64, i64, i32, P]
         L.pva_merge_partials.restype = ctypes.c_int
@@ -96,6 +100,8 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_float, P]
         L.pva_noalloc_scratch_bytes.restype = sz
         L.pva_noalloc_scratch_bytes.argtypes = []
+        L.pva_noalloc_error.restype = ctypes.c_int
+        L.pva_noalloc_error.argtypes = [ctypes.POINTER(i32), P]
         L.pva_attn_fwd_host.restype = ctypes.c_int
         L.pva_attn_fwd_host.argtypes = [P, P, P, P, i32, MP, WP, i32, P, P, ctypes.c_float,
                                         P, P, P, P, P, sz, P, P, P]

@@ -15,7 +15,7 @@ import torch
 from . import _lib
 from ._lib import MaskDesc, Slice, WorklistParams, check, lib
 from .workloads import (MASK_CAUSAL, MASK_SHARED_QUESTION, MASK_SLICES, MASK_SLIDING_WINDOW,
-                        MASK_ZIGZAG_PAIR)
+                        MASK_ZIGZAG_PAIR, MASK_ZIGZAG_STEP)
 
 SLICE_FULL, SLICE_CAUSAL, SLICE_INV_CAUSAL, SLICE_BI_CAUSAL = 0, 1, 2, 3
 TILE = 128
@@ -33,12 +33,13 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 def make_mask(kind: int = MASK_CAUSAL, q_tokens: int = 0, k_tokens: int = 0, window: int = 0,
               num_prefix_docs: int = 0, cp: int = 0, q_rank: int = 0, k_rank: int = 0,
-              slices: Optional[np.ndarray] = None) -> MaskDesc:
+              slices: Optional[np.ndarray] = None, ring_step: int = 0) -> MaskDesc:
     """pva_mask_desc.  ``slices``: int32 [n, 8] rows (q_row0, q_len, q_pos0, k_row0, k_len,
     k_pos0, type, window); the array is kept alive on the returned object."""
     m = MaskDesc()
     m.kind, m.window, m.num_prefix_docs = kind, window, num_prefix_docs
     m.cp, m.q_rank, m.k_rank = cp, q_rank, k_rank
+    m.ring_step = ring_step
     m.q_tokens, m.k_tokens = q_tokens, k_tokens
     if slices is not None:
         arr = np.ascontiguousarray(slices, dtype=np.int32).reshape(-1, 8)
@@ -179,6 +180,13 @@ def zigzag_shard(cu_seqlens: torch.Tensor, cp: int, rank: int, gather_map: torch
     check("pva_zigzag_shard", lib().pva_zigzag_shard(
         _ptr(cu_seqlens), cu_seqlens.numel() - 1, cp, rank, _ptr(gather_map), _ptr(chunk_table),
         _stream(stream)))
+
+
+def zigzag_ring_map(cu_seqlens: torch.Tensor, cp: int, ring_map: torch.Tensor,
+                    stream=None) -> None:
+    """Ring order of all cp zigzag shards (pva_zigzag_ring_map) into ring_map [T] int32."""
+    check("pva_zigzag_ring_map", lib().pva_zigzag_ring_map(
+        _ptr(cu_seqlens), cu_seqlens.numel() - 1, cp, _ptr(ring_map), _stream(stream)))
 
 
 def gather_rows(src: torch.Tensor, index_map: torch.Tensor, dst: torch.Tensor,

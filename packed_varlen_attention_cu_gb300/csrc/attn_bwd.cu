@@ -1063,13 +1063,15 @@ extern "C" pva_status pva_attn_bwd(const void* q, const void* k, const void* v, 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t es = grads_are_fp32 ? 4 : 2;
     // Keys that no slice covers get no gradient: explicit slices, and a zigzag
-    // pair's key chunks that lie after every query chunk of their document.
+    // pair's (or ring step's) key chunks that lie after every query chunk of
+    // their document.
     // Queries outside every segment: explicit slices only.
     if (mask->kind == PVA_MASK_SLICES &&
         cudaMemsetAsync(dq, 0, (size_t)mask->q_tokens * params->num_q_heads * head_dim * es, st) !=
             cudaSuccess)
         return PVA_ERR_CUDA;
-    if ((mask->kind == PVA_MASK_SLICES || mask->kind == PVA_MASK_ZIGZAG_PAIR) &&
+    if ((mask->kind == PVA_MASK_SLICES || mask->kind == PVA_MASK_ZIGZAG_PAIR ||
+         mask->kind == PVA_MASK_ZIGZAG_STEP) &&
         (cudaMemsetAsync(dk, 0, (size_t)mask->k_tokens * params->num_kv_heads * head_dim * es,
                          st) != cudaSuccess ||
          cudaMemsetAsync(dv, 0, (size_t)mask->k_tokens * params->num_kv_heads * head_dim * es,

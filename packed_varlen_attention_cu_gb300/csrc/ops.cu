@@ -27,64 +27,94 @@ int grid_for(int64_t work_items, int threads) {
 }
 
 // ------------------------------------------------------------------ merge
-// One thread per 16-byte chunk of O.  The host only accepts head dims whose
-// chunk count per row divides 32, so a row never straddles two warps.
+// Each (token, head) row of O is cpr = d / kElems 16-byte chunks; a warp
+// covers 32 / cpr whole rows (the host accepts only head dims whose chunk
+// count divides 32).  Per row, the lane holding chunk 0 loads the two LSEs and
+// computes the weights once; the row's other lanes receive them by shuffle.
+// Each thread handles kUnroll chunks per pass (whole warps at a stride of the
+// grid), all loads issued before any arithmetic, so that enough bytes are in
+// flight to keep HBM busy.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeUnroll = 4;
+
 template <bool F32>
-__global__ void __launch_bounds__(256) merge_kernel(const void* __restrict__ oa_, const float* la,
-                                                    const void* __restrict__ ob_, const float* lb,
-                                                    void* out_, float* lout, int64_t tokens,
-                                                    int32_t heads, int32_t d) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(
+    const void* __restrict__ oa_, const float* la, const void* __restrict__ ob_, const float* lb,
+    void* out_, float* lout, int64_t tokens, int32_t heads, int32_t d) {
     constexpr int kElems = F32 ? 4 : 8;
     const int32_t cpr = d / kElems;  // chunks per row
     const int64_t nchunks = tokens * heads * cpr;
+    const int lane = threadIdx.x & 31;
+    const int lead = lane & ~(cpr - 1);  // lane of chunk 0 of this lane's row
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-         idx - threadIdx.x % 32 < nchunks; idx += stride) {
-        const bool act = idx < nchunks;
-        const int64_t row = act ? idx / cpr : 0;
-        const int32_t chunk = (int32_t)(idx - row * cpr);
-        const int64_t t = row / heads;
-        const int32_t h = (int32_t)(row - t * heads);
-        const int64_t li = (int64_t)h * tokens + t;
-        float a = -INFINITY, b = -INFINITY;
-        if (act) {
-            a = la[li];
-            b = lb[li];
+    const uint4* oa = reinterpret_cast<const uint4*>(oa_);
+    const uint4* ob = reinterpret_cast<const uint4*>(ob_);
+    uint4* out = reinterpret_cast<uint4*>(out_);
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane; base < nchunks;
+         base += kMergeUnroll * stride) {
+        uint4 x[kMergeUnroll], y[kMergeUnroll];
+        float a[kMergeUnroll], b[kMergeUnroll];
+        int64_t li[kMergeUnroll];
+#pragma unroll
+        for (int u = 0; u < kMergeUnroll; ++u) {
+            const int64_t idx = base + u * stride + lane;
+            const bool act = idx < nchunks;
+            const int64_t row = idx / cpr;
+            const int64_t t = row / heads;
+            li[u] = (int64_t)(row - t * heads) * tokens + t;
+            a[u] = b[u] = -INFINITY;
+            if (act && lane == lead) {
+                a[u] = la[li[u]];
+                b[u] = lb[li[u]];
+            }
+            if (act) {
+                x[u] = oa[idx];
+                y[u] = ob[idx];
+            }
         }
-        float wa = 0.f, wb = 0.f, l = -INFINITY;
-        if (a != -INFINITY || b != -INFINITY) {
-            const float mx = fmaxf(a, b);
-            l = mx + logf(expf(a - mx) + expf(b - mx));
-            wa = expf(a - l);
-            wb = expf(b - l);
-        }
-        if (act) {
+#pragma unroll
+        for (int u = 0; u < kMergeUnroll; ++u) {
+            const int64_t idx = base + u * stride + lane;
+            const bool act = idx < nchunks;
+            float wa = 0.f, wb = 0.f, l = -INFINITY;
+            if (lane == lead && (a[u] != -INFINITY || b[u] != -INFINITY)) {
+                //   l = ln(e^a + e^b),  w_a = e^(a - l),  w_b = e^(b - l)
+                const float mx = fmaxf(a[u], b[u]);
+                const float ea = expf(a[u] - mx), eb = expf(b[u] - mx);
+                const float inv = 1.f / (ea + eb);
+                l = mx + logf(ea + eb);
+                wa = ea * inv;
+                wb = eb * inv;
+            }
+            wa = __shfl_sync(0xffffffffu, wa, lead);
+            wb = __shfl_sync(0xffffffffu, wb, lead);
+            if (!act) continue;
             if (F32) {
-                const float4 x = reinterpret_cast<const float4*>(oa_)[idx];
-                const float4 y = reinterpret_cast<const float4*>(ob_)[idx];
-                reinterpret_cast<float4*>(out_)[idx] =
-                    make_float4(wa * x.x + wb * y.x, wa * x.y + wb * y.y, wa * x.z + wb * y.z,
-                                wa * x.w + wb * y.w);
+                const float4 fx = *reinterpret_cast<const float4*>(&x[u]);
+                const float4 fy = *reinterpret_cast<const float4*>(&y[u]);
+                const float4 o = make_float4(wa * fx.x + wb * fy.x, wa * fx.y + wb * fy.y,
+                                             wa * fx.z + wb * fy.z, wa * fx.w + wb * fy.w);
+                out[idx] = *reinterpret_cast<const uint4*>(&o);
             } else {
-                const uint4 x = reinterpret_cast<const uint4*>(oa_)[idx];
-                const uint4 y = reinterpret_cast<const uint4*>(ob_)[idx];
-                const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+                const uint32_t xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                const uint32_t ys[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
                 uint32_t r[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
-                    const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[e]));
+                    const float2 fx =
+                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
+                    const float2 fy =
+                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[e]));
                     const __nv_bfloat162 o =
                         __floats2bfloat162_rn(wa * fx.x + wb * fy.x, wa * fx.y + wb * fy.y);
                     r[e] = *reinterpret_cast<const uint32_t*>(&o);
                 }
-                reinterpret_cast<uint4*>(out_)[idx] = make_uint4(r[0], r[1], r[2], r[3]);
+                out[idx] = make_uint4(r[0], r[1], r[2], r[3]);
             }
+            // the lead lane read the input LSEs itself, so the (possibly in-place)
+            // output LSE may be written now
+            if (lane == lead) lout[li[u]] = l;
         }
-        // every lane of the row has read the input LSEs before the (possibly
-        // in-place) output LSE is written
-        __syncwarp();
-        if (act && chunk == 0) lout[li] = l;
     }
 }
 
@@ -98,71 +128,78 @@ __device__ __forceinline__ void zz_chunk(int32_t len, int32_t cp, int32_t c, int
 
 constexpr int kZzThreads = 1024;
 
-// One CTA: per-document rank-local offsets in shared memory (block scan),
-// then every local row is mapped to its global token.
+// One CTA: for each rank of [rank_begin, rank_end), per-document rank-local
+// offsets in shared memory (block scan), then every local row is mapped to its
+// global token; the ranks' shards follow each other in `map`.
 __global__ void __launch_bounds__(kZzThreads) zigzag_kernel(const int32_t* cu, int32_t nd,
-                                                             int32_t cp, int32_t rank,
-                                                             int32_t* map, int32_t* table) {
+                                                             int32_t cp, int32_t rank_begin,
+                                                             int32_t rank_end, int32_t* map,
+                                                             int32_t* table) {
     extern __shared__ int32_t loc[];  // [nd + 1]
     __shared__ int32_t warp_sum[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    if (tid == 0) carry = 0;
-    __syncthreads();
-    const int32_t c0 = rank, c1 = 2 * cp - 1 - rank;
-    for (int32_t d0 = 0; d0 < nd; d0 += kZzThreads) {
-        const int32_t d = d0 + tid;
-        int32_t v = 0;
-        if (d < nd) {
-            const int32_t len = cu[d + 1] - cu[d];
+    int32_t row0 = 0;  // first map entry of the current rank
+    for (int32_t rank = rank_begin; rank < rank_end; ++rank) {
+        if (tid == 0) carry = 0;
+        __syncthreads();
+        const int32_t c0 = rank, c1 = 2 * cp - 1 - rank;
+        for (int32_t d0 = 0; d0 < nd; d0 += kZzThreads) {
+            const int32_t d = d0 + tid;
+            int32_t v = 0;
+            if (d < nd) {
+                const int32_t len = cu[d + 1] - cu[d];
+                int32_t o0, l0, o1, l1;
+                zz_chunk(len, cp, c0, o0, l0);
+                zz_chunk(len, cp, c1, o1, l1);
+                v = l0 + l1;
+                if (table) {
+                    int32_t* r = table + (int64_t)d * 8;
+                    r[0] = d; r[1] = c0; r[2] = cu[d] + o0; r[3] = l0;
+                    r[4] = d; r[5] = c1; r[6] = cu[d] + o1; r[7] = l1;
+                }
+            }
+            int32_t inc = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += t;
+            }
+            if (lane == 31) warp_sum[w] = inc;
+            __syncthreads();
+            if (w == 0) {
+                int32_t x = warp_sum[lane];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int32_t t = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += t;
+                }
+                warp_sum[lane] = x;
+            }
+            __syncthreads();
+            if (d < nd) loc[d] = carry + (w > 0 ? warp_sum[w - 1] : 0) + inc - v;
+            __syncthreads();
+            if (tid == 0) carry += warp_sum[31];
+            __syncthreads();
+        }
+        if (tid == 0) loc[nd] = carry;
+        __syncthreads();
+        const int32_t total = loc[nd];
+        for (int32_t i = tid; i < total; i += kZzThreads) {
+            int32_t lo = 0, hi = nd - 1;  // last document with loc[d] <= i
+            while (lo < hi) {
+                const int32_t mid = (lo + hi + 1) >> 1;
+                if (loc[mid] <= i) lo = mid;
+                else hi = mid - 1;
+            }
+            const int32_t d = lo, len = cu[d + 1] - cu[d], j = i - loc[d];
             int32_t o0, l0, o1, l1;
             zz_chunk(len, cp, c0, o0, l0);
             zz_chunk(len, cp, c1, o1, l1);
-            v = l0 + l1;
-            if (table) {
-                int32_t* r = table + (int64_t)d * 8;
-                r[0] = d; r[1] = c0; r[2] = cu[d] + o0; r[3] = l0;
-                r[4] = d; r[5] = c1; r[6] = cu[d] + o1; r[7] = l1;
-            }
+            map[row0 + i] = cu[d] + (j < l0 ? o0 + j : o1 + (j - l0));
         }
-        int32_t inc = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int32_t t = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += t;
-        }
-        if (lane == 31) warp_sum[w] = inc;
-        __syncthreads();
-        if (w == 0) {
-            int32_t x = warp_sum[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int32_t t = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += t;
-            }
-            warp_sum[lane] = x;
-        }
-        __syncthreads();
-        if (d < nd) loc[d] = carry + (w > 0 ? warp_sum[w - 1] : 0) + inc - v;
-        __syncthreads();
-        if (tid == 0) carry += warp_sum[31];
-        __syncthreads();
-    }
-    if (tid == 0) loc[nd] = carry;
-    __syncthreads();
-    const int32_t total = loc[nd];
-    for (int32_t i = tid; i < total; i += kZzThreads) {
-        int32_t lo = 0, hi = nd - 1;  // last document with loc[d] <= i
-        while (lo < hi) {
-            const int32_t mid = (lo + hi + 1) >> 1;
-            if (loc[mid] <= i) lo = mid;
-            else hi = mid - 1;
-        }
-        const int32_t d = lo, len = cu[d + 1] - cu[d], j = i - loc[d];
-        int32_t o0, l0, o1, l1;
-        zz_chunk(len, cp, c0, o0, l0);
-        zz_chunk(len, cp, c1, o1, l1);
-        map[i] = cu[d] + (j < l0 ? o0 + j : o1 + (j - l0));
+        row0 += total;
+        __syncthreads();  // loc[] is rewritten for the next rank
     }
 }
 
@@ -206,13 +243,13 @@ extern "C" pva_status pva_merge_partials(const void* o_a, const float* lse_a, co
         return PVA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int64_t chunks = tokens * heads * (head_dim / (o_is_fp32 ? 4 : 8));
-    const int grid = grid_for(chunks, 256);
+    const int grid = grid_for((chunks + kMergeUnroll - 1) / kMergeUnroll, kMergeThreads);
     if (o_is_fp32)
-        merge_kernel<true><<<grid, 256, 0, st>>>(o_a, lse_a, o_b, lse_b, out, lse_out, tokens, heads,
-                                                 head_dim);
+        merge_kernel<true><<<grid, kMergeThreads, 0, st>>>(o_a, lse_a, o_b, lse_b, out, lse_out,
+                                                           tokens, heads, head_dim);
     else
-        merge_kernel<false><<<grid, 256, 0, st>>>(o_a, lse_a, o_b, lse_b, out, lse_out, tokens,
-                                                  heads, head_dim);
+        merge_kernel<false><<<grid, kMergeThreads, 0, st>>>(o_a, lse_a, o_b, lse_b, out, lse_out,
+                                                            tokens, heads, head_dim);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
 
@@ -229,8 +266,24 @@ extern "C" pva_status pva_zigzag_shard(const int32_t* cu_seqlens_dev, int32_t nu
                              (int)smem) != cudaSuccess)
         return PVA_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    zigzag_kernel<<<1, kZzThreads, smem, st>>>(cu_seqlens_dev, num_docs, cp, rank, gather_map_dev,
-                                               chunk_table_dev);
+    zigzag_kernel<<<1, kZzThreads, smem, st>>>(cu_seqlens_dev, num_docs, cp, rank, rank + 1,
+                                               gather_map_dev, chunk_table_dev);
+    return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
+}
+
+extern "C" pva_status pva_zigzag_ring_map(const int32_t* cu_seqlens_dev, int32_t num_docs,
+                                          int32_t cp, int32_t* ring_map_dev, void* stream) {
+    if (!cu_seqlens_dev || !ring_map_dev || num_docs < 0 || cp < 1) return PVA_ERR_INVALID_ARG;
+    const size_t smem = ((size_t)num_docs + 1) * sizeof(int32_t);
+    if (smem > 200 * 1024) return PVA_ERR_UNSUPPORTED;
+    if (num_docs == 0) return PVA_OK;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(zigzag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return PVA_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    zigzag_kernel<<<1, kZzThreads, smem, st>>>(cu_seqlens_dev, num_docs, cp, 0, cp, ring_map_dev,
+                                               nullptr);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
 

@@ -89,7 +89,7 @@ struct PlanArgs {
     uint8_t* base;
     const int32_t* cu;
     int32_t num_docs, kind, window, num_prefix, cp, q_rank, k_rank, num_slices;
-    int32_t tile_m, hq, hkv, q_tokens, k_tokens;
+    int32_t tile_m, hq, hkv, q_tokens, k_tokens, ring_step;
 };
 
 __device__ __forceinline__ void set_error(WlHeader* h, int32_t code) { atomicCAS(&h->error, 0, code); }
@@ -134,11 +134,21 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
             if (tid == 0) set_error(h, kErrBadWorklist);
             return;
         }
-        // pass 1: per-document segment / slice counts and zigzag local offsets
-        for (int d0 = 0; d0 < nd; d0 += kPlanThreads) {
-            const int d = d0 + tid;
+        // Items: the documents, or for a zigzag ring step the (rank, document)
+        // pairs in rank-major order (the order of the ring-ordered Q / K rows).
+        const bool ring = a.kind == PVA_MASK_ZIGZAG_STEP;
+        const int32_t items = ring ? a.cp * nd : nd;
+        // zigzag pair / ring step: the query rank and the key rank of item i
+        auto ranks_of = [&](int i, int32_t& qr, int32_t& kr) {
+            qr = ring ? i / nd : a.q_rank;
+            kr = ring ? (qr - a.ring_step + a.cp) % a.cp : a.k_rank;
+        };
+        // pass 1: per-item segment / slice counts and zigzag local offsets
+        for (int i0 = 0; i0 < items; i0 += kPlanThreads) {
+            const int i = i0 + tid;
             int32_t v[4] = {0, 0, 0, 0};
-            if (d < nd) {
+            if (i < items) {
+                const int d = ring ? i % nd : i;
                 const int32_t len = a.cu[d + 1] - a.cu[d];
                 if (a.kind == PVA_MASK_CAUSAL || a.kind == PVA_MASK_SLIDING_WINDOW) {
                     v[0] = v[1] = len > 0;
@@ -146,8 +156,10 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
                     v[0] = len > 0;
                     v[1] = len > 0 ? (d >= a.num_prefix ? s_npref + 1 : 1) : 0;
                 } else {
-                    const int32_t qc[2] = {a.q_rank, 2 * a.cp - 1 - a.q_rank};
-                    const int32_t kc[2] = {a.k_rank, 2 * a.cp - 1 - a.k_rank};
+                    int32_t qr, kr;
+                    ranks_of(i, qr, kr);
+                    const int32_t qc[2] = {qr, 2 * a.cp - 1 - qr};
+                    const int32_t kc[2] = {kr, 2 * a.cp - 1 - kr};
                     int32_t qo[2], ql[2], ko[2], kl[2];
                     for (int e = 0; e < 2; ++e) {
                         zz_chunk_dev(len, a.cp, qc[e], qo[e], ql[e]);
@@ -165,8 +177,8 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
             }
             int32_t tot[4];
             block_scan_excl<4>(v, tot, sm4);
-            if (d < nd) {
-                for (int k = 0; k < 4; ++k) scan[k * (nd + 1) + d] = carry[k] + v[k];
+            if (i < items) {
+                for (int k = 0; k < 4; ++k) scan[k * (items + 1) + i] = carry[k] + v[k];
             }
             __syncthreads();
             if (tid == 0)
@@ -174,10 +186,11 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
             __syncthreads();
         }
         if (tid == 0) {
-            for (int k = 0; k < 4; ++k) scan[k * (nd + 1) + nd] = carry[k];
+            for (int k = 0; k < 4; ++k) scan[k * (items + 1) + items] = carry[k];
             s_nseg = carry[0];
             s_nsl = carry[1];
-            if (a.kind == PVA_MASK_ZIGZAG_PAIR && (carry[2] != a.q_tokens || carry[3] != a.k_tokens))
+            if ((a.kind == PVA_MASK_ZIGZAG_PAIR || ring) &&
+                (carry[2] != a.q_tokens || carry[3] != a.k_tokens))
                 s_bad = 1;
             if (carry[0] > h->cap_segs || carry[1] > h->cap_slices) s_bad = 2;
         }
@@ -186,10 +199,11 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
             if (tid == 0) set_error(h, s_bad == 2 ? kErrCapacity : kErrBadWorklist);
             return;
         }
-        // pass 2: write the slices and segments of every document
-        for (int d = tid; d < nd; d += kPlanThreads) {
+        // pass 2: write the slices and segments of every item
+        for (int i = tid; i < items; i += kPlanThreads) {
+            const int d = ring ? i % nd : i;
             const int32_t len = a.cu[d + 1] - a.cu[d];
-            int32_t sg = scan[d], sl = scan[(nd + 1) + d];
+            int32_t sg = scan[i], sl = scan[(items + 1) + i];
             if (a.kind == PVA_MASK_CAUSAL || a.kind == PVA_MASK_SLIDING_WINDOW) {
                 if (len <= 0) continue;
                 const int32_t w = a.kind == PVA_MASK_SLIDING_WINDOW ? a.window : 0;
@@ -208,14 +222,21 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
                 slices[sl++] = WlSlice{a.cu[d], len, 0, a.cu[d], len, 0, PVA_SLICE_CAUSAL, 0};
                 segs[sg] = WlSeg{a.cu[d], len, 0, first, sl - first, 0, 0, 0};
             } else {
-                const int32_t qc[2] = {a.q_rank, 2 * a.cp - 1 - a.q_rank};
-                const int32_t kc[2] = {a.k_rank, 2 * a.cp - 1 - a.k_rank};
+                int32_t qr, kr;
+                ranks_of(i, qr, kr);
+                const int32_t qc[2] = {qr, 2 * a.cp - 1 - qr};
+                const int32_t kc[2] = {kr, 2 * a.cp - 1 - kr};
                 int32_t qo[2], ql[2], ko[2], kl[2];
                 for (int e = 0; e < 2; ++e) {
                     zz_chunk_dev(len, a.cp, qc[e], qo[e], ql[e]);
                     zz_chunk_dev(len, a.cp, kc[e], ko[e], kl[e]);
                 }
-                const int32_t qloc = scan[2 * (nd + 1) + d], kloc = scan[3 * (nd + 1) + d];
+                // first Q row of the item; its K rows: in a pair's K shard, the
+                // item's own k-length scan; in ring order, where rank kr's rows
+                // of document d start (the query-row scan of item (kr, d))
+                const int32_t qloc = scan[2 * (items + 1) + i];
+                const int32_t kloc =
+                    ring ? scan[2 * (items + 1) + kr * nd + d] : scan[3 * (items + 1) + i];
                 const int32_t krow[2] = {kloc, kloc + kl[0]};
                 int32_t qrow = qloc;
                 for (int e = 0; e < 2; ++e) {
@@ -1082,7 +1103,7 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
         return false;
     if (num_ctas <= 0 || num_ctas > kMaxBins) return false;
     if (m->q_tokens < 0 || m->k_tokens < 0) return false;
-    int64_t cap_segs = 0, cap_slices = 0, max_group = 1;
+    int64_t cap_segs = 0, cap_slices = 0, max_group = 1, scan_items = num_docs;
     switch (m->kind) {
     case PVA_MASK_CAUSAL:
         cap_segs = cap_slices = num_docs;
@@ -1103,6 +1124,16 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
             return false;
         cap_segs = 2 * (int64_t)num_docs;
         cap_slices = 4 * (int64_t)num_docs;
+        max_group = 2;
+        break;
+    case PVA_MASK_ZIGZAG_STEP:
+        if (m->cp < 1 || m->ring_step < 0 || m->ring_step >= m->cp ||
+            (int64_t)m->cp * num_docs > (INT32_MAX / 8))
+            return false;
+        if (m->q_tokens != m->k_tokens) return false;
+        cap_segs = 2 * (int64_t)m->cp * num_docs;
+        cap_slices = 4 * (int64_t)m->cp * num_docs;
+        scan_items = (int64_t)m->cp * num_docs;
         max_group = 2;
         break;
     case PVA_MASK_SLICES: {
@@ -1176,7 +1207,7 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     f.units = o; o = align256(o + cap_units * (int64_t)sizeof(WlUnit));
     f.runs = o; o = align256(o + (int64_t)h->cap_runs * sizeof(WlRun));
     f.cta_off = o; o = align256(o + ((int64_t)num_ctas + 1) * 4);
-    f.doc_scan = o; o = align256(o + 4 * ((int64_t)num_docs + 1) * 4);
+    f.doc_scan = o; o = align256(o + 4 * (scan_items + 1) * 4);
     f.dorder = o; o = align256(o + cap_units * 4);
     f.cls_work = o; o = align256(o + 64 * 8);
     f.total = o;
@@ -1247,6 +1278,7 @@ extern "C" pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t 
     pa.hkv = params->num_kv_heads;
     pa.q_tokens = mask->q_tokens;
     pa.k_tokens = mask->k_tokens;
+    pa.ring_step = mask->ring_step;
     wl_plan_kernel<<<1, kPlanThreads, 0, st>>>(pa);
     UnitArgs ua{base, params->tile_m, params->tile_n, params->num_q_heads, params->num_kv_heads,
                 (long long)params->c_tile};

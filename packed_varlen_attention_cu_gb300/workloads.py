@@ -32,6 +32,7 @@ MASK_SLIDING_WINDOW = 1
 MASK_SHARED_QUESTION = 2
 MASK_ZIGZAG_PAIR = 3
 MASK_SLICES = 4
+MASK_ZIGZAG_STEP = 5
 
 
 def lognormal_doc_lengths(total: int, mu: float, sigma: float, lo: int, hi: int,

@@ -18,12 +18,14 @@ ORACLE_MASK_KIND = {W.MASK_CAUSAL: oracle.MASK_CAUSAL,
                     W.MASK_SLIDING_WINDOW: oracle.MASK_SLIDING_WINDOW,
                     W.MASK_SHARED_QUESTION: oracle.MASK_SHARED_QUESTION,
                     W.MASK_ZIGZAG_PAIR: oracle.MASK_ZIGZAG_PAIR,
-                    W.MASK_SLICES: oracle.MASK_SLICES}
+                    W.MASK_SLICES: oracle.MASK_SLICES,
+                    W.MASK_ZIGZAG_STEP: oracle.MASK_ZIGZAG_STEP}
 
 
-def oracle_mask(kind, window=0, num_prefix=0, cp=0, q_rank=0, k_rank=0, slices=None):
+def oracle_mask(kind, window=0, num_prefix=0, cp=0, q_rank=0, k_rank=0, slices=None,
+                ring_step=0):
     return oracle.Mask(ORACLE_MASK_KIND[kind], window=window, num_prefix=num_prefix, cp=cp,
-                       q_rank=q_rank, k_rank=k_rank, slices=slices)
+                       q_rank=q_rank, k_rank=k_rank, slices=slices, ring_step=ring_step)
 
 
 def compare(out, lse, ref_o, ref_l, label=""):

@@ -8,6 +8,8 @@ positions with an optional window) and check them against the mask predicate
 written from the definitions: every allowed pair is computed exactly once per
 head and no tile in a run is empty.
 """
+import itertools
+
 import numpy as np
 import pytest
 
@@ -205,3 +207,38 @@ def test_dispatch_order_is_lpt_over_power_of_two_classes(oracle_mod):
     assert np.all(np.diff(oh)[np.diff(kh) == 0] > 0)
     ct, ot = cost[order][~head], order[~head]
     assert np.all((np.diff(ct) < 0) | ((np.diff(ct) == 0) & (np.diff(ot) > 0)))
+
+
+def _list_schedule(costs, order, m):
+    """Graham's list scheduling: units in `order`, each started on the machine
+    that becomes free first (lowest id on ties); returns the makespan."""
+    free = [0] * m
+    for u in order:
+        b = min(range(m), key=lambda i: (free[i], i))
+        free[b] += int(costs[u])
+    return max(free)
+
+
+def test_dispatch_order_list_scheduling_within_graham_bound(oracle_mod):
+    """The pages' LPT rule assigns each unit to the least loaded worker.  Run
+    at run time, "least loaded" is the worker that frees up first, i.e. list
+    scheduling in the dispatch order, with a unit's cost as its duration.  For
+    any order Graham's bound holds: makespan <= (2 - 1/m) OPT, with OPT found
+    here by brute force over all assignments; with the order fully sorted by
+    cost (every class at or below the split) the LPT bound 4/3 - 1/(3m) holds
+    too."""
+    rng = np.random.default_rng(11)
+    for trial in range(80):
+        n = int(rng.integers(1, 9))
+        m = int(rng.integers(1, 4))
+        costs = rng.integers(0, 300, size=n)
+        order = oracle_mod.dispatch_order(costs, m)
+        assert sorted(order.tolist()) == list(range(n))
+        span = _list_schedule(costs, order, m)
+        opt = min(max(np.bincount(np.array(a), weights=costs, minlength=m))
+                  for a in itertools.product(range(m), repeat=n))
+        assert span >= opt
+        assert span * m <= (2 * m - 1) * opt + 1e-9
+        srt = sorted(range(n), key=lambda u: (-int(costs[u]), u))
+        if order.tolist() == srt:
+            assert span * 3 * m <= (4 * m - 1) * opt + 1e-9
