@@ -48,6 +48,8 @@ WORKLOADS = {
     "window": (W.sliding_window, "sliding window 4096: docs 131072/65536/49152/16384, "
                                  "16/4 heads, d=128"),
     "tiny": (W.tiny_pack, "tiny pack: 2048 tokens, lognormal(5,1) clip [16,1024], 4/4 heads, d=64"),
+    "short": (W.short_docs, "short-document pack: 131072 tokens, lognormal(ln 64, 0.75) clip "
+                            "[8, 512], 32 q / 8 kv heads, d=128"),
 }
 
 
@@ -61,7 +63,7 @@ def make_workload(args):
                        W.lognormal_doc_lengths(args.pack_tokens, math.log(2048.0), 1.5, 1,
                                                65536, 0), 32, 8, 128, cp=8)
         desc = desc.replace("128K", f"{args.pack_tokens}-token")
-    elif args.workload == "longtail" and args.longtail_packs != 8:
+    elif args.workload == "longtail" and getattr(args, "longtail_packs", 8) != 8:
         w = W.long_tail_gqa(args.longtail_packs)
         desc = desc.replace("8 packs", f"{args.longtail_packs} pack(s)")
     else:
@@ -258,7 +260,8 @@ def run_pva(args, rank, world, local):
         args.c_tile = fitted
         del cal_wl, cal_busy
     params = api.make_params(hq, hkv, num_ctas=0, c_tile=args.c_tile,
-                             refine_iters=args.refine_iters, dispatch=DISPATCH[args.dispatch])
+                             refine_iters=args.refine_iters, dispatch=DISPATCH[args.dispatch],
+                             pack_docs=1 if args.pack_docs else 0)
     wl = api.alloc_worklist(w.num_docs, mask, params, dev)
 
     api.build_worklist(cu, mask, params, wl)
@@ -315,8 +318,8 @@ def run_pva(args, rank, world, local):
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     # a summary covers one workload at its full size; a shrunk pack has none
-    traffic = None if (args.pack_tokens or args.longtail_packs != 8) else profile_traffic("attn_fwd.cu",
-                                                            f"attn_fwd_{args.workload}.txt")
+    shrunk = args.pack_tokens or args.longtail_packs != 8
+    traffic = None if shrunk else profile_traffic("attn_fwd.cu", f"attn_fwd_{args.workload}.txt")
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -330,7 +333,7 @@ def run_pva(args, rank, world, local):
                    "l2": f"inputs larger than L2: Q+K+V+O+LSE = {io_bytes / 1e9:.2f} GB "
                          f"> {L2_BYTES / 1e6:.0f} MB, no flush",
                    "num_ctas": num_ctas, "c_tile": args.c_tile, "c_tile_fit": fit,
-                   "dispatch": args.dispatch,
+                   "dispatch": args.dispatch, "pack_docs": bool(args.pack_docs),
                    "refine_iters": args.refine_iters,
                    "parallelism": f"{world} independent replica(s), one per GPU"},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
@@ -703,6 +706,8 @@ def main(argv=None):
     ap.add_argument("--dispatch", choices=tuple(DISPATCH), default="dynamic",
                     help="forward units: claimed in LPT order at run time, or the builder's "
                          "static per-CTA LPT lists")
+    ap.add_argument("--pack-docs", action="store_true",
+                    help="short documents share tiles (pva_worklist_params.pack_docs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-zigzag", action="store_true")

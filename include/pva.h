@@ -131,7 +131,13 @@ typedef struct {
                            unit cost = exact allowed pairs
                                        + c_tile * (sub-tiles * kv tiles + sub-tiles) */
     int32_t dispatch;   /* pva_dispatch: how the forward kernel's CTAs take their units */
-    int32_t reserved_;  /* 0 */
+    int32_t pack_docs;  /* 1: short documents share tiles ("03 · 长文负载均衡" §4.1: a block
+                           shorter than a tile is still charged as a whole tile).  CAUSAL and
+                           SLIDING_WINDOW masks: consecutive documents shorter than tile_m are
+                           grouped greedily, in order, into groups of at most tile_m rows; a
+                           group of two or more non-empty documents is one query tile against
+                           one key tile, each row masked to its own document.  Other mask kinds
+                           ignore it.  0: every document has its own tiles. */
 } pva_worklist_params;
 
 /* How the forward kernel hands units to its persistent CTAs.  Both follow the

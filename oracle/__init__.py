@@ -87,7 +87,7 @@ def lib():
         _lib.or_wlb_choose.argtypes = [P, i32, i32, i32, i32, P]
         _lib.or_worklist.restype = ctypes.c_int
         _lib.or_worklist.argtypes = [P, i32, ctypes.POINTER(_Mask), i32, i32, i32, i32, i32,
-                                     i64, i32, P, P, P, P, P, P, P, P]
+                                     i64, i32, i32, P, P, P, P, P, P, P, P, P]
         _lib.or_refine_move_swap.restype = ctypes.c_int
         _lib.or_refine_move_swap.argtypes = [P, i64, i32, P, P, i32]
         _lib.or_fit_tile_cost.restype = i64
@@ -320,20 +320,23 @@ UNIT_FIELDS = ("uid", "seg", "t0", "t1", "h0", "h1", "kvh", "run_begin", "run_co
 
 
 def worklist(cu: np.ndarray, mask: Mask, tile_m: int, tile_n: int, hq: int, hkv: int,
-             num_ctas: int, c_tile: int = 0, refine_iters: int = 0) -> dict:
-    """Worklist of the method (segments, slices, units in CTA order, runs, CSR)."""
+             num_ctas: int, c_tile: int = 0, refine_iters: int = 0, pack_docs: int = 0) -> dict:
+    """Worklist of the method (segments, slices, units in CTA order, runs, CSR).
+    pack_docs: short documents share tiles (packed slices, type 4, with the rows
+    that start a document in "slice_masks" [n, 4] uint32)."""
     cu = np.ascontiguousarray(cu, dtype=np.int32)
     nd = cu.shape[0] - 1
     counts = np.zeros(5, dtype=np.int64)
     m = mask.c()
     L = lib()
     rc = L.or_worklist(_ptr(cu), nd, ctypes.byref(m), tile_m, tile_n, hq, hkv, num_ctas,
-                       int(c_tile), int(refine_iters), _ptr(counts), None, None, None, None,
-                       None, None, None)
+                       int(c_tile), int(refine_iters), int(pack_docs), _ptr(counts), None, None,
+                       None, None, None, None, None, None)
     if rc != 0:
         raise ValueError(f"or_worklist failed ({rc})")
     nseg, nsl, nu, nr = (int(x) for x in counts[:4])
     slices = np.zeros((max(nsl, 1), 8), dtype=np.int32)
+    smasks = np.zeros((max(nsl, 1), 4), dtype=np.uint32)
     segs = np.zeros((max(nseg, 1), 5), dtype=np.int32)
     units = np.zeros((max(nu, 1), 10), dtype=np.int32)
     cost = np.zeros(max(nu, 1), dtype=np.int64)
@@ -341,12 +344,13 @@ def worklist(cu: np.ndarray, mask: Mask, tile_m: int, tile_n: int, hq: int, hkv:
     runs = np.zeros((max(nr, 1), 3), dtype=np.int32)
     off = np.zeros(num_ctas + 1, dtype=np.int32)
     rc = L.or_worklist(_ptr(cu), nd, ctypes.byref(m), tile_m, tile_n, hq, hkv, num_ctas,
-                       int(c_tile), int(refine_iters), _ptr(counts), _ptr(slices), _ptr(segs),
-                       _ptr(units),
+                       int(c_tile), int(refine_iters), int(pack_docs), _ptr(counts),
+                       _ptr(slices), _ptr(smasks), _ptr(segs), _ptr(units),
                        _ptr(cost), _ptr(pairs), _ptr(runs), _ptr(off))
     if rc != 0:
         raise ValueError(f"or_worklist failed ({rc})")
-    return {"slices": slices[:nsl], "segs": segs[:nseg], "units": units[:nu],
+    return {"slices": slices[:nsl], "slice_masks": smasks[:nsl], "segs": segs[:nseg],
+            "units": units[:nu],
             "unit_cost": cost[:nu], "unit_pairs": pairs[:nu], "runs": runs[:nr],
             "cta_off": off, "pairs_per_head": int(counts[4])}
 

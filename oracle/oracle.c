@@ -753,6 +753,7 @@ void or_merge(const double *oa, const double *la, const double *ob, const double
 /* ------------------------------------------------------------------------ */
 typedef struct {
     int32_t q_row0, q_len, q_pos0, k_row0, k_len, k_pos0, type, window;
+    uint32_t dmask[4]; /* packed slices: bit r set when row r starts a document */
 } slice_t;
 
 typedef struct {
@@ -821,22 +822,57 @@ static void derive_zigzag_pair(const int32_t *cu, int32_t ndocs, int32_t cp, int
     }
 }
 
-/* Slices of every mask kind, in the order the worklist enumerates them. */
-static int derive_plan(const int32_t *cu, int32_t ndocs, const or_mask_t *m, plan_t *p) {
+/* Slices of every mask kind, in the order the worklist enumerates them.    */
+/* pack_docs (causal and sliding-window masks): [P1] §4.1 notes that a block */
+/* shorter than a tile is still charged as a whole tile.  Reading: walking   */
+/* the documents in order, a group opens at a document shorter than tile_m   */
+/* and takes the following documents while each is shorter than tile_m and  */
+/* the group's rows stay <= tile_m.  A group with two or more non-empty      */
+/* documents is one segment with one PACKED slice over its rows (positions   */
+/* counted from its first row, every row seeing its own document causally);  */
+/* otherwise its documents keep their own segments.                          */
+static int derive_plan(const int32_t *cu, int32_t ndocs, const or_mask_t *m, plan_t *p,
+                       int32_t pack_docs, int32_t tile_m) {
     memset(p, 0, sizeof *p);
     switch (m->kind) {
     case OR_MASK_CAUSAL:
-    case OR_MASK_SLIDING_WINDOW:
-        for (int32_t d = 0; d < ndocs; ++d) {
+    case OR_MASK_SLIDING_WINDOW: {
+        int32_t w = m->kind == OR_MASK_SLIDING_WINDOW ? m->window : 0;
+        int32_t d = 0;
+        while (d < ndocs) {
             int32_t len = cu[d + 1] - cu[d];
-            if (len <= 0) continue;
-            int64_t first = p->nsl;
-            slice_t s = {cu[d], len, 0, cu[d], len, 0, OR_SLICE_CAUSAL,
-                         m->kind == OR_MASK_SLIDING_WINDOW ? m->window : 0};
-            push_slice(p, s);
-            push_seg(p, cu[d], len, 0, first);
+            int32_t y = d + 1, rows = len, nonempty = len > 0;
+            if (pack_docs && len < tile_m) {
+                while (y < ndocs && cu[y + 1] - cu[y] < tile_m && rows + (cu[y + 1] - cu[y]) <= tile_m) {
+                    rows += cu[y + 1] - cu[y];
+                    nonempty += cu[y + 1] > cu[y];
+                    ++y;
+                }
+            }
+            if (nonempty >= 2) {
+                slice_t s = {cu[d], rows, 0, cu[d], rows, 0, OR_SLICE_PACKED, w, {0, 0, 0, 0}};
+                for (int32_t z = d; z < y; ++z)
+                    if (cu[z + 1] > cu[z]) {
+                        int32_t r = cu[z] - cu[d];
+                        s.dmask[r / 32] |= 1u << (r % 32);
+                    }
+                int64_t first = p->nsl;
+                push_slice(p, s);
+                push_seg(p, cu[d], rows, 0, first);
+            } else {
+                for (int32_t z = d; z < y; ++z) {
+                    int32_t l = cu[z + 1] - cu[z];
+                    if (l <= 0) continue;
+                    int64_t first = p->nsl;
+                    slice_t s = {cu[z], l, 0, cu[z], l, 0, OR_SLICE_CAUSAL, w, {0, 0, 0, 0}};
+                    push_slice(p, s);
+                    push_seg(p, cu[z], l, 0, first);
+                }
+            }
+            d = y;
         }
         return 0;
+    }
     case OR_MASK_SHARED_QUESTION:
         if (m->num_prefix < 0 || m->num_prefix > ndocs) return -1;
         for (int32_t d = 0; d < ndocs; ++d) {
@@ -924,6 +960,15 @@ static void row_interval(const slice_t *s, int32_t r, int64_t *lo, int64_t *hi) 
         l = d;
         h = (int64_t)s->k_len - s->q_len + r + 1;
         break;
+    case OR_SLICE_PACKED: {
+        /* own document: from the nearest document start at or before row r */
+        int32_t st = r;
+        while (st > 0 && !((s->dmask[st / 32] >> (st % 32)) & 1u)) --st;
+        l = st;
+        h = d + 1;
+        if (s->window > 0 && d - s->window + 1 > l) l = d - s->window + 1;
+        break;
+    }
     default: /* FULL */
         break;
     }
@@ -1137,13 +1182,15 @@ int64_t or_fit_tile_cost(const int64_t *P, const int64_t *U, const double *t, in
 
 int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t tile_m,
                 int32_t tile_n, int32_t Hq, int32_t Hkv, int32_t num_ctas, int64_t c_tile,
-                int32_t refine_iters,
-                int64_t *counts, int32_t *slices_out, int32_t *segs_out, int32_t *units_out,
+                int32_t refine_iters, int32_t pack_docs,
+                int64_t *counts, int32_t *slices_out, uint32_t *slice_masks_out,
+                int32_t *segs_out, int32_t *units_out,
                 int64_t *unit_cost_out, int64_t *unit_pairs_out, int32_t *runs_out,
                 int32_t *cta_off_out) {
     if (tile_m <= 0 || tile_n <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_ctas <= 0) return -1;
+    if (pack_docs && tile_m > 128) return -1; /* a packed slice's rows fit one 128-bit mask */
     plan_t p;
-    if (derive_plan(cu, ndocs, m, &p) != 0) {
+    if (derive_plan(cu, ndocs, m, &p, pack_docs, tile_m) != 0) {
         free(p.sl);
         free(p.sg);
         return -2;
@@ -1179,6 +1226,8 @@ int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t ti
         int32_t *o = slices_out + 8 * i;
         o[0] = s->q_row0; o[1] = s->q_len; o[2] = s->q_pos0; o[3] = s->k_row0;
         o[4] = s->k_len; o[5] = s->k_pos0; o[6] = s->type; o[7] = s->window;
+        if (slice_masks_out)
+            for (int e = 0; e < 4; ++e) slice_masks_out[4 * i + e] = s->dmask[e];
     }
     for (int64_t g = 0; g < p.nsg; ++g) {
         int32_t *o = segs_out + 5 * g;

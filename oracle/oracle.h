@@ -20,7 +20,8 @@ enum {
     OR_MASK_SLICES = 4,
     OR_MASK_ZIGZAG_STEP = 5
 };
-enum { OR_SLICE_FULL = 0, OR_SLICE_CAUSAL = 1, OR_SLICE_INV_CAUSAL = 2, OR_SLICE_BI_CAUSAL = 3 };
+enum { OR_SLICE_FULL = 0, OR_SLICE_CAUSAL = 1, OR_SLICE_INV_CAUSAL = 2, OR_SLICE_BI_CAUSAL = 3,
+       OR_SLICE_PACKED = 4 /* short documents sharing one tile (worklist only) */ };
 
 typedef struct {
     int32_t kind;
@@ -62,8 +63,9 @@ int64_t or_fit_tile_cost(const int64_t *P, const int64_t *U, const double *t, in
                          double *coef);
 int or_worklist(const int32_t *cu, int32_t ndocs, const or_mask_t *m, int32_t tile_m,
                 int32_t tile_n, int32_t Hq, int32_t Hkv, int32_t num_ctas, int64_t c_tile,
-                int32_t refine_iters,
-                int64_t *counts, int32_t *slices_out, int32_t *segs_out, int32_t *units_out,
+                int32_t refine_iters, int32_t pack_docs,
+                int64_t *counts, int32_t *slices_out, uint32_t *slice_masks_out,
+                int32_t *segs_out, int32_t *units_out,
                 int64_t *unit_cost_out, int64_t *unit_pairs_out, int32_t *runs_out,
                 int32_t *cta_off_out);
 

@@ -50,7 +50,7 @@ class WorklistParams(ctypes.Structure):
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("num_ctas", ctypes.c_int32), ("refine_iters", ctypes.c_int32),
                 ("c_tile", ctypes.c_int64), ("dispatch", ctypes.c_int32),
-                ("reserved_", ctypes.c_int32)]
+                ("pack_docs", ctypes.c_int32)]
 
 
 class PvaError(RuntimeError):

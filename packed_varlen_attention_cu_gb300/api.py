@@ -68,10 +68,12 @@ def default_c_tile(head_dim: int) -> int:
 
 def make_params(num_q_heads: int, num_kv_heads: int, num_ctas: int = 0, c_tile: int = 0,
                 tile_m: int = TILE, tile_n: int = TILE, refine_iters: int = 0,
-                dispatch: int = DISPATCH_DYNAMIC) -> WorklistParams:
+                dispatch: int = DISPATCH_DYNAMIC, pack_docs: int = 0) -> WorklistParams:
+    """pva_worklist_params.  pack_docs = 1: short documents share tiles."""
     p = WorklistParams()
     p.refine_iters = refine_iters
     p.dispatch = dispatch
+    p.pack_docs = pack_docs
     p.tile_m, p.tile_n = tile_m, tile_n
     p.num_q_heads, p.num_kv_heads = num_q_heads, num_kv_heads
     p.num_ctas, p.c_tile = num_ctas, c_tile
@@ -341,9 +343,9 @@ def worklist_counts(worklist: torch.Tensor, stream=None) -> dict:
 
 # ----------------------------------------------------------------- decoding
 _HDR = np.dtype([("i32", "<i4", 20), ("c_tile", "<i8"), ("pair_sum", "<u8"), ("tile_sum", "<u8"),
-                 ("off", "<i8", 13)])
+                 ("off", "<i8", 14)])
 _OFF = ("slices", "segs", "units_enum", "keys", "order", "assign", "units", "runs",
-        "cta_off", "doc_scan", "dorder", "cls_work", "total")
+        "cta_off", "doc_scan", "dorder", "cls_work", "smask", "total")
 
 
 def decode_worklist(worklist: torch.Tensor) -> dict:
@@ -361,8 +363,8 @@ def decode_worklist(worklist: torch.Tensor) -> dict:
     hd = {n: int(x) for n, x in zip(names, i32)}
     off = {n: int(x) for n, x in zip(_OFF, h["off"])}
     # after the offsets: lpt_steps, refine_iters, refine_rounds, dispatch_next,
-    # dispatch_done, dispatch, dispatch_split
-    tail = np.frombuffer(raw[_HDR.itemsize:_HDR.itemsize + 28].tobytes(), dtype="<i4")
+    # dispatch_done, dispatch, dispatch_split, pack_docs
+    tail = np.frombuffer(raw[_HDR.itemsize:_HDR.itemsize + 32].tobytes(), dtype="<i4")
     dispatch = tail[5]
 
     def arr(name, dtype, n, width):
@@ -377,6 +379,8 @@ def decode_worklist(worklist: torch.Tensor) -> dict:
     pairs = units[:, 14:16].copy().view("<i8").reshape(-1)
     return {"header": hd, "pair_sum": int(h["pair_sum"]), "tile_sum": int(h["tile_sum"]),
             "slices": arr("slices", "<i4", hd["nslices"], 8),
+            "slice_masks": arr("smask", "<u4", hd["nslices"], 4),
+            "pack_docs": int(tail[7]),
             "segs": arr("segs", "<i4", hd["nsegs"], 8),
             "units": units[:, :10].copy(), "unit_ntiles": units[:, 10].copy(),
             "unit_cost": costs, "unit_pairs": pairs,

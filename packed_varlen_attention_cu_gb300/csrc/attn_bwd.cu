@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const WlRun run = runs[u.run_begin + rr];
                     const WlSlice s = slices[run.slice];
                     int64_t klo, khi;  // allowed keys of this row (slice-local)
-                    slice_keys_of_query(s, q_pos, klo, khi);
+                    slice_keys_of_query(s, q_pos, klo, khi, slice_mask(p.wl, h, s, run.slice));
                     const int32_t lim_hi = valid ? (int32_t)khi : 0;
                     const int32_t lim_lo = (int32_t)klo;
                     for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int32_t m = 0; m < u.gcount && live; ++m) {
                         const WlSlice sm = slices[gsl[u.gbegin + m]];
                         int32_t qlo, qhi;
-                        bwd_q_span(sm, u.kt, qlo, qhi);
+                        bwd_q_span(sm, u.kt, qlo, qhi, slice_mask(p.wl, h, sm, gsl[u.gbegin + m]));
                         for (int32_t t = qlo; t < qhi && live; ++t) {
                             const int32_t nq = min(128, sm.q_len - t * 128);
                             const int32_t halves = nq > 64 ? 2 : 1;
@@ -764,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int32_t m = 0; m < u.gcount && live; ++m) {
                     const WlSlice sm = slices[gsl[u.gbegin + m]];
                     int32_t qlo, qhi;
-                    bwd_q_span(sm, u.kt, qlo, qhi);
+                    bwd_q_span(sm, u.kt, qlo, qhi, slice_mask(p.wl, h, sm, gsl[u.gbegin + m]));
                     for (int32_t t = qlo; t < qhi && live; ++t) {
                         const int32_t nq = min(128, sm.q_len - t * 128);
                         const uint32_t halves = nq > 64 ? 2 : 1;
@@ -836,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int32_t m = 0; m < u.gcount && live; ++m) {
                     const WlSlice s = slices[gsl[u.gbegin + m]];
                     int32_t qlo, qhi;
-                    bwd_q_span(s, u.kt, qlo, qhi);
+                    bwd_q_span(s, u.kt, qlo, qhi, slice_mask(p.wl, h, s, gsl[u.gbegin + m]));
                     for (int32_t t = qlo; t < qhi && live; ++t) {
                         const int32_t qrow0 = s.q_row0 + t * 128;
                         const int32_t nq = min(128, s.q_len - t * 128);
@@ -896,11 +896,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int32_t hh = 0; hh < G && live; ++hh) {
                 for (int32_t m = 0; m < u.gcount && live; ++m) {
                 const WlSlice s = slices[gsl[u.gbegin + m]];
+                const uint32_t* pm = slice_mask(p.wl, h, s, gsl[u.gbegin + m]);
                 const int32_t k_pos = s.k_pos0 + u.kt * 128 + kr;
                 int64_t qa, qb;  // query positions that may see this key
-                slice_queries_of_key(s, k_pos, qa, qb);
+                slice_queries_of_key(s, k_pos, qa, qb, pm);
                 int32_t qlo, qhi;
-                bwd_q_span(s, u.kt, qlo, qhi);
+                bwd_q_span(s, u.kt, qlo, qhi, pm);
                 for (int32_t t = qlo; t < qhi && live; ++t) {
                     // this q tile's rows: query c has position q_pos0 + t*128 + c
                     const int32_t nq = min(128, s.q_len - t * 128);

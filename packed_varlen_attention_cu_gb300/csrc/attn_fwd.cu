@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // allowed keys of this row, relative to the slice's first key:
                 // [lim_lo, lim_hi) (by the slice's MaskType; nothing for padding rows)
                 int64_t klo, khi;
-                slice_keys_of_query(s, q_pos, klo, khi);
+                slice_keys_of_query(s, q_pos, klo, khi, slice_mask(p.wl, h, s, run.slice));
                 const int32_t lim_hi = valid ? (int32_t)khi : 0;
                 const int32_t lim_lo = (int32_t)klo;
                 for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {

@@ -13,9 +13,10 @@
 //   units      WlUnit[cap_units]          units grouped by CTA, in enumeration order inside a CTA
 //   runs       WlRun[cap_runs]            per unit and slice: kv tile span [lo, hi)
 //   cta_off    int32[num_ctas + 1]        CSR offsets of the CTAs into `units`
-//   doc_scan   int32[4 * (num_docs + 1)]  per-document scan scratch
+//   doc_scan   int32[6 * (items + 1)]     per-document (or per rank and document) scan scratch
 //   dorder     int32[cap_units]           uid of the r-th unit in dispatch order
 //   cls_work   uint64[64]                 summed cost per dispatch class
+//   smask      uint32[cap_slices][4]      per packed slice: rows that start a document
 // A worklist built for dynamic dispatch has no LPT bins: order, assign,
 // units and cta_off are left unwritten (units_enum and dorder describe it).
 #pragma once
@@ -33,6 +34,53 @@ constexpr int kCostBits = 40;  // unit cost < 2^40
 struct WlSlice {
     int32_t q_row0, q_len, q_pos0, k_row0, k_len, k_pos0, type, window;
 };
+
+// Slice type of a tile shared by several short documents (built by the
+// worklist, never passed in by a caller): a group of consecutive documents,
+// each shorter than a tile, whose rows fit in one tile.  Its q and k ranges
+// are the group's rows, positions count from the group's first row, and a
+// row sees the keys of its own document at positions <= its own (and inside
+// the window, if any).  Bit r of the slice's 128-bit smask entry is set when
+// row r starts a document.
+constexpr int32_t kSlicePacked = 4;
+
+// First row of the document holding row r (0 <= r < 128) of a packed slice.
+__host__ __device__ inline int32_t packed_doc_start(const uint32_t* m, int32_t r) {
+    for (int32_t w = r >> 5; w >= 0; --w) {
+        uint32_t bits = m[w];
+        if (w == (r >> 5)) bits &= (r & 31) == 31 ? 0xffffffffu : ((2u << (r & 31)) - 1u);
+        if (bits) {
+#ifdef __CUDA_ARCH__
+            return w * 32 + 31 - __clz(bits);
+#else
+            int32_t b = 31;
+            while (!(bits >> b)) --b;
+            return w * 32 + b;
+#endif
+        }
+    }
+    return 0;
+}
+
+// One past the last row of the document holding row r of a packed slice of
+// `len` rows.
+__host__ __device__ inline int32_t packed_doc_end(const uint32_t* m, int32_t r, int32_t len) {
+    for (int32_t w = (r + 1) >> 5; w < 4 && w * 32 < len; ++w) {
+        uint32_t bits = m[w];
+        if (w == ((r + 1) >> 5)) bits &= ~((1u << ((r + 1) & 31)) - 1u);
+        if (bits) {
+#ifdef __CUDA_ARCH__
+            const int32_t b = w * 32 + __ffs(bits) - 1;
+#else
+            int32_t z = 0;
+            while (!((bits >> z) & 1u)) ++z;
+            const int32_t b = w * 32 + z;
+#endif
+            return b < len ? b : len;
+        }
+    }
+    return len;
+}
 
 struct WlSeg {
     int32_t q_row0, q_len, q_pos0, slice_begin, slice_count, unit_base, run_base, ntiles;
@@ -69,7 +117,7 @@ struct WlRun {
 
 struct WlOffsets {
     int64_t slices, segs, units_enum, keys, order, assign, units, runs, cta_off, doc_scan, dorder,
-        cls_work, total;
+        cls_work, smask, total;
 };
 
 struct WlHeader {
@@ -93,7 +141,7 @@ struct WlHeader {
     int32_t dispatch_next, dispatch_done;
     int32_t dispatch;  // pva_dispatch the worklist was built for (dorder exists if DYNAMIC)
     int32_t dispatch_split;  // classes <= this one are dispatched in exact LPT order
-    int32_t pad_[1];
+    int32_t pack_docs;       // short documents share tiles (pva_worklist_params.pack_docs)
 };
 static_assert(sizeof(WlHeader) <= 256, "header fits in 256 bytes");
 
@@ -127,13 +175,18 @@ static_assert(sizeof(BwdHeader) <= 256, "backward header fits in 256 bytes");
 // INV_CAUSAL k >= q (each with an optional window |q - k| < w), BI_CAUSAL
 // k >= q and k_end - k >= q_end - q.
 // Keys of slice s a query at position qp may see, as slice-local key indices
-// [lo, hi) (empty when hi <= lo).
+// [lo, hi) (empty when hi <= lo).  pm: the slice's smask entry (packed slices).
 __host__ __device__ inline void slice_keys_of_query(const WlSlice& s, int64_t qp, int64_t& lo,
-                                                    int64_t& hi) {
+                                                    int64_t& hi, const uint32_t* pm = nullptr) {
     const int64_t d = qp - s.k_pos0;  // local index of the key at the query's position
     lo = 0;
     hi = s.k_len;
-    if (s.type == 1) {  // CAUSAL
+    if (s.type == kSlicePacked) {  // own document, causal (positions = rows of the group)
+        const int32_t r = (int32_t)(qp - s.q_pos0);
+        lo = pm ? packed_doc_start(pm, r) : r;
+        hi = d + 1;
+        if (s.window > 0 && d - s.window + 1 > lo) lo = d - s.window + 1;
+    } else if (s.type == 1) {  // CAUSAL
         hi = d + 1;
         if (s.window > 0) lo = d - s.window + 1;
     } else if (s.type == 2) {  // INV_CAUSAL
@@ -150,11 +203,16 @@ __host__ __device__ inline void slice_keys_of_query(const WlSlice& s, int64_t qp
 // Query positions [lo, hi) of slice s that may see a key at position kp (both
 // ends are non-decreasing in kp for every type).
 __host__ __device__ inline void slice_queries_of_key(const WlSlice& s, int64_t kp, int64_t& lo,
-                                                     int64_t& hi) {
+                                                     int64_t& hi, const uint32_t* pm = nullptr) {
     lo = s.q_pos0;
     hi = (int64_t)s.q_pos0 + s.q_len;
     int64_t a = lo, b = hi;
-    if (s.type == 1) {  // CAUSAL
+    if (s.type == kSlicePacked) {  // the key's document, from the key's position on
+        const int32_t j = (int32_t)(kp - s.k_pos0);
+        a = kp;
+        b = (int64_t)s.q_pos0 + (pm ? packed_doc_end(pm, j, s.q_len) : j + 1);
+        if (s.window > 0 && kp + s.window < b) b = kp + s.window;
+    } else if (s.type == 1) {  // CAUSAL
         a = kp;
         if (s.window > 0) b = kp + s.window;
     } else if (s.type == 2) {  // INV_CAUSAL
@@ -171,17 +229,25 @@ __host__ __device__ inline void slice_queries_of_key(const WlSlice& s, int64_t k
 // q tiles [qlo, qhi) of slice `sl` (aligned at its query start, like the
 // forward) holding a row that may see a key of key tile kt of the slice.
 __host__ __device__ inline void bwd_q_span(const WlSlice& sl, int32_t kt, int32_t& qlo,
-                                           int32_t& qhi) {
+                                           int32_t& qhi, const uint32_t* pm = nullptr) {
     const int32_t ka = kt * 128, kb = (sl.k_len < ka + 128) ? sl.k_len : ka + 128;
     qlo = qhi = 0;
     if (kb <= ka) return;
     int64_t a0, a1, b0, b1;
-    slice_queries_of_key(sl, (int64_t)sl.k_pos0 + ka, a0, a1);
-    slice_queries_of_key(sl, (int64_t)sl.k_pos0 + kb - 1, b0, b1);
+    slice_queries_of_key(sl, (int64_t)sl.k_pos0 + ka, a0, a1, pm);
+    slice_queries_of_key(sl, (int64_t)sl.k_pos0 + kb - 1, b0, b1, pm);
     const int64_t r_lo = a0 - sl.q_pos0, r_hi = b1 - sl.q_pos0;
     if (r_hi <= r_lo) return;
     qlo = (int32_t)(r_lo / 128);
     qhi = (int32_t)((r_hi + 127) / 128);
+}
+
+// The smask entry of slice `si` if it is a packed slice, else nullptr.
+__host__ __device__ inline const uint32_t* slice_mask(const uint8_t* wl, const WlHeader* h,
+                                                      const WlSlice& s, int32_t si) {
+    return s.type == kSlicePacked
+               ? reinterpret_cast<const uint32_t*>(wl + h->off.smask) + 4 * (int64_t)si
+               : nullptr;
 }
 
 // Device error codes (stored in WlHeader::error).

@@ -89,7 +89,7 @@ struct PlanArgs {
     uint8_t* base;
     const int32_t* cu;
     int32_t num_docs, kind, window, num_prefix, cp, q_rank, k_rank, num_slices;
-    int32_t tile_m, hq, hkv, q_tokens, k_tokens, ring_step;
+    int32_t tile_m, hq, hkv, q_tokens, k_tokens, ring_step, pack_docs;
 };
 
 __device__ __forceinline__ void set_error(WlHeader* h, int32_t code) { atomicCAS(&h->error, 0, code); }
@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
     WlSlice* slices = reinterpret_cast<WlSlice*>(a.base + a.hinit.off.slices);
     WlSeg* segs = reinterpret_cast<WlSeg*>(a.base + a.hinit.off.segs);
     int32_t* scan = reinterpret_cast<int32_t*>(a.base + a.hinit.off.doc_scan);
+    uint32_t* smask = reinterpret_cast<uint32_t*>(a.base + a.hinit.off.smask);
     const int tid = threadIdx.x;
     const int nd = a.num_docs;
     __shared__ int32_t sm4[32][4];
@@ -143,6 +144,42 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
             qr = ring ? i / nd : a.q_rank;
             kr = ring ? (qr - a.ring_step + a.cp) % a.cp : a.k_rank;
         };
+        // Short documents sharing tiles (per-document masks, pack_docs): a run of
+        // consecutive documents shorter than a tile is cut greedily, in order,
+        // into groups of at most tile_m rows; a group holding two or more
+        // non-empty documents becomes one query segment with one packed slice.
+        // grp[d]: first document of d's packed group (-1: d is not packed);
+        // gend[head]: one past the group's last document.
+        int32_t* grp = scan + 4 * (items + 1);
+        int32_t* gend = scan + 5 * (items + 1);
+        const bool pack = a.pack_docs != 0 &&
+                          (a.kind == PVA_MASK_CAUSAL || a.kind == PVA_MASK_SLIDING_WINDOW);
+        if (pack) {
+            auto short_doc = [&](int32_t d) { return a.cu[d + 1] - a.cu[d] < a.tile_m; };
+            for (int d = tid; d < nd; d += kPlanThreads) {
+                if (!short_doc(d)) {
+                    grp[d] = -1;
+                    continue;
+                }
+                if (d > 0 && short_doc(d - 1)) continue;  // not the first of its run
+                // this thread cuts the whole run of short documents starting at d
+                int32_t x = d;
+                while (x < nd && short_doc(x)) {
+                    const int32_t head = x;
+                    int32_t rows = a.cu[x + 1] - a.cu[x], nonempty = rows > 0, y = x + 1;
+                    while (y < nd && short_doc(y) && rows + (a.cu[y + 1] - a.cu[y]) <= a.tile_m) {
+                        const int32_t l = a.cu[y + 1] - a.cu[y];
+                        rows += l;
+                        nonempty += l > 0;
+                        ++y;
+                    }
+                    for (int32_t z = head; z < y; ++z) grp[z] = nonempty >= 2 ? head : -1;
+                    if (nonempty >= 2) gend[head] = y;
+                    x = y;
+                }
+            }
+            __syncthreads();
+        }
         // pass 1: per-item segment / slice counts and zigzag local offsets
         for (int i0 = 0; i0 < items; i0 += kPlanThreads) {
             const int i = i0 + tid;
@@ -151,7 +188,8 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
                 const int d = ring ? i % nd : i;
                 const int32_t len = a.cu[d + 1] - a.cu[d];
                 if (a.kind == PVA_MASK_CAUSAL || a.kind == PVA_MASK_SLIDING_WINDOW) {
-                    v[0] = v[1] = len > 0;
+                    if (pack && grp[d] >= 0) v[0] = v[1] = grp[d] == d;  // the group's head
+                    else v[0] = v[1] = len > 0;
                 } else if (a.kind == PVA_MASK_SHARED_QUESTION) {
                     v[0] = len > 0;
                     v[1] = len > 0 ? (d >= a.num_prefix ? s_npref + 1 : 1) : 0;
@@ -205,8 +243,23 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
             const int32_t len = a.cu[d + 1] - a.cu[d];
             int32_t sg = scan[i], sl = scan[(items + 1) + i];
             if (a.kind == PVA_MASK_CAUSAL || a.kind == PVA_MASK_SLIDING_WINDOW) {
-                if (len <= 0) continue;
                 const int32_t w = a.kind == PVA_MASK_SLIDING_WINDOW ? a.window : 0;
+                if (pack && grp[d] >= 0) {
+                    if (grp[d] != d) continue;
+                    // the group [d, gend[d]): its rows, and the rows that start a document
+                    const int32_t g0 = a.cu[d], rows = a.cu[gend[d]] - g0;
+                    uint32_t m[4] = {0u, 0u, 0u, 0u};
+                    for (int32_t z = d; z < gend[d]; ++z)
+                        if (a.cu[z + 1] > a.cu[z]) {
+                            const int32_t r = a.cu[z] - g0;
+                            m[r >> 5] |= 1u << (r & 31);
+                        }
+                    slices[sl] = WlSlice{g0, rows, 0, g0, rows, 0, kSlicePacked, w};
+                    reinterpret_cast<uint4*>(smask)[sl] = make_uint4(m[0], m[1], m[2], m[3]);
+                    segs[sg] = WlSeg{g0, rows, 0, sl, 1, 0, 0, 0};
+                    continue;
+                }
+                if (len <= 0) continue;
                 slices[sl] = WlSlice{a.cu[d], len, 0, a.cu[d], len, 0, PVA_SLICE_CAUSAL, w};
                 segs[sg] = WlSeg{a.cu[d], len, 0, sl, 1, 0, 0, 0};
             } else if (a.kind == PVA_MASK_SHARED_QUESTION) {
@@ -344,14 +397,15 @@ __global__ void __launch_bounds__(kPlanThreads) wl_plan_kernel(PlanArgs a) {
 
 // kv-tile span [lo_t, hi_t) and allowed-pair count of q tile t against slice
 // s, by the whole warp: lane l takes rows r0 + l, r0 + l + 32, ...
-__device__ void tile_span_warp(const WlSeg& g, const WlSlice& s, int32_t t, int32_t tile_m,
-                               int32_t tile_n, int32_t& lo_t, int32_t& hi_t, long long& pairs) {
+__device__ void tile_span_warp(const WlSeg& g, const WlSlice& s, const uint32_t* pm, int32_t t,
+                               int32_t tile_m, int32_t tile_n, int32_t& lo_t, int32_t& hi_t,
+                               long long& pairs) {
     long long mn = 0x7fffffffffffffffLL, mx = -1, cnt = 0;
     const int32_t r0 = t * tile_m;
     const int32_t r1 = min(r0 + tile_m, g.q_len);
     for (int32_t r = r0 + (int32_t)(threadIdx.x & 31); r < r1; r += 32) {
         int64_t lo, hi;
-        slice_keys_of_query(s, (int64_t)s.q_pos0 + r, lo, hi);
+        slice_keys_of_query(s, (int64_t)s.q_pos0 + r, lo, hi, pm);
         if (hi <= lo) continue;
         cnt += hi - lo;
         mn = lo < mn ? lo : mn;
@@ -441,13 +495,14 @@ __global__ void __launch_bounds__(kUnitWarps * 32) wl_units_kernel(UnitArgs a) {
         int32_t ntiles = 0;
         for (int32_t si = 0; si < g.slice_count; ++si) {
             const WlSlice sl = slices[g.slice_begin + si];
+            const uint32_t* pm = slice_mask(a.base, h, sl, g.slice_begin + si);
             int32_t rlo = 0, rhi = 0;
             bool have = false;
             const int32_t ts[2] = {w.t0, w.t1};
             for (int k = 0; k < nsub; ++k) {
                 int32_t a0, b0;
                 long long pr;
-                tile_span_warp(g, sl, ts[k], a.tile_m, a.tile_n, a0, b0, pr);
+                tile_span_warp(g, sl, pm, ts[k], a.tile_m, a.tile_n, a0, b0, pr);
                 pairs += pr;
                 if (b0 > a0) {
                     if (!have || a0 < rlo) rlo = a0;
@@ -1062,7 +1117,8 @@ __global__ void __launch_bounds__(kBwdPlanThreads)
             int64_t steps = 0;
             for (int32_t m = 0; m < gcount; ++m) {
                 int32_t qlo, qhi;
-                bwd_q_span(slices[sidx[i + m]], kt, qlo, qhi);
+                const WlSlice& sm = slices[sidx[i + m]];
+                bwd_q_span(sm, kt, qlo, qhi, slice_mask(wl, h, sm, sidx[i + m]));
                 steps += qhi - qlo;
             }
             for (int32_t g = 0; g < hkv; ++g) {
@@ -1099,7 +1155,8 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     if (p->tile_m <= 0 || p->tile_n <= 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
         p->num_q_heads % p->num_kv_heads != 0 || p->c_tile < 0 || p->refine_iters < 0 ||
         p->refine_iters > 1000 || (p->dispatch != PVA_DISPATCH_DYNAMIC &&
-                                   p->dispatch != PVA_DISPATCH_STATIC))
+                                   p->dispatch != PVA_DISPATCH_STATIC) ||
+        (p->pack_docs != 0 && p->pack_docs != 1) || (p->pack_docs && p->tile_m > 128))
         return false;
     if (num_ctas <= 0 || num_ctas > kMaxBins) return false;
     if (m->q_tokens < 0 || m->k_tokens < 0) return false;
@@ -1196,6 +1253,8 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     h->refine_iters = p->refine_iters;
     h->refine_rounds = 0;
     h->dispatch = p->dispatch;
+    h->pack_docs =
+        p->pack_docs && (m->kind == PVA_MASK_CAUSAL || m->kind == PVA_MASK_SLIDING_WINDOW) ? 1 : 0;
     int64_t o = 256;
     WlOffsets& f = h->off;
     f.slices = o; o = align256(o + (int64_t)h->cap_slices * sizeof(WlSlice));
@@ -1207,9 +1266,10 @@ bool plan_layout(int32_t num_docs, const pva_mask_desc* m, const pva_worklist_pa
     f.units = o; o = align256(o + cap_units * (int64_t)sizeof(WlUnit));
     f.runs = o; o = align256(o + (int64_t)h->cap_runs * sizeof(WlRun));
     f.cta_off = o; o = align256(o + ((int64_t)num_ctas + 1) * 4);
-    f.doc_scan = o; o = align256(o + 4 * (scan_items + 1) * 4);
+    f.doc_scan = o; o = align256(o + 6 * (scan_items + 1) * 4);
     f.dorder = o; o = align256(o + cap_units * 4);
     f.cls_work = o; o = align256(o + 64 * 8);
+    f.smask = o; o = align256(o + (int64_t)h->cap_slices * 16);
     f.total = o;
     return true;
 }
@@ -1279,6 +1339,7 @@ extern "C" pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t 
     pa.q_tokens = mask->q_tokens;
     pa.k_tokens = mask->k_tokens;
     pa.ring_step = mask->ring_step;
+    pa.pack_docs = h.pack_docs;
     wl_plan_kernel<<<1, kPlanThreads, 0, st>>>(pa);
     UnitArgs ua{base, params->tile_m, params->tile_n, params->num_q_heads, params->num_kv_heads,
                 (long long)params->c_tile};

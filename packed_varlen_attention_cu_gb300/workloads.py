@@ -127,6 +127,14 @@ def sliding_window() -> Workload:
                     mask_kind=MASK_SLIDING_WINDOW, window=4096)
 
 
+def short_docs(seed: int = 0) -> Workload:
+    """131072-token pack of short documents (lognormal median 64, sigma 0.75, clip [8, 512]),
+    32 q / 8 kv heads, d=128: many documents shorter than a 128-row tile."""
+    return Workload("short-document pack T=131072 H=32/8 d=128",
+                    lognormal_doc_lengths(131072, math.log(64.0), 0.75, 8, 512, seed),
+                    32, 8, 128, seed=seed)
+
+
 def make_qkv(total_q: int, total_k: int, hq: int, hkv: int, d: int, seed: int,
              scale: float = 1.0, device: str = "cpu"):
     """bf16 Q [Tq,Hq,d], K and V [Tk,Hkv,d] drawn N(0,1)*scale from a seeded generator."""

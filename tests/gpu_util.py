@@ -51,11 +51,12 @@ def compare(out, lse, ref_o, ref_l, label=""):
 
 
 def run_gpu(q, k, v, cu_np, mask, hq, hkv, num_ctas=0, c_tile=0, out_fp32=False, scale=0.0,
-            dispatch=api.DISPATCH_DYNAMIC):
+            dispatch=api.DISPATCH_DYNAMIC, pack_docs=0):
     """Build the worklist and run the forward; returns (out, lse, worklist)."""
     dev = torch.device("cuda")
     cu = torch.from_numpy(np.ascontiguousarray(cu_np, dtype=np.int32)).to(dev)
-    params = api.make_params(hq, hkv, num_ctas=num_ctas, c_tile=c_tile, dispatch=dispatch)
+    params = api.make_params(hq, hkv, num_ctas=num_ctas, c_tile=c_tile, dispatch=dispatch,
+                             pack_docs=pack_docs)
     wl = api.alloc_worklist(cu.numel() - 1, mask, params, dev)
     api.build_worklist(cu, mask, params, wl)
     tq, _, d = q.shape

@@ -18,10 +18,12 @@ from gpu_util import oracle_mask
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_worklist(cu_np, mask, hq, hkv, num_ctas, c_tile, dispatch=api.DISPATCH_STATIC):
+def _gpu_worklist(cu_np, mask, hq, hkv, num_ctas, c_tile, dispatch=api.DISPATCH_STATIC,
+                  pack_docs=0):
     dev = torch.device("cuda")
     cu = torch.from_numpy(np.ascontiguousarray(cu_np, dtype=np.int32)).to(dev)
-    params = api.make_params(hq, hkv, num_ctas=num_ctas, c_tile=c_tile, dispatch=dispatch)
+    params = api.make_params(hq, hkv, num_ctas=num_ctas, c_tile=c_tile, dispatch=dispatch,
+                             pack_docs=pack_docs)
     wl = api.alloc_worklist(cu.numel() - 1, mask, params, dev)
     api.build_worklist(cu, mask, params, wl)
     torch.cuda.synchronize()
@@ -45,6 +47,8 @@ def _assert_same(g, o):
     else:
         np.testing.assert_array_equal(g["cta_off"], o["cta_off"])
     np.testing.assert_array_equal(g["slices"], o["slices"].reshape(-1, 8))
+    packed = o["slices"].reshape(-1, 8)[:, 6] == 4  # short documents sharing a tile
+    np.testing.assert_array_equal(g["slice_masks"][packed], o["slice_masks"][packed])
     np.testing.assert_array_equal(g["segs"][:, :5], o["segs"].reshape(-1, 5))
     np.testing.assert_array_equal(g["units"], ou)
     np.testing.assert_array_equal(g["unit_cost"], oc)
@@ -268,3 +272,29 @@ def test_fit_tile_cost_matches_oracle(oracle_mod):
     assert ct == oct_
     np.testing.assert_allclose(coef, ocoef, rtol=1e-9, atol=1e-12)
     assert 0 <= ct <= 1 << 24 and max(coef) > 0 and min(coef) >= 0
+
+
+PACK_CASES = [
+    ("tiny", lambda: W.tiny_pack(), W.MASK_CAUSAL, 0),
+    ("short docs", lambda: W.Workload("short docs", [5, 130, 1, 9, 0, 12, 3, 128, 40, 40, 40,
+                                                     8, 15, 127, 1] * 6, 4, 2, 64), W.MASK_CAUSAL, 0),
+    ("short docs window", lambda: W.Workload("short docs window", [30, 2, 2, 0, 60, 61, 7, 300, 1]
+                                             * 5, 6, 2, 128), W.MASK_SLIDING_WINDOW, 17),
+    ("long-tail 2 packs", lambda: W.long_tail_gqa(2), W.MASK_CAUSAL, 0),
+]
+
+
+@pytest.mark.parametrize("name,mk,kind,window", PACK_CASES, ids=[c[0] for c in PACK_CASES])
+@pytest.mark.parametrize("dispatch", [api.DISPATCH_STATIC, api.DISPATCH_DYNAMIC])
+def test_worklist_packed_short_docs_bit_exact(oracle_mod, name, mk, kind, window, dispatch):
+    w = mk()
+    cu = w.cu_seqlens
+    T = w.total_tokens
+    mask = api.make_mask(kind, T, T, window=window)
+    g, counts = _gpu_worklist(cu, mask, w.num_q_heads, w.num_kv_heads, 13, 7, dispatch,
+                              pack_docs=1)
+    o = oracle_mod.worklist(cu, oracle_mask(kind, window), 128, 128, w.num_q_heads,
+                            w.num_kv_heads, 13, 7, pack_docs=1)
+    assert g["pack_docs"] == 1
+    _assert_same(g, o)
+    assert counts["pairs_per_head"] == o["pairs_per_head"]

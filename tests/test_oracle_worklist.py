@@ -16,13 +16,17 @@ import pytest
 from packed_varlen_attention_cu_gb300 import workloads as W
 
 
-def slice_accepts(sl, i, j):
+def slice_accepts(sl, i, j, smask=None):
     q_row0, q_len, q_pos0, k_row0, k_len, k_pos0, typ, win = (int(x) for x in sl)
     if not (q_row0 <= i < q_row0 + q_len and k_row0 <= j < k_row0 + k_len):
         return False
     if typ == 0:
         return True
     qp, kp = q_pos0 + i - q_row0, k_pos0 + j - k_row0
+    if typ == 4:  # packed: the row's own document (rows that start one are flagged)
+        starts = [r for r in range(q_len) if (int(smask[r // 32]) >> (r % 32)) & 1]
+        if max(st for st in starts if st <= qp) > kp:
+            return False
     return kp <= qp and (win <= 0 or qp - kp < win)
 
 
@@ -38,6 +42,7 @@ def coverage(wl, tq, tk, hq, tile_m, tile_n):
         for r in range(rb, rb + rc):
             sidx, lo, hi = (int(x) for x in wl["runs"][r])
             sl = wl["slices"][sidx]
+            sm = wl["slice_masks"][sidx] if "slice_masks" in wl else None
             assert sl[0] == sg[0] and sl[1] == sg[1]
             for kt in range(lo, hi):
                 k0 = sl[3] + kt * tile_n
@@ -48,7 +53,7 @@ def coverage(wl, tq, tk, hq, tile_m, tile_n):
                     r1 = min(r0 + tile_m, sg[0] + sg[1])
                     for i in range(r0, r1):
                         for j in range(k0, k1):
-                            if slice_accepts(sl, i, j):
+                            if slice_accepts(sl, i, j, sm):
                                 cov[h, i, j] += 1
                                 cnt += 1
                                 hit += 1
@@ -242,3 +247,56 @@ def test_dispatch_order_list_scheduling_within_graham_bound(oracle_mod):
         srt = sorted(range(n), key=lambda u: (-int(costs[u]), u))
         if order.tolist() == srt:
             assert span * 3 * m <= (4 * m - 1) * opt + 1e-9
+
+
+# ------------------------------------------------------ short documents sharing tiles
+def test_packed_groups_hand_worked(oracle_mod):
+    """"03 · 长文负载均衡" §4.1: a block shorter than a tile is charged as a whole
+    tile.  With tile 16: documents 2-4 (1, 9, 0 rows; 12 would overflow), 5-6
+    (12 + 3; 16 is not short) and 8-11 (4 x 4 = 16 rows) share tiles; 0, 12
+    (alone in their group), 1 and 7 (not shorter than a tile) keep their own."""
+    lengths = [5, 17, 1, 9, 0, 12, 3, 16, 4, 4, 4, 4, 15]
+    cu = W.cu_seqlens_of(lengths)
+    wl = oracle_mod.worklist(cu, oracle_mod.Mask(), 16, 16, 1, 1, num_ctas=2, pack_docs=1)
+    sl, sm = wl["slices"], wl["slice_masks"]
+    got = [(int(r[0]), int(r[1]), int(r[6])) for r in sl]
+    c = [int(x) for x in cu]
+    assert got == [(c[0], 5, 1), (c[1], 17, 1), (c[2], 10, 4), (c[5], 15, 4), (c[7], 16, 1),
+                   (c[8], 16, 4), (c[12], 15, 1)]
+    assert [int(x) for x in sm[2]] == [0b11, 0, 0, 0]           # rows 0 and 1 start documents
+    assert [int(x) for x in sm[3]] == [1 | (1 << 12), 0, 0, 0]
+    assert [int(x) for x in sm[5]] == [1 | (1 << 4) | (1 << 8) | (1 << 12), 0, 0, 0]
+    # a packed slice is one q tile against one kv tile
+    assert len(wl["segs"]) == 7 and all(int(g[4]) == 1 for g in wl["segs"])
+
+
+PACK_CASES = [
+    ([5, 17, 1, 9, 0, 12, 3, 16, 4, 4, 4, 4, 15], W.MASK_CAUSAL, {}),
+    ([3, 1, 2, 7, 30, 2, 2, 0, 6, 1], W.MASK_SLIDING_WINDOW, {"window": 3}),
+    ([8, 8, 8, 8, 1, 1], W.MASK_CAUSAL, {}),
+]
+
+
+@pytest.mark.parametrize("lengths,kind,kw", PACK_CASES)
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (3, 1)])
+@pytest.mark.parametrize("tile", [8, 16])
+def test_packed_worklist_covers_allowed_pairs_once(oracle_mod, lengths, kind, kw, hq, hkv, tile):
+    cu = W.cu_seqlens_of(lengths)
+    T = int(cu[-1])
+    m = oracle_mod.Mask(kind, **kw)
+    wl = oracle_mod.worklist(cu, m, tile, tile, hq, hkv, num_ctas=3, c_tile=2, pack_docs=1)
+    plain = oracle_mod.worklist(cu, m, tile, tile, hq, hkv, num_ctas=3, c_tile=2)
+    A = oracle_mod.allowed_matrix(cu, m)
+    cov, per_unit, empty = coverage(wl, T, T, hq, tile, tile)
+    for h in range(hq):
+        np.testing.assert_array_equal(cov[h], A.astype(np.int32))
+    assert empty == 0
+    np.testing.assert_array_equal(per_unit, wl["unit_pairs"])
+    assert wl["pairs_per_head"] == plain["pairs_per_head"] == int(A.sum())
+    assert (wl["slices"][:, 6] == 4).any()
+    # fewer computed tiles and fewer units than one tile grid per document
+    def tiles(w):
+        return sum((2 if u[5] >= 0 else 1) * sum(int(w["runs"][r][2] - w["runs"][r][1])
+                                                 for r in range(u[7], u[7] + u[8]))
+                   for u in w["units"])
+    assert tiles(wl) < tiles(plain) and len(wl["units"]) < len(plain["units"])
