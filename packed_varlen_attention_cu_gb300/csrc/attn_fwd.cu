@@ -72,7 +72,9 @@ struct Cfg {
     // V_j (at +kTileBytes), waited for and released once per kv tile
     static constexpr int kRingStages = kSplitP ? kStages / 2 : kStages;
     static constexpr int kStageBytes = kSplitP ? 2 * kTileBytes : kTileBytes;
-    static constexpr int kSmem = 2 * kTileBytes + kStages * kTileBytes + 1024;
+    // per softmax warp, 32 rows x 128 bytes of O staged for a TMA store
+    static constexpr int kStageOutBytes = 8 * 4096;
+    static constexpr int kSmem = 2 * kTileBytes + kStages * kTileBytes + kStageOutBytes + 1024;
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
 };
@@ -147,13 +149,15 @@ __device__ __forceinline__ void write_empty_rows(const AttnParams& p, const SubT
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                    const AttnParams p) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* sQ[2] = {smem, smem + C::kTileBytes};
     uint8_t* sKV = smem + 2 * C::kTileBytes;
+    uint8_t* sStage = sKV + C::kStages * C::kTileBytes;  // 4 KB per softmax warp, 1 KB aligned
     __shared__ Shared sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -228,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&tmo);
     }
     tc_fence_before();
     __syncthreads();
@@ -237,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // every role ends here: all 384 threads meet, warp 1 frees tensor memory
     auto finish = [&]() {
+        // the output stores issued from the staging buffers have completed
+        if (warp >= 4 && lane == 0) bulk_wait_all();
         tc_fence_before();
         named_barrier(1, kThreads);
         if (warp == 1) {
@@ -784,6 +791,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float lse_new =
                 l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
             float* lrow = p.lse + (int64_t)st.head * p.q_tokens + st.q_row + r;
+            // every row of this warp belongs to the sub-tile (warp-uniform)
+            const bool warp_full = __all_sync(0xffffffffu, valid);
             if (valid && p.accumulate) {
                 // fused ring step: merge this partial into the running fp32 (O, LSE)
                 //   lse = ln(e^lse_run + e^lse_new),
@@ -812,6 +821,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     *lrow = mx + logf(ea + eb);
                 }
+            } else if (!p.accumulate && warp_full) {
+                // all 32 rows of this warp belong to the sub-tile: stage them in shared
+                // memory, 128 bytes of every row at a time (128-byte swizzle: 16-byte
+                // chunk k of row `lane` at (k ^ (lane % 8)) * 16), and write each 32-row
+                // block with one TMA store, so that the stores leave the warp as whole
+                // rows instead of one 16-byte piece of 32 different rows per instruction
+                uint8_t* stg = sStage + (warp - 4) * 4096;
+                const uint32_t row_addr = smem_u32(stg) + lane * 128;
+                const int32_t row0 = st.q_row + (warp & 3) * 32;
+                if (p.out_fp32) {
+#pragma unroll
+                    for (int cb = 0; cb < D / 32; ++cb) {
+                        if (lane == 0) bulk_wait_read_all();  // the buffer's last store has read it
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            st_shared_v4(row_addr + ((k ^ (lane & 7)) << 4),
+                                         __float_as_uint(__uint_as_float(o[cb][4 * k]) * inv),
+                                         __float_as_uint(__uint_as_float(o[cb][4 * k + 1]) * inv),
+                                         __float_as_uint(__uint_as_float(o[cb][4 * k + 2]) * inv),
+                                         __float_as_uint(__uint_as_float(o[cb][4 * k + 3]) * inv));
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&tmo, stg, cb * 32, st.head, row0);
+                            bulk_commit_group();
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int cb = 0; cb < D / 64; ++cb) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t* v = &o[2 * cb + (k >> 2)][(k & 3) * 8];
+                            st_shared_v4(row_addr + ((k ^ (lane & 7)) << 4),
+                                         pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                                         pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                                         pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                                         pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&tmo, stg, cb * 64, st.head, row0);
+                            bulk_commit_group();
+                        }
+                    }
+                }
+                *lrow = lse_new;
             } else if (valid) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -855,7 +915,7 @@ std::atomic<int32_t> g_withhold_kv{0};  // pva_debug_withhold_kv_load
 
 template <int D>
 pva_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                  const AttnParams& ap, cudaStream_t st) {
+                  const CUtensorMap& mo, const AttnParams& ap, cudaStream_t st) {
     auto kern = attn_fwd_kernel<D>;
     // setmaxnreg.inc draws from the registers the block was launched with: the
     // split must fit in (threads x registers per thread) or the increase would
@@ -867,7 +927,7 @@ pva_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem) !=
         cudaSuccess)
         return PVA_ERR_CUDA;
-    kern<<<ap.num_ctas, kThreads, Cfg<D>::kSmem, st>>>(mq, mk, mv, ap);
+    kern<<<ap.num_ctas, kThreads, Cfg<D>::kSmem, st>>>(mq, mk, mv, mo, ap);
     return cudaGetLastError() == cudaSuccess ? PVA_OK : PVA_ERR_CUDA;
 }
 
@@ -904,13 +964,15 @@ pva_status attn_fwd_impl(const void* q, const void* k, const void* v,
     if (nc <= 0) return PVA_ERR_CUDA;
     if (nc > kMaxBins) return PVA_ERR_INVALID_ARG;
     if (mask->q_tokens == 0) return PVA_OK;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     const void* kp = mask->k_tokens > 0 ? k : q;  // no key rows: maps are never read
     const void* vp = mask->k_tokens > 0 ? v : q;
     const int32_t kh = mask->k_tokens > 0 ? params->num_kv_heads : params->num_q_heads;
     if (!make_map(&mq, q, mask->q_tokens, params->num_q_heads, head_dim) ||
         !make_map(&mk, kp, mask->k_tokens, kh, head_dim) ||
-        !make_map(&mv, vp, mask->k_tokens, kh, head_dim))
+        !make_map(&mv, vp, mask->k_tokens, kh, head_dim) ||
+        !make_map(&mo, out, mask->q_tokens, params->num_q_heads, head_dim, 32,
+                  out_is_fp32 ? 4 : 2))
         return PVA_ERR_CUDA;
     AttnParams ap;
     ap.wl = reinterpret_cast<const uint8_t*>(worklist_dev);
@@ -929,7 +991,8 @@ pva_status attn_fwd_impl(const void* q, const void* k, const void* v,
     ap.withhold_kv = g_withhold_kv.load(std::memory_order_relaxed);
     ap.dynamic = params->dispatch == PVA_DISPATCH_STATIC ? 0 : 1;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return head_dim == 128 ? launch<128>(mq, mk, mv, ap, st) : launch<64>(mq, mk, mv, ap, st);
+    return head_dim == 128 ? launch<128>(mq, mk, mv, mo, ap, st)
+                           : launch<64>(mq, mk, mv, mo, ap, st);
 }
 
 }  // namespace
