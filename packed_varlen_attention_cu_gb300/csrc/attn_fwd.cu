@@ -622,22 +622,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_base + 256 + i * 128;
         uint32_t s_cnt = 0, o_cnt = 0;
         bool live = true;
-        for (uint32_t nu = 0; live; ++nu) {
-            int32_t idx;
-            live = uring_get(sh.ur, nu, idx, abort_flag, err_word, kErrTimeoutBase + 14, kWaitNs);
-            if (!live || idx < 0) break;
-            const WlUnit wu = ubase[idx];
+        // The roles take unit n from the producer's ring; the softmax takes the
+        // next one before its epilogue (the producer published it once it had
+        // issued this unit's loads), so that the unit's description is read from
+        // global memory while the epilogue runs.
+        int32_t idx = -1;
+        WlUnit wu;
+        auto take_unit = [&](uint32_t n) {
+            live = uring_get(sh.ur, n, idx, abort_flag, err_word, kErrTimeoutBase + 14, kWaitNs);
+            if (live && idx >= 0) wu = ubase[idx];
+        };
+        take_unit(0);
+        for (uint32_t nu = 0; live && idx >= 0; ++nu) {
             const Unit u = decode_unit(wu, segs);
-            if (i >= u.nsub) continue;
+            if (i >= u.nsub) {
+                take_unit(nu + 1);
+                continue;
+            }
             const SubTile st = i == 0 ? u.st[0] : u.st[1];
             if (u.ntiles == 0) {
                 // no key for these rows: O = 0, LSE = -inf, which a running
                 // (O, LSE) absorbs unchanged
                 if (!p.accumulate) write_empty_rows(p, st, r, D);
+                take_unit(nu + 1);
                 continue;
             }
             const bool valid = r < st.nrows;
             const int32_t q_pos = st.q_pos + r;
+            if (p.accumulate && valid) {
+                // the epilogue reads this row's running O and LSE back: start moving
+                // them from DRAM to L2 now, so that the read does not wait on DRAM
+                const float* orow =
+                    reinterpret_cast<const float*>(p.out) + ((int64_t)(st.q_row + r) * p.hq + st.head) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) prefetch_l2(orow + c * 32);
+                prefetch_l2(p.lse + (int64_t)st.head * p.q_tokens + st.q_row + r);
+            }
             float m_used = -INFINITY, l_sum = 0.f;
             for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
                 const WlRun run = runs[u.run_begin + rr];
@@ -770,6 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l_sum += ps.x + ps.y;
                 }
             }
+            if (!live) break;
+            take_unit(nu + 1);
             if (!live) break;
             // epilogue: O / l -> global, LSE
             live = mbar_wait(&sh.o_full[i], o_cnt & 1, abort_flag, err_word, kErrTimeoutBase + 10,
