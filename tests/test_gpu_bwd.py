@@ -174,3 +174,24 @@ def test_bwd_128k_pack_sampled(oracle_mod):
     gk = got[1][kj[:, 0], kj[:, 1]]
     gv = got[2][kj[:, 0], kj[:, 1]]
     _check((gq, gk, gv), (rq, rk, rv), "128K pack sampled")
+
+
+@pytest.mark.parametrize("t", [0, 1, 3])
+def test_bwd_zigzag_ring_step(oracle_mod, t):
+    """One ring step of every rank at once (PVA_MASK_ZIGZAG_STEP, Q/K/V in ring
+    order): key chunks that no query of their step sees get a zero gradient."""
+    cp = 4
+    lengths = [700, 130, 1, 260, 33]
+    cu = W.cu_seqlens_of(lengths)
+    T = int(cu[-1])
+    hq, hkv, d = 4, 2, 128
+    q, k, v = W.make_qkv(T, T, hq, hkv, d, 60 + t)
+    dout = W.make_qkv(T, T, hq, hkv, d, 160 + t)[0]
+    ring = oracle_mod.ring_map(cu, cp)
+    qs, ks, vs, ds = q[ring], k[ring], v[ring], dout[ring]
+    mask = api.make_mask(W.MASK_ZIGZAG_STEP, T, T, cp=cp, ring_step=t)
+    got = _bwd(qs, ks, vs, cu, mask, hq, hkv, ds, True)
+    ref = oracle_mod.attention_bwd(oracle_mod.bf16_bits(qs), oracle_mod.bf16_bits(ks),
+                                   oracle_mod.bf16_bits(vs), oracle_mod.bf16_bits(ds), cu,
+                                   oracle_mask(W.MASK_ZIGZAG_STEP, cp=cp, ring_step=t))
+    _check(got, ref, f"ring step t={t}")
