@@ -190,7 +190,8 @@ pva_status pva_build_worklist(const int32_t* cu_seqlens_dev, int32_t num_docs,
  *   softmax_scale   <= 0 selects 1/sqrt(head_dim)
  *   cta_busy_ns     DEVICE uint64 [num_ctas, 2] (start, end) globaltimer stamps, or NULL
  * cu_seqlens_dev and mask describe the same problem as the worklist and are
- * used only for argument checks. */
+ * used only for argument checks.  With mask->q_tokens = 0 the call does nothing
+ * and returns PVA_OK (q, k, v, out and lse may then be NULL). */
 pva_status pva_attn_fwd(const void* q, const void* k, const void* v,
                         const int32_t* cu_seqlens_dev, const pva_mask_desc* mask,
                         const pva_worklist_params* params, int32_t head_dim,

@@ -195,6 +195,9 @@ def gather_rows(src: torch.Tensor, index_map: torch.Tensor, dst: torch.Tensor,
                 scatter: bool = False, stream=None) -> None:
     """dst[i] = src[map[i]] (or dst[map[i]] = src[i]) over the first dimension."""
     rows = index_map.numel()
+    # the library sees raw pointers: the map's own side must hold `rows` rows
+    if (src if scatter else dst).shape[0] < rows:
+        raise ValueError("gather_rows: the map has more entries than the tensor it fills has rows")
     row_bytes = src[0].numel() * src.element_size()
     indexed = dst.shape[0] if scatter else src.shape[0]
     check("pva_gather_rows", lib().pva_gather_rows(

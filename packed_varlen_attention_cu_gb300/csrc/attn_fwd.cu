@@ -968,7 +968,9 @@ pva_status attn_fwd_impl(const void* q, const void* k, const void* v,
                          const void* worklist_dev, void* out, int32_t out_is_fp32, float* lse,
                          float softmax_scale, uint64_t* cta_busy_ns, int32_t accumulate,
                          void* stream) {
-    if (!mask || !params || !worklist_dev || !out || !lse || !q) return PVA_ERR_INVALID_ARG;
+    if (!mask || !params || !worklist_dev) return PVA_ERR_INVALID_ARG;
+    if (mask->q_tokens == 0 && mask->k_tokens >= 0) return PVA_OK;  // no query row: nothing to do
+    if (!out || !lse || !q) return PVA_ERR_INVALID_ARG;
     if (mask->kind != PVA_MASK_SLICES && !cu_seqlens_dev) return PVA_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return PVA_ERR_UNSUPPORTED;
     if (params->tile_m != 128 || params->tile_n != 128) return PVA_ERR_UNSUPPORTED;

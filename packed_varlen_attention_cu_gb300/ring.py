@@ -138,10 +138,12 @@ class ZigzagRing:
     def _step_pairs(self, q, k, v, st, merge_events):
         cp = self.cp
         for r in range(cp):
+            # the map buffer has at least one entry; a rank may own no rows at all
+            mp = self.maps[r][: self.lens[r]]
             api.zigzag_shard(self.cu, cp, r, self.maps[r], None, st)
-            api.gather_rows(q, self.maps[r], self.qs[r], stream=st)
-            api.gather_rows(k, self.maps[r], self.ks[r], stream=st)
-            api.gather_rows(v, self.maps[r], self.vs[r], stream=st)
+            api.gather_rows(q, mp, self.qs[r], stream=st)
+            api.gather_rows(k, mp, self.ks[r], stream=st)
+            api.gather_rows(v, mp, self.vs[r], stream=st)
         for r in range(cp):
             n = self.lens[r]
             for t in range(cp):

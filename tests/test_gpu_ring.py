@@ -151,3 +151,23 @@ def test_ring_map_bit_exact(oracle_mod):
             api.zigzag_ring_map(torch.from_numpy(cu).cuda(), cp, m)
             torch.cuda.synchronize()
             np.testing.assert_array_equal(m.cpu().numpy(), oracle_mod.ring_map(cu, cp))
+
+
+@pytest.mark.parametrize("per_step,fused", SCHEMES, ids=SCHEME_IDS)
+def test_ring_cp8_documents_shorter_than_the_ranks(oracle_mod, per_step, fused):
+    """Documents shorter than 2cp leave some ranks without rows of them, and rank
+    7 here without any row at all: its shard and every pair with it are empty."""
+    lengths = [1, 5, 3, 0, 6, 2]
+    cu = W.cu_seqlens_of(lengths)
+    T = int(cu[-1])
+    assert min(api.zigzag_shard_len(cu, 8, r) for r in range(8)) == 0
+    hq, hkv, d = 2, 1, 64
+    q, k, v = W.make_qkv(T, T, hq, hkv, d, 77)
+    ring = _run_ring(q.cuda(), k.cuda(), v.cuda(), cu, 8, hq, hkv, d, per_step, fused)
+    rows = np.repeat(np.arange(T), hq)
+    heads = np.tile(np.arange(hq), T)
+    o, l = _pick(ring, rows, heads)
+    o, l = o.reshape(T, hq, d), l.reshape(T, hq).T
+    ref_o, ref_l = oracle_mod.attention(oracle_mod.bf16_bits(q), oracle_mod.bf16_bits(k),
+                                        oracle_mod.bf16_bits(v), cu, oracle_mask(W.MASK_CAUSAL))
+    compare(o, l, ref_o, ref_l, "cp=8, documents shorter than 2cp")
