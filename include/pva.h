@@ -282,8 +282,12 @@ size_t pva_bwd_plan_bytes(int32_t num_docs, const pva_mask_desc* mask,
                           const pva_worklist_params* params);
 
 /* Build the backward plan on the device from a built forward worklist of the
- * same problem: kv-major units, their cost (q-tile steps over the group's
- * heads + 1), sorted by cost descending; CTAs take them in snake order.
+ * same problem: kv-major units and their cost (q-tile steps over the group's
+ * heads + 1).  Under static dispatch they are sorted by cost descending and
+ * the CTAs take them in snake order; under dynamic dispatch the CTAs claim
+ * them by power-of-two cost class (descending), inside a class group by
+ * group, kv head by kv head, key tiles ascending (concurrent units then read
+ * the same documents' query tiles from L2).
  *   worklist_dev DEVICE (pva_build_worklist output);  plan_dev DEVICE, 256-B
  *   aligned, plan_bytes >= pva_bwd_plan_bytes() */
 pva_status pva_build_bwd_plan(const void* worklist_dev, int32_t num_docs,

@@ -14,7 +14,8 @@
 //             then dS in the element-wise warps, then dQ += dS K (TS MMA);
 //   bwd_dkdv  kv-major over the backward plan: per 128-key tile of one key
 //             group (the slices sharing a key range) and one kv head, every q
-//             tile of every slice of the group and every head: S^T = K Q^T and
+//             tile of every slice of the group, each for every head of the kv
+//             head's group (a q tile's heads back to back): S^T = K Q^T and
 //             dP^T = V dO^T, then P^T and dS^T, then dV += P^T dO and
 //             dK += dS^T Q, accumulated in tensor memory over the group; a
 //             loader warp stages each 64-query half's LSE and D ahead.
@@ -602,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t n = bh->nunits, B = gridDim.x;
     const int32_t G = p.hq / p.hkv;
     // dispatch as the forward worklist says: units claimed at run time in the
-    // plan's LPT order (dynamic), or dealt to the CTAs in snake order (static)
+    // plan's order (dynamic: cost classes, then group, kv head and key tile),
+    // or dealt to the CTAs in snake order of decreasing cost (static)
     const bool dyn = h->dispatch == PVA_DISPATCH_DYNAMIC;
     BwdHeader* bhw = const_cast<BwdHeader*>(bh);
     if (!dyn && (int32_t)blockIdx.x >= n) return;
@@ -664,15 +666,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(sV + b * 16384, &tmv, &sh.a_full, b * 64, u.kvh, s.k_row0 + u.kt * 128);
                 }
                 ++a_it;
-                for (int32_t hh = 0; hh < G && live; ++hh) {
-                    const int32_t head = u.kvh * G + hh;
-                    for (int32_t m = 0; m < u.gcount && live; ++m) {
-                        const WlSlice sm = slices[gsl[u.gbegin + m]];
-                        int32_t qlo, qhi;
-                        bwd_q_span(sm, u.kt, qlo, qhi, slice_mask(p.wl, h, sm, gsl[u.gbegin + m]));
-                        for (int32_t t = qlo; t < qhi && live; ++t) {
-                            const int32_t nq = min(128, sm.q_len - t * 128);
-                            const int32_t halves = nq > 64 ? 2 : 1;
+                for (int32_t m = 0; m < u.gcount && live; ++m) {
+                    const WlSlice sm = slices[gsl[u.gbegin + m]];
+                    int32_t qlo, qhi;
+                    bwd_q_span(sm, u.kt, qlo, qhi, slice_mask(p.wl, h, sm, gsl[u.gbegin + m]));
+                    for (int32_t t = qlo; t < qhi && live; ++t) {
+                        const int32_t nq = min(128, sm.q_len - t * 128);
+                        const int32_t halves = nq > 64 ? 2 : 1;
+                        for (int32_t hh = 0; hh < G && live; ++hh) {
+                            const int32_t head = u.kvh * G + hh;
                             for (int32_t hf = 0; hf < halves && live; ++hf) {
                                 const uint32_t st = it % kItems;
                                 live = mbar_wait(&sh.r_empty[st], ((it / kItems) & 1) ^ 1,
@@ -760,14 +762,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   kErrTimeoutBase + 33, kWaitNs);
             if (!live) break;
             first = true;
-            for (int32_t hh = 0; hh < G && live; ++hh) {
-                for (int32_t m = 0; m < u.gcount && live; ++m) {
-                    const WlSlice sm = slices[gsl[u.gbegin + m]];
-                    int32_t qlo, qhi;
-                    bwd_q_span(sm, u.kt, qlo, qhi, slice_mask(p.wl, h, sm, gsl[u.gbegin + m]));
-                    for (int32_t t = qlo; t < qhi && live; ++t) {
-                        const int32_t nq = min(128, sm.q_len - t * 128);
-                        const uint32_t halves = nq > 64 ? 2 : 1;
+            for (int32_t m = 0; m < u.gcount && live; ++m) {
+                const WlSlice sm = slices[gsl[u.gbegin + m]];
+                int32_t qlo, qhi;
+                bwd_q_span(sm, u.kt, qlo, qhi, slice_mask(p.wl, h, sm, gsl[u.gbegin + m]));
+                for (int32_t t = qlo; t < qhi && live; ++t) {
+                    const int32_t nq = min(128, sm.q_len - t * 128);
+                    const uint32_t halves = nq > 64 ? 2 : 1;
+                    for (int32_t hh = 0; hh < G && live; ++hh) {
                         for (uint32_t hf = 0; hf < halves && live; ++hf) {
                             const uint32_t st = it % kItems;
                             live = mbar_wait_warp(&sh.r_full[st], (it / kItems) & 1, abort_flag,
@@ -831,16 +833,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!live || idx < 0) break;
             const BwdUnit u = bunits[idx];
             if (u.cost <= 1) continue;
-            for (int32_t hh = 0; hh < G && live; ++hh) {
-                const int32_t head = u.kvh * G + hh;
-                for (int32_t m = 0; m < u.gcount && live; ++m) {
-                    const WlSlice s = slices[gsl[u.gbegin + m]];
-                    int32_t qlo, qhi;
-                    bwd_q_span(s, u.kt, qlo, qhi, slice_mask(p.wl, h, s, gsl[u.gbegin + m]));
-                    for (int32_t t = qlo; t < qhi && live; ++t) {
-                        const int32_t qrow0 = s.q_row0 + t * 128;
-                        const int32_t nq = min(128, s.q_len - t * 128);
-                        const uint32_t halves = nq > 64 ? 2 : 1;
+            for (int32_t m = 0; m < u.gcount && live; ++m) {
+                const WlSlice s = slices[gsl[u.gbegin + m]];
+                int32_t qlo, qhi;
+                bwd_q_span(s, u.kt, qlo, qhi, slice_mask(p.wl, h, s, gsl[u.gbegin + m]));
+                for (int32_t t = qlo; t < qhi && live; ++t) {
+                    const int32_t qrow0 = s.q_row0 + t * 128;
+                    const int32_t nq = min(128, s.q_len - t * 128);
+                    const uint32_t halves = nq > 64 ? 2 : 1;
+                    for (int32_t hh = 0; hh < G && live; ++hh) {
+                        const int32_t head = u.kvh * G + hh;
                         for (uint32_t hf = 0; hf < halves && live; ++hf, ++li) {
                             const uint32_t slot = li % kLdSlots;
                             live = mbar_wait_warp(&sh.ld_empty[slot], ((li / kLdSlots) & 1) ^ 1,
@@ -893,8 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
-            for (int32_t hh = 0; hh < G && live; ++hh) {
-                for (int32_t m = 0; m < u.gcount && live; ++m) {
+            for (int32_t m = 0; m < u.gcount && live; ++m) {
                 const WlSlice s = slices[gsl[u.gbegin + m]];
                 const uint32_t* pm = slice_mask(p.wl, h, s, gsl[u.gbegin + m]);
                 const int32_t k_pos = s.k_pos0 + u.kt * 128 + kr;
@@ -909,6 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t c_lo = (int32_t)max((int64_t)0, qa - cpos0);
                     const int32_t c_hi = kvalid ? (int32_t)min((int64_t)nq, qb - cpos0) : 0;
                     const uint32_t halves = nq > 64 ? 2 : 1;
+                    for (int32_t hh = 0; hh < G && live; ++hh) {
                     for (uint32_t hf = 0; hf < halves && live; ++hf, ++gu) {
                         const uint32_t b = gu & 1;
                         // this warpgroup's 32 query columns [h0, h0 + 32) of the half:
@@ -965,7 +967,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         ++li;
                     }
-                }
+                    }
                 }
             }
             if (!live) break;

@@ -1026,7 +1026,11 @@ __global__ void __launch_bounds__(kMaxBins) wl_lpt_kernel(uint8_t* base, int32_t
 // 2. A block scan over the groups of their key-tile counts.
 // 3. One unit per (group, key tile, kv head) with its cost (q-tile steps over
 //    the group's slices and the heads of the kv head's group, + 1) and a sort
-//    key (cost desc, uid asc).
+//    key.  Static dispatch deals units by cost (desc, uid asc).  Dynamic
+//    dispatch claims them by power-of-two cost class (desc); inside a class in
+//    uid order, which runs group by group, kv head by kv head, key tiles
+//    ascending, so that the CTAs running at the same time read the same
+//    documents' query tiles while the classes still put large units first.
 constexpr int kBwdPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kBwdPlanThreads)
@@ -1050,6 +1054,7 @@ __global__ void __launch_bounds__(kBwdPlanThreads)
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(plan + bh->off_keys);
     int32_t* gsl = reinterpret_cast<int32_t*>(plan + bh->off_gslices);
     const int32_t hkv = bh->hkv, G = bh->hq / bh->hkv;
+    const bool dyn = h->dispatch == PVA_DISPATCH_DYNAMIC;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     int32_t np2 = 1;
     while (np2 < ns) np2 <<= 1;
@@ -1113,7 +1118,7 @@ __global__ void __launch_bounds__(kBwdPlanThreads)
         int32_t base = carry;
         for (int j = 0; j < w; ++j) base += warp_tot[j];
         const int32_t first = base + inc - nk;  // this group's first key tile
-        for (int32_t kt = 0; kt < nk; ++kt) {
+        auto steps_of = [&](int32_t kt) -> int64_t {
             int64_t steps = 0;
             for (int32_t m = 0; m < gcount; ++m) {
                 int32_t qlo, qhi;
@@ -1121,8 +1126,13 @@ __global__ void __launch_bounds__(kBwdPlanThreads)
                 bwd_q_span(sm, kt, qlo, qhi, slice_mask(wl, h, sm, sidx[i + m]));
                 steps += qhi - qlo;
             }
+            return steps;
+        };
+        for (int32_t kt = 0; kt < nk; ++kt) {
+            const int64_t steps = steps_of(kt);
             for (int32_t g = 0; g < hkv; ++g) {
-                const int32_t uid = (first + kt) * hkv + g;
+                // units of one (group, kv head) are consecutive, key tiles ascending
+                const int32_t uid = first * hkv + g * nk + kt;
                 if (uid >= bh->cap_units) {
                     atomicCAS(&bh->error, 0, kErrCapacity);
                     continue;
@@ -1134,7 +1144,11 @@ __global__ void __launch_bounds__(kBwdPlanThreads)
                 u.kvh = g;
                 u.cost = (int64_t)G * steps + 1;
                 units[uid] = u;
-                const unsigned long long inv = ((1ULL << kCostBits) - 1) - (unsigned long long)u.cost;
+                // dynamic: the unit's power-of-two cost class (cost >= 1)
+                const unsigned long long c =
+                    dyn ? 1ULL << (63 - __clzll((unsigned long long)u.cost))
+                        : (unsigned long long)u.cost;
+                const unsigned long long inv = ((1ULL << kCostBits) - 1) - c;
                 keys[uid] = (inv << kUidBits) | (unsigned long long)uid;
             }
         }
