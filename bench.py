@@ -360,9 +360,11 @@ def run_e2e(args, ctx, world):
     """Same metric through the public C ABI with host buffers
     (pva_attn_fwd_host): per step, H2D of Q/K/V/cu_seqlens from pinned memory,
     worklist + attention, D2H of O/LSE, all enqueued by the one call.  Steps
-    alternate two streams with their own device buffers, as a caller streaming
-    packs would, so a step's copies in overlap the previous step's attention
-    and copies out; every step still moves all of its bytes."""
+    rotate over args.e2e_streams streams with their own device buffers, as a
+    caller streaming packs would, so a step's copies in overlap the previous
+    steps' attention and copies out (a stream's next copy in waits for its own
+    copy out, so two streams leave the link idle while a step computes); every
+    step still moves all of its bytes."""
     import torch
 
     from packed_varlen_attention_cu_gb300 import api
@@ -373,21 +375,22 @@ def run_e2e(args, ctx, world):
     T, hq, d = q.shape
     o_h = torch.empty((T, hq, d), dtype=torch.bfloat16).pin_memory()
     l_h = torch.empty((hq, T), dtype=torch.float32).pin_memory()
-    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    ns = max(1, args.e2e_streams)
+    streams = [torch.cuda.Stream(device=dev) for _ in range(ns)]
     bufs = [api.alloc_host_path_buffers(hq_, hk_, w.num_docs, mask, params, dev)
-            for _ in range(2)]
+            for _ in range(ns)]
     nsteps = [0]
 
     def step():
-        i = nsteps[0] % 2
+        i = nsteps[0] % ns
         nsteps[0] += 1
         api.attn_fwd_host(hq_, hk_, hv_, hcu, w.num_docs, mask, params, o_h, l_h, bufs[i],
                           0.0, streams[i])
 
-    for _ in range(4):
+    for _ in range(max(4, ns)):
         step()
     torch.cuda.synchronize()
-    K = max(4, (args.steps // 5) // 2 * 2)
+    K = max(4 * ns, (args.steps // 5) // ns * ns)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -409,7 +412,7 @@ def run_e2e(args, ctx, world):
     d2h = o_h.numel() * 2 + l_h.numel() * 4
     return {"value": round(f / t / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": round(t / K * 1e3, 4),
-            "path": "pva_attn_fwd_host (pinned host buffers), two streams alternating"}
+            "path": f"pva_attn_fwd_host (pinned host buffers), {ns} streams in rotation"}
 
 
 def run_zigzag(args, ctx, world, per_step=False, fused=False):
@@ -710,6 +713,8 @@ def main(argv=None):
                     help="short documents share tiles (pva_worklist_params.pack_docs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=3,
+                    help="streams (each with its own device buffers) the e2e steps rotate over")
     ap.add_argument("--no-zigzag", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--fit-cost", action="store_true",
