@@ -87,6 +87,7 @@ struct AttnParams {
     int32_t q_tokens, k_tokens, hq, hkv, out_fp32, num_ctas;
     float scale_log2;
     int32_t accumulate;   // merge into the running fp32 (out, lse) instead of writing
+                          // (selects the kernel instantiation)
     int32_t withhold_kv;  // test hook: the producer of CTA 0 (static dispatch) or of the CTA
                           // that claimed LPT rank 0 (dynamic) skips its K/V item 1
     int32_t dynamic;      // 1: claim units in LPT order from the worklist's counter
@@ -146,7 +147,9 @@ __device__ __forceinline__ void write_empty_rows(const AttnParams& p, const SubT
     p.lse[(int64_t)st.head * p.q_tokens + st.q_row + r] = -INFINITY;
 }
 
-template <int D>
+// ACC: the fused ring step (pva_attn_fwd_accumulate), a separate instantiation
+// so that each kernel carries only the epilogue it runs.
+template <int D, bool ACC>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -632,24 +635,168 @@ __global__ void __launch_bounds__(kThreads, 1)
             live = uring_get(sh.ur, n, idx, abort_flag, err_word, kErrTimeoutBase + 14, kWaitNs);
             if (live && idx >= 0) wu = ubase[idx];
         };
+        // The epilogue of a unit (O / l and the LSE out) runs after the softmax of
+        // the next unit's first kv tile has handed its P over, so that the tensor
+        // pipe computes that tile's PV and the next QK meanwhile instead of
+        // waiting for the stores (or during a unit without tiles for this
+        // sub-tile, which would leave its warps idle).  pst, pm,
+        // pl: the pending unit's sub-tile and its running max and sum.  The fused
+        // ring step (ACC: read-modify-write of the running fp32 O and LSE) runs its
+        // epilogue at once: deferred, it measured slower.
+        bool pend = false;
+        SubTile pst{0, 0, 0, 0};
+        float pm = 0.f, pl = 0.f;
+        auto epilogue = [&]() {
+            pend = false;
+            live = mbar_wait(&sh.o_full[i], o_cnt & 1, abort_flag, err_word, kErrTimeoutBase + 10,
+                             kWaitNs);
+            if (!live) return;
+            ++o_cnt;
+            const SubTile& st = pst;
+            const bool valid = r < st.nrows;
+            const float m_used = pm, l_sum = pl;
+            tc_fence_after();
+            const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            const int64_t row = (int64_t)(st.q_row + r) * p.hq + st.head;
+            // read the whole row of O, hand the tensor memory back to the MMA
+            // warp, then normalise and store
+            uint32_t o[D / 32][32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, o[c]);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
+            tc_fence_before();
+            mbar_arrive(&sh.o_empty[i]);
+            const float lse_new =
+                l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+            float* lrow = p.lse + (int64_t)st.head * p.q_tokens + st.q_row + r;
+            // every row of this warp belongs to the sub-tile (warp-uniform)
+            const bool warp_full = __all_sync(0xffffffffu, valid);
+            if constexpr (ACC) {
+              if (valid) {
+                // fused ring step: merge this partial into the running fp32 (O, LSE)
+                //   lse = ln(e^lse_run + e^lse_new),
+                //   O = e^(lse_run - lse) O_run + e^(lse_new - lse) O_new
+                // a row without keys here (lse_new = -inf) keeps its running values
+                if (lse_new != -INFINITY) {
+                    const float lse_old = *lrow;
+                    const float mx = fmaxf(lse_old, lse_new);
+                    const float ea = lse_old == -INFINITY ? 0.f : expf(lse_old - mx);
+                    const float eb = expf(lse_new - mx);
+                    const float wa = ea / (ea + eb), wb = eb / (ea + eb) * inv;
+                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * D);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            // a running value never merged before may be anything
+                            const float4 x = ea == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                       : dst[c * 8 + e];
+                            dst[c * 8 + e] =
+                                make_float4(wa * x.x + wb * __uint_as_float(o[c][4 * e]),
+                                            wa * x.y + wb * __uint_as_float(o[c][4 * e + 1]),
+                                            wa * x.z + wb * __uint_as_float(o[c][4 * e + 2]),
+                                            wa * x.w + wb * __uint_as_float(o[c][4 * e + 3]));
+                        }
+                    }
+                    *lrow = mx + logf(ea + eb);
+                }
+              }
+            } else if (warp_full) {
+                // all 32 rows of this warp belong to the sub-tile: stage them in shared
+                // memory, 128 bytes of every row at a time (128-byte swizzle: 16-byte
+                // chunk k of row `lane` at (k ^ (lane % 8)) * 16), and write each 32-row
+                // block with one TMA store, so that the stores leave the warp as whole
+                // rows instead of one 16-byte piece of 32 different rows per instruction
+                uint8_t* stg = sStage + (warp - 4) * 4096;
+                const uint32_t row_addr = smem_u32(stg) + lane * 128;
+                const int32_t row0 = st.q_row + (warp & 3) * 32;
+                if (p.out_fp32) {
+#pragma unroll
+                    for (int cb = 0; cb < D / 32; ++cb) {
+                        if (lane == 0) bulk_wait_read_all();  // the buffer's last store has read it
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            st_shared_v4(row_addr + ((k ^ (lane & 7)) << 4),
+                                         __float_as_uint(__uint_as_float(o[cb][4 * k]) * inv),
+                                         __float_as_uint(__uint_as_float(o[cb][4 * k + 1]) * inv),
+                                         __float_as_uint(__uint_as_float(o[cb][4 * k + 2]) * inv),
+                                         __float_as_uint(__uint_as_float(o[cb][4 * k + 3]) * inv));
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&tmo, stg, cb * 32, st.head, row0);
+                            bulk_commit_group();
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int cb = 0; cb < D / 64; ++cb) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t* v = &o[2 * cb + (k >> 2)][(k & 3) * 8];
+                            st_shared_v4(row_addr + ((k ^ (lane & 7)) << 4),
+                                         pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                                         pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                                         pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                                         pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&tmo, stg, cb * 64, st.head, row0);
+                            bulk_commit_group();
+                        }
+                    }
+                }
+                *lrow = lse_new;
+            } else if (valid) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    if (p.out_fp32) {
+                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) +
+                                                                row * D + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(o[c][4 * e]) * inv,
+                                                 __uint_as_float(o[c][4 * e + 1]) * inv,
+                                                 __uint_as_float(o[c][4 * e + 2]) * inv,
+                                                 __uint_as_float(o[c][4 * e + 3]) * inv);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_uint4(
+                                pack_bf16x2(__uint_as_float(o[c][8 * e]) * inv, __uint_as_float(o[c][8 * e + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(o[c][8 * e + 2]) * inv, __uint_as_float(o[c][8 * e + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(o[c][8 * e + 4]) * inv, __uint_as_float(o[c][8 * e + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(o[c][8 * e + 6]) * inv, __uint_as_float(o[c][8 * e + 7]) * inv));
+                    }
+                }
+                *lrow = lse_new;
+            }
+        };
         take_unit(0);
         for (uint32_t nu = 0; live && idx >= 0; ++nu) {
             const Unit u = decode_unit(wu, segs);
-            if (i >= u.nsub) {
+            if (i >= u.nsub || u.ntiles == 0) {
+                // this sub-tile has no tiles here: the pending epilogue runs now
+                if (!ACC && pend) epilogue();
+                if (!live) break;
+                // no key for these rows: O = 0, LSE = -inf, which a running
+                // (O, LSE) absorbs unchanged
+                if (i < u.nsub && !ACC) write_empty_rows(p, u.st[i], r, D);
                 take_unit(nu + 1);
                 continue;
             }
             const SubTile st = i == 0 ? u.st[0] : u.st[1];
-            if (u.ntiles == 0) {
-                // no key for these rows: O = 0, LSE = -inf, which a running
-                // (O, LSE) absorbs unchanged
-                if (!p.accumulate) write_empty_rows(p, st, r, D);
-                take_unit(nu + 1);
-                continue;
-            }
             const bool valid = r < st.nrows;
             const int32_t q_pos = st.q_pos + r;
-            if (p.accumulate && valid) {
+            if (ACC && valid) {
                 // the epilogue reads this row's running O and LSE back: start moving
                 // them from DRAM to L2 now, so that the read does not wait on DRAM
                 const float* orow =
@@ -788,139 +935,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const float2 ps = __fadd2_rn(__fadd2_rn(part[0], part[1]), __fadd2_rn(part[2], part[3]));
                     l_sum += ps.x + ps.y;
+                    if (!ACC && pend) {
+                        epilogue();
+                        if (!live) break;
+                    }
                 }
             }
             if (!live) break;
             take_unit(nu + 1);
             if (!live) break;
-            // epilogue: O / l -> global, LSE
-            live = mbar_wait(&sh.o_full[i], o_cnt & 1, abort_flag, err_word, kErrTimeoutBase + 10,
-                             kWaitNs);
-            if (!live) break;
-            ++o_cnt;
-            tc_fence_after();
-            const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-            const int64_t row = (int64_t)(st.q_row + r) * p.hq + st.head;
-            // read the whole row of O, hand the tensor memory back to the MMA
-            // warp, then normalise and store
-            uint32_t o[D / 32][32];
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, o[c]);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
-            tc_fence_before();
-            mbar_arrive(&sh.o_empty[i]);
-            const float lse_new =
-                l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
-            float* lrow = p.lse + (int64_t)st.head * p.q_tokens + st.q_row + r;
-            // every row of this warp belongs to the sub-tile (warp-uniform)
-            const bool warp_full = __all_sync(0xffffffffu, valid);
-            if (valid && p.accumulate) {
-                // fused ring step: merge this partial into the running fp32 (O, LSE)
-                //   lse = ln(e^lse_run + e^lse_new),
-                //   O = e^(lse_run - lse) O_run + e^(lse_new - lse) O_new
-                // a row without keys here (lse_new = -inf) keeps its running values
-                if (lse_new != -INFINITY) {
-                    const float lse_old = *lrow;
-                    const float mx = fmaxf(lse_old, lse_new);
-                    const float ea = lse_old == -INFINITY ? 0.f : expf(lse_old - mx);
-                    const float eb = expf(lse_new - mx);
-                    const float wa = ea / (ea + eb), wb = eb / (ea + eb) * inv;
-                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + row * D);
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            // a running value never merged before may be anything
-                            const float4 x = ea == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                                       : dst[c * 8 + e];
-                            dst[c * 8 + e] =
-                                make_float4(wa * x.x + wb * __uint_as_float(o[c][4 * e]),
-                                            wa * x.y + wb * __uint_as_float(o[c][4 * e + 1]),
-                                            wa * x.z + wb * __uint_as_float(o[c][4 * e + 2]),
-                                            wa * x.w + wb * __uint_as_float(o[c][4 * e + 3]));
-                        }
-                    }
-                    *lrow = mx + logf(ea + eb);
-                }
-            } else if (!p.accumulate && warp_full) {
-                // all 32 rows of this warp belong to the sub-tile: stage them in shared
-                // memory, 128 bytes of every row at a time (128-byte swizzle: 16-byte
-                // chunk k of row `lane` at (k ^ (lane % 8)) * 16), and write each 32-row
-                // block with one TMA store, so that the stores leave the warp as whole
-                // rows instead of one 16-byte piece of 32 different rows per instruction
-                uint8_t* stg = sStage + (warp - 4) * 4096;
-                const uint32_t row_addr = smem_u32(stg) + lane * 128;
-                const int32_t row0 = st.q_row + (warp & 3) * 32;
-                if (p.out_fp32) {
-#pragma unroll
-                    for (int cb = 0; cb < D / 32; ++cb) {
-                        if (lane == 0) bulk_wait_read_all();  // the buffer's last store has read it
-                        __syncwarp();
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            st_shared_v4(row_addr + ((k ^ (lane & 7)) << 4),
-                                         __float_as_uint(__uint_as_float(o[cb][4 * k]) * inv),
-                                         __float_as_uint(__uint_as_float(o[cb][4 * k + 1]) * inv),
-                                         __float_as_uint(__uint_as_float(o[cb][4 * k + 2]) * inv),
-                                         __float_as_uint(__uint_as_float(o[cb][4 * k + 3]) * inv));
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_3d(&tmo, stg, cb * 32, st.head, row0);
-                            bulk_commit_group();
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int cb = 0; cb < D / 64; ++cb) {
-                        if (lane == 0) bulk_wait_read_all();
-                        __syncwarp();
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const uint32_t* v = &o[2 * cb + (k >> 2)][(k & 3) * 8];
-                            st_shared_v4(row_addr + ((k ^ (lane & 7)) << 4),
-                                         pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
-                                         pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
-                                         pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
-                                         pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_3d(&tmo, stg, cb * 64, st.head, row0);
-                            bulk_commit_group();
-                        }
-                    }
-                }
-                *lrow = lse_new;
-            } else if (valid) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    if (p.out_fp32) {
-                        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) +
-                                                                row * D + c * 32);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            dst[e] = make_float4(__uint_as_float(o[c][4 * e]) * inv,
-                                                 __uint_as_float(o[c][4 * e + 1]) * inv,
-                                                 __uint_as_float(o[c][4 * e + 2]) * inv,
-                                                 __uint_as_float(o[c][4 * e + 3]) * inv);
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(
-                            reinterpret_cast<__nv_bfloat16*>(p.out) + row * D + c * 32);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_uint4(
-                                pack_bf16x2(__uint_as_float(o[c][8 * e]) * inv, __uint_as_float(o[c][8 * e + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(o[c][8 * e + 2]) * inv, __uint_as_float(o[c][8 * e + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(o[c][8 * e + 4]) * inv, __uint_as_float(o[c][8 * e + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(o[c][8 * e + 6]) * inv, __uint_as_float(o[c][8 * e + 7]) * inv));
-                    }
-                }
-                *lrow = lse_new;
+            pend = true;
+            pst = st;
+            pm = m_used;
+            pl = l_sum;
+            if constexpr (ACC) {
+                epilogue();
+                if (!live) break;
             }
         }
+        if (!ACC && live && pend) epilogue();
         finish();
     }
 
@@ -938,7 +971,7 @@ std::atomic<int32_t> g_withhold_kv{0};  // pva_debug_withhold_kv_load
 template <int D>
 pva_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                   const CUtensorMap& mo, const AttnParams& ap, cudaStream_t st) {
-    auto kern = attn_fwd_kernel<D>;
+    auto kern = ap.accumulate ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>;
     // setmaxnreg.inc draws from the registers the block was launched with: the
     // split must fit in (threads x registers per thread) or the increase would
     // never be granted.
