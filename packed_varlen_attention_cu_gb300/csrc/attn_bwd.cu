@@ -10,8 +10,9 @@
 //   bwd_dq    q-major over the forward worklist's units, dispatched as the
 //             worklist says (static per-CTA LPT lists, or claimed at run time):
 //             per query sub-tile (Q and dO copied into tensor memory), every
-//             kv tile of its runs as two 64-key halves: S and dP (TS MMAs),
-//             then dS in the element-wise warps, then dQ += dS K (TS MMA);
+//             kv tile of its runs as two 64-key halves: S and dP (TS MMAs,
+//             issued by two warps), then dS in the element-wise warps, then
+//             dQ += dS K (TS MMA);
 //   bwd_dkdv  kv-major over the backward plan: per 128-key tile of one key
 //             group (the slices sharing a key range) and one kv head, every q
 //             tile of every slice of the group, each for every head of the kv
@@ -40,8 +41,9 @@
 namespace pva {
 namespace {
 
-// warp 0 TMA, warp 1 MMA, warps 4-11 element-wise + epilogue (two warpgroups
-// taking alternate half-items)
+// warp 0 TMA, warp 1 MMA (bwd_dq: warp 3 issues its dP MMAs), warp 2 the dK/dV
+// pass's (LSE, D) loader, warps 4-11 element-wise + epilogue (two warpgroups
+// sharing every half-item)
 constexpr int kThreads = 384;
 // bwd_dkdv's register split (kSplitRegs): the TMA/MMA warpgroup gives registers
 // to the two element-wise warpgroups
@@ -81,7 +83,7 @@ constexpr int kLdSlots = 8;
 constexpr int kMaxStages = 12;
 
 struct BShared {
-    uint64_t a_full, a_empty, o_full, o_empty, done;
+    uint64_t a_full, a_empty, o_full, o_empty, done, done2;
     uint64_t s2_full[2], p2_full[2];  // per half-item tensor-memory buffer
     uint64_t r_full[kMaxStages], r_empty[kMaxStages];
     UnitRing<8> ur;  // the producer hands each unit's index to the other roles
@@ -165,23 +167,26 @@ __device__ __forceinline__ void store_zero_row(void* base, int64_t row_elem, boo
     }
 }
 
+// issuers: MMA-issuing warps; each commits once to a_empty, s2_full and r_empty
+// per use and reads every unit
 __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_threads,
-                                              int extra_readers) {
+                                              int extra_readers, int issuers) {
     mbar_init(&sh.a_full, 1);
-    mbar_init(&sh.a_empty, 1);
+    mbar_init(&sh.a_empty, issuers);
     mbar_init(&sh.o_full, 1);
     mbar_init(&sh.o_empty, elem_threads / 32);
     mbar_init(&sh.done, 1);
+    mbar_init(&sh.done2, 1);
     for (int b = 0; b < 2; ++b) {
-        mbar_init(&sh.s2_full[b], 1);
+        mbar_init(&sh.s2_full[b], issuers);
         mbar_init(&sh.p2_full[b], elem_threads / 32);  // one arrival per element-wise warp
     }
     for (int s = 0; s < stages; ++s) {
         mbar_init(&sh.r_full[s], 1);
-        mbar_init(&sh.r_empty[s], 1);
+        mbar_init(&sh.r_empty[s], issuers);
     }
-    // unit readers: the MMA warp (one arrival) and every element-wise thread
-    uring_init(sh.ur, 1 + elem_threads + extra_readers);
+    // unit readers: the MMA warps (one arrival each) and every element-wise thread
+    uring_init(sh.ur, issuers + elem_threads + extra_readers);
     for (int s = 0; s < kLdSlots; ++s) {
         mbar_init(&sh.ld_full[s], 32);
         mbar_init(&sh.ld_empty[s], elem_threads / 32);
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
     const int32_t ub = dyn ? 0 : cta_off[blockIdx.x], ue = dyn ? 0 : cta_off[blockIdx.x + 1];
     if (!dyn && ub >= ue) return;
-    if (tid == 0) init_barriers(sh, C::kStagesDq, 256, 0);
+    if (tid == 0) init_barriers(sh, C::kStagesDq, 256, 0, 2);
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -337,7 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t it = 0, a_it = 0, gu = 0, o_cnt = 0;
         bool live = true;
         const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
-        const uint64_t dDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
         const uint64_t dKn = sdesc_sw128(smem_u32(sKV), 16, 1024);    // K-major, 64-row atoms
         const uint64_t dKm = sdesc_sw128(smem_u32(sKV), 8192, 1024);  // MN-major, 64-row atoms
         constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, false);
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Q and dO of the sub-tile, copied into tensor memory as the A operands of
         // S = Q K^T and dP = dO V^T (TS MMAs read only the K / V halves from shared
         // memory, so N = 64 runs at the full rate)
-        const uint32_t tQA = tmem + 256 + D, tDOA = tmem + 256 + D + D / 2;
+        const uint32_t tQA = tmem + 256 + D;
         bool pend = false, first = true;
         uint32_t pend_u = 0, pend_st = 0;
         auto finish_pending = [&]() -> bool {
@@ -387,9 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
                     tmem_cp_elect(tQA + k * 8, dQd + off16);
-                    tmem_cp_elect(tDOA + k * 8, dDO + off16);
                 }
-                mma_commit_elect(&sh.a_empty);  // Q, dO copied: the producer may refill them
+                mma_commit_elect(&sh.a_empty);  // Q copied (warp 3 copies dO)
                 first = true;
                 for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
                     const WlRun run = runs[u.run_begin + rr];
@@ -405,19 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_fence_after();
                             const uint32_t b = gu & 1;
                             const uint64_t oK = (st * 2 * kHalfBytes) >> 4;
-                            const uint64_t oV = (st * 2 * kHalfBytes + kHalfBytes) >> 4;
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
-                                // Q, dO (tensor memory) against the K, V halves (64-row atoms)
+                                // Q (tensor memory) against the K half (64-row atoms)
                                 const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
                                 mma_ts_elect(tmem + 64 * b, tQA + k * 8, dKn + oK + kq, kIdescHalf,
                                              k > 0);
-                            }
-#pragma unroll
-                            for (int k = 0; k < D / 16; ++k) {
-                                const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
-                                mma_ts_elect(tmem + 128 + 64 * b, tDOA + k * 8, dKn + oV + kq,
-                                             kIdescHalf, k > 0);
                             }
                             mma_commit_elect(&sh.s2_full[b]);
                             if (pend && !finish_pending()) {
@@ -441,6 +437,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit_elect(&sh.done);
         mbar_wait_drain(&sh.done, 0, kDrainNs);
+        __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------------------- dP issuer (whole warp)
+        // dP = dO V^T of every half-item into buffer b = half-item % 2, from a warp
+        // of its own: one issuing warp spends about as long issuing a half-item's
+        // 20 MMAs as the tensor pipe takes to run them.  The dP buffer is reused
+        // once the element-wise warps have read it (p2_full of two half-items ago);
+        // the stage is released by both issuers (r_empty counts two commits).
+        uint32_t it = 0, a_it = 0, gu = 0;
+        bool live = true;
+        const uint64_t dDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
+        const uint64_t dKn = sdesc_sw128(smem_u32(sKV), 16, 1024);  // K-major, 64-row atoms
+        constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, false);
+        const uint32_t tDOA = tmem + 256 + D + D / 2;
+        for (uint32_t nu = 0; live; ++nu) {
+            int32_t idx;
+            live = uring_get_warp(sh.ur, nu, idx, abort_flag, err_word, kErrTimeoutBase + 46,
+                                  kWaitNs);
+            if (!live || idx < 0) break;
+            const WlUnit u = ubase[idx];
+            if (u.ntiles == 0) continue;
+            const int nsub = u.h1 >= 0 ? 2 : 1;
+            for (int i = 0; i < nsub && live; ++i) {
+                live = mbar_wait_warp(&sh.a_full, a_it & 1, abort_flag, err_word,
+                                      kErrTimeoutBase + 47, kWaitNs);
+                if (!live) break;
+                tc_fence_after();
+                // dO of the sub-tile into tensor memory (after this warp's last dP of
+                // the previous sub-tile, in issue order)
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                    tmem_cp_elect(tDOA + k * 8, dDO + (k >> 2) * 1024 + (k & 3) * 2);
+                mma_commit_elect(&sh.a_empty);
+                for (int32_t rr = 0; rr < u.run_count && live; ++rr) {
+                    const WlRun run = runs[u.run_begin + rr];
+                    const WlSlice s = slices[run.slice];
+                    for (int32_t jt = run.lo; jt < run.hi && live; ++jt) {
+                        const int32_t halves = min(128, s.k_len - jt * 128) > 64 ? 2 : 1;
+                        for (int32_t hf = 0; hf < halves && live; ++hf) {
+                            const uint32_t st = it % C::kStagesDq;
+                            const uint32_t b = gu & 1;
+                            live = mbar_wait_warp(&sh.r_full[st], (it / C::kStagesDq) & 1,
+                                                  abort_flag, err_word, kErrTimeoutBase + 48,
+                                                  kWaitNs);
+                            if (!live) break;
+                            if (gu >= 2) {
+                                live = mbar_wait_warp(&sh.p2_full[b], ((gu - 2) >> 1) & 1,
+                                                      abort_flag, err_word, kErrTimeoutBase + 49,
+                                                      kWaitNs);
+                                if (!live) break;
+                            }
+                            tc_fence_after();
+                            const uint64_t oV = (st * 2 * kHalfBytes + kHalfBytes) >> 4;
+#pragma unroll
+                            for (int k = 0; k < D / 16; ++k) {
+                                const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
+                                mma_ts_elect(tmem + 128 + 64 * b, tDOA + k * 8, dKn + oV + kq,
+                                             kIdescHalf, k > 0);
+                            }
+                            mma_commit_elect(&sh.s2_full[b]);
+                            mma_commit_elect(&sh.r_empty[st]);
+                            ++gu;
+                            ++it;
+                        }
+                    }
+                }
+                if (!live) break;
+                ++a_it;
+            }
+        }
+        mma_commit_elect(&sh.done2);
+        mbar_wait_drain(&sh.done2, 0, kDrainNs);
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- dS and the dQ epilogue
@@ -609,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     BwdHeader* bhw = const_cast<BwdHeader*>(bh);
     if (!dyn && (int32_t)blockIdx.x >= n) return;
     // unit readers beyond the MMA and element-wise warps: the loader warp
-    if (tid == 0) init_barriers(sh, kItems, 256, 1);
+    if (tid == 0) init_barriers(sh, kItems, 256, 1, 1);
     // (LSE log2, D) of the 64 queries of each staged half-item
     __shared__ __align__(16) float2 s_ld[kLdSlots][64];
     if (warp == 1) {
