@@ -342,7 +342,7 @@ def run_pva(args, rank, world, local):
                      "traffic": traffic,
                      "peak_source": f"{peak_src} bf16_tflops (burst); frac vs sustained "
                                     f"{peak_sus}: {achieved / peak_sus:.4f}",
-                     "kernel": "attn_fwd_kernel<128>" if d == 128 else "attn_fwd_kernel<64>",
+                     "kernel": "attn_fwd_kernel<128, false>" if d == 128 else "attn_fwd_kernel<64, false>",
                      "algorithmic_flops_per_launch": flops,
                      "avg_launch_ms": round(attn_avg_s * 1e3, 4)},
         "imbalance": None if imbalance is None else round(imbalance, 4),
