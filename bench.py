@@ -390,7 +390,8 @@ def run_e2e(args, ctx, world):
     for _ in range(max(4, ns)):
         step()
     torch.cuda.synchronize()
-    K = max(4 * ns, (args.steps // 5) // ns * ns)
+    # at least six rounds of the rotation, so that its fill and drain weigh little
+    K = max(6 * ns, (args.steps // 5) // ns * ns)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()

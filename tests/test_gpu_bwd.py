@@ -195,3 +195,59 @@ def test_bwd_zigzag_ring_step(oracle_mod, t):
                                    oracle_mod.bf16_bits(vs), oracle_mod.bf16_bits(ds), cu,
                                    oracle_mask(W.MASK_ZIGZAG_STEP, cp=cp, ring_step=t))
     _check(got, ref, f"ring step t={t}")
+
+
+def _bwd_with(q, k, v, cu, mask, params, dout):
+    """Forward and backward with explicit worklist params; bf16 gradients on the device."""
+    dev = torch.device("cuda")
+    nd = len(cu) - 1
+    cu_d = torch.from_numpy(np.ascontiguousarray(cu, dtype=np.int32)).to(dev)
+    wl = api.alloc_worklist(nd, mask, params, dev)
+    api.build_worklist(cu_d, mask, params, wl)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=dev)
+    api.attn_fwd(qd, kd, vd, cu_d, mask, params, wl, out, lse)
+    plan = api.alloc_bwd_plan(nd, mask, params, dev)
+    api.build_bwd_plan(wl, nd, mask, params, plan)
+    grads = [torch.full(t.shape, float("nan"), dtype=torch.bfloat16, device=dev) for t in (q, k, v)]
+    api.attn_bwd(qd, kd, vd, out, lse, dout.to(dev), cu_d, nd, mask, params, wl, plan, *grads)
+    torch.cuda.synchronize()
+    assert api.worklist_error(wl) == 0
+    return grads
+
+
+@pytest.mark.parametrize("num_ctas", [0, 5])
+def test_bwd_bitwise_equal_across_dispatch(num_ctas):
+    # Each gradient row is summed by one CTA in an order fixed by its unit (dQ: the
+    # forward unit's kv tiles; dK/dV: the plan unit's q tiles and heads), so the
+    # dispatch mode and the CTA count change who computes a row, never its value.
+    lengths = [300, 1, 777, 128, 0, 64, 1500, 129]
+    hq, hkv, d = 8, 2, 128
+    cu = W.cu_seqlens_of(lengths)
+    T = int(cu[-1])
+    q, k, v = W.make_qkv(T, T, hq, hkv, d, 5)
+    dout = W.make_qkv(T, T, hq, hkv, d, 105)[0]
+    mask = api.make_mask(W.MASK_CAUSAL, T, T)
+    runs = [_bwd_with(q, k, v, cu, mask, api.make_params(hq, hkv, num_ctas=num_ctas, dispatch=dp),
+                      dout)
+            for dp in (api.DISPATCH_DYNAMIC, api.DISPATCH_STATIC)]
+    for name, a, b in zip(("dq", "dk", "dv"), *runs):
+        assert torch.isfinite(a.float()).all(), name
+        assert torch.equal(a, b), name
+
+
+def test_bwd_static_dispatch_matches_oracle(oracle_mod):
+    lengths = [200, 513, 7, 300]
+    hq, hkv, d = 4, 2, 64
+    cu = W.cu_seqlens_of(lengths)
+    T = int(cu[-1])
+    q, k, v = W.make_qkv(T, T, hq, hkv, d, 11)
+    dout = W.make_qkv(T, T, hq, hkv, d, 111)[0]
+    mask = api.make_mask(W.MASK_CAUSAL, T, T)
+    got = _bwd_with(q, k, v, cu, mask,
+                    api.make_params(hq, hkv, num_ctas=3, dispatch=api.DISPATCH_STATIC), dout)
+    ref = oracle_mod.attention_bwd(oracle_mod.bf16_bits(q), oracle_mod.bf16_bits(k),
+                                   oracle_mod.bf16_bits(v), oracle_mod.bf16_bits(dout), cu,
+                                   oracle_mask(W.MASK_CAUSAL))
+    _check([t.float().cpu().numpy().astype(np.float64) for t in got], ref, "static dispatch")
