@@ -597,25 +597,43 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
     if (kDispatchKeys) {
         // the split: the highest non-empty class c with less work below it than
         // num_ctas * 2^(c+1) (capped at 38)
-        if (threadIdx.x == 0) {
-            const int64_t B = a.num_ctas;
-            unsigned long long below = 0;
-            for (int c = 0; c < 64; ++c) below += a.cls_work[c];
-            int32_t split = 0;
-            for (int c = 63; c >= 0; --c) {
-                if (a.cls_work[c] == 0) continue;
-                below -= a.cls_work[c];  // work of the classes under c
-                if (below < ((unsigned long long)B << (c + 1))) {
-                    split = c < 38 ? c : 38;
-                    break;
+        // one warp: lane l holds classes l and l + 32; an exclusive prefix sum over
+        // the 64 class totals gives each class the work below it (one thread walking
+        // the 64 totals spent ~20 us in dependent L2 loads)
+        if (threadIdx.x < 32) {
+            const unsigned full = 0xffffffffu;
+            const int lane = threadIdx.x;
+            const unsigned long long w0 = a.cls_work[lane], w1 = a.cls_work[lane + 32];
+            unsigned long long p0 = w0, p1 = w1;
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long x0 = __shfl_up_sync(full, p0, o);
+                const unsigned long long x1 = __shfl_up_sync(full, p1, o);
+                if (lane >= o) {
+                    p0 += x0;
+                    p1 += x1;
                 }
             }
-            s_split = split;
-            if (blockIdx.x == 0) *a.split = split;
+            p1 += __shfl_sync(full, p0, 31);  // classes 32.. also sit above all of 0..31
+            const unsigned long long B = (unsigned long long)a.num_ctas;
+            // class c qualifies: non-empty, and less work under it than B * 2^(c+1)
+            const int s0 = lane + 1, s1 = lane + 33 < 63 ? lane + 33 : 63;
+            const bool q0 = w0 != 0 && p0 - w0 < (B << s0);
+            const bool q1 = w1 != 0 && p1 - w1 < (B << s1);
+            const unsigned m0 = __ballot_sync(full, q0), m1 = __ballot_sync(full, q1);
+            // the highest qualifying class, capped at 38 (0 when none qualifies)
+            int32_t split = m1 ? 63 - __clz(m1) : (m0 ? 31 - __clz(m0) : 0);
+            split = split < 38 ? split : 38;
+            if (lane == 0) {
+                s_split = split;
+                if (blockIdx.x == 0) *a.split = split;
+            }
         }
         __syncthreads();
     }
-    for (int32_t i = threadIdx.x; i < kSortChunk; i += kSortThreads) {
+    // sort the smallest power of two >= m keys (the tail of a chunk is padding)
+    int32_t np2 = 2;
+    while (np2 < m) np2 <<= 1;
+    for (int32_t i = threadIdx.x; i < np2; i += kSortThreads) {
         unsigned long long key = ~0ULL;
         if (i < m) {
             if (kDispatchKeys) {
@@ -633,9 +651,9 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
         sk[i] = key;
     }
     __syncthreads();
-    for (int32_t size = 2; size <= kSortChunk; size <<= 1) {
+    for (int32_t size = 2; size <= np2; size <<= 1) {
         for (int32_t stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int32_t t = threadIdx.x; t < kSortChunk / 2; t += kSortThreads) {
+            for (int32_t t = threadIdx.x; t < np2 / 2; t += kSortThreads) {
                 const int32_t lo = 2 * t - (t & (stride - 1));
                 const int32_t hi = lo + stride;
                 const bool up = (lo & size) == 0;
@@ -651,7 +669,7 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
             // stage or the next one reaches across warps, and after the last
             const int32_t next = stride > 1 ? stride >> 1 : size;
             static_assert(kSortChunk / 2 == kSortThreads, "one pair per thread and stage");
-            const bool last = stride == 1 && size == kSortChunk;
+            const bool last = stride == 1 && size == np2;
             if (stride > 32 || next > 32 || last) __syncthreads();
             else __syncwarp();
         }
