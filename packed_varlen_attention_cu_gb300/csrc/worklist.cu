@@ -630,10 +630,16 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
         }
         __syncthreads();
     }
-    // sort the smallest power of two >= m keys (the tail of a chunk is padding)
-    int32_t np2 = 2;
+    // Bitonic sort of the smallest power of two >= max(m, 64) keys (the tail of a
+    // chunk is padding, ~0).  Warp w holds keys [64 w, 64 w + 64) in registers, two
+    // per lane (k0 = key 64 w + 2 lane, k1 the next): every stage with a stride of
+    // at most 32 runs there with shuffles, only the wider ones go through shared
+    // memory.  Same network and result as the all-shared-memory form.
+    int32_t np2 = 64;
     while (np2 < m) np2 <<= 1;
-    for (int32_t i = threadIdx.x; i < np2; i += kSortThreads) {
+    const int32_t e0 = 2 * (int32_t)threadIdx.x;  // index of k0
+    const bool holds = e0 < np2;
+    auto key_at = [&](int32_t i) -> unsigned long long {
         unsigned long long key = ~0ULL;
         if (i < m) {
             if (kDispatchKeys) {
@@ -648,11 +654,39 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
                 key = keys[c0 + i];
             }
         }
-        sk[i] = key;
-    }
-    __syncthreads();
-    for (int32_t size = 2; size <= np2; size <<= 1) {
-        for (int32_t stride = size >> 1; stride > 0; stride >>= 1) {
+        return key;
+    };
+    unsigned long long k0 = holds ? key_at(e0) : ~0ULL, k1 = holds ? key_at(e0 + 1) : ~0ULL;
+    // stages stride = top .. 1 of merge size `size` on the warp's registers; the pair
+    // (lo, lo + stride) ends ascending when (lo & size) == 0, descending otherwise
+    auto warp_stages = [&](int32_t size, int32_t top) {
+        for (int32_t stride = top; stride > 0; stride >>= 1) {
+            if (stride == 1) {
+                const bool up = (e0 & size) == 0;
+                if ((k0 > k1) == up) {
+                    const unsigned long long t = k0;
+                    k0 = k1;
+                    k1 = t;
+                }
+            } else {
+                const unsigned long long o0 = __shfl_xor_sync(0xffffffffu, k0, stride >> 1);
+                const unsigned long long o1 = __shfl_xor_sync(0xffffffffu, k1, stride >> 1);
+                const bool lower = (e0 & stride) == 0;
+                const bool up = ((lower ? e0 : e0 - stride) & size) == 0;
+                const bool keep_min = lower == up;
+                k0 = keep_min ? (k0 < o0 ? k0 : o0) : (k0 > o0 ? k0 : o0);
+                k1 = keep_min ? (k1 < o1 ? k1 : o1) : (k1 > o1 ? k1 : o1);
+            }
+        }
+    };
+    for (int32_t size = 2; size <= 64; size <<= 1) warp_stages(size, size >> 1);
+    for (int32_t size = 128; size <= np2; size <<= 1) {
+        if (holds) {
+            sk[e0] = k0;
+            sk[e0 + 1] = k1;
+        }
+        __syncthreads();
+        for (int32_t stride = size >> 1; stride >= 64; stride >>= 1) {
             for (int32_t t = threadIdx.x; t < np2 / 2; t += kSortThreads) {
                 const int32_t lo = 2 * t - (t & (stride - 1));
                 const int32_t hi = lo + stride;
@@ -663,18 +697,18 @@ __global__ void __launch_bounds__(kSortThreads) wl_sort_chunks_kernel(SortArgs a
                     sk[hi] = x;
                 }
             }
-            // a stage of stride <= 32 only touches its warp's own 64 keys (thread t
-            // pairs keys in [64 (t / 32), 64 (t / 32) + 64)): between two such
-            // stages a warp barrier suffices; a block barrier is needed when this
-            // stage or the next one reaches across warps, and after the last
-            const int32_t next = stride > 1 ? stride >> 1 : size;
-            static_assert(kSortChunk / 2 == kSortThreads, "one pair per thread and stage");
-            const bool last = stride == 1 && size == np2;
-            if (stride > 32 || next > 32 || last) __syncthreads();
-            else __syncwarp();
+            __syncthreads();
         }
+        if (holds) {
+            k0 = sk[e0];
+            k1 = sk[e0 + 1];
+        }
+        warp_stages(size, 32);
+        __syncthreads();  // every warp has read its keys before the next size rewrites them
     }
-    for (int32_t i = threadIdx.x; i < m; i += kSortThreads) keys[c0 + i] = sk[i];
+    static_assert(kSortChunk / 2 == kSortThreads, "two keys per thread");
+    if (e0 < m) keys[c0 + e0] = k0;
+    if (e0 + 1 < m) keys[c0 + e0 + 1] = k1;
 }
 
 // kMode kRankLpt: keys are (~cost, uid) and order[rank] = uid (LPT order).
