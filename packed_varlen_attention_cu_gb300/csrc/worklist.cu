@@ -1170,38 +1170,46 @@ __global__ void __launch_bounds__(kBwdPlanThreads)
         int32_t base = carry;
         for (int j = 0; j < w; ++j) base += warp_tot[j];
         const int32_t first = base + inc - nk;  // this group's first key tile
-        auto steps_of = [&](int32_t kt) -> int64_t {
-            int64_t steps = 0;
-            for (int32_t m = 0; m < gcount; ++m) {
-                int32_t qlo, qhi;
-                const WlSlice& sm = slices[sidx[i + m]];
-                bwd_q_span(sm, kt, qlo, qhi, slice_mask(wl, h, sm, sidx[i + m]));
-                steps += qhi - qlo;
-            }
-            return steps;
-        };
-        for (int32_t kt = 0; kt < nk; ++kt) {
-            const int64_t steps = steps_of(kt);
-            for (int32_t g = 0; g < hkv; ++g) {
-                // units of one (group, kv head) are consecutive, key tiles ascending
-                const int32_t uid = first * hkv + g * nk + kt;
-                if (uid >= bh->cap_units) {
-                    atomicCAS(&bh->error, 0, kErrCapacity);
-                    continue;
+        // The warp's groups one after the other, each group's key tiles spread over
+        // the 32 lanes (a long document's hundreds of key tiles took one thread
+        // most of the plan's time).
+        unsigned leaders = __ballot_sync(0xffffffffu, nk > 0);
+        while (leaders) {
+            const int src = __ffs(leaders) - 1;
+            leaders &= leaders - 1;
+            const int32_t gi = __shfl_sync(0xffffffffu, i, src);
+            const int32_t gfirst = __shfl_sync(0xffffffffu, first, src);
+            const int32_t gnk = __shfl_sync(0xffffffffu, nk, src);
+            const int32_t gcnt = __shfl_sync(0xffffffffu, gcount, src);
+            for (int32_t kt = lane; kt < gnk; kt += 32) {
+                int64_t steps = 0;
+                for (int32_t m = 0; m < gcnt; ++m) {
+                    int32_t qlo, qhi;
+                    const WlSlice& sm = slices[sidx[gi + m]];
+                    bwd_q_span(sm, kt, qlo, qhi, slice_mask(wl, h, sm, sidx[gi + m]));
+                    steps += qhi - qlo;
                 }
-                BwdUnit u;
-                u.gbegin = i;
-                u.gcount = gcount;
-                u.kt = kt;
-                u.kvh = g;
-                u.cost = (int64_t)G * steps + 1;
-                units[uid] = u;
-                // dynamic: the unit's power-of-two cost class (cost >= 1)
-                const unsigned long long c =
-                    dyn ? 1ULL << (63 - __clzll((unsigned long long)u.cost))
-                        : (unsigned long long)u.cost;
-                const unsigned long long inv = ((1ULL << kCostBits) - 1) - c;
-                keys[uid] = (inv << kUidBits) | (unsigned long long)uid;
+                for (int32_t g = 0; g < hkv; ++g) {
+                    // units of one (group, kv head) are consecutive, key tiles ascending
+                    const int32_t uid = gfirst * hkv + g * gnk + kt;
+                    if (uid >= bh->cap_units) {
+                        atomicCAS(&bh->error, 0, kErrCapacity);
+                        continue;
+                    }
+                    BwdUnit u;
+                    u.gbegin = gi;
+                    u.gcount = gcnt;
+                    u.kt = kt;
+                    u.kvh = g;
+                    u.cost = (int64_t)G * steps + 1;
+                    units[uid] = u;
+                    // dynamic: the unit's power-of-two cost class (cost >= 1)
+                    const unsigned long long c =
+                        dyn ? 1ULL << (63 - __clzll((unsigned long long)u.cost))
+                            : (unsigned long long)u.cost;
+                    const unsigned long long inv = ((1ULL << kCostBits) - 1) - c;
+                    keys[uid] = (inv << kUidBits) | (unsigned long long)uid;
+                }
             }
         }
         __syncthreads();
