@@ -51,8 +51,12 @@ namespace {
 
 constexpr int kThreads = 384;
 // register split: the producer/MMA warpgroup hands registers to the two
-// softmax warpgroups (128 * kRegsCtrl + 256 * kRegsSoftmax <= 384 * 168)
-constexpr uint32_t kRegsCtrl = 72, kRegsSoftmax = 216;
+// softmax warpgroups (128 * ctrl + 256 * softmax <= 384 * 168; multiples of 8):
+// 72 / 216 at d = 128, 56 / 224 at d = 64 (fewer softmax spills there)
+template <int D>
+struct Regs {
+    static constexpr uint32_t kCtrl = D == 64 ? 56 : 72, kSoftmax = D == 64 ? 224 : 216;
+};
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 constexpr float kRescaleThreshold = 8.0f;     // log2 domain
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.dynamic && tid == 0) dispatch_exit(&hw->dispatch_next, &hw->dispatch_done);
     };
     if (warp < 4) {
-      regs_dealloc<kRegsCtrl>();
+      regs_dealloc<Regs<D>::kCtrl>();
       if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
@@ -616,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       finish();
       return;
     } else {
-        regs_alloc<kRegsSoftmax>();
+        regs_alloc<Regs<D>::kSoftmax>();
         // ------------------------------------------------------- softmax / epilogue
         const int i = (warp - 4) >> 2;           // sub-tile of this warpgroup
         const int r = (warp & 3) * 32 + lane;    // query row = tensor-memory lane
@@ -977,7 +981,8 @@ pva_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
     // never be granted.
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return PVA_ERR_CUDA;
-    if ((int64_t)fa.numRegs * kThreads < 128 * (int64_t)kRegsCtrl + 256 * (int64_t)kRegsSoftmax)
+    if ((int64_t)fa.numRegs * kThreads <
+        128 * (int64_t)Regs<D>::kCtrl + 256 * (int64_t)Regs<D>::kSoftmax)
         return PVA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmem) !=
         cudaSuccess)
