@@ -168,12 +168,13 @@ __device__ __forceinline__ void store_zero_row(void* base, int64_t row_elem, boo
 }
 
 // issuers: MMA-issuing warps; each commits once to a_empty, s2_full and r_empty
-// per use and reads every unit
+// per use and reads every unit.  acc_issuers: the warps that commit o_full (the
+// ones whose MMAs write the accumulators)
 __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_threads,
-                                              int extra_readers, int issuers) {
+                                              int extra_readers, int issuers, int acc_issuers) {
     mbar_init(&sh.a_full, 1);
     mbar_init(&sh.a_empty, issuers);
-    mbar_init(&sh.o_full, 1);
+    mbar_init(&sh.o_full, acc_issuers);
     mbar_init(&sh.o_empty, elem_threads / 32);
     mbar_init(&sh.done, 1);
     mbar_init(&sh.done2, 1);
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
     const int32_t ub = dyn ? 0 : cta_off[blockIdx.x], ue = dyn ? 0 : cta_off[blockIdx.x + 1];
     if (!dyn && ub >= ue) return;
-    if (tid == 0) init_barriers(sh, C::kStagesDq, 256, 0, 2);
+    if (tid == 0) init_barriers(sh, C::kStagesDq, 256, 0, 2, 1);
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -677,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     BwdHeader* bhw = const_cast<BwdHeader*>(bh);
     if (!dyn && (int32_t)blockIdx.x >= n) return;
     // unit readers beyond the MMA and element-wise warps: the loader warp
-    if (tid == 0) init_barriers(sh, kItems, 256, 1, 1);
+    if (tid == 0) init_barriers(sh, kItems, 256, 1, 2, 2);
     // (LSE log2, D) of the 64 queries of each staged half-item
     __shared__ __align__(16) float2 s_ld[kLdSlots][64];
     if (warp == 1) {
@@ -774,21 +775,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer (whole warp)
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------- MMA issuers (whole warps)
         // Half-items: the 64 queries [64 hf, 64 hf + 64) of one (head, slice, q tile)
-        // item.  S^T and dP^T of half-item u go to buffer u % 2 (64 columns each);
-        // they are issued before dV/dK of half-item u - 1, so the element-wise
-        // warps work on u - 1 while the tensor pipe computes u.
+        // item.  Warp 1 issues S^T = K Q^T and dV += P^T dO, warp 3 dP^T = V dO^T and
+        // dK += dS^T Q: one warp spent longer issuing a half-item's 24 MMAs and
+        // waiting for its operands than the tensor pipe took to run them.  S^T and
+        // dP^T of half-item u go to buffer u % 2 (64 columns each); each warp issues
+        // them before its dV or dK MMAs of half-item u - 1, so the element-wise warps
+        // work on u - 1 while the tensor pipe computes u.  A warp reuses its half of
+        // buffer u % 2 only after its own MMAs that read it (issue order); s2_full,
+        // r_empty, a_empty and o_full count one commit from each warp.
+        const bool sdv = warp == 1;
+        const int site = sdv ? 0 : 17;  // wait sites 33-36 (warp 1), 50-53 (warp 3)
         uint32_t it = 0, a_it = 0, gu = 0, o_cnt = 0;
         bool live = true;
-        const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
-        const uint64_t dV = sdesc_sw128(smem_u32(sV), 16, 1024);
+        const uint64_t dA = sdesc_sw128(smem_u32(sdv ? sK : sV), 16, 1024);
         const uint64_t dRn = sdesc_sw128(smem_u32(sR), 16, 1024);    // K-major
         const uint64_t dRm = sdesc_sw128(smem_u32(sR), 8192, 1024);  // MN-major, 64-row atoms
         constexpr uint32_t kIdescHalf = idesc_bf16_f32(128, 64, false);
-        const uint32_t tVa = tmem + 256, tKa = tmem + 256 + D;
-        // the half-item whose dV/dK MMAs are still to be issued
+        // this warp's buffer half, accumulator, and the operands of its two GEMMs
+        // within a ring stage: S^T reads the Q half, dV the dO half; dP^T the dO
+        // half, dK the Q half
+        const uint32_t tBuf = tmem + (sdv ? 0 : 128);
+        const uint32_t tAcc = tmem + 256 + (sdv ? 0 : D);
+        const uint32_t offN = sdv ? 0 : kHalfBytes, offAcc = sdv ? kHalfBytes : 0;
+        // the half-item whose dV or dK MMAs are still to be issued
         bool pend = false, first = true;
         uint32_t pend_u = 0, pend_st = 0;
         auto finish_pending = [&]() -> bool {
@@ -797,22 +809,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // unit's epilogue must have read them (waited only here, so that S^T and
             // dP^T of the first half-items overlap that epilogue)
             if (first && !mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
-                                         kErrTimeoutBase + 34, kWaitNs))
+                                         kErrTimeoutBase + 34 + site, kWaitNs))
                 return false;
             if (!mbar_wait_warp(&sh.p2_full[b], (pend_u >> 1) & 1, abort_flag, err_word,
-                                kErrTimeoutBase + 36, kWaitNs))
+                                kErrTimeoutBase + 36 + site, kWaitNs))
                 return false;
             tc_fence_after();
-            const uint64_t oQ = (pend_st * 2 * kHalfBytes) >> 4;
-            const uint64_t oO = (pend_st * 2 * kHalfBytes + kHalfBytes) >> 4;
+            const uint64_t oB = (pend_st * 2 * kHalfBytes + offAcc) >> 4;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_ts_elect(tVa, tmem + 64 * b + kslice_col(k), dRm + oO + k * 128, C::kIdescNN,
-                             (!first || k > 0) ? 1u : 0u);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_ts_elect(tKa, tmem + 128 + 64 * b + kslice_col(k), dRm + oQ + k * 128,
-                             C::kIdescNN,
+                mma_ts_elect(tAcc, tBuf + 64 * b + kslice_col(k), dRm + oB + k * 128, C::kIdescNN,
                              (!first || k > 0) ? 1u : 0u);
             first = false;
             mma_commit_elect(&sh.r_empty[pend_st]);
@@ -821,13 +827,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         for (uint32_t rd = 0; live; ++rd) {
             int32_t idx;
-            live = uring_get_warp(sh.ur, rd, idx, abort_flag, err_word, kErrTimeoutBase + 40,
-                                  kWaitNs);
+            live = uring_get_warp(sh.ur, rd, idx, abort_flag, err_word,
+                                  kErrTimeoutBase + (sdv ? 40 : 54), kWaitNs);
             if (!live || idx < 0) break;
             const BwdUnit u = bunits[idx];
             if (u.cost <= 1) continue;
             live = mbar_wait_warp(&sh.a_full, a_it & 1, abort_flag, err_word,
-                                  kErrTimeoutBase + 33, kWaitNs);
+                                  kErrTimeoutBase + 33 + site, kWaitNs);
             if (!live) break;
             first = true;
             for (int32_t m = 0; m < u.gcount && live; ++m) {
@@ -841,26 +847,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (uint32_t hf = 0; hf < halves && live; ++hf) {
                             const uint32_t st = it % kItems;
                             live = mbar_wait_warp(&sh.r_full[st], (it / kItems) & 1, abort_flag,
-                                                  err_word, kErrTimeoutBase + 35, kWaitNs);
+                                                  err_word, kErrTimeoutBase + 35 + site, kWaitNs);
                             if (!live) break;
                             tc_fence_after();
                             const uint32_t b = gu & 1;
-                            const uint64_t oQ = (st * 2 * kHalfBytes) >> 4;
-                            const uint64_t oO = (st * 2 * kHalfBytes + kHalfBytes) >> 4;
+                            const uint64_t oN = (st * 2 * kHalfBytes + offN) >> 4;
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
-                                // K (resident, 128-row atoms) and the Q half (64-row atoms)
+                                // K or V (resident, 128-row atoms) against the Q or dO
+                                // half (64-row atoms)
                                 const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
                                 const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
-                                mma_ss_elect(tmem + 64 * b, dK + off16, dRn + oQ + kq, kIdescHalf,
+                                mma_ss_elect(tBuf + 64 * b, dA + off16, dRn + oN + kq, kIdescHalf,
                                              k > 0);
-                            }
-#pragma unroll
-                            for (int k = 0; k < D / 16; ++k) {
-                                const uint32_t kq = (k >> 2) * 512 + (k & 3) * 2;
-                                const uint32_t off16 = (k >> 2) * 1024 + (k & 3) * 2;
-                                mma_ss_elect(tmem + 128 + 64 * b, dV + off16, dRn + oO + kq,
-                                             kIdescHalf, k > 0);
                             }
                             mma_commit_elect(&sh.s2_full[b]);
                             if (pend && !finish_pending()) {
@@ -883,8 +882,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++o_cnt;
             ++a_it;
         }
-        mma_commit_elect(&sh.done);
-        mbar_wait_drain(&sh.done, 0, kDrainNs);
+        uint64_t* done = sdv ? &sh.done : &sh.done2;
+        mma_commit_elect(done);
+        mbar_wait_drain(done, 0, kDrainNs);
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------- (LSE, D) loader
