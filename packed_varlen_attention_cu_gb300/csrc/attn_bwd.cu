@@ -576,18 +576,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tmem_ld_wait(sv);
                                 tmem_ld_wait(pv);
                                 uint32_t dsw[32];
+                                const float2 sc = make_float2(p.scale_log2, p.scale_log2);
+                                const float2 nl = make_float2(-lse2, -lse2);
+                                const float2 nd = make_float2(-dd, -dd);
 #pragma unroll
                                 for (int e = 0; e < 32; e += 2) {
                                     const int col = hf * 64 + c * 32 + e;
-                                    float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - lse2);
-                                    float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - lse2);
+                                    const float2 x =
+                                        __ffma2_rn(make_float2(__uint_as_float(sv[e]),
+                                                               __uint_as_float(sv[e + 1])),
+                                                   sc, nl);
+                                    float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
                                     if (need_mask) {
                                         if (col < c_lo || col >= c_hi) p0 = 0.f;
                                         if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
                                     }
-                                    const float g0 = p0 * (__uint_as_float(pv[e]) - dd);
-                                    const float g1 = p1 * (__uint_as_float(pv[e + 1]) - dd);
-                                    dsw[e >> 1] = pack_bf16x2(g0, g1);
+                                    const float2 g = __fmul2_rn(
+                                        make_float2(p0, p1),
+                                        __fadd2_rn(make_float2(__uint_as_float(pv[e]),
+                                                               __uint_as_float(pv[e + 1])),
+                                                   nd));
+                                    dsw[e >> 1] = pack_bf16x2(g.x, g.y);
                                 }
                                 tmem_st16(tSb + c * 32, dsw);
                             }
@@ -679,8 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!dyn && (int32_t)blockIdx.x >= n) return;
     // unit readers beyond the MMA and element-wise warps: the loader warp
     if (tid == 0) init_barriers(sh, kItems, 256, 1, 2, 2);
-    // (LSE log2, D) of the 64 queries of each staged half-item
-    __shared__ __align__(16) float2 s_ld[kLdSlots][64];
+    // -LSE log2 e and -D of the 64 queries of each staged half-item
+    __shared__ __align__(16) float s_nl[kLdSlots][64];
+    __shared__ __align__(16) float s_nd[kLdSlots][64];
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -888,8 +898,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------------- (LSE, D) loader
-        // Walks the half-items in the element-wise warps' order and stages the
-        // (LSE log2, D) of their 64 queries up to kLdSlots half-items ahead, so
+        // Walks the half-items in the element-wise warps' order and stages -LSE
+        // log2 e and -D of their 64 queries up to kLdSlots half-items ahead, so
         // the global-load latency stays off the element-wise warps' path.  A
         // query past the tile gets LSE = +inf: every P of it is 0.
         uint32_t li = 0;
@@ -927,7 +937,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (l != -INFINITY) l2 = l * 1.4426950408889634f;
                                     dd = p.dvec[li_];
                                 }
-                                s_ld[slot][c * 32 + lane] = make_float2(l2, dd);
+                                s_nl[slot][c * 32 + lane] = -l2;
+                                s_nd[slot][c * 32 + lane] = -dd;
                             }
                             mbar_arrive(&sh.ld_full[slot]);  // every lane, after its writes
                         }
@@ -990,7 +1001,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         live = mbar_wait(&sh.ld_full[slot], (li / kLdSlots) & 1, abort_flag,
                                          err_word, kErrTimeoutBase + 43, kWaitNs);
                         if (!live) break;
-                        const float2* my_ld = s_ld[slot] + wg * 32;
+                        const float* my_nl = s_nl[slot] + wg * 32;
+                        const float* my_nd = s_nd[slot] + wg * 32;
                         // columns [c_lo, c_hi) of this key row are allowed; the warp
                         // masks only when some row of it has a limit inside its columns
                         const bool need_mask =
@@ -1008,20 +1020,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tmem_ld_wait(sv);
                             tmem_ld_wait(pv);
                             uint32_t pw[32], dw[32];
+                            const float2 sc = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-                            for (int e = 0; e < 32; e += 2) {
-                                const float4 ld = *reinterpret_cast<const float4*>(&my_ld[e]);
-                                float p0 = ex2_approx(__uint_as_float(sv[e]) * p.scale_log2 - ld.x);
-                                float p1 = ex2_approx(__uint_as_float(sv[e + 1]) * p.scale_log2 - ld.z);
-                                if (need_mask) {
-                                    const int col = h0 + e;
-                                    if (col < c_lo || col >= c_hi) p0 = 0.f;
-                                    if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                            for (int e = 0; e < 32; e += 4) {
+                                const float4 nl = *reinterpret_cast<const float4*>(&my_nl[e]);
+                                const float4 nd = *reinterpret_cast<const float4*>(&my_nd[e]);
+#pragma unroll
+                                for (int j = 0; j < 4; j += 2) {
+                                    const float2 x = __ffma2_rn(
+                                        make_float2(__uint_as_float(sv[e + j]),
+                                                    __uint_as_float(sv[e + j + 1])),
+                                        sc, j == 0 ? make_float2(nl.x, nl.y)
+                                                   : make_float2(nl.z, nl.w));
+                                    float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                                    if (need_mask) {
+                                        const int col = h0 + e + j;
+                                        if (col < c_lo || col >= c_hi) p0 = 0.f;
+                                        if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                                    }
+                                    const float2 g = __fmul2_rn(
+                                        make_float2(p0, p1),
+                                        __fadd2_rn(make_float2(__uint_as_float(pv[e + j]),
+                                                               __uint_as_float(pv[e + j + 1])),
+                                                   j == 0 ? make_float2(nd.x, nd.y)
+                                                          : make_float2(nd.z, nd.w)));
+                                    pw[(e + j) >> 1] = pack_bf16x2(p0, p1);
+                                    dw[(e + j) >> 1] = pack_bf16x2(g.x, g.y);
                                 }
-                                const float g0 = p0 * (__uint_as_float(pv[e]) - ld.y);
-                                const float g1 = p1 * (__uint_as_float(pv[e + 1]) - ld.w);
-                                pw[e >> 1] = pack_bf16x2(p0, p1);
-                                dw[e >> 1] = pack_bf16x2(g0, g1);
                             }
                             tmem_st16(tSb + c * 32, pw);
                             tmem_st16(tPb + c * 32, dw);
