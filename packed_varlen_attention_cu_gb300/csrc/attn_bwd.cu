@@ -24,7 +24,8 @@
 // columns each) so that its P / dS are ready as early as possible.
 // Tensor-memory columns: bwd_dq S [0,128) dP [128,256) dQ [256,256+d), then Q and
 // dO as bf16 MMA A operands (d/2 columns each);
-// bwd_dkdv S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d,256+2d).
+// bwd_dkdv with nb S^T / dP^T buffers (2 at d = 128, 3 at d = 64): S^T [0,64 nb)
+// dP^T [64 nb,128 nb) dV [128 nb,128 nb+d) dK [128 nb+d,128 nb+2d).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -60,6 +61,9 @@ struct BCfg {
     // shared memory per block (bwd_dkdv also holds 2.3 KB of static staging)
     static constexpr int kStagesDq = D == 128 ? 5 : 12;
     static constexpr int kStagesKv = D == 128 ? 4 : 11;
+    // bwd_dkdv's S^T / dP^T buffers (64 + 64 tensor-memory columns each): d = 64
+    // leaves room for a third beside dV and dK
+    static constexpr uint32_t kBufsKv = D == 64 ? 3 : 2;  // at most 3
     static constexpr int kSmemDq = 2 * kTileBytes + kStagesDq * kTileBytes + 1024;
     static constexpr int kSmemKv = 2 * kTileBytes + kStagesKv * kTileBytes + 1024;
     static constexpr uint32_t kIdescNN = idesc_bf16_f32(128, D, true);     // B MN-major
@@ -84,7 +88,7 @@ constexpr int kMaxStages = 12;
 
 struct BShared {
     uint64_t a_full, a_empty, o_full, o_empty, done, done2;
-    uint64_t s2_full[2], p2_full[2];  // per half-item tensor-memory buffer
+    uint64_t s2_full[3], p2_full[3];  // per half-item tensor-memory buffer
     uint64_t r_full[kMaxStages], r_empty[kMaxStages];
     UnitRing<8> ur;  // the producer hands each unit's index to the other roles
     // bwd_dkdv: (LSE log2, D) of each half-item's 64 queries, staged ahead by a
@@ -178,7 +182,7 @@ __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_
     mbar_init(&sh.o_empty, elem_threads / 32);
     mbar_init(&sh.done, 1);
     mbar_init(&sh.done2, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
         mbar_init(&sh.s2_full[b], issuers);
         mbar_init(&sh.p2_full[b], elem_threads / 32);  // one arrival per element-wise warp
     }
@@ -656,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 64-column atom (a stage: Q half at +0, dO half at +D/64 * 8 KB)
     using C = BCfg<D>;
     constexpr int kItems = C::kStagesKv;        // half-items in the ring
+    constexpr uint32_t NB = C::kBufsKv;         // S^T / dP^T buffers
     constexpr int kHalfBytes = 64 * D * 2;      // one 64-row bf16 half tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -791,11 +796,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // item.  Warp 1 issues S^T = K Q^T and dV += P^T dO, warp 3 dP^T = V dO^T and
         // dK += dS^T Q: one warp spent longer issuing a half-item's 24 MMAs and
         // waiting for its operands than the tensor pipe took to run them.  S^T and
-        // dP^T of half-item u go to buffer u % 2 (64 columns each); each warp issues
-        // them before its dV or dK MMAs of half-item u - 1, so the element-wise warps
-        // work on u - 1 while the tensor pipe computes u.  A warp reuses its half of
-        // buffer u % 2 only after its own MMAs that read it (issue order); s2_full,
-        // r_empty, a_empty and o_full count one commit from each warp.
+        // dP^T of half-item u go to buffer u % NB (64 columns each); each warp issues
+        // them before its dV or dK MMAs of half-item u - NB + 1, so the element-wise
+        // warps work on the NB - 1 half-items before u while the tensor pipe computes
+        // u.  A warp reuses its half of buffer u % NB only after its own MMAs that
+        // read it (issue order); s2_full, r_empty, a_empty and o_full count one commit
+        // from each warp.
         const bool sdv = warp == 1;
         const int site = sdv ? 0 : 17;  // wait sites 33-36 (warp 1), 50-53 (warp 3)
         uint32_t it = 0, a_it = 0, gu = 0, o_cnt = 0;
@@ -807,32 +813,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this warp's buffer half, accumulator, and the operands of its two GEMMs
         // within a ring stage: S^T reads the Q half, dV the dO half; dP^T the dO
         // half, dK the Q half
-        const uint32_t tBuf = tmem + (sdv ? 0 : 128);
-        const uint32_t tAcc = tmem + 256 + (sdv ? 0 : D);
+        const uint32_t tBuf = tmem + (sdv ? 0 : 64 * NB);
+        const uint32_t tAcc = tmem + 128 * NB + (sdv ? 0 : D);
         const uint32_t offN = sdv ? 0 : kHalfBytes, offAcc = sdv ? kHalfBytes : 0;
-        // the half-item whose dV or dK MMAs are still to be issued
-        bool pend = false, first = true;
-        uint32_t pend_u = 0, pend_st = 0;
+        // the half-items (oldest first) whose dV or dK MMAs are still to be issued
+        bool first = true;
+        uint32_t npend = 0, pu0 = 0, pu1 = 0, ps0 = 0, ps1 = 0;  // NB - 1 <= 2 of them
         auto finish_pending = [&]() -> bool {
-            const uint32_t b = pend_u & 1;
+            const uint32_t pu = pu0, pst = ps0;
+            const uint32_t b = pu % NB;
             // the unit's first dV/dK MMAs overwrite the accumulators: the previous
             // unit's epilogue must have read them (waited only here, so that S^T and
             // dP^T of the first half-items overlap that epilogue)
             if (first && !mbar_wait_warp(&sh.o_empty, (o_cnt & 1) ^ 1, abort_flag, err_word,
                                          kErrTimeoutBase + 34 + site, kWaitNs))
                 return false;
-            if (!mbar_wait_warp(&sh.p2_full[b], (pend_u >> 1) & 1, abort_flag, err_word,
+            if (!mbar_wait_warp(&sh.p2_full[b], (pu / NB) & 1, abort_flag, err_word,
                                 kErrTimeoutBase + 36 + site, kWaitNs))
                 return false;
             tc_fence_after();
-            const uint64_t oB = (pend_st * 2 * kHalfBytes + offAcc) >> 4;
+            const uint64_t oB = (pst * 2 * kHalfBytes + offAcc) >> 4;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mma_ts_elect(tAcc, tBuf + 64 * b + kslice_col(k), dRm + oB + k * 128, C::kIdescNN,
                              (!first || k > 0) ? 1u : 0u);
             first = false;
-            mma_commit_elect(&sh.r_empty[pend_st]);
-            pend = false;
+            mma_commit_elect(&sh.r_empty[pst]);
+            pu0 = pu1;
+            ps0 = ps1;
+            --npend;
             return true;
         };
         for (uint32_t rd = 0; live; ++rd) {
@@ -860,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   err_word, kErrTimeoutBase + 35 + site, kWaitNs);
                             if (!live) break;
                             tc_fence_after();
-                            const uint32_t b = gu & 1;
+                            const uint32_t b = gu % NB;
                             const uint64_t oN = (st * 2 * kHalfBytes + offN) >> 4;
 #pragma unroll
                             for (int k = 0; k < D / 16; ++k) {
@@ -872,13 +881,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              k > 0);
                             }
                             mma_commit_elect(&sh.s2_full[b]);
-                            if (pend && !finish_pending()) {
+                            if (npend == NB - 1 && !finish_pending()) {
                                 live = false;
                                 break;
                             }
-                            pend = true;
-                            pend_u = gu;
-                            pend_st = st;
+                            if (npend == 0) {
+                                pu0 = gu;
+                                ps0 = st;
+                            } else {
+                                pu1 = gu;
+                                ps1 = st;
+                            }
+                            ++npend;
                             ++gu;
                             ++it;
                         }
@@ -886,7 +900,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!live) break;
-            if (pend && !finish_pending()) break;
+            while (npend > 0 && finish_pending()) {
+            }
+            if (npend > 0) break;
             mma_commit_elect(&sh.a_empty);
             mma_commit_elect(&sh.o_full);
             ++o_cnt;
@@ -955,8 +971,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wg = (warp - 4) >> 2;
         const int kr = (warp & 3) * 32 + lane;  // key row = tensor-memory lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_base, tV = tmem + lane_base + 256,
-                       tK = tmem + lane_base + 256 + D;
+        const uint32_t tS = tmem + lane_base, tV = tmem + lane_base + 128 * NB,
+                       tK = tmem + lane_base + 128 * NB + D;
         uint32_t gu = 0, o_cnt = 0, li = 0;
         bool live = true;
         for (uint32_t rd = 0; live; ++rd) {
@@ -991,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t halves = nq > 64 ? 2 : 1;
                     for (int32_t hh = 0; hh < G && live; ++hh) {
                     for (uint32_t hf = 0; hf < halves && live; ++hf, ++gu) {
-                        const uint32_t b = gu & 1;
+                        const uint32_t b = gu % NB;
                         // this warpgroup's 32 query columns [h0, h0 + 32) of the half:
                         // their (LSE log2, D) into the warp's slots, loaded before the
                         // wait for S^T; a query past the tile has LSE = +inf, so every
@@ -1007,11 +1023,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // masks only when some row of it has a limit inside its columns
                         const bool need_mask =
                             __any_sync(0xffffffffu, c_lo > h0 || c_hi < min(h0 + 32, nq));
-                        live = mbar_wait(&sh.s2_full[b], (gu >> 1) & 1, abort_flag, err_word,
+                        live = mbar_wait(&sh.s2_full[b], (gu / NB) & 1, abort_flag, err_word,
                                          kErrTimeoutBase + 37, kWaitNs);
                         if (!live) break;
                         tc_fence_after();
-                        const uint32_t tSb = tS + 64 * b, tPb = tS + 128 + 64 * b;
+                        const uint32_t tSb = tS + 64 * b, tPb = tS + 64 * NB + 64 * b;
                         {
                             const int c = wg;
                             uint32_t sv[32], pv[32];
