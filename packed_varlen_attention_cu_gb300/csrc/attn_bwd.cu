@@ -173,9 +173,11 @@ __device__ __forceinline__ void store_zero_row(void* base, int64_t row_elem, boo
 
 // issuers: MMA-issuing warps; each commits once to a_empty, s2_full and r_empty
 // per use and reads every unit.  acc_issuers: the warps that commit o_full (the
-// ones whose MMAs write the accumulators)
+// ones whose MMAs write the accumulators).  item_warps: the element-wise warps
+// that work on each half-item (p2_full and ld_empty count one arrival each)
 __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_threads,
-                                              int extra_readers, int issuers, int acc_issuers) {
+                                              int extra_readers, int issuers, int acc_issuers,
+                                              int item_warps) {
     mbar_init(&sh.a_full, 1);
     mbar_init(&sh.a_empty, issuers);
     mbar_init(&sh.o_full, acc_issuers);
@@ -184,7 +186,7 @@ __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_
     mbar_init(&sh.done2, 1);
     for (int b = 0; b < 3; ++b) {
         mbar_init(&sh.s2_full[b], issuers);
-        mbar_init(&sh.p2_full[b], elem_threads / 32);  // one arrival per element-wise warp
+        mbar_init(&sh.p2_full[b], item_warps);
     }
     for (int s = 0; s < stages; ++s) {
         mbar_init(&sh.r_full[s], 1);
@@ -194,7 +196,7 @@ __device__ __forceinline__ void init_barriers(BShared& sh, int stages, int elem_
     uring_init(sh.ur, issuers + elem_threads + extra_readers);
     for (int s = 0; s < kLdSlots; ++s) {
         mbar_init(&sh.ld_full[s], 32);
-        mbar_init(&sh.ld_empty[s], elem_threads / 32);
+        mbar_init(&sh.ld_empty[s], item_warps);
     }
     sh.abort_flag = 0;
     fence_barrier_init();
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t* cta_off = reinterpret_cast<const int32_t*>(p.wl + h->off.cta_off);
     const int32_t ub = dyn ? 0 : cta_off[blockIdx.x], ue = dyn ? 0 : cta_off[blockIdx.x + 1];
     if (!dyn && ub >= ue) return;
-    if (tid == 0) init_barriers(sh, C::kStagesDq, 256, 0, 2, 1);
+    if (tid == 0) init_barriers(sh, C::kStagesDq, 256, 0, 2, 1, 8);
     if (warp == 1) {
         tmem_alloc(&sh.tmem_base, 512);
         tmem_relinquish();
@@ -661,6 +663,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = BCfg<D>;
     constexpr int kItems = C::kStagesKv;        // half-items in the ring
     constexpr uint32_t NB = C::kBufsKv;         // S^T / dP^T buffers
+    // d = 64: the warpgroups take alternate half-items (all 64 columns each)
+    // instead of sharing each one; with three buffers the chain through a
+    // half-item has room for the longer pass, and each pass's fixed costs
+    // (tensor-memory round trips, hand-offs) cover twice the columns
+    constexpr bool kAlt = D == 64;
     constexpr int kHalfBytes = 64 * D * 2;      // one 64-row bf16 half tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -692,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     BwdHeader* bhw = const_cast<BwdHeader*>(bh);
     if (!dyn && (int32_t)blockIdx.x >= n) return;
     // unit readers beyond the MMA and element-wise warps: the loader warp
-    if (tid == 0) init_barriers(sh, kItems, 256, 1, 2, 2);
+    if (tid == 0) init_barriers(sh, kItems, 256, 1, 2, 2, kAlt ? 4 : 8);
     // -LSE log2 e and -D of the 64 queries of each staged half-item
     __shared__ __align__(16) float s_nl[kLdSlots][64];
     __shared__ __align__(16) float s_nd[kLdSlots][64];
@@ -965,9 +972,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- P^T, dS^T and the dK/dV epilogue
-        // Two warpgroups share every half-item: wg takes its 32 query columns
-        // [32 wg, 32 wg + 32), so a half-item's P^T and dS^T are ready in half
-        // the time; at the end of a unit wg 0 stores dV and wg 1 dK.
+        // d = 128: two warpgroups share every half-item, wg taking its 32 query
+        // columns [32 wg, 32 wg + 32), so a half-item's P^T and dS^T are ready in
+        // half the time; d = 64: warpgroup u % 2 takes half-item u.  At the end
+        // of a unit wg 0 stores dV and wg 1 dK.
         const int wg = (warp - 4) >> 2;
         const int kr = (warp & 3) * 32 + lane;  // key row = tensor-memory lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -1008,28 +1016,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int32_t hh = 0; hh < G && live; ++hh) {
                     for (uint32_t hf = 0; hf < halves && live; ++hf, ++gu) {
                         const uint32_t b = gu % NB;
-                        // this warpgroup's 32 query columns [h0, h0 + 32) of the half:
-                        // their (LSE log2, D) into the warp's slots, loaded before the
-                        // wait for S^T; a query past the tile has LSE = +inf, so every
-                        // P of it is 0
-                        const int h0 = (int)hf * 64 + wg * 32;
+                        if (kAlt && (gu & 1) != (uint32_t)wg) {  // the other warpgroup's
+                            ++li;
+                            continue;
+                        }
+                        // the staged -LSE log2 e and -D of the half's 64 queries; a query
+                        // past the tile has LSE = +inf, so every P of it is 0
                         const uint32_t slot = li % kLdSlots;
                         live = mbar_wait(&sh.ld_full[slot], (li / kLdSlots) & 1, abort_flag,
                                          err_word, kErrTimeoutBase + 43, kWaitNs);
                         if (!live) break;
-                        const float* my_nl = s_nl[slot] + wg * 32;
-                        const float* my_nd = s_nd[slot] + wg * 32;
-                        // columns [c_lo, c_hi) of this key row are allowed; the warp
-                        // masks only when some row of it has a limit inside its columns
-                        const bool need_mask =
-                            __any_sync(0xffffffffu, c_lo > h0 || c_hi < min(h0 + 32, nq));
+                        // columns [c_lo, c_hi) of this key row are allowed; the warp masks a
+                        // chunk of 32 only when some row of it has a limit inside the chunk
+                        // (d = 128: decided before the wait for S^T; d = 64 per chunk, which
+                        // needs fewer registers)
+                        const int hw = (int)hf * 64 + wg * 32;
+                        const bool mask_w =
+                            !kAlt && __any_sync(0xffffffffu, c_lo > hw || c_hi < min(hw + 32, nq));
                         live = mbar_wait(&sh.s2_full[b], (gu / NB) & 1, abort_flag, err_word,
                                          kErrTimeoutBase + 37, kWaitNs);
                         if (!live) break;
                         tc_fence_after();
                         const uint32_t tSb = tS + 64 * b, tPb = tS + 64 * NB + 64 * b;
-                        {
-                            const int c = wg;
+                        // P^T and dS^T of query columns [h0, h0 + 32) of the q tile, packed
+                        // over the first 16 of the chunk's S^T and dP^T columns
+                        auto chunk = [&](const int c, const bool need_mask) {
+                            const int h0 = (int)hf * 64 + c * 32;
+                            const float* my_nl = s_nl[slot] + c * 32;
+                            const float* my_nd = s_nd[slot] + c * 32;
                             uint32_t sv[32], pv[32];
                             tmem_ld32(tSb + c * 32, sv);
                             tmem_ld32(tPb + c * 32, pv);
@@ -1066,6 +1080,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             tmem_st16(tSb + c * 32, pw);
                             tmem_st16(tPb + c * 32, dw);
+                        };
+                        if constexpr (kAlt) {
+#pragma unroll 1
+                            for (int c = 0; c < 2; ++c) {
+                                const int h0 = (int)hf * 64 + c * 32;
+                                chunk(c, __any_sync(0xffffffffu,
+                                                    c_lo > h0 || c_hi < min(h0 + 32, nq)));
+                            }
+                        } else {
+                            chunk(wg, mask_w);
                         }
                         tmem_st_wait();
                         tc_fence_before();
