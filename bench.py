@@ -390,8 +390,11 @@ def run_e2e(args, ctx, world):
     for _ in range(max(4, ns)):
         step()
     torch.cuda.synchronize()
-    # at least six rounds of the rotation, so that its fill and drain weigh little
-    K = max(6 * ns, (args.steps // 5) // ns * ns)
+    # at least twenty rounds of the rotation: each window starts with the link and
+    # the SMs idle and ends with the last step's compute and copy out, which the
+    # steps of a continuous stream of packs would overlap (about one step's
+    # compute plus its copy out per window)
+    K = max(20 * ns, (args.steps // 2) // ns * ns)
     cur = torch.cuda.current_stream()
     # The host link is shared with the rest of the machine and its rate moves between
     # runs, so three windows of K steps are timed and the median window is reported
