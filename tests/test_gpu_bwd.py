@@ -151,10 +151,13 @@ def test_bwd_plan_rejects_partly_overlapping_key_ranges():
     assert api.lib().pva_bwd_plan_bytes(1, ctypes.byref(m), ctypes.byref(p)) == 0
 
 
-def test_bwd_128k_pack_sampled(oracle_mod):
-    """The bench's configuration (128K causal pack, 32 q / 8 kv heads, d = 128, bf16
-    gradients): sampled dq rows and dk/dv keys against the oracle, each by definition."""
-    w = W.zigzag_pack()
+@pytest.mark.parametrize("wname", ["zigzag_pack", "long_tail_gqa"])
+def test_bwd_full_workload_sampled(oracle_mod, wname):
+    """The bench's configurations: the 128K causal pack (32 q / 8 kv heads, d = 128)
+    and the eight long-tail GQA packs (14 q / 2 kv heads, d = 64: three S^T/dP^T
+    buffers, warpgroups on alternate half-items), bf16 gradients: sampled dq rows
+    and dk/dv keys against the oracle, each by definition."""
+    w = getattr(W, wname)()
     cu = w.cu_seqlens
     T, hq, hkv, d = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
     q, k, v = W.workload_qkv(w, device="cpu")
@@ -173,7 +176,7 @@ def test_bwd_128k_pack_sampled(oracle_mod):
     gq = got[0][qj[:, 0], qj[:, 1]]
     gk = got[1][kj[:, 0], kj[:, 1]]
     gv = got[2][kj[:, 0], kj[:, 1]]
-    _check((gq, gk, gv), (rq, rk, rv), "128K pack sampled")
+    _check((gq, gk, gv), (rq, rk, rv), f"{wname} sampled")
 
 
 @pytest.mark.parametrize("t", [0, 1, 3])
